@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the delta-rule linear-attention forward on GB300.
+
+One JSON line on rank 0.  Headline (``value``): chunked prefill tokens/s on the
+long-sequence workload (B=1, T=32768, H=32, dk=dv=128, bf16 q/k/v, fp32
+state carried in from N(0, 0.02^2), decay = -softplus(N(-4,1)), chunk 64),
+with the counted chunk-GEMM FLOPs reported against the bf16 tensor peak.  The
+same line carries the decode workload (B=256, H=32, d=128, 128 single-token
+steps over a 512 MiB fp32 state) as state GB/s against the HBM peak.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own independent copy of the
+workload on its own GPU (different seed; heads are independent, no collective
+on the data path) and rank 0 reports the aggregate over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kda_inputs import WORKLOADS, make_decode_state, make_decode_step, make_prefill  # noqa: E402
+
+METRIC = "prefill tokens/s & % bf16 TC peak; decode state GB/s vs HBM peak (1×GB300)"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def counted_prefill_flops(B, T, H, dk, dv, C):
+    """Chunk-GEMM FLOPs counted per token-head: 2C(3dk + 2dv) + 6 dk dv
+    (Gram/scores/WY products at chunk C with triangular products counted dense,
+    plus the three state products), times B*T*H."""
+    return float(B) * T * H * (2 * C * (3 * dk + 2 * dv) + 6 * dk * dv)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def to_dev(x, dev, dtype):
+    import torch
+    return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to(dev, dtype)
+
+
+# --------------------------------------------------------------------------- prefill
+def bench_prefill(args, world, rank, dev, peaks):
+    import torch
+    import delta_rule_linear_gb300 as kda
+
+    wl = WORKLOADS[3]
+    d = make_prefill(wl, seed=rank)
+    q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
+    beta, decay, h0 = (to_dev(d[n], dev, torch.float32) for n in ("beta", "decay", "h0"))
+    B, T, H, dk, dv, C = wl.B, wl.T, wl.H, wl.dk, wl.dv, wl.chunk
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=dev)
+    hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    from delta_rule_linear_gb300 import _lib
+    ws = torch.empty(_lib.chunk_fwd_workspace_bytes(B, T, H, dk, dv, C, _lib.KDA_BF16),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.chunk_fwd(q, k, v, beta, decay, h0, chunk_size=C, out=o, final_state=hT,
+                      workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    if kda.query_device_error(ws) != 0:
+        raise RuntimeError("device error recorded during the prefill benchmark")
+
+    # end to end through the C ABI with host buffers: H2D inputs, kernels, D2H outputs
+    pin = lambda x: x.cpu().pin_memory()  # noqa: E731
+    hq, hk, hv, hb, hd, hh0 = (pin(x) for x in (q, k, v, beta, decay, h0))
+    ho = torch.empty_like(o, device="cpu").pin_memory()
+    hhT = torch.empty_like(hT, device="cpu").pin_memory()
+    dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    db, dd, dh0 = torch.empty_like(beta), torch.empty_like(decay), torch.empty_like(h0)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hb, hd, hh0))
+    d2h = ho.numel() * ho.element_size() + hhT.numel() * hhT.element_size()
+
+    def e2e_step():
+        for dst, src in ((dq, hq), (dk_, hk), (dv_, hv), (db, hb), (dd, hd), (dh0, hh0)):
+            dst.copy_(src, non_blocking=True)
+        kda.chunk_fwd(dq, dk_, dv_, db, dd, dh0, chunk_size=C, out=o, final_state=hT,
+                      workspace=ws, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hhT.copy_(hT, non_blocking=True)
+
+    e2e_steps = max(2, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    tokens = B * T
+    flops = counted_prefill_flops(B, T, H, dk, dv, C)
+    peak_tf = peaks["bf16_tflops"]
+    achieved_tf = flops / (ms * 1e-3) / 1e12
+    min_bytes = B * T * H * (2 * dk + 2 * dv) * 2 + B * T * H * 8 + 2 * B * H * dk * dv * 4
+    return {
+        "ms": ms_max, "tokens_per_s": tokens * world / (ms_max * 1e-3),
+        "clocks": clk.summary(),
+        "roofline": {"bound": "tensor", "achieved": round(achieved_tf, 3), "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 5), "traffic": None,
+                     "kernel": "chunk prefill (whole step)",
+                     "flops_per_launch": flops,
+                     "hbm_frac_of_min_bytes": round(min_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5)},
+        "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps * 1,
+        "shape": dict(B=B, T=T, H=H, dk=dk, dv=dv, chunk=C),
+    }
+
+
+# --------------------------------------------------------------------------- decode
+def bench_decode(args, world, rank, dev, peaks):
+    import torch
+    import delta_rule_linear_gb300 as kda
+
+    wl = WORKLOADS[4]
+    state = to_dev(make_decode_state(wl, seed=rank), dev, torch.float32)
+    nsteps = wl.steps
+    toks = []
+    for s in range(nsteps):
+        st = make_decode_step(wl, s, seed=rank)
+        toks.append(tuple(to_dev(st[n], dev, torch.bfloat16) for n in ("q", "k", "v")) +
+                    tuple(to_dev(st[n], dev, torch.float32) for n in ("beta", "decay")))
+    o = torch.empty((wl.B, 1, wl.H, wl.dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def run(n):
+        for s in range(n):
+            q, k, v, b, g = toks[s % nsteps]
+            kda.decode_step(q, k, v, b, g, state, out=o, stream=stream)
+
+    run(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        ev0.record(stream)
+        run(nsteps)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1) / nsteps
+    ms_max = max_over_ranks(ms, world)
+    state_bytes = 2.0 * wl.B * wl.H * wl.dk * wl.dv * 4
+    gbs = state_bytes / (ms * 1e-3) / 1e9
+    return {
+        "ms_per_decode_step": ms_max, "steps": nsteps,
+        "state_GBps": state_bytes * world / (ms_max * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "frac_of_8TBps_nominal": round(gbs / NOMINAL_HBM_GBS, 4), "traffic": None,
+                     "kernel": "decode step", "bytes_per_launch": state_bytes},
+        "clocks": clk.summary(),
+        "gpu_launches": nsteps,
+        "shape": dict(B=wl.B, H=wl.H, dk=wl.dk, dv=wl.dv),
+    }
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_prefill_sample(heads_in_sample, seed=0, threads=0):
+    """Time the fp64 oracle on `heads_in_sample` heads of the long-sequence workload."""
+    import oracle
+    wl = WORKLOADS[3]
+    d = make_prefill(wl, seed=seed)
+    sel = list(range(heads_in_sample))
+    sub = {n: (None if d[n] is None else np.ascontiguousarray(d[n][:, :, sel]))
+           for n in ("q", "k", "v", "beta", "decay")}
+    h0 = np.ascontiguousarray(d["h0"][:, sel])
+    t0 = time.perf_counter()
+    _, _, used = oracle.forward(sub["q"], sub["k"], sub["v"], sub["beta"], sub["decay"], h0,
+                                threads=threads, return_threads=True)
+    dt = time.perf_counter() - t0
+    tokens_equiv = wl.B * wl.T * heads_in_sample / wl.H
+    return tokens_equiv / dt, dt, used
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle on the host cores, same workload."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    heads = 2
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_prefill_sample(1)
+    vals, secs, used = [], 0.0, 0
+    for _ in range(args.steps):
+        v, dt, used = oracle_prefill_sample(heads)
+        vals.append(v)
+        secs += dt
+    value = statistics.median(vals)
+    wl = WORKLOADS[3]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "dk": wl.dk,
+                   "dv": wl.dv, "chunk_size": wl.chunk},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": f"{heads} of {wl.H} heads x full T={wl.T}, per step; "
+                                   "tokens/s scaled by heads/H"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    # the CPU baseline runs first, before any GPU work, so its threads never share
+    # the process with a live CUDA context being forked
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        v, dt, used = oracle_prefill_sample(2)
+        cpu = {"value": v, "unit": "tokens/s", "cores": used, "kind": "oracle",
+               "sample": f"2 of 32 heads x full T=32768 ({dt:.1f} s); tokens/s scaled by heads/H"}
+
+    import torch
+    world, rank, local = dist_setup()
+    from delta_rule_linear_gb300 import build as b
+    if rank == 0 or world == 1:
+        b.build()
+    barrier(world)
+    import delta_rule_linear_gb300 as kda
+    kda.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+
+    pre = bench_prefill(args, world, rank, dev, peaks)
+    dec = None if args.no_decode else bench_decode(args, world, rank, dev, peaks)
+    if rank != 0:
+        return
+    wl = WORKLOADS[3]
+    pre["roofline"]["peak_source"] = peak_src
+    line = {
+        "metric": METRIC, "value": pre["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "dk": wl.dk,
+                   "dv": wl.dv, "chunk_size": wl.chunk, "state": "fp32 carried in",
+                   "l2_flush": "none: inputs (805 MB) and decode state (512 MiB) exceed L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": pre["roofline"],
+        "cpu_baseline": cpu,
+        "e2e": pre["e2e"],
+        "gpu_launches": pre["gpu_launches"],
+        "clocks": pre["clocks"],
+    }
+    if dec is not None:
+        dec["roofline"]["peak_source"] = peak_src
+        line["decode"] = dec
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

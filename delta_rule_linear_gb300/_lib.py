@@ -1,0 +1,239 @@
+"""ctypes binding of libkda.so (include/kda.h).  Argument marshalling only.
+
+Every compute step runs in the library's CUDA kernels; PyTorch is used here for
+device memory (output, state and workspace tensors) and for the current stream.
+There is no CPU fallback: a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_F32, KDA_BF16 = 0, 1
+STATUS = {
+    0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE",
+    4: "KDA_ERR_UNSUPPORTED", 5: "KDA_ERR_ALIGN", 6: "KDA_ERR_WORKSPACE", 7: "KDA_ERR_CUDA",
+    8: "KDA_ERR_DEVICE_TIMEOUT", 9: "KDA_ERR_INDEX",
+}
+# Every symbol include/kda.h declares.
+EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace", "kda_chunk_fwd",
+           "kda_recurrent_fwd", "kda_decode_step", "kda_varlen_fwd_workspace", "kda_varlen_fwd",
+           "kda_query_device_error")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, where: str, lib=None):
+        msg = STATUS.get(code, str(code))
+        if lib is not None:
+            msg += ": " + lib.kda_status_string(code).decode()
+        super().__init__(f"{where}: {msg}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libkda.so (built in-tree by ``delta_rule_linear_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"libkda.so not found at {p}: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(p)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.kda_status_string.argtypes = [I]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_version.argtypes = []
+        lib.kda_version.restype = I
+        lib.kda_chunk_fwd_workspace.argtypes = [I, I, I, I, I, I, I]
+        lib.kda_chunk_fwd_workspace.restype = Z
+        lib.kda_varlen_fwd_workspace.argtypes = [I, I, I, I, I, I, I]
+        lib.kda_varlen_fwd_workspace.restype = Z
+        lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, Z, P]
+        lib.kda_chunk_fwd.restype = I
+        lib.kda_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+        lib.kda_recurrent_fwd.restype = I
+        lib.kda_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, I, P]
+        lib.kda_decode_step.restype = I
+        lib.kda_varlen_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, I, F, I, I,
+                                       P, Z, P]
+        lib.kda_varlen_fwd.restype = I
+        lib.kda_query_device_error.argtypes = [P, P]
+        lib.kda_query_device_error.restype = I
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _check(t, name, dtype=None, shape=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _raise(code, where, lib):
+    if code != 0:
+        raise KdaError(code, where, lib)
+
+
+def chunk_fwd_workspace_bytes(B, T, H, dk, dv, chunk_size, dtype_code):
+    return int(load().kda_chunk_fwd_workspace(B, T, H, dk, dv, chunk_size, dtype_code))
+
+
+def varlen_fwd_workspace_bytes(N, total_T, H, dk, dv, chunk_size, dtype_code):
+    return int(load().kda_varlen_fwd_workspace(N, total_T, H, dk, dv, chunk_size, dtype_code))
+
+
+def _workspace(nbytes, device, workspace):
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def chunk_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None, chunk_size=64,
+              use_qk_l2norm=True, out=None, final_state=None, workspace=None, stream=None):
+    """kda_chunk_fwd: chunked prefill.  Returns (o [B,T,H,dv], final_state [B,H,dk,dv] fp32)."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, H, dv))
+    _check(beta, "beta", torch.float32, (B, T, H)); _check(decay, "decay", torch.float32, (B, T, H))
+    _check(initial_state, "initial_state", torch.float32, (B, H, dk, dv))
+    o = out if out is not None else torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    _check(o, "out", q.dtype, (B, T, H, dv))
+    hT = final_state if final_state is not None else torch.empty((B, H, dk, dv), dtype=torch.float32,
+                                                                  device=q.device)
+    _check(hT, "final_state", torch.float32, (B, H, dk, dv))
+    need = lib.kda_chunk_fwd_workspace(B, T, H, dk, dv, chunk_size, dt)
+    if need == 0:
+        raise KdaError(4, "kda_chunk_fwd_workspace", lib)
+    ws = _workspace(need, q.device, workspace)
+    rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state),
+                           _ptr(o), _ptr(hT), B, T, H, dk, dv, dt, float(scale or 0.0),
+                           int(chunk_size), int(bool(use_qk_l2norm)), _ptr(ws),
+                           ws.numel() * ws.element_size(), _stream(stream))
+    _raise(rc, "kda_chunk_fwd", lib)
+    return o, hT
+
+
+def recurrent_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None,
+                  use_qk_l2norm=True, out=None, final_state=None, stream=None):
+    """kda_recurrent_fwd: token-by-token prefill.  Returns (o, final_state)."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, H, dv))
+    _check(beta, "beta", torch.float32, (B, T, H)); _check(decay, "decay", torch.float32, (B, T, H))
+    _check(initial_state, "initial_state", torch.float32, (B, H, dk, dv))
+    o = out if out is not None else torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    hT = final_state if final_state is not None else torch.empty((B, H, dk, dv), dtype=torch.float32,
+                                                                  device=q.device)
+    rc = lib.kda_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay),
+                               _ptr(initial_state), _ptr(o), _ptr(hT), B, T, H, dk, dv, dt,
+                               float(scale or 0.0), int(bool(use_qk_l2norm)), _stream(stream))
+    _raise(rc, "kda_recurrent_fwd", lib)
+    return o, hT
+
+
+def decode_step(q, k, v, beta, decay, state, *, scale=None, use_qk_l2norm=True, out=None,
+                stream=None):
+    """kda_decode_step: one token per sequence; ``state`` [B,H,dk,dv] fp32 is updated in place.
+
+    q, k: [B,1,H,dk] (or [B,H,dk]); v: [B,1,H,dv]; beta, decay: [B,1,H] (decay may be None).
+    Returns o with v's shape.
+    """
+    lib = load()
+    B, H, dk, dv = state.shape
+    dt = _dtype_code(q)
+    _check(q, "q"); _check(k, "k", q.dtype); _check(v, "v", q.dtype)
+    _check(beta, "beta", torch.float32); _check(decay, "decay", torch.float32)
+    _check(state, "state", torch.float32)
+    if q.numel() != B * H * dk or v.numel() != B * H * dv or beta.numel() != B * H:
+        raise ValueError("decode inputs do not match the state's [B,H,dk,dv]")
+    o = out if out is not None else torch.empty_like(v)
+    rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(state),
+                             _ptr(o), B, H, dk, dv, dt, float(scale or 0.0),
+                             int(bool(use_qk_l2norm)), _stream(stream))
+    _raise(rc, "kda_decode_step", lib)
+    return o
+
+
+def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_seqlens_cpu=None,
+               scale=None, chunk_size=64, use_qk_l2norm=True, out=None, final_state=None,
+               workspace=None, stream=None):
+    """kda_varlen_fwd: packed sequences [1,total,H,D] split by cu_seqlens [N+1] (int32, device).
+
+    Returns (o [1,total,H,dv], final_state [N,H,dk,dv] fp32).
+    """
+    lib = load()
+    _, total, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dt = _dtype_code(q)
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (1, total, H, dv))
+    _check(beta, "beta", torch.float32, (1, total, H))
+    _check(decay, "decay", torch.float32, (1, total, H))
+    _check(cu_seqlens, "cu_seqlens", torch.int32)
+    _check(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
+    host = None
+    if cu_seqlens_cpu is not None:
+        host = cu_seqlens_cpu.to(torch.int32).contiguous()
+        if host.is_cuda:
+            raise ValueError("cu_seqlens_cpu must be a host tensor")
+    o = out if out is not None else torch.empty((1, total, H, dv), dtype=q.dtype, device=q.device)
+    hT = final_state if final_state is not None else torch.empty((N, H, dk, dv), dtype=torch.float32,
+                                                                  device=q.device)
+    need = lib.kda_varlen_fwd_workspace(N, total, H, dk, dv, chunk_size, dt)
+    if need == 0:
+        raise KdaError(4, "kda_varlen_fwd_workspace", lib)
+    ws = _workspace(need, q.device, workspace)
+    rc = lib.kda_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(cu_seqlens),
+                            _ptr(host), N, total, H, dk, dv, _ptr(initial_state), _ptr(o), _ptr(hT),
+                            dt, float(scale or 0.0), int(chunk_size), int(bool(use_qk_l2norm)),
+                            _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _raise(rc, "kda_varlen_fwd", lib)
+    return o, hT
+
+
+def query_device_error(workspace, stream=None) -> int:
+    """kda_query_device_error: device error word of the last call on ``workspace`` (0 = none)."""
+    return int(load().kda_query_device_error(_ptr(workspace), _stream(stream)))

@@ -1,0 +1,223 @@
+// kda_api.cu -- the C ABI of include/kda.h: argument checks, workspace carving,
+// dispatch to the kernels.  Nothing here allocates device memory.
+#include <math.h>
+#include <string.h>
+
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+
+using namespace kda;
+
+namespace {
+
+constexpr size_t kWsHeader = sizeof(WsHeader);
+
+bool supported_head(int d) { return d == 32 || d == 64 || d == 128; }
+bool supported_chunk(int c) { return c == 16 || c == 32 || c == 64; }
+bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+float resolve_scale(float scale, int dk) { return scale > 0.f ? scale : 1.0f / sqrtf((float)dk); }
+
+// Copies initial_state into final_state (or zero-fills it) for every sequence;
+// used when a call has no tokens to process.
+__global__ void state_passthrough_kernel(const float *h0, float *hT, size_t count) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count;
+         i += (size_t)gridDim.x * blockDim.x)
+        hT[i] = h0 ? h0[i] : 0.f;
+}
+
+kda_status check_common(const void *q, const void *k, const void *v, const float *beta,
+                        const float *decay, const float *h0, const void *o, const float *hT,
+                        long rows, int H, int dk, int dv, kda_dtype dtype) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+    if (H <= 0 || dk <= 0 || dv <= 0 || rows < 0) return KDA_ERR_SHAPE;
+    if (!supported_head(dk) || !supported_head(dv)) return KDA_ERR_UNSUPPORTED;
+    if (rows > 0 && (!q || !k || !v || !beta || !o)) return KDA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(h0) ||
+        !aligned16(hT) || !aligned4(beta) || !aligned4(decay))
+        return KDA_ERR_ALIGN;
+    return KDA_OK;
+}
+
+kda_status launch_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+
+namespace kda {
+cudaError_t launch_state_passthrough(const SeqBatch &a, cudaStream_t s) {
+    if (!a.hT) return cudaSuccess;
+    const size_t count = (size_t)a.nseq * a.H * a.dk * a.dv;
+    if (count == 0) return cudaSuccess;
+    if (a.h0 == a.hT) return cudaSuccess;  // aliasing: already in place
+    const int grid = (int)((count + 255) / 256 < 4096 ? (count + 255) / 256 : 4096);
+    state_passthrough_kernel<<<grid, 256, 0, s>>>(a.h0, a.hT, count);
+    return cudaGetLastError();
+}
+}  // namespace kda
+
+extern "C" {
+
+const char *kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_NULL: return "a required pointer is NULL";
+        case KDA_ERR_SHAPE: return "invalid size";
+        case KDA_ERR_DTYPE: return "unknown dtype";
+        case KDA_ERR_UNSUPPORTED: return "unsupported head dimension or chunk size";
+        case KDA_ERR_ALIGN: return "pointer not aligned (16 bytes for tensors, 4 for beta/decay)";
+        case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDA_ERR_CUDA: return "CUDA launch or runtime error";
+        case KDA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
+        case KDA_ERR_INDEX: return "cu_seqlens invalid (not monotone, or not 0..total_T)";
+    }
+    return "unknown status";
+}
+
+int kda_version(void) { return (0 << 16) | 1; }
+
+size_t kda_chunk_fwd_workspace(int B, int T, int H, int dk, int dv, int chunk_size,
+                               kda_dtype dtype) {
+    if (B < 0 || T < 0 || H <= 0) return 0;
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return 0;
+    if (!supported_head(dk) || !supported_head(dv) || !supported_chunk(chunk_size)) return 0;
+    return kWsHeader;
+}
+
+size_t kda_varlen_fwd_workspace(int N, int total_T, int H, int dk, int dv, int chunk_size,
+                                kda_dtype dtype) {
+    if (N < 0 || total_T < 0 || H <= 0) return 0;
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return 0;
+    if (!supported_head(dk) || !supported_head(dv) || !supported_chunk(chunk_size)) return 0;
+    return kWsHeader;
+}
+
+static kda_status run_prefill(SeqBatch &a, bool chunked, cudaStream_t st) {
+    if (a.nseq == 0) return KDA_OK;
+    if (a.T == 0) return launch_status(launch_state_passthrough(a, st));
+    cudaError_t e = chunked ? launch_chunk_simt(a, st) : launch_recurrent(a, st);
+    return launch_status(e);
+}
+
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *beta,
+                         const float *decay, const float *initial_state, void *o,
+                         float *final_state, int B, int T, int H, int dk, int dv,
+                         kda_dtype dtype, float scale, int chunk_size, int use_qk_l2norm,
+                         void *ws, size_t ws_bytes, kda_stream_t stream) {
+    if (B < 0 || T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, decay, initial_state, o, final_state,
+                                (long)B * T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (!supported_chunk(chunk_size)) return KDA_ERR_UNSUPPORTED;
+    const size_t need = kda_chunk_fwd_workspace(B, T, H, dk, dv, chunk_size, dtype);
+    if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
+    SeqBatch a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = decay; a.h0 = initial_state;
+    a.o = o; a.hT = final_state; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
+    a.dk = dk; a.dv = dv; a.chunk = chunk_size;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    a.ws = static_cast<WsHeader *>(ws);
+    a.ws_body = static_cast<char *>(ws) + kWsHeader;
+    a.ws_body_bytes = ws_bytes - kWsHeader;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
+    return run_prefill(a, true, st);
+}
+
+kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *beta,
+                             const float *decay, const float *initial_state, void *o,
+                             float *final_state, int B, int T, int H, int dk, int dv,
+                             kda_dtype dtype, float scale, int use_qk_l2norm,
+                             kda_stream_t stream) {
+    if (B < 0 || T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, decay, initial_state, o, final_state,
+                                (long)B * T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    SeqBatch a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = decay; a.h0 = initial_state;
+    a.o = o; a.hT = final_state; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
+    a.dk = dk; a.dv = dv; a.chunk = 0;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    return run_prefill(a, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *beta,
+                           const float *decay, float *state, void *o, int B, int H, int dk,
+                           int dv, kda_dtype dtype, float scale, int use_qk_l2norm,
+                           kda_stream_t stream) {
+    if (B < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, decay, state, o, state, B, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (B > 0 && !state) return KDA_ERR_NULL;
+    if (B == 0) return KDA_OK;
+    DecodeArgs a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = decay; a.state = state; a.o = o;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    return launch_status(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_varlen_fwd(const void *q, const void *k, const void *v, const float *beta,
+                          const float *decay, const int *cu_seqlens, const int *cu_seqlens_host,
+                          int N, int total_T, int H, int dk, int dv, const float *initial_state,
+                          void *o, float *final_state, kda_dtype dtype, float scale,
+                          int chunk_size, int use_qk_l2norm, void *ws, size_t ws_bytes,
+                          kda_stream_t stream) {
+    if (N < 0 || total_T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, decay, initial_state, o, final_state,
+                                total_T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (!supported_chunk(chunk_size)) return KDA_ERR_UNSUPPORTED;
+    if (N > 0 && !cu_seqlens) return KDA_ERR_NULL;
+    if (!aligned4(cu_seqlens)) return KDA_ERR_ALIGN;
+    const size_t need = kda_varlen_fwd_workspace(N, total_T, H, dk, dv, chunk_size, dtype);
+    if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
+    int max_len = total_T;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != total_T) return KDA_ERR_INDEX;
+        max_len = 0;
+        for (int n = 0; n < N; ++n) {
+            const int L = cu_seqlens_host[n + 1] - cu_seqlens_host[n];
+            if (L < 0) return KDA_ERR_INDEX;
+            if (L > max_len) max_len = L;
+        }
+    }
+    if (N == 0) return KDA_OK;
+    SeqBatch a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = decay; a.h0 = initial_state;
+    a.o = o; a.hT = final_state; a.cu_seqlens = cu_seqlens; a.nseq = N; a.T = max_len; a.H = H;
+    a.dk = dk; a.dv = dv; a.chunk = chunk_size;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    a.ws = static_cast<WsHeader *>(ws);
+    a.ws_body = static_cast<char *>(ws) + kWsHeader;
+    a.ws_body_bytes = ws_bytes - kWsHeader;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
+    // Every sequence runs the chunk loop from its own cu_seqlens range; a sequence
+    // of length 0 falls through the loop and stores its initial state.
+    return launch_status(launch_chunk_simt(a, st));
+}
+
+kda_status kda_query_device_error(const void *ws, kda_stream_t stream) {
+    if (!ws) return KDA_ERR_NULL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    WsHeader h;
+    if (cudaMemcpyAsync(&h, ws, sizeof(int) * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
+    if (h.error != 0) {
+        if (cudaMemsetAsync(const_cast<void *>(ws), 0, sizeof(int) * 2, st) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
+        return static_cast<kda_status>(h.error);
+    }
+    return KDA_OK;
+}
+
+}  // extern "C"

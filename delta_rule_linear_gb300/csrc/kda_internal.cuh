@@ -1,0 +1,98 @@
+// kda_internal.cuh -- declarations shared by the translation units of libkda.so.
+//
+// The C ABI (include/kda.h) validates arguments on the host and then calls one of
+// the launchers declared here.  Each launcher enqueues its kernels on the given
+// stream and returns the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Element type of q, k, v, o.
+enum class DType : int { F32 = 0, BF16 = 1 };
+
+// Workspace header: the first 256 bytes of every workspace.  Kernels with a
+// bounded wait record the first failure code in `error` (atomicCAS from 0).
+struct WsHeader {
+    int error;          // 0 = none; otherwise a kda_status value
+    int where;          // kernel-defined location of the failure (diagnostic)
+    int pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+// A batch of independent sequences that share H, dk, dv.  Sequence n covers
+// token rows [seq_start(n), seq_start(n) + seq_len(n)) of the flattened
+// [rows, H, D] token arrays.  Equal-length batches use cu_seqlens == nullptr and
+// sequence n = batch entry b starts at b * T; packed varlen batches read the
+// device prefix array cu_seqlens [nseq + 1].
+struct SeqBatch {
+    const void *q;            // [rows, H, dk]   (Tin)
+    const void *k;            // [rows, H, dk]   (Tin)
+    const void *v;            // [rows, H, dv]   (Tin)
+    const float *beta;        // [rows, H]
+    const float *decay;       // [rows, H] or nullptr (zeros)
+    const float *h0;          // [nseq, H, dk, dv] or nullptr (zeros)
+    void *o;                  // [rows, H, dv]   (Tin)
+    float *hT;                // [nseq, H, dk, dv] or nullptr
+    const int *cu_seqlens;    // device [nseq + 1] or nullptr (equal length)
+    int nseq;                 // B (equal length) or N (varlen)
+    int T;                    // equal-length T; varlen: max sequence length (launch sizing)
+    int H, dk, dv;
+    int chunk;
+    DType dtype;
+    float scale;              // already resolved (> 0)
+    int use_l2;
+    WsHeader *ws;             // workspace header (device)
+    void *ws_body;            // workspace after the header
+    size_t ws_body_bytes;
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v;
+    const float *beta, *decay;
+    float *state;
+    void *o;
+    int B, H, dk, dv;
+    DType dtype;
+    float scale;
+    int use_l2;
+};
+
+// Launchers (each returns the cudaGetLastError() status of its launches).
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_recurrent(const SeqBatch &a, cudaStream_t s);
+cudaError_t launch_chunk_simt(const SeqBatch &a, cudaStream_t s);
+size_t chunk_simt_smem_bytes(int dk, int dv, int chunk);
+// Copies (or zero-fills) final_state from initial_state for empty sequences.
+cudaError_t launch_state_passthrough(const SeqBatch &a, cudaStream_t s);
+
+// L2 normalisation floor: x / max(||x||, kNormEps).
+constexpr float kNormEps = 1e-12f;
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Token row range of sequence n.
+__device__ __forceinline__ void seq_range(const SeqBatch &p, int n, long &start, int &len) {
+    if (p.cu_seqlens) {
+        int a = p.cu_seqlens[n], b = p.cu_seqlens[n + 1];
+        start = a;
+        len = b - a;
+    } else {
+        start = (long)n * p.T;
+        len = p.T;
+    }
+}
+
+}  // namespace kda

@@ -1,0 +1,204 @@
+// scan.cu -- single-token decode and the token-by-token (recurrent) prefill.
+//
+// Both run the recurrence of ejkernel kda() ("The core recurrence") one token at
+// a time with the fp32 state held in registers:
+//     r = S^T k^,  p = S^T q~,  u = beta (v - r),
+//     o = alpha p + (k^ . q~) u,  S <- alpha S + k^ u^T,   alpha = exp(decay)
+// (o = h_t^T q~ expanded with h_t = alpha S + k^ u^T; with alpha = 1 this is the
+// step of TileOPs DeltaNetRecurrentFwdOp).
+//
+// One CTA owns one (sequence, head, value-slab) and keeps its [dk x slab] slice of
+// the state in registers: thread (rg, cg) holds float4 column group cg of rows
+// rg, rg + RG, rg + 2RG, ...  A warp therefore touches consecutive rows of one
+// head, i.e. one contiguous stretch of the key-major state: every state access is
+// a coalesced 128-bit load or store, and the state crosses HBM exactly once in
+// and once out per call.  The two reductions over dk (S^T k and S^T q) are
+// in-thread sums followed by one shared-memory pass over the row groups.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+
+struct ScanParams {
+    const void *q, *k, *v;
+    const float *beta, *decay;
+    const float *h0;   // may equal hT (decode updates in place)
+    void *o;
+    float *hT;
+    const int *cu_seqlens;
+    int nseq, T, H, DV;
+    float scale;
+    int use_l2;
+};
+
+template <typename Tin, int DK, int DVS>
+__global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
+    constexpr int TPR = DVS / 4;          // threads per state row (one float4 each)
+    constexpr int RG = kThreads / TPR;    // row groups
+    constexpr int R = DK / RG;            // rows per thread
+    static_assert(R >= 1 && DK % RG == 0, "state slab does not tile the block");
+    static_assert(2 * DK <= kThreads && DVS <= kThreads, "staging assumes small heads");
+
+    __shared__ float s_k[DK], s_q[DK], s_v[DVS];
+    __shared__ __align__(16) float s_u[DVS];
+    __shared__ __align__(16) float s_red[2][RG][DVS];
+    __shared__ float s_sc[8];
+
+    const int nslab = p.DV / DVS;
+    const int slab = blockIdx.x % nslab;
+    const int h = (blockIdx.x / nslab) % p.H;
+    const int n = blockIdx.x / (nslab * p.H);
+    long start;
+    int len;
+    if (p.cu_seqlens) {
+        start = p.cu_seqlens[n];
+        len = p.cu_seqlens[n + 1] - p.cu_seqlens[n];
+    } else {
+        start = (long)n * p.T;
+        len = p.T;
+    }
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid % TPR, rg = tid / TPR;
+    const int col0 = slab * DVS;
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    Tin *o = static_cast<Tin *>(p.o);
+
+    const size_t sbase = ((size_t)n * p.H + h) * DK * p.DV + col0 + 4 * cg;
+    float4 S[R];
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int i = rg + RG * m;
+        S[m] = p.h0 ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)i * p.DV))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    for (int t = 0; t < len; ++t) {
+        const long row = start + t;
+        const size_t qk_off = ((size_t)row * p.H + h) * DK;
+        const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
+        if (tid < DK) s_k[tid] = to_f32(k[qk_off + tid]);
+        else if (tid < 2 * DK) s_q[tid - DK] = to_f32(q[qk_off + tid - DK]);
+        if (tid < DVS) s_v[tid] = to_f32(v[v_off + tid]);
+        if (tid == 0) {
+            s_sc[0] = p.beta[(size_t)row * p.H + h];
+            s_sc[1] = p.decay ? p.decay[(size_t)row * p.H + h] : 0.f;
+        }
+        __syncthreads();
+
+        if (warp < 3) {  // ||k||^2, ||q||^2, k.q
+            float acc = 0.f;
+            for (int i = lane; i < DK; i += 32) {
+                const float a = (warp == 1) ? s_q[i] : s_k[i];
+                const float b = (warp == 0) ? s_k[i] : s_q[i];
+                acc = fmaf(a, b, acc);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) s_sc[2 + warp] = acc;
+        }
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f), pq = r;
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            const int i = rg + RG * m;
+            const float kk = s_k[i], qq = s_q[i];
+            r.x = fmaf(S[m].x, kk, r.x); r.y = fmaf(S[m].y, kk, r.y);
+            r.z = fmaf(S[m].z, kk, r.z); r.w = fmaf(S[m].w, kk, r.w);
+            pq.x = fmaf(S[m].x, qq, pq.x); pq.y = fmaf(S[m].y, qq, pq.y);
+            pq.z = fmaf(S[m].z, qq, pq.z); pq.w = fmaf(S[m].w, qq, pq.w);
+        }
+        *reinterpret_cast<float4 *>(&s_red[0][rg][4 * cg]) = r;
+        *reinterpret_cast<float4 *>(&s_red[1][rg][4 * cg]) = pq;
+        __syncthreads();
+
+        const float kn = p.use_l2 ? 1.f / fmaxf(sqrtf(s_sc[2]), kNormEps) : 1.f;
+        const float qn = p.scale * (p.use_l2 ? 1.f / fmaxf(sqrtf(s_sc[3]), kNormEps) : 1.f);
+        const float alpha = expf(s_sc[1]);
+        if (tid < DVS) {
+            float rs = 0.f, ps = 0.f;
+#pragma unroll 8
+            for (int g = 0; g < RG; ++g) {
+                rs += s_red[0][g][tid];
+                ps += s_red[1][g][tid];
+            }
+            const float u = s_sc[0] * (s_v[tid] - kn * rs);
+            const float out = alpha * (qn * ps) + (kn * qn * s_sc[4]) * u;
+            s_u[tid] = u;
+            o[v_off + tid] = from_f32<Tin>(out);
+        }
+        __syncthreads();
+
+        const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            const float kk = kn * s_k[rg + RG * m];
+            S[m].x = fmaf(alpha, S[m].x, kk * u4.x);
+            S[m].y = fmaf(alpha, S[m].y, kk * u4.y);
+            S[m].z = fmaf(alpha, S[m].z, kk * u4.z);
+            S[m].w = fmaf(alpha, S[m].w, kk * u4.w);
+        }
+        __syncthreads();  // staging buffers are rewritten by the next token
+    }
+
+    if (p.hT) {
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            const int i = rg + RG * m;
+            __stcs(reinterpret_cast<float4 *>(p.hT + sbase + (size_t)i * p.DV), S[m]);
+        }
+    }
+}
+
+template <typename Tin, int DK>
+cudaError_t launch_dk(const ScanParams &p, int dvs, int grid, cudaStream_t s) {
+    switch (dvs) {
+        case 32: scan_kernel<Tin, DK, 32><<<grid, kThreads, 0, s>>>(p); break;
+        case 64: scan_kernel<Tin, DK, 64><<<grid, kThreads, 0, s>>>(p); break;
+        case 128: scan_kernel<Tin, DK, 128><<<grid, kThreads, 0, s>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_typed(const ScanParams &p, int dk, int dvs, int grid, cudaStream_t s) {
+    switch (dk) {
+        case 32: return launch_dk<Tin, 32>(p, dvs, grid, s);
+        case 64: return launch_dk<Tin, 64>(p, dvs, grid, s);
+        case 128: return launch_dk<Tin, 128>(p, dvs, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_scan(const ScanParams &p, DType dt, int dk, int dvs, cudaStream_t s) {
+    const long grid = (long)p.nseq * p.H * (p.DV / dvs);
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    return dt == DType::BF16 ? launch_typed<__nv_bfloat16>(p, dk, dvs, (int)grid, s)
+                             : launch_typed<float>(p, dk, dvs, (int)grid, s);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
+    ScanParams p{};
+    p.q = a.q; p.k = a.k; p.v = a.v; p.beta = a.beta; p.decay = a.decay;
+    p.h0 = a.state; p.hT = a.state; p.o = a.o; p.cu_seqlens = nullptr;
+    p.nseq = a.B; p.T = 1; p.H = a.H; p.DV = a.dv; p.scale = a.scale; p.use_l2 = a.use_l2;
+    return launch_scan(p, a.dtype, a.dk, a.dv, s);  // one CTA per head, whole value width
+}
+
+cudaError_t launch_recurrent(const SeqBatch &a, cudaStream_t s) {
+    ScanParams p{};
+    p.q = a.q; p.k = a.k; p.v = a.v; p.beta = a.beta; p.decay = a.decay;
+    p.h0 = a.h0; p.hT = a.hT; p.o = a.o; p.cu_seqlens = a.cu_seqlens;
+    p.nseq = a.nseq; p.T = a.T; p.H = a.H; p.DV = a.dv; p.scale = a.scale; p.use_l2 = a.use_l2;
+    // 32-column slabs: a long prefill is latency-bound per token, so spread the
+    // independent value columns over more CTAs.
+    return launch_scan(p, a.dtype, a.dk, 32, s);
+}
+
+}  // namespace kda

@@ -1,0 +1,180 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) delta-rule linear-attention forward.
+ *
+ * What is computed (ejkernel "kernels._xla.kernel_delta_attention._interface",
+ * kda(), "The core recurrence"), per batch entry b and head h, with the memory
+ * h_t a [dk, dv] matrix:
+ *
+ *     k^_t = l2(k_t),  q~_t = scale * l2(q_t)          (l2 only if use_qk_l2norm)
+ *     u_t  = beta_t * (v_t - h_{t-1}^T k^_t)
+ *     h_t  = exp(decay_t) * h_{t-1} + k^_t u_t^T
+ *     o_t  = h_t^T q~_t
+ *
+ * h_0 = initial_state (zeros when NULL); final_state = h_T.  scale <= 0 selects
+ * dk^-0.5 (kda() "Parameters": softmax_scale).  decay NULL means zeros, i.e. no
+ * decay (kda() "Parameters": decay).  l2(x) = x / max(||x||, 1e-12).
+ *
+ * Layouts (all row-major and contiguous, element counts not bytes):
+ *   q, k          [B, T, H, dk]    dtype given by `dtype`
+ *   v, o          [B, T, H, dv]    dtype given by `dtype` (o has the dtype of q/v)
+ *   beta, decay   [B, T, H]        float32
+ *   state         [B, H, dk, dv]   float32, key-major (TileOPs "Linear Attention
+ *                                   Operators", GDNFwdOp: key-major fp32 state)
+ * Packed variable-length calls use B == 1, T == total tokens, and one state per
+ * sequence, [N, H, dk, dv] (TileOPs DeltaNetFwdOp: cu_seqlens).
+ *
+ * Ownership: the caller owns every buffer, including the workspace; the library
+ * allocates no device memory and keeps no state between calls.  All pointers
+ * passed to the compute entry points are DEVICE pointers (cudaMalloc'd or
+ * equivalent) unless named *_host.
+ *
+ * Asynchrony and errors: every compute call only enqueues work on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream) and returns.  Argument
+ * errors are detected on the host and returned before anything is enqueued.
+ * A launch failure returns KDA_ERR_CUDA.  No call aborts, throws or traps.
+ * A kernel whose bounded wait runs out records KDA_ERR_DEVICE_TIMEOUT in the
+ * workspace header, read back by kda_query_device_error().
+ *
+ * Supported shapes: dk, dv in {32, 64, 128}; chunk_size in {16, 32, 64}.
+ * The bf16 chunked prefill runs on the tcgen05 tensor-core path when
+ * dk == dv in {64, 128} and chunk_size == 64; every other supported shape runs
+ * on the fp32 CUDA-core chunk path.  Anything else returns KDA_ERR_UNSUPPORTED.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that this header needs no CUDA header. */
+struct CUstream_st;
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,           /* a required pointer is NULL                         */
+    KDA_ERR_SHAPE = 2,          /* a size is negative/zero where it must be positive   */
+    KDA_ERR_DTYPE = 3,          /* unknown kda_dtype                                  */
+    KDA_ERR_UNSUPPORTED = 4,    /* valid but not served (head dims, chunk size)        */
+    KDA_ERR_ALIGN = 5,          /* a pointer is not 16-byte aligned                    */
+    KDA_ERR_WORKSPACE = 6,      /* workspace NULL or smaller than the query returned   */
+    KDA_ERR_CUDA = 7,           /* a CUDA launch or runtime call failed                */
+    KDA_ERR_DEVICE_TIMEOUT = 8, /* a kernel's bounded wait ran out (see above)         */
+    KDA_ERR_INDEX = 9           /* cu_seqlens not monotone / not ending at total_T     */
+} kda_status;
+
+/* Element type of q, k, v and o.  beta, decay and the state are always float32
+ * (TileOPs DeltaNetFwdOp: the recurrent state is FP32). */
+typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *kda_status_string(kda_status s);
+
+/* Library version, (major << 16) | minor. */
+int kda_version(void);
+
+/*
+ * Workspace bytes that kda_chunk_fwd needs for these sizes (host-only query, no
+ * CUDA call).  Always at least 256 bytes (the header that holds the device error
+ * word).  Returns 0 if the sizes are invalid or unsupported.
+ */
+size_t kda_chunk_fwd_workspace(int B, int T, int H, int dk, int dv, int chunk_size,
+                               kda_dtype dtype);
+
+/*
+ * Chunked prefill (kda() "Algorithm Modes": chunked -- parallel inside a chunk,
+ * sequential across chunks; the chunk-local form is the WY / UT-transform
+ * representation that TileOPs DeltaNetChunkFwdOp names prepare_wy_repr -> w, u).
+ *
+ *   q, k, v, beta        inputs, layouts above; must not be NULL when B*T > 0.
+ *   decay                [B,T,H] float32, or NULL for no decay.
+ *   initial_state        [B,H,dk,dv] float32, or NULL for zeros.
+ *   o                    [B,T,H,dv] output, dtype of q.
+ *   final_state          [B,H,dk,dv] float32 output; may alias initial_state
+ *                        (the state is read before it is overwritten), or NULL
+ *                        when the caller does not want it.
+ *   scale                query scale; <= 0 selects dk^-0.5.
+ *   chunk_size           16, 32 or 64 (result does not depend on it beyond rounding).
+ *   use_qk_l2norm        nonzero: L2-normalise q and k rows (kda() default: True).
+ *   ws, ws_bytes         device workspace, at least kda_chunk_fwd_workspace() bytes,
+ *                        16-byte aligned; contents need not be initialised.
+ * T == 0 is allowed: o is untouched and final_state = initial_state (or zeros).
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *beta, const float *decay,
+                         const float *initial_state, void *o, float *final_state,
+                         int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                         float scale, int chunk_size, int use_qk_l2norm,
+                         void *ws, size_t ws_bytes, kda_stream_t stream);
+
+/*
+ * Recurrent prefill (kda() "Algorithm Modes": recurrent -- the pure sequential
+ * scan; kda(use_chunked=False)).  Same arguments as kda_chunk_fwd without the
+ * chunk size; needs no workspace.  One CUDA-core kernel, one token at a time.
+ */
+kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v,
+                             const float *beta, const float *decay,
+                             const float *initial_state, void *o, float *final_state,
+                             int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                             float scale, int use_qk_l2norm, kda_stream_t stream);
+
+/*
+ * Single-token decode (kda() "Algorithm Modes": single-step, seq_len == 1 with
+ * an initial state; TileOPs DeltaNetRecurrentFwdOp gives the decay-free step
+ *   v_new = beta (v - S^T k), o = S^T q + (q.k) v_new, S_new = S + k v_new^T).
+ * With alpha = exp(decay) this kernel computes, per (b, h):
+ *   r = S^T k^, p = S^T q~, u = beta (v - r), o = alpha p + (k^ . q~) u,
+ *   S <- alpha S + k^ u^T           (in place).
+ *   q, k  [B,1,H,dk];  v, o [B,1,H,dv];  beta, decay [B,1,H] (decay may be NULL);
+ *   state [B,H,dk,dv] float32, read and overwritten in place; must not be NULL.
+ * Needs no workspace.  o must not alias any input.
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const float *beta, const float *decay, float *state, void *o,
+                           int B, int H, int dk, int dv, kda_dtype dtype, float scale,
+                           int use_qk_l2norm, kda_stream_t stream);
+
+/* Workspace bytes for kda_varlen_fwd (host-only query).  0 if invalid/unsupported. */
+size_t kda_varlen_fwd_workspace(int N, int total_T, int H, int dk, int dv, int chunk_size,
+                                kda_dtype dtype);
+
+/*
+ * Packed variable-length chunked prefill (TileOPs DeltaNetFwdOp / GDNFwdOp:
+ * token tensors with B == 1, cu_seqlens [N+1] marks the sequences, one state per
+ * sequence; lengths need not be multiples of the chunk size).
+ *   q, k  [1,total_T,H,dk];  v, o [1,total_T,H,dv];  beta, decay [1,total_T,H].
+ *   cu_seqlens        device int32 [N+1], cu_seqlens[0] == 0, non-decreasing,
+ *                     cu_seqlens[N] == total_T.
+ *   cu_seqlens_host   optional host copy of the same array; when given, it is
+ *                     validated (KDA_ERR_INDEX) and used to size the launch;
+ *                     when NULL the device array is trusted as documented.
+ *   initial_state     [N,H,dk,dv] float32 or NULL (zeros);
+ *   final_state       [N,H,dk,dv] float32 or NULL; may alias initial_state.
+ * No chunk crosses a sequence boundary; a sequence of length 0 gets
+ * final_state = initial_state.
+ */
+kda_status kda_varlen_fwd(const void *q, const void *k, const void *v,
+                          const float *beta, const float *decay,
+                          const int *cu_seqlens, const int *cu_seqlens_host,
+                          int N, int total_T, int H, int dk, int dv,
+                          const float *initial_state, void *o, float *final_state,
+                          kda_dtype dtype, float scale, int chunk_size, int use_qk_l2norm,
+                          void *ws, size_t ws_bytes, kda_stream_t stream);
+
+/*
+ * Read the device error word that the kernels of the most recent kda_chunk_fwd /
+ * kda_varlen_fwd call on `ws` recorded (KDA_OK if none), then clear it.  Each of
+ * those calls clears the word on its stream before its kernels run.
+ * Synchronises `stream`; use the stream of that call.
+ */
+kda_status kda_query_device_error(const void *ws, kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,139 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared symbol,
+answers workspace queries, and rejects bad arguments before touching the device.
+
+None of these calls reaches a CUDA launch (argument errors return first), so they
+run without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from delta_rule_linear_gb300 import build as b
+    b.build()
+    from delta_rule_linear_gb300 import _lib
+    return _lib.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(kda_[a-z_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    for n in ("kda_chunk_fwd", "kda_decode_step", "kda_varlen_fwd", "kda_chunk_fwd_workspace",
+              "kda_varlen_fwd_workspace", "kda_query_device_error", "kda_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from delta_rule_linear_gb300 import _lib
+    names = _declared_functions()
+    assert set(_lib.EXPORTS) == set(names), (set(_lib.EXPORTS) ^ set(names))
+    for n in names:
+        assert hasattr(lib, n), f"libkda.so does not export {n}"
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = lib.kda_status_string(code)
+        assert s and isinstance(s, bytes)
+    assert lib.kda_status_string(0) == b"ok"
+    assert lib.kda_status_string(1234) == b"unknown status"
+
+
+def test_workspace_queries(lib):
+    assert lib.kda_chunk_fwd_workspace(2, 2048, 16, 128, 128, 64, 1) >= 256
+    assert lib.kda_chunk_fwd_workspace(1, 64, 2, 32, 32, 16, 0) >= 256
+    assert lib.kda_chunk_fwd_workspace(1, 64, 2, 48, 32, 16, 0) == 0      # unsupported dk
+    assert lib.kda_chunk_fwd_workspace(1, 64, 2, 32, 32, 24, 0) == 0      # unsupported chunk
+    assert lib.kda_chunk_fwd_workspace(-1, 64, 2, 32, 32, 16, 0) == 0
+    assert lib.kda_chunk_fwd_workspace(1, 64, 2, 32, 32, 16, 7) == 0      # bad dtype
+    assert lib.kda_varlen_fwd_workspace(16, 34816, 16, 64, 64, 64, 1) >= 256
+    assert lib.kda_varlen_fwd_workspace(16, 34816, 0, 64, 64, 64, 1) == 0
+
+
+def _fake(addr=0x1000):
+    return ctypes.c_void_p(addr)
+
+
+def _chunk(lib, **kw):
+    a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), decay=None, h0=None, o=_fake(),
+             hT=None, B=1, T=64, H=2, dk=32, dv=32, dt=0, scale=0.0, chunk=16, l2=1,
+             ws=_fake(), ws_bytes=256, stream=None)
+    a.update(kw)
+    return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["beta"], a["decay"], a["h0"], a["o"],
+                             a["hT"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["dt"],
+                             a["scale"], a["chunk"], a["l2"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_chunk_fwd_rejects_bad_arguments(lib):
+    assert _chunk(lib, q=None) == 1                 # KDA_ERR_NULL
+    assert _chunk(lib, beta=None) == 1
+    assert _chunk(lib, B=-1) == 2                   # KDA_ERR_SHAPE
+    assert _chunk(lib, H=0) == 2
+    assert _chunk(lib, dt=5) == 3                   # KDA_ERR_DTYPE
+    assert _chunk(lib, dk=48) == 4                  # KDA_ERR_UNSUPPORTED
+    assert _chunk(lib, dv=256) == 4
+    assert _chunk(lib, chunk=128) == 4
+    assert _chunk(lib, q=_fake(0x1008)) == 5        # KDA_ERR_ALIGN
+    assert _chunk(lib, beta=_fake(0x1002)) == 5
+    assert _chunk(lib, ws=None) == 6                # KDA_ERR_WORKSPACE
+    assert _chunk(lib, ws_bytes=8) == 6
+    assert _chunk(lib, ws=_fake(0x1004)) == 5
+
+
+def test_decode_rejects_bad_arguments(lib):
+    def call(**kw):
+        a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), decay=None, state=_fake(),
+                 o=_fake(), B=4, H=2, dk=64, dv=64, dt=1, scale=0.0, l2=1, stream=None)
+        a.update(kw)
+        return lib.kda_decode_step(a["q"], a["k"], a["v"], a["beta"], a["decay"], a["state"],
+                                   a["o"], a["B"], a["H"], a["dk"], a["dv"], a["dt"], a["scale"],
+                                   a["l2"], a["stream"])
+    assert call(state=None) == 1
+    assert call(k=None) == 1
+    assert call(B=-2) == 2
+    assert call(dk=96) == 4
+    assert call(state=_fake(0x1010 + 4)) == 5
+    assert call(B=0) == 0                           # nothing to do, no launch
+
+
+def test_varlen_rejects_bad_cu_seqlens(lib):
+    def call(host, N=3, total=10, **kw):
+        hs = (ctypes.c_int * len(host))(*host)
+        a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), decay=None, cu=_fake(),
+                 h0=None, o=_fake(), hT=None, H=2, dk=64, dv=64, dt=1, chunk=64, l2=1,
+                 ws=_fake(), ws_bytes=256)
+        a.update(kw)
+        return lib.kda_varlen_fwd(a["q"], a["k"], a["v"], a["beta"], a["decay"], a["cu"],
+                                  ctypes.cast(hs, ctypes.c_void_p), N, total, a["H"], a["dk"],
+                                  a["dv"], a["h0"], a["o"], a["hT"], a["dt"], 0.0, a["chunk"],
+                                  a["l2"], a["ws"], a["ws_bytes"], None)
+    assert call([0, 4, 3, 10]) == 9                 # not monotone
+    assert call([1, 4, 6, 10]) == 9                 # does not start at 0
+    assert call([0, 4, 6, 9]) == 9                  # does not end at total_T
+    assert call([0, 4, 6, 10], cu=None) == 1
+    assert call([0, 4, 6, 10], chunk=48) == 4
+
+
+def test_query_device_error_rejects_null(lib):
+    assert lib.kda_query_device_error(None, None) == 1
+
+
+def test_python_binding_refuses_host_tensors():
+    import torch
+    import delta_rule_linear_gb300 as kda
+    x = torch.zeros(1, 4, 1, 32)
+    with pytest.raises(ValueError):
+        kda.chunk_fwd(x, x, x, torch.zeros(1, 4, 1), chunk_size=16)
