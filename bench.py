@@ -145,12 +145,11 @@ def to_dev(x, dev, dtype):
 
 
 # --------------------------------------------------------------------------- prefill
-def bench_prefill(args, world, rank, dev, peaks):
+def bench_prefill(args, world, rank, dev, peaks, d):
     import torch
     import delta_rule_linear_gb300 as kda
 
     wl = WORKLOADS[3]
-    d = make_prefill(wl, seed=rank)
     q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
     beta, decay, h0 = (to_dev(d[n], dev, torch.float32) for n in ("beta", "decay", "h0"))
     B, T, H, dk, dv, C = wl.B, wl.T, wl.H, wl.dk, wl.dv, wl.chunk
@@ -282,11 +281,10 @@ def bench_decode(args, world, rank, dev, peaks):
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def oracle_prefill_sample(heads_in_sample, seed=0, threads=0):
-    """Time the fp64 oracle on `heads_in_sample` heads of the long-sequence workload."""
+def oracle_prefill_sample(d, heads_in_sample, threads=0):
+    """Time the fp64 oracle on the first `heads_in_sample` heads of the long-sequence workload."""
     import oracle
     wl = WORKLOADS[3]
-    d = make_prefill(wl, seed=seed)
     sel = list(range(heads_in_sample))
     sub = {n: (None if d[n] is None else np.ascontiguousarray(d[n][:, :, sel]))
            for n in ("q", "k", "v", "beta", "decay")}
@@ -300,21 +298,25 @@ def oracle_prefill_sample(heads_in_sample, seed=0, threads=0):
 
 
 def run_reference(args, world, rank):
-    """The reference arm: the fp64 CPU oracle on the host cores, same workload."""
+    """The reference arm: the fp64 CPU oracle on the host cores, same workload.
+
+    Each step runs the oracle on 8 of the 32 heads over the full T (about a
+    second of wall time on 16 cores); tokens/s is scaled by the head fraction."""
     if rank != 0:
         return
     import oracle
     oracle.build()
-    heads = 2
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        oracle_prefill_sample(1)
+    wl = WORKLOADS[3]
+    d = make_prefill(wl, seed=0)
+    heads = 8
+    for _ in range(min(args.warmup, 1)):
+        oracle_prefill_sample(d, 1)
     vals, secs, used = [], 0.0, 0
     for _ in range(args.steps):
-        v, dt, used = oracle_prefill_sample(heads)
+        v, dt, used = oracle_prefill_sample(d, heads)
         vals.append(v)
         secs += dt
     value = statistics.median(vals)
-    wl = WORKLOADS[3]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -338,7 +340,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="run one workload (profiling); the default runs both")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -347,15 +350,18 @@ def main():
         run_reference(args, world, rank)
         return
 
-    # the CPU baseline runs first, before any GPU work, so its threads never share
-    # the process with a live CUDA context being forked
+    # inputs of the prefill workload are drawn once; the CPU baseline runs on them
+    # first, before any CUDA work starts in this process
+    d = make_prefill(WORKLOADS[3], seed=rank) if args.only != "decode" else None
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and d is not None:
         import oracle
         oracle.build()
-        v, dt, used = oracle_prefill_sample(2)
+        heads = WORKLOADS[3].H
+        v, dt, used = oracle_prefill_sample(d, heads)
         cpu = {"value": v, "unit": "tokens/s", "cores": used, "kind": "oracle",
-               "sample": f"2 of 32 heads x full T=32768 ({dt:.1f} s); tokens/s scaled by heads/H"}
+               "sample": f"all {heads} heads x full T=32768, fp64 per-token scan, "
+                         f"{dt:.1f} s wall on {used} threads"}
 
     import torch
     world, rank, local = dist_setup()
@@ -369,9 +375,12 @@ def main():
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
 
-    pre = bench_prefill(args, world, rank, dev, peaks)
-    dec = None if args.no_decode else bench_decode(args, world, rank, dev, peaks)
+    pre = bench_prefill(args, world, rank, dev, peaks, d) if d is not None else None
+    dec = bench_decode(args, world, rank, dev, peaks) if args.only != "prefill" else None
     if rank != 0:
+        return
+    if pre is None:
+        print(json.dumps({"metric": METRIC, "workload": "decode only", "decode": dec}), flush=True)
         return
     wl = WORKLOADS[3]
     pre["roofline"]["peak_source"] = peak_src
