@@ -34,6 +34,10 @@ from kda_inputs import WORKLOADS, make_decode_state, make_decode_step, make_pref
 
 METRIC = "prefill tokens/s & % bf16 TC peak; decode state GB/s vs HBM peak (1×GB300)"
 NOMINAL_HBM_GBS = 8000.0
+# DRAM bytes (read + write) per launch from one ncu capture of the kernel as it is
+# now; set to None whenever that kernel changes until it is captured again.
+#   decode: profiles/decode_scan_kernel_b256_h32_d128.md
+NCU_TRAFFIC = {"decode": 543.35e6 + 478.43e6, "prefill": None}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -221,7 +225,7 @@ def bench_prefill(args, world, rank, dev, peaks, d):
         "ms": ms_max, "tokens_per_s": tokens * world / (ms_max * 1e-3),
         "clocks": clk.summary(),
         "roofline": {"bound": "tensor", "achieved": round(achieved_tf, 3), "peak": peak_tf,
-                     "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 5), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 5), "traffic": NCU_TRAFFIC["prefill"],
                      "kernel": "chunk prefill (whole step)",
                      "flops_per_launch": flops,
                      "hbm_frac_of_min_bytes": round(min_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5)},
@@ -272,7 +276,7 @@ def bench_decode(args, world, rank, dev, peaks):
         "state_GBps": state_bytes * world / (ms_max * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                     "frac_of_8TBps_nominal": round(gbs / NOMINAL_HBM_GBS, 4), "traffic": None,
+                     "frac_of_8TBps_nominal": round(gbs / NOMINAL_HBM_GBS, 4), "traffic": NCU_TRAFFIC["decode"],
                      "kernel": "decode step", "bytes_per_launch": state_bytes},
         "clocks": clk.summary(),
         "gpu_launches": nsteps,
