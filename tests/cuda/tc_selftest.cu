@@ -174,6 +174,85 @@ __global__ void gemm_tma_kernel(const __grid_constant__ CUtensorMap mapA,
     if (warp == 0) tmem_dealloc(tm, tcols);
 }
 
+// Probe of the TMEM placement of an M=64 result and of MN-major sub-block addressing:
+// D = A[64][K] * B[K][N0..N0+N) where B is staged as an MN-major SW128 tile 64 elements
+// wide and the descriptor starts n_off elements (a multiple of 8) into each row.
+// Every one of the 128 TMEM lanes x N columns is copied to D[128][N], so the host can
+// see which lanes hold the 64 result rows.
+__global__ void gemm_m64_probe_kernel(const __nv_bfloat16 *A, const __nv_bfloat16 *B, float *D,
+                                      int N, int K, int n_off, uint32_t tcols, int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const int kp = ((K + 63) / 64) * 64;
+    uint8_t *sA = smem;                 // K-major, 64 rows
+    uint8_t *sB = sA + 64 * kp * 2;     // MN-major, one 64-wide block
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tbase;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int idx = tid; idx < 64 * K; idx += blockDim.x) {
+        const int r = idx / K, k = idx % K;
+        *reinterpret_cast<__nv_bfloat16 *>(sA + kmajor_sw128_offset(64, r, k)) = A[idx];
+    }
+    for (int idx = tid; idx < K * 64; idx += blockDim.x) {
+        const int k = idx / 64, n = idx % 64;
+        *reinterpret_cast<__nv_bfloat16 *>(sB + mnmajor_sw128_offset(K, n, k)) = B[idx];
+    }
+    fence_proxy_async();
+    if (warp == 0) {
+        tmem_alloc(&tbase, tcols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tbase;
+    // clear every lane of the N columns first so that untouched lanes read as zero
+    {
+        uint32_t z[16];
+        for (int j = 0; j < 16; ++j) z[j] = 0u;
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            asm volatile(
+                "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+                    tm + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0),
+                "r"(z[0]), "r"(z[1]), "r"(z[2]), "r"(z[3]), "r"(z[4]), "r"(z[5]), "r"(z[6]),
+                "r"(z[7]), "r"(z[8]), "r"(z[9]), "r"(z[10]), "r"(z[11]), "r"(z[12]), "r"(z[13]),
+                "r"(z[14]), "r"(z[15])
+                : "memory");
+        }
+        tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        const uint32_t idesc = idesc_bf16_f32(64, N, false, true);
+        const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB) + (uint32_t)n_off * 2u;
+        for (int ks = 0; ks < K / 16; ++ks)
+            mma_bf16_ss(tm, desc_kmajor_sw128(a0, 64, ks), desc_mnmajor_sw128(b0, K, ks), idesc,
+                        ks > 0 ? 1u : 0u);
+        mma_commit(&bar);
+    }
+    const bool ok = mbar_wait(&bar, 0, kWaitNs);
+    if (!ok && lane == 0) atomicExch(status, 1);
+    tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(tm + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, r);
+            tmem_ld_wait();
+            for (int j = 0; j < 16; ++j) D[(32 * warp + lane) * N + c0 + j] = __uint_as_float(r[j]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, tcols);
+}
+
 bool map2d(CUtensorMap *m, const void *base, int rows, int cols, int box_rows) {
     const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
     const uint64_t strides[1] = {(uint64_t)cols * 2};
@@ -238,6 +317,24 @@ extern "C" int selftest_gemm_tma(const void *A, const void *B, float *D, int N, 
     const size_t smem = 1024 + (size_t)128 * K * 2 + (size_t)K * N * 2;
     cudaFuncSetAttribute(gemm_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     gemm_tma_kernel<<<1, 128, smem>>>(ma, mb, D, N, K, tmem_cols_for(N), st);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return 1000 + (int)e;
+    return finish(st);
+}
+
+extern "C" int selftest_gemm_m64_probe(const void *A, const void *B, float *D, int N, int K,
+                                       int n_off) {
+    if (K % 16 || K > 256 || N % 16 || N < 16 || n_off % 8 || n_off + N > 64) return -1;
+    int *st;
+    cudaMalloc(&st, sizeof(int));
+    cudaMemset(st, 0, sizeof(int));
+    const int kp = ((K + 63) / 64) * 64;
+    const size_t smem = 1024 + (size_t)64 * kp * 2 + (size_t)K * 64 * 2;
+    cudaFuncSetAttribute(gemm_m64_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    gemm_m64_probe_kernel<<<1, 128, smem>>>(static_cast<const __nv_bfloat16 *>(A),
+                                            static_cast<const __nv_bfloat16 *>(B), D, N, K, n_off,
+                                            tmem_cols_for(N), st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return 1000 + (int)e;
     return finish(st);

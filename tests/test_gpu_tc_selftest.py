@@ -82,3 +82,27 @@ def test_mma_from_tma_operands(lib, N, K):
     ref = _ref(A, B)
     err = np.max(np.abs(dD.cpu().numpy() - ref)) / np.max(np.abs(ref))
     assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("N,K,n_off", [(64, 64, 0), (32, 64, 0), (32, 64, 32), (16, 128, 48),
+                                       (32, 192, 32)])
+def test_m64_result_lanes_and_mn_offset(lib, N, K, n_off):
+    """An M=64 MMA leaves result row r in TMEM lane r (lanes 64..127 untouched), and an
+    MN-major operand can start n_off elements into its 128-byte swizzle rows."""
+    import torch
+    lib.selftest_gemm_m64_probe.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3
+    rng = np.random.default_rng(N + K + n_off)
+    A, B = _bf16(rng, (64, K)), _bf16(rng, (K, 64))
+    dA, dB = A.cuda(), B.cuda()
+    dD = torch.full((128, N), 7.0, dtype=torch.float32, device="cuda")
+    rc = lib.selftest_gemm_m64_probe(dA.data_ptr(), dB.data_ptr(), dD.data_ptr(), N, K, n_off)
+    assert rc == 0, rc
+    D = dD.cpu().numpy()
+    ref = A.double().numpy() @ B.double().numpy()[:, n_off:n_off + N]
+    scale = np.max(np.abs(ref))
+    h1 = np.max(np.abs(D[:64] - ref)) / scale
+    lanes = np.array([32 * (r // 16) + r % 16 for r in range(64)])
+    h2 = np.max(np.abs(D[lanes] - ref)) / scale
+    print(f"M=64 N={N} K={K} off={n_off}: rows-in-lanes-0..63 err {h1:.2e}, "
+          f"16-rows-per-quadrant err {h2:.2e}")
+    assert h1 < 1e-5 and np.all(D[64:] == 0.0), (h1, h2)
