@@ -1,0 +1,884 @@
+// chunk_tc.cu -- bf16 chunked prefill on the tcgen05 tensor cores (sm_103a).
+//
+// Chunked mode of ejkernel kda() ("Algorithm Modes": parallel inside a chunk,
+// sequential across chunks) for dk = dv = D in {64, 128}, chunk C = 64.  With the
+// chunk-local quantities of the WY / UT-transform form (the representation TileOPs
+// DeltaNetChunkFwdOp computes as prepare_wy_repr -> w, u),
+//
+//   L[t][s] = beta_t (k^_t . k^_s) exp(G_{t-1} - G_s)   (s < t),   T = (I + L)^{-1}
+//   P  = T diag(beta),   W = P diag(exp G_{t-1}) K^,   K~_s = exp(G_C - G_s) k^_s
+//   Aqk[t][s] = (q~_t . k^_s) exp(G_t - G_s)            (s <= t)
+//
+// one chunk maps the state S it starts from and its values V to the next state and
+// its outputs by a single affine map:
+//
+//   [ S_next ]   [ exp(G_C) I - K~^T W    K~^T P  ] [ S ]
+//   [   O    ] = [ diag(exp G) Q~ - Aqk W  Aqk P   ] [ V ]      =:  E_c [S; V]
+//
+// (S_next = exp(G_C) S + K~^T U and O = diag(exp G) Q~ S + Aqk U with U = P V - W S.)
+// E_c does not depend on the state, so it is built for every chunk in parallel:
+//
+//  * prep_kernel  -- one CTA per (sequence, head, chunk): TMA loads q, k; tcgen05
+//    products [K;Q] K^T, K^T diag(f) [T'|P], Aqk [T'|P], Z k; a blocked fp32
+//    forward-substitution inverse on CUDA cores; writes E_c (bf16) to scratch.
+//  * chain_kernel -- one CTA per (sequence, head, value tile): walks the chunks in
+//    order; per chunk ONE dependent tensor-core product D = E_c [S; V_tile] gives the
+//    next state (fp32 in TMEM, stored back as the bf16 operand) and the outputs.
+//    A producer warp streams E_c and V by TMA two chunks ahead; an MMA warp issues;
+//    four epilogue warps turn the next state into the next operand and store o.
+//
+// Every wait on an mbarrier is bounded; on time-out the kernel records
+// KDA_ERR_DEVICE_TIMEOUT in the workspace header and unwinds (no trap).
+#include "kda_internal.cuh"
+#include "tc_ptx.cuh"
+#include "tma_host.cuh"
+
+namespace kda {
+namespace {
+
+using namespace ptx;
+
+constexpr int kC = 64;                        // chunk length
+constexpr uint64_t kWaitNs = 2000000000ull;   // bounded waits: 2 s
+constexpr int kStatusDeviceTimeout = 8;       // KDA_ERR_DEVICE_TIMEOUT
+
+struct TcParams {
+    int nseq, H, T;            // T: equal-length sequence length (unused for varlen)
+    int use_l2;
+    float scale;
+    const int *cu_seqlens;     // nullptr: equal length
+    const int *chunk_base;     // varlen: [nseq + 1] chunk prefix, device
+    int nc_equal;              // equal length: chunks per sequence
+    const float *beta, *decay; // [rows, H]
+    const float *h0;           // [nseq, H, D, D] or nullptr
+    float *hT;                 // [nseq, H, D, D] or nullptr
+    __nv_bfloat16 *o;          // [rows, H, D]
+    __nv_bfloat16 *E;          // scratch: [slots][D + 64][D + 64]
+    WsHeader *ws;
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void record_error(WsHeader *ws, int where) {
+    if (ws && atomicCAS(&ws->error, 0, kStatusDeviceTimeout) == 0) ws->where = where;
+}
+
+__device__ __forceinline__ void seq_info(const TcParams &p, int n, long &start, int &len) {
+    if (p.cu_seqlens) {
+        start = p.cu_seqlens[n];
+        len = p.cu_seqlens[n + 1] - p.cu_seqlens[n];
+    } else {
+        start = (long)n * p.T;
+        len = p.T;
+    }
+}
+__device__ __forceinline__ int chunk_base_of(const TcParams &p, int n) {
+    return p.cu_seqlens ? p.chunk_base[n] : n * p.nc_equal;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---------------------------------------------------------------------------------
+// T = (I + L)^{-1} for a 64 x 64 strictly-lower L, fp32 in shared memory (row pitch
+// 65), by 128 threads: the four 16 x 16 diagonal blocks by column-wise forward
+// substitution, then the off-diagonal blocks by distance from the diagonal,
+//   T_ij = -T_ii sum_{k=j}^{i-1} L_ik T_kj.
+// The unused upper blocks of L hold the partial sums X_ij.
+// ---------------------------------------------------------------------------------
+__device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
+    constexpr int P = 65;
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane < 16) {
+        const int b0 = 16 * warp, j = lane, col = b0 + j;
+        for (int r = 0; r < 16; ++r) {
+            const int row = b0 + r;
+            float x = (r == j) ? 1.f : 0.f;
+            for (int s = j; s < r; ++s) x = fmaf(-sL[row * P + b0 + s], sT[(b0 + s) * P + col], x);
+            sT[row * P + col] = x;
+        }
+    }
+    for (int idx = tid; idx < 64 * 64; idx += 128) {
+        const int r = idx >> 6, c = idx & 63;
+        if ((c >> 4) > (r >> 4)) sT[r * P + c] = 0.f;
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {
+        const int nblk = 4 - d;
+        for (int e = tid; e < nblk * 256; e += 128) {
+            const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int j = b, i = b + d;
+            float x = 0.f;
+            for (int k = j; k < i; ++k)
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    x = fmaf(sL[(16 * i + r) * P + 16 * k + m], sT[(16 * k + m) * P + 16 * j + cc], x);
+            sL[(16 * j + r) * P + 16 * i + cc] = x;
+        }
+        __syncthreads();
+        for (int e = tid; e < nblk * 256; e += 128) {
+            const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int j = b, i = b + d;
+            float x = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                x = fmaf(sT[(16 * i + r) * P + 16 * i + m], sL[(16 * j + m) * P + 16 * i + cc], x);
+            sT[(16 * i + r) * P + 16 * j + cc] = -x;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// prep_kernel
+// ---------------------------------------------------------------------------------
+template <int D>
+struct PrepSmem {
+    static constexpr int NB = D / 64;
+    static constexpr int KQ = 0;                      // [K;Q] tile, K-major SW128: NB x 16 KB
+    static constexpr int R1 = KQ + NB * 16384;        // L, T fp32 [64][65]; later Z1, Z2
+    static constexpr int R2 = R1 + 33792;             // Bf, B: MN-major [64 t][128], 16 KB each
+    static constexpr int R3 = R2 + 32768;             // Aqk: K-major [64 t][64 s], 8 KB
+    static constexpr int MISC = R3 + 8192;            // per-token scalars
+    static constexpr int BYTES = MISC + 10 * 64 * 4 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) prep_kernel(const __grid_constant__ CUtensorMap map_q,
+                                                   const __grid_constant__ CUtensorMap map_k,
+                                                   TcParams p) {
+    using Ly = PrepSmem<D>;
+    constexpr int NB = D / 64;
+    constexpr int R = D + 64;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_fail;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int g = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    int n, c;
+    if (p.cu_seqlens) {
+        if (g >= p.chunk_base[p.nseq]) return;
+        int lo = 0, hi = p.nseq;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.chunk_base[mid] <= g) lo = mid; else hi = mid;
+        }
+        n = lo;
+        c = g - p.chunk_base[n];
+    } else {
+        n = g / p.nc_equal;
+        c = g % p.nc_equal;
+    }
+    long start;
+    int len;
+    seq_info(p, n, start, len);
+    const long row0 = start + (long)c * kC;
+    const int nv = min(kC, len - c * kC);
+    __nv_bfloat16 *Eout = p.E + ((long)(chunk_base_of(p, n) + c) * p.H + h) * (long)(R * R);
+
+    uint8_t *sKQ = sm + Ly::KQ;
+    float *sL = reinterpret_cast<float *>(sm + Ly::R1);
+    float *sT = sL + 64 * 65;
+    uint8_t *sZ1 = sm + Ly::R1;
+    uint8_t *sZ2 = sm + Ly::R1 + D * 128;
+    uint8_t *sBf = sm + Ly::R2;
+    uint8_t *sB = sm + Ly::R2 + 16384;
+    uint8_t *sA = sm + Ly::R3;
+    float *mbeta = reinterpret_cast<float *>(sm + Ly::MISC);
+    float *mdec = mbeta + 64, *mG = mdec + 64, *mGp = mG + 64, *mkn = mGp + 64, *mqn = mkn + 64;
+    float *mf = mqn + 64, *meg = mf + 64, *mcw = meg + 64;
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        s_fail = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_slot;
+    const uint32_t tq = (uint32_t)(32 * warp) << 16;   // this warp's TMEM lane quadrant
+
+    if (tid == 0) {
+        mbar_expect_tx(&bar_tma, NB * 2 * 64 * 128);
+        for (int kb = 0; kb < NB; ++kb) {
+            tma_load_3d(sKQ + kb * 16384, &map_k, &bar_tma, kb * 64, h, (int)row0);
+            tma_load_3d(sKQ + kb * 16384 + 8192, &map_q, &bar_tma, kb * 64, h, (int)row0);
+        }
+    }
+    if (tid < 64) {
+        const long gi = (row0 + tid) * p.H + h;
+        mbeta[tid] = tid < nv ? p.beta[gi] : 0.f;
+        mdec[tid] = (tid < nv && p.decay) ? p.decay[gi] : 0.f;
+    }
+    __syncthreads();
+    if (tid < 64) {   // in-chunk cumulative log-decay, G_{t-1} and G_t
+        float run = 0.f;
+        for (int r = 0; r < tid; ++r) run += mdec[r];
+        mGp[tid] = run;
+        run += mdec[tid];
+        mG[tid] = run;
+        meg[tid] = expf(run);
+    }
+    if (!mbar_wait(&bar_tma, 0, kWaitNs)) s_fail = 1;
+    __syncthreads();
+    bool ok = s_fail == 0;
+
+    // ---- MMA1: D1[0:128, 0:64] = [K; Q] K^T  (contraction over the head dim)
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16_f32(128, 64, false, false);
+        const uint32_t a0 = smem_u32(sKQ);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16_ss(tm, desc_kmajor_sw128(a0, 128, ks), desc_kmajor_sw128(a0, 128, ks), id,
+                        ks > 0 ? 1u : 0u);
+        mma_commit(&bar_mma);
+    }
+    if (tid >= 64 && ok) {   // query norms (the swizzle only permutes a row's chunks)
+        const int t = tid - 64;
+        float ss = 0.f;
+        for (int kb = 0; kb < NB; ++kb) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(sKQ + kb * 16384 + 8192 + t * 128);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 w = row[j];
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = bf16lo(ws[e]), b = bf16hi(ws[e]);
+                    ss = fmaf(a, a, fmaf(b, b, ss));
+                }
+            }
+        }
+        mqn[t] = p.use_l2 ? p.scale / fmaxf(sqrtf(ss), kNormEps) : p.scale;
+    }
+    if (ok && !mbar_wait(&bar_mma, 0, kWaitNs)) s_fail = 1;
+    tc_fence_after();
+
+    // ---- epilogue 1: norms, L (fp32, smem) and Aqk (bf16 operand)
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tm + tq + 0, r0);
+    tmem_ld32(tm + tq + 32, r1);
+    tmem_ld_wait();
+    if (tid < 64) {
+        float diag = 0.f;
+#pragma unroll
+        for (int s = 0; s < 32; ++s) {
+            if (s == tid) diag = __uint_as_float(r0[s]);
+            if (s + 32 == tid) diag = __uint_as_float(r1[s]);
+        }
+        mkn[tid] = p.use_l2 ? 1.f / fmaxf(sqrtf(diag), kNormEps) : 1.f;
+    }
+    __syncthreads();
+    ok = s_fail == 0;
+    const float gC = mG[63];
+    if (tid < 64) {
+        const int t = tid;
+        const float kt = mkn[t], bt = mbeta[t], gpt = mGp[t];
+        mf[t] = t < nv ? expf(gC - mG[t]) * kt : 0.f;
+        mcw[t] = mbeta[t] * expf(gpt) * kt;    // column weight of T' = T diag(beta e^{G_{s-1}} kn_s)
+        float *Lrow = sL + t * 65;
+#pragma unroll
+        for (int s = 0; s < 64; ++s) {
+            const float gram = __uint_as_float(s < 32 ? r0[s] : r1[s - 32]);
+            Lrow[s] = (s < t && t < nv) ? bt * kt * mkn[s] * gram * expf(gpt - mG[s]) : 0.f;
+        }
+    } else {
+        const int t = tid - 64;
+        const float qt = mqn[t], gt = mG[t];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float v2[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int s = cc * 8 + e * 2 + u;
+                    const float qk = __uint_as_float(s < 32 ? r0[s] : r1[s - 32]);
+                    v2[u] = (s <= t && t < nv) ? qt * mkn[s] * qk * expf(gt - mG[s]) : 0.f;
+                }
+                pk[e] = pack_bf16(v2[0], v2[1]);
+            }
+            *reinterpret_cast<uint4 *>(sA + t * 128 + ((cc ^ (t & 7)) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+    fence_proxy_async();
+    __syncthreads();
+
+    // ---- T = (I + L)^{-1}
+    invert_unit_lower_64(sL, sT, tid);
+
+    // ---- B = [T' | P], Bf = diag(f) B   (MN-major: row t, columns s)
+    {
+        const int t = tid >> 1, half = tid & 1;
+        const float *Trow = sT + t * 65;
+        const float ft = mf[t];
+        uint8_t *dB = sB + half * 8192 + t * 128;
+        uint8_t *dBf = sBf + half * 8192 + t * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+            uint32_t pk[4], pf[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s = cc * 8 + e * 2;
+                const float w0 = half ? mbeta[s] : mcw[s];
+                const float w1 = half ? mbeta[s + 1] : mcw[s + 1];
+                const float a = Trow[s] * w0, b = Trow[s + 1] * w1;
+                pk[e] = pack_bf16(a, b);
+                pf[e] = pack_bf16(a * ft, b * ft);
+            }
+            const int off = (cc ^ (t & 7)) << 4;
+            *reinterpret_cast<uint4 *>(dB + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4 *>(dBf + off) = make_uint4(pf[0], pf[1], pf[2], pf[3]);
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA2: D2a[:, 0:128] = K^T diag(f) [T'|P]  (M = D);  D2b[:, 128:256] = Aqk [T'|P]
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t ida = idesc_bf16_f32(D, 128, true, true);
+        const uint32_t idb = idesc_bf16_f32(64, 128, false, true);
+        const uint32_t kq = smem_u32(sKQ), bf = smem_u32(sBf), bb = smem_u32(sB), aa = smem_u32(sA);
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_ss(tm, desc_mnmajor_sw128(kq, 128, ks), desc_mnmajor_sw128(bf, 64, ks), ida,
+                        ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_ss(tm + 128, desc_kmajor_sw128(aa, 64, ks), desc_mnmajor_sw128(bb, 64, ks), idb,
+                        ks > 0 ? 1u : 0u);
+        mma_commit(&bar_mma);
+    }
+    if (ok && !mbar_wait(&bar_mma, 1, kWaitNs)) s_fail = 1;
+    tc_fence_after();
+
+    // ---- epilogue 2: Z1, Z2 operands; the V-columns of E (K~^T P, Aqk P)
+    {
+        // rows of D2a: M = D (M = 128: row = lane of quadrant; M = 64: 16 rows per quadrant)
+        const bool has_row = (D == 128) || (lane < 16);
+        const int i = (D == 128) ? tid : 16 * warp + lane;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t v[32];
+            tmem_ld32(tm + tq + 64 * half, v);
+            uint32_t v2[32];
+            tmem_ld32(tm + tq + 64 * half + 32, v2);
+            tmem_ld_wait();
+            if (has_row) {
+                if (half == 0) {   // Z1[i][s] -> K-major operand, rows i, 64 columns
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = cc * 8 + e * 2;
+                            const float a = __uint_as_float(s < 32 ? v[s] : v2[s - 32]);
+                            const float b = __uint_as_float(s + 1 < 32 ? v[s + 1] : v2[s + 1 - 32]);
+                            pk[e] = pack_bf16(a, b);
+                        }
+                        *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((cc ^ (i & 7)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                } else {           // E[i][D + s] = (K~^T P)[i][s]
+                    uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)i * R + D);
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = cc * 8 + e * 2;
+                            const float a = __uint_as_float(s < 32 ? v[s] : v2[s - 32]);
+                            const float b = __uint_as_float(s + 1 < 32 ? v[s + 1] : v2[s + 1 - 32]);
+                            pk[e] = pack_bf16(a, b);
+                        }
+                        dst[cc] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+            }
+        }
+        // rows of D2b (M = 64): t = 16 * warp + lane for lane < 16
+        const int t = 16 * warp + lane;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t v[32], v2[32];
+            tmem_ld32(tm + tq + 128 + 64 * half, v);
+            tmem_ld32(tm + tq + 128 + 64 * half + 32, v2);
+            tmem_ld_wait();
+            if (lane < 16) {
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = cc * 8 + e * 2;
+                        const float a = __uint_as_float(s < 32 ? v[s] : v2[s - 32]);
+                        const float b = __uint_as_float(s + 1 < 32 ? v[s + 1] : v2[s + 1 - 32]);
+                        pk[e] = pack_bf16(a, b);
+                    }
+                    if (half == 0)
+                        *reinterpret_cast<uint4 *>(sZ2 + t * 128 + ((cc ^ (t & 7)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    else
+                        reinterpret_cast<uint4 *>(Eout + (long)(D + t) * R + D)[cc] =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    ok = s_fail == 0;
+
+    // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64)
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t ida = idesc_bf16_f32(D, D, false, true);
+        const uint32_t idb = idesc_bf16_f32(64, D, false, true);
+        const uint32_t kq = smem_u32(sKQ), z1 = smem_u32(sZ1), z2 = smem_u32(sZ2);
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_ss(tm, desc_kmajor_sw128(z1, D, ks), desc_mnmajor_sw128(kq, 128, ks), ida,
+                        ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_ss(tm + 128, desc_kmajor_sw128(z2, 64, ks), desc_mnmajor_sw128(kq, 128, ks),
+                        idb, ks > 0 ? 1u : 0u);
+        mma_commit(&bar_mma);
+    }
+    if (ok && !mbar_wait(&bar_mma, 0, kWaitNs)) s_fail = 1;
+    tc_fence_after();
+
+    // ---- epilogue 3: the state columns of E
+    {
+        const float gamma_c = meg[63];
+        const bool has_row = (D == 128) || (lane < 16);
+        const int i = (D == 128) ? tid : 16 * warp + lane;
+        for (int c0 = 0; c0 < D; c0 += 32) {   // E[i][j] = gamma_C delta_ij - (K~^T W)[i][j]
+            uint32_t v[32];
+            tmem_ld32(tm + tq + c0, v);
+            tmem_ld_wait();
+            if (has_row) {
+                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)i * R + c0);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = cc * 8 + e * 2;
+                        const float a = (c0 + j == i ? gamma_c : 0.f) - __uint_as_float(v[j]);
+                        const float b = (c0 + j + 1 == i ? gamma_c : 0.f) - __uint_as_float(v[j + 1]);
+                        pk[e] = pack_bf16(a, b);
+                    }
+                    dst[cc] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+        }
+        const int t = 16 * warp + lane;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j]
+        const float qs = (lane < 16) ? meg[t] * mqn[t] : 0.f;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tm + tq + 128 + c0, v);
+            tmem_ld_wait();
+            if (lane < 16) {
+                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)(D + t) * R + c0);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int j0 = c0 + cc * 8;   // 8 consecutive head-dim indices: one chunk of q
+                    const uint4 qw = *reinterpret_cast<const uint4 *>(
+                        sKQ + (j0 >> 6) * 16384 + 8192 + t * 128 + ((((j0 & 63) >> 3) ^ (t & 7)) << 4));
+                    const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = cc * 8 + e * 2;
+                        const float a = qs * bf16lo(qv[e]) - __uint_as_float(v[j]);
+                        const float b = qs * bf16hi(qv[e]) - __uint_as_float(v[j + 1]);
+                        pk[e] = pack_bf16(a, b);
+                    }
+                    dst[cc] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+        }
+    }
+    if (tid == 0 && s_fail) record_error(p.ws, 1);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+// ---------------------------------------------------------------------------------
+// chain_kernel
+// ---------------------------------------------------------------------------------
+template <int D, int NT>
+struct ChainCfg {
+    static constexpr int R = D + 64;               // rows / columns of E
+    static constexpr int NKB = R / 64;             // 64-wide K blocks of E
+    static constexpr int E_BYTES = R * R * 2;      // one stage of E (K-major SW128)
+    static constexpr int B_BYTES = R * 128;        // [S; V] operand (MN-major, one 64 block)
+    static constexpr int SMEM = 2 * E_BYTES + 2 * B_BYTES + 1024;
+    static constexpr int S_THREADS = D == 128 ? 128 : 64;   // threads owning state rows
+    static constexpr int O_THREADS = D == 128 ? 128 : 64;   // threads arriving on o_free
+    static constexpr uint32_t TCOLS = (3 * NT <= 32) ? 32 : (3 * NT <= 64) ? 64 : (3 * NT <= 128) ? 128 : 256;
+};
+
+template <int D, int NT>
+__global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ CUtensorMap map_E,
+                                                       const __grid_constant__ CUtensorMap map_v,
+                                                       TcParams p) {
+    using Cf = ChainCfg<D, NT>;
+    constexpr int R = Cf::R;
+    static_assert(NT == 16 || NT == 32 || NT == 64, "value tile");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    uint8_t *sE0 = sm, *sB0 = sm + 2 * Cf::E_BYTES;
+    __shared__ uint64_t e_full[2], e_empty[2], s_ready[2], o_done[2], o_free[2], s_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int s_fail;
+
+    const int ntile = D / NT;
+    const int tile = blockIdx.x % ntile;
+    const int h = (blockIdx.x / ntile) % p.H;
+    const int n = blockIdx.x / (ntile * p.H);
+    long start;
+    int len;
+    seq_info(p, n, start, len);
+    const int nc = (len + kC - 1) / kC;
+    const long slot0 = (long)chunk_base_of(p, n) * p.H + h;
+    const int col0 = tile * NT;
+    const int vblk = col0 & ~63, noff = col0 & 63;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&e_full[s], 1);
+            mbar_init(&e_empty[s], 1);
+            mbar_init(&s_ready[s], Cf::S_THREADS);
+            mbar_init(&o_done[s], 1);
+            mbar_init(&o_free[s], Cf::O_THREADS);
+        }
+        mbar_init(&s_done, 1);
+        fence_mbar_init();
+        s_fail = 0;
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, Cf::TCOLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer: E_c and the V tile, two chunks ahead
+        if (lane == 0) {
+            for (int c = 0; c < nc && !s_fail; ++c) {
+                const int s = c & 1;
+                if (c >= 2 && !mbar_wait(&e_empty[s], ((c >> 1) - 1) & 1, kWaitNs)) {
+                    s_fail = 1;
+                    record_error(p.ws, 10);
+                    break;
+                }
+                mbar_expect_tx(&e_full[s], Cf::E_BYTES + 64 * 128);
+                uint8_t *dE = sE0 + s * Cf::E_BYTES;
+                const int slot = (int)(slot0 + (long)c * p.H);
+                for (int kb = 0; kb < Cf::NKB; ++kb)
+                    tma_load_3d(dE + kb * (R * 128), &map_E, &e_full[s], kb * 64, 0, slot);
+                tma_load_3d(sB0 + s * Cf::B_BYTES + D * 128, &map_v, &e_full[s], vblk, h,
+                            (int)(start + (long)c * kC));
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16_f32(128, NT, false, true);
+            const uint32_t idO = idesc_bf16_f32(64, NT, false, true);
+            for (int c = 0; c < nc && !s_fail; ++c) {
+                const int s = c & 1;
+                const uint32_t ph = (c >> 1) & 1;
+                if (!mbar_wait(&e_full[s], ph, kWaitNs) || !mbar_wait(&s_ready[s], ph, kWaitNs)) {
+                    s_fail = 1;
+                    record_error(p.ws, 11);
+                    break;
+                }
+                if (c >= 2 && !mbar_wait(&o_free[s], ((c >> 1) - 1) & 1, kWaitNs)) {
+                    s_fail = 1;
+                    record_error(p.ws, 12);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t e0 = smem_u32(sE0 + s * Cf::E_BYTES);
+                const uint32_t b0 = smem_u32(sB0 + s * Cf::B_BYTES) + (uint32_t)noff * 2u;
+                if (D == 128) {
+                    for (int ks = 0; ks < R / 16; ++ks)
+                        mma_bf16_ss(tm, desc_kmajor_sw128(e0, R, ks), desc_mnmajor_sw128(b0, R, ks),
+                                    idS, ks > 0 ? 1u : 0u);
+                    mma_commit(&s_done);
+                    for (int ks = 0; ks < R / 16; ++ks)
+                        mma_bf16_ss(tm + (uint32_t)(NT * (1 + s)),
+                                    desc_kmajor_sw128(e0 + 128 * 128, R, ks),
+                                    desc_mnmajor_sw128(b0, R, ks), idO, ks > 0 ? 1u : 0u);
+                } else {
+                    for (int ks = 0; ks < R / 16; ++ks)
+                        mma_bf16_ss(tm + (uint32_t)(NT * s), desc_kmajor_sw128(e0, R, ks),
+                                    desc_mnmajor_sw128(b0, R, ks), idS, ks > 0 ? 1u : 0u);
+                    mma_commit(&s_done);
+                }
+                mma_commit(&o_done[s]);
+                mma_commit(&e_empty[s]);
+            }
+        }
+    } else {
+        // ---------------- epilogue warps 2..5 (TMEM quadrant q = warp % 4)
+        const int q = warp & 3;
+        const bool s_thread = (D == 128) || (q < 2);
+        const bool o_thread = (D == 128) || (q >= 2);
+        const int i = 32 * q + lane;   // state row owned by this thread
+        const size_t st_off = (((size_t)n * p.H + h) * D + i) * D + col0;
+        __nv_bfloat16 *obase = p.o + (size_t)h * D + col0;
+
+        if (s_thread) {
+            float v[NT];
+#pragma unroll
+            for (int j = 0; j < NT; j += 4) {
+                const float4 x = p.h0 ? *reinterpret_cast<const float4 *>(p.h0 + st_off + j)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
+            }
+            if (nc == 0) {
+                if (p.hT)
+#pragma unroll
+                    for (int j = 0; j < NT; j += 4)
+                        *reinterpret_cast<float4 *>(p.hT + st_off + j) =
+                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            } else {
+                uint8_t *row = sB0 + i * 128;
+#pragma unroll
+                for (int cc = 0; cc < NT / 8; ++cc) {
+                    const int ch = ((noff >> 3) + cc) ^ (i & 7);
+                    *reinterpret_cast<uint4 *>(row + (ch << 4)) =
+                        make_uint4(pack_bf16(v[8 * cc], v[8 * cc + 1]), pack_bf16(v[8 * cc + 2], v[8 * cc + 3]),
+                                   pack_bf16(v[8 * cc + 4], v[8 * cc + 5]), pack_bf16(v[8 * cc + 6], v[8 * cc + 7]));
+                }
+                fence_proxy_async();
+                mbar_arrive(&s_ready[0]);
+            }
+        }
+        for (int c = 0; c < nc; ++c) {
+            const int s = c & 1;
+            if (s_thread) {
+                bool okw = !s_fail && mbar_wait(&s_done, c & 1, kWaitNs);
+                if (!okw) {
+                    s_fail = 1;
+                    record_error(p.ws, 13);
+                    break;
+                }
+                tc_fence_after();
+                uint32_t v[NT];
+                const uint32_t col = (D == 128) ? 0u : (uint32_t)(NT * s);
+                if (NT >= 32) {
+#pragma unroll
+                    for (int j = 0; j < NT; j += 32)
+                        tmem_ld32(tm + ((uint32_t)(32 * q) << 16) + col + j,
+                                  *reinterpret_cast<uint32_t(*)[32]>(v + j));
+                } else {
+                    tmem_ld16(tm + ((uint32_t)(32 * q) << 16) + col, *reinterpret_cast<uint32_t(*)[16]>(v));
+                }
+                tmem_ld_wait();
+                if (c + 1 < nc) {
+                    uint8_t *row = sB0 + ((c + 1) & 1) * Cf::B_BYTES + i * 128;
+#pragma unroll
+                    for (int cc = 0; cc < NT / 8; ++cc) {
+                        const int ch = ((noff >> 3) + cc) ^ (i & 7);
+                        const float *f = reinterpret_cast<const float *>(v + 8 * cc);
+                        *reinterpret_cast<uint4 *>(row + (ch << 4)) =
+                            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                       pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    }
+                    fence_proxy_async();
+                    tc_fence_before();
+                    mbar_arrive(&s_ready[(c + 1) & 1]);
+                } else if (p.hT) {
+#pragma unroll
+                    for (int j = 0; j < NT; j += 4)
+                        *reinterpret_cast<float4 *>(p.hT + st_off + j) =
+                            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                        __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                }
+            }
+            if (o_thread) {
+                bool okw = !s_fail && mbar_wait(&o_done[s], (c >> 1) & 1, kWaitNs);
+                if (!okw) {
+                    s_fail = 1;
+                    record_error(p.ws, 14);
+                    break;
+                }
+                tc_fence_after();
+                uint32_t v[NT];
+                // D = 128: outputs are an M = 64 result (16 rows per quadrant, lanes 0-15);
+                // D = 64: outputs are rows 64..127 of the M = 128 result (quadrants 2, 3).
+                const uint32_t col = (D == 128) ? (uint32_t)(NT * (1 + s)) : (uint32_t)(NT * s);
+                if (NT >= 32) {
+#pragma unroll
+                    for (int j = 0; j < NT; j += 32)
+                        tmem_ld32(tm + ((uint32_t)(32 * q) << 16) + col + j,
+                                  *reinterpret_cast<uint32_t(*)[32]>(v + j));
+                } else {
+                    tmem_ld16(tm + ((uint32_t)(32 * q) << 16) + col, *reinterpret_cast<uint32_t(*)[16]>(v));
+                }
+                tmem_ld_wait();
+                const int t = (D == 128) ? 16 * q + lane : 32 * (q - 2) + lane;
+                const int nv = min(kC, len - c * kC);
+                if ((D == 64 || lane < 16) && t < nv) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(obase + (size_t)(start + (long)c * kC + t) * p.H * D);
+#pragma unroll
+                    for (int cc = 0; cc < NT / 8; ++cc) {
+                        const float *f = reinterpret_cast<const float *>(v + 8 * cc);
+                        dst[cc] = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                             pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&o_free[s]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tm, Cf::TCOLS);
+}
+
+// cu_seqlens -> chunk prefix: base[n] = sum_{m < n} ceil(len_m / 64), base[N] = total.
+__global__ void chunk_table_kernel(const int *cu, int N, int *base) {
+    __shared__ int warp_tot[32];
+    __shared__ int carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int s0 = 0; s0 < N; s0 += 1024) {
+        const int n = s0 + tid;
+        const int v = n < N ? (cu[n + 1] - cu[n] + kC - 1) / kC : 0;
+        int x = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_tot[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += y;
+            }
+            warp_tot[lane] = w;   // inclusive over warps
+        }
+        __syncthreads();
+        const int before = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
+        if (n < N) base[n] = before;
+        __syncthreads();
+        if (tid == 0) carry += warp_tot[31];
+        __syncthreads();
+    }
+    if (tid == 0) base[N] = carry;
+}
+
+bool map_tokens(CUtensorMap *m, const void *base, long rows, int H, int D) {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)H, (uint64_t)rows};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)H * D * 2};
+    const uint32_t box[3] = {64u, 1u, 64u};
+    return make_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, true);
+}
+
+bool map_E(CUtensorMap *m, const void *base, long slots, int R) {
+    const uint64_t dims[3] = {(uint64_t)R, (uint64_t)R, (uint64_t)slots};
+    const uint64_t strides[2] = {(uint64_t)R * 2, (uint64_t)R * R * 2};
+    const uint32_t box[3] = {64u, (uint32_t)R, 1u};
+    return make_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, true);
+}
+
+constexpr size_t kTableBytes(int nseq) { return (((size_t)(nseq + 1) * 4 + 255) / 256) * 256; }
+
+template <int D, int NT>
+cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
+    constexpr int R = D + 64;
+    TcParams p{};
+    p.nseq = a.nseq; p.H = a.H; p.T = a.T; p.use_l2 = a.use_l2; p.scale = a.scale;
+    p.cu_seqlens = a.cu_seqlens;
+    p.nc_equal = (a.T + kC - 1) / kC;
+    p.beta = a.beta; p.decay = a.decay; p.h0 = a.h0; p.hT = a.hT;
+    p.o = static_cast<__nv_bfloat16 *>(a.o);
+    p.ws = a.ws;
+    uint8_t *body = static_cast<uint8_t *>(a.ws_body);
+    int *table = reinterpret_cast<int *>(body);
+    p.chunk_base = a.cu_seqlens ? table : nullptr;
+    p.E = reinterpret_cast<__nv_bfloat16 *>(body + kTableBytes(a.nseq));
+
+    CUtensorMap mq, mk, mv, me;
+    if (!map_tokens(&mq, a.q, total_rows, a.H, D) || !map_tokens(&mk, a.k, total_rows, a.H, D) ||
+        !map_tokens(&mv, a.v, total_rows, a.H, D) || !map_E(&me, p.E, slots_bound, R))
+        return cudaErrorInvalidValue;
+
+    if (a.cu_seqlens) {
+        chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.nseq, table);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const long chunks_bound = slots_bound / a.H;
+    cudaError_t e = cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PrepSmem<D>::BYTES);
+    if (e != cudaSuccess) return e;
+    prep_kernel<D><<<(unsigned)(chunks_bound * a.H), 128, PrepSmem<D>::BYTES, st>>>(mq, mk, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    using Cf = ChainCfg<D, NT>;
+    e = cudaFuncSetAttribute(chain_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    if (e != cudaSuccess) return e;
+    chain_kernel<D, NT><<<(unsigned)((long)a.nseq * a.H * (D / NT)), 192, Cf::SMEM, st>>>(me, mv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunk_tc_supported(int dk, int dv, int chunk, DType dt) {
+    return dt == DType::BF16 && dk == dv && (dk == 64 || dk == 128) && chunk == kC;
+}
+
+// Scratch bytes after the workspace header: the chunk table and one E slot per
+// (chunk, head).  slots_bound: an upper bound on the number of chunks times H.
+size_t chunk_tc_scratch_bytes(int nseq, long slots_bound, int d) {
+    const long R = d + 64;
+    return kTableBytes(nseq) + (size_t)slots_bound * R * R * 2;
+}
+
+long chunk_tc_slots_bound(int nseq, long total_rows, int H, int T_equal, bool varlen) {
+    if (!varlen) return (long)nseq * ((T_equal + kC - 1) / kC) * H;
+    return ((total_rows + kC - 1) / kC + nseq) * (long)H;
+}
+
+cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
+    if (a.dk == 128) return run_tc<128, 32>(a, total_rows, slots_bound, st);
+    if (a.dk == 64) return run_tc<64, 32>(a, total_rows, slots_bound, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

@@ -76,11 +76,16 @@ const char *kda_status_string(kda_status s) {
 
 int kda_version(void) { return (0 << 16) | 1; }
 
+static DType to_dtype(kda_dtype d) { return d == KDA_BF16 ? DType::BF16 : DType::F32; }
+
 size_t kda_chunk_fwd_workspace(int B, int T, int H, int dk, int dv, int chunk_size,
                                kda_dtype dtype) {
     if (B < 0 || T < 0 || H <= 0) return 0;
     if (dtype != KDA_F32 && dtype != KDA_BF16) return 0;
     if (!supported_head(dk) || !supported_head(dv) || !supported_chunk(chunk_size)) return 0;
+    if (chunk_tc_supported(dk, dv, chunk_size, to_dtype(dtype)) && B > 0 && T > 0)
+        return kWsHeader +
+               chunk_tc_scratch_bytes(B, chunk_tc_slots_bound(B, (long)B * T, H, T, false), dk);
     return kWsHeader;
 }
 
@@ -89,13 +94,25 @@ size_t kda_varlen_fwd_workspace(int N, int total_T, int H, int dk, int dv, int c
     if (N < 0 || total_T < 0 || H <= 0) return 0;
     if (dtype != KDA_F32 && dtype != KDA_BF16) return 0;
     if (!supported_head(dk) || !supported_head(dv) || !supported_chunk(chunk_size)) return 0;
+    if (chunk_tc_supported(dk, dv, chunk_size, to_dtype(dtype)) && N > 0)
+        return kWsHeader +
+               chunk_tc_scratch_bytes(N, chunk_tc_slots_bound(N, total_T, H, 0, true), dk);
     return kWsHeader;
 }
 
-static kda_status run_prefill(SeqBatch &a, bool chunked, cudaStream_t st) {
+// total_rows: rows of the token arrays (B*T, or total_T for varlen).
+static kda_status run_prefill(SeqBatch &a, bool chunked, long total_rows, cudaStream_t st) {
     if (a.nseq == 0) return KDA_OK;
-    if (a.T == 0) return launch_status(launch_state_passthrough(a, st));
-    cudaError_t e = chunked ? launch_chunk_simt(a, st) : launch_recurrent(a, st);
+    if (!a.cu_seqlens && a.T == 0) return launch_status(launch_state_passthrough(a, st));
+    cudaError_t e;
+    if (!chunked) {
+        e = launch_recurrent(a, st);
+    } else if (chunk_tc_supported(a.dk, a.dv, a.chunk, a.dtype)) {
+        const long bound = chunk_tc_slots_bound(a.nseq, total_rows, a.H, a.T, a.cu_seqlens != nullptr);
+        e = launch_chunk_tc(a, total_rows, bound, st);
+    } else {
+        e = launch_chunk_simt(a, st);
+    }
     return launch_status(e);
 }
 
@@ -123,7 +140,7 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const floa
     a.ws_body_bytes = ws_bytes - kWsHeader;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
-    return run_prefill(a, true, st);
+    return run_prefill(a, true, (long)B * T, st);
 }
 
 kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *beta,
@@ -141,7 +158,7 @@ kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const 
     a.dk = dk; a.dv = dv; a.chunk = 0;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
-    return run_prefill(a, false, reinterpret_cast<cudaStream_t>(stream));
+    return run_prefill(a, false, (long)B * T, reinterpret_cast<cudaStream_t>(stream));
 }
 
 kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *beta,
@@ -201,7 +218,7 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v, const flo
     if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
     // Every sequence runs the chunk loop from its own cu_seqlens range; a sequence
     // of length 0 falls through the loop and stores its initial state.
-    return launch_status(launch_chunk_simt(a, st));
+    return run_prefill(a, true, total_T, st);
 }
 
 kda_status kda_query_device_error(const void *ws, kda_stream_t stream) {

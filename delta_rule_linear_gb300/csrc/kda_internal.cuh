@@ -69,6 +69,15 @@ size_t chunk_simt_smem_bytes(int dk, int dv, int chunk);
 // Copies (or zero-fills) final_state from initial_state for empty sequences.
 cudaError_t launch_state_passthrough(const SeqBatch &a, cudaStream_t s);
 
+// Tensor-core chunked prefill (bf16, dk == dv in {64, 128}, chunk 64).
+bool chunk_tc_supported(int dk, int dv, int chunk, DType dt);
+// Upper bound on (chunks x heads) for a batch: equal length uses T_equal, varlen the
+// total row count plus one partial chunk per sequence.
+long chunk_tc_slots_bound(int nseq, long total_rows, int H, int T_equal, bool varlen);
+// Workspace bytes after the header for that bound.
+size_t chunk_tc_scratch_bytes(int nseq, long slots_bound, int d);
+cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t s);
+
 // L2 normalisation floor: x / max(||x||, kNormEps).
 constexpr float kNormEps = 1e-12f;
 
