@@ -128,8 +128,13 @@ def _workspace(nbytes, device, workspace):
 
 
 def chunk_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None, chunk_size=64,
-              use_qk_l2norm=True, out=None, final_state=None, workspace=None, stream=None):
-    """kda_chunk_fwd: chunked prefill.  Returns (o [B,T,H,dv], final_state [B,H,dk,dv] fp32)."""
+              use_qk_l2norm=True, out=None, final_state=None, workspace=None, stream=None,
+              check_device=False):
+    """kda_chunk_fwd: chunked prefill.  Returns (o [B,T,H,dv], final_state [B,H,dk,dv] fp32).
+
+    check_device=True synchronises the stream afterwards and raises if a kernel recorded
+    a device error (a bounded wait that ran out) in the workspace header.
+    """
     lib = load()
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -151,6 +156,8 @@ def chunk_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None, chun
                            int(chunk_size), int(bool(use_qk_l2norm)), _ptr(ws),
                            ws.numel() * ws.element_size(), _stream(stream))
     _raise(rc, "kda_chunk_fwd", lib)
+    if check_device:
+        _raise(query_device_error(ws, stream), "kda_chunk_fwd (device)", lib)
     return o, hT
 
 
@@ -199,10 +206,10 @@ def decode_step(q, k, v, beta, decay, state, *, scale=None, use_qk_l2norm=True, 
 
 def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_seqlens_cpu=None,
                scale=None, chunk_size=64, use_qk_l2norm=True, out=None, final_state=None,
-               workspace=None, stream=None):
+               workspace=None, stream=None, check_device=False):
     """kda_varlen_fwd: packed sequences [1,total,H,D] split by cu_seqlens [N+1] (int32, device).
 
-    Returns (o [1,total,H,dv], final_state [N,H,dk,dv] fp32).
+    Returns (o [1,total,H,dv], final_state [N,H,dk,dv] fp32).  check_device as in chunk_fwd.
     """
     lib = load()
     _, total, H, dk = q.shape
@@ -231,6 +238,8 @@ def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_
                             dt, float(scale or 0.0), int(chunk_size), int(bool(use_qk_l2norm)),
                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _raise(rc, "kda_varlen_fwd", lib)
+    if check_device:
+        _raise(query_device_error(ws, stream), "kda_varlen_fwd (device)", lib)
     return o, hT
 
 

@@ -191,9 +191,6 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v, const flo
     if (!supported_chunk(chunk_size)) return KDA_ERR_UNSUPPORTED;
     if (N > 0 && !cu_seqlens) return KDA_ERR_NULL;
     if (!aligned4(cu_seqlens)) return KDA_ERR_ALIGN;
-    const size_t need = kda_varlen_fwd_workspace(N, total_T, H, dk, dv, chunk_size, dtype);
-    if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
-    if (!aligned16(ws)) return KDA_ERR_ALIGN;
     int max_len = total_T;
     if (cu_seqlens_host) {
         if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != total_T) return KDA_ERR_INDEX;
@@ -204,6 +201,9 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v, const flo
             if (L > max_len) max_len = L;
         }
     }
+    const size_t need = kda_varlen_fwd_workspace(N, total_T, H, dk, dv, chunk_size, dtype);
+    if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
     if (N == 0) return KDA_OK;
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = decay; a.h0 = initial_state;

@@ -17,11 +17,19 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module")
 def kda():
+    """The binding, with every prefill call checking the device error word afterwards
+    (a kernel whose bounded wait ran out makes the call raise)."""
+    import functools
+    import types
+
     import delta_rule_linear_gb300 as m
     from delta_rule_linear_gb300 import build as b
     b.build()
     m.load()
-    return m
+    return types.SimpleNamespace(
+        chunk_fwd=functools.partial(m.chunk_fwd, check_device=True),
+        varlen_fwd=functools.partial(m.varlen_fwd, check_device=True),
+        recurrent_fwd=m.recurrent_fwd, decode_step=m.decode_step)
 
 
 @pytest.fixture(scope="module")
@@ -206,8 +214,10 @@ def test_decode_equals_prefill(kda, dev):
                                     sl(t["decay"]), st))
     torch.cuda.synchronize()
     od = torch.cat(outs, dim=1)
+    # the decode path is fp32 throughout; the bf16 prefill runs its products on bf16
+    # operands, so the two agree to the bf16 bar
     assert max_rel(to_np(od), to_np(o)) <= 2e-2
-    assert frob_rel(to_np(st), to_np(h)) <= 1e-3
+    assert frob_rel(to_np(st), to_np(h)) <= 1e-2
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
