@@ -524,56 +524,64 @@ __global__ void __launch_bounds__(128) prep_kernel(const __grid_constant__ CUten
 }
 
 // ---------------------------------------------------------------------------------
-// chain_kernel
+// chain_kernel -- one CTA per (sequence, head), transposed so that M = dv:
+//
+//   D^T[j][r] = sum_k A[j][k] E_c[r][k],   A = [S^T | V_c^T]   (dv rows, D + 64 columns)
+//
+// hence D^T[j][r] = S_next[r][j] for r < D and O[r - D][j] for r >= D: the next
+// state and the chunk's outputs come out of the same instructions.  The V half
+// (4 k-steps) needs only E_c and V_c, so it is issued into the next of two TMEM
+// accumulators while the epilogue of the previous chunk is still running; only the
+// state half (D / 16 k-steps) waits for S_c.  A tcgen05 MMA of M = 128 costs about
+// the same per k-step for any N up to 128-192, which is why the whole head (and
+// its outputs) is one wide product rather than several narrow ones.
+// The state is carried as the bf16 operand S^T, rebuilt every chunk from the fp32
+// accumulator; the final state is stored from the fp32 accumulator.
 // ---------------------------------------------------------------------------------
-template <int D, int NT>
+template <int D>
 struct ChainCfg {
-    static constexpr int R = D + 64;               // rows / columns of E
-    static constexpr int NKB = R / 64;             // 64-wide K blocks of E
-    static constexpr int E_BYTES = R * R * 2;      // one stage of E (K-major SW128)
-    static constexpr int B_BYTES = R * 128;        // [S; V] operand (MN-major, one 64 block)
-    static constexpr int SMEM = 2 * E_BYTES + 2 * B_BYTES + 1024;
-    static constexpr int S_THREADS = D == 128 ? 128 : 64;   // threads owning state rows
-    static constexpr int O_THREADS = D == 128 ? 128 : 64;   // threads arriving on o_free
-    static constexpr uint32_t TCOLS = (3 * NT <= 32) ? 32 : (3 * NT <= 64) ? 64 : (3 * NT <= 128) ? 128 : 256;
+    static constexpr int R = D + 64;              // rows / columns of E_c
+    static constexpr int NKB = R / 64;            // 64-wide K blocks of E_c
+    static constexpr int NB = D / 64;             // 64-wide blocks of the head dim
+    static constexpr int E_BYTES = R * R * 2;     // one stage of E_c (K-major SW128, R rows)
+    static constexpr int AS_BYTES = D * D * 2;    // S^T operand (K-major SW128, D rows)
+    static constexpr int AV_BYTES = 64 * D * 2;   // one stage of V_c (MN-major SW128)
+    static constexpr int SMEM = 2 * E_BYTES + AS_BYTES + 2 * AV_BYTES + 1024;
+    static constexpr uint32_t TCOLS = (2 * R <= 256) ? 256u : 512u;   // two accumulators
 };
 
-template <int D, int NT>
+template <int D>
 __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ CUtensorMap map_E,
                                                        const __grid_constant__ CUtensorMap map_v,
                                                        TcParams p) {
-    using Cf = ChainCfg<D, NT>;
+    using Cf = ChainCfg<D>;
     constexpr int R = Cf::R;
-    static_assert(NT == 16 || NT == 32 || NT == 64, "value tile");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *sE0 = sm, *sB0 = sm + 2 * Cf::E_BYTES;
-    __shared__ uint64_t e_full[2], e_empty[2], s_ready[2], o_done[2], o_free[2], s_done;
+    uint8_t *sE0 = sm;
+    uint8_t *sAS = sm + 2 * Cf::E_BYTES;
+    uint8_t *sAV0 = sAS + Cf::AS_BYTES;
+    __shared__ uint64_t e_full[2], e_empty[2], d_full[2], d_free[2], s_ready;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_fail;
 
-    const int ntile = D / NT;
-    const int tile = blockIdx.x % ntile;
-    const int h = (blockIdx.x / ntile) % p.H;
-    const int n = blockIdx.x / (ntile * p.H);
+    const int h = blockIdx.x % p.H;
+    const int n = blockIdx.x / p.H;
     long start;
     int len;
     seq_info(p, n, start, len);
     const int nc = (len + kC - 1) / kC;
     const long slot0 = (long)chunk_base_of(p, n) * p.H + h;
-    const int col0 = tile * NT;
-    const int vblk = col0 & ~63, noff = col0 & 63;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(&e_full[s], 1);
             mbar_init(&e_empty[s], 1);
-            mbar_init(&s_ready[s], Cf::S_THREADS);
-            mbar_init(&o_done[s], 1);
-            mbar_init(&o_free[s], Cf::O_THREADS);
+            mbar_init(&d_full[s], 1);
+            mbar_init(&d_free[s], 128);
         }
-        mbar_init(&s_done, 1);
+        mbar_init(&s_ready, 128);
         fence_mbar_init();
         s_fail = 0;
     }
@@ -587,7 +595,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
     const uint32_t tm = tmem_slot;
 
     if (warp == 0) {
-        // ---------------- producer: E_c and the V tile, two chunks ahead
+        // ---------------- producer: E_c and V_c by TMA, two chunks ahead
         if (lane == 0) {
             for (int c = 0; c < nc && !s_fail; ++c) {
                 const int s = c & 1;
@@ -596,173 +604,141 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
                     record_error(p.ws, 10);
                     break;
                 }
-                mbar_expect_tx(&e_full[s], Cf::E_BYTES + 64 * 128);
+                mbar_expect_tx(&e_full[s], Cf::E_BYTES + Cf::AV_BYTES);
                 uint8_t *dE = sE0 + s * Cf::E_BYTES;
                 const int slot = (int)(slot0 + (long)c * p.H);
                 for (int kb = 0; kb < Cf::NKB; ++kb)
                     tma_load_3d(dE + kb * (R * 128), &map_E, &e_full[s], kb * 64, 0, slot);
-                tma_load_3d(sB0 + s * Cf::B_BYTES + D * 128, &map_v, &e_full[s], vblk, h,
-                            (int)(start + (long)c * kC));
+                uint8_t *dV = sAV0 + s * Cf::AV_BYTES;
+                for (int mb = 0; mb < Cf::NB; ++mb)
+                    tma_load_3d(dV + mb * 8192, &map_v, &e_full[s], mb * 64, h,
+                                (int)(start + (long)c * kC));
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idS = idesc_bf16_f32(128, NT, false, true);
-            const uint32_t idO = idesc_bf16_f32(64, NT, false, true);
+            const uint32_t idV = idesc_bf16_f32(D, R, true, false);
+            const uint32_t idS = idesc_bf16_f32(D, R, false, false);
+            const uint32_t as0 = smem_u32(sAS);
             for (int c = 0; c < nc && !s_fail; ++c) {
-                const int s = c & 1;
-                const uint32_t ph = (c >> 1) & 1;
-                if (!mbar_wait(&e_full[s], ph, kWaitNs) || !mbar_wait(&s_ready[s], ph, kWaitNs)) {
+                const int b = c & 1;
+                if (!mbar_wait(&e_full[b], (c >> 1) & 1, kWaitNs) ||
+                    (c >= 2 && !mbar_wait(&d_free[b], ((c >> 1) - 1) & 1, kWaitNs))) {
                     s_fail = 1;
                     record_error(p.ws, 11);
                     break;
                 }
-                if (c >= 2 && !mbar_wait(&o_free[s], ((c >> 1) - 1) & 1, kWaitNs)) {
+                tc_fence_after();
+                const uint32_t e0 = smem_u32(sE0 + b * Cf::E_BYTES);
+                const uint32_t av0 = smem_u32(sAV0 + b * Cf::AV_BYTES);
+                const uint32_t dcol = tm + (uint32_t)(b * R);
+                for (int ks = 0; ks < 4; ++ks)   // V half: E_c columns D .. D + 63
+                    mma_bf16_ss(dcol, desc_mnmajor_sw128(av0, 64, ks),
+                                desc_kmajor_sw128(e0, R, D / 16 + ks), idV, ks > 0 ? 1u : 0u);
+                if (!mbar_wait(&s_ready, c & 1, kWaitNs)) {
                     s_fail = 1;
                     record_error(p.ws, 12);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t e0 = smem_u32(sE0 + s * Cf::E_BYTES);
-                const uint32_t b0 = smem_u32(sB0 + s * Cf::B_BYTES) + (uint32_t)noff * 2u;
-                if (D == 128) {
-                    for (int ks = 0; ks < R / 16; ++ks)
-                        mma_bf16_ss(tm, desc_kmajor_sw128(e0, R, ks), desc_mnmajor_sw128(b0, R, ks),
-                                    idS, ks > 0 ? 1u : 0u);
-                    mma_commit(&s_done);
-                    for (int ks = 0; ks < R / 16; ++ks)
-                        mma_bf16_ss(tm + (uint32_t)(NT * (1 + s)),
-                                    desc_kmajor_sw128(e0 + 128 * 128, R, ks),
-                                    desc_mnmajor_sw128(b0, R, ks), idO, ks > 0 ? 1u : 0u);
-                } else {
-                    for (int ks = 0; ks < R / 16; ++ks)
-                        mma_bf16_ss(tm + (uint32_t)(NT * s), desc_kmajor_sw128(e0, R, ks),
-                                    desc_mnmajor_sw128(b0, R, ks), idS, ks > 0 ? 1u : 0u);
-                    mma_commit(&s_done);
-                }
-                mma_commit(&o_done[s]);
-                mma_commit(&e_empty[s]);
+                for (int ks = 0; ks < D / 16; ++ks)   // state half: E_c columns 0 .. D - 1
+                    mma_bf16_ss(dcol, desc_kmajor_sw128(as0, D, ks), desc_kmajor_sw128(e0, R, ks),
+                                idS, 1u);
+                mma_commit(&d_full[b]);
+                mma_commit(&e_empty[b]);
             }
         }
     } else {
-        // ---------------- epilogue warps 2..5 (TMEM quadrant q = warp % 4)
+        // ---------------- epilogue warps 2..5: TMEM quadrant q, value column j
         const int q = warp & 3;
-        const bool s_thread = (D == 128) || (q < 2);
-        const bool o_thread = (D == 128) || (q >= 2);
-        const int i = 32 * q + lane;   // state row owned by this thread
-        const size_t st_off = (((size_t)n * p.H + h) * D + i) * D + col0;
-        __nv_bfloat16 *obase = p.o + (size_t)h * D + col0;
+        const bool has_row = (D == 128) || (lane < 16);   // M = 64: 16 rows per quadrant
+        const int j = (D == 128) ? 32 * q + lane : 16 * q + lane;
+        const uint32_t lrow = (uint32_t)(32 * q) << 16;
+        const size_t hbase = ((size_t)n * p.H + h) * D * D;
 
-        if (s_thread) {
-            float v[NT];
+        if (has_row) {   // S_0^T row j from initial_state[:, j]
+            for (int i0 = 0; i0 < D; i0 += 8) {
+                float x[8];
 #pragma unroll
-            for (int j = 0; j < NT; j += 4) {
-                const float4 x = p.h0 ? *reinterpret_cast<const float4 *>(p.h0 + st_off + j)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
-            }
-            if (nc == 0) {
-                if (p.hT)
+                for (int e = 0; e < 8; ++e) x[e] = p.h0 ? p.h0[hbase + (size_t)(i0 + e) * D + j] : 0.f;
+                if (nc == 0) {
+                    if (p.hT)
 #pragma unroll
-                    for (int j = 0; j < NT; j += 4)
-                        *reinterpret_cast<float4 *>(p.hT + st_off + j) =
-                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-            } else {
-                uint8_t *row = sB0 + i * 128;
-#pragma unroll
-                for (int cc = 0; cc < NT / 8; ++cc) {
-                    const int ch = ((noff >> 3) + cc) ^ (i & 7);
-                    *reinterpret_cast<uint4 *>(row + (ch << 4)) =
-                        make_uint4(pack_bf16(v[8 * cc], v[8 * cc + 1]), pack_bf16(v[8 * cc + 2], v[8 * cc + 3]),
-                                   pack_bf16(v[8 * cc + 4], v[8 * cc + 5]), pack_bf16(v[8 * cc + 6], v[8 * cc + 7]));
+                        for (int e = 0; e < 8; ++e) p.hT[hbase + (size_t)(i0 + e) * D + j] = x[e];
+                } else {
+                    const int ci = (i0 & 63) >> 3;
+                    *reinterpret_cast<uint4 *>(sAS + (i0 >> 6) * D * 128 + j * 128 + ((ci ^ (j & 7)) << 4)) =
+                        make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                                   pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
                 }
-                fence_proxy_async();
-                mbar_arrive(&s_ready[0]);
             }
         }
+        fence_proxy_async();
+        mbar_arrive(&s_ready);
+
         for (int c = 0; c < nc; ++c) {
-            const int s = c & 1;
-            if (s_thread) {
-                bool okw = !s_fail && mbar_wait(&s_done, c & 1, kWaitNs);
-                if (!okw) {
-                    s_fail = 1;
-                    record_error(p.ws, 13);
-                    break;
-                }
-                tc_fence_after();
-                uint32_t v[NT];
-                const uint32_t col = (D == 128) ? 0u : (uint32_t)(NT * s);
-                if (NT >= 32) {
-#pragma unroll
-                    for (int j = 0; j < NT; j += 32)
-                        tmem_ld32(tm + ((uint32_t)(32 * q) << 16) + col + j,
-                                  *reinterpret_cast<uint32_t(*)[32]>(v + j));
-                } else {
-                    tmem_ld16(tm + ((uint32_t)(32 * q) << 16) + col, *reinterpret_cast<uint32_t(*)[16]>(v));
-                }
-                tmem_ld_wait();
-                if (c + 1 < nc) {
-                    uint8_t *row = sB0 + ((c + 1) & 1) * Cf::B_BYTES + i * 128;
-#pragma unroll
-                    for (int cc = 0; cc < NT / 8; ++cc) {
-                        const int ch = ((noff >> 3) + cc) ^ (i & 7);
-                        const float *f = reinterpret_cast<const float *>(v + 8 * cc);
-                        *reinterpret_cast<uint4 *>(row + (ch << 4)) =
-                            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                       pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-                    }
-                    fence_proxy_async();
-                    tc_fence_before();
-                    mbar_arrive(&s_ready[(c + 1) & 1]);
-                } else if (p.hT) {
-#pragma unroll
-                    for (int j = 0; j < NT; j += 4)
-                        *reinterpret_cast<float4 *>(p.hT + st_off + j) =
-                            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                        __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-                }
+            const int b = c & 1;
+            if (s_fail || !mbar_wait(&d_full[b], (c >> 1) & 1, kWaitNs)) {
+                s_fail = 1;
+                record_error(p.ws, 13);
+                break;
             }
-            if (o_thread) {
-                bool okw = !s_fail && mbar_wait(&o_done[s], (c >> 1) & 1, kWaitNs);
-                if (!okw) {
-                    s_fail = 1;
-                    record_error(p.ws, 14);
-                    break;
-                }
-                tc_fence_after();
-                uint32_t v[NT];
-                // D = 128: outputs are an M = 64 result (16 rows per quadrant, lanes 0-15);
-                // D = 64: outputs are rows 64..127 of the M = 128 result (quadrants 2, 3).
-                const uint32_t col = (D == 128) ? (uint32_t)(NT * (1 + s)) : (uint32_t)(NT * s);
-                if (NT >= 32) {
-#pragma unroll
-                    for (int j = 0; j < NT; j += 32)
-                        tmem_ld32(tm + ((uint32_t)(32 * q) << 16) + col + j,
-                                  *reinterpret_cast<uint32_t(*)[32]>(v + j));
-                } else {
-                    tmem_ld16(tm + ((uint32_t)(32 * q) << 16) + col, *reinterpret_cast<uint32_t(*)[16]>(v));
-                }
+            tc_fence_after();
+            const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
+            const bool last = (c + 1 == nc);
+#pragma unroll 1
+            for (int i0 = 0; i0 < D; i0 += 32) {   // state part: S_next[i0 + e][j]
+                uint32_t v[32];
+                tmem_ld32(dcol + i0, v);
                 tmem_ld_wait();
-                const int t = (D == 128) ? 16 * q + lane : 32 * (q - 2) + lane;
-                const int nv = min(kC, len - c * kC);
-                if ((D == 64 || lane < 16) && t < nv) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(obase + (size_t)(start + (long)c * kC + t) * p.H * D);
+                if (has_row) {
+                    if (!last) {
 #pragma unroll
-                    for (int cc = 0; cc < NT / 8; ++cc) {
-                        const float *f = reinterpret_cast<const float *>(v + 8 * cc);
-                        dst[cc] = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                             pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const int ci = ((i0 & 63) >> 3) + cc;
+                            *reinterpret_cast<uint4 *>(sAS + (i0 >> 6) * D * 128 + j * 128 +
+                                                       ((ci ^ (j & 7)) << 4)) =
+                                make_uint4(pack_bf16(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
+                                           pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
+                                           pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
+                                           pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
+                        }
+                    } else if (p.hT) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            p.hT[hbase + (size_t)(i0 + e) * D + j] = __uint_as_float(v[e]);
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&o_free[s]);
             }
+            if (!last) fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&s_ready);   // S_{c+1}^T is in place
+            const int nv = min(kC, len - c * kC);
+            __nv_bfloat16 *ocol = p.o + (size_t)h * D + j;
+            const size_t ostride = (size_t)p.H * D;
+#pragma unroll 1
+            for (int t0 = 0; t0 < kC; t0 += 32) {   // output part: O[t0 + e][j]
+                uint32_t v[32];
+                tmem_ld32(dcol + D + t0, v);
+                tmem_ld_wait();
+                if (has_row) {
+                    const size_t rbase = (size_t)(start + (long)c * kC + t0);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (t0 + e < nv) ocol[(rbase + e) * ostride] = __float2bfloat16_rn(__uint_as_float(v[e]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&d_free[b]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tm, Cf::TCOLS);
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tm, Cf::TCOLS);
+    }
 }
 
 // cu_seqlens -> chunk prefix: base[n] = sum_{m < n} ceil(len_m / 64), base[N] = total.
@@ -818,7 +794,7 @@ bool map_E(CUtensorMap *m, const void *base, long slots, int R) {
 
 constexpr size_t kTableBytes(int nseq) { return (((size_t)(nseq + 1) * 4 + 255) / 256) * 256; }
 
-template <int D, int NT>
+template <int D>
 cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
     constexpr int R = D + 64;
     TcParams p{};
@@ -850,10 +826,10 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     prep_kernel<D><<<(unsigned)(chunks_bound * a.H), 128, PrepSmem<D>::BYTES, st>>>(mq, mk, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    using Cf = ChainCfg<D, NT>;
-    e = cudaFuncSetAttribute(chain_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    using Cf = ChainCfg<D>;
+    e = cudaFuncSetAttribute(chain_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (e != cudaSuccess) return e;
-    chain_kernel<D, NT><<<(unsigned)((long)a.nseq * a.H * (D / NT)), 192, Cf::SMEM, st>>>(me, mv, p);
+    chain_kernel<D><<<(unsigned)((long)a.nseq * a.H), 192, Cf::SMEM, st>>>(me, mv, p);
     return cudaGetLastError();
 }
 
@@ -876,8 +852,8 @@ long chunk_tc_slots_bound(int nseq, long total_rows, int H, int T_equal, bool va
 }
 
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
-    if (a.dk == 128) return run_tc<128, 32>(a, total_rows, slots_bound, st);
-    if (a.dk == 64) return run_tc<64, 32>(a, total_rows, slots_bound, st);
+    if (a.dk == 128) return run_tc<128>(a, total_rows, slots_bound, st);
+    if (a.dk == 64) return run_tc<64>(a, total_rows, slots_bound, st);
     return cudaErrorInvalidValue;
 }
 
