@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(&e_full[s], 1);
-            mbar_init(&e_empty[s], 1);
+            mbar_init(&e_empty[s], 128);   // released by the epilogue (it stages o there)
             mbar_init(&d_full[s], 1);
             mbar_init(&d_free[s], 128);
         }
@@ -646,7 +646,6 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
                     mma_bf16_ss(dcol, desc_kmajor_sw128(as0, D, ks), desc_kmajor_sw128(e0, R, ks),
                                 idS, 1u);
                 mma_commit(&d_full[b]);
-                mma_commit(&e_empty[b]);
             }
         }
     } else {
@@ -687,50 +686,59 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
             tc_fence_after();
             const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
             const bool last = (c + 1 == nc);
-#pragma unroll 1
-            for (int i0 = 0; i0 < D; i0 += 32) {   // state part: S_next[i0 + e][j]
-                uint32_t v[32];
-                tmem_ld32(dcol + i0, v);
+            {   // state part: S_next[i][j], all D columns loaded before one wait
+                uint32_t v[D];
+#pragma unroll
+                for (int i0 = 0; i0 < D; i0 += 32)
+                    tmem_ld32(dcol + i0, *reinterpret_cast<uint32_t(*)[32]>(v + i0));
                 tmem_ld_wait();
                 if (has_row) {
                     if (!last) {
 #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            const int ci = ((i0 & 63) >> 3) + cc;
-                            *reinterpret_cast<uint4 *>(sAS + (i0 >> 6) * D * 128 + j * 128 +
-                                                       ((ci ^ (j & 7)) << 4)) =
+                        for (int cc = 0; cc < D / 8; ++cc)
+                            *reinterpret_cast<uint4 *>(sAS + (cc >> 3) * D * 128 + j * 128 +
+                                                       (((cc & 7) ^ (j & 7)) << 4)) =
                                 make_uint4(pack_bf16(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
                                            pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
                                            pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
                                            pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
-                        }
                     } else if (p.hT) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            p.hT[hbase + (size_t)(i0 + e) * D + j] = __uint_as_float(v[e]);
+                        for (int i = 0; i < D; ++i)
+                            p.hT[hbase + (size_t)i * D + j] = __uint_as_float(v[i]);
                     }
                 }
             }
             if (!last) fence_proxy_async();
             tc_fence_before();
             mbar_arrive(&s_ready);   // S_{c+1}^T is in place
-            const int nv = min(kC, len - c * kC);
-            __nv_bfloat16 *ocol = p.o + (size_t)h * D + j;
-            const size_t ostride = (size_t)p.H * D;
-#pragma unroll 1
-            for (int t0 = 0; t0 < kC; t0 += 32) {   // output part: O[t0 + e][j]
-                uint32_t v[32];
-                tmem_ld32(dcol + D + t0, v);
+            {   // output part: O[t][j], staged row-major [t][j] in the consumed E_c stage,
+                // then written out as whole rows with 16-byte stores
+                uint32_t v[kC];
+                tmem_ld32(dcol + D, *reinterpret_cast<uint32_t(*)[32]>(v));
+                tmem_ld32(dcol + D + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                 tmem_ld_wait();
-                if (has_row) {
-                    const size_t rbase = (size_t)(start + (long)c * kC + t0);
+                tc_fence_before();
+                mbar_arrive(&d_free[b]);   // the accumulator may be overwritten from here on
+                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sE0 + b * Cf::E_BYTES);
+                if (has_row)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (t0 + e < nv) ocol[(rbase + e) * ostride] = __float2bfloat16_rn(__uint_as_float(v[e]));
+                    for (int t = 0; t < kC; ++t) stg[t * D + j] = __float2bfloat16_rn(__uint_as_float(v[t]));
+                named_sync(1, 128);
+                const int nv = min(kC, len - c * kC);
+                const int et = tid - 64;   // 0..127 over the epilogue warps
+                constexpr int CPR = D / 8;  // 16-byte pieces per output row
+                __nv_bfloat16 *obase = p.o + ((size_t)(start + (long)c * kC) * p.H + h) * D;
+#pragma unroll
+                for (int k = et; k < kC * CPR; k += 128) {
+                    const int t = k / CPR, cc = k % CPR;
+                    if (t < nv)
+                        *reinterpret_cast<uint4 *>(obase + (size_t)t * p.H * D + cc * 8) =
+                            *reinterpret_cast<const uint4 *>(stg + t * D + cc * 8);
                 }
+                fence_proxy_async();        // the stage is refilled by TMA next
+                mbar_arrive(&e_empty[b]);
             }
-            tc_fence_before();
-            mbar_arrive(&d_free[b]);
         }
     }
     tc_fence_before();
