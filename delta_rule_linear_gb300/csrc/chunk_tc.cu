@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
     uint8_t *sE0 = sm;
     uint8_t *sAS = sm + 2 * Cf::E_BYTES;
     uint8_t *sAV0 = sAS + Cf::AS_BYTES;
-    __shared__ uint64_t e_full[2], e_empty[2], d_full[2], d_free[2], s_ready;
+    __shared__ uint64_t e_full[2], e_empty[2], v_full[2], v_empty[2], d_full[2], d_free[2], s_ready;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_fail;
 
@@ -577,7 +577,9 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(&e_full[s], 1);
-            mbar_init(&e_empty[s], 128);   // released by the epilogue (it stages o there)
+            mbar_init(&e_empty[s], 1);     // released by the MMA commit
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 128);   // released by the epilogue (it stages o there)
             mbar_init(&d_full[s], 1);
             mbar_init(&d_free[s], 128);
         }
@@ -595,7 +597,8 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
     const uint32_t tm = tmem_slot;
 
     if (warp == 0) {
-        // ---------------- producer: E_c and V_c by TMA, two chunks ahead
+        // ---------------- producers: lane 0 streams E_c (stage freed by the MMAs),
+        // lane 1 streams V_c (stage freed by the epilogue, which stages o there)
         if (lane == 0) {
             for (int c = 0; c < nc && !s_fail; ++c) {
                 const int s = c & 1;
@@ -604,14 +607,24 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
                     record_error(p.ws, 10);
                     break;
                 }
-                mbar_expect_tx(&e_full[s], Cf::E_BYTES + Cf::AV_BYTES);
+                mbar_expect_tx(&e_full[s], Cf::E_BYTES);
                 uint8_t *dE = sE0 + s * Cf::E_BYTES;
                 const int slot = (int)(slot0 + (long)c * p.H);
                 for (int kb = 0; kb < Cf::NKB; ++kb)
                     tma_load_3d(dE + kb * (R * 128), &map_E, &e_full[s], kb * 64, 0, slot);
+            }
+        } else if (lane == 1) {
+            for (int c = 0; c < nc && !s_fail; ++c) {
+                const int s = c & 1;
+                if (c >= 2 && !mbar_wait(&v_empty[s], ((c >> 1) - 1) & 1, kWaitNs)) {
+                    s_fail = 1;
+                    record_error(p.ws, 15);
+                    break;
+                }
+                mbar_expect_tx(&v_full[s], Cf::AV_BYTES);
                 uint8_t *dV = sAV0 + s * Cf::AV_BYTES;
                 for (int mb = 0; mb < Cf::NB; ++mb)
-                    tma_load_3d(dV + mb * 8192, &map_v, &e_full[s], mb * 64, h,
+                    tma_load_3d(dV + mb * 8192, &map_v, &v_full[s], mb * 64, h,
                                 (int)(start + (long)c * kC));
             }
         }
@@ -624,6 +637,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
             for (int c = 0; c < nc && !s_fail; ++c) {
                 const int b = c & 1;
                 if (!mbar_wait(&e_full[b], (c >> 1) & 1, kWaitNs) ||
+                    !mbar_wait(&v_full[b], (c >> 1) & 1, kWaitNs) ||
                     (c >= 2 && !mbar_wait(&d_free[b], ((c >> 1) - 1) & 1, kWaitNs))) {
                     s_fail = 1;
                     record_error(p.ws, 11);
@@ -646,6 +660,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
                     mma_bf16_ss(dcol, desc_kmajor_sw128(as0, D, ks), desc_kmajor_sw128(e0, R, ks),
                                 idS, 1u);
                 mma_commit(&d_full[b]);
+                mma_commit(&e_empty[b]);
             }
         }
     } else {
@@ -712,15 +727,15 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
             if (!last) fence_proxy_async();
             tc_fence_before();
             mbar_arrive(&s_ready);   // S_{c+1}^T is in place
-            {   // output part: O[t][j], staged row-major [t][j] in the consumed E_c stage,
-                // then written out as whole rows with 16-byte stores
+            {   // output part: O[t][j], staged row-major [t][j] in the consumed V_c stage
+                // (exactly 64 x D bf16), then written out as whole rows with 16-byte stores
                 uint32_t v[kC];
                 tmem_ld32(dcol + D, *reinterpret_cast<uint32_t(*)[32]>(v));
                 tmem_ld32(dcol + D + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(&d_free[b]);   // the accumulator may be overwritten from here on
-                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sE0 + b * Cf::E_BYTES);
+                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sAV0 + b * Cf::AV_BYTES);
                 if (has_row)
 #pragma unroll
                     for (int t = 0; t < kC; ++t) stg[t * D + j] = __float2bfloat16_rn(__uint_as_float(v[t]));
@@ -737,7 +752,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
                             *reinterpret_cast<const uint4 *>(stg + t * D + cc * 8);
                 }
                 fence_proxy_async();        // the stage is refilled by TMA next
-                mbar_arrive(&e_empty[b]);
+                mbar_arrive(&v_empty[b]);
             }
         }
     }
