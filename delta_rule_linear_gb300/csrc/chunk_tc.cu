@@ -546,12 +546,14 @@ struct ChainCfg {
     static constexpr int E_BYTES = R * R * 2;     // one stage of E_c (K-major SW128, R rows)
     static constexpr int AS_BYTES = D * D * 2;    // S^T operand (K-major SW128, D rows)
     static constexpr int AV_BYTES = 64 * D * 2;   // one stage of V_c (MN-major SW128)
-    static constexpr int SMEM = 2 * E_BYTES + AS_BYTES + 2 * AV_BYTES + 1024;
+    static constexpr int O_BYTES = 64 * D * 2;    // output staging [64][D] bf16
+    static constexpr int SMEM = 2 * E_BYTES + AS_BYTES + 2 * AV_BYTES + O_BYTES + 1024;
     static constexpr uint32_t TCOLS = (2 * R <= 256) ? 256u : 512u;   // two accumulators
+    static constexpr int THREADS = 320;           // producer, MMA, 4 state + 4 output warps
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ CUtensorMap map_E,
+__global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ CUtensorMap map_E,
                                                        const __grid_constant__ CUtensorMap map_v,
                                                        TcParams p) {
     using Cf = ChainCfg<D>;
@@ -561,6 +563,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
     uint8_t *sE0 = sm;
     uint8_t *sAS = sm + 2 * Cf::E_BYTES;
     uint8_t *sAV0 = sAS + Cf::AS_BYTES;
+    uint8_t *sO = sAV0 + 2 * Cf::AV_BYTES;
     __shared__ uint64_t e_full[2], e_empty[2], v_full[2], v_empty[2], d_full[2], d_free[2], s_ready;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_fail;
@@ -579,9 +582,9 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
             mbar_init(&e_full[s], 1);
             mbar_init(&e_empty[s], 1);     // released by the MMA commit
             mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 128);   // released by the epilogue (it stages o there)
+            mbar_init(&v_empty[s], 1);     // released by the MMA commit
             mbar_init(&d_full[s], 1);
-            mbar_init(&d_free[s], 128);
+            mbar_init(&d_free[s], 256);    // both epilogue groups read the accumulator
         }
         mbar_init(&s_ready, 128);
         fence_mbar_init();
@@ -661,10 +664,12 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
                                 idS, 1u);
                 mma_commit(&d_full[b]);
                 mma_commit(&e_empty[b]);
+                mma_commit(&v_empty[b]);
             }
         }
-    } else {
-        // ---------------- epilogue warps 2..5: TMEM quadrant q, value column j
+    } else if (warp < 6) {
+        // ---------------- state epilogue, warps 2..5: TMEM quadrant q, value column j.
+        // Turns the fp32 next state into the bf16 S^T operand (the critical path).
         const int q = warp & 3;
         const bool has_row = (D == 128) || (lane < 16);   // M = 64: 16 rows per quadrant
         const int j = (D == 128) ? 32 * q + lane : 16 * q + lane;
@@ -701,58 +706,69 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
             tc_fence_after();
             const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
             const bool last = (c + 1 == nc);
-            {   // state part: S_next[i][j], all D columns loaded before one wait
-                uint32_t v[D];
+            uint32_t v[D];
 #pragma unroll
-                for (int i0 = 0; i0 < D; i0 += 32)
-                    tmem_ld32(dcol + i0, *reinterpret_cast<uint32_t(*)[32]>(v + i0));
-                tmem_ld_wait();
-                if (has_row) {
-                    if (!last) {
+            for (int i0 = 0; i0 < D; i0 += 32)
+                tmem_ld32(dcol + i0, *reinterpret_cast<uint32_t(*)[32]>(v + i0));
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&d_free[b]);
+            if (has_row) {
+                if (!last) {
 #pragma unroll
-                        for (int cc = 0; cc < D / 8; ++cc)
-                            *reinterpret_cast<uint4 *>(sAS + (cc >> 3) * D * 128 + j * 128 +
-                                                       (((cc & 7) ^ (j & 7)) << 4)) =
-                                make_uint4(pack_bf16(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
-                                           pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
-                                           pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
-                                           pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
-                    } else if (p.hT) {
+                    for (int cc = 0; cc < D / 8; ++cc)
+                        *reinterpret_cast<uint4 *>(sAS + (cc >> 3) * D * 128 + j * 128 +
+                                                   (((cc & 7) ^ (j & 7)) << 4)) =
+                            make_uint4(pack_bf16(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
+                                       pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
+                                       pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
+                                       pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
+                } else if (p.hT) {
 #pragma unroll
-                        for (int i = 0; i < D; ++i)
-                            p.hT[hbase + (size_t)i * D + j] = __uint_as_float(v[i]);
-                    }
+                    for (int i = 0; i < D; ++i) p.hT[hbase + (size_t)i * D + j] = __uint_as_float(v[i]);
                 }
             }
             if (!last) fence_proxy_async();
-            tc_fence_before();
             mbar_arrive(&s_ready);   // S_{c+1}^T is in place
-            {   // output part: O[t][j], staged row-major [t][j] in the consumed V_c stage
-                // (exactly 64 x D bf16), then written out as whole rows with 16-byte stores
-                uint32_t v[kC];
-                tmem_ld32(dcol + D, *reinterpret_cast<uint32_t(*)[32]>(v));
-                tmem_ld32(dcol + D + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&d_free[b]);   // the accumulator may be overwritten from here on
-                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sAV0 + b * Cf::AV_BYTES);
-                if (has_row)
+        }
+    } else {
+        // ---------------- output epilogue, warps 6..9: O[t][j] from the same
+        // accumulator, staged row-major [t][j] and written out as whole 16-byte rows.
+        const int q = warp & 3;
+        const bool has_row = (D == 128) || (lane < 16);
+        const int j = (D == 128) ? 32 * q + lane : 16 * q + lane;
+        const uint32_t lrow = (uint32_t)(32 * q) << 16;
+        const int et = tid - 192;       // 0..127 over the output warps
+        __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sO);
+        constexpr int CPR = D / 8;      // 16-byte pieces per output row
+        for (int c = 0; c < nc; ++c) {
+            const int b = c & 1;
+            if (s_fail || !mbar_wait(&d_full[b], (c >> 1) & 1, kWaitNs)) {
+                s_fail = 1;
+                record_error(p.ws, 14);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
+            uint32_t v[kC];
+            tmem_ld32(dcol + D, *reinterpret_cast<uint32_t(*)[32]>(v));
+            tmem_ld32(dcol + D + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&d_free[b]);
+            named_sync(1, 128);          // the previous chunk's rows have been written out
+            if (has_row)
 #pragma unroll
-                    for (int t = 0; t < kC; ++t) stg[t * D + j] = __float2bfloat16_rn(__uint_as_float(v[t]));
-                named_sync(1, 128);
-                const int nv = min(kC, len - c * kC);
-                const int et = tid - 64;   // 0..127 over the epilogue warps
-                constexpr int CPR = D / 8;  // 16-byte pieces per output row
-                __nv_bfloat16 *obase = p.o + ((size_t)(start + (long)c * kC) * p.H + h) * D;
+                for (int t = 0; t < kC; ++t) stg[t * D + j] = __float2bfloat16_rn(__uint_as_float(v[t]));
+            named_sync(1, 128);
+            const int nv = min(kC, len - c * kC);
+            __nv_bfloat16 *obase = p.o + ((size_t)(start + (long)c * kC) * p.H + h) * D;
 #pragma unroll
-                for (int k = et; k < kC * CPR; k += 128) {
-                    const int t = k / CPR, cc = k % CPR;
-                    if (t < nv)
-                        *reinterpret_cast<uint4 *>(obase + (size_t)t * p.H * D + cc * 8) =
-                            *reinterpret_cast<const uint4 *>(stg + t * D + cc * 8);
-                }
-                fence_proxy_async();        // the stage is refilled by TMA next
-                mbar_arrive(&v_empty[b]);
+            for (int k = et; k < kC * CPR; k += 128) {
+                const int t = k / CPR, cc = k % CPR;
+                if (t < nv)
+                    *reinterpret_cast<uint4 *>(obase + (size_t)t * p.H * D + cc * 8) =
+                        *reinterpret_cast<const uint4 *>(stg + t * D + cc * 8);
             }
         }
     }
@@ -852,7 +868,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     using Cf = ChainCfg<D>;
     e = cudaFuncSetAttribute(chain_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (e != cudaSuccess) return e;
-    chain_kernel<D><<<(unsigned)((long)a.nseq * a.H), 192, Cf::SMEM, st>>>(me, mv, p);
+    chain_kernel<D><<<(unsigned)((long)a.nseq * a.H), Cf::THREADS, Cf::SMEM, st>>>(me, mv, p);
     return cudaGetLastError();
 }
 
