@@ -600,9 +600,14 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
     const uint32_t tm = tmem_slot;
 
     if (warp == 0) {
-        // ---------------- producers: lane 0 streams E_c (stage freed by the MMAs),
-        // lane 1 streams V_c (stage freed by the epilogue, which stages o there)
+        // ---------------- producers: lane 0 streams E_c, lane 1 streams V_c, each into
+        // two shared-memory stages freed by the MMA commit; both also prefetch the
+        // tiles kPrefetch chunks ahead into L2 so that the stage loads hit L2.
+        constexpr int kPrefetch = 4;
         if (lane == 0) {
+            for (int c = 0; c < kPrefetch && c < nc; ++c)
+                for (int kb = 0; kb < Cf::NKB; ++kb)
+                    tma_prefetch_l2_3d(&map_E, kb * 64, 0, (int)(slot0 + (long)c * p.H));
             for (int c = 0; c < nc && !s_fail; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !mbar_wait(&e_empty[s], ((c >> 1) - 1) & 1, kWaitNs)) {
@@ -615,8 +620,14 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
                 const int slot = (int)(slot0 + (long)c * p.H);
                 for (int kb = 0; kb < Cf::NKB; ++kb)
                     tma_load_3d(dE + kb * (R * 128), &map_E, &e_full[s], kb * 64, 0, slot);
+                if (c + kPrefetch < nc)
+                    for (int kb = 0; kb < Cf::NKB; ++kb)
+                        tma_prefetch_l2_3d(&map_E, kb * 64, 0, (int)(slot0 + (long)(c + kPrefetch) * p.H));
             }
         } else if (lane == 1) {
+            for (int c = 0; c < kPrefetch && c < nc; ++c)
+                for (int mb = 0; mb < Cf::NB; ++mb)
+                    tma_prefetch_l2_3d(&map_v, mb * 64, h, (int)(start + (long)c * kC));
             for (int c = 0; c < nc && !s_fail; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !mbar_wait(&v_empty[s], ((c >> 1) - 1) & 1, kWaitNs)) {
@@ -629,6 +640,9 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
                 for (int mb = 0; mb < Cf::NB; ++mb)
                     tma_load_3d(dV + mb * 8192, &map_v, &v_full[s], mb * 64, h,
                                 (int)(start + (long)c * kC));
+                if (c + kPrefetch < nc)
+                    for (int mb = 0; mb < Cf::NB; ++mb)
+                        tma_prefetch_l2_3d(&map_v, mb * 64, h, (int)(start + (long)(c + kPrefetch) * kC));
             }
         }
     } else if (warp == 1) {
