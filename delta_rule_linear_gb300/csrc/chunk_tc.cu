@@ -21,11 +21,11 @@
 //  * prep_kernel  -- one CTA per (sequence, head, chunk): TMA loads q, k; tcgen05
 //    products [K;Q] K^T, K^T diag(f) [T'|P], Aqk [T'|P], Z k; a blocked fp32
 //    forward-substitution inverse on CUDA cores; writes E_c (bf16) to scratch.
-//  * chain_kernel -- one CTA per (sequence, head, value tile): walks the chunks in
-//    order; per chunk ONE dependent tensor-core product D = E_c [S; V_tile] gives the
-//    next state (fp32 in TMEM, stored back as the bf16 operand) and the outputs.
-//    A producer warp streams E_c and V by TMA two chunks ahead; an MMA warp issues;
-//    four epilogue warps turn the next state into the next operand and store o.
+//  * chain_kernel -- one CTA per (sequence, head): walks the chunks in order; per
+//    chunk one product D^T = [S^T | V^T] E_c^T (M = dv) gives the next state (fp32 in
+//    TMEM, stored back as the bf16 operand) and the outputs.  Producer lanes stream
+//    E_c and V_c by TMA; an MMA warp issues; four warps turn the next state into the
+//    next operand, four others store o.
 //
 // Every wait on an mbarrier is bounded; on time-out the kernel records
 // KDA_ERR_DEVICE_TIMEOUT in the workspace header and unwinds (no trap).
