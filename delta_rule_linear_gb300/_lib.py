@@ -23,8 +23,8 @@ STATUS = {
 }
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace", "kda_chunk_fwd",
-           "kda_recurrent_fwd", "kda_decode_step", "kda_varlen_fwd_workspace", "kda_varlen_fwd",
-           "kda_query_device_error")
+           "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "kda_decode_step",
+           "kda_varlen_fwd_workspace", "kda_varlen_fwd", "kda_query_device_error")
 
 
 class KdaError(RuntimeError):
@@ -63,6 +63,8 @@ def load(path: str | None = None):
         lib.kda_varlen_fwd_workspace.restype = Z
         lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, Z, P]
         lib.kda_chunk_fwd.restype = I
+        lib.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P]
+        lib.kda_chunk_fwd_noalloc.restype = I
         lib.kda_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.kda_recurrent_fwd.restype = I
         lib.kda_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, I, P]
@@ -158,6 +160,35 @@ def chunk_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None, chun
     _raise(rc, "kda_chunk_fwd", lib)
     if check_device:
         _raise(query_device_error(ws, stream), "kda_chunk_fwd (device)", lib)
+    return o, hT
+
+
+def chunk_fwd_noalloc(q, k, v, beta, decay=None, initial_state=None, *, scale=None,
+                      chunk_size=64, use_qk_l2norm=True, out=None, final_state=None, stream=None):
+    """kda_chunk_fwd_noalloc: chunked prefill with the library's built-in scratch.
+
+    For callers that cannot hand over device memory for a workspace.  bf16 q/k/v with
+    dk == dv in {64, 128} and chunk 64 only; raises KdaError(KDA_ERR_WORKSPACE) when the
+    problem needs more than the built-in 64 MiB.  Calls that overlap on the GPU race on
+    that one buffer, so keep them ordered.  Returns (o, final_state).
+    """
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, H, dv))
+    _check(beta, "beta", torch.float32, (B, T, H)); _check(decay, "decay", torch.float32, (B, T, H))
+    _check(initial_state, "initial_state", torch.float32, (B, H, dk, dv))
+    o = out if out is not None else torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    _check(o, "out", q.dtype, (B, T, H, dv))
+    hT = final_state if final_state is not None else torch.empty((B, H, dk, dv), dtype=torch.float32,
+                                                                  device=q.device)
+    _check(hT, "final_state", torch.float32, (B, H, dk, dv))
+    rc = lib.kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay),
+                                   _ptr(initial_state), _ptr(o), _ptr(hT), B, T, H, dk, dv, dt,
+                                   float(scale or 0.0), int(chunk_size), int(bool(use_qk_l2norm)),
+                                   _stream(stream))
+    _raise(rc, "kda_chunk_fwd_noalloc", lib)
     return o, hT
 
 

@@ -112,6 +112,35 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          void *ws, size_t ws_bytes, kda_stream_t stream);
 
 /*
+ * Chunked prefill that allocates nothing and takes no workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate device memory
+ * where they call us -- a plugin inside a framework that owns the memory pool, code on a
+ * latency-critical path where cudaMalloc/cudaFree would synchronise the device, or a
+ * caller with no spare memory to hand over.
+ *
+ * Same arguments and results as kda_chunk_fwd without ws/ws_bytes, for the tensor-core
+ * shapes only: dtype KDA_BF16, dk == dv in {64, 128}, chunk_size 64 (anything else
+ * returns KDA_ERR_UNSUPPORTED).  Its scratch is one 64 MiB array that the library keeps
+ * on every GPU that loads it, until the process exits; a problem whose scratch would not
+ * fit returns KDA_ERR_WORKSPACE before anything is enqueued.  The scratch needed is
+ * 256 + ceil(4(B+1)/256)*256 + B * ceil(T/64) * H * (D+64)^2 * 2 bytes, i.e. at most
+ * 910 (chunk, head) pairs at D = 128 and 2047 at D = 64.
+ *
+ * The first call on a device looks the array's device address up (with that device
+ * current); make that first call before any stream capture.  Every call shares the one
+ * array, so calls that overlap on the GPU (on different streams, or from different
+ * threads without ordering) race and corrupt each other's results; order them.  A kernel
+ * time-out of this entry point is recorded in the array's own header, which the caller
+ * cannot query; kda_query_device_error does not apply.
+ */
+kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                 const float *beta, const float *decay,
+                                 const float *initial_state, void *o, float *final_state,
+                                 int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                                 float scale, int chunk_size, int use_qk_l2norm,
+                                 kda_stream_t stream);
+
+/*
  * Recurrent prefill (kda() "Algorithm Modes": recurrent -- the pure sequential
  * scan; kda(use_chunked=False)).  Same arguments as kda_chunk_fwd without the
  * chunk size; needs no workspace.  One CUDA-core kernel, one token at a time.
