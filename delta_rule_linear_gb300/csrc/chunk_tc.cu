@@ -88,31 +88,37 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 
 // ---------------------------------------------------------------------------------
 // T = (I + L)^{-1} for a 64 x 64 strictly-lower L, fp32 in shared memory (row pitch
-// 65), by 128 threads: the four 16 x 16 diagonal blocks by column-wise forward
-// substitution, then the off-diagonal blocks by distance from the diagonal,
-//   T_ij = -T_ii sum_{k=j}^{i-1} L_ik T_kj.
+// 65), by NT threads: the four 16 x 16 diagonal blocks by forward substitution (one
+// lane per column, the column kept in registers), then the off-diagonal blocks by
+// distance from the diagonal,  T_ij = -T_ii sum_{k=j}^{i-1} L_ik T_kj.
 // The unused upper blocks of L hold the partial sums X_ij.
 // ---------------------------------------------------------------------------------
+template <int NT>
 __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
     constexpr int P = 65;
     const int warp = tid >> 5, lane = tid & 31;
-    if (lane < 16) {
-        const int b0 = 16 * warp, j = lane, col = b0 + j;
+    if (warp < 4 && lane < 16) {
+        const int b0 = 16 * warp, j = lane;
+        float x[16];
+#pragma unroll
         for (int r = 0; r < 16; ++r) {
-            const int row = b0 + r;
-            float x = (r == j) ? 1.f : 0.f;
-            for (int s = j; s < r; ++s) x = fmaf(-sL[row * P + b0 + s], sT[(b0 + s) * P + col], x);
-            sT[row * P + col] = x;
+            float acc = (r == j) ? 1.f : 0.f;
+            const float *Lr = sL + (b0 + r) * P + b0;
+#pragma unroll
+            for (int s = 0; s < r; ++s) acc = fmaf(-Lr[s], x[s], acc);   // x[s] = 0 for s < j
+            x[r] = acc;
         }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
     }
-    for (int idx = tid; idx < 64 * 64; idx += 128) {
+    for (int idx = tid; idx < 64 * 64; idx += NT) {
         const int r = idx >> 6, c = idx & 63;
         if ((c >> 4) > (r >> 4)) sT[r * P + c] = 0.f;
     }
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
         const int nblk = 4 - d;
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += NT) {
             const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int j = b, i = b + d;
             float x = 0.f;
@@ -123,7 +129,7 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
             sL[(16 * j + r) * P + 16 * i + cc] = x;
         }
         __syncthreads();
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += NT) {
             const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int j = b, i = b + d;
             float x = 0.f;
@@ -136,9 +142,26 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
     }
 }
 
+// 8 fp32 -> one 16-byte group of bf16
+__device__ __forceinline__ uint4 pack8(const float *f) {
+    return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                      pack_bf16(f[6], f[7]));
+}
+__device__ __forceinline__ uint4 pack8u(const uint32_t *u) {
+    return make_uint4(pack_bf16(__uint_as_float(u[0]), __uint_as_float(u[1])),
+                      pack_bf16(__uint_as_float(u[2]), __uint_as_float(u[3])),
+                      pack_bf16(__uint_as_float(u[4]), __uint_as_float(u[5])),
+                      pack_bf16(__uint_as_float(u[6]), __uint_as_float(u[7])));
+}
+
 // ---------------------------------------------------------------------------------
-// prep_kernel
+// prep_kernel -- builds E_c for one (sequence, head, chunk).  256 threads: the two
+// warps w and w + 4 share TMEM lane quadrant w % 4 and split each result row's
+// columns between them.  Rows of an M = 128 result: 32 q + lane; of an M = 64
+// result: 16 q + lane for lane < 16.
 // ---------------------------------------------------------------------------------
+constexpr int kPrepThreads = 256;
+
 template <int D>
 struct PrepSmem {
     static constexpr int NB = D / 64;
@@ -151,9 +174,9 @@ struct PrepSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(128) prep_kernel(const __grid_constant__ CUtensorMap map_q,
-                                                   const __grid_constant__ CUtensorMap map_k,
-                                                   TcParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_constant__ CUtensorMap map_q,
+                                                               const __grid_constant__ CUtensorMap map_k,
+                                                               TcParams p) {
     using Ly = PrepSmem<D>;
     constexpr int NB = D / 64;
     constexpr int R = D + 64;
@@ -163,6 +186,10 @@ __global__ void __launch_bounds__(128) prep_kernel(const __grid_constant__ CUten
     __shared__ uint32_t tmem_slot;
     __shared__ int s_fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hh = warp >> 2;
+    const int i128 = 32 * q4 + lane;
+    const int i64 = 16 * q4 + lane;
+    const bool has64 = lane < 16;
 
     const int g = blockIdx.x / p.H, h = blockIdx.x % p.H;
     int n, c;
@@ -212,7 +239,7 @@ __global__ void __launch_bounds__(128) prep_kernel(const __grid_constant__ CUten
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = tmem_slot;
-    const uint32_t tq = (uint32_t)(32 * warp) << 16;   // this warp's TMEM lane quadrant
+    const uint32_t tq = (uint32_t)(32 * q4) << 16;   // this warp's TMEM lane quadrant
 
     if (tid == 0) {
         mbar_expect_tx(&bar_tma, NB * 2 * 64 * 128);
@@ -227,13 +254,19 @@ __global__ void __launch_bounds__(128) prep_kernel(const __grid_constant__ CUten
         mdec[tid] = (tid < nv && p.decay) ? p.decay[gi] : 0.f;
     }
     __syncthreads();
-    if (tid < 64) {   // in-chunk cumulative log-decay, G_{t-1} and G_t
-        float run = 0.f;
-        for (int r = 0; r < tid; ++r) run += mdec[r];
-        mGp[tid] = run;
-        run += mdec[tid];
-        mG[tid] = run;
-        meg[tid] = expf(run);
+    if (warp == 0) {   // in-chunk cumulative log-decay: lane owns tokens 2 lane, 2 lane + 1
+        const float d0 = mdec[2 * lane], d1 = mdec[2 * lane + 1];
+        float incl = d0 + d1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const float excl = incl - (d0 + d1);
+        mGp[2 * lane] = excl;
+        mG[2 * lane] = excl + d0;
+        mGp[2 * lane + 1] = excl + d0;
+        mG[2 * lane + 1] = incl;
     }
     if (!mbar_wait(&bar_tma, 0, kWaitNs)) s_fail = 1;
     __syncthreads();
@@ -249,104 +282,101 @@ __global__ void __launch_bounds__(128) prep_kernel(const __grid_constant__ CUten
                         ks > 0 ? 1u : 0u);
         mma_commit(&bar_mma);
     }
-    if (tid >= 64 && ok) {   // query norms (the swizzle only permutes a row's chunks)
-        const int t = tid - 64;
+    if (tid >= 128 && ok) {   // query norms: two threads per row (the swizzle permutes chunks only)
+        const int t = (tid - 128) >> 1, part = tid & 1;
         float ss = 0.f;
-        for (int kb = 0; kb < NB; ++kb) {
-            const uint4 *row = reinterpret_cast<const uint4 *>(sKQ + kb * 16384 + 8192 + t * 128);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 w = row[j];
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        for (int cc = 0; cc < NB * 4; ++cc) {
+            const int chunk = part * NB * 4 + cc;
+            const uint4 w = *reinterpret_cast<const uint4 *>(sKQ + (chunk >> 3) * 16384 + 8192 +
+                                                             t * 128 + ((chunk & 7) << 4));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = bf16lo(ws[e]), b = bf16hi(ws[e]);
-                    ss = fmaf(a, a, fmaf(b, b, ss));
-                }
+            for (int e = 0; e < 4; ++e) {
+                const float a = bf16lo(ws[e]), b = bf16hi(ws[e]);
+                ss = fmaf(a, a, fmaf(b, b, ss));
             }
         }
-        mqn[t] = p.use_l2 ? p.scale / fmaxf(sqrtf(ss), kNormEps) : p.scale;
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (part == 0) mqn[t] = p.use_l2 ? p.scale / fmaxf(sqrtf(ss), kNormEps) : p.scale;
     }
+    if (tid < 64) meg[tid] = __expf(mG[tid]);
     if (ok && !mbar_wait(&bar_mma, 0, kWaitNs)) s_fail = 1;
     tc_fence_after();
 
-    // ---- epilogue 1: norms, L (fp32, smem) and Aqk (bf16 operand)
-    uint32_t r0[32], r1[32];
-    tmem_ld32(tm + tq + 0, r0);
-    tmem_ld32(tm + tq + 32, r1);
+    // ---- epilogue 1: norms, L (fp32, smem) and Aqk (bf16 operand); columns 32 hh ..
+    uint32_t r[32];
+    tmem_ld32(tm + tq + 32 * hh, r);
     tmem_ld_wait();
-    if (tid < 64) {
+    if (i128 < 64 && (i128 >> 5) == hh) {   // this half holds the Gram diagonal of row i128
         float diag = 0.f;
 #pragma unroll
-        for (int s = 0; s < 32; ++s) {
-            if (s == tid) diag = __uint_as_float(r0[s]);
-            if (s + 32 == tid) diag = __uint_as_float(r1[s]);
-        }
-        mkn[tid] = p.use_l2 ? 1.f / fmaxf(sqrtf(diag), kNormEps) : 1.f;
+        for (int s = 0; s < 32; ++s)
+            if (s == (i128 & 31)) diag = __uint_as_float(r[s]);
+        mkn[i128] = p.use_l2 ? 1.f / fmaxf(sqrtf(diag), kNormEps) : 1.f;
     }
     __syncthreads();
     ok = s_fail == 0;
     const float gC = mG[63];
-    if (tid < 64) {
-        const int t = tid;
+    if (i128 < 64) {
+        const int t = i128;
         const float kt = mkn[t], bt = mbeta[t], gpt = mGp[t];
-        mf[t] = t < nv ? expf(gC - mG[t]) * kt : 0.f;
-        mcw[t] = mbeta[t] * expf(gpt) * kt;    // column weight of T' = T diag(beta e^{G_{s-1}} kn_s)
-        float *Lrow = sL + t * 65;
+        if (hh == 0) {
+            mf[t] = t < nv ? __expf(gC - mG[t]) * kt : 0.f;
+            mcw[t] = bt * __expf(gpt) * kt;   // column weight of T' = T diag(beta e^{G_{s-1}} kn)
+        }
+        float *Lrow = sL + t * 65 + 32 * hh;
+        const float bk = bt * kt;
 #pragma unroll
-        for (int s = 0; s < 64; ++s) {
-            const float gram = __uint_as_float(s < 32 ? r0[s] : r1[s - 32]);
-            Lrow[s] = (s < t && t < nv) ? bt * kt * mkn[s] * gram * expf(gpt - mG[s]) : 0.f;
+        for (int s2 = 0; s2 < 32; ++s2) {
+            const int s = 32 * hh + s2;
+            const float val = bk * mkn[s] * __uint_as_float(r[s2]) * __expf(gpt - mG[s]);
+            Lrow[s2] = (s < t && t < nv) ? val : 0.f;
         }
     } else {
-        const int t = tid - 64;
+        const int t = i128 - 64;
         const float qt = mqn[t], gt = mG[t];
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            uint32_t pk[4];
+        for (int cc = 0; cc < 4; ++cc) {
+            float f[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float v2[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int s = cc * 8 + e * 2 + u;
-                    const float qk = __uint_as_float(s < 32 ? r0[s] : r1[s - 32]);
-                    v2[u] = (s <= t && t < nv) ? qt * mkn[s] * qk * expf(gt - mG[s]) : 0.f;
-                }
-                pk[e] = pack_bf16(v2[0], v2[1]);
+            for (int e = 0; e < 8; ++e) {
+                const int s = 32 * hh + cc * 8 + e;
+                const float val = qt * mkn[s] * __uint_as_float(r[cc * 8 + e]) *
+                                  __expf(gt - mG[s]);
+                f[e] = (s <= t && t < nv) ? val : 0.f;
             }
-            *reinterpret_cast<uint4 *>(sA + t * 128 + ((cc ^ (t & 7)) << 4)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            const int chunk = 4 * hh + cc;
+            *reinterpret_cast<uint4 *>(sA + t * 128 + ((chunk ^ (t & 7)) << 4)) = pack8(f);
         }
     }
     fence_proxy_async();
     __syncthreads();
 
     // ---- T = (I + L)^{-1}
-    invert_unit_lower_64(sL, sT, tid);
+    invert_unit_lower_64<kPrepThreads>(sL, sT, tid);
 
-    // ---- B = [T' | P], Bf = diag(f) B   (MN-major: row t, columns s)
+    // ---- B = [T' | P], Bf = diag(f) B   (MN-major: row t, columns s); 4 threads per row
     {
-        const int t = tid >> 1, half = tid & 1;
+        const int t = tid >> 2, half = (tid >> 1) & 1, grp = tid & 1;
         const float *Trow = sT + t * 65;
         const float ft = mf[t];
+        const float *w = half ? mbeta : mcw;
         uint8_t *dB = sB + half * 8192 + t * 128;
         uint8_t *dBf = sBf + half * 8192 + t * 128;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            uint32_t pk[4], pf[4];
+        for (int cc = 0; cc < 4; ++cc) {
+            const int chunk = grp * 4 + cc;
+            float f[8], fb[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int s = cc * 8 + e * 2;
-                const float w0 = half ? mbeta[s] : mcw[s];
-                const float w1 = half ? mbeta[s + 1] : mcw[s + 1];
-                const float a = Trow[s] * w0, b = Trow[s + 1] * w1;
-                pk[e] = pack_bf16(a, b);
-                pf[e] = pack_bf16(a * ft, b * ft);
+            for (int e = 0; e < 8; ++e) {
+                const int s = chunk * 8 + e;
+                f[e] = Trow[s] * w[s];
+                fb[e] = f[e] * ft;
             }
-            const int off = (cc ^ (t & 7)) << 4;
-            *reinterpret_cast<uint4 *>(dB + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4 *>(dBf + off) = make_uint4(pf[0], pf[1], pf[2], pf[3]);
+            const int off = (chunk ^ (t & 7)) << 4;
+            *reinterpret_cast<uint4 *>(dB + off) = pack8(f);
+            *reinterpret_cast<uint4 *>(dBf + off) = pack8(fb);
         }
     }
     fence_proxy_async();
@@ -370,76 +400,38 @@ __global__ void __launch_bounds__(128) prep_kernel(const __grid_constant__ CUten
     if (ok && !mbar_wait(&bar_mma, 1, kWaitNs)) s_fail = 1;
     tc_fence_after();
 
-    // ---- epilogue 2: Z1, Z2 operands; the V-columns of E (K~^T P, Aqk P)
+    // ---- epilogue 2: Z1, Z2 operands (column half 0); the V columns of E (half 1)
     {
-        // rows of D2a: M = D (M = 128: row = lane of quadrant; M = 64: 16 rows per quadrant)
-        const bool has_row = (D == 128) || (lane < 16);
-        const int i = (D == 128) ? tid : 16 * warp + lane;
+        uint32_t v[64];
+        tmem_ld32(tm + tq + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32(tm + tq + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_wait();
+        const bool has_row = (D == 128) || has64;
+        const int i = (D == 128) ? i128 : i64;
+        if (has_row) {
+            if (hh == 0) {   // Z1[i][s]: K-major operand, rows i
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t v[32];
-            tmem_ld32(tm + tq + 64 * half, v);
-            uint32_t v2[32];
-            tmem_ld32(tm + tq + 64 * half + 32, v2);
-            tmem_ld_wait();
-            if (has_row) {
-                if (half == 0) {   // Z1[i][s] -> K-major operand, rows i, 64 columns
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((cc ^ (i & 7)) << 4)) = pack8u(v + 8 * cc);
+            } else {         // E[i][D + s] = (K~^T P)[i][s]
+                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)i * R + D);
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int s = cc * 8 + e * 2;
-                            const float a = __uint_as_float(s < 32 ? v[s] : v2[s - 32]);
-                            const float b = __uint_as_float(s + 1 < 32 ? v[s + 1] : v2[s + 1 - 32]);
-                            pk[e] = pack_bf16(a, b);
-                        }
-                        *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((cc ^ (i & 7)) << 4)) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
-                } else {           // E[i][D + s] = (K~^T P)[i][s]
-                    uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)i * R + D);
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int s = cc * 8 + e * 2;
-                            const float a = __uint_as_float(s < 32 ? v[s] : v2[s - 32]);
-                            const float b = __uint_as_float(s + 1 < 32 ? v[s + 1] : v2[s + 1 - 32]);
-                            pk[e] = pack_bf16(a, b);
-                        }
-                        dst[cc] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
-                }
+                for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8u(v + 8 * cc);
             }
         }
-        // rows of D2b (M = 64): t = 16 * warp + lane for lane < 16
-        const int t = 16 * warp + lane;
+        tmem_ld32(tm + tq + 128 + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32(tm + tq + 128 + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_wait();
+        if (has64) {
+            const int t = i64;
+            if (hh == 0) {   // Z2[t][s]
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t v[32], v2[32];
-            tmem_ld32(tm + tq + 128 + 64 * half, v);
-            tmem_ld32(tm + tq + 128 + 64 * half + 32, v2);
-            tmem_ld_wait();
-            if (lane < 16) {
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(sZ2 + t * 128 + ((cc ^ (t & 7)) << 4)) = pack8u(v + 8 * cc);
+            } else {         // E[D + t][D + s] = (Aqk P)[t][s]
+                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)(D + t) * R + D);
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = cc * 8 + e * 2;
-                        const float a = __uint_as_float(s < 32 ? v[s] : v2[s - 32]);
-                        const float b = __uint_as_float(s + 1 < 32 ? v[s + 1] : v2[s + 1 - 32]);
-                        pk[e] = pack_bf16(a, b);
-                    }
-                    if (half == 0)
-                        *reinterpret_cast<uint4 *>(sZ2 + t * 128 + ((cc ^ (t & 7)) << 4)) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    else
-                        reinterpret_cast<uint4 *>(Eout + (long)(D + t) * R + D)[cc] =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
+                for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8u(v + 8 * cc);
             }
         }
     }
@@ -465,54 +457,55 @@ __global__ void __launch_bounds__(128) prep_kernel(const __grid_constant__ CUten
     if (ok && !mbar_wait(&bar_mma, 0, kWaitNs)) s_fail = 1;
     tc_fence_after();
 
-    // ---- epilogue 3: the state columns of E
+    // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
     {
+        constexpr int HALF = D / 2;
         const float gamma_c = meg[63];
-        const bool has_row = (D == 128) || (lane < 16);
-        const int i = (D == 128) ? tid : 16 * warp + lane;
-        for (int c0 = 0; c0 < D; c0 += 32) {   // E[i][j] = gamma_C delta_ij - (K~^T W)[i][j]
+        const bool has_row = (D == 128) || has64;
+        const int i = (D == 128) ? i128 : i64;
+#pragma unroll
+        for (int c0 = 0; c0 < HALF; c0 += 32) {   // E[i][j] = gamma_C delta_ij - (K~^T W)[i][j]
             uint32_t v[32];
-            tmem_ld32(tm + tq + c0, v);
+            const int col = hh * HALF + c0;
+            tmem_ld32(tm + tq + col, v);
             tmem_ld_wait();
             if (has_row) {
-                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)i * R + c0);
+                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)i * R + col);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t pk[4];
+                    float f[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = cc * 8 + e * 2;
-                        const float a = (c0 + j == i ? gamma_c : 0.f) - __uint_as_float(v[j]);
-                        const float b = (c0 + j + 1 == i ? gamma_c : 0.f) - __uint_as_float(v[j + 1]);
-                        pk[e] = pack_bf16(a, b);
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = col + cc * 8 + e;
+                        f[e] = (j == i ? gamma_c : 0.f) - __uint_as_float(v[cc * 8 + e]);
                     }
-                    dst[cc] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[cc] = pack8(f);
                 }
             }
         }
-        const int t = 16 * warp + lane;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j]
-        const float qs = (lane < 16) ? meg[t] * mqn[t] : 0.f;
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        const int t = i64;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j]
+        const float qs = has64 ? meg[t] * mqn[t] : 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < HALF; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tm + tq + 128 + c0, v);
+            const int col = hh * HALF + c0;
+            tmem_ld32(tm + tq + 128 + col, v);
             tmem_ld_wait();
-            if (lane < 16) {
-                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)(D + t) * R + c0);
+            if (has64) {
+                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)(D + t) * R + col);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    const int j0 = c0 + cc * 8;   // 8 consecutive head-dim indices: one chunk of q
+                    const int j0 = col + cc * 8;   // 8 consecutive head-dim indices: one chunk of q
                     const uint4 qw = *reinterpret_cast<const uint4 *>(
                         sKQ + (j0 >> 6) * 16384 + 8192 + t * 128 + ((((j0 & 63) >> 3) ^ (t & 7)) << 4));
                     const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
-                    uint32_t pk[4];
+                    float f[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int j = cc * 8 + e * 2;
-                        const float a = qs * bf16lo(qv[e]) - __uint_as_float(v[j]);
-                        const float b = qs * bf16hi(qv[e]) - __uint_as_float(v[j + 1]);
-                        pk[e] = pack_bf16(a, b);
+                        f[2 * e] = qs * bf16lo(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e]);
+                        f[2 * e + 1] = qs * bf16hi(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e + 1]);
                     }
-                    dst[cc] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[cc] = pack8(f);
                 }
             }
         }
@@ -876,7 +869,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     cudaError_t e = cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PrepSmem<D>::BYTES);
     if (e != cudaSuccess) return e;
-    prep_kernel<D><<<(unsigned)(chunks_bound * a.H), 128, PrepSmem<D>::BYTES, st>>>(mq, mk, p);
+    prep_kernel<D><<<(unsigned)(chunks_bound * a.H), kPrepThreads, PrepSmem<D>::BYTES, st>>>(mq, mk, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     using Cf = ChainCfg<D>;
