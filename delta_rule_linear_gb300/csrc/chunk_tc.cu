@@ -176,6 +176,7 @@ struct PrepSmem {
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_constant__ CUtensorMap map_q,
                                                                const __grid_constant__ CUtensorMap map_k,
+                                                               const __grid_constant__ CUtensorMap map_E,
                                                                TcParams p) {
     using Ly = PrepSmem<D>;
     constexpr int NB = D / 64;
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
     seq_info(p, n, start, len);
     const long row0 = start + (long)c * kC;
     const int nv = min(kC, len - c * kC);
-    __nv_bfloat16 *Eout = p.E + ((long)(chunk_base_of(p, n) + c) * p.H + h) * (long)(R * R);
+    const long slot = (long)(chunk_base_of(p, n) + c) * p.H + h;   // E_c slot of this chunk
 
     uint8_t *sKQ = sm + Ly::KQ;
     float *sL = reinterpret_cast<float *>(sm + Ly::R1);
@@ -221,6 +222,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
     uint8_t *sBf = sm + Ly::R2;
     uint8_t *sB = sm + Ly::R2 + 16384;
     uint8_t *sA = sm + Ly::R3;
+    // E_c staging (K-major SW128, NB + 1 blocks of R rows): reuses R1..R3 once they are dead
+    // (the V-column block NB after MMA2, the state-column blocks after MMA3)
+    uint8_t *sEst = sm + Ly::R1;
+    static_assert(Ly::R1 + (NB + 1) * (R * 128) <= Ly::MISC, "E_c staging overlaps the scalars");
     float *mbeta = reinterpret_cast<float *>(sm + Ly::MISC);
     float *mdec = mbeta + 64, *mG = mdec + 64, *mGp = mG + 64, *mkn = mGp + 64, *mqn = mkn + 64;
     float *mf = mqn + 64, *meg = mf + 64, *mcw = meg + 64;
@@ -413,10 +418,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc)
                     *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((cc ^ (i & 7)) << 4)) = pack8u(v + 8 * cc);
-            } else {         // E[i][D + s] = (K~^T P)[i][s]
-                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)i * R + D);
+            } else {         // E[i][D + s] = (K~^T P)[i][s] -> staging block NB
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8u(v + 8 * cc);
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(sEst + NB * (R * 128) + i * 128 + ((cc ^ (i & 7)) << 4)) =
+                        pack8u(v + 8 * cc);
             }
         }
         tmem_ld32(tm + tq + 128 + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(v));
@@ -428,10 +434,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc)
                     *reinterpret_cast<uint4 *>(sZ2 + t * 128 + ((cc ^ (t & 7)) << 4)) = pack8u(v + 8 * cc);
-            } else {         // E[D + t][D + s] = (Aqk P)[t][s]
-                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)(D + t) * R + D);
+            } else {         // E[D + t][D + s] = (Aqk P)[t][s] -> staging block NB
+                const int rr = D + t;
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8u(v + 8 * cc);
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(sEst + NB * (R * 128) + rr * 128 + ((cc ^ (rr & 7)) << 4)) =
+                        pack8u(v + 8 * cc);
             }
         }
     }
@@ -440,8 +448,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
     __syncthreads();
     ok = s_fail == 0;
 
-    // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64)
+    // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64);
+    // meanwhile the V-column block of E_c goes out by TMA
     if (tid == 0 && ok) {
+        tma_store_3d(&map_E, sEst + NB * (R * 128), NB * 64, 0, (int)slot);
+        bulk_commit();
         tc_fence_after();
         const uint32_t ida = idesc_bf16_f32(D, D, false, true);
         const uint32_t idb = idesc_bf16_f32(64, D, false, true);
@@ -470,7 +481,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
             tmem_ld32(tm + tq + col, v);
             tmem_ld_wait();
             if (has_row) {
-                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)i * R + col);
+                uint8_t *dst = sEst + (col >> 6) * (R * 128) + i * 128;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     float f[8];
@@ -479,7 +490,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
                         const int j = col + cc * 8 + e;
                         f[e] = (j == i ? gamma_c : 0.f) - __uint_as_float(v[cc * 8 + e]);
                     }
-                    dst[cc] = pack8(f);
+                    const int chunk = ((col & 63) >> 3) + cc;
+                    *reinterpret_cast<uint4 *>(dst + ((chunk ^ (i & 7)) << 4)) = pack8(f);
                 }
             }
         }
@@ -492,7 +504,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
             tmem_ld32(tm + tq + 128 + col, v);
             tmem_ld_wait();
             if (has64) {
-                uint4 *dst = reinterpret_cast<uint4 *>(Eout + (long)(D + t) * R + col);
+                const int rr = D + t;
+                uint8_t *dst = sEst + (col >> 6) * (R * 128) + rr * 128;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int j0 = col + cc * 8;   // 8 consecutive head-dim indices: one chunk of q
@@ -505,15 +518,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
                         f[2 * e] = qs * bf16lo(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e]);
                         f[2 * e + 1] = qs * bf16hi(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e + 1]);
                     }
-                    dst[cc] = pack8(f);
+                    const int chunk = ((col & 63) >> 3) + cc;
+                    *reinterpret_cast<uint4 *>(dst + ((chunk ^ (rr & 7)) << 4)) = pack8(f);
                 }
             }
         }
     }
-    if (tid == 0 && s_fail) record_error(p.ws, 1);
+    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (tid == 0) {
+        if (s_fail) record_error(p.ws, 1);
+        for (int kb = 0; kb < NB; ++kb)   // the state-column blocks of E_c
+            tma_store_3d(&map_E, sEst + kb * (R * 128), kb * 64, 0, (int)slot);
+        bulk_commit();
+        bulk_wait_read0();   // shared memory must stay valid until the stores have read it
+    }
+    if (warp == 0) {
+        __syncwarp();
+        tmem_dealloc(tm, 256);
+    }
 }
 
 // ---------------------------------------------------------------------------------
@@ -869,7 +893,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     cudaError_t e = cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PrepSmem<D>::BYTES);
     if (e != cudaSuccess) return e;
-    prep_kernel<D><<<(unsigned)(chunks_bound * a.H), kPrepThreads, PrepSmem<D>::BYTES, st>>>(mq, mk, p);
+    prep_kernel<D><<<(unsigned)(chunks_bound * a.H), kPrepThreads, PrepSmem<D>::BYTES, st>>>(mq, mk, me, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     using Cf = ChainCfg<D>;
