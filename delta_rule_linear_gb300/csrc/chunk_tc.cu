@@ -98,45 +98,74 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
     constexpr int P = 65;
     const int warp = tid >> 5, lane = tid & 31;
     if (warp < 4 && lane < 16) {
+        // diagonal block `warp`, column j = lane: x_r = delta_rj - sum_{s<r} L[r][s] x_s
         const int b0 = 16 * warp, j = lane;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            float acc = (r == j) ? 1.f : 0.f;
             const float *Lr = sL + (b0 + r) * P + b0;
+            float l[16];
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc = fmaf(-Lr[s], x[s], acc);   // x[s] = 0 for s < j
-            x[r] = acc;
+            for (int s = 0; s < r; ++s) l[s] = Lr[s];   // independent loads, issued together
+            float a0 = (r == j) ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+            for (int s = 0; s < r; ++s) {               // x_s = 0 for s < j
+                if (s & 1) a1 = fmaf(-l[s], x[s], a1);
+                else a0 = fmaf(-l[s], x[s], a0);
+            }
+            x[r] = a0 + a1;
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
-    }
-    for (int idx = tid; idx < 64 * 64; idx += NT) {
-        const int r = idx >> 6, c = idx & 63;
-        if ((c >> 4) > (r >> 4)) sT[r * P + c] = 0.f;
+    } else {
+        // the other NT - 64 threads zero the six strictly-upper 16 x 16 blocks of T
+        const int zt = warp < 4 ? warp * 16 + (lane - 16) : 64 + (warp - 4) * 32 + lane;
+        for (int idx = zt; idx < 6 * 256; idx += NT - 64) {
+            const int blk = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
+            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);          // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            sT[(16 * bi + r) * P + 16 * bj + c] = 0.f;
+        }
     }
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
         const int nblk = 4 - d;
+        // X_ij = sum_{k=j}^{i-1} L_ik T_kj, kept in the (unused) upper block (j, i) of L
         for (int e = tid; e < nblk * 256; e += NT) {
-            const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int j = b, i = b + d;
-            float x = 0.f;
-            for (int k = j; k < i; ++k)
+            const int bb = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int j = bb, i = bb + d;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = j; k < i; ++k) {
+                float l[16], t[16];
+                const float *Lr = sL + (16 * i + r) * P + 16 * k;
+                const float *Tc = sT + (16 * k) * P + 16 * j + cc;
 #pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    x = fmaf(sL[(16 * i + r) * P + 16 * k + m], sT[(16 * k + m) * P + 16 * j + cc], x);
-            sL[(16 * j + r) * P + 16 * i + cc] = x;
+                for (int m = 0; m < 16; ++m) {
+                    l[m] = Lr[m];
+                    t[m] = Tc[m * P];
+                }
+#pragma unroll
+                for (int m = 0; m < 16; ++m) acc[m & 3] = fmaf(l[m], t[m], acc[m & 3]);
+            }
+            sL[(16 * j + r) * P + 16 * i + cc] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
         __syncthreads();
+        // T_ij = -T_ii X_ij
         for (int e = tid; e < nblk * 256; e += NT) {
-            const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int j = b, i = b + d;
-            float x = 0.f;
+            const int bb = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int j = bb, i = bb + d;
+            float l[16], t[16];
+            const float *Tr = sT + (16 * i + r) * P + 16 * i;
+            const float *Xc = sL + (16 * j) * P + 16 * i + cc;
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                x = fmaf(sT[(16 * i + r) * P + 16 * i + m], sL[(16 * j + m) * P + 16 * i + cc], x);
-            sT[(16 * i + r) * P + 16 * j + cc] = -x;
+            for (int m = 0; m < 16; ++m) {
+                l[m] = Tr[m];
+                t[m] = Xc[m * P];
+            }
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc[m & 3] = fmaf(l[m], t[m], acc[m & 3]);
+            sT[(16 * i + r) * P + 16 * j + cc] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
         }
         __syncthreads();
     }
@@ -332,23 +361,39 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
         }
         float *Lrow = sL + t * 65 + 32 * hh;
         const float bk = bt * kt;
+        float kn_s[32], g_s[32];   // this half's per-token scalars, by 16-byte loads
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float4 a = reinterpret_cast<const float4 *>(mkn + 32 * hh)[e];
+            const float4 b = reinterpret_cast<const float4 *>(mG + 32 * hh)[e];
+            kn_s[4 * e] = a.x; kn_s[4 * e + 1] = a.y; kn_s[4 * e + 2] = a.z; kn_s[4 * e + 3] = a.w;
+            g_s[4 * e] = b.x; g_s[4 * e + 1] = b.y; g_s[4 * e + 2] = b.z; g_s[4 * e + 3] = b.w;
+        }
 #pragma unroll
         for (int s2 = 0; s2 < 32; ++s2) {
             const int s = 32 * hh + s2;
-            const float val = bk * mkn[s] * __uint_as_float(r[s2]) * __expf(gpt - mG[s]);
+            const float val = bk * kn_s[s2] * __uint_as_float(r[s2]) * __expf(gpt - g_s[s2]);
             Lrow[s2] = (s < t && t < nv) ? val : 0.f;
         }
     } else {
         const int t = i128 - 64;
         const float qt = mqn[t], gt = mG[t];
+        float kn_s[32], g_s[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float4 a = reinterpret_cast<const float4 *>(mkn + 32 * hh)[e];
+            const float4 b = reinterpret_cast<const float4 *>(mG + 32 * hh)[e];
+            kn_s[4 * e] = a.x; kn_s[4 * e + 1] = a.y; kn_s[4 * e + 2] = a.z; kn_s[4 * e + 3] = a.w;
+            g_s[4 * e] = b.x; g_s[4 * e + 1] = b.y; g_s[4 * e + 2] = b.z; g_s[4 * e + 3] = b.w;
+        }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
             float f[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int s = 32 * hh + cc * 8 + e;
-                const float val = qt * mkn[s] * __uint_as_float(r[cc * 8 + e]) *
-                                  __expf(gt - mG[s]);
+                const float val = qt * kn_s[cc * 8 + e] * __uint_as_float(r[cc * 8 + e]) *
+                                  __expf(gt - g_s[cc * 8 + e]);
                 f[e] = (s <= t && t < nv) ? val : 0.f;
             }
             const int chunk = 4 * hh + cc;
@@ -369,14 +414,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
         const float *w = half ? mbeta : mcw;
         uint8_t *dB = sB + half * 8192 + t * 128;
         uint8_t *dBf = sBf + half * 8192 + t * 128;
+        float tv[32], wv[32];   // this thread's 32 columns, loaded before use
+#pragma unroll
+        for (int e = 0; e < 32; ++e) tv[e] = Trow[grp * 32 + e];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float4 a = reinterpret_cast<const float4 *>(w + grp * 32)[e];
+            wv[4 * e] = a.x; wv[4 * e + 1] = a.y; wv[4 * e + 2] = a.z; wv[4 * e + 3] = a.w;
+        }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
             const int chunk = grp * 4 + cc;
             float f[8], fb[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const int s = chunk * 8 + e;
-                f[e] = Trow[s] * w[s];
+                f[e] = tv[cc * 8 + e] * wv[cc * 8 + e];
                 fb[e] = f[e] * ft;
             }
             const int off = (chunk ^ (t & 7)) << 4;
