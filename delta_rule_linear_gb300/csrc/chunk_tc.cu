@@ -88,14 +88,19 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 
 // ---------------------------------------------------------------------------------
 // T = (I + L)^{-1} for a 64 x 64 strictly-lower L, fp32 in shared memory (row pitch
-// 65), by NT threads: the four 16 x 16 diagonal blocks by forward substitution (one
-// lane per column, the column kept in registers), then the off-diagonal blocks by
-// distance from the diagonal,  T_ij = -T_ii sum_{k=j}^{i-1} L_ik T_kj.
-// The unused upper blocks of L hold the partial sums X_ij.
+// kLP = 68 floats: 16-byte aligned rows), by NT = 256 threads: the four 16 x 16 diagonal
+// blocks by forward substitution (one lane per column, the column kept in registers),
+// then the off-diagonal blocks by distance from the diagonal,
+//   T_ij = -T_ii X_ij,  X_ij = sum_{k=j}^{i-1} L_ik T_kj,
+// each thread computing 8 consecutive outputs of one row with 16-byte loads.  The unused
+// upper blocks of L hold the partial sums X_ij.
 // ---------------------------------------------------------------------------------
+constexpr int kLP = 68;
+
 template <int NT>
 __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
-    constexpr int P = 65;
+    static_assert(NT == 256, "the work split below assumes 256 threads");
+    constexpr int P = kLP;
     const int warp = tid >> 5, lane = tid & 31;
     if (warp < 4 && lane < 16) {
         // diagonal block `warp`, column j = lane: x_r = delta_rj - sum_{s<r} L[r][s] x_s
@@ -118,7 +123,7 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
     } else {
-        // the other NT - 64 threads zero the six strictly-upper 16 x 16 blocks of T
+        // the other 192 threads zero the six strictly-upper 16 x 16 blocks of T
         const int zt = warp < 4 ? warp * 16 + (lane - 16) : 64 + (warp - 4) * 32 + lane;
         for (int idx = zt; idx < 6 * 256; idx += NT - 64) {
             const int blk = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
@@ -129,43 +134,57 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
     }
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
-        const int nblk = 4 - d;
-        // X_ij = sum_{k=j}^{i-1} L_ik T_kj, kept in the (unused) upper block (j, i) of L
-        for (int e = tid; e < nblk * 256; e += NT) {
-            const int bb = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int j = bb, i = bb + d;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int items = (4 - d) * 32;        // (block, row, 8-column group)
+        const int bb = tid >> 5, r = (tid >> 1) & 15, c0 = (tid & 1) * 8;
+        const int j = bb, i = bb + d;
+        if (tid < items) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             for (int k = j; k < i; ++k) {
-                float l[16], t[16];
                 const float *Lr = sL + (16 * i + r) * P + 16 * k;
-                const float *Tc = sT + (16 * k) * P + 16 * j + cc;
+                float l[16];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    l[m] = Lr[m];
-                    t[m] = Tc[m * P];
+                for (int m4 = 0; m4 < 4; ++m4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(Lr + 4 * m4);
+                    l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
                 }
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc[m & 3] = fmaf(l[m], t[m], acc[m & 3]);
+                for (int m = 0; m < 16; ++m) {
+                    const float *Tr = sT + (16 * k + m) * P + 16 * j + c0;
+                    const float4 t0 = *reinterpret_cast<const float4 *>(Tr);
+                    const float4 t1 = *reinterpret_cast<const float4 *>(Tr + 4);
+                    acc[0] = fmaf(l[m], t0.x, acc[0]); acc[1] = fmaf(l[m], t0.y, acc[1]);
+                    acc[2] = fmaf(l[m], t0.z, acc[2]); acc[3] = fmaf(l[m], t0.w, acc[3]);
+                    acc[4] = fmaf(l[m], t1.x, acc[4]); acc[5] = fmaf(l[m], t1.y, acc[5]);
+                    acc[6] = fmaf(l[m], t1.z, acc[6]); acc[7] = fmaf(l[m], t1.w, acc[7]);
+                }
             }
-            sL[(16 * j + r) * P + 16 * i + cc] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            float *X = sL + (16 * j + r) * P + 16 * i + c0;   // upper block (j, i)
+            *reinterpret_cast<float4 *>(X) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4 *>(X + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
         __syncthreads();
-        // T_ij = -T_ii X_ij
-        for (int e = tid; e < nblk * 256; e += NT) {
-            const int bb = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int j = bb, i = bb + d;
-            float l[16], t[16];
+        if (tid < items) {
             const float *Tr = sT + (16 * i + r) * P + 16 * i;
-            const float *Xc = sL + (16 * j) * P + 16 * i + cc;
+            float l[16];
+#pragma unroll
+            for (int m4 = 0; m4 < 4; ++m4) {
+                const float4 v = *reinterpret_cast<const float4 *>(Tr + 4 * m4);
+                l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
+            }
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
-                l[m] = Tr[m];
-                t[m] = Xc[m * P];
+                const float *Xr = sL + (16 * j + m) * P + 16 * i + c0;
+                const float4 x0 = *reinterpret_cast<const float4 *>(Xr);
+                const float4 x1 = *reinterpret_cast<const float4 *>(Xr + 4);
+                acc[0] = fmaf(l[m], x0.x, acc[0]); acc[1] = fmaf(l[m], x0.y, acc[1]);
+                acc[2] = fmaf(l[m], x0.z, acc[2]); acc[3] = fmaf(l[m], x0.w, acc[3]);
+                acc[4] = fmaf(l[m], x1.x, acc[4]); acc[5] = fmaf(l[m], x1.y, acc[5]);
+                acc[6] = fmaf(l[m], x1.z, acc[6]); acc[7] = fmaf(l[m], x1.w, acc[7]);
             }
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int m = 0; m < 16; ++m) acc[m & 3] = fmaf(l[m], t[m], acc[m & 3]);
-            sT[(16 * i + r) * P + 16 * j + cc] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
+            float *Tij = sT + (16 * i + r) * P + 16 * j + c0;
+            *reinterpret_cast<float4 *>(Tij) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+            *reinterpret_cast<float4 *>(Tij + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
         }
         __syncthreads();
     }
@@ -195,8 +214,8 @@ template <int D>
 struct PrepSmem {
     static constexpr int NB = D / 64;
     static constexpr int KQ = 0;                      // [K;Q] tile, K-major SW128: NB x 16 KB
-    static constexpr int R1 = KQ + NB * 16384;        // L, T fp32 [64][65]; later Z1, Z2
-    static constexpr int R2 = R1 + 33792;             // Bf, B: MN-major [64 t][128], 16 KB each
+    static constexpr int R1 = KQ + NB * 16384;        // L, T fp32 [64][kLP]; later Z1, Z2
+    static constexpr int R2 = R1 + 35840;             // Bf, B: MN-major [64 t][128], 16 KB each
     static constexpr int R3 = R2 + 32768;             // Aqk: K-major [64 t][64 s], 8 KB
     static constexpr int MISC = R3 + 8192;            // per-token scalars
     static constexpr int BYTES = MISC + 10 * 64 * 4 + 1024;
@@ -245,7 +264,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
 
     uint8_t *sKQ = sm + Ly::KQ;
     float *sL = reinterpret_cast<float *>(sm + Ly::R1);
-    float *sT = sL + 64 * 65;
+    float *sT = sL + 64 * kLP;
     uint8_t *sZ1 = sm + Ly::R1;
     uint8_t *sZ2 = sm + Ly::R1 + D * 128;
     uint8_t *sBf = sm + Ly::R2;
@@ -359,7 +378,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
             mf[t] = t < nv ? __expf(gC - mG[t]) * kt : 0.f;
             mcw[t] = bt * __expf(gpt) * kt;   // column weight of T' = T diag(beta e^{G_{s-1}} kn)
         }
-        float *Lrow = sL + t * 65 + 32 * hh;
+        float *Lrow = sL + t * kLP + 32 * hh;
         const float bk = bt * kt;
         float kn_s[32], g_s[32];   // this half's per-token scalars, by 16-byte loads
 #pragma unroll
@@ -369,12 +388,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
             kn_s[4 * e] = a.x; kn_s[4 * e + 1] = a.y; kn_s[4 * e + 2] = a.z; kn_s[4 * e + 3] = a.w;
             g_s[4 * e] = b.x; g_s[4 * e + 1] = b.y; g_s[4 * e + 2] = b.z; g_s[4 * e + 3] = b.w;
         }
+        float lv[32];
 #pragma unroll
         for (int s2 = 0; s2 < 32; ++s2) {
             const int s = 32 * hh + s2;
             const float val = bk * kn_s[s2] * __uint_as_float(r[s2]) * __expf(gpt - g_s[s2]);
-            Lrow[s2] = (s < t && t < nv) ? val : 0.f;
+            lv[s2] = (s < t && t < nv) ? val : 0.f;
         }
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            reinterpret_cast<float4 *>(Lrow)[e] = make_float4(lv[4 * e], lv[4 * e + 1], lv[4 * e + 2], lv[4 * e + 3]);
     } else {
         const int t = i128 - 64;
         const float qt = mqn[t], gt = mG[t];
@@ -409,14 +432,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
     // ---- B = [T' | P], Bf = diag(f) B   (MN-major: row t, columns s); 4 threads per row
     {
         const int t = tid >> 2, half = (tid >> 1) & 1, grp = tid & 1;
-        const float *Trow = sT + t * 65;
+        const float *Trow = sT + t * kLP;
         const float ft = mf[t];
         const float *w = half ? mbeta : mcw;
         uint8_t *dB = sB + half * 8192 + t * 128;
         uint8_t *dBf = sBf + half * 8192 + t * 128;
         float tv[32], wv[32];   // this thread's 32 columns, loaded before use
 #pragma unroll
-        for (int e = 0; e < 32; ++e) tv[e] = Trow[grp * 32 + e];
+        for (int e = 0; e < 8; ++e) {
+            const float4 a = reinterpret_cast<const float4 *>(Trow + grp * 32)[e];
+            tv[4 * e] = a.x; tv[4 * e + 1] = a.y; tv[4 * e + 2] = a.z; tv[4 * e + 3] = a.w;
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float4 a = reinterpret_cast<const float4 *>(w + grp * 32)[e];
