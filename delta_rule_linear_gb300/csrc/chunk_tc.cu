@@ -16,19 +16,32 @@
 //   [   O    ] = [ diag(exp G) Q~ - Aqk W  Aqk P   ] [ V ]      =:  E_c [S; V]
 //
 // (S_next = exp(G_C) S + K~^T U and O = diag(exp G) Q~ S + Aqk U with U = P V - W S.)
-// E_c does not depend on the state, so it is built for every chunk in parallel:
+// E_c does not depend on the state, so it is built for every chunk in parallel (the
+// "prep" role), and a walk over the chunks applies it (the "chain" role):
 //
-//  * prep_kernel  -- one CTA per (sequence, head, chunk): TMA loads q, k; tcgen05
-//    products [K;Q] K^T, K^T diag(f) [T'|P], Aqk [T'|P], Z k; a blocked fp32
-//    forward-substitution inverse on CUDA cores; writes E_c (bf16) to scratch.
-//  * chain_kernel -- one CTA per (sequence, head): walks the chunks in order; per
-//    chunk one product D^T = [S^T | V^T] E_c^T (M = dv) gives the next state (fp32 in
-//    TMEM, stored back as the bf16 operand) and the outputs.  Producer lanes stream
-//    E_c and V_c by TMA; an MMA warp issues; four warps turn the next state into the
-//    next operand, four others store o.
+//  * prep -- a group of 256 threads builds E_c for one (sequence, head, chunk) at a
+//    time and moves on to the next: TMA loads q, k; tcgen05 products [K;Q] K^T,
+//    K^T diag(f) [T'|P], Aqk [T'|P], Z k; a blocked fp32 forward-substitution inverse
+//    on CUDA cores; E_c (bf16) goes to scratch by TMA stores.  The next chunk's q, k
+//    load is issued as soon as the current chunk has finished reading them.  Two
+//    groups share one CTA (and its 512 TMEM columns).
+//  * chain -- one CTA per (sequence, head) walks the chunks in order; per chunk one
+//    product D^T = [S^T | V^T] E_c^T (M = dv) gives the next state (fp32 in TMEM,
+//    stored back as the bf16 operand) and the outputs.  Producer lanes stream E_c and
+//    V_c by TMA; an MMA warp issues; eight warps turn the next state into the next
+//    operand, four others store o.
 //
-// Every wait on an mbarrier is bounded; on time-out the kernel records
+// When the (sequence, head) pairs fill at most half of the SMs, both roles run in one
+// cooperative launch: the first CTAs are chains, the rest prep groups that produce the
+// chunks in chunk-major order and publish each E_c with a release flag, which the
+// chain polls (acquire) before its TMA load.  The chains then run alongside the prep
+// work instead of after it.  Otherwise prep runs as its own persistent launch,
+// followed by the chain launch.
+//
+// Every wait (mbarrier or flag) is bounded; on time-out the kernel records
 // KDA_ERR_DEVICE_TIMEOUT in the workspace header and unwinds (no trap).
+#include <algorithm>
+
 #include "kda_internal.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.cuh"
@@ -54,7 +67,13 @@ struct TcParams {
     float *hT;                 // [nseq, H, D, D] or nullptr
     __nv_bfloat16 *o;          // [rows, H, D]
     __nv_bfloat16 *E;          // scratch: [slots][D + 64][D + 64]
+    uint32_t *flags;           // scratch: [slots], E_c published (single-launch mode) or nullptr
     WsHeader *ws;
+    long nsh;                  // (sequence, head) pairs
+    long n_items;              // prep work items (valid or not)
+    int maxnc;                 // chunk-major items: chunks of the longest sequence
+    int chunk_major;           // items ordered (chunk, sequence, head) instead of by slot
+    int nchain;                // CTAs with the chain role (the first ones)
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -78,6 +97,49 @@ __device__ __forceinline__ int chunk_base_of(const TcParams &p, int n) {
     return p.cu_seqlens ? p.chunk_base[n] : n * p.nc_equal;
 }
 
+// One prep work item: chunk c of sequence n, head h.
+struct ChunkItem {
+    long row0, slot;   // first token row; E_c slot (= flag index)
+    int h, nv;         // head; valid tokens in the chunk (1..64)
+};
+
+// Work item `item` -> chunk.  Chunk-major order (chunk, then (sequence, head)) lets the
+// chains of the single-launch mode start as soon as the first chunks are built; slot
+// order is compact for varlen batches.  Returns false for an item past a sequence's end.
+__device__ __forceinline__ bool item_info(const TcParams &p, long item, ChunkItem &it) {
+    int n, c;
+    if (p.chunk_major) {
+        const long j = item % p.nsh;
+        c = (int)(item / p.nsh);
+        n = (int)(j / p.H);
+        it.h = (int)(j % p.H);
+    } else {
+        const long g = item / p.H;
+        it.h = (int)(item % p.H);
+        if (p.cu_seqlens) {
+            if (g >= p.chunk_base[p.nseq]) return false;
+            int lo = 0, hi = p.nseq;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (p.chunk_base[mid] <= g) lo = mid; else hi = mid;
+            }
+            n = lo;
+            c = (int)(g - p.chunk_base[n]);
+        } else {
+            n = (int)(g / p.nc_equal);
+            c = (int)(g % p.nc_equal);
+        }
+    }
+    long start;
+    int len;
+    seq_info(p, n, start, len);
+    if ((long)c * kC >= len) return false;
+    it.row0 = start + (long)c * kC;
+    it.nv = min(kC, len - c * kC);
+    it.slot = (long)(chunk_base_of(p, n) + c) * p.H + it.h;
+    return true;
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -88,9 +150,10 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 
 // ---------------------------------------------------------------------------------
 // T = (I + L)^{-1} for a 64 x 64 strictly-lower L, fp32 in shared memory (row pitch
-// kLP = 68 floats: 16-byte aligned rows), by NT = 256 threads: the four 16 x 16 diagonal
-// blocks by forward substitution (one lane per column, the column kept in registers),
-// then the off-diagonal blocks by distance from the diagonal,
+// kLP = 68 floats: 16-byte aligned rows), by the NT = 256 threads of one group (named
+// barrier `bar`): the four 16 x 16 diagonal blocks by forward substitution (one lane
+// per column, the column kept in registers), then the off-diagonal blocks by distance
+// from the diagonal,
 //   T_ij = -T_ii X_ij,  X_ij = sum_{k=j}^{i-1} L_ik T_kj,
 // each thread computing 8 consecutive outputs of one row with 16-byte loads.  The unused
 // upper blocks of L hold the partial sums X_ij.
@@ -98,7 +161,7 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 constexpr int kLP = 68;
 
 template <int NT>
-__device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
+__device__ void invert_unit_lower_64(float *sL, float *sT, int tid, int bar) {
     static_assert(NT == 256, "the work split below assumes 256 threads");
     constexpr int P = kLP;
     const int warp = tid >> 5, lane = tid & 31;
@@ -132,7 +195,7 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
             sT[(16 * bi + r) * P + 16 * bj + c] = 0.f;
         }
     }
-    __syncthreads();
+    named_sync(bar, NT);
     for (int d = 1; d < 4; ++d) {
         const int items = (4 - d) * 32;        // (block, row, 8-column group)
         const int bb = tid >> 5, r = (tid >> 1) & 15, c0 = (tid & 1) * 8;
@@ -162,7 +225,7 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
             *reinterpret_cast<float4 *>(X) = make_float4(acc[0], acc[1], acc[2], acc[3]);
             *reinterpret_cast<float4 *>(X + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
-        __syncthreads();
+        named_sync(bar, NT);
         if (tid < items) {
             const float *Tr = sT + (16 * i + r) * P + 16 * i;
             float l[16];
@@ -186,7 +249,7 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid) {
             *reinterpret_cast<float4 *>(Tij) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
             *reinterpret_cast<float4 *>(Tij + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
         }
-        __syncthreads();
+        named_sync(bar, NT);
     }
 }
 
@@ -203,12 +266,13 @@ __device__ __forceinline__ uint4 pack8u(const uint32_t *u) {
 }
 
 // ---------------------------------------------------------------------------------
-// prep_kernel -- builds E_c for one (sequence, head, chunk).  256 threads: the two
-// warps w and w + 4 share TMEM lane quadrant w % 4 and split each result row's
-// columns between them.  Rows of an M = 128 result: 32 q + lane; of an M = 64
-// result: 16 q + lane for lane < 16.
+// prep -- one group of 256 threads builds E_c chunk after chunk.  The two warps w and
+// w + 4 of a group share TMEM lane quadrant w % 4 and split each result row's columns
+// between them.  Rows of an M = 128 result: 32 q + lane; of an M = 64 result:
+// 16 q + lane for lane < 16.
 // ---------------------------------------------------------------------------------
-constexpr int kPrepThreads = 256;
+constexpr int kGroupThreads = 256;
+constexpr int kTcThreads = 512;               // prep: two groups; chain: 14 warps used
 
 template <int D>
 struct PrepSmem {
@@ -217,50 +281,50 @@ struct PrepSmem {
     static constexpr int R1 = KQ + NB * 16384;        // L, T fp32 [64][kLP]; later Z1, Z2
     static constexpr int R2 = R1 + 35840;             // Bf, B: MN-major [64 t][128], 16 KB each
     static constexpr int R3 = R2 + 32768;             // Aqk: K-major [64 t][64 s], 8 KB
-    static constexpr int MISC = R3 + 8192;            // per-token scalars
-    static constexpr int BYTES = MISC + 10 * 64 * 4 + 1024;
+    static constexpr int MISC = R3 + 8192;            // per-token scalars, 9 x 64 floats
+    static constexpr int CTRL = MISC + 9 * 64 * 4;    // the group's mbarriers and status
+    static constexpr int GROUP = ((CTRL + 64 + 1023) / 1024) * 1024;   // one group's share
 };
 
+struct PrepCtrl {
+    uint64_t bar_tma, bar_mma;
+    int fail;
+};
+
+// q, k tiles of one chunk into the [K;Q] region (k rows 0-63, q rows 64-127 of each
+// 64-column block)
+template <int NB>
+__device__ __forceinline__ void load_kq(const CUtensorMap *map_q, const CUtensorMap *map_k,
+                                        uint8_t *sKQ, uint64_t *bar, const ChunkItem &it) {
+    mbar_expect_tx(bar, NB * 2 * 64 * 128);
+    for (int kb = 0; kb < NB; ++kb) {
+        tma_load_3d(sKQ + kb * 16384, map_k, bar, kb * 64, it.h, (int)it.row0);
+        tma_load_3d(sKQ + kb * 16384 + 8192, map_q, bar, kb * 64, it.h, (int)it.row0);
+    }
+}
+
+// E_c of `slot` is in global memory: wait for the bulk stores, then release the flag
+__device__ __forceinline__ void publish_slot(const TcParams &p, long slot) {
+    bulk_wait0();
+    fence_proxy_async_global();
+    st_release_gpu(p.flags + slot, 1u);
+}
+
 template <int D>
-__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_constant__ CUtensorMap map_q,
-                                                               const __grid_constant__ CUtensorMap map_k,
-                                                               const __grid_constant__ CUtensorMap map_E,
-                                                               TcParams p) {
+__device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUtensorMap *map_k,
+                                           const CUtensorMap *map_E, const TcParams &p,
+                                           uint8_t *sm, uint32_t tm, int tid, int bar, long item,
+                                           long stride) {
     using Ly = PrepSmem<D>;
     constexpr int NB = D / 64;
     constexpr int R = D + 64;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = align1024(smem_raw);
-    __shared__ uint64_t bar_tma, bar_mma;
-    __shared__ uint32_t tmem_slot;
-    __shared__ int s_fail;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(sm + Ly::CTRL);
+    const int warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hh = warp >> 2;
     const int i128 = 32 * q4 + lane;
     const int i64 = 16 * q4 + lane;
     const bool has64 = lane < 16;
-
-    const int g = blockIdx.x / p.H, h = blockIdx.x % p.H;
-    int n, c;
-    if (p.cu_seqlens) {
-        if (g >= p.chunk_base[p.nseq]) return;
-        int lo = 0, hi = p.nseq;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (p.chunk_base[mid] <= g) lo = mid; else hi = mid;
-        }
-        n = lo;
-        c = g - p.chunk_base[n];
-    } else {
-        n = g / p.nc_equal;
-        c = g % p.nc_equal;
-    }
-    long start;
-    int len;
-    seq_info(p, n, start, len);
-    const long row0 = start + (long)c * kC;
-    const int nv = min(kC, len - c * kC);
-    const long slot = (long)(chunk_base_of(p, n) + c) * p.H + h;   // E_c slot of this chunk
+    const uint32_t tq = (uint32_t)(32 * q4) << 16;   // this warp's TMEM lane quadrant
 
     uint8_t *sKQ = sm + Ly::KQ;
     float *sL = reinterpret_cast<float *>(sm + Ly::R1);
@@ -278,348 +342,362 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
     float *mdec = mbeta + 64, *mG = mdec + 64, *mGp = mG + 64, *mkn = mGp + 64, *mqn = mkn + 64;
     float *mf = mqn + 64, *meg = mf + 64, *mcw = meg + 64;
 
-    if (tid == 0) {
-        mbar_init(&bar_tma, 1);
-        mbar_init(&bar_mma, 1);
-        fence_mbar_init();
-        s_fail = 0;
-    }
-    if (warp == 0) {
-        tmem_alloc(&tmem_slot, 256);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tm = tmem_slot;
-    const uint32_t tq = (uint32_t)(32 * q4) << 16;   // this warp's TMEM lane quadrant
-
-    if (tid == 0) {
-        mbar_expect_tx(&bar_tma, NB * 2 * 64 * 128);
-        for (int kb = 0; kb < NB; ++kb) {
-            tma_load_3d(sKQ + kb * 16384, &map_k, &bar_tma, kb * 64, h, (int)row0);
-            tma_load_3d(sKQ + kb * 16384 + 8192, &map_q, &bar_tma, kb * 64, h, (int)row0);
-        }
-    }
+    ChunkItem cur;
+    while (item < p.n_items && !item_info(p, item, cur)) item += stride;
+    if (item >= p.n_items) return;
+    if (tid == 0) load_kq<NB>(map_q, map_k, sKQ, &ctl->bar_tma, cur);
+    float nbeta = 0.f, ndec = 0.f;   // tid < 64: this chunk's beta, decay of token tid
     if (tid < 64) {
-        const long gi = (row0 + tid) * p.H + h;
-        mbeta[tid] = tid < nv ? p.beta[gi] : 0.f;
-        mdec[tid] = (tid < nv && p.decay) ? p.decay[gi] : 0.f;
+        const long gi = (cur.row0 + tid) * p.H + cur.h;
+        nbeta = tid < cur.nv ? p.beta[gi] : 0.f;
+        ndec = (tid < cur.nv && p.decay) ? p.decay[gi] : 0.f;
     }
-    __syncthreads();
-    if (warp == 0) {   // in-chunk cumulative log-decay: lane owns tokens 2 lane, 2 lane + 1
-        const float d0 = mdec[2 * lane], d1 = mdec[2 * lane + 1];
-        float incl = d0 + d1;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        const float excl = incl - (d0 + d1);
-        mGp[2 * lane] = excl;
-        mG[2 * lane] = excl + d0;
-        mGp[2 * lane + 1] = excl + d0;
-        mG[2 * lane + 1] = incl;
-    }
-    if (!mbar_wait(&bar_tma, 0, kWaitNs)) s_fail = 1;
-    __syncthreads();
-    bool ok = s_fail == 0;
+    long pend = -1;   // thread 0: slot whose stores are in flight and not yet published
 
-    // ---- MMA1: D1[0:128, 0:64] = [K; Q] K^T  (contraction over the head dim)
-    if (tid == 0 && ok) {
+    for (uint32_t it = 0;; ++it) {
+        const uint32_t ph = it & 1;   // bar_tma completes once per chunk, bar_mma three times
+        const int nv = cur.nv;
+        if (tid < 64) {
+            mbeta[tid] = nbeta;
+            mdec[tid] = ndec;
+        }
+        named_sync(bar, kGroupThreads);
+        if (warp == 0) {   // in-chunk cumulative log-decay: lane owns tokens 2 lane, 2 lane + 1
+            const float d0 = mdec[2 * lane], d1 = mdec[2 * lane + 1];
+            float incl = d0 + d1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const float excl = incl - (d0 + d1);
+            mGp[2 * lane] = excl;
+            mG[2 * lane] = excl + d0;
+            mGp[2 * lane + 1] = excl + d0;
+            mG[2 * lane + 1] = incl;
+        }
+        if (!mbar_wait(&ctl->bar_tma, ph, kWaitNs)) ctl->fail = 1;
+        named_sync(bar, kGroupThreads);
+        bool ok = ctl->fail == 0;
+
+        // ---- MMA1: D1[0:128, 0:64] = [K; Q] K^T  (contraction over the head dim)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16_f32(128, 64, false, false);
+            const uint32_t a0 = smem_u32(sKQ);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16_ss(tm, desc_kmajor_sw128(a0, 128, ks), desc_kmajor_sw128(a0, 128, ks), id,
+                            ks > 0 ? 1u : 0u);
+            mma_commit(&ctl->bar_mma);
+            if (pend >= 0) {   // the previous chunk's stores have long been under way
+                publish_slot(p, pend);
+                pend = -1;
+            }
+        }
+        if (tid >= 128 && ok) {   // query norms: two threads per row (the swizzle permutes chunks only)
+            const int t = (tid - 128) >> 1, part = tid & 1;
+            float ss = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < NB * 4; ++cc) {
+                const int chunk = part * NB * 4 + cc;
+                const uint4 w = *reinterpret_cast<const uint4 *>(sKQ + (chunk >> 3) * 16384 + 8192 +
+                                                                 t * 128 + ((chunk & 7) << 4));
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = bf16lo(ws[e]), b = bf16hi(ws[e]);
+                    ss = fmaf(a, a, fmaf(b, b, ss));
+                }
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            if (part == 0) mqn[t] = p.use_l2 ? p.scale / fmaxf(sqrtf(ss), kNormEps) : p.scale;
+        }
+        if (tid < 64) meg[tid] = __expf(mG[tid]);
+        if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
-        const uint32_t id = idesc_bf16_f32(128, 64, false, false);
-        const uint32_t a0 = smem_u32(sKQ);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16_ss(tm, desc_kmajor_sw128(a0, 128, ks), desc_kmajor_sw128(a0, 128, ks), id,
-                        ks > 0 ? 1u : 0u);
-        mma_commit(&bar_mma);
-    }
-    if (tid >= 128 && ok) {   // query norms: two threads per row (the swizzle permutes chunks only)
-        const int t = (tid - 128) >> 1, part = tid & 1;
-        float ss = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < NB * 4; ++cc) {
-            const int chunk = part * NB * 4 + cc;
-            const uint4 w = *reinterpret_cast<const uint4 *>(sKQ + (chunk >> 3) * 16384 + 8192 +
-                                                             t * 128 + ((chunk & 7) << 4));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float a = bf16lo(ws[e]), b = bf16hi(ws[e]);
-                ss = fmaf(a, a, fmaf(b, b, ss));
-            }
-        }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        if (part == 0) mqn[t] = p.use_l2 ? p.scale / fmaxf(sqrtf(ss), kNormEps) : p.scale;
-    }
-    if (tid < 64) meg[tid] = __expf(mG[tid]);
-    if (ok && !mbar_wait(&bar_mma, 0, kWaitNs)) s_fail = 1;
-    tc_fence_after();
 
-    // ---- epilogue 1: norms, L (fp32, smem) and Aqk (bf16 operand); columns 32 hh ..
-    uint32_t r[32];
-    tmem_ld32(tm + tq + 32 * hh, r);
-    tmem_ld_wait();
-    if (i128 < 64 && (i128 >> 5) == hh) {   // this half holds the Gram diagonal of row i128
-        float diag = 0.f;
-#pragma unroll
-        for (int s = 0; s < 32; ++s)
-            if (s == (i128 & 31)) diag = __uint_as_float(r[s]);
-        mkn[i128] = p.use_l2 ? 1.f / fmaxf(sqrtf(diag), kNormEps) : 1.f;
-    }
-    __syncthreads();
-    ok = s_fail == 0;
-    const float gC = mG[63];
-    if (i128 < 64) {
-        const int t = i128;
-        const float kt = mkn[t], bt = mbeta[t], gpt = mGp[t];
-        if (hh == 0) {
-            mf[t] = t < nv ? __expf(gC - mG[t]) * kt : 0.f;
-            mcw[t] = bt * __expf(gpt) * kt;   // column weight of T' = T diag(beta e^{G_{s-1}} kn)
-        }
-        float *Lrow = sL + t * kLP + 32 * hh;
-        const float bk = bt * kt;
-        float kn_s[32], g_s[32];   // this half's per-token scalars, by 16-byte loads
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 a = reinterpret_cast<const float4 *>(mkn + 32 * hh)[e];
-            const float4 b = reinterpret_cast<const float4 *>(mG + 32 * hh)[e];
-            kn_s[4 * e] = a.x; kn_s[4 * e + 1] = a.y; kn_s[4 * e + 2] = a.z; kn_s[4 * e + 3] = a.w;
-            g_s[4 * e] = b.x; g_s[4 * e + 1] = b.y; g_s[4 * e + 2] = b.z; g_s[4 * e + 3] = b.w;
-        }
-        float lv[32];
-#pragma unroll
-        for (int s2 = 0; s2 < 32; ++s2) {
-            const int s = 32 * hh + s2;
-            const float val = bk * kn_s[s2] * __uint_as_float(r[s2]) * __expf(gpt - g_s[s2]);
-            lv[s2] = (s < t && t < nv) ? val : 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            reinterpret_cast<float4 *>(Lrow)[e] = make_float4(lv[4 * e], lv[4 * e + 1], lv[4 * e + 2], lv[4 * e + 3]);
-    } else {
-        const int t = i128 - 64;
-        const float qt = mqn[t], gt = mG[t];
-        float kn_s[32], g_s[32];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 a = reinterpret_cast<const float4 *>(mkn + 32 * hh)[e];
-            const float4 b = reinterpret_cast<const float4 *>(mG + 32 * hh)[e];
-            kn_s[4 * e] = a.x; kn_s[4 * e + 1] = a.y; kn_s[4 * e + 2] = a.z; kn_s[4 * e + 3] = a.w;
-            g_s[4 * e] = b.x; g_s[4 * e + 1] = b.y; g_s[4 * e + 2] = b.z; g_s[4 * e + 3] = b.w;
-        }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = 32 * hh + cc * 8 + e;
-                const float val = qt * kn_s[cc * 8 + e] * __uint_as_float(r[cc * 8 + e]) *
-                                  __expf(gt - g_s[cc * 8 + e]);
-                f[e] = (s <= t && t < nv) ? val : 0.f;
-            }
-            const int chunk = 4 * hh + cc;
-            *reinterpret_cast<uint4 *>(sA + t * 128 + ((chunk ^ (t & 7)) << 4)) = pack8(f);
-        }
-    }
-    fence_proxy_async();
-    __syncthreads();
-
-    // ---- T = (I + L)^{-1}
-    invert_unit_lower_64<kPrepThreads>(sL, sT, tid);
-
-    // ---- B = [T' | P], Bf = diag(f) B   (MN-major: row t, columns s); 4 threads per row
-    {
-        const int t = tid >> 2, half = (tid >> 1) & 1, grp = tid & 1;
-        const float *Trow = sT + t * kLP;
-        const float ft = mf[t];
-        const float *w = half ? mbeta : mcw;
-        uint8_t *dB = sB + half * 8192 + t * 128;
-        uint8_t *dBf = sBf + half * 8192 + t * 128;
-        float tv[32], wv[32];   // this thread's 32 columns, loaded before use
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 a = reinterpret_cast<const float4 *>(Trow + grp * 32)[e];
-            tv[4 * e] = a.x; tv[4 * e + 1] = a.y; tv[4 * e + 2] = a.z; tv[4 * e + 3] = a.w;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 a = reinterpret_cast<const float4 *>(w + grp * 32)[e];
-            wv[4 * e] = a.x; wv[4 * e + 1] = a.y; wv[4 * e + 2] = a.z; wv[4 * e + 3] = a.w;
-        }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const int chunk = grp * 4 + cc;
-            float f[8], fb[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                f[e] = tv[cc * 8 + e] * wv[cc * 8 + e];
-                fb[e] = f[e] * ft;
-            }
-            const int off = (chunk ^ (t & 7)) << 4;
-            *reinterpret_cast<uint4 *>(dB + off) = pack8(f);
-            *reinterpret_cast<uint4 *>(dBf + off) = pack8(fb);
-        }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- MMA2: D2a[:, 0:128] = K^T diag(f) [T'|P]  (M = D);  D2b[:, 128:256] = Aqk [T'|P]
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        const uint32_t ida = idesc_bf16_f32(D, 128, true, true);
-        const uint32_t idb = idesc_bf16_f32(64, 128, false, true);
-        const uint32_t kq = smem_u32(sKQ), bf = smem_u32(sBf), bb = smem_u32(sB), aa = smem_u32(sA);
-        for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(tm, desc_mnmajor_sw128(kq, 128, ks), desc_mnmajor_sw128(bf, 64, ks), ida,
-                        ks > 0 ? 1u : 0u);
-        for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(tm + 128, desc_kmajor_sw128(aa, 64, ks), desc_mnmajor_sw128(bb, 64, ks), idb,
-                        ks > 0 ? 1u : 0u);
-        mma_commit(&bar_mma);
-    }
-    if (ok && !mbar_wait(&bar_mma, 1, kWaitNs)) s_fail = 1;
-    tc_fence_after();
-
-    // ---- epilogue 2: Z1, Z2 operands (column half 0); the V columns of E (half 1)
-    {
-        uint32_t v[64];
-        tmem_ld32(tm + tq + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_ld32(tm + tq + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld_wait();
-        const bool has_row = (D == 128) || has64;
-        const int i = (D == 128) ? i128 : i64;
-        if (has_row) {
-            if (hh == 0) {   // Z1[i][s]: K-major operand, rows i
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc)
-                    *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((cc ^ (i & 7)) << 4)) = pack8u(v + 8 * cc);
-            } else {         // E[i][D + s] = (K~^T P)[i][s] -> staging block NB
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc)
-                    *reinterpret_cast<uint4 *>(sEst + NB * (R * 128) + i * 128 + ((cc ^ (i & 7)) << 4)) =
-                        pack8u(v + 8 * cc);
-            }
-        }
-        tmem_ld32(tm + tq + 128 + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_ld32(tm + tq + 128 + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld_wait();
-        if (has64) {
-            const int t = i64;
-            if (hh == 0) {   // Z2[t][s]
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc)
-                    *reinterpret_cast<uint4 *>(sZ2 + t * 128 + ((cc ^ (t & 7)) << 4)) = pack8u(v + 8 * cc);
-            } else {         // E[D + t][D + s] = (Aqk P)[t][s] -> staging block NB
-                const int rr = D + t;
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc)
-                    *reinterpret_cast<uint4 *>(sEst + NB * (R * 128) + rr * 128 + ((cc ^ (rr & 7)) << 4)) =
-                        pack8u(v + 8 * cc);
-            }
-        }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    ok = s_fail == 0;
-
-    // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64);
-    // meanwhile the V-column block of E_c goes out by TMA
-    if (tid == 0 && ok) {
-        tma_store_3d(&map_E, sEst + NB * (R * 128), NB * 64, 0, (int)slot);
-        bulk_commit();
-        tc_fence_after();
-        const uint32_t ida = idesc_bf16_f32(D, D, false, true);
-        const uint32_t idb = idesc_bf16_f32(64, D, false, true);
-        const uint32_t kq = smem_u32(sKQ), z1 = smem_u32(sZ1), z2 = smem_u32(sZ2);
-        for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(tm, desc_kmajor_sw128(z1, D, ks), desc_mnmajor_sw128(kq, 128, ks), ida,
-                        ks > 0 ? 1u : 0u);
-        for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(tm + 128, desc_kmajor_sw128(z2, 64, ks), desc_mnmajor_sw128(kq, 128, ks),
-                        idb, ks > 0 ? 1u : 0u);
-        mma_commit(&bar_mma);
-    }
-    if (ok && !mbar_wait(&bar_mma, 0, kWaitNs)) s_fail = 1;
-    tc_fence_after();
-
-    // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
-    {
-        constexpr int HALF = D / 2;
-        const float gamma_c = meg[63];
-        const bool has_row = (D == 128) || has64;
-        const int i = (D == 128) ? i128 : i64;
-#pragma unroll
-        for (int c0 = 0; c0 < HALF; c0 += 32) {   // E[i][j] = gamma_C delta_ij - (K~^T W)[i][j]
-            uint32_t v[32];
-            const int col = hh * HALF + c0;
-            tmem_ld32(tm + tq + col, v);
+        // ---- epilogue 1: norms, L (fp32, smem) and Aqk (bf16 operand); columns 32 hh ..
+        {
+            uint32_t r[32];
+            tmem_ld32(tm + tq + 32 * hh, r);
             tmem_ld_wait();
-            if (has_row) {
-                uint8_t *dst = sEst + (col >> 6) * (R * 128) + i * 128;
+            if (i128 < 64 && (i128 >> 5) == hh) {   // this half holds the Gram diagonal of row i128
+                float diag = 0.f;
+#pragma unroll
+                for (int s = 0; s < 32; ++s)
+                    if (s == (i128 & 31)) diag = __uint_as_float(r[s]);
+                mkn[i128] = p.use_l2 ? 1.f / fmaxf(sqrtf(diag), kNormEps) : 1.f;
+            }
+            named_sync(bar, kGroupThreads);
+            const float gC = mG[63];
+            if (i128 < 64) {
+                const int t = i128;
+                const float kt = mkn[t], bt = mbeta[t], gpt = mGp[t];
+                if (hh == 0) {
+                    mf[t] = t < nv ? __expf(gC - mG[t]) * kt : 0.f;
+                    mcw[t] = bt * __expf(gpt) * kt;   // column weight of T' = T diag(beta e^{G_{s-1}} kn)
+                }
+                float *Lrow = sL + t * kLP + 32 * hh;
+                const float bk = bt * kt;
+                float kn_s[32], g_s[32];   // this half's per-token scalars, by 16-byte loads
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 a = reinterpret_cast<const float4 *>(mkn + 32 * hh)[e];
+                    const float4 b = reinterpret_cast<const float4 *>(mG + 32 * hh)[e];
+                    kn_s[4 * e] = a.x; kn_s[4 * e + 1] = a.y; kn_s[4 * e + 2] = a.z; kn_s[4 * e + 3] = a.w;
+                    g_s[4 * e] = b.x; g_s[4 * e + 1] = b.y; g_s[4 * e + 2] = b.z; g_s[4 * e + 3] = b.w;
+                }
+                float lv[32];
+#pragma unroll
+                for (int s2 = 0; s2 < 32; ++s2) {
+                    const int s = 32 * hh + s2;
+                    const float val = bk * kn_s[s2] * __uint_as_float(r[s2]) * __expf(gpt - g_s[s2]);
+                    lv[s2] = (s < t && t < nv) ? val : 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    reinterpret_cast<float4 *>(Lrow)[e] =
+                        make_float4(lv[4 * e], lv[4 * e + 1], lv[4 * e + 2], lv[4 * e + 3]);
+            } else {
+                const int t = i128 - 64;
+                const float qt = mqn[t], gt = mG[t];
+                float kn_s[32], g_s[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 a = reinterpret_cast<const float4 *>(mkn + 32 * hh)[e];
+                    const float4 b = reinterpret_cast<const float4 *>(mG + 32 * hh)[e];
+                    kn_s[4 * e] = a.x; kn_s[4 * e + 1] = a.y; kn_s[4 * e + 2] = a.z; kn_s[4 * e + 3] = a.w;
+                    g_s[4 * e] = b.x; g_s[4 * e + 1] = b.y; g_s[4 * e + 2] = b.z; g_s[4 * e + 3] = b.w;
+                }
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     float f[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int j = col + cc * 8 + e;
-                        f[e] = (j == i ? gamma_c : 0.f) - __uint_as_float(v[cc * 8 + e]);
+                        const int s = 32 * hh + cc * 8 + e;
+                        const float val = qt * kn_s[cc * 8 + e] * __uint_as_float(r[cc * 8 + e]) *
+                                          __expf(gt - g_s[cc * 8 + e]);
+                        f[e] = (s <= t && t < nv) ? val : 0.f;
                     }
-                    const int chunk = ((col & 63) >> 3) + cc;
-                    *reinterpret_cast<uint4 *>(dst + ((chunk ^ (i & 7)) << 4)) = pack8(f);
+                    const int chunk = 4 * hh + cc;
+                    *reinterpret_cast<uint4 *>(sA + t * 128 + ((chunk ^ (t & 7)) << 4)) = pack8(f);
                 }
             }
         }
-        const int t = i64;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j]
-        const float qs = has64 ? meg[t] * mqn[t] : 0.f;
+        fence_proxy_async();
+        named_sync(bar, kGroupThreads);
+        ok = ctl->fail == 0;
+
+        // ---- T = (I + L)^{-1}
+        invert_unit_lower_64<kGroupThreads>(sL, sT, tid, bar);
+
+        // ---- B = [T' | P], Bf = diag(f) B   (MN-major: row t, columns s); 4 threads per row
+        {
+            const int t = tid >> 2, half = (tid >> 1) & 1, grp = tid & 1;
+            const float *Trow = sT + t * kLP;
+            const float ft = mf[t];
+            const float *w = half ? mbeta : mcw;
+            uint8_t *dB = sB + half * 8192 + t * 128;
+            uint8_t *dBf = sBf + half * 8192 + t * 128;
+            float tv[32], wv[32];   // this thread's 32 columns, loaded before use
 #pragma unroll
-        for (int c0 = 0; c0 < HALF; c0 += 32) {
-            uint32_t v[32];
-            const int col = hh * HALF + c0;
-            tmem_ld32(tm + tq + 128 + col, v);
+            for (int e = 0; e < 8; ++e) {
+                const float4 a = reinterpret_cast<const float4 *>(Trow + grp * 32)[e];
+                tv[4 * e] = a.x; tv[4 * e + 1] = a.y; tv[4 * e + 2] = a.z; tv[4 * e + 3] = a.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 a = reinterpret_cast<const float4 *>(w + grp * 32)[e];
+                wv[4 * e] = a.x; wv[4 * e + 1] = a.y; wv[4 * e + 2] = a.z; wv[4 * e + 3] = a.w;
+            }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int chunk = grp * 4 + cc;
+                float f[8], fb[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    f[e] = tv[cc * 8 + e] * wv[cc * 8 + e];
+                    fb[e] = f[e] * ft;
+                }
+                const int off = (chunk ^ (t & 7)) << 4;
+                *reinterpret_cast<uint4 *>(dB + off) = pack8(f);
+                *reinterpret_cast<uint4 *>(dBf + off) = pack8(fb);
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        named_sync(bar, kGroupThreads);
+
+        // ---- MMA2: D2a[:, 0:128] = K^T diag(f) [T'|P]  (M = D);  D2b[:, 128:256] = Aqk [T'|P]
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t ida = idesc_bf16_f32(D, 128, true, true);
+            const uint32_t idb = idesc_bf16_f32(64, 128, false, true);
+            const uint32_t kq = smem_u32(sKQ), bf = smem_u32(sBf), bb = smem_u32(sB), aa = smem_u32(sA);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tm, desc_mnmajor_sw128(kq, 128, ks), desc_mnmajor_sw128(bf, 64, ks), ida,
+                            ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tm + 128, desc_kmajor_sw128(aa, 64, ks), desc_mnmajor_sw128(bb, 64, ks), idb,
+                            ks > 0 ? 1u : 0u);
+            mma_commit(&ctl->bar_mma);
+        }
+        if (ok && !mbar_wait(&ctl->bar_mma, ph ^ 1u, kWaitNs)) ctl->fail = 1;
+        tc_fence_after();
+
+        // ---- epilogue 2: Z1, Z2 operands (column half 0); the V columns of E (half 1)
+        {
+            uint32_t v[64];
+            tmem_ld32(tm + tq + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(v));
+            tmem_ld32(tm + tq + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            tmem_ld_wait();
+            const bool has_row = (D == 128) || has64;
+            const int i = (D == 128) ? i128 : i64;
+            if (has_row) {
+                if (hh == 0) {   // Z1[i][s]: K-major operand, rows i
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc)
+                        *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((cc ^ (i & 7)) << 4)) = pack8u(v + 8 * cc);
+                } else {         // E[i][D + s] = (K~^T P)[i][s] -> staging block NB
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc)
+                        *reinterpret_cast<uint4 *>(sEst + NB * (R * 128) + i * 128 + ((cc ^ (i & 7)) << 4)) =
+                            pack8u(v + 8 * cc);
+                }
+            }
+            tmem_ld32(tm + tq + 128 + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(v));
+            tmem_ld32(tm + tq + 128 + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
             tmem_ld_wait();
             if (has64) {
-                const int rr = D + t;
-                uint8_t *dst = sEst + (col >> 6) * (R * 128) + rr * 128;
+                const int t = i64;
+                if (hh == 0) {   // Z2[t][s]
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int j0 = col + cc * 8;   // 8 consecutive head-dim indices: one chunk of q
-                    const uint4 qw = *reinterpret_cast<const uint4 *>(
-                        sKQ + (j0 >> 6) * 16384 + 8192 + t * 128 + ((((j0 & 63) >> 3) ^ (t & 7)) << 4));
-                    const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
-                    float f[8];
+                    for (int cc = 0; cc < 8; ++cc)
+                        *reinterpret_cast<uint4 *>(sZ2 + t * 128 + ((cc ^ (t & 7)) << 4)) = pack8u(v + 8 * cc);
+                } else {         // E[D + t][D + s] = (Aqk P)[t][s] -> staging block NB
+                    const int rr = D + t;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        f[2 * e] = qs * bf16lo(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e]);
-                        f[2 * e + 1] = qs * bf16hi(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e + 1]);
-                    }
-                    const int chunk = ((col & 63) >> 3) + cc;
-                    *reinterpret_cast<uint4 *>(dst + ((chunk ^ (rr & 7)) << 4)) = pack8(f);
+                    for (int cc = 0; cc < 8; ++cc)
+                        *reinterpret_cast<uint4 *>(sEst + NB * (R * 128) + rr * 128 + ((cc ^ (rr & 7)) << 4)) =
+                            pack8u(v + 8 * cc);
                 }
             }
         }
+        fence_proxy_async();
+        tc_fence_before();
+        named_sync(bar, kGroupThreads);
+        ok = ctl->fail == 0;
+
+        // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64);
+        // meanwhile the V-column block of E_c goes out by TMA
+        if (tid == 0 && ok) {
+            tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, (int)cur.slot);
+            bulk_commit();
+            tc_fence_after();
+            const uint32_t ida = idesc_bf16_f32(D, D, false, true);
+            const uint32_t idb = idesc_bf16_f32(64, D, false, true);
+            const uint32_t kq = smem_u32(sKQ), z1 = smem_u32(sZ1), z2 = smem_u32(sZ2);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tm, desc_kmajor_sw128(z1, D, ks), desc_mnmajor_sw128(kq, 128, ks), ida,
+                            ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tm + 128, desc_kmajor_sw128(z2, 64, ks), desc_mnmajor_sw128(kq, 128, ks),
+                            idb, ks > 0 ? 1u : 0u);
+            mma_commit(&ctl->bar_mma);
+        }
+        if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
+        tc_fence_after();
+
+        // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
+        {
+            constexpr int HALF = D / 2;
+            const float gamma_c = meg[63];
+            const bool has_row = (D == 128) || has64;
+            const int i = (D == 128) ? i128 : i64;
+#pragma unroll
+            for (int c0 = 0; c0 < HALF; c0 += 32) {   // E[i][j] = gamma_C delta_ij - (K~^T W)[i][j]
+                uint32_t v[32];
+                const int col = hh * HALF + c0;
+                tmem_ld32(tm + tq + col, v);
+                tmem_ld_wait();
+                if (has_row) {
+                    uint8_t *dst = sEst + (col >> 6) * (R * 128) + i * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = col + cc * 8 + e;
+                            f[e] = (j == i ? gamma_c : 0.f) - __uint_as_float(v[cc * 8 + e]);
+                        }
+                        const int chunk = ((col & 63) >> 3) + cc;
+                        *reinterpret_cast<uint4 *>(dst + ((chunk ^ (i & 7)) << 4)) = pack8(f);
+                    }
+                }
+            }
+            const int t = i64;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j]
+            const float qs = has64 ? meg[t] * mqn[t] : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < HALF; c0 += 32) {
+                uint32_t v[32];
+                const int col = hh * HALF + c0;
+                tmem_ld32(tm + tq + 128 + col, v);
+                tmem_ld_wait();
+                if (has64) {
+                    const int rr = D + t;
+                    uint8_t *dst = sEst + (col >> 6) * (R * 128) + rr * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int j0 = col + cc * 8;   // 8 consecutive head-dim indices: one chunk of q
+                        const uint4 qw = *reinterpret_cast<const uint4 *>(
+                            sKQ + (j0 >> 6) * 16384 + 8192 + t * 128 + ((((j0 & 63) >> 3) ^ (t & 7)) << 4));
+                        const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            f[2 * e] = qs * bf16lo(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e]);
+                            f[2 * e + 1] = qs * bf16hi(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e + 1]);
+                        }
+                        const int chunk = ((col & 63) >> 3) + cc;
+                        *reinterpret_cast<uint4 *>(dst + ((chunk ^ (rr & 7)) << 4)) = pack8(f);
+                    }
+                }
+            }
+        }
+
+        // ---- next chunk of this group: its scalars are fetched while this one finishes
+        long nitem = item + stride;
+        ChunkItem nx;
+        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
+        const bool more = nitem < p.n_items;
+        if (more && tid < 64) {
+            const long gi = (nx.row0 + tid) * p.H + nx.h;
+            nbeta = tid < nx.nv ? p.beta[gi] : 0.f;
+            ndec = (tid < nx.nv && p.decay) ? p.decay[gi] : 0.f;
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        named_sync(bar, kGroupThreads);
+        const bool failed = ctl->fail != 0;
+        if (tid == 0) {
+            if (failed) record_error(p.ws, 1);
+            for (int kb = 0; kb < NB; ++kb)   // the state-column blocks of E_c
+                tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)cur.slot);
+            bulk_commit();
+            if (more && !failed)   // [K;Q] is free: every read of it is behind the barrier
+                load_kq<NB>(map_q, map_k, sKQ, &ctl->bar_tma, nx);
+            bulk_wait_read0();     // the staging area must stay valid until the stores have read it
+            if (p.flags) pend = cur.slot;
+        }
+        if (!more || failed) break;
+        item = nitem;
+        cur = nx;
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        if (s_fail) record_error(p.ws, 1);
-        for (int kb = 0; kb < NB; ++kb)   // the state-column blocks of E_c
-            tma_store_3d(&map_E, sEst + kb * (R * 128), kb * 64, 0, (int)slot);
-        bulk_commit();
-        bulk_wait_read0();   // shared memory must stay valid until the stores have read it
-    }
-    if (warp == 0) {
-        __syncwarp();
-        tmem_dealloc(tm, 256);
-    }
+    if (tid == 0 && pend >= 0) publish_slot(p, pend);
 }
 
 // ---------------------------------------------------------------------------------
-// chain_kernel -- one CTA per (sequence, head), transposed so that M = dv:
+// chain -- one CTA per (sequence, head), transposed so that M = dv:
 //
 //   D^T[j][r] = sum_k A[j][k] E_c[r][k],   A = [S^T | V_c^T]   (dv rows, D + 64 columns)
 //
@@ -632,6 +710,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
 // its outputs) is one wide product rather than several narrow ones.
 // The state is carried as the bf16 operand S^T, rebuilt every chunk from the fp32
 // accumulator; the final state is stored from the fp32 accumulator.
+// Warps: 0 producers, 1 MMA, 2..9 state epilogue (two per TMEM lane quadrant, one
+// half of the state columns each), 10..13 output epilogue; any others idle.
 // ---------------------------------------------------------------------------------
 template <int D>
 struct ChainCfg {
@@ -644,17 +724,16 @@ struct ChainCfg {
     static constexpr int O_BYTES = 64 * D * 2;    // output staging [64][D] bf16
     static constexpr int SMEM = 2 * E_BYTES + AS_BYTES + 2 * AV_BYTES + O_BYTES + 1024;
     static constexpr uint32_t TCOLS = (2 * R <= 256) ? 256u : 512u;   // two accumulators
-    static constexpr int THREADS = 320;           // producer, MMA, 4 state + 4 output warps
+    static constexpr int THREADS = 448;           // producer, MMA, 8 state + 4 output warps
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ CUtensorMap map_E,
-                                                       const __grid_constant__ CUtensorMap map_v,
-                                                       TcParams p) {
+__device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUtensorMap *map_v,
+                                           const TcParams &p, uint8_t *sm, int task,
+                                           bool wait_flags) {
     using Cf = ChainCfg<D>;
     constexpr int R = Cf::R;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = align1024(smem_raw);
+    constexpr int HALF = D / 2;
     uint8_t *sE0 = sm;
     uint8_t *sAS = sm + 2 * Cf::E_BYTES;
     uint8_t *sAV0 = sAS + Cf::AS_BYTES;
@@ -663,8 +742,8 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_fail;
 
-    const int h = blockIdx.x % p.H;
-    const int n = blockIdx.x / p.H;
+    const int h = task % p.H;
+    const int n = task / p.H;
     long start;
     int len;
     seq_info(p, n, start, len);
@@ -679,9 +758,9 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);     // released by the MMA commit
             mbar_init(&d_full[s], 1);
-            mbar_init(&d_free[s], 256);    // both epilogue groups read the accumulator
+            mbar_init(&d_free[s], 384);    // the state and the output warps read the accumulator
         }
-        mbar_init(&s_ready, 128);
+        mbar_init(&s_ready, 256);
         fence_mbar_init();
         s_fail = 0;
     }
@@ -697,12 +776,15 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
     if (warp == 0) {
         // ---------------- producers: lane 0 streams E_c, lane 1 streams V_c, each into
         // two shared-memory stages freed by the MMA commit; both also prefetch the
-        // tiles kPrefetch chunks ahead into L2 so that the stage loads hit L2.
+        // tiles kPrefetch chunks ahead into L2 so that the stage loads hit L2 (E_c only
+        // when it was built by an earlier launch; in the single launch it is waited for
+        // by flag and was just written, so it sits in L2 already).
         constexpr int kPrefetch = 4;
         if (lane == 0) {
-            for (int c = 0; c < kPrefetch && c < nc; ++c)
-                for (int kb = 0; kb < Cf::NKB; ++kb)
-                    tma_prefetch_l2_3d(&map_E, kb * 64, 0, (int)(slot0 + (long)c * p.H));
+            if (!wait_flags)
+                for (int c = 0; c < kPrefetch && c < nc; ++c)
+                    for (int kb = 0; kb < Cf::NKB; ++kb)
+                        tma_prefetch_l2_3d(map_E, kb * 64, 0, (int)(slot0 + (long)c * p.H));
             for (int c = 0; c < nc && !s_fail; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !mbar_wait(&e_empty[s], ((c >> 1) - 1) & 1, kWaitNs)) {
@@ -710,19 +792,37 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
                     record_error(p.ws, 10);
                     break;
                 }
+                const int slot = (int)(slot0 + (long)c * p.H);
+                if (wait_flags) {   // E_c published by its prep group
+                    const uint32_t *f = p.flags + slot;
+                    const uint64_t t0 = globaltimer_ns();
+                    bool got = true;
+                    while (ld_acquire_gpu(f) == 0u) {
+                        if (globaltimer_ns() - t0 > kWaitNs) {
+                            got = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!got) {
+                        s_fail = 1;
+                        record_error(p.ws, 16);
+                        break;
+                    }
+                    fence_proxy_async_global();
+                }
                 mbar_expect_tx(&e_full[s], Cf::E_BYTES);
                 uint8_t *dE = sE0 + s * Cf::E_BYTES;
-                const int slot = (int)(slot0 + (long)c * p.H);
                 for (int kb = 0; kb < Cf::NKB; ++kb)
-                    tma_load_3d(dE + kb * (R * 128), &map_E, &e_full[s], kb * 64, 0, slot);
-                if (c + kPrefetch < nc)
+                    tma_load_3d(dE + kb * (R * 128), map_E, &e_full[s], kb * 64, 0, slot);
+                if (!wait_flags && c + kPrefetch < nc)
                     for (int kb = 0; kb < Cf::NKB; ++kb)
-                        tma_prefetch_l2_3d(&map_E, kb * 64, 0, (int)(slot0 + (long)(c + kPrefetch) * p.H));
+                        tma_prefetch_l2_3d(map_E, kb * 64, 0, (int)(slot0 + (long)(c + kPrefetch) * p.H));
             }
         } else if (lane == 1) {
             for (int c = 0; c < kPrefetch && c < nc; ++c)
                 for (int mb = 0; mb < Cf::NB; ++mb)
-                    tma_prefetch_l2_3d(&map_v, mb * 64, h, (int)(start + (long)c * kC));
+                    tma_prefetch_l2_3d(map_v, mb * 64, h, (int)(start + (long)c * kC));
             for (int c = 0; c < nc && !s_fail; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !mbar_wait(&v_empty[s], ((c >> 1) - 1) & 1, kWaitNs)) {
@@ -733,11 +833,11 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
                 mbar_expect_tx(&v_full[s], Cf::AV_BYTES);
                 uint8_t *dV = sAV0 + s * Cf::AV_BYTES;
                 for (int mb = 0; mb < Cf::NB; ++mb)
-                    tma_load_3d(dV + mb * 8192, &map_v, &v_full[s], mb * 64, h,
+                    tma_load_3d(dV + mb * 8192, map_v, &v_full[s], mb * 64, h,
                                 (int)(start + (long)c * kC));
                 if (c + kPrefetch < nc)
                     for (int mb = 0; mb < Cf::NB; ++mb)
-                        tma_prefetch_l2_3d(&map_v, mb * 64, h, (int)(start + (long)(c + kPrefetch) * kC));
+                        tma_prefetch_l2_3d(map_v, mb * 64, h, (int)(start + (long)(c + kPrefetch) * kC));
             }
         }
     } else if (warp == 1) {
@@ -776,17 +876,19 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
                 mma_commit(&v_empty[b]);
             }
         }
-    } else if (warp < 6) {
-        // ---------------- state epilogue, warps 2..5: TMEM quadrant q, value column j.
-        // Turns the fp32 next state into the bf16 S^T operand (the critical path).
-        const int q = warp & 3;
+    } else if (warp < 10) {
+        // ---------------- state epilogue, warps 2..9: TMEM quadrant q, value column j,
+        // state rows i in [ch D/2, (ch + 1) D/2).  Turns the fp32 next state into the
+        // bf16 S^T operand (the critical path).
+        const int q = warp & 3, ch = (warp - 2) >> 2;
         const bool has_row = (D == 128) || (lane < 16);   // M = 64: 16 rows per quadrant
         const int j = (D == 128) ? 32 * q + lane : 16 * q + lane;
         const uint32_t lrow = (uint32_t)(32 * q) << 16;
         const size_t hbase = ((size_t)n * p.H + h) * D * D;
+        const int i_lo = ch * HALF;
 
         if (has_row) {   // S_0^T row j from initial_state[:, j]
-            for (int i0 = 0; i0 < D; i0 += 8) {
+            for (int i0 = i_lo; i0 < i_lo + HALF; i0 += 8) {
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = p.h0 ? p.h0[hbase + (size_t)(i0 + e) * D + j] : 0.f;
@@ -813,11 +915,11 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
                 break;
             }
             tc_fence_after();
-            const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
+            const uint32_t dcol = tm + lrow + (uint32_t)(b * R) + (uint32_t)i_lo;
             const bool last = (c + 1 == nc);
-            uint32_t v[D];
+            uint32_t v[HALF];
 #pragma unroll
-            for (int i0 = 0; i0 < D; i0 += 32)
+            for (int i0 = 0; i0 < HALF; i0 += 32)
                 tmem_ld32(dcol + i0, *reinterpret_cast<uint32_t(*)[32]>(v + i0));
             tmem_ld_wait();
             tc_fence_before();
@@ -825,29 +927,28 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
             if (has_row) {
                 if (!last) {
 #pragma unroll
-                    for (int cc = 0; cc < D / 8; ++cc)
-                        *reinterpret_cast<uint4 *>(sAS + (cc >> 3) * D * 128 + j * 128 +
-                                                   (((cc & 7) ^ (j & 7)) << 4)) =
-                            make_uint4(pack_bf16(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
-                                       pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
-                                       pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
-                                       pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
+                    for (int cc = 0; cc < HALF / 8; ++cc) {
+                        const int gc = (i_lo >> 3) + cc;   // 8-column group of S^T row j
+                        *reinterpret_cast<uint4 *>(sAS + (gc >> 3) * D * 128 + j * 128 +
+                                                   (((gc & 7) ^ (j & 7)) << 4)) = pack8u(v + 8 * cc);
+                    }
                 } else if (p.hT) {
 #pragma unroll
-                    for (int i = 0; i < D; ++i) p.hT[hbase + (size_t)i * D + j] = __uint_as_float(v[i]);
+                    for (int i = 0; i < HALF; ++i)
+                        p.hT[hbase + (size_t)(i_lo + i) * D + j] = __uint_as_float(v[i]);
                 }
             }
             if (!last) fence_proxy_async();
             mbar_arrive(&s_ready);   // S_{c+1}^T is in place
         }
-    } else {
-        // ---------------- output epilogue, warps 6..9: O[t][j] from the same
+    } else if (warp < 14) {
+        // ---------------- output epilogue, warps 10..13: O[t][j] from the same
         // accumulator, staged row-major [t][j] and written out as whole 16-byte rows.
         const int q = warp & 3;
         const bool has_row = (D == 128) || (lane < 16);
         const int j = (D == 128) ? 32 * q + lane : 16 * q + lane;
         const uint32_t lrow = (uint32_t)(32 * q) << 16;
-        const int et = tid - 192;       // 0..127 over the output warps
+        const int et = tid - 320;       // 0..127 over the output warps
         __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sO);
         constexpr int CPR = D / 8;      // 16-byte pieces per output row
         for (int c = 0; c < nc; ++c) {
@@ -887,6 +988,60 @@ __global__ void __launch_bounds__(320, 1) chain_kernel(const __grid_constant__ C
         __syncwarp();
         tmem_dealloc(tm, Cf::TCOLS);
     }
+}
+
+// ---------------------------------------------------------------------------------
+// tc_kernel -- CTAs [0, nchain) take the chain role (one (sequence, head) each), the
+// others two prep groups each.  With nchain > 0 the launch is cooperative, so that
+// every chain's producers are co-resident with the prep groups they wait for.
+// ---------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant__ CUtensorMap map_q,
+                                                           const __grid_constant__ CUtensorMap map_k,
+                                                           const __grid_constant__ CUtensorMap map_v,
+                                                           const __grid_constant__ CUtensorMap map_E,
+                                                           TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    if ((int)blockIdx.x < p.nchain) {
+        chain_body<D>(&map_E, &map_v, p, sm, (int)blockIdx.x, p.flags != nullptr);
+        return;
+    }
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, grp = tid >> 8;
+    uint8_t *gsm = sm + grp * PrepSmem<D>::GROUP;
+    if ((tid & (kGroupThreads - 1)) == 0) {
+        PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(gsm + PrepSmem<D>::CTRL);
+        mbar_init(&ctl->bar_tma, 1);
+        mbar_init(&ctl->bar_mma, 1);
+        fence_mbar_init();
+        ctl->fail = 0;
+    }
+    if (tid < 32) {   // 256 columns for each group
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const long gidx = (long)((int)blockIdx.x - p.nchain) * 2 + grp;
+    const long ngroups = (long)((int)gridDim.x - p.nchain) * 2;
+    prep_group<D>(&map_q, &map_k, &map_E, p, gsm, tmem_base + (uint32_t)(grp * 256),
+                  tid & (kGroupThreads - 1), 1 + grp, gidx, ngroups);
+    tc_fence_before();
+    __syncthreads();
+    if (tid < 32) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(ChainCfg<D>::THREADS, 1) chain_kernel(const __grid_constant__ CUtensorMap map_E,
+                                                                        const __grid_constant__ CUtensorMap map_v,
+                                                                        TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    chain_body<D>(&map_E, &map_v, p, align1024(smem_raw), (int)blockIdx.x, false);
 }
 
 // cu_seqlens -> chunk prefix: base[n] = sum_{m < n} ceil(len_m / 64), base[N] = total.
@@ -941,10 +1096,12 @@ bool map_E(CUtensorMap *m, const void *base, long slots, int R) {
 }
 
 constexpr size_t kTableBytes(int nseq) { return (((size_t)(nseq + 1) * 4 + 255) / 256) * 256; }
+constexpr size_t kFlagBytes(long slots) { return (((size_t)slots * 4 + 255) / 256) * 256; }
 
 template <int D>
 cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
     constexpr int R = D + 64;
+    using Cf = ChainCfg<D>;
     TcParams p{};
     p.nseq = a.nseq; p.H = a.H; p.T = a.T; p.use_l2 = a.use_l2; p.scale = a.scale;
     p.cu_seqlens = a.cu_seqlens;
@@ -954,30 +1111,68 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.ws = a.ws;
     uint8_t *body = static_cast<uint8_t *>(a.ws_body);
     int *table = reinterpret_cast<int *>(body);
+    uint32_t *flags = reinterpret_cast<uint32_t *>(body + kTableBytes(a.nseq));
     p.chunk_base = a.cu_seqlens ? table : nullptr;
-    p.E = reinterpret_cast<__nv_bfloat16 *>(body + kTableBytes(a.nseq));
+    p.E = reinterpret_cast<__nv_bfloat16 *>(body + kTableBytes(a.nseq) + kFlagBytes(slots_bound));
+    p.nsh = (long)a.nseq * a.H;
+    p.maxnc = (a.T + kC - 1) / kC;   // varlen: a.T bounds the longest sequence
 
     CUtensorMap mq, mk, mv, me;
     if (!map_tokens(&mq, a.q, total_rows, a.H, D) || !map_tokens(&mk, a.k, total_rows, a.H, D) ||
         !map_tokens(&mv, a.v, total_rows, a.H, D) || !map_E(&me, p.E, slots_bound, R))
         return cudaErrorInvalidValue;
 
+    cudaError_t e;
     if (a.cu_seqlens) {
         chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.nseq, table);
-        cudaError_t e = cudaGetLastError();
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const long chunks_bound = slots_bound / a.H;
-    cudaError_t e = cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PrepSmem<D>::BYTES);
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int prep_smem = 2 * PrepSmem<D>::GROUP + 1024;
+    const int one_smem = std::max(prep_smem, Cf::SMEM);
+    e = cudaFuncSetAttribute(tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, one_smem);
     if (e != cudaSuccess) return e;
-    prep_kernel<D><<<(unsigned)(chunks_bound * a.H), kPrepThreads, PrepSmem<D>::BYTES, st>>>(mq, mk, me, p);
+
+    // Single launch when the chains take at most half of the SMs: chains and prep
+    // groups co-resident (cooperative launch), E_c handed over by flags.
+    if (p.nsh <= nsm / 2) {
+        TcParams pf = p;
+        pf.flags = flags;
+        pf.chunk_major = 1;
+        pf.n_items = (long)pf.maxnc * pf.nsh;
+        pf.nchain = (int)pf.nsh;
+        if ((e = cudaMemsetAsync(flags, 0, (size_t)slots_bound * 4, st)) != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)nsm);
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = (size_t)one_smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tc_kernel<D>, mq, mk, mv, me, pf);
+        if (e == cudaSuccess) return cudaSuccess;
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        (void)cudaGetLastError();   // fewer SMs available than reported: two launches
+    }
+
+    // Two launches: persistent prep groups over the E_c slots, then the chains.
+    p.flags = nullptr;
+    p.chunk_major = 0;
+    p.n_items = slots_bound;
+    p.nchain = 0;
+    const long ctas = std::min<long>((slots_bound + 1) / 2, (long)nsm);
+    tc_kernel<D><<<(unsigned)ctas, kTcThreads, prep_smem, st>>>(mq, mk, mv, me, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    using Cf = ChainCfg<D>;
     e = cudaFuncSetAttribute(chain_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (e != cudaSuccess) return e;
-    chain_kernel<D><<<(unsigned)((long)a.nseq * a.H), Cf::THREADS, Cf::SMEM, st>>>(me, mv, p);
+    chain_kernel<D><<<(unsigned)p.nsh, Cf::THREADS, Cf::SMEM, st>>>(me, mv, p);
     return cudaGetLastError();
 }
 
@@ -987,11 +1182,11 @@ bool chunk_tc_supported(int dk, int dv, int chunk, DType dt) {
     return dt == DType::BF16 && dk == dv && (dk == 64 || dk == 128) && chunk == kC;
 }
 
-// Scratch bytes after the workspace header: the chunk table and one E slot per
-// (chunk, head).  slots_bound: an upper bound on the number of chunks times H.
+// Scratch bytes after the workspace header: the chunk table, one flag and one E slot
+// per (chunk, head).  slots_bound: an upper bound on the number of chunks times H.
 size_t chunk_tc_scratch_bytes(int nseq, long slots_bound, int d) {
     const long R = d + 64;
-    return kTableBytes(nseq) + (size_t)slots_bound * R * R * 2;
+    return kTableBytes(nseq) + kFlagBytes(slots_bound) + (size_t)slots_bound * R * R * 2;
 }
 
 long chunk_tc_slots_bound(int nseq, long total_rows, int H, int T_equal, bool varlen) {

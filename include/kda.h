@@ -39,6 +39,9 @@
  * The bf16 chunked prefill runs on the tcgen05 tensor-core path when
  * dk == dv in {64, 128} and chunk_size == 64; every other supported shape runs
  * on the fp32 CUDA-core chunk path.  Anything else returns KDA_ERR_UNSUPPORTED.
+ * When the (sequence, head) pairs number at most half of the GPU's SMs, the
+ * tensor-core path is one cooperative kernel launch (it occupies every SM until it
+ * ends); otherwise it is two ordinary launches.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -123,8 +126,9 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
  * returns KDA_ERR_UNSUPPORTED).  Its scratch is one 64 MiB array that the library keeps
  * on every GPU that loads it, until the process exits; a problem whose scratch would not
  * fit returns KDA_ERR_WORKSPACE before anything is enqueued.  The scratch needed is
- * 256 + ceil(4(B+1)/256)*256 + B * ceil(T/64) * H * (D+64)^2 * 2 bytes, i.e. at most
- * 910 (chunk, head) pairs at D = 128 and 2047 at D = 64.
+ * 256 + ceil(4(B+1)/256)*256 + ceil(4S/256)*256 + S * (D+64)^2 * 2 bytes with
+ * S = B * ceil(T/64) * H (chunk, head) pairs, i.e. at most S = 910 at D = 128 and
+ * 2047 at D = 64.
  *
  * The first call on a device looks the array's device address up (with that device
  * current); make that first call before any stream capture.  Every call shares the one
