@@ -65,6 +65,8 @@ struct TcParams {
     const float *beta, *decay; // [rows, H]
     const float *h0;           // [nseq, H, D, D] or nullptr
     float *hT;                 // [nseq, H, D, D] or nullptr
+    const __nv_bfloat16 *q, *k;   // [rows, H, D]
+    long rows;                 // token rows of q, k, v
     __nv_bfloat16 *o;          // [rows, H, D]
     __nv_bfloat16 *E;          // scratch: [slots][D + 64][D + 64]
     uint32_t *flags;           // scratch: [slots], E_c published (single-launch mode) or nullptr
@@ -151,14 +153,100 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 // ---------------------------------------------------------------------------------
 // T = (I + L)^{-1} for a 64 x 64 strictly-lower L, fp32 in shared memory (row pitch
 // kLP = 68 floats: 16-byte aligned rows), by the NT = 256 threads of one group (named
-// barrier `bar`): the four 16 x 16 diagonal blocks by forward substitution (one lane
-// per column, the column kept in registers), then the off-diagonal blocks by distance
-// from the diagonal,
-//   T_ij = -T_ii X_ij,  X_ij = sum_{k=j}^{i-1} L_ik T_kj,
-// each thread computing 8 consecutive outputs of one row with 16-byte loads.  The unused
-// upper blocks of L hold the partial sums X_ij.
+// barrier `bar`), on the 4 x 4 grid of 16 x 16 blocks:
+//  * the diagonal blocks T_ii by forward substitution, one lane per column, the column
+//    in registers, right-looking (x_s, once final, is subtracted from every later row,
+//    so the dependent chain is one FMA per row);
+//  * the off-diagonal blocks  T_ij = -T_ii X_ij,  X_ij = sum_{k=j}^{i-1} L_ik T_kj,
+//    with X_ij accumulated as soon as each T_kj is known: six steps
+//      X_10 X_21 X_32 X_20 | T_10 T_21 T_32, X_31 | X_20 X_31 X_30 | T_20 T_31 | X_30 | T_30
+//    in which every thread takes 4, 2 or 1 consecutive outputs of one row.
+// The unused upper blocks of L hold the partial sums X_ij (X_ij in block (j, i)).
 // ---------------------------------------------------------------------------------
 constexpr int kLP = 68;
+
+// X_ij[r][c0 .. c0+W) = (acc ? X_ij : 0) + sum_{k in [k0,k1)} L_ik T_kj   (X_ij in L's upper block (j, i))
+template <int W>
+__device__ __forceinline__ void inv_op_x(float *sL, const float *sT, int i, int j, int k0, int k1,
+                                         bool accumulate, int r, int c0) {
+    constexpr int P = kLP;
+    float acc[W];
+    float *X = sL + (16 * j + r) * P + 16 * i + c0;
+    if (accumulate) {
+        if constexpr (W == 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(X);
+            acc[0] = x.x; acc[1] = x.y; acc[2] = x.z; acc[3] = x.w;
+        } else if constexpr (W == 2) {
+            const float2 x = *reinterpret_cast<const float2 *>(X);
+            acc[0] = x.x; acc[1] = x.y;
+        } else {
+            acc[0] = X[0];
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < W; ++e) acc[e] = 0.f;
+    }
+    for (int k = k0; k < k1; ++k) {
+        const float *Lr = sL + (16 * i + r) * P + 16 * k;
+        float l[16];
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const float4 v = *reinterpret_cast<const float4 *>(Lr + 4 * m4);
+            l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float *Tr = sT + (16 * k + m) * P + 16 * j + c0;
+            if constexpr (W == 4) {
+                const float4 t = *reinterpret_cast<const float4 *>(Tr);
+                acc[0] = fmaf(l[m], t.x, acc[0]); acc[1] = fmaf(l[m], t.y, acc[1]);
+                acc[2] = fmaf(l[m], t.z, acc[2]); acc[3] = fmaf(l[m], t.w, acc[3]);
+            } else if constexpr (W == 2) {
+                const float2 t = *reinterpret_cast<const float2 *>(Tr);
+                acc[0] = fmaf(l[m], t.x, acc[0]); acc[1] = fmaf(l[m], t.y, acc[1]);
+            } else {
+                acc[0] = fmaf(l[m], Tr[0], acc[0]);
+            }
+        }
+    }
+    if constexpr (W == 4) *reinterpret_cast<float4 *>(X) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    else if constexpr (W == 2) *reinterpret_cast<float2 *>(X) = make_float2(acc[0], acc[1]);
+    else X[0] = acc[0];
+}
+
+// T_ij[r][c0 .. c0+W) = -(T_ii X_ij)[r][c0 ..)
+template <int W>
+__device__ __forceinline__ void inv_op_t(const float *sL, float *sT, int i, int j, int r, int c0) {
+    constexpr int P = kLP;
+    const float *Ar = sT + (16 * i + r) * P + 16 * i;
+    float a[16];
+#pragma unroll
+    for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 v = *reinterpret_cast<const float4 *>(Ar + 4 * m4);
+        a[4 * m4] = v.x; a[4 * m4 + 1] = v.y; a[4 * m4 + 2] = v.z; a[4 * m4 + 3] = v.w;
+    }
+    float acc[W];
+#pragma unroll
+    for (int e = 0; e < W; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const float *Xr = sL + (16 * j + m) * P + 16 * i + c0;
+        if constexpr (W == 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(Xr);
+            acc[0] = fmaf(a[m], x.x, acc[0]); acc[1] = fmaf(a[m], x.y, acc[1]);
+            acc[2] = fmaf(a[m], x.z, acc[2]); acc[3] = fmaf(a[m], x.w, acc[3]);
+        } else if constexpr (W == 2) {
+            const float2 x = *reinterpret_cast<const float2 *>(Xr);
+            acc[0] = fmaf(a[m], x.x, acc[0]); acc[1] = fmaf(a[m], x.y, acc[1]);
+        } else {
+            acc[0] = fmaf(a[m], Xr[0], acc[0]);
+        }
+    }
+    float *Tij = sT + (16 * i + r) * P + 16 * j + c0;
+    if constexpr (W == 4) *reinterpret_cast<float4 *>(Tij) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+    else if constexpr (W == 2) *reinterpret_cast<float2 *>(Tij) = make_float2(-acc[0], -acc[1]);
+    else Tij[0] = -acc[0];
+}
 
 template <int NT>
 __device__ void invert_unit_lower_64(float *sL, float *sT, int tid, int bar) {
@@ -168,23 +256,17 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid, int bar) {
     if (warp < 4 && lane < 16) {
         // diagonal block `warp`, column j = lane: x_r = delta_rj - sum_{s<r} L[r][s] x_s
         const int b0 = 16 * warp, j = lane;
-        float x[16];
+        float acc[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const float *Lr = sL + (b0 + r) * P + b0;
-            float l[16];
+        for (int r = 0; r < 16; ++r) acc[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int s = 0; s < r; ++s) l[s] = Lr[s];   // independent loads, issued together
-            float a0 = (r == j) ? 1.f : 0.f, a1 = 0.f;
+        for (int s = 0; s < 15; ++s) {
+            const float xs = acc[s];
 #pragma unroll
-            for (int s = 0; s < r; ++s) {               // x_s = 0 for s < j
-                if (s & 1) a1 = fmaf(-l[s], x[s], a1);
-                else a0 = fmaf(-l[s], x[s], a0);
-            }
-            x[r] = a0 + a1;
+            for (int r = s + 1; r < 16; ++r) acc[r] = fmaf(-sL[(b0 + r) * P + b0 + s], xs, acc[r]);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
+        for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = acc[r];
     } else {
         // the other 192 threads zero the six strictly-upper 16 x 16 blocks of T
         const int zt = warp < 4 ? warp * 16 + (lane - 16) : 64 + (warp - 4) * 32 + lane;
@@ -196,61 +278,40 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid, int bar) {
         }
     }
     named_sync(bar, NT);
-    for (int d = 1; d < 4; ++d) {
-        const int items = (4 - d) * 32;        // (block, row, 8-column group)
-        const int bb = tid >> 5, r = (tid >> 1) & 15, c0 = (tid & 1) * 8;
-        const int j = bb, i = bb + d;
-        if (tid < items) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int k = j; k < i; ++k) {
-                const float *Lr = sL + (16 * i + r) * P + 16 * k;
-                float l[16];
-#pragma unroll
-                for (int m4 = 0; m4 < 4; ++m4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(Lr + 4 * m4);
-                    l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
-                }
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float *Tr = sT + (16 * k + m) * P + 16 * j + c0;
-                    const float4 t0 = *reinterpret_cast<const float4 *>(Tr);
-                    const float4 t1 = *reinterpret_cast<const float4 *>(Tr + 4);
-                    acc[0] = fmaf(l[m], t0.x, acc[0]); acc[1] = fmaf(l[m], t0.y, acc[1]);
-                    acc[2] = fmaf(l[m], t0.z, acc[2]); acc[3] = fmaf(l[m], t0.w, acc[3]);
-                    acc[4] = fmaf(l[m], t1.x, acc[4]); acc[5] = fmaf(l[m], t1.y, acc[5]);
-                    acc[6] = fmaf(l[m], t1.z, acc[6]); acc[7] = fmaf(l[m], t1.w, acc[7]);
-                }
-            }
-            float *X = sL + (16 * j + r) * P + 16 * i + c0;   // upper block (j, i)
-            *reinterpret_cast<float4 *>(X) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            *reinterpret_cast<float4 *>(X + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        }
-        named_sync(bar, NT);
-        if (tid < items) {
-            const float *Tr = sT + (16 * i + r) * P + 16 * i;
-            float l[16];
-#pragma unroll
-            for (int m4 = 0; m4 < 4; ++m4) {
-                const float4 v = *reinterpret_cast<const float4 *>(Tr + 4 * m4);
-                l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
-            }
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float *Xr = sL + (16 * j + m) * P + 16 * i + c0;
-                const float4 x0 = *reinterpret_cast<const float4 *>(Xr);
-                const float4 x1 = *reinterpret_cast<const float4 *>(Xr + 4);
-                acc[0] = fmaf(l[m], x0.x, acc[0]); acc[1] = fmaf(l[m], x0.y, acc[1]);
-                acc[2] = fmaf(l[m], x0.z, acc[2]); acc[3] = fmaf(l[m], x0.w, acc[3]);
-                acc[4] = fmaf(l[m], x1.x, acc[4]); acc[5] = fmaf(l[m], x1.y, acc[5]);
-                acc[6] = fmaf(l[m], x1.z, acc[6]); acc[7] = fmaf(l[m], x1.w, acc[7]);
-            }
-            float *Tij = sT + (16 * i + r) * P + 16 * j + c0;
-            *reinterpret_cast<float4 *>(Tij) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-            *reinterpret_cast<float4 *>(Tij + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
-        }
-        named_sync(bar, NT);
+    const int slot = tid >> 6, t64 = tid & 63;
+    const int r4 = t64 >> 2, c4 = (t64 & 3) * 4;          // 64 threads x 4 outputs
+    // S0: X_10, X_21, X_32, X_20 from the diagonal inverses
+    {
+        const int i = slot == 3 ? 2 : slot + 1, j = slot == 3 ? 0 : slot;
+        inv_op_x<4>(sL, sT, i, j, j, j + 1, false, r4, c4);
     }
+    named_sync(bar, NT);
+    // S1: T_10, T_21, T_32; X_31 = L_31 T_11
+    if (slot < 3) inv_op_t<4>(sL, sT, slot + 1, slot, r4, c4);
+    else inv_op_x<4>(sL, sT, 3, 1, 1, 2, false, r4, c4);
+    named_sync(bar, NT);
+    // S2: X_20 += L_21 T_10;  X_31 += L_32 T_21;  X_30 = L_30 T_00 + L_31 T_10 (two column halves)
+    if (slot == 0) inv_op_x<4>(sL, sT, 2, 0, 1, 2, true, r4, c4);
+    else if (slot == 1) inv_op_x<4>(sL, sT, 3, 1, 2, 3, true, r4, c4);
+    else {
+        const int r2 = t64 >> 2, c2 = (slot - 2) * 8 + (t64 & 3) * 2;
+        inv_op_x<2>(sL, sT, 3, 0, 0, 2, false, r2, c2);
+    }
+    named_sync(bar, NT);
+    // S3: T_20, T_31 (128 threads each, 2 outputs)
+    {
+        const int half = tid >> 7, t128 = tid & 127;
+        const int r2 = t128 >> 3, c2 = (t128 & 7) * 2;
+        if (half == 0) inv_op_t<2>(sL, sT, 2, 0, r2, c2);
+        else inv_op_t<2>(sL, sT, 3, 1, r2, c2);
+    }
+    named_sync(bar, NT);
+    // S4: X_30 += L_32 T_20 (one output per thread)
+    inv_op_x<1>(sL, sT, 3, 0, 2, 3, true, tid >> 4, tid & 15);
+    named_sync(bar, NT);
+    // S5: T_30
+    inv_op_t<1>(sL, sT, 3, 0, tid >> 4, tid & 15);
+    named_sync(bar, NT);
 }
 
 // 8 fp32 -> one 16-byte group of bf16
@@ -287,25 +348,43 @@ struct PrepSmem {
 };
 
 struct PrepCtrl {
-    uint64_t bar_tma, bar_mma;
+    uint64_t bar_mma;
     int fail;
 };
 
-// q, k tiles of one chunk into the [K;Q] region (k rows 0-63, q rows 64-127 of each
-// 64-column block)
-template <int NB>
-__device__ __forceinline__ void load_kq(const CUtensorMap *map_q, const CUtensorMap *map_k,
-                                        uint8_t *sKQ, uint64_t *bar, const ChunkItem &it) {
-    mbar_expect_tx(bar, NB * 2 * 64 * 128);
-    for (int kb = 0; kb < NB; ++kb) {
-        tma_load_3d(sKQ + kb * 16384, map_k, bar, kb * 64, it.h, (int)it.row0);
-        tma_load_3d(sKQ + kb * 16384 + 8192, map_q, bar, kb * 64, it.h, (int)it.row0);
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// q, k of one chunk into the [K;Q] region (K-major SW128; k rows 0-63, q rows 64-127 of
+// each 64-column block) by 16-byte cp.async copies spread over the group's threads.
+// These go through the load path, not the TMA unit, where they would queue behind the
+// E_c stores.  Rows past the token array are filled with zeros.
+template <int D>
+__device__ __forceinline__ void load_kq(const TcParams &p, uint8_t *sKQ, const ChunkItem &it, int tid) {
+    constexpr int PPR = D / 8;                               // 16-byte pieces per row
+    constexpr int PER = 2 * 64 * PPR / kGroupThreads;        // pieces per thread
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+        const int pidx = tid + kGroupThreads * m;
+        const int tensor = pidx / (64 * PPR);                // 0: k, 1: q
+        const int rem = pidx % (64 * PPR);
+        const int row = rem / PPR, pc = rem % PPR;
+        const long grow = it.row0 + row;
+        const bool in = grow < p.rows;
+        const __nv_bfloat16 *src = (tensor ? p.q : p.k) + ((in ? grow : 0) * p.H + it.h) * D + 8 * pc;
+        uint8_t *dst = sKQ + (pc >> 3) * 16384 + tensor * 8192 + row * 128 + (((pc & 7) ^ (row & 7)) << 4);
+        cp_async16(dst, src, in ? 16u : 0u);
     }
+    cp_async_commit();
 }
 
-// E_c of `slot` is in global memory: wait for the bulk stores, then release the flag
-__device__ __forceinline__ void publish_slot(const TcParams &p, long slot) {
-    bulk_wait0();
+// E_c of `slot` is in global memory (its bulk stores have completed): release the flag
+__device__ __forceinline__ void release_slot(const TcParams &p, long slot) {
     fence_proxy_async_global();
     st_release_gpu(p.flags + slot, 1u);
 }
@@ -345,23 +424,40 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     ChunkItem cur;
     while (item < p.n_items && !item_info(p, item, cur)) item += stride;
     if (item >= p.n_items) return;
-    if (tid == 0) load_kq<NB>(map_q, map_k, sKQ, &ctl->bar_tma, cur);
-    float nbeta = 0.f, ndec = 0.f;   // tid < 64: this chunk's beta, decay of token tid
-    if (tid < 64) {
-        const long gi = (cur.row0 + tid) * p.H + cur.h;
-        nbeta = tid < cur.nv ? p.beta[gi] : 0.f;
-        ndec = (tid < cur.nv && p.decay) ? p.decay[gi] : 0.f;
-    }
-    long pend = -1;   // thread 0: slot whose stores are in flight and not yet published
+    load_kq<D>(p, sKQ, cur, tid);
+    long pend = -1;     // thread 0: slot whose stores are in flight and not yet published
+    long staged = -1;   // thread 0: slot whose state-column blocks wait in the staging area
 
     for (uint32_t it = 0;; ++it) {
-        const uint32_t ph = it & 1;   // bar_tma completes once per chunk, bar_mma three times
+        const uint32_t ph = it & 1;   // bar_mma completes three times per chunk
         const int nv = cur.nv;
         if (tid < 64) {
-            mbeta[tid] = nbeta;
-            mdec[tid] = ndec;
+            const long gi = (cur.row0 + tid) * p.H + cur.h;
+            mbeta[tid] = tid < nv ? p.beta[gi] : 0.f;
+            mdec[tid] = (tid < nv && p.decay) ? p.decay[gi] : 0.f;
         }
+        cp_async_wait_all();   // this thread's share of q, k ...
+        fence_proxy_async();   // ... visible to the tensor core behind the barrier
         named_sync(bar, kGroupThreads);
+        bool ok = ctl->fail == 0;
+        if (tid == 0 && staged >= 0) {   // the previous chunk's state-column blocks of E_c
+            for (int kb = 0; kb < NB; ++kb)
+                tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
+            bulk_commit();
+            if (p.flags) pend = staged;
+            staged = -1;
+        }
+
+        // ---- MMA1: D1[0:128, 0:64] = [K; Q] K^T  (contraction over the head dim)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16_f32(128, 64, false, false);
+            const uint32_t a0 = smem_u32(sKQ);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16_ss(tm, desc_kmajor_sw128(a0, 128, ks), desc_kmajor_sw128(a0, 128, ks), id,
+                            ks > 0 ? 1u : 0u);
+            mma_commit(&ctl->bar_mma);
+        }
         if (warp == 0) {   // in-chunk cumulative log-decay: lane owns tokens 2 lane, 2 lane + 1
             const float d0 = mdec[2 * lane], d1 = mdec[2 * lane + 1];
             float incl = d0 + d1;
@@ -375,24 +471,6 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             mG[2 * lane] = excl + d0;
             mGp[2 * lane + 1] = excl + d0;
             mG[2 * lane + 1] = incl;
-        }
-        if (!mbar_wait(&ctl->bar_tma, ph, kWaitNs)) ctl->fail = 1;
-        named_sync(bar, kGroupThreads);
-        bool ok = ctl->fail == 0;
-
-        // ---- MMA1: D1[0:128, 0:64] = [K; Q] K^T  (contraction over the head dim)
-        if (tid == 0 && ok) {
-            tc_fence_after();
-            const uint32_t id = idesc_bf16_f32(128, 64, false, false);
-            const uint32_t a0 = smem_u32(sKQ);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16_ss(tm, desc_kmajor_sw128(a0, 128, ks), desc_kmajor_sw128(a0, 128, ks), id,
-                            ks > 0 ? 1u : 0u);
-            mma_commit(&ctl->bar_mma);
-            if (pend >= 0) {   // the previous chunk's stores have long been under way
-                publish_slot(p, pend);
-                pend = -1;
-            }
         }
         if (tid >= 128 && ok) {   // query norms: two threads per row (the swizzle permutes chunks only)
             const int t = (tid - 128) >> 1, part = tid & 1;
@@ -412,6 +490,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);
             if (part == 0) mqn[t] = p.use_l2 ? p.scale / fmaxf(sqrtf(ss), kNormEps) : p.scale;
         }
+        named_sync(bar, kGroupThreads);   // the log-decay prefix is in place
         if (tid < 64) meg[tid] = __expf(mG[tid]);
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
@@ -428,6 +507,9 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                     if (s == (i128 & 31)) diag = __uint_as_float(r[s]);
                 mkn[i128] = p.use_l2 ? 1.f / fmaxf(sqrtf(diag), kNormEps) : 1.f;
             }
+            // the previous chunk's E_c stores must have read the staging area before
+            // it is overwritten behind this barrier
+            if (tid == 0) bulk_wait_read0();
             named_sync(bar, kGroupThreads);
             const float gC = mG[63];
             if (i128 < 64) {
@@ -588,11 +670,15 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         named_sync(bar, kGroupThreads);
         ok = ctl->fail == 0;
 
+        // ---- next chunk of this group
+        long nitem = item + stride;
+        ChunkItem nx;
+        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
+        const bool more = nitem < p.n_items;
+
         // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64);
-        // meanwhile the V-column block of E_c goes out by TMA
+        // then the V-column block of E_c goes out by TMA
         if (tid == 0 && ok) {
-            tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, (int)cur.slot);
-            bulk_commit();
             tc_fence_after();
             const uint32_t ida = idesc_bf16_f32(D, D, false, true);
             const uint32_t idb = idesc_bf16_f32(64, D, false, true);
@@ -604,9 +690,14 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                 mma_bf16_ss(tm + 128, desc_kmajor_sw128(z2, 64, ks), desc_mnmajor_sw128(kq, 128, ks),
                             idb, ks > 0 ? 1u : 0u);
             mma_commit(&ctl->bar_mma);
+            tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, (int)cur.slot);
+            bulk_commit();
         }
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
+        // [K;Q] is free once MMA3 has read it (epilogue 3 takes q from global memory):
+        // the next chunk's q, k load starts now
+        if (ok && more) load_kq<D>(p, sKQ, nx, tid);
 
         // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
         {
@@ -637,10 +728,16 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             }
             const int t = i64;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j]
             const float qs = has64 ? meg[t] * mqn[t] : 0.f;
+            const bool qrow = has64 && t < nv;   // past the sequence's end q is taken as 0
+            const uint4 *qg = reinterpret_cast<const uint4 *>(p.q + ((cur.row0 + t) * p.H + cur.h) * D);
 #pragma unroll
             for (int c0 = 0; c0 < HALF; c0 += 32) {
                 uint32_t v[32];
                 const int col = hh * HALF + c0;
+                uint4 qw4[4];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    qw4[cc] = qrow ? __ldg(qg + (col >> 3) + cc) : make_uint4(0u, 0u, 0u, 0u);
                 tmem_ld32(tm + tq + 128 + col, v);
                 tmem_ld_wait();
                 if (has64) {
@@ -648,9 +745,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                     uint8_t *dst = sEst + (col >> 6) * (R * 128) + rr * 128;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        const int j0 = col + cc * 8;   // 8 consecutive head-dim indices: one chunk of q
-                        const uint4 qw = *reinterpret_cast<const uint4 *>(
-                            sKQ + (j0 >> 6) * 16384 + 8192 + t * 128 + ((((j0 & 63) >> 3) ^ (t & 7)) << 4));
+                        const uint4 qw = qw4[cc];   // head-dim indices col + 8 cc .. + 7
                         const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
                         float f[8];
 #pragma unroll
@@ -665,35 +760,34 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             }
         }
 
-        // ---- next chunk of this group: its scalars are fetched while this one finishes
-        long nitem = item + stride;
-        ChunkItem nx;
-        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
-        const bool more = nitem < p.n_items;
-        if (more && tid < 64) {
-            const long gi = (nx.row0 + tid) * p.H + nx.h;
-            nbeta = tid < nx.nv ? p.beta[gi] : 0.f;
-            ndec = (tid < nx.nv && p.decay) ? p.decay[gi] : 0.f;
-        }
         fence_proxy_async();
         tc_fence_before();
         named_sync(bar, kGroupThreads);
         const bool failed = ctl->fail != 0;
         if (tid == 0) {
             if (failed) record_error(p.ws, 1);
-            for (int kb = 0; kb < NB; ++kb)   // the state-column blocks of E_c
-                tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)cur.slot);
-            bulk_commit();
-            if (more && !failed)   // [K;Q] is free: every read of it is behind the barrier
-                load_kq<NB>(map_q, map_k, sKQ, &ctl->bar_tma, nx);
-            bulk_wait_read0();     // the staging area must stay valid until the stores have read it
-            if (p.flags) pend = cur.slot;
+            if (pend >= 0) {   // all but this chunk's V-block store group are complete
+                bulk_wait1();
+                release_slot(p, pend);
+                pend = -1;
+            }
+            staged = cur.slot;   // stored once the next chunk has started
         }
         if (!more || failed) break;
         item = nitem;
         cur = nx;
     }
-    if (tid == 0 && pend >= 0) publish_slot(p, pend);
+    cp_async_wait_all();
+    if (tid == 0) {   // the last chunk's state-column blocks; shared memory must outlive the stores
+        for (int kb = 0; kb < NB; ++kb)
+            tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
+        bulk_commit();
+        bulk_wait0();
+        if (p.flags) {
+            if (pend >= 0) release_slot(p, pend);
+            release_slot(p, staged);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------------
@@ -1012,7 +1106,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     uint8_t *gsm = sm + grp * PrepSmem<D>::GROUP;
     if ((tid & (kGroupThreads - 1)) == 0) {
         PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(gsm + PrepSmem<D>::CTRL);
-        mbar_init(&ctl->bar_tma, 1);
         mbar_init(&ctl->bar_mma, 1);
         fence_mbar_init();
         ctl->fail = 0;
@@ -1107,6 +1200,9 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.cu_seqlens = a.cu_seqlens;
     p.nc_equal = (a.T + kC - 1) / kC;
     p.beta = a.beta; p.decay = a.decay; p.h0 = a.h0; p.hT = a.hT;
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.k = static_cast<const __nv_bfloat16 *>(a.k);
+    p.rows = total_rows;
     p.o = static_cast<__nv_bfloat16 *>(a.o);
     p.ws = a.ws;
     uint8_t *body = static_cast<uint8_t *>(a.ws_body);

@@ -118,6 +118,7 @@ __device__ __forceinline__ void bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait1() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 // Order this thread's generic-proxy shared-memory writes before later async-proxy
 // (TMA / tcgen05) reads of the same memory.
 __device__ __forceinline__ void fence_proxy_async() {
