@@ -17,6 +17,7 @@ on the data path) and rank 0 reports the aggregate over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -37,7 +38,8 @@ NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes (read + write) per launch from one ncu capture of the kernel as it is
 # now; set to None whenever that kernel changes until it is captured again.
 #   decode: profiles/decode_scan_kernel_b256_h32_d128.md
-NCU_TRAFFIC = {"decode": 543.35e6 + 478.43e6, "prefill": None}
+#   prefill: profiles/tc_kernel_long_prefill_d128.md
+NCU_TRAFFIC = {"decode": 543.35e6 + 478.43e6, "prefill": 863.00e6 + 1.43e9}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -149,11 +151,27 @@ def to_dev(x, dev, dtype):
 
 
 # --------------------------------------------------------------------------- prefill
+def prefill_workload(args):
+    """The long-sequence workload, or the same with T overridden (profiling captures only)."""
+    wl = WORKLOADS[3]
+    if args.prefill_T:
+        wl = dataclasses.replace(wl, T=args.prefill_T, name=f"{wl.name} [T overridden: {args.prefill_T}]")
+    return wl
+
+
+def tc_prefill_launches(B, H, dev):
+    """Kernels of ours per tensor-core chunked prefill call: one when the (sequence, head)
+    pairs fit in half of the SMs (single cooperative launch), else prep + chain."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return 1 if B * H <= sms // 2 else 2
+
+
 def bench_prefill(args, world, rank, dev, peaks, d):
     import torch
     import delta_rule_linear_gb300 as kda
 
-    wl = WORKLOADS[3]
+    wl = prefill_workload(args)
     q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
     beta, decay, h0 = (to_dev(d[n], dev, torch.float32) for n in ("beta", "decay", "h0"))
     B, T, H, dk, dv, C = wl.B, wl.T, wl.H, wl.dk, wl.dv, wl.chunk
@@ -226,12 +244,12 @@ def bench_prefill(args, world, rank, dev, peaks, d):
         "clocks": clk.summary(),
         "roofline": {"bound": "tensor", "achieved": round(achieved_tf, 3), "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 5), "traffic": NCU_TRAFFIC["prefill"],
-                     "kernel": "chunk prefill (whole step)",
+                     "kernel": "tc_kernel (the whole step: one launch holds the prep groups and the chains)",
                      "flops_per_launch": flops,
                      "hbm_frac_of_min_bytes": round(min_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5)},
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps * 1,
+        "gpu_launches": args.steps * tc_prefill_launches(B, H, dev),
         "shape": dict(B=B, T=T, H=H, dk=dk, dv=dv, chunk=C),
     }
 
@@ -346,6 +364,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="run one workload (profiling); the default runs both")
+    ap.add_argument("--prefill-T", type=int, default=0,
+                    help="profiling only: override T of the prefill workload (no CPU baseline)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -356,9 +376,9 @@ def main():
 
     # inputs of the prefill workload are drawn once; the CPU baseline runs on them
     # first, before any CUDA work starts in this process
-    d = make_prefill(WORKLOADS[3], seed=rank) if args.only != "decode" else None
+    d = make_prefill(prefill_workload(args), seed=rank) if args.only != "decode" else None
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and d is not None:
+    if rank == 0 and not args.no_cpu_baseline and not args.prefill_T and d is not None:
         import oracle
         oracle.build()
         heads = WORKLOADS[3].H
@@ -386,7 +406,7 @@ def main():
     if pre is None:
         print(json.dumps({"metric": METRIC, "workload": "decode only", "decode": dec}), flush=True)
         return
-    wl = WORKLOADS[3]
+    wl = prefill_workload(args)
     pre["roofline"]["peak_source"] = peak_src
     line = {
         "metric": METRIC, "value": pre["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
