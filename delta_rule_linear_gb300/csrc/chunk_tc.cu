@@ -472,14 +472,16 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             mGp[2 * lane + 1] = excl + d0;
             mG[2 * lane + 1] = incl;
         }
-        if (tid >= 128 && ok) {   // query norms: two threads per row (the swizzle permutes chunks only)
+        if (tid >= 128 && ok) {   // query norms: two threads per row, each summing half of its chunks
             const int t = (tid - 128) >> 1, part = tid & 1;
             float ss = 0.f;
 #pragma unroll
             for (int cc = 0; cc < NB * 4; ++cc) {
+                // logical chunk `chunk` sits at (chunk ^ t) % 8 in its block; reading that slot
+                // keeps the eight rows of a warp on eight different bank groups
                 const int chunk = part * NB * 4 + cc;
                 const uint4 w = *reinterpret_cast<const uint4 *>(sKQ + (chunk >> 3) * 16384 + 8192 +
-                                                                 t * 128 + ((chunk & 7) << 4));
+                                                                 t * 128 + (((chunk ^ t) & 7) << 4));
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -693,6 +695,17 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, (int)cur.slot);
             bulk_commit();
         }
+        // q of this thread's output row for epilogue 3, fetched (from L2) while MMA3 runs
+        constexpr int QP = D / 16;   // 16-byte pieces of half a row
+        uint4 qpre[QP];
+        {
+            const int t = i64;
+            const bool qrow = has64 && t < nv;   // past the sequence's end q is taken as 0
+            const uint4 *qg = reinterpret_cast<const uint4 *>(p.q + ((cur.row0 + t) * p.H + cur.h) * D) +
+                              hh * QP;
+#pragma unroll
+            for (int e = 0; e < QP; ++e) qpre[e] = qrow ? __ldg(qg + e) : make_uint4(0u, 0u, 0u, 0u);
+        }
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
         // [K;Q] is free once MMA3 has read it (epilogue 3 takes q from global memory):
@@ -700,11 +713,38 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         if (ok && more) load_kq<D>(p, sKQ, nx, tid);
 
         // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
+        // (the q~ rows first, so that the prefetched q is dead before the K~^T W rows)
         {
             constexpr int HALF = D / 2;
             const float gamma_c = meg[63];
             const bool has_row = (D == 128) || has64;
             const int i = (D == 128) ? i128 : i64;
+            const int t = i64;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j]
+            const float qs = has64 ? meg[t] * mqn[t] : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < HALF; c0 += 32) {
+                uint32_t v[32];
+                const int col = hh * HALF + c0;
+                tmem_ld32(tm + tq + 128 + col, v);
+                tmem_ld_wait();
+                if (has64) {
+                    const int rr = D + t;
+                    uint8_t *dst = sEst + (col >> 6) * (R * 128) + rr * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint4 qw = qpre[(c0 >> 3) + cc];   // head-dim indices col + 8 cc .. + 7
+                        const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            f[2 * e] = qs * bf16lo(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e]);
+                            f[2 * e + 1] = qs * bf16hi(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e + 1]);
+                        }
+                        const int chunk = ((col & 63) >> 3) + cc;
+                        *reinterpret_cast<uint4 *>(dst + ((chunk ^ (rr & 7)) << 4)) = pack8(f);
+                    }
+                }
+            }
 #pragma unroll
             for (int c0 = 0; c0 < HALF; c0 += 32) {   // E[i][j] = gamma_C delta_ij - (K~^T W)[i][j]
                 uint32_t v[32];
@@ -723,38 +763,6 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                         }
                         const int chunk = ((col & 63) >> 3) + cc;
                         *reinterpret_cast<uint4 *>(dst + ((chunk ^ (i & 7)) << 4)) = pack8(f);
-                    }
-                }
-            }
-            const int t = i64;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j]
-            const float qs = has64 ? meg[t] * mqn[t] : 0.f;
-            const bool qrow = has64 && t < nv;   // past the sequence's end q is taken as 0
-            const uint4 *qg = reinterpret_cast<const uint4 *>(p.q + ((cur.row0 + t) * p.H + cur.h) * D);
-#pragma unroll
-            for (int c0 = 0; c0 < HALF; c0 += 32) {
-                uint32_t v[32];
-                const int col = hh * HALF + c0;
-                uint4 qw4[4];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    qw4[cc] = qrow ? __ldg(qg + (col >> 3) + cc) : make_uint4(0u, 0u, 0u, 0u);
-                tmem_ld32(tm + tq + 128 + col, v);
-                tmem_ld_wait();
-                if (has64) {
-                    const int rr = D + t;
-                    uint8_t *dst = sEst + (col >> 6) * (R * 128) + rr * 128;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const uint4 qw = qw4[cc];   // head-dim indices col + 8 cc .. + 7
-                        const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            f[2 * e] = qs * bf16lo(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e]);
-                            f[2 * e + 1] = qs * bf16hi(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e + 1]);
-                        }
-                        const int chunk = ((col & 63) >> 3) + cc;
-                        *reinterpret_cast<uint4 *>(dst + ((chunk ^ (rr & 7)) << 4)) = pack8(f);
                     }
                 }
             }
