@@ -155,8 +155,7 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 // kLP = 68 floats: 16-byte aligned rows), by the NT = 256 threads of one group (named
 // barrier `bar`), on the 4 x 4 grid of 16 x 16 blocks:
 //  * the diagonal blocks T_ii by forward substitution, one lane per column, the column
-//    in registers, right-looking (x_s, once final, is subtracted from every later row,
-//    so the dependent chain is one FMA per row);
+//    in registers, each row of L read with 16-byte loads;
 //  * the off-diagonal blocks  T_ij = -T_ii X_ij,  X_ij = sum_{k=j}^{i-1} L_ik T_kj,
 //    with X_ij accumulated as soon as each T_kj is known: six steps
 //      X_10 X_21 X_32 X_20 | T_10 T_21 T_32, X_31 | X_20 X_31 X_30 | T_20 T_31 | X_30 | T_30
@@ -254,19 +253,30 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid, int bar) {
     constexpr int P = kLP;
     const int warp = tid >> 5, lane = tid & 31;
     if (warp < 4 && lane < 16) {
-        // diagonal block `warp`, column j = lane: x_r = delta_rj - sum_{s<r} L[r][s] x_s
+        // diagonal block `warp`, column j = lane: x_r = delta_rj - sum_{s<r} L[r][s] x_s, the
+        // row of L read with 16-byte loads (unrolled, so the terms with early x_s are summed
+        // while the later ones are still being computed)
         const int b0 = 16 * warp, j = lane;
-        float acc[16];
+        float x[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) acc[r] = (r == j) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) {
+            const float4 *Lr = reinterpret_cast<const float4 *>(sL + (b0 + r) * P + b0);
+            float l[16];
 #pragma unroll
-        for (int s = 0; s < 15; ++s) {
-            const float xs = acc[s];
+            for (int m4 = 0; m4 < (r + 3) / 4; ++m4) {
+                const float4 v = Lr[m4];
+                l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
+            }
+            float a0 = (r == j) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
-            for (int r = s + 1; r < 16; ++r) acc[r] = fmaf(-sL[(b0 + r) * P + b0 + s], xs, acc[r]);
+            for (int s = 0; s < r; ++s) {   // x_s = 0 for s < j
+                if (s & 1) a1 = fmaf(-l[s], x[s], a1);
+                else a0 = fmaf(-l[s], x[s], a0);
+            }
+            x[r] = a0 + a1;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = acc[r];
+        for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
     } else {
         // the other 192 threads zero the six strictly-upper 16 x 16 blocks of T
         const int zt = warp < 4 ? warp * 16 + (lane - 16) : 64 + (warp - 4) * 32 + lane;
@@ -357,15 +367,27 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
                  "r"(src_bytes)
                  : "memory");
 }
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // q, k of one chunk into the [K;Q] region (K-major SW128; k rows 0-63, q rows 64-127 of
-// each 64-column block) by 16-byte cp.async copies spread over the group's threads.
-// These go through the load path, not the TMA unit, where they would queue behind the
-// E_c stores.  Rows past the token array are filled with zeros.
+// each 64-column block) by 16-byte cp.async copies spread over the group's threads, and
+// its beta, decay (zero past the chunk's valid tokens, decay zero when absent) into the
+// per-token scalars.  These go through the load path, not the TMA unit, where they would
+// queue behind the E_c stores.  Rows past the token array are filled with zeros.
 template <int D>
-__device__ __forceinline__ void load_kq(const TcParams &p, uint8_t *sKQ, const ChunkItem &it, int tid) {
+__device__ __forceinline__ void load_kq(const TcParams &p, uint8_t *sKQ, float *mbeta, float *mdec,
+                                        const ChunkItem &it, int tid) {
+    if (tid < 64) {
+        const long gi = (it.row0 + (tid < it.nv ? tid : 0)) * p.H + it.h;
+        cp_async4(mbeta + tid, p.beta + gi, tid < it.nv ? 4u : 0u);
+        cp_async4(mdec + tid, p.decay ? p.decay + gi : p.beta + gi, (tid < it.nv && p.decay) ? 4u : 0u);
+    }
     constexpr int PPR = D / 8;                               // 16-byte pieces per row
     constexpr int PER = 2 * 64 * PPR / kGroupThreads;        // pieces per thread
 #pragma unroll
@@ -424,19 +446,14 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     ChunkItem cur;
     while (item < p.n_items && !item_info(p, item, cur)) item += stride;
     if (item >= p.n_items) return;
-    load_kq<D>(p, sKQ, cur, tid);
+    load_kq<D>(p, sKQ, mbeta, mdec, cur, tid);
     long pend = -1;     // thread 0: slot whose stores are in flight and not yet published
     long staged = -1;   // thread 0: slot whose state-column blocks wait in the staging area
 
     for (uint32_t it = 0;; ++it) {
         const uint32_t ph = it & 1;   // bar_mma completes three times per chunk
         const int nv = cur.nv;
-        if (tid < 64) {
-            const long gi = (cur.row0 + tid) * p.H + cur.h;
-            mbeta[tid] = tid < nv ? p.beta[gi] : 0.f;
-            mdec[tid] = (tid < nv && p.decay) ? p.decay[gi] : 0.f;
-        }
-        cp_async_wait_all();   // this thread's share of q, k ...
+        cp_async_wait_all();   // this thread's share of q, k, beta, decay ...
         fence_proxy_async();   // ... visible to the tensor core behind the barrier
         named_sync(bar, kGroupThreads);
         bool ok = ctl->fail == 0;
@@ -708,9 +725,17 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         }
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
+        // The previous chunk's E_c is complete in global memory (all but this chunk's V-block
+        // store group are done): publish it now, before this thread has loads in flight that
+        // the release would have to wait for.
+        if (tid == 0 && pend >= 0) {
+            bulk_wait1();
+            release_slot(p, pend);
+            pend = -1;
+        }
         // [K;Q] is free once MMA3 has read it (epilogue 3 takes q from global memory):
         // the next chunk's q, k load starts now
-        if (ok && more) load_kq<D>(p, sKQ, nx, tid);
+        if (ok && more) load_kq<D>(p, sKQ, mbeta, mdec, nx, tid);
 
         // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
         // (the q~ rows first, so that the prefetched q is dead before the K~^T W rows)
@@ -774,11 +799,6 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         const bool failed = ctl->fail != 0;
         if (tid == 0) {
             if (failed) record_error(p.ws, 1);
-            if (pend >= 0) {   // all but this chunk's V-block store group are complete
-                bulk_wait1();
-                release_slot(p, pend);
-                pend = -1;
-            }
             staged = cur.slot;   // stored once the next chunk has started
         }
         if (!more || failed) break;
