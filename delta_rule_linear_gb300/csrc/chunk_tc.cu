@@ -150,6 +150,44 @@ __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// B = [T' | P] and Bf = diag(f) B (bf16, MN-major SW128: row t, 64 columns s per half,
+// half 0 T' = T diag(w), half 1 P = T diag(beta)) for W consecutive columns s.. of row t
+// of T.  W = 4, 2, 1: 8-, 4- or 2-byte stores inside one 16-byte chunk.
+struct BTiles {
+    uint8_t *b, *bf;             // B, Bf: two 8 KB halves each
+    const float *w, *beta, *f;   // column weights of T', of P; row weights of Bf
+};
+
+template <int W>
+__device__ __forceinline__ void put_b(const BTiles &bt, int t, int s, const float *val) {
+    const float ft = bt.f[t];
+    float b0[W], b1[W];
+#pragma unroll
+    for (int e = 0; e < W; ++e) {
+        b0[e] = val[e] * bt.w[s + e];
+        b1[e] = val[e] * bt.beta[s + e];
+    }
+    const int off = t * 128 + ((((s >> 3) ^ t) & 7) << 4) + (s & 7) * 2;
+    if constexpr (W == 4) {
+        *reinterpret_cast<uint2 *>(bt.b + off) = make_uint2(pack_bf16(b0[0], b0[1]), pack_bf16(b0[2], b0[3]));
+        *reinterpret_cast<uint2 *>(bt.b + 8192 + off) = make_uint2(pack_bf16(b1[0], b1[1]), pack_bf16(b1[2], b1[3]));
+        *reinterpret_cast<uint2 *>(bt.bf + off) =
+            make_uint2(pack_bf16(b0[0] * ft, b0[1] * ft), pack_bf16(b0[2] * ft, b0[3] * ft));
+        *reinterpret_cast<uint2 *>(bt.bf + 8192 + off) =
+            make_uint2(pack_bf16(b1[0] * ft, b1[1] * ft), pack_bf16(b1[2] * ft, b1[3] * ft));
+    } else if constexpr (W == 2) {
+        *reinterpret_cast<uint32_t *>(bt.b + off) = pack_bf16(b0[0], b0[1]);
+        *reinterpret_cast<uint32_t *>(bt.b + 8192 + off) = pack_bf16(b1[0], b1[1]);
+        *reinterpret_cast<uint32_t *>(bt.bf + off) = pack_bf16(b0[0] * ft, b0[1] * ft);
+        *reinterpret_cast<uint32_t *>(bt.bf + 8192 + off) = pack_bf16(b1[0] * ft, b1[1] * ft);
+    } else {
+        *reinterpret_cast<__nv_bfloat16 *>(bt.b + off) = __float2bfloat16_rn(b0[0]);
+        *reinterpret_cast<__nv_bfloat16 *>(bt.b + 8192 + off) = __float2bfloat16_rn(b1[0]);
+        *reinterpret_cast<__nv_bfloat16 *>(bt.bf + off) = __float2bfloat16_rn(b0[0] * ft);
+        *reinterpret_cast<__nv_bfloat16 *>(bt.bf + 8192 + off) = __float2bfloat16_rn(b1[0] * ft);
+    }
+}
+
 // ---------------------------------------------------------------------------------
 // T = (I + L)^{-1} for a 64 x 64 strictly-lower L, fp32 in shared memory (row pitch
 // kLP = 68 floats: 16-byte aligned rows), by the NT = 256 threads of one group (named
@@ -213,9 +251,10 @@ __device__ __forceinline__ void inv_op_x(float *sL, const float *sT, int i, int 
     else X[0] = acc[0];
 }
 
-// T_ij[r][c0 .. c0+W) = -(T_ii X_ij)[r][c0 ..)
+// T_ij[r][c0 .. c0+W) = -(T_ii X_ij)[r][c0 ..), also written into B and Bf
 template <int W>
-__device__ __forceinline__ void inv_op_t(const float *sL, float *sT, int i, int j, int r, int c0) {
+__device__ __forceinline__ void inv_op_t(const float *sL, float *sT, const BTiles &bt, int i, int j,
+                                         int r, int c0) {
     constexpr int P = kLP;
     const float *Ar = sT + (16 * i + r) * P + 16 * i;
     float a[16];
@@ -241,14 +280,17 @@ __device__ __forceinline__ void inv_op_t(const float *sL, float *sT, int i, int 
             acc[0] = fmaf(a[m], Xr[0], acc[0]);
         }
     }
+#pragma unroll
+    for (int e = 0; e < W; ++e) acc[e] = -acc[e];
     float *Tij = sT + (16 * i + r) * P + 16 * j + c0;
-    if constexpr (W == 4) *reinterpret_cast<float4 *>(Tij) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-    else if constexpr (W == 2) *reinterpret_cast<float2 *>(Tij) = make_float2(-acc[0], -acc[1]);
-    else Tij[0] = -acc[0];
+    if constexpr (W == 4) *reinterpret_cast<float4 *>(Tij) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    else if constexpr (W == 2) *reinterpret_cast<float2 *>(Tij) = make_float2(acc[0], acc[1]);
+    else Tij[0] = acc[0];
+    put_b<W>(bt, 16 * i + r, 16 * j + c0, acc);
 }
 
 template <int NT>
-__device__ void invert_unit_lower_64(float *sL, float *sT, int tid, int bar) {
+__device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int tid, int bar) {
     static_assert(NT == 256, "the work split below assumes 256 threads");
     constexpr int P = kLP;
     const int warp = tid >> 5, lane = tid & 31;
@@ -278,26 +320,33 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid, int bar) {
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
     } else {
-        // the other 192 threads zero the six strictly-upper 16 x 16 blocks of T
+        // the other 192 threads zero the six strictly-upper 16 x 16 blocks of B and Bf:
+        // 6 blocks x 16 rows x 2 chunks x 4 tiles (B, Bf; T' and P halves)
         const int zt = warp < 4 ? warp * 16 + (lane - 16) : 64 + (warp - 4) * 32 + lane;
-        for (int idx = zt; idx < 6 * 256; idx += NT - 64) {
-            const int blk = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
+        for (int idx = zt; idx < 6 * 16 * 2 * 4; idx += NT - 64) {
+            const int ch = idx & 1, r = (idx >> 1) & 15, blk = (idx >> 5) % 6, tile = idx / 192;
             const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);          // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
             const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            sT[(16 * bi + r) * P + 16 * bj + c] = 0.f;
+            const int t = 16 * bi + r;
+            uint8_t *base = (tile & 1 ? bt.bf : bt.b) + (tile >> 1) * 8192;
+            *reinterpret_cast<uint4 *>(base + t * 128 + ((((2 * bj + ch) ^ t) & 7) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
     }
     named_sync(bar, NT);
     const int slot = tid >> 6, t64 = tid & 63;
     const int r4 = t64 >> 2, c4 = (t64 & 3) * 4;          // 64 threads x 4 outputs
-    // S0: X_10, X_21, X_32, X_20 from the diagonal inverses
+    // S0: X_10, X_21, X_32, X_20 from the diagonal inverses; the diagonal blocks into B
     {
         const int i = slot == 3 ? 2 : slot + 1, j = slot == 3 ? 0 : slot;
         inv_op_x<4>(sL, sT, i, j, j, j + 1, false, r4, c4);
+        const float4 d = *reinterpret_cast<const float4 *>(sT + (16 * slot + r4) * P + 16 * slot + c4);
+        const float dv[4] = {d.x, d.y, d.z, d.w};
+        put_b<4>(bt, 16 * slot + r4, 16 * slot + c4, dv);
     }
     named_sync(bar, NT);
     // S1: T_10, T_21, T_32; X_31 = L_31 T_11
-    if (slot < 3) inv_op_t<4>(sL, sT, slot + 1, slot, r4, c4);
+    if (slot < 3) inv_op_t<4>(sL, sT, bt, slot + 1, slot, r4, c4);
     else inv_op_x<4>(sL, sT, 3, 1, 1, 2, false, r4, c4);
     named_sync(bar, NT);
     // S2: X_20 += L_21 T_10;  X_31 += L_32 T_21;  X_30 = L_30 T_00 + L_31 T_10 (two column halves)
@@ -312,15 +361,17 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, int tid, int bar) {
     {
         const int half = tid >> 7, t128 = tid & 127;
         const int r2 = t128 >> 3, c2 = (t128 & 7) * 2;
-        if (half == 0) inv_op_t<2>(sL, sT, 2, 0, r2, c2);
-        else inv_op_t<2>(sL, sT, 3, 1, r2, c2);
+        if (half == 0) inv_op_t<2>(sL, sT, bt, 2, 0, r2, c2);
+        else inv_op_t<2>(sL, sT, bt, 3, 1, r2, c2);
     }
     named_sync(bar, NT);
     // S4: X_30 += L_32 T_20 (one output per thread)
     inv_op_x<1>(sL, sT, 3, 0, 2, 3, true, tid >> 4, tid & 15);
     named_sync(bar, NT);
     // S5: T_30
-    inv_op_t<1>(sL, sT, 3, 0, tid >> 4, tid & 15);
+    inv_op_t<1>(sL, sT, bt, 3, 0, tid >> 4, tid & 15);
+    fence_proxy_async();   // B, Bf are tensor-core operands
+    tc_fence_before();
     named_sync(bar, NT);
 }
 
@@ -375,32 +426,36 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t s
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// q, k of one chunk into the [K;Q] region (K-major SW128; k rows 0-63, q rows 64-127 of
-// each 64-column block) by 16-byte cp.async copies spread over the group's threads, and
-// its beta, decay (zero past the chunk's valid tokens, decay zero when absent) into the
-// per-token scalars.  These go through the load path, not the TMA unit, where they would
-// queue behind the E_c stores.  Rows past the token array are filled with zeros.
+// q or k of one chunk into its rows of the [K;Q] region (K-major SW128; k rows 0-63, q rows
+// 64-127 of each 64-column block) by 16-byte cp.async copies spread over warps 1..7 of the
+// group (warp 0 keeps no loads in flight, so that thread 0's flag release never waits for
+// them).  These go through the load path, not the TMA unit, where they would queue behind
+// the E_c stores.  Rows past the token array are filled with zeros.
 template <int D>
-__device__ __forceinline__ void load_kq(const TcParams &p, uint8_t *sKQ, float *mbeta, float *mdec,
-                                        const ChunkItem &it, int tid) {
-    if (tid < 64) {
-        const long gi = (it.row0 + (tid < it.nv ? tid : 0)) * p.H + it.h;
-        cp_async4(mbeta + tid, p.beta + gi, tid < it.nv ? 4u : 0u);
-        cp_async4(mdec + tid, p.decay ? p.decay + gi : p.beta + gi, (tid < it.nv && p.decay) ? 4u : 0u);
-    }
+__device__ __forceinline__ void load_rows(const TcParams &p, uint8_t *sKQ, const ChunkItem &it,
+                                          int tid, bool q) {
     constexpr int PPR = D / 8;                               // 16-byte pieces per row
-    constexpr int PER = 2 * 64 * PPR / kGroupThreads;        // pieces per thread
-#pragma unroll
-    for (int m = 0; m < PER; ++m) {
-        const int pidx = tid + kGroupThreads * m;
-        const int tensor = pidx / (64 * PPR);                // 0: k, 1: q
-        const int rem = pidx % (64 * PPR);
-        const int row = rem / PPR, pc = rem % PPR;
+    const __nv_bfloat16 *g = q ? p.q : p.k;
+    if (tid < 32) return;
+    for (int pidx = tid - 32; pidx < 64 * PPR; pidx += kGroupThreads - 32) {
+        const int row = pidx / PPR, pc = pidx % PPR;
         const long grow = it.row0 + row;
         const bool in = grow < p.rows;
-        const __nv_bfloat16 *src = (tensor ? p.q : p.k) + ((in ? grow : 0) * p.H + it.h) * D + 8 * pc;
-        uint8_t *dst = sKQ + (pc >> 3) * 16384 + tensor * 8192 + row * 128 + (((pc & 7) ^ (row & 7)) << 4);
+        const __nv_bfloat16 *src = g + ((in ? grow : 0) * p.H + it.h) * D + 8 * pc;
+        uint8_t *dst = sKQ + (pc >> 3) * 16384 + (q ? 8192 : 0) + row * 128 + (((pc & 7) ^ (row & 7)) << 4);
         cp_async16(dst, src, in ? 16u : 0u);
+    }
+    cp_async_commit();
+}
+// beta, decay of one chunk into the per-token scalars (zero past the chunk's valid tokens;
+// decay zero when absent)
+__device__ __forceinline__ void load_scalars(const TcParams &p, float *mbeta, float *mdec,
+                                             const ChunkItem &it, int tid) {
+    const int t = tid - 64;   // warps 2, 3
+    if (t >= 0 && t < 64) {
+        const long gi = (it.row0 + (t < it.nv ? t : 0)) * p.H + it.h;
+        cp_async4(mbeta + t, p.beta + gi, t < it.nv ? 4u : 0u);
+        cp_async4(mdec + t, p.decay ? p.decay + gi : p.beta + gi, (t < it.nv && p.decay) ? 4u : 0u);
     }
     cp_async_commit();
 }
@@ -446,7 +501,9 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     ChunkItem cur;
     while (item < p.n_items && !item_info(p, item, cur)) item += stride;
     if (item >= p.n_items) return;
-    load_kq<D>(p, sKQ, mbeta, mdec, cur, tid);
+    load_rows<D>(p, sKQ, cur, tid, true);
+    load_rows<D>(p, sKQ, cur, tid, false);
+    load_scalars(p, mbeta, mdec, cur, tid);
     long pend = -1;     // thread 0: slot whose stores are in flight and not yet published
     long staged = -1;   // thread 0: slot whose state-column blocks wait in the staging area
 
@@ -457,8 +514,12 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         fence_proxy_async();   // ... visible to the tensor core behind the barrier
         named_sync(bar, kGroupThreads);
         bool ok = ctl->fail == 0;
-        if (tid == 0 && staged >= 0) {   // the previous chunk's state-column blocks of E_c
-            for (int kb = 0; kb < NB; ++kb)
+        long nitem = item + stride;   // this group's next chunk
+        ChunkItem nx;
+        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
+        const bool more = nitem < p.n_items;
+        if (tid == 0 && staged >= 0) {   // the previous chunk's E_c, one bulk group
+            for (int kb = 0; kb <= NB; ++kb)
                 tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
             bulk_commit();
             if (p.flags) pend = staged;
@@ -530,6 +591,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             // it is overwritten behind this barrier
             if (tid == 0) bulk_wait_read0();
             named_sync(bar, kGroupThreads);
+            // MMA1 and the query norms are done with q: the next chunk's q load starts now
+            if (ok && more) load_rows<D>(p, sKQ, nx, tid, true);
             const float gC = mG[63];
             if (i128 < 64) {
                 const int t = i128;
@@ -589,45 +652,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         named_sync(bar, kGroupThreads);
         ok = ctl->fail == 0;
 
-        // ---- T = (I + L)^{-1}
-        invert_unit_lower_64<kGroupThreads>(sL, sT, tid, bar);
-
-        // ---- B = [T' | P], Bf = diag(f) B   (MN-major: row t, columns s); 4 threads per row
-        {
-            const int t = tid >> 2, half = (tid >> 1) & 1, grp = tid & 1;
-            const float *Trow = sT + t * kLP;
-            const float ft = mf[t];
-            const float *w = half ? mbeta : mcw;
-            uint8_t *dB = sB + half * 8192 + t * 128;
-            uint8_t *dBf = sBf + half * 8192 + t * 128;
-            float tv[32], wv[32];   // this thread's 32 columns, loaded before use
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float4 a = reinterpret_cast<const float4 *>(Trow + grp * 32)[e];
-                tv[4 * e] = a.x; tv[4 * e + 1] = a.y; tv[4 * e + 2] = a.z; tv[4 * e + 3] = a.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float4 a = reinterpret_cast<const float4 *>(w + grp * 32)[e];
-                wv[4 * e] = a.x; wv[4 * e + 1] = a.y; wv[4 * e + 2] = a.z; wv[4 * e + 3] = a.w;
-            }
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int chunk = grp * 4 + cc;
-                float f[8], fb[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    f[e] = tv[cc * 8 + e] * wv[cc * 8 + e];
-                    fb[e] = f[e] * ft;
-                }
-                const int off = (chunk ^ (t & 7)) << 4;
-                *reinterpret_cast<uint4 *>(dB + off) = pack8(f);
-                *reinterpret_cast<uint4 *>(dBf + off) = pack8(fb);
-            }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        named_sync(bar, kGroupThreads);
+        // ---- T = (I + L)^{-1}, written as B = [T' | P], Bf = diag(f) B (MN-major: row t, columns s)
+        invert_unit_lower_64<kGroupThreads>(sL, sT, BTiles{sB, sBf, mcw, mbeta, mf}, tid, bar);
 
         // ---- MMA2: D2a[:, 0:128] = K^T diag(f) [T'|P]  (M = D);  D2b[:, 128:256] = Aqk [T'|P]
         if (tid == 0 && ok) {
@@ -689,14 +715,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         named_sync(bar, kGroupThreads);
         ok = ctl->fail == 0;
 
-        // ---- next chunk of this group
-        long nitem = item + stride;
-        ChunkItem nx;
-        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
-        const bool more = nitem < p.n_items;
-
-        // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64);
-        // then the V-column block of E_c goes out by TMA
+        // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64)
         if (tid == 0 && ok) {
             tc_fence_after();
             const uint32_t ida = idesc_bf16_f32(D, D, false, true);
@@ -709,8 +728,6 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                 mma_bf16_ss(tm + 128, desc_kmajor_sw128(z2, 64, ks), desc_mnmajor_sw128(kq, 128, ks),
                             idb, ks > 0 ? 1u : 0u);
             mma_commit(&ctl->bar_mma);
-            tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, (int)cur.slot);
-            bulk_commit();
         }
         // q of this thread's output row for epilogue 3, fetched (from L2) while MMA3 runs
         constexpr int QP = D / 16;   // 16-byte pieces of half a row
@@ -725,17 +742,12 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         }
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
-        // The previous chunk's E_c is complete in global memory (all but this chunk's V-block
-        // store group are done): publish it now, before this thread has loads in flight that
-        // the release would have to wait for.
-        if (tid == 0 && pend >= 0) {
-            bulk_wait1();
-            release_slot(p, pend);
-            pend = -1;
+        // the k rows are free once MMA3 has read them, beta and decay after the inverse:
+        // the rest of the next chunk's load starts now
+        if (ok && more) {
+            load_rows<D>(p, sKQ, nx, tid, false);
+            load_scalars(p, mbeta, mdec, nx, tid);
         }
-        // [K;Q] is free once MMA3 has read it (epilogue 3 takes q from global memory):
-        // the next chunk's q, k load starts now
-        if (ok && more) load_kq<D>(p, sKQ, mbeta, mdec, nx, tid);
 
         // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
         // (the q~ rows first, so that the prefetched q is dead before the K~^T W rows)
@@ -799,6 +811,11 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         const bool failed = ctl->fail != 0;
         if (tid == 0) {
             if (failed) record_error(p.ws, 1);
+            if (pend >= 0) {   // the previous chunk's E_c, stored since this chunk's start
+                bulk_wait0();
+                release_slot(p, pend);
+                pend = -1;
+            }
             staged = cur.slot;   // stored once the next chunk has started
         }
         if (!more || failed) break;
@@ -806,8 +823,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         cur = nx;
     }
     cp_async_wait_all();
-    if (tid == 0) {   // the last chunk's state-column blocks; shared memory must outlive the stores
-        for (int kb = 0; kb < NB; ++kb)
+    if (tid == 0) {   // the last chunk's E_c; shared memory must outlive the stores
+        for (int kb = 0; kb <= NB; ++kb)
             tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
         bulk_commit();
         bulk_wait0();
