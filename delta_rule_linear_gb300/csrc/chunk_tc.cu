@@ -518,8 +518,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         ChunkItem nx;
         while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
         const bool more = nitem < p.n_items;
-        if (tid == 0 && staged >= 0) {   // the previous chunk's E_c, one bulk group
-            for (int kb = 0; kb <= NB; ++kb)
+        if (tid == 0 && staged >= 0) {   // the previous chunk's state-column blocks of E_c
+            for (int kb = 0; kb < NB; ++kb)
                 tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
             bulk_commit();
             if (p.flags) pend = staged;
@@ -715,7 +715,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         named_sync(bar, kGroupThreads);
         ok = ctl->fail == 0;
 
-        // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64)
+        // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64);
+        // then the V-column block of E_c goes out by TMA, to drain during epilogue 3
         if (tid == 0 && ok) {
             tc_fence_after();
             const uint32_t ida = idesc_bf16_f32(D, D, false, true);
@@ -728,6 +729,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                 mma_bf16_ss(tm + 128, desc_kmajor_sw128(z2, 64, ks), desc_mnmajor_sw128(kq, 128, ks),
                             idb, ks > 0 ? 1u : 0u);
             mma_commit(&ctl->bar_mma);
+            tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, (int)cur.slot);
+            bulk_commit();
         }
         // q of this thread's output row for epilogue 3, fetched (from L2) while MMA3 runs
         constexpr int QP = D / 16;   // 16-byte pieces of half a row
@@ -811,8 +814,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         const bool failed = ctl->fail != 0;
         if (tid == 0) {
             if (failed) record_error(p.ws, 1);
-            if (pend >= 0) {   // the previous chunk's E_c, stored since this chunk's start
-                bulk_wait0();
+            if (pend >= 0) {   // the previous chunk's E_c: all groups but this chunk's V block are done
+                bulk_wait1();
                 release_slot(p, pend);
                 pend = -1;
             }
@@ -823,8 +826,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         cur = nx;
     }
     cp_async_wait_all();
-    if (tid == 0) {   // the last chunk's E_c; shared memory must outlive the stores
-        for (int kb = 0; kb <= NB; ++kb)
+    if (tid == 0) {   // the last chunk's state columns; shared memory must outlive the stores
+        for (int kb = 0; kb < NB; ++kb)
             tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
         bulk_commit();
         bulk_wait0();
