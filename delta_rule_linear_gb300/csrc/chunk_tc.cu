@@ -289,8 +289,9 @@ __device__ __forceinline__ void inv_op_t(const float *sL, float *sT, const BTile
     put_b<W>(bt, 16 * i + r, 16 * j + c0, acc);
 }
 
-template <int NT>
-__device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int tid, int bar) {
+template <int NT, typename IdleWork>
+__device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int tid, int bar,
+                                     IdleWork &&idle) {
     static_assert(NT == 256, "the work split below assumes 256 threads");
     constexpr int P = kLP;
     const int warp = tid >> 5, lane = tid & 31;
@@ -332,6 +333,7 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
             *reinterpret_cast<uint4 *>(base + t * 128 + ((((2 * bj + ch) ^ t) & 7) << 4)) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
+        idle();   // work of the caller's that fits in the substitution's shadow
     }
     named_sync(bar, NT);
     const int slot = tid >> 6, t64 = tid & 63;
@@ -395,6 +397,10 @@ __device__ __forceinline__ uint4 pack8u(const uint32_t *u) {
 // ---------------------------------------------------------------------------------
 constexpr int kGroupThreads = 256;
 constexpr int kTcThreads = 512;               // prep: two groups; chain: 14 warps used
+// The group's thread that issues the E_c stores, waits for them and publishes E_c: it sits
+// in warp 4, which is idle for most of the diagonal-block inverse, where the gpu-scope
+// release (over a thousand cycles) is hidden; warp 4 issues no other loads.
+constexpr int kStoreThread = 128;
 
 template <int D>
 struct PrepSmem {
@@ -427,17 +433,19 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // q or k of one chunk into its rows of the [K;Q] region (K-major SW128; k rows 0-63, q rows
-// 64-127 of each 64-column block) by 16-byte cp.async copies spread over warps 1..7 of the
-// group (warp 0 keeps no loads in flight, so that thread 0's flag release never waits for
-// them).  These go through the load path, not the TMA unit, where they would queue behind
-// the E_c stores.  Rows past the token array are filled with zeros.
+// 64-127 of each 64-column block) by 16-byte cp.async copies spread over the group's warps
+// other than 0 (the MMA issuer) and 4 (the store thread, whose flag release would wait for
+// loads in flight).  These go through the load path, not the TMA unit, where they would
+// queue behind the E_c stores.  Rows past the token array are filled with zeros.
 template <int D>
 __device__ __forceinline__ void load_rows(const TcParams &p, uint8_t *sKQ, const ChunkItem &it,
                                           int tid, bool q) {
     constexpr int PPR = D / 8;                               // 16-byte pieces per row
     const __nv_bfloat16 *g = q ? p.q : p.k;
-    if (tid < 32) return;
-    for (int pidx = tid - 32; pidx < 64 * PPR; pidx += kGroupThreads - 32) {
+    const int w = tid >> 5;
+    if (w == 0 || w == 4) return;
+    const int lt = (w < 4 ? tid - 32 : tid - 64);   // 0 .. 191
+    for (int pidx = lt; pidx < 64 * PPR; pidx += kGroupThreads - 64) {
         const int row = pidx / PPR, pc = pidx % PPR;
         const long grow = it.row0 + row;
         const bool in = grow < p.rows;
@@ -504,8 +512,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     load_rows<D>(p, sKQ, cur, tid, true);
     load_rows<D>(p, sKQ, cur, tid, false);
     load_scalars(p, mbeta, mdec, cur, tid);
-    long pend = -1;     // thread 0: slot whose stores are in flight and not yet published
-    long staged = -1;   // thread 0: slot whose state-column blocks wait in the staging area
+    long pend = -1;     // store thread: slot whose stores are in flight and not yet published
+    long staged = -1;   // store thread: slot whose state-column blocks wait in the staging area
 
     for (uint32_t it = 0;; ++it) {
         const uint32_t ph = it & 1;   // bar_mma completes three times per chunk
@@ -518,7 +526,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         ChunkItem nx;
         while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
         const bool more = nitem < p.n_items;
-        if (tid == 0 && staged >= 0) {   // the previous chunk's state-column blocks of E_c
+        if (tid == kStoreThread && staged >= 0) {   // the previous chunk's state-column blocks of E_c
             for (int kb = 0; kb < NB; ++kb)
                 tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
             bulk_commit();
@@ -589,7 +597,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             }
             // the previous chunk's E_c stores must have read the staging area before
             // it is overwritten behind this barrier
-            if (tid == 0) bulk_wait_read0();
+            if (tid == kStoreThread) bulk_wait_read0();
             named_sync(bar, kGroupThreads);
             // MMA1 and the query norms are done with q: the next chunk's q load starts now
             if (ok && more) load_rows<D>(p, sKQ, nx, tid, true);
@@ -653,7 +661,13 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         ok = ctl->fail == 0;
 
         // ---- T = (I + L)^{-1}, written as B = [T' | P], Bf = diag(f) B (MN-major: row t, columns s)
-        invert_unit_lower_64<kGroupThreads>(sL, sT, BTiles{sB, sBf, mcw, mbeta, mf}, tid, bar);
+        invert_unit_lower_64<kGroupThreads>(sL, sT, BTiles{sB, sBf, mcw, mbeta, mf}, tid, bar, [&] {
+            if (tid == kStoreThread && pend >= 0) {   // the previous chunk's E_c: its stores
+                bulk_wait0();                         // (this chunk's start, previous MMA3) are done
+                release_slot(p, pend);
+                pend = -1;
+            }
+        });
 
         // ---- MMA2: D2a[:, 0:128] = K^T diag(f) [T'|P]  (M = D);  D2b[:, 128:256] = Aqk [T'|P]
         if (tid == 0 && ok) {
@@ -715,8 +729,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         named_sync(bar, kGroupThreads);
         ok = ctl->fail == 0;
 
-        // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64);
-        // then the V-column block of E_c goes out by TMA, to drain during epilogue 3
+        // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64)
         if (tid == 0 && ok) {
             tc_fence_after();
             const uint32_t ida = idesc_bf16_f32(D, D, false, true);
@@ -729,6 +742,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                 mma_bf16_ss(tm + 128, desc_kmajor_sw128(z2, 64, ks), desc_mnmajor_sw128(kq, 128, ks),
                             idb, ks > 0 ? 1u : 0u);
             mma_commit(&ctl->bar_mma);
+        }
+        if (tid == kStoreThread && ok) {   // the V-column block, to drain during MMA3 and epilogue 3
             tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, (int)cur.slot);
             bulk_commit();
         }
@@ -812,21 +827,14 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         tc_fence_before();
         named_sync(bar, kGroupThreads);
         const bool failed = ctl->fail != 0;
-        if (tid == 0) {
-            if (failed) record_error(p.ws, 1);
-            if (pend >= 0) {   // the previous chunk's E_c: all groups but this chunk's V block are done
-                bulk_wait1();
-                release_slot(p, pend);
-                pend = -1;
-            }
-            staged = cur.slot;   // stored once the next chunk has started
-        }
+        if (tid == 0 && failed) record_error(p.ws, 1);
+        if (tid == kStoreThread) staged = cur.slot;   // stored once the next chunk has started
         if (!more || failed) break;
         item = nitem;
         cur = nx;
     }
     cp_async_wait_all();
-    if (tid == 0) {   // the last chunk's state columns; shared memory must outlive the stores
+    if (tid == kStoreThread) {   // the last chunk's state columns; shared memory must outlive the stores
         for (int kb = 0; kb < NB; ++kb)
             tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
         bulk_commit();
