@@ -96,6 +96,12 @@ def _decay(rng, shape, kind):
     if kind == "long":
         x = z.astype(np.float64) - 4.0
         return (-np.logaddexp(0.0, x)).astype(np.float32)  # -softplus(N(-4, 1))
+    if kind == "strong":   # about -1.8 per token: a 64-token chunk spans far more than e^-80
+        return (-(1.0 + np.abs(z))).astype(np.float32)
+    if kind == "mixed":    # along T, 64-token blocks alternate between "train" and "strong"
+        t = np.arange(shape[1]).reshape((1, -1) + (1,) * (len(shape) - 2))
+        strong = (t // 64) % 2 == 1
+        return np.where(strong, -(1.0 + np.abs(z)), -0.05 * np.abs(z)).astype(np.float32)
     raise ValueError(kind)
 
 

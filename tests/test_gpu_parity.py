@@ -157,6 +157,18 @@ def test_head_dims(kda, oracle_mod, dev, dims, dtype):
         assert_parity(dtype, o, ro, h, rh, tag=f"dk={dk} dv={dv} rec={recurrent}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("decay", ["strong", "mixed"])
+def test_strong_decay(kda, oracle_mod, dev, D, decay):
+    """Chunks whose log-decay sum falls far below -80, where any factorisation of the decay
+    ratios exp(G_a - G_b) into per-token exponentials would overflow fp32; "mixed"
+    alternates such chunks with weakly decaying ones along the sequence."""
+    d = make_custom(2, 300, 2, D, D, dtype="bf16", decay=decay, h0="normal002", seed=D + len(decay))
+    o, h = _run_chunk(kda, d, dev, "bf16", 64)
+    ro, rh = oracle_mod.forward(d["q"], d["k"], d["v"], d["beta"], d["decay"], d["h0"])
+    assert_parity("bf16", o, ro, h, rh, tag=f"D={D} decay={decay}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_no_decay_no_state_no_l2_custom_scale(kda, oracle_mod, dev, dtype):
     d = make_custom(2, 100, 2, 64, 64, dtype=dtype, decay="none", h0="zero", seed=3,
