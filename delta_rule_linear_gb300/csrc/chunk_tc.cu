@@ -109,15 +109,17 @@ struct ChunkItem {
 // chains of the single-launch mode start as soon as the first chunks are built; slot
 // order is compact for varlen batches.  Returns false for an item past a sequence's end.
 __device__ __forceinline__ bool item_info(const TcParams &p, long item, ChunkItem &it) {
+    // item < (chunks x heads) < 2^31 (the E_c scratch bounds it), so 32-bit division is exact
+    const unsigned u = (unsigned)item;
     int n, c;
     if (p.chunk_major) {
-        const long j = item % p.nsh;
-        c = (int)(item / p.nsh);
-        n = (int)(j / p.H);
-        it.h = (int)(j % p.H);
+        const unsigned nsh = (unsigned)p.nsh, j = u % nsh;
+        c = (int)(u / nsh);
+        n = (int)(j / (unsigned)p.H);
+        it.h = (int)(j % (unsigned)p.H);
     } else {
-        const long g = item / p.H;
-        it.h = (int)(item % p.H);
+        const long g = (long)(u / (unsigned)p.H);
+        it.h = (int)(u % (unsigned)p.H);
         if (p.cu_seqlens) {
             if (g >= p.chunk_base[p.nseq]) return false;
             int lo = 0, hi = p.nseq;
@@ -144,6 +146,15 @@ __device__ __forceinline__ bool item_info(const TcParams &p, long item, ChunkIte
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// acc += a * b on a pair of floats by one paired fp32 FMA (each lane rounded as fmaf)
+__device__ __forceinline__ void fma2(float2 &acc, float2 a, float2 b) {
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%0, %1};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+}
 
 // Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(int id, int count) {
@@ -207,48 +218,54 @@ template <int W>
 __device__ __forceinline__ void inv_op_x(float *sL, const float *sT, int i, int j, int k0, int k1,
                                          bool accumulate, int r, int c0) {
     constexpr int P = kLP;
-    float acc[W];
     float *X = sL + (16 * j + r) * P + 16 * i + c0;
-    if (accumulate) {
-        if constexpr (W == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(X);
-            acc[0] = x.x; acc[1] = x.y; acc[2] = x.z; acc[3] = x.w;
-        } else if constexpr (W == 2) {
-            const float2 x = *reinterpret_cast<const float2 *>(X);
-            acc[0] = x.x; acc[1] = x.y;
+    if constexpr (W >= 2) {   // W/2 pairs of outputs, paired FMAs
+        float2 acc[W / 2];
+        if (accumulate) {
+#pragma unroll
+            for (int e = 0; e < W / 2; ++e) acc[e] = reinterpret_cast<const float2 *>(X)[e];
         } else {
-            acc[0] = X[0];
+#pragma unroll
+            for (int e = 0; e < W / 2; ++e) acc[e] = make_float2(0.f, 0.f);
         }
-    } else {
+        for (int k = k0; k < k1; ++k) {
+            const float *Lr = sL + (16 * i + r) * P + 16 * k;
+            float l[16];
 #pragma unroll
-        for (int e = 0; e < W; ++e) acc[e] = 0.f;
-    }
-    for (int k = k0; k < k1; ++k) {
-        const float *Lr = sL + (16 * i + r) * P + 16 * k;
-        float l[16];
+            for (int m4 = 0; m4 < 4; ++m4) {
+                const float4 v = *reinterpret_cast<const float4 *>(Lr + 4 * m4);
+                l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
+            }
 #pragma unroll
-        for (int m4 = 0; m4 < 4; ++m4) {
-            const float4 v = *reinterpret_cast<const float4 *>(Lr + 4 * m4);
-            l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
-        }
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float *Tr = sT + (16 * k + m) * P + 16 * j + c0;
-            if constexpr (W == 4) {
-                const float4 t = *reinterpret_cast<const float4 *>(Tr);
-                acc[0] = fmaf(l[m], t.x, acc[0]); acc[1] = fmaf(l[m], t.y, acc[1]);
-                acc[2] = fmaf(l[m], t.z, acc[2]); acc[3] = fmaf(l[m], t.w, acc[3]);
-            } else if constexpr (W == 2) {
-                const float2 t = *reinterpret_cast<const float2 *>(Tr);
-                acc[0] = fmaf(l[m], t.x, acc[0]); acc[1] = fmaf(l[m], t.y, acc[1]);
-            } else {
-                acc[0] = fmaf(l[m], Tr[0], acc[0]);
+            for (int m = 0; m < 16; ++m) {
+                const float2 *Tr = reinterpret_cast<const float2 *>(sT + (16 * k + m) * P + 16 * j + c0);
+                const float2 lm = make_float2(l[m], l[m]);
+                if constexpr (W == 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(Tr);
+                    fma2(acc[0], lm, make_float2(t.x, t.y));
+                    fma2(acc[1], lm, make_float2(t.z, t.w));
+                } else {
+                    fma2(acc[0], lm, Tr[0]);
+                }
             }
         }
+#pragma unroll
+        for (int e = 0; e < W / 2; ++e) reinterpret_cast<float2 *>(X)[e] = acc[e];
+    } else {
+        float acc = accumulate ? X[0] : 0.f;
+        for (int k = k0; k < k1; ++k) {
+            const float *Lr = sL + (16 * i + r) * P + 16 * k;
+            float l[16];
+#pragma unroll
+            for (int m4 = 0; m4 < 4; ++m4) {
+                const float4 v = *reinterpret_cast<const float4 *>(Lr + 4 * m4);
+                l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
+            }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc = fmaf(l[m], sT[(16 * k + m) * P + 16 * j + c0], acc);
+        }
+        X[0] = acc;
     }
-    if constexpr (W == 4) *reinterpret_cast<float4 *>(X) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    else if constexpr (W == 2) *reinterpret_cast<float2 *>(X) = make_float2(acc[0], acc[1]);
-    else X[0] = acc[0];
 }
 
 // T_ij[r][c0 .. c0+W) = -(T_ii X_ij)[r][c0 ..), also written into B and Bf
@@ -264,21 +281,31 @@ __device__ __forceinline__ void inv_op_t(const float *sL, float *sT, const BTile
         a[4 * m4] = v.x; a[4 * m4 + 1] = v.y; a[4 * m4 + 2] = v.z; a[4 * m4 + 3] = v.w;
     }
     float acc[W];
+    if constexpr (W >= 2) {
+        float2 pr[W / 2];
 #pragma unroll
-    for (int e = 0; e < W; ++e) acc[e] = 0.f;
+        for (int e = 0; e < W / 2; ++e) pr[e] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const float *Xr = sL + (16 * j + m) * P + 16 * i + c0;
-        if constexpr (W == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(Xr);
-            acc[0] = fmaf(a[m], x.x, acc[0]); acc[1] = fmaf(a[m], x.y, acc[1]);
-            acc[2] = fmaf(a[m], x.z, acc[2]); acc[3] = fmaf(a[m], x.w, acc[3]);
-        } else if constexpr (W == 2) {
-            const float2 x = *reinterpret_cast<const float2 *>(Xr);
-            acc[0] = fmaf(a[m], x.x, acc[0]); acc[1] = fmaf(a[m], x.y, acc[1]);
-        } else {
-            acc[0] = fmaf(a[m], Xr[0], acc[0]);
+        for (int m = 0; m < 16; ++m) {
+            const float2 *Xr = reinterpret_cast<const float2 *>(sL + (16 * j + m) * P + 16 * i + c0);
+            const float2 am = make_float2(a[m], a[m]);
+            if constexpr (W == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(Xr);
+                fma2(pr[0], am, make_float2(x.x, x.y));
+                fma2(pr[1], am, make_float2(x.z, x.w));
+            } else {
+                fma2(pr[0], am, Xr[0]);
+            }
         }
+#pragma unroll
+        for (int e = 0; e < W / 2; ++e) {
+            acc[2 * e] = pr[e].x;
+            acc[2 * e + 1] = pr[e].y;
+        }
+    } else {
+        acc[0] = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc[0] = fmaf(a[m], sL[(16 * j + m) * P + 16 * i + c0], acc[0]);
     }
 #pragma unroll
     for (int e = 0; e < W; ++e) acc[e] = -acc[e];
@@ -310,13 +337,12 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
                 const float4 v = Lr[m4];
                 l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
             }
-            float a0 = (r == j) ? 1.f : 0.f, a1 = 0.f;
+            float2 acc = make_float2(0.f, 0.f);   // sum_{s<r} L[r][s] x_s, by pairs of s
 #pragma unroll
-            for (int s = 0; s < r; ++s) {   // x_s = 0 for s < j
-                if (s & 1) a1 = fmaf(-l[s], x[s], a1);
-                else a0 = fmaf(-l[s], x[s], a0);
-            }
-            x[r] = a0 + a1;
+            for (int s = 0; s + 1 < r; s += 2)  // x_s = 0 for s < j
+                fma2(acc, make_float2(l[s], l[s + 1]), make_float2(x[s], x[s + 1]));
+            if (r & 1) acc.x = fmaf(l[r - 1], x[r - 1], acc.x);
+            x[r] = ((r == j) ? 1.f : 0.f) - (acc.x + acc.y);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
@@ -1347,6 +1373,7 @@ long chunk_tc_slots_bound(int nseq, long total_rows, int H, int T_equal, bool va
 }
 
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
+    if (slots_bound >= (1L << 31) || total_rows >= (1L << 31)) return cudaErrorInvalidValue;   // 32-bit indexing
     if (a.dk == 128) return run_tc<128>(a, total_rows, slots_bound, st);
     if (a.dk == 64) return run_tc<64>(a, total_rows, slots_bound, st);
     return cudaErrorInvalidValue;
