@@ -31,7 +31,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from kda_inputs import WORKLOADS, make_decode_state, make_decode_step, make_prefill  # noqa: E402
+from kda_inputs import (WORKLOADS, make_decode_state, make_decode_step, make_prefill,  # noqa: E402
+                        make_varlen)
 
 METRIC = "prefill tokens/s & % bf16 TC peak; decode state GB/s vs HBM peak (1×GB300)"
 NOMINAL_HBM_GBS = 8000.0
@@ -39,7 +40,11 @@ NOMINAL_HBM_GBS = 8000.0
 # now; set to None whenever that kernel changes until it is captured again.
 #   decode: profiles/decode_scan_kernel_b256_h32_d128.md
 #   prefill: profiles/tc_kernel_long_prefill_d128.md
-NCU_TRAFFIC = {"decode": 543.35e6 + 478.43e6, "prefill": 863.00e6 + 1.43e9}
+NCU_TRAFFIC = {"decode": 543.35e6 + 478.43e6, "prefill": 957.02e6 + 1.43e9}
+# sm__pipe_tensor_cycles_active (fraction of elapsed) of the prefill kernel, from the
+# mid-size (T=8192) full capture in profiles/tc_kernel_long_prefill_d128.md; None once the
+# kernel changes until it is captured again.
+NCU_TENSOR_PIPE = {"prefill": 0.125}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -246,12 +251,77 @@ def bench_prefill(args, world, rank, dev, peaks, d):
                      "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 5), "traffic": NCU_TRAFFIC["prefill"],
                      "kernel": "tc_kernel (the whole step: one launch holds the prep groups and the chains)",
                      "flops_per_launch": flops,
+                     "recurrence_min_flops": 6.0 * B * T * H * dk * dv,
+                     "ncu_tensor_pipe_active": NCU_TENSOR_PIPE["prefill"],
                      "hbm_frac_of_min_bytes": round(min_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5)},
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps * tc_prefill_launches(B, H, dev),
         "shape": dict(B=B, T=T, H=H, dk=dk, dv=dv, chunk=C),
     }
+
+
+# --------------------------------------------------------------------------- other prefill configs
+def bench_secondary(args, world, rank, dev, peaks):
+    """The training-shape prefill (workload 2) and the packed varlen prefill (workload 5),
+    reported beside the headline: tokens/s and counted FLOPs against the bf16 peak."""
+    import torch
+    import delta_rule_linear_gb300 as kda
+    from delta_rule_linear_gb300 import _lib
+    stream = torch.cuda.current_stream()
+    out = {}
+
+    def timed(step):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    wl = WORKLOADS[2]
+    d = make_prefill(wl, seed=rank)
+    q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
+    beta, decay = (to_dev(d[n], dev, torch.float32) for n in ("beta", "decay"))
+    o = torch.empty_like(v)
+    hT = torch.empty((wl.B, wl.H, wl.dk, wl.dv), dtype=torch.float32, device=dev)
+    ws = torch.empty(_lib.chunk_fwd_workspace_bytes(wl.B, wl.T, wl.H, wl.dk, wl.dv, wl.chunk,
+                                                    _lib.KDA_BF16), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: kda.chunk_fwd(q, k, v, beta, decay, None, chunk_size=wl.chunk, out=o,
+                                     final_state=hT, workspace=ws, stream=stream))
+    flops = counted_prefill_flops(wl.B, wl.T, wl.H, wl.dk, wl.dv, wl.chunk)
+    out["training_prefill"] = {
+        "workload": wl.name, "ms_per_call": ms, "tokens_per_s": wl.B * wl.T * world / (ms * 1e-3),
+        "tc_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
+        "gpu_launches_per_call": tc_prefill_launches(wl.B, wl.H, dev)}
+
+    wl = WORKLOADS[5]
+    d = make_varlen(wl, seed=rank)
+    q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
+    beta = to_dev(d["beta"], dev, torch.float32)
+    cu_cpu = torch.from_numpy(d["cu_seqlens"])
+    cu = cu_cpu.to(dev)
+    N, total = len(d["cu_seqlens"]) - 1, int(d["cu_seqlens"][-1])
+    o = torch.empty_like(v)
+    hT = torch.empty((N, wl.H, wl.dk, wl.dv), dtype=torch.float32, device=dev)
+    ws = torch.empty(_lib.varlen_fwd_workspace_bytes(N, total, wl.H, wl.dk, wl.dv, wl.chunk,
+                                                     _lib.KDA_BF16), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: kda.varlen_fwd(q, k, v, beta, cu, None, None, cu_seqlens_cpu=cu_cpu,
+                                      chunk_size=wl.chunk, out=o, final_state=hT, workspace=ws,
+                                      stream=stream))
+    flops = counted_prefill_flops(1, total, wl.H, wl.dk, wl.dv, wl.chunk)
+    out["varlen_prefill"] = {
+        "workload": wl.name, "tokens": total, "ms_per_call": ms,
+        "tokens_per_s": total * world / (ms * 1e-3),
+        "tc_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
+        # the chunk table, then prep and chain (N*H = 256 pairs exceed half the SMs)
+        "gpu_launches_per_call": 1 + tc_prefill_launches(N, wl.H, dev)}
+    return out
 
 
 # --------------------------------------------------------------------------- decode
@@ -358,11 +428,11 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "secondary"], default=None,
                     help="run one workload (profiling); the default runs both")
     ap.add_argument("--prefill-T", type=int, default=0,
                     help="profiling only: override T of the prefill workload (no CPU baseline)")
@@ -376,7 +446,7 @@ def main():
 
     # inputs of the prefill workload are drawn once; the CPU baseline runs on them
     # first, before any CUDA work starts in this process
-    d = make_prefill(prefill_workload(args), seed=rank) if args.only != "decode" else None
+    d = make_prefill(prefill_workload(args), seed=rank) if args.only in (None, "prefill") else None
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.prefill_T and d is not None:
         import oracle
@@ -400,11 +470,13 @@ def main():
     peaks, peak_src = load_peaks()
 
     pre = bench_prefill(args, world, rank, dev, peaks, d) if d is not None else None
-    dec = bench_decode(args, world, rank, dev, peaks) if args.only != "prefill" else None
+    dec = bench_decode(args, world, rank, dev, peaks) if args.only in (None, "decode") else None
+    sec = bench_secondary(args, world, rank, dev, peaks) if args.only in (None, "secondary") else None
     if rank != 0:
         return
     if pre is None:
-        print(json.dumps({"metric": METRIC, "workload": "decode only", "decode": dec}), flush=True)
+        print(json.dumps({"metric": METRIC, "workload": f"{args.only} only", "decode": dec,
+                          "secondary": sec}), flush=True)
         return
     wl = prefill_workload(args)
     pre["roofline"]["peak_source"] = peak_src
@@ -426,6 +498,8 @@ def main():
     if dec is not None:
         dec["roofline"]["peak_source"] = peak_src
         line["decode"] = dec
+    if sec is not None:
+        line.update(sec)
     print(json.dumps(line), flush=True)
 
 
