@@ -1135,6 +1135,13 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                 break;
             }
             tc_fence_after();
+            {   // E_c of this chunk has been consumed: drop its lines from L2 without the
+                // write-back to HBM (nothing reads the slot again)
+                const char *eg = reinterpret_cast<const char *>(p.E) +
+                                 (size_t)(slot0 + (long)c * p.H) * Cf::E_BYTES;
+                for (int l = et; l < Cf::E_BYTES / 128; l += 128)
+                    asm volatile("discard.global.L2 [%0], 128;" ::"l"(eg + (size_t)l * 128) : "memory");
+            }
             const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
             uint32_t v[kC];
             tmem_ld32(dcol + D, *reinterpret_cast<uint32_t(*)[32]>(v));
