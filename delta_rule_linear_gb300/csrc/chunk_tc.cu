@@ -160,6 +160,9 @@ __device__ __forceinline__ void fma2(float2 &acc, float2 a, float2 b) {
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+__device__ __forceinline__ void named_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 // B = [T' | P] and Bf = diag(f) B (bf16, MN-major SW128: row t, 64 columns s per half,
 // half 0 T' = T diag(w), half 1 P = T diag(beta)) for W consecutive columns s.. of row t
@@ -500,11 +503,19 @@ __device__ __forceinline__ void release_slot(const TcParams &p, long slot) {
     st_release_gpu(p.flags + slot, 1u);
 }
 
+// The two prep groups of a CTA run the same phases; when they run them at the same time
+// they contend for issue slots and shared memory.  With `stagger`, group 1 starts its first
+// chunk only when group 0 has finished its first epilogue 1 (named barrier kStaggerBar:
+// group 0 arrives once, group 1 waits once); the offset of about a third of a chunk
+// persists (measured: 0.962 -> 0.949 ms on a 32 x 32768-token prefill; a two-thirds offset
+// gained nothing).
+constexpr int kStaggerBar = 3;
+
 template <int D>
 __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUtensorMap *map_k,
                                            const CUtensorMap *map_E, const TcParams &p,
                                            uint8_t *sm, uint32_t tm, int tid, int bar, long item,
-                                           long stride) {
+                                           long stride, bool stagger) {
     using Ly = PrepSmem<D>;
     constexpr int NB = D / 64;
     constexpr int R = D + 64;
@@ -532,9 +543,14 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     float *mdec = mbeta + 64, *mG = mdec + 64, *mGp = mG + 64, *mkn = mGp + 64, *mqn = mkn + 64;
     float *mf = mqn + 64, *meg = mf + 64, *mcw = meg + 64;
 
+    const bool lead = stagger && bar == 1, follow = stagger && bar == 2;
+    if (follow) named_sync(kStaggerBar, 2 * kGroupThreads);
     ChunkItem cur;
     while (item < p.n_items && !item_info(p, item, cur)) item += stride;
-    if (item >= p.n_items) return;
+    if (item >= p.n_items) {
+        if (lead) named_arrive(kStaggerBar, 2 * kGroupThreads);
+        return;
+    }
     load_rows<D>(p, sKQ, cur, tid, true);
     load_rows<D>(p, sKQ, cur, tid, false);
     load_scalars(p, mbeta, mdec, cur, tid);
@@ -685,6 +701,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         fence_proxy_async();
         named_sync(bar, kGroupThreads);
         ok = ctl->fail == 0;
+        if (lead && it == 0) named_arrive(kStaggerBar, 2 * kGroupThreads);
 
         // ---- T = (I + L)^{-1}, written as B = [T' | P], Bf = diag(f) B (MN-major: row t, columns s)
         invert_unit_lower_64<kGroupThreads>(sL, sT, BTiles{sB, sBf, mcw, mbeta, mf}, tid, bar, [&] {
@@ -694,6 +711,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                 pend = -1;
             }
         });
+
 
         // ---- MMA2: D2a[:, 0:128] = K^T diag(f) [T'|P]  (M = D);  D2b[:, 128:256] = Aqk [T'|P]
         if (tid == 0 && ok) {
@@ -1208,8 +1226,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     tc_fence_after();
     const long gidx = (long)((int)blockIdx.x - p.nchain) * 2 + grp;
     const long ngroups = (long)((int)gridDim.x - p.nchain) * 2;
+    const bool stagger = p.n_items >= 16 * ngroups;   // long runs only: the offset costs a start-up delay
     prep_group<D>(&map_q, &map_k, &map_E, p, gsm, tmem_base + (uint32_t)(grp * 256),
-                  tid & (kGroupThreads - 1), 1 + grp, gidx, ngroups);
+                  tid & (kGroupThreads - 1), 1 + grp, gidx, ngroups, stagger);
     tc_fence_before();
     __syncthreads();
     if (tid < 32) {
