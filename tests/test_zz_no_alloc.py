@@ -30,7 +30,8 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(kda):
     import torch
     dev = torch.device("cuda:0")
     cases = [((1, 1000, 8, 128), "long", "normal002", 11),
-             ((2, 300, 4, 64), "train", "zero", 12)]
+             ((2, 300, 4, 64), "train", "zero", 12),
+             ((4, 70, 20, 64), "train", "normal002", 13)]   # B*H = 80: the two-launch path
     for (B, T, H, D), decay, h0, seed in cases:
         d = make_custom(B, T, H, D, D, dtype="bf16", decay=decay, h0=h0, seed=seed)
         t = inputs_to_dev(d, dev, "bf16")
