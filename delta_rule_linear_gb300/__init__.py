@@ -9,11 +9,11 @@ served by a C-ABI CUDA library (``libkda.so``, declared in ``include/kda.h``):
 chunked prefill, recurrent prefill, single-token decode and packed varlen prefill.
 This package is the thin binding; all compute runs in the library's kernels.
 """
-from ._lib import (KdaError, chunk_fwd, chunk_fwd_noalloc, decode_step, load,  # noqa: F401
-                   query_device_error, recurrent_fwd, varlen_fwd)
+from ._lib import (KdaError, chunk_fwd, chunk_fwd_noalloc, decode_step, diag_wait_timeout,  # noqa: F401
+                   load, query_device_error, recurrent_fwd, varlen_fwd)
 
 __all__ = ["kda", "chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
-           "varlen_fwd", "query_device_error", "load", "KdaError"]
+           "varlen_fwd", "query_device_error", "diag_wait_timeout", "load", "KdaError"]
 
 
 def kda(query, key, value, beta, decay=None, *, softmax_scale=None, chunk_size=64,

@@ -24,7 +24,8 @@ STATUS = {
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace", "kda_chunk_fwd",
            "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "kda_decode_step",
-           "kda_varlen_fwd_workspace", "kda_varlen_fwd", "kda_query_device_error")
+           "kda_varlen_fwd_workspace", "kda_varlen_fwd", "kda_query_device_error",
+           "kda_diag_wait_timeout")
 
 
 class KdaError(RuntimeError):
@@ -74,6 +75,8 @@ def load(path: str | None = None):
         lib.kda_varlen_fwd.restype = I
         lib.kda_query_device_error.argtypes = [P, P]
         lib.kda_query_device_error.restype = I
+        lib.kda_diag_wait_timeout.argtypes = [P, Z, ctypes.c_uint, P]
+        lib.kda_diag_wait_timeout.restype = I
         _lib = lib
         return lib
 
@@ -277,3 +280,13 @@ def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_
 def query_device_error(workspace, stream=None) -> int:
     """kda_query_device_error: device error word of the last call on ``workspace`` (0 = none)."""
     return int(load().kda_query_device_error(_ptr(workspace), _stream(stream)))
+
+
+def diag_wait_timeout(workspace, limit_us, stream=None) -> None:
+    """kda_diag_wait_timeout: enqueue the failure-detection probe on ``workspace``; its
+    bounded waits run out after ``limit_us`` each and record KDA_ERR_DEVICE_TIMEOUT, which
+    query_device_error(workspace) then returns."""
+    lib = load()
+    nbytes = workspace.numel() * workspace.element_size()
+    _raise(lib.kda_diag_wait_timeout(_ptr(workspace), nbytes, int(limit_us), _stream(stream)),
+           "kda_diag_wait_timeout", lib)

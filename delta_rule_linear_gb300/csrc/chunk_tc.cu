@@ -86,6 +86,19 @@ __device__ __forceinline__ void record_error(WsHeader *ws, int where) {
     if (ws && atomicCAS(&ws->error, 0, kStatusDeviceTimeout) == 0) ws->where = where;
 }
 
+// Wait until another CTA has released *f (gpu-scope acquire), giving up after limit_ns;
+// on success the async proxy is ordered after the acquire (for a TMA load of the data the
+// flag publishes).
+__device__ __forceinline__ bool wait_flag_acquire(const uint32_t *f, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(f) == 0u) {
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+        __nanosleep(64);
+    }
+    fence_proxy_async_global();
+    return true;
+}
+
 __device__ __forceinline__ void seq_info(const TcParams &p, int n, long &start, int &len) {
     if (p.cu_seqlens) {
         start = p.cu_seqlens[n];
@@ -987,23 +1000,10 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                     break;
                 }
                 const int slot = (int)(slot0 + (long)c * p.H);
-                if (wait_flags) {   // E_c published by its prep group
-                    const uint32_t *f = p.flags + slot;
-                    const uint64_t t0 = globaltimer_ns();
-                    bool got = true;
-                    while (ld_acquire_gpu(f) == 0u) {
-                        if (globaltimer_ns() - t0 > kWaitNs) {
-                            got = false;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                    if (!got) {
-                        s_fail = 1;
-                        record_error(p.ws, 16);
-                        break;
-                    }
-                    fence_proxy_async_global();
+                if (wait_flags && !wait_flag_acquire(p.flags + slot, kWaitNs)) {   // E_c published
+                    s_fail = 1;
+                    record_error(p.ws, 16);
+                    break;
                 }
                 mbar_expect_tx(&e_full[s], Cf::E_BYTES);
                 uint8_t *dE = sE0 + s * Cf::E_BYTES;
@@ -1245,6 +1245,19 @@ __global__ void __launch_bounds__(ChainCfg<D>::THREADS, 1) chain_kernel(const __
     chain_body<D>(&map_E, &map_v, p, align1024(smem_raw), (int)blockIdx.x, false);
 }
 
+// Failure-detection probe: the two bounded waits of the kernels above, run against events
+// that never happen (an mbarrier phase nobody arrives on, a flag nobody releases) with a
+// short limit; each time-out is recorded in the workspace header like a kernel's would be.
+__global__ void timeout_probe_kernel(WsHeader *ws, const uint32_t *never, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0, limit_ns)) record_error(ws, 90);
+        if (!wait_flag_acquire(never, limit_ns)) record_error(ws, 91);
+    }
+}
+
 // cu_seqlens -> chunk prefix: base[n] = sum_{m < n} ceil(len_m / 64), base[N] = total.
 __global__ void chunk_table_kernel(const int *cu, int N, int *base) {
     __shared__ int warp_tot[32];
@@ -1396,6 +1409,14 @@ size_t chunk_tc_scratch_bytes(int nseq, long slots_bound, int d) {
 long chunk_tc_slots_bound(int nseq, long total_rows, int H, int T_equal, bool varlen) {
     if (!varlen) return (long)nseq * ((T_equal + kC - 1) / kC) * H;
     return ((total_rows + kC - 1) / kC + nseq) * (long)H;
+}
+
+cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t st) {
+    uint32_t *never = &ws->probe;   // zeroed here, released by nobody
+    cudaError_t e = cudaMemsetAsync(never, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    timeout_probe_kernel<<<1, 32, 0, st>>>(ws, never, limit_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {

@@ -237,4 +237,18 @@ kda_status kda_query_device_error(const void *ws, kda_stream_t stream) {
     return KDA_OK;
 }
 
+kda_status kda_diag_wait_timeout(void *ws, size_t ws_bytes, unsigned limit_us,
+                                 kda_stream_t stream) {
+    if (!ws) return KDA_ERR_NULL;
+    if (ws_bytes < kWsHeader) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
+    if (limit_us == 0 || limit_us > 2000000u) return KDA_ERR_SHAPE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
+    return launch_timeout_probe(static_cast<WsHeader *>(ws), (uint64_t)limit_us * 1000u, st) ==
+                   cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
+}
+
 }  // extern "C"

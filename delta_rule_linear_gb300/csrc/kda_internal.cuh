@@ -19,7 +19,8 @@ enum class DType : int { F32 = 0, BF16 = 1 };
 struct WsHeader {
     int error;          // 0 = none; otherwise a kda_status value
     int where;          // kernel-defined location of the failure (diagnostic)
-    int pad[62];
+    unsigned probe;     // flag that the failure-detection probe waits on and nobody releases
+    int pad[61];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -77,6 +78,9 @@ long chunk_tc_slots_bound(int nseq, long total_rows, int H, int T_equal, bool va
 // Workspace bytes after the header for that bound.
 size_t chunk_tc_scratch_bytes(int nseq, long slots_bound, int d);
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t s);
+// One CTA runs the tensor-core kernels' bounded waits against events that never happen,
+// each giving up after limit_ns and recording KDA_ERR_DEVICE_TIMEOUT in the header.
+cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t s);
 
 // L2 normalisation floor: x / max(||x||, kNormEps).
 constexpr float kNormEps = 1e-12f;

@@ -206,6 +206,20 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v,
  */
 kda_status kda_query_device_error(const void *ws, kda_stream_t stream);
 
+/*
+ * Failure-detection probe (diagnostic; the pages have no counterpart).  Enqueues one small
+ * kernel that runs the two bounded waits of the tensor-core prefill -- on an mbarrier phase
+ * and on a publication flag -- against events that never happen, with a limit of
+ * `limit_us` microseconds each (1 .. 2,000,000) instead of the kernels' 2 s.  Each wait
+ * gives up, records KDA_ERR_DEVICE_TIMEOUT in the header of `ws` and returns; nothing
+ * traps, and the context stays usable.  kda_query_device_error(ws) then returns
+ * KDA_ERR_DEVICE_TIMEOUT once.  ws: device workspace of at least 256 bytes, 16-byte
+ * aligned (its header only is used).  Returns KDA_ERR_NULL, KDA_ERR_WORKSPACE,
+ * KDA_ERR_ALIGN, KDA_ERR_SHAPE (limit out of range) or KDA_ERR_CUDA on a launch failure.
+ */
+kda_status kda_diag_wait_timeout(void *ws, size_t ws_bytes, unsigned limit_us,
+                                 kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -137,3 +137,14 @@ def test_python_binding_refuses_host_tensors():
     x = torch.zeros(1, 4, 1, 32)
     with pytest.raises(ValueError):
         kda.chunk_fwd(x, x, x, torch.zeros(1, 4, 1), chunk_size=16)
+
+
+def test_diag_wait_timeout_argument_errors(lib):
+    """The probe's argument checks return before any CUDA call (a dummy aligned address
+    is never dereferenced)."""
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.kda_diag_wait_timeout(None, 4096, 1000, None) == 1        # KDA_ERR_NULL
+    assert lib.kda_diag_wait_timeout(fake, 100, 1000, None) == 6         # KDA_ERR_WORKSPACE
+    assert lib.kda_diag_wait_timeout(ctypes.c_void_p(0x10004), 4096, 1000, None) == 5   # ALIGN
+    assert lib.kda_diag_wait_timeout(fake, 4096, 0, None) == 2           # KDA_ERR_SHAPE
+    assert lib.kda_diag_wait_timeout(fake, 4096, 2_000_001, None) == 2
