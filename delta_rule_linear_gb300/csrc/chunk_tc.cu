@@ -424,6 +424,12 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
     return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
                       pack_bf16(f[6], f[7]));
 }
+__device__ __forceinline__ uint4 pack8un(const uint32_t *u) {   // of the negated values
+    return make_uint4(pack_bf16(-__uint_as_float(u[0]), -__uint_as_float(u[1])),
+                      pack_bf16(-__uint_as_float(u[2]), -__uint_as_float(u[3])),
+                      pack_bf16(-__uint_as_float(u[4]), -__uint_as_float(u[5])),
+                      pack_bf16(-__uint_as_float(u[6]), -__uint_as_float(u[7])));
+}
 __device__ __forceinline__ uint4 pack8u(const uint32_t *u) {
     return make_uint4(pack_bf16(__uint_as_float(u[0]), __uint_as_float(u[1])),
                       pack_bf16(__uint_as_float(u[2]), __uint_as_float(u[3])),
@@ -544,7 +550,11 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     float *sL = reinterpret_cast<float *>(sm + Ly::R1);
     float *sT = sL + 64 * kLP;
     uint8_t *sZ1 = sm + Ly::R1;
-    uint8_t *sZ2 = sm + Ly::R1 + D * 128;
+    // Z2 and, 8 KB after it, the diagonal block of MMA3b's A operand: clear of the V-column
+    // staging block of E_c (R1 + R*128 .. + R*128 at D = 64), which epilogue 2 writes too
+    uint8_t *sZ2 = sm + Ly::R1 + (D == 128 ? D * 128 : 32768);
+    static_assert(D == 128 ? (D * 128 + 16384 <= NB * (R * 128)) : (32768 >= (NB + 1) * (R * 128)),
+                  "MMA3b's A operand overlaps the V-column staging");
     uint8_t *sBf = sm + Ly::R2;
     uint8_t *sB = sm + Ly::R2 + 16384;
     uint8_t *sA = sm + Ly::R3;
@@ -654,8 +664,6 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             // it is overwritten behind this barrier
             if (tid == kStoreThread) bulk_wait_read0();
             named_sync(bar, kGroupThreads);
-            // MMA1 and the query norms are done with q: the next chunk's q load starts now
-            if (ok && more) load_rows<D>(p, sKQ, nx, tid, true);
             const float gC = mG[63];
             if (i128 < 64) {
                 const int t = i128;
@@ -768,10 +776,17 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             tmem_ld_wait();
             if (has64) {
                 const int t = i64;
-                if (hh == 0) {   // Z2[t][s]
+                if (hh == 0) {   // A of MMA3b: [-Z2 | diag(a)], a_t = exp(G_t) q-scale_t (0 past nv)
+                    const float a = t < nv ? meg[t] * mqn[t] : 0.f;
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        *reinterpret_cast<uint4 *>(sZ2 + t * 128 + ((cc ^ (t & 7)) << 4)) = pack8u(v + 8 * cc);
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const int off = t * 128 + ((cc ^ (t & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(sZ2 + off) = pack8un(v + 8 * cc);
+                        float dg[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) dg[e] = (8 * cc + e == t) ? a : 0.f;
+                        *reinterpret_cast<uint4 *>(sZ2 + 8192 + off) = pack8(dg);
+                    }
                 } else {         // E[D + t][D + s] = (Aqk P)[t][s] -> staging block NB
                     const int rr = D + t;
 #pragma unroll
@@ -786,7 +801,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         named_sync(bar, kGroupThreads);
         ok = ctl->fail == 0;
 
-        // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = Z2 k  (M = 64)
+        // ---- MMA3: D3a[:, 0:D] = Z1 k  (M = D);  D3b[:, 128:128+D] = diag(a) q - Z2 k  (M = 64)
         if (tid == 0 && ok) {
             tc_fence_after();
             const uint32_t ida = idesc_bf16_f32(D, D, false, true);
@@ -795,7 +810,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16_ss(tm, desc_kmajor_sw128(z1, D, ks), desc_mnmajor_sw128(kq, 128, ks), ida,
                             ks > 0 ? 1u : 0u);
-            for (int ks = 0; ks < 4; ++ks)
+            for (int ks = 0; ks < 8; ++ks)   // [-Z2 | diag(a)] [k; q]: the q~ rows of E_c in one go
                 mma_bf16_ss(tm + 128, desc_kmajor_sw128(z2, 64, ks), desc_mnmajor_sw128(kq, 128, ks),
                             idb, ks > 0 ? 1u : 0u);
             mma_commit(&ctl->bar_mma);
@@ -804,35 +819,23 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, (int)cur.slot);
             bulk_commit();
         }
-        // q of this thread's output row for epilogue 3, fetched (from L2) while MMA3 runs
-        constexpr int QP = D / 16;   // 16-byte pieces of half a row
-        uint4 qpre[QP];
-        {
-            const int t = i64;
-            const bool qrow = has64 && t < nv;   // past the sequence's end q is taken as 0
-            const uint4 *qg = reinterpret_cast<const uint4 *>(p.q + ((cur.row0 + t) * p.H + cur.h) * D) +
-                              hh * QP;
-#pragma unroll
-            for (int e = 0; e < QP; ++e) qpre[e] = qrow ? __ldg(qg + e) : make_uint4(0u, 0u, 0u, 0u);
-        }
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
-        // the k rows are free once MMA3 has read them, beta and decay after the inverse:
-        // the rest of the next chunk's load starts now
+        // [K;Q] is free once MMA3 has read it, beta and decay after the inverse: the next
+        // chunk's load starts now
         if (ok && more) {
+            load_rows<D>(p, sKQ, nx, tid, true);
             load_rows<D>(p, sKQ, nx, tid, false);
             load_scalars(p, mbeta, mdec, nx, tid);
         }
 
         // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
-        // (the q~ rows first, so that the prefetched q is dead before the K~^T W rows)
         {
             constexpr int HALF = D / 2;
             const float gamma_c = meg[63];
             const bool has_row = (D == 128) || has64;
             const int i = (D == 128) ? i128 : i64;
-            const int t = i64;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j]
-            const float qs = has64 ? meg[t] * mqn[t] : 0.f;
+            const int t = i64;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j] = D3b[t][j]
 #pragma unroll
             for (int c0 = 0; c0 < HALF; c0 += 32) {
                 uint32_t v[32];
@@ -844,16 +847,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                     uint8_t *dst = sEst + (col >> 6) * (R * 128) + rr * 128;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        const uint4 qw = qpre[(c0 >> 3) + cc];   // head-dim indices col + 8 cc .. + 7
-                        const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            f[2 * e] = qs * bf16lo(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e]);
-                            f[2 * e + 1] = qs * bf16hi(qv[e]) - __uint_as_float(v[cc * 8 + 2 * e + 1]);
-                        }
                         const int chunk = ((col & 63) >> 3) + cc;
-                        *reinterpret_cast<uint4 *>(dst + ((chunk ^ (rr & 7)) << 4)) = pack8(f);
+                        *reinterpret_cast<uint4 *>(dst + ((chunk ^ (rr & 7)) << 4)) = pack8u(v + 8 * cc);
                     }
                 }
             }
