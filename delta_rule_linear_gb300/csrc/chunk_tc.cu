@@ -445,9 +445,9 @@ __device__ __forceinline__ uint4 pack8u(const uint32_t *u) {
 // ---------------------------------------------------------------------------------
 constexpr int kGroupThreads = 256;
 constexpr int kTcThreads = 512;               // prep: two groups; chain: 14 warps used
-// The group's thread that issues the E_c stores, waits for them and publishes E_c: it sits
-// in warp 4, which is idle for most of the diagonal-block inverse, where the gpu-scope
-// release (over a thousand cycles) is hidden; warp 4 issues no other loads.
+// The group's thread that issues the E_c stores, waits for them and publishes E_c: a thread
+// other than the MMA issuer (whose release would also wait for its MMAs), in warp 4, which
+// issues no loads that the release would have to wait for.
 constexpr int kStoreThread = 128;
 
 template <int D>
@@ -725,13 +725,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         if (lead && it == 0) named_arrive(kStaggerBar, 2 * kGroupThreads);
 
         // ---- T = (I + L)^{-1}, written as B = [T' | P], Bf = diag(f) B (MN-major: row t, columns s)
-        invert_unit_lower_64<kGroupThreads>(sL, sT, BTiles{sB, sBf, mcw, mbeta, mf}, tid, bar, [&] {
-            if (tid == kStoreThread && pend >= 0) {   // the previous chunk's E_c: its stores
-                bulk_wait0();                         // (this chunk's start, previous MMA3) are done
-                release_slot(p, pend);
-                pend = -1;
-            }
-        });
+        invert_unit_lower_64<kGroupThreads>(sL, sT, BTiles{sB, sBf, mcw, mbeta, mf}, tid, bar, [] {});
 
 
         // ---- MMA2: D2a[:, 0:128] = K^T diag(f) [T'|P]  (M = D);  D2b[:, 128:256] = Aqk [T'|P]
@@ -747,6 +741,14 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                 mma_bf16_ss(tm + 128, desc_kmajor_sw128(aa, 64, ks), desc_mnmajor_sw128(bb, 64, ks), idb,
                             ks > 0 ? 1u : 0u);
             mma_commit(&ctl->bar_mma);
+        }
+        // The previous chunk's E_c is published while MMA2 runs (the whole group waits for it
+        // anyway): its stores (this chunk's start, the previous MMA3) have completed, and the
+        // gpu-scope release, about a thousand cycles, overlaps the MMA.
+        if (tid == kStoreThread && pend >= 0) {
+            bulk_wait0();
+            release_slot(p, pend);
+            pend = -1;
         }
         if (ok && !mbar_wait(&ctl->bar_mma, ph ^ 1u, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
