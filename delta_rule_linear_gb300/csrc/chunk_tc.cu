@@ -838,41 +838,33 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             const bool has_row = (D == 128) || has64;
             const int i = (D == 128) ? i128 : i64;
             const int t = i64;   // E[D + t][j] = exp(G_t) q~_t[j] - (Aqk W)[t][j] = D3b[t][j]
+            static_assert(HALF == 64 || HALF == 32, "half a row of the head dim");
+            uint32_t v[HALF];   // both TMEM loads of a half row in flight together
+            tmem_ld32(tm + tq + 128 + hh * HALF, *reinterpret_cast<uint32_t(*)[32]>(v));
+            if (HALF == 64) tmem_ld32(tm + tq + 128 + hh * HALF + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * (HALF / 64)));
+            tmem_ld_wait();
+            if (has64) {
+                const int rr = D + t;
 #pragma unroll
-            for (int c0 = 0; c0 < HALF; c0 += 32) {
-                uint32_t v[32];
-                const int col = hh * HALF + c0;
-                tmem_ld32(tm + tq + 128 + col, v);
-                tmem_ld_wait();
-                if (has64) {
-                    const int rr = D + t;
-                    uint8_t *dst = sEst + (col >> 6) * (R * 128) + rr * 128;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int chunk = ((col & 63) >> 3) + cc;
-                        *reinterpret_cast<uint4 *>(dst + ((chunk ^ (rr & 7)) << 4)) = pack8u(v + 8 * cc);
-                    }
+                for (int cc = 0; cc < HALF / 8; ++cc) {
+                    const int col = hh * HALF + 8 * cc;
+                    *reinterpret_cast<uint4 *>(sEst + (col >> 6) * (R * 128) + rr * 128 +
+                                               ((((col & 63) >> 3) ^ (rr & 7)) << 4)) = pack8u(v + 8 * cc);
                 }
             }
+            tmem_ld32(tm + tq + hh * HALF, *reinterpret_cast<uint32_t(*)[32]>(v));
+            if (HALF == 64) tmem_ld32(tm + tq + hh * HALF + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * (HALF / 64)));
+            tmem_ld_wait();
+            if (has_row) {   // E[i][j] = gamma_C delta_ij - (K~^T W)[i][j]
 #pragma unroll
-            for (int c0 = 0; c0 < HALF; c0 += 32) {   // E[i][j] = gamma_C delta_ij - (K~^T W)[i][j]
-                uint32_t v[32];
-                const int col = hh * HALF + c0;
-                tmem_ld32(tm + tq + col, v);
-                tmem_ld_wait();
-                if (has_row) {
-                    uint8_t *dst = sEst + (col >> 6) * (R * 128) + i * 128;
+                for (int cc = 0; cc < HALF / 8; ++cc) {
+                    const int col = hh * HALF + 8 * cc;
+                    float f[8];
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = col + cc * 8 + e;
-                            f[e] = (j == i ? gamma_c : 0.f) - __uint_as_float(v[cc * 8 + e]);
-                        }
-                        const int chunk = ((col & 63) >> 3) + cc;
-                        *reinterpret_cast<uint4 *>(dst + ((chunk ^ (i & 7)) << 4)) = pack8(f);
-                    }
+                    for (int e = 0; e < 8; ++e)
+                        f[e] = (col + e == i ? gamma_c : 0.f) - __uint_as_float(v[8 * cc + e]);
+                    *reinterpret_cast<uint4 *>(sEst + (col >> 6) * (R * 128) + i * 128 +
+                                               ((((col & 63) >> 3) ^ (i & 7)) << 4)) = pack8(f);
                 }
             }
         }
