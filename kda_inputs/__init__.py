@@ -12,8 +12,8 @@ aarch64.  Order inside one workload: sequence lengths (varlen only), q, k, v,
 beta logits, decay normals, initial state.  Decode draws the initial state from
 the base seed and each step's token from the seed pair (seed, step + 1).
 
-The five workloads follow the shapes and distributions of the task's five
-benchmark configurations:
+The five workloads follow the shapes and distributions of the five benchmark
+configurations:
 
   1 tiny      fp32, B=1 T=64 H=2 d=32, chunk 16, zero state, l2 on,
               q,k,v ~ N(0,1), beta = sigmoid(N(0,1)), decay = -0.01|N(0,1)|
@@ -25,6 +25,11 @@ benchmark configurations:
               decay = -0.01|N(0,1)| per step, l2 on
   5 varlen    bf16, 16 sequences of length U[256, 4096], H=16 d=64, chunk 64,
               decay None, zero state per sequence, l2 on
+
+Per-key-channel decay (TileOPs KDAFwdOp, g [B,T,H,K]) draws, after q, k, v and the
+beta logits, g = -gate_scale * U[0,1) per token and key channel: the gate regimes of
+the kda-neuron-kernels README ("Functional warning": scales 0.01, 0.3, 2.0; its
+examples draw -rand * 0.01).
 """
 from __future__ import annotations
 
@@ -33,7 +38,8 @@ from dataclasses import dataclass, field
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "round_to_bf16", "make_prefill", "make_varlen",
-           "make_decode_state", "make_decode_step", "make_custom"]
+           "make_decode_state", "make_decode_step", "make_custom", "make_gk",
+           "make_gk_decode_step"]
 
 
 @dataclass(frozen=True)
@@ -170,3 +176,42 @@ def make_decode_step(wl: Workload, step: int, seed: int = 0):
     beta = _sigmoid(rng.standard_normal((B, 1, H), dtype=np.float32))
     dec = _decay(rng, (B, 1, H), wl.decay)
     return dict(q=q, k=k, v=v, beta=beta, decay=dec)
+
+
+def make_gk(B, T, H, dk, dv, *, dtype="bf16", gate_scale=0.01, h0="zero", seed=0,
+            lengths=None):
+    """Inputs with one log decay per key channel: g [B,T,H,dk] = -gate_scale * U[0,1).
+
+    With ``lengths`` the batch is packed: token arrays [1, total, H, .] and
+    ``cu_seqlens`` int32 [N+1]; the state then has N rows.  Without it, B sequences
+    of T tokens.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = {}
+    if lengths is not None:
+        lengths = np.asarray(lengths, dtype=np.int64)
+        cu = np.zeros(len(lengths) + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(lengths)
+        out["cu_seqlens"] = cu
+        B, T, nstate = 1, int(cu[-1]), len(lengths)
+    else:
+        nstate = B
+    q = _cast(rng.standard_normal((B, T, H, dk), dtype=np.float32), dtype)
+    k = _cast(rng.standard_normal((B, T, H, dk), dtype=np.float32), dtype)
+    v = _cast(rng.standard_normal((B, T, H, dv), dtype=np.float32), dtype)
+    beta = _sigmoid(rng.standard_normal((B, T, H), dtype=np.float32))
+    g = (-gate_scale * rng.random((B, T, H, dk), dtype=np.float32)).astype(np.float32)
+    st = _h0(rng, (nstate, H, dk, dv), h0)
+    out.update(q=q, k=k, v=v, beta=beta, g=g, h0=st)
+    return out
+
+
+def make_gk_decode_step(B, H, dk, dv, step, *, dtype="bf16", gate_scale=0.01, seed=0):
+    """One token per sequence with per-channel decay: q, k, g [B,1,H,dk], v [B,1,H,dv]."""
+    rng = np.random.Generator(np.random.PCG64([seed, step + 1]))
+    q = _cast(rng.standard_normal((B, 1, H, dk), dtype=np.float32), dtype)
+    k = _cast(rng.standard_normal((B, 1, H, dk), dtype=np.float32), dtype)
+    v = _cast(rng.standard_normal((B, 1, H, dv), dtype=np.float32), dtype)
+    beta = _sigmoid(rng.standard_normal((B, 1, H), dtype=np.float32))
+    g = (-gate_scale * rng.random((B, 1, H, dk), dtype=np.float32)).astype(np.float32)
+    return dict(q=q, k=k, v=v, beta=beta, g=g)

@@ -9,8 +9,10 @@ It restates page 1 (ejkernel ``kernels._xla.kernel_delta_attention._interface``,
 chunked WY form derived from that recurrence (``kda()`` "Algorithm Modes":
 chunked = parallel inside a chunk, sequential across chunks), plus the packed
 variable-length layout of TileOPs "Linear Attention Operators", DeltaNetFwdOp
-(``cu_seqlens``, one state per sequence).  The arithmetic lives in
-``kda_oracle.c``; this module only builds it with gcc and marshals numpy arrays.
+(``cu_seqlens``, one state per sequence), plus the per-key-channel decay of
+KDAFwdOp on the same page (``forward_gk``: g [.., dk], either decay placement).
+The arithmetic lives in ``kda_oracle.c``; this module only builds it with gcc
+and marshals numpy arrays.
 """
 from __future__ import annotations
 
@@ -57,6 +59,9 @@ def _load():
             lib.kda_oracle_varlen.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I,
                                               D, I, I, I, P, I, I]
             lib.kda_oracle_varlen.restype = I
+            lib.kda_oracle_gk.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I,
+                                          D, I, I, I, I, P, I, I]
+            lib.kda_oracle_gk.restype = I
             lib.kda_oracle_threads.argtypes = []
             lib.kda_oracle_threads.restype = I
             _lib = lib
@@ -161,3 +166,43 @@ def decode_steps(steps, h0, *, scale=None, use_l2=True, heads=None, threads=0):
         h = h_new
         outs.append(o)
     return outs, h
+
+
+def forward_gk(q, k, v, beta, g=None, h0=None, *, cu_seqlens=None, scale=None, use_l2=True,
+               decayed_read=False, chunk=None, heads=None, threads=0):
+    """fp64 forward with one log decay per key channel (TileOPs KDAFwdOp).
+
+    Equal length: q, k, g [B,T,H,dk]; v [B,T,H,dv]; beta [B,T,H]; h0 [B,H,dk,dv].
+    Packed (``cu_seqlens`` [N+1] given): the token arrays have B == 1 and h0 is
+    [N,H,dk,dv].  ``decayed_read`` selects where the delta term reads the memory
+    (False: h_{t-1} as in kda()'s printed recurrence; True: diag(exp g_t) h_{t-1},
+    the gated delta rule).  ``chunk=None`` runs the recurrent scan, an integer
+    the chunked form.  ``heads`` restricts to flat indices n*H+h (others NaN).
+    Returns (o, hT).
+    """
+    q, k, v, beta, g = _f32(q), _f32(k), _f32(v), _f32(beta), _f32(g)
+    h0 = _f64(h0)
+    Bq, T, H, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape[:3] == q.shape[:3]
+    assert beta.shape == (Bq, T, H)
+    assert g is None or g.shape == q.shape
+    cu = None
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+        assert Bq == 1 and int(cu[0]) == 0 and int(cu[-1]) == T
+        N = int(cu.size) - 1
+    else:
+        N = Bq
+    assert h0 is None or h0.shape == (N, H, dk, dv)
+    o = np.full((Bq, T, H, dv), np.nan, dtype=np.float64)
+    hT = np.full((N, H, dk, dv), np.nan, dtype=np.float64)
+    lst = None if heads is None else np.ascontiguousarray(np.asarray(heads, dtype=np.int32))
+    rc = _load().kda_oracle_gk(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(o), _ptr(hT), _ptr(cu),
+        N, T, H, dk, dv, float(scale) if scale else 0.0, int(bool(use_l2)),
+        int(bool(decayed_read)), 0 if chunk is None else 1, int(chunk or 0),
+        _ptr(lst), 0 if lst is None else int(lst.size), int(threads))
+    if rc < 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return o, hT

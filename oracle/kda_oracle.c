@@ -22,6 +22,13 @@
  *   [P2] TileOPs "Linear Attention Operators", DeltaNetFwdOp: packed
  *        variable-length mode with cu_seqlens, one state per sequence,
  *        key-major fp32 state.
+ *   [P3] TileOPs "Linear Attention Operators", KDAFwdOp (Kimi Delta
+ *        Attention): the gated delta rule with one log-space decay per key
+ *        channel, g [B,T,H,K]; GLARecurrentFwdOp prints the per-channel
+ *        retention as diag(exp(gk)) applied to the state.
+ *   [P4] kda-neuron-kernels README, "What this package provides" and
+ *        "Functional warning": the exact chunked form uses the per-channel
+ *        factor exp(gc_i - gc_j) inside the chunk; the recurrent form is exact.
  *
  * Readings taken where the page is silent (each also listed in the design
  * notes of the repository):
@@ -51,6 +58,7 @@
 typedef struct {
     const float *q, *k, *v;       /* first token of the sequence, head h  */
     const float *beta, *decay;    /* idem; decay may be NULL (zeros)      */
+    const float *gk;              /* per-channel decay [.., dk] or NULL   */
     long tok_stride_qk;           /* elements between tokens in q/k       */
     long tok_stride_v;            /* elements between tokens in v/o       */
     long tok_stride_g;            /* elements between tokens in beta/decay*/
@@ -65,6 +73,8 @@ typedef struct {
     int chunk;
     double scale;
     int use_l2;
+    int per_channel;              /* 1: decay per key channel (gk)        */
+    int decayed_read;             /* 1: the delta reads the decayed state */
 } oracle_opts;
 
 /* Read row x (length n, float32) into out (double), L2-normalised when asked,
@@ -248,6 +258,178 @@ static void chunked_problem(const oracle_problem *p, const oracle_opts *op)
 }
 
 /* ---------------------------------------------------------------------- */
+/*
+ * Per-key-channel decay [P3 KDAFwdOp, GLARecurrentFwdOp; P4].  The scalar
+ * retention exp(decay_t) of [P1] becomes the diagonal D_t = diag(exp(g_t)),
+ * g_t the dk-vector of log decays of token t: row i of the [dk,dv] memory
+ * (key channel i) is scaled by exp(g_t[i]).  Where the delta term reads the
+ * memory is taken from a flag:
+ *   decayed_read = 0 (the order printed in [P1]):
+ *       u_t = beta_t (v_t - h_{t-1}^T k_t),          h_t = D_t h_{t-1} + k_t u_t^T
+ *   decayed_read = 1 (the gated delta rule that [P3] names):
+ *       u_t = beta_t (v_t - (D_t h_{t-1})^T k_t),    h_t = D_t h_{t-1} + k_t u_t^T
+ * and o_t = h_t^T (scale q_t) in both.  With every channel sharing one value,
+ * decayed_read = 0 is the scalar recurrence above.  g NULL means zeros.
+ */
+static void scan_problem_gk(const oracle_problem *p, const oracle_opts *op)
+{
+    const int dk = p->dk, dv = p->dv;
+    double *h = (double *)calloc((size_t)dk * dv, sizeof(double));
+    double *kk = (double *)malloc(sizeof(double) * dk);
+    double *qq = (double *)malloc(sizeof(double) * dk);
+    double *a = (double *)malloc(sizeof(double) * dk);
+    double *r = (double *)malloc(sizeof(double) * dv);
+    double *u = (double *)malloc(sizeof(double) * dv);
+    if (p->h0) memcpy(h, p->h0, sizeof(double) * (size_t)dk * dv);
+
+    for (int t = 0; t < p->T; ++t) {
+        load_row(p->k + t * p->tok_stride_qk, dk, op->use_l2, 1.0, kk);
+        load_row(p->q + t * p->tok_stride_qk, dk, op->use_l2, op->scale, qq);
+        const float *vt = p->v + t * p->tok_stride_v;
+        const double b = (double)p->beta[t * p->tok_stride_g];
+        for (int i = 0; i < dk; ++i)
+            a[i] = p->gk ? exp((double)p->gk[t * p->tok_stride_qk + i]) : 1.0;
+
+        /* readout of the memory the delta term sees */
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < dk; ++i)
+                acc += (op->decayed_read ? a[i] : 1.0) * h[(size_t)i * dv + j] * kk[i];
+            r[j] = acc;
+        }
+        for (int j = 0; j < dv; ++j) u[j] = b * ((double)vt[j] - r[j]);
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j)
+                h[(size_t)i * dv + j] = a[i] * h[(size_t)i * dv + j] + kk[i] * u[j];
+        double *ot = p->o + t * p->tok_stride_v;
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < dk; ++i) acc += h[(size_t)i * dv + j] * qq[i];
+            ot[j] = acc;
+        }
+    }
+    if (p->hT) memcpy(p->hT, h, sizeof(double) * (size_t)dk * dv);
+    free(h); free(kk); free(qq); free(a); free(r); free(u);
+}
+
+/*
+ * Chunked form of the per-channel recurrence, derived from it the same way as
+ * the scalar chunked form above, with the cumulative decays now dk-vectors:
+ * G_t[c] = sum of g_s[c] over the chunk's tokens s <= t, P_t[c] = G_{t-1}[c]
+ * (0 for the first token), and R_t = G_t when the delta reads the decayed
+ * memory, R_t = P_t otherwise.  For a chunk of n tokens starting from S:
+ *
+ *   L[t][s]   = beta_t sum_c k_t[c] k_s[c] exp(R_t[c] - G_s[c])       s < t
+ *   T         = (I + L)^{-1}
+ *   W         = T diag(beta) [k_t * exp(R_t)]_t                         [n, dk]
+ *   U         = T diag(beta) V - W S
+ *   Aqk[t][s] = sum_c q_t[c] k_s[c] exp(G_t[c] - G_s[c])               s <= t
+ *   O         = [q_t * exp(G_t)]_t S + Aqk U
+ *   S_next    = diag(exp(G_n)) S + sum_s [k_s * exp(G_n - G_s)] u_s^T
+ *
+ * ("*" is the elementwise product.)  Every exponent is a difference G_a - G_b
+ * (or R_a - G_b) with a later index first, so it is <= 0 when g <= 0.  The
+ * per-channel factors are kept inside the sums over c exactly as written: no
+ * factorisation, no sub-chunk split.
+ */
+static void chunked_problem_gk(const oracle_problem *p, const oracle_opts *op)
+{
+    const int dk = p->dk, dv = p->dv, C = op->chunk;
+    double *S = (double *)calloc((size_t)dk * dv, sizeof(double));
+    double *K = (double *)malloc(sizeof(double) * (size_t)C * dk);
+    double *Q = (double *)malloc(sizeof(double) * (size_t)C * dk);
+    double *V = (double *)malloc(sizeof(double) * (size_t)C * dv);
+    double *bt = (double *)malloc(sizeof(double) * C);
+    double *G = (double *)malloc(sizeof(double) * (size_t)C * dk);
+    double *R = (double *)malloc(sizeof(double) * (size_t)C * dk);
+    double *L = (double *)calloc((size_t)C * C, sizeof(double));
+    double *Tm = (double *)calloc((size_t)C * C, sizeof(double));
+    double *Aqk = (double *)calloc((size_t)C * C, sizeof(double));
+    double *W = (double *)malloc(sizeof(double) * (size_t)C * dk);
+    double *U = (double *)malloc(sizeof(double) * (size_t)C * dv);
+    double *Sn = (double *)malloc(sizeof(double) * (size_t)dk * dv);
+    double *run = (double *)malloc(sizeof(double) * dk);
+    if (p->h0) memcpy(S, p->h0, sizeof(double) * (size_t)dk * dv);
+
+    for (int c0 = 0; c0 < p->T; c0 += C) {
+        const int n = (p->T - c0 < C) ? (p->T - c0) : C;
+        for (int c = 0; c < dk; ++c) run[c] = 0.0;
+        for (int t = 0; t < n; ++t) {
+            const int tt = c0 + t;
+            load_row(p->k + tt * p->tok_stride_qk, dk, op->use_l2, 1.0, K + (size_t)t * dk);
+            load_row(p->q + tt * p->tok_stride_qk, dk, op->use_l2, op->scale, Q + (size_t)t * dk);
+            for (int j = 0; j < dv; ++j) V[(size_t)t * dv + j] = (double)p->v[tt * p->tok_stride_v + j];
+            bt[t] = (double)p->beta[tt * p->tok_stride_g];
+            for (int c = 0; c < dk; ++c) {
+                const double prev = run[c];
+                run[c] += p->gk ? (double)p->gk[tt * p->tok_stride_qk + c] : 0.0;
+                G[(size_t)t * dk + c] = run[c];
+                R[(size_t)t * dk + c] = op->decayed_read ? run[c] : prev;
+            }
+        }
+        for (int t = 0; t < n; ++t)
+            for (int s = 0; s < n; ++s) {
+                double kk = 0.0, qk = 0.0;
+                for (int c = 0; c < dk; ++c) {
+                    const double ks = K[(size_t)s * dk + c], Gs = G[(size_t)s * dk + c];
+                    if (s < t) kk += K[(size_t)t * dk + c] * ks * exp(R[(size_t)t * dk + c] - Gs);
+                    if (s <= t) qk += Q[(size_t)t * dk + c] * ks * exp(G[(size_t)t * dk + c] - Gs);
+                }
+                L[(size_t)t * C + s] = (s < t) ? bt[t] * kk : 0.0;
+                Aqk[(size_t)t * C + s] = (s <= t) ? qk : 0.0;
+            }
+        /* T = (I + L)^{-1}, column by column (forward substitution) */
+        for (int j = 0; j < n; ++j)
+            for (int t = 0; t < n; ++t) {
+                double x = (t == j) ? 1.0 : 0.0;
+                for (int s = 0; s < t; ++s) x -= L[(size_t)t * C + s] * Tm[(size_t)s * C + j];
+                Tm[(size_t)t * C + j] = x;
+            }
+        /* W, then U = T diag(beta) V - W S */
+        for (int t = 0; t < n; ++t)
+            for (int c = 0; c < dk; ++c) {
+                double acc = 0.0;
+                for (int s = 0; s < n; ++s)
+                    acc += Tm[(size_t)t * C + s] * bt[s] * K[(size_t)s * dk + c] *
+                           exp(R[(size_t)s * dk + c]);
+                W[(size_t)t * dk + c] = acc;
+            }
+        for (int t = 0; t < n; ++t)
+            for (int j = 0; j < dv; ++j) {
+                double tv = 0.0, ws = 0.0;
+                for (int s = 0; s < n; ++s) tv += Tm[(size_t)t * C + s] * bt[s] * V[(size_t)s * dv + j];
+                for (int c = 0; c < dk; ++c) ws += W[(size_t)t * dk + c] * S[(size_t)c * dv + j];
+                U[(size_t)t * dv + j] = tv - ws;
+            }
+        /* O = [q_t * exp(G_t)] S + Aqk U */
+        for (int t = 0; t < n; ++t) {
+            double *ot = p->o + (c0 + t) * p->tok_stride_v;
+            for (int j = 0; j < dv; ++j) {
+                double qs = 0.0, au = 0.0;
+                for (int c = 0; c < dk; ++c)
+                    qs += Q[(size_t)t * dk + c] * exp(G[(size_t)t * dk + c]) * S[(size_t)c * dv + j];
+                for (int s = 0; s <= t; ++s) au += Aqk[(size_t)t * C + s] * U[(size_t)s * dv + j];
+                ot[j] = qs + au;
+            }
+        }
+        /* S_next = diag(exp(G_n)) S + sum_s [k_s * exp(G_n - G_s)] u_s^T */
+        const double *Gn = G + (size_t)(n - 1) * dk;
+        for (int c = 0; c < dk; ++c)
+            for (int j = 0; j < dv; ++j) {
+                double acc = exp(Gn[c]) * S[(size_t)c * dv + j];
+                for (int s = 0; s < n; ++s)
+                    acc += exp(Gn[c] - G[(size_t)s * dk + c]) * K[(size_t)s * dk + c] *
+                           U[(size_t)s * dv + j];
+                Sn[(size_t)c * dv + j] = acc;
+            }
+        memcpy(S, Sn, sizeof(double) * (size_t)dk * dv);
+    }
+    if (p->hT) memcpy(p->hT, S, sizeof(double) * (size_t)dk * dv);
+    free(S); free(K); free(Q); free(V); free(bt); free(G); free(R); free(L);
+    free(Tm); free(Aqk); free(W); free(U); free(Sn); free(run);
+}
+
+/* ---------------------------------------------------------------------- */
 /* Thread pool over independent problems (plain pthreads, static striding). */
 
 typedef struct {
@@ -261,8 +443,14 @@ static void *worker(void *arg)
 {
     worker_arg *w = (worker_arg *)arg;
     for (int i = w->tid; i < w->nprob; i += w->nthreads) {
-        if (w->opts->mode == 0) scan_problem(&w->probs[i], w->opts);
-        else chunked_problem(&w->probs[i], w->opts);
+        if (w->opts->per_channel) {
+            if (w->opts->mode == 0) scan_problem_gk(&w->probs[i], w->opts);
+            else chunked_problem_gk(&w->probs[i], w->opts);
+        } else if (w->opts->mode == 0) {
+            scan_problem(&w->probs[i], w->opts);
+        } else {
+            chunked_problem(&w->probs[i], w->opts);
+        }
     }
     return NULL;
 }
@@ -309,7 +497,7 @@ int kda_oracle_forward(const float *q, const float *k, const float *v,
 {
     if (B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
     if (mode == 1 && chunk <= 0) return -2;
-    oracle_opts op = { mode, chunk, scale > 0.0 ? scale : 1.0 / sqrt((double)dk), use_l2 };
+    oracle_opts op = { mode, chunk, scale > 0.0 ? scale : 1.0 / sqrt((double)dk), use_l2, 0, 0 };
     int nprob = bh_list ? n_bh : B * H;
     oracle_problem *pr = (oracle_problem *)malloc(sizeof(oracle_problem) * (nprob > 0 ? nprob : 1));
     for (int i = 0; i < nprob; ++i) {
@@ -322,6 +510,7 @@ int kda_oracle_forward(const float *q, const float *k, const float *v,
         p->v = v + ((size_t)b * T * H + h) * dv;
         p->beta = beta + (size_t)b * T * H + h;
         p->decay = decay ? decay + (size_t)b * T * H + h : NULL;
+        p->gk = NULL;
         p->tok_stride_qk = (long)H * dk;
         p->tok_stride_v = (long)H * dv;
         p->tok_stride_g = H;
@@ -353,7 +542,7 @@ int kda_oracle_varlen(const float *q, const float *k, const float *v,
     if (mode == 1 && chunk <= 0) return -2;
     for (int n = 0; n < N; ++n)
         if (cu_seqlens[n + 1] < cu_seqlens[n]) return -4;
-    oracle_opts op = { mode, chunk, scale > 0.0 ? scale : 1.0 / sqrt((double)dk), use_l2 };
+    oracle_opts op = { mode, chunk, scale > 0.0 ? scale : 1.0 / sqrt((double)dk), use_l2, 0, 0 };
     int nprob = nh_list ? n_nh : N * H;
     oracle_problem *pr = (oracle_problem *)malloc(sizeof(oracle_problem) * (nprob > 0 ? nprob : 1));
     for (int i = 0; i < nprob; ++i) {
@@ -367,6 +556,7 @@ int kda_oracle_varlen(const float *q, const float *k, const float *v,
         p->v = v + (t0 * H + h) * dv;
         p->beta = beta + t0 * H + h;
         p->decay = decay ? decay + t0 * H + h : NULL;
+        p->gk = NULL;
         p->tok_stride_qk = (long)H * dk;
         p->tok_stride_v = (long)H * dv;
         p->tok_stride_g = H;
@@ -374,6 +564,56 @@ int kda_oracle_varlen(const float *q, const float *k, const float *v,
         p->o = o + (t0 * H + h) * dv;
         p->hT = hT ? hT + (size_t)nh * dk * dv : NULL;
         p->T = cu_seqlens[n + 1] - cu_seqlens[n]; p->dk = dk; p->dv = dv;
+    }
+    int used = run_all(pr, nprob, &op, nthreads);
+    free(pr);
+    return used;
+}
+
+/*
+ * Per-key-channel decay [P3 KDAFwdOp], equal-length (cu_seqlens NULL: N
+ * sequences of T tokens, token arrays [N,T,H,.]) or packed (cu_seqlens [N+1]:
+ * token arrays [1,total,H,.], one state per sequence).  g is [rows,H,dk]
+ * float32 or NULL (no decay).  decayed_read selects where the delta term reads
+ * the memory (see scan_problem_gk).  mode 0 = recurrent scan, 1 = chunked
+ * form.  list (flat n*H+h) restricts the work when not NULL.
+ */
+int kda_oracle_gk(const float *q, const float *k, const float *v,
+                  const float *beta, const float *g, const double *h0,
+                  double *o, double *hT, const int *cu_seqlens,
+                  int N, int T, int H, int dk, int dv,
+                  double scale, int use_l2, int decayed_read, int mode, int chunk,
+                  const int *list, int n_list, int nthreads)
+{
+    if (N < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+    if (mode == 1 && chunk <= 0) return -2;
+    if (cu_seqlens)
+        for (int n = 0; n < N; ++n)
+            if (cu_seqlens[n + 1] < cu_seqlens[n]) return -4;
+    oracle_opts op = { mode, chunk, scale > 0.0 ? scale : 1.0 / sqrt((double)dk), use_l2,
+                       1, decayed_read ? 1 : 0 };
+    int nprob = list ? n_list : N * H;
+    oracle_problem *pr = (oracle_problem *)malloc(sizeof(oracle_problem) * (nprob > 0 ? nprob : 1));
+    for (int i = 0; i < nprob; ++i) {
+        int nh = list ? list[i] : i;
+        if (nh < 0 || nh >= N * H) { free(pr); return -3; }
+        int n = nh / H, h = nh % H;
+        size_t t0 = cu_seqlens ? (size_t)cu_seqlens[n] : (size_t)n * T;
+        oracle_problem *p = &pr[i];
+        p->q = q + (t0 * H + h) * dk;
+        p->k = k + (t0 * H + h) * dk;
+        p->v = v + (t0 * H + h) * dv;
+        p->beta = beta + t0 * H + h;
+        p->decay = NULL;
+        p->gk = g ? g + (t0 * H + h) * dk : NULL;
+        p->tok_stride_qk = (long)H * dk;
+        p->tok_stride_v = (long)H * dv;
+        p->tok_stride_g = H;
+        p->h0 = h0 ? h0 + (size_t)nh * dk * dv : NULL;
+        p->o = o + (t0 * H + h) * dv;
+        p->hT = hT ? hT + (size_t)nh * dk * dv : NULL;
+        p->T = cu_seqlens ? cu_seqlens[n + 1] - cu_seqlens[n] : T;
+        p->dk = dk; p->dv = dv;
     }
     int used = run_all(pr, nprob, &op, nthreads);
     free(pr);
