@@ -6,14 +6,17 @@ Forward of the recurrence on ejkernel ``kernels._xla.kernel_delta_attention._int
     h_t = exp(decay_t) h_{t-1} + k_t (beta_t (v_t - h_{t-1}^T k_t))^T,   o_t = h_t^T (scale q_t)
 
 served by a C-ABI CUDA library (``libkda.so``, declared in ``include/kda.h``):
-chunked prefill, recurrent prefill, single-token decode and packed varlen prefill.
+chunked prefill, recurrent prefill, single-token decode and packed varlen prefill;
+and the per-key-channel decay of TileOPs KDAFwdOp (g [B,T,H,dk], ``gk_*``).
 This package is the thin binding; all compute runs in the library's kernels.
 """
 from ._lib import (KdaError, chunk_fwd, chunk_fwd_noalloc, decode_step, diag_wait_timeout,  # noqa: F401
-                   load, query_device_error, recurrent_fwd, varlen_fwd)
+                   gk_decode_step, gk_recurrent_fwd, load, query_device_error, recurrent_fwd,
+                   varlen_fwd)
 
 __all__ = ["kda", "chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
-           "varlen_fwd", "query_device_error", "diag_wait_timeout", "load", "KdaError"]
+           "varlen_fwd", "gk_recurrent_fwd", "gk_decode_step", "query_device_error",
+           "diag_wait_timeout", "load", "KdaError"]
 
 
 def kda(query, key, value, beta, decay=None, *, softmax_scale=None, chunk_size=64,

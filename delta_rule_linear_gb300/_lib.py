@@ -24,7 +24,8 @@ STATUS = {
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace", "kda_chunk_fwd",
            "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "kda_decode_step",
-           "kda_varlen_fwd_workspace", "kda_varlen_fwd", "kda_query_device_error",
+           "kda_varlen_fwd_workspace", "kda_varlen_fwd", "kda_gk_recurrent_fwd",
+           "kda_gk_varlen_recurrent_fwd", "kda_gk_decode_step", "kda_query_device_error",
            "kda_diag_wait_timeout")
 
 
@@ -73,6 +74,14 @@ def load(path: str | None = None):
         lib.kda_varlen_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, I, F, I, I,
                                        P, Z, P]
         lib.kda_varlen_fwd.restype = I
+        lib.kda_gk_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I,
+                                             P]
+        lib.kda_gk_recurrent_fwd.restype = I
+        lib.kda_gk_varlen_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P,
+                                                    I, F, I, I, P]
+        lib.kda_gk_varlen_recurrent_fwd.restype = I
+        lib.kda_gk_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, P]
+        lib.kda_gk_decode_step.restype = I
         lib.kda_query_device_error.argtypes = [P, P]
         lib.kda_query_device_error.restype = I
         lib.kda_diag_wait_timeout.argtypes = [P, Z, ctypes.c_uint, P]
@@ -275,6 +284,73 @@ def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_
     if check_device:
         _raise(query_device_error(ws, stream), "kda_varlen_fwd (device)", lib)
     return o, hT
+
+
+def gk_recurrent_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None,
+                     cu_seqlens_cpu=None, scale=None, use_qk_l2norm=True, decayed_read=False,
+                     out=None, final_state=None, stream=None):
+    """kda_gk_recurrent_fwd / kda_gk_varlen_recurrent_fwd: token-by-token prefill with one
+    log decay per key channel, g with q's shape (fp32).  ``decayed_read`` selects where the
+    delta term reads the memory.  With ``cu_seqlens`` (int32, device, [N+1]) the token
+    arrays are packed [1,total,H,.] and the states are [N,H,dk,dv].  Returns (o, final_state).
+    """
+    lib = load()
+    Bq, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    N = Bq if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (Bq, T, H, dv))
+    _check(beta, "beta", torch.float32, (Bq, T, H)); _check(g, "g", torch.float32, q.shape)
+    _check(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
+    o = out if out is not None else torch.empty((Bq, T, H, dv), dtype=q.dtype, device=q.device)
+    _check(o, "out", q.dtype, (Bq, T, H, dv))
+    hT = final_state if final_state is not None else torch.empty((N, H, dk, dv), dtype=torch.float32,
+                                                                  device=q.device)
+    _check(hT, "final_state", torch.float32, (N, H, dk, dv))
+    if cu_seqlens is None:
+        rc = lib.kda_gk_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                      _ptr(initial_state), _ptr(o), _ptr(hT), Bq, T, H, dk, dv, dt,
+                                      float(scale or 0.0), int(bool(use_qk_l2norm)),
+                                      int(bool(decayed_read)), _stream(stream))
+        _raise(rc, "kda_gk_recurrent_fwd", lib)
+        return o, hT
+    if Bq != 1:
+        raise ValueError("packed sequences need token arrays with B == 1")
+    _check(cu_seqlens, "cu_seqlens", torch.int32)
+    host = None
+    if cu_seqlens_cpu is not None:
+        host = cu_seqlens_cpu.to(torch.int32).contiguous()
+        if host.is_cuda:
+            raise ValueError("cu_seqlens_cpu must be a host tensor")
+    rc = lib.kda_gk_varlen_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                         _ptr(cu_seqlens), _ptr(host), N, T, H, dk, dv,
+                                         _ptr(initial_state), _ptr(o), _ptr(hT), dt,
+                                         float(scale or 0.0), int(bool(use_qk_l2norm)),
+                                         int(bool(decayed_read)), _stream(stream))
+    _raise(rc, "kda_gk_varlen_recurrent_fwd", lib)
+    return o, hT
+
+
+def gk_decode_step(q, k, v, beta, g, state, *, scale=None, use_qk_l2norm=True,
+                   decayed_read=False, out=None, stream=None):
+    """kda_gk_decode_step: one token per sequence with per-channel decay g [B,1,H,dk] fp32
+    (or None); ``state`` [B,H,dk,dv] fp32 is updated in place.  Returns o with v's shape."""
+    lib = load()
+    B, H, dk, dv = state.shape
+    dt = _dtype_code(q)
+    _check(q, "q"); _check(k, "k", q.dtype); _check(v, "v", q.dtype)
+    _check(beta, "beta", torch.float32); _check(g, "g", torch.float32)
+    _check(state, "state", torch.float32)
+    if q.numel() != B * H * dk or v.numel() != B * H * dv or beta.numel() != B * H or (
+            g is not None and g.numel() != B * H * dk):
+        raise ValueError("decode inputs do not match the state's [B,H,dk,dv]")
+    o = out if out is not None else torch.empty_like(v)
+    rc = lib.kda_gk_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(state),
+                                _ptr(o), B, H, dk, dv, dt, float(scale or 0.0),
+                                int(bool(use_qk_l2norm)), int(bool(decayed_read)),
+                                _stream(stream))
+    _raise(rc, "kda_gk_decode_step", lib)
+    return o
 
 
 def query_device_error(workspace, stream=None) -> int:

@@ -221,6 +221,77 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v, const flo
     return run_prefill(a, true, total_T, st);
 }
 
+kda_status kda_gk_recurrent_fwd(const void *q, const void *k, const void *v, const float *beta,
+                                const float *g, const float *initial_state, void *o,
+                                float *final_state, int B, int T, int H, int dk, int dv,
+                                kda_dtype dtype, float scale, int use_qk_l2norm,
+                                int decayed_read, kda_stream_t stream) {
+    if (B < 0 || T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, nullptr, initial_state, o, final_state,
+                                (long)B * T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (!aligned16(g)) return KDA_ERR_ALIGN;
+    SeqBatch a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
+    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.o = o; a.hT = final_state; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
+    a.dk = dk; a.dv = dv; a.chunk = 0;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    return run_prefill(a, false, (long)B * T, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kda_status kda_gk_varlen_recurrent_fwd(const void *q, const void *k, const void *v,
+                                       const float *beta, const float *g,
+                                       const int *cu_seqlens, const int *cu_seqlens_host,
+                                       int N, int total_T, int H, int dk, int dv,
+                                       const float *initial_state, void *o, float *final_state,
+                                       kda_dtype dtype, float scale, int use_qk_l2norm,
+                                       int decayed_read, kda_stream_t stream) {
+    if (N < 0 || total_T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, nullptr, initial_state, o, final_state,
+                                total_T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (!aligned16(g)) return KDA_ERR_ALIGN;
+    if (N > 0 && !cu_seqlens) return KDA_ERR_NULL;
+    if (!aligned4(cu_seqlens)) return KDA_ERR_ALIGN;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != total_T) return KDA_ERR_INDEX;
+        for (int n = 0; n < N; ++n)
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INDEX;
+    }
+    if (N == 0) return KDA_OK;
+    SeqBatch a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
+    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.o = o; a.hT = final_state; a.cu_seqlens = cu_seqlens; a.nseq = N; a.T = total_T; a.H = H;
+    a.dk = dk; a.dv = dv; a.chunk = 0;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    // every sequence scans its own cu_seqlens range; one of length 0 stores its
+    // initial state (or zeros)
+    return launch_status(launch_recurrent(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_gk_decode_step(const void *q, const void *k, const void *v, const float *beta,
+                              const float *g, float *state, void *o, int B, int H, int dk,
+                              int dv, kda_dtype dtype, float scale, int use_qk_l2norm,
+                              int decayed_read, kda_stream_t stream) {
+    if (B < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, nullptr, state, o, state, B, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (!aligned16(g)) return KDA_ERR_ALIGN;
+    if (B > 0 && !state) return KDA_ERR_NULL;
+    if (B == 0) return KDA_OK;
+    DecodeArgs a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.state = state; a.o = o;
+    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    return launch_status(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_query_device_error(const void *ws, kda_stream_t stream) {
     if (!ws) return KDA_ERR_NULL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

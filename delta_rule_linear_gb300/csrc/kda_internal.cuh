@@ -35,6 +35,9 @@ struct SeqBatch {
     const void *v;            // [rows, H, dv]   (Tin)
     const float *beta;        // [rows, H]
     const float *decay;       // [rows, H] or nullptr (zeros)
+    const float *gk;          // per-channel decay [rows, H, dk] or nullptr (per_channel only)
+    int per_channel;          // 1: the decay is gk, one value per key channel
+    int decayed_read;         // per_channel: the delta term reads the decayed state
     const float *h0;          // [nseq, H, dk, dv] or nullptr (zeros)
     void *o;                  // [rows, H, dv]   (Tin)
     float *hT;                // [nseq, H, dk, dv] or nullptr
@@ -54,6 +57,8 @@ struct SeqBatch {
 struct DecodeArgs {
     const void *q, *k, *v;
     const float *beta, *decay;
+    const float *gk;          // per-channel decay [B, H, dk] or nullptr (per_channel only)
+    int per_channel, decayed_read;
     float *state;
     void *o;
     int B, H, dk, dv;

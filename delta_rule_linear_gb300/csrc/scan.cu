@@ -7,6 +7,13 @@
 // (o = h_t^T q~ expanded with h_t = alpha S + k^ u^T; with alpha = 1 this is the
 // step of TileOPs DeltaNetRecurrentFwdOp).
 //
+// With a decay per key channel (TileOPs KDAFwdOp, g [.., dk]; GLARecurrentFwdOp:
+// diag(exp(gk)) S) alpha becomes the diagonal D = diag(exp(g_t)):
+//     r = S^T k^ or (D S)^T k^ (decayed read),  p = (D S)^T q~ = S^T (D q~),
+//     o = p + (k^ . q~) u,  S <- D S + k^ u^T,
+// i.e. the per-row factor exp(g_t[i]) scales row i of the state, and folds into the
+// k and q entries of the two reductions.
+//
 // One CTA owns one (sequence, head, value-slab) and keeps its [dk x slab] slice of
 // the state in registers: thread (rg, cg) holds float4 column group cg of rows
 // rg, rg + RG, rg + 2RG, ...  A warp therefore touches consecutive rows of one
@@ -24,6 +31,7 @@ constexpr int kThreads = 256;
 struct ScanParams {
     const void *q, *k, *v;
     const float *beta, *decay;
+    const float *gk;   // per-channel decay [rows, H, DK] (GK kernels only; may be null)
     const float *h0;   // may equal hT (decode updates in place)
     void *o;
     float *hT;
@@ -31,9 +39,10 @@ struct ScanParams {
     int nseq, T, H, DV;
     float scale;
     int use_l2;
+    int decayed_read;  // GK kernels: the delta term reads D S instead of S
 };
 
-template <typename Tin, int DK, int DVS>
+template <typename Tin, int DK, int DVS, bool GK>
 __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
     constexpr int TPR = DVS / 4;          // threads per state row (one float4 each)
     constexpr int RG = kThreads / TPR;    // row groups
@@ -42,6 +51,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
     static_assert(2 * DK <= kThreads && DVS <= kThreads, "staging assumes small heads");
 
     __shared__ float s_k[DK], s_q[DK], s_v[DVS];
+    __shared__ float s_a[GK ? DK : 1];   // exp(g_t[i]) per key channel
     __shared__ __align__(16) float s_u[DVS];
     __shared__ __align__(16) float s_red[2][RG][DVS];
     __shared__ float s_sc[8];
@@ -80,8 +90,12 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
         const long row = start + t;
         const size_t qk_off = ((size_t)row * p.H + h) * DK;
         const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
-        if (tid < DK) s_k[tid] = to_f32(k[qk_off + tid]);
-        else if (tid < 2 * DK) s_q[tid - DK] = to_f32(q[qk_off + tid - DK]);
+        if (tid < DK) {
+            s_k[tid] = to_f32(k[qk_off + tid]);
+            if constexpr (GK) s_a[tid] = p.gk ? expf(p.gk[qk_off + tid]) : 1.f;
+        } else if (tid < 2 * DK) {
+            s_q[tid - DK] = to_f32(q[qk_off + tid - DK]);
+        }
         if (tid < DVS) s_v[tid] = to_f32(v[v_off + tid]);
         if (tid == 0) {
             s_sc[0] = p.beta[(size_t)row * p.H + h];
@@ -104,7 +118,12 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
 #pragma unroll
         for (int m = 0; m < R; ++m) {
             const int i = rg + RG * m;
-            const float kk = s_k[i], qq = s_q[i];
+            float kk = s_k[i], qq = s_q[i];
+            if constexpr (GK) {
+                const float ai = s_a[i];
+                qq *= ai;
+                if (p.decayed_read) kk *= ai;
+            }
             r.x = fmaf(S[m].x, kk, r.x); r.y = fmaf(S[m].y, kk, r.y);
             r.z = fmaf(S[m].z, kk, r.z); r.w = fmaf(S[m].w, kk, r.w);
             pq.x = fmaf(S[m].x, qq, pq.x); pq.y = fmaf(S[m].y, qq, pq.y);
@@ -125,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
                 ps += s_red[1][g][tid];
             }
             const float u = s_sc[0] * (s_v[tid] - kn * rs);
-            const float out = alpha * (qn * ps) + (kn * qn * s_sc[4]) * u;
+            const float out = (GK ? 1.f : alpha) * (qn * ps) + (kn * qn * s_sc[4]) * u;
             s_u[tid] = u;
             o[v_off + tid] = from_f32<Tin>(out);
         }
@@ -135,10 +154,11 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
 #pragma unroll
         for (int m = 0; m < R; ++m) {
             const float kk = kn * s_k[rg + RG * m];
-            S[m].x = fmaf(alpha, S[m].x, kk * u4.x);
-            S[m].y = fmaf(alpha, S[m].y, kk * u4.y);
-            S[m].z = fmaf(alpha, S[m].z, kk * u4.z);
-            S[m].w = fmaf(alpha, S[m].w, kk * u4.w);
+            const float am = GK ? s_a[rg + RG * m] : alpha;
+            S[m].x = fmaf(am, S[m].x, kk * u4.x);
+            S[m].y = fmaf(am, S[m].y, kk * u4.y);
+            S[m].z = fmaf(am, S[m].z, kk * u4.z);
+            S[m].w = fmaf(am, S[m].w, kk * u4.w);
         }
         __syncthreads();  // staging buffers are rewritten by the next token
     }
@@ -152,33 +172,37 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
     }
 }
 
-template <typename Tin, int DK>
+template <typename Tin, int DK, bool GK>
 cudaError_t launch_dk(const ScanParams &p, int dvs, int grid, cudaStream_t s) {
     switch (dvs) {
-        case 32: scan_kernel<Tin, DK, 32><<<grid, kThreads, 0, s>>>(p); break;
-        case 64: scan_kernel<Tin, DK, 64><<<grid, kThreads, 0, s>>>(p); break;
-        case 128: scan_kernel<Tin, DK, 128><<<grid, kThreads, 0, s>>>(p); break;
+        case 32: scan_kernel<Tin, DK, 32, GK><<<grid, kThreads, 0, s>>>(p); break;
+        case 64: scan_kernel<Tin, DK, 64, GK><<<grid, kThreads, 0, s>>>(p); break;
+        case 128: scan_kernel<Tin, DK, 128, GK><<<grid, kThreads, 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 
-template <typename Tin>
+template <typename Tin, bool GK>
 cudaError_t launch_typed(const ScanParams &p, int dk, int dvs, int grid, cudaStream_t s) {
     switch (dk) {
-        case 32: return launch_dk<Tin, 32>(p, dvs, grid, s);
-        case 64: return launch_dk<Tin, 64>(p, dvs, grid, s);
-        case 128: return launch_dk<Tin, 128>(p, dvs, grid, s);
+        case 32: return launch_dk<Tin, 32, GK>(p, dvs, grid, s);
+        case 64: return launch_dk<Tin, 64, GK>(p, dvs, grid, s);
+        case 128: return launch_dk<Tin, 128, GK>(p, dvs, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_scan(const ScanParams &p, DType dt, int dk, int dvs, cudaStream_t s) {
+// gk selects the per-key-channel kernels (p.gk may still be null: no decay).
+cudaError_t launch_scan(const ScanParams &p, DType dt, int dk, int dvs, bool gk, cudaStream_t s) {
     const long grid = (long)p.nseq * p.H * (p.DV / dvs);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    return dt == DType::BF16 ? launch_typed<__nv_bfloat16>(p, dk, dvs, (int)grid, s)
-                             : launch_typed<float>(p, dk, dvs, (int)grid, s);
+    if (gk)
+        return dt == DType::BF16 ? launch_typed<__nv_bfloat16, true>(p, dk, dvs, (int)grid, s)
+                                 : launch_typed<float, true>(p, dk, dvs, (int)grid, s);
+    return dt == DType::BF16 ? launch_typed<__nv_bfloat16, false>(p, dk, dvs, (int)grid, s)
+                             : launch_typed<float, false>(p, dk, dvs, (int)grid, s);
 }
 
 }  // namespace
@@ -188,7 +212,9 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     p.q = a.q; p.k = a.k; p.v = a.v; p.beta = a.beta; p.decay = a.decay;
     p.h0 = a.state; p.hT = a.state; p.o = a.o; p.cu_seqlens = nullptr;
     p.nseq = a.B; p.T = 1; p.H = a.H; p.DV = a.dv; p.scale = a.scale; p.use_l2 = a.use_l2;
-    return launch_scan(p, a.dtype, a.dk, a.dv, s);  // one CTA per head, whole value width
+    p.gk = a.gk; p.decayed_read = a.decayed_read;
+    // one CTA per head, whole value width
+    return launch_scan(p, a.dtype, a.dk, a.dv, a.per_channel != 0, s);
 }
 
 cudaError_t launch_recurrent(const SeqBatch &a, cudaStream_t s) {
@@ -196,9 +222,10 @@ cudaError_t launch_recurrent(const SeqBatch &a, cudaStream_t s) {
     p.q = a.q; p.k = a.k; p.v = a.v; p.beta = a.beta; p.decay = a.decay;
     p.h0 = a.h0; p.hT = a.hT; p.o = a.o; p.cu_seqlens = a.cu_seqlens;
     p.nseq = a.nseq; p.T = a.T; p.H = a.H; p.DV = a.dv; p.scale = a.scale; p.use_l2 = a.use_l2;
+    p.gk = a.gk; p.decayed_read = a.decayed_read;
     // 32-column slabs: a long prefill is latency-bound per token, so spread the
     // independent value columns over more CTAs.
-    return launch_scan(p, a.dtype, a.dk, 32, s);
+    return launch_scan(p, a.dtype, a.dk, 32, a.per_channel != 0, s);
 }
 
 }  // namespace kda

@@ -199,6 +199,47 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v,
                           void *ws, size_t ws_bytes, kda_stream_t stream);
 
 /*
+ * Per-key-channel decay: Kimi Delta Attention (TileOPs "Linear Attention Operators",
+ * KDAFwdOp: the gated delta rule with one log-space decay per key channel, g [B,T,H,K];
+ * GLARecurrentFwdOp writes that retention as diag(exp(gk)) applied to the state).
+ * Per (b, h), with D_t = diag(exp(g_t)) scaling row i (key channel i) of the memory:
+ *
+ *     decayed_read == 0:   u_t = beta_t * (v_t - h_{t-1}^T k^_t)
+ *     decayed_read != 0:   u_t = beta_t * (v_t - (D_t h_{t-1})^T k^_t)   (gated delta rule)
+ *     h_t = D_t h_{t-1} + k^_t u_t^T,      o_t = h_t^T q~_t
+ *
+ * k^, q~, scale and use_qk_l2norm as above.  With every channel of g_t equal to decay_t
+ * and decayed_read == 0 this is the recurrence at the top of this header; without decay
+ * the two placements coincide.
+ *   g   [B,T,H,dk] float32, the layout of q and k; NULL means no decay.  16-byte aligned.
+ * Every other argument, layout and rule as kda_recurrent_fwd / kda_varlen_fwd /
+ * kda_decode_step.  These run on CUDA cores, token by token (exact for any decay
+ * strength), and need no workspace.
+ */
+kda_status kda_gk_recurrent_fwd(const void *q, const void *k, const void *v,
+                                const float *beta, const float *g,
+                                const float *initial_state, void *o, float *final_state,
+                                int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                                float scale, int use_qk_l2norm, int decayed_read,
+                                kda_stream_t stream);
+
+/* Packed form: q, k, g [1,total_T,H,dk]; v, o [1,total_T,H,dv]; beta [1,total_T,H];
+ * cu_seqlens / cu_seqlens_host and the [N,H,dk,dv] states as kda_varlen_fwd. */
+kda_status kda_gk_varlen_recurrent_fwd(const void *q, const void *k, const void *v,
+                                       const float *beta, const float *g,
+                                       const int *cu_seqlens, const int *cu_seqlens_host,
+                                       int N, int total_T, int H, int dk, int dv,
+                                       const float *initial_state, void *o, float *final_state,
+                                       kda_dtype dtype, float scale, int use_qk_l2norm,
+                                       int decayed_read, kda_stream_t stream);
+
+/* One token per sequence: q, k, g [B,1,H,dk]; the state is updated in place. */
+kda_status kda_gk_decode_step(const void *q, const void *k, const void *v,
+                              const float *beta, const float *g, float *state, void *o,
+                              int B, int H, int dk, int dv, kda_dtype dtype, float scale,
+                              int use_qk_l2norm, int decayed_read, kda_stream_t stream);
+
+/*
  * Read the device error word that the kernels of the most recent kda_chunk_fwd /
  * kda_varlen_fwd call on `ws` recorded (KDA_OK if none), then clear it.  Each of
  * those calls clears the word on its stream before its kernels run.

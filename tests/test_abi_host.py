@@ -148,3 +148,46 @@ def test_diag_wait_timeout_argument_errors(lib):
     assert lib.kda_diag_wait_timeout(ctypes.c_void_p(0x10004), 4096, 1000, None) == 5   # ALIGN
     assert lib.kda_diag_wait_timeout(fake, 4096, 0, None) == 2           # KDA_ERR_SHAPE
     assert lib.kda_diag_wait_timeout(fake, 4096, 2_000_001, None) == 2
+
+
+def test_gk_entry_points_reject_bad_arguments(lib):
+    """Per-key-channel decay: the same checks, plus g's 16-byte alignment."""
+    def rec(**kw):
+        a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), g=_fake(), h0=None, o=_fake(),
+                 hT=None, B=1, T=64, H=2, dk=64, dv=64, dt=1, l2=1, dr=1)
+        a.update(kw)
+        return lib.kda_gk_recurrent_fwd(a["q"], a["k"], a["v"], a["beta"], a["g"], a["h0"],
+                                        a["o"], a["hT"], a["B"], a["T"], a["H"], a["dk"],
+                                        a["dv"], a["dt"], 0.0, a["l2"], a["dr"], None)
+    assert rec(q=None) == 1
+    assert rec(T=-1) == 2
+    assert rec(dt=9) == 3
+    assert rec(dk=80) == 4
+    assert rec(g=_fake(0x1004)) == 5
+    assert rec(B=0) == 0                            # nothing to do, no launch
+
+    def dec(**kw):
+        a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), g=None, state=_fake(),
+                 o=_fake(), B=4, H=2, dk=128, dv=128, dt=1, l2=1, dr=0)
+        a.update(kw)
+        return lib.kda_gk_decode_step(a["q"], a["k"], a["v"], a["beta"], a["g"], a["state"],
+                                      a["o"], a["B"], a["H"], a["dk"], a["dv"], a["dt"], 0.0,
+                                      a["l2"], a["dr"], None)
+    assert dec(state=None) == 1
+    assert dec(g=_fake(0x1008)) == 5
+    assert dec(dv=16) == 4
+    assert dec(B=0) == 0
+
+    def var(host, N=3, total=10, **kw):
+        hs = (ctypes.c_int * len(host))(*host)
+        a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), g=_fake(), cu=_fake(),
+                 h0=None, o=_fake(), hT=None, H=2, dk=64, dv=64, dt=1)
+        a.update(kw)
+        return lib.kda_gk_varlen_recurrent_fwd(a["q"], a["k"], a["v"], a["beta"], a["g"],
+                                               a["cu"], ctypes.cast(hs, ctypes.c_void_p), N,
+                                               total, a["H"], a["dk"], a["dv"], a["h0"], a["o"],
+                                               a["hT"], a["dt"], 0.0, 1, 0, None)
+    assert var([0, 4, 3, 10]) == 9
+    assert var([0, 4, 6, 9]) == 9
+    assert var([0, 4, 6, 10], cu=None) == 1
+    assert var([0, 4, 6, 10], g=_fake(0x100c)) == 5
