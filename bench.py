@@ -31,8 +31,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from kda_inputs import (WORKLOADS, make_decode_state, make_decode_step, make_prefill,  # noqa: E402
-                        make_varlen)
+from kda_inputs import (WORKLOADS, make_decode_state, make_decode_step, make_gk,  # noqa: E402
+                        make_gk_decode_step, make_prefill, make_varlen)
 
 METRIC = "prefill tokens/s & % bf16 TC peak; decode state GB/s vs HBM peak (1×GB300)"
 NOMINAL_HBM_GBS = 8000.0
@@ -324,6 +324,79 @@ def bench_secondary(args, world, rank, dev, peaks):
     return out
 
 
+# --------------------------------------------------------------------------- per-channel decay
+def bench_gk(args, world, rank, dev, peaks):
+    """Per-key-channel decay (TileOPs KDAFwdOp, g [B,T,H,K] = -0.01 U[0,1), the draw of the
+    kda-neuron-kernels README's examples): the batched decode step at the decode workload's
+    shape (HBM-bound: the fp32 state in and out), and the token-by-token prefill at the
+    training shape."""
+    import torch
+    import delta_rule_linear_gb300 as kda
+    stream = torch.cuda.current_stream()
+    out = {}
+
+    B, H, D, nsteps = 256, 32, 128, 32
+    rng = np.random.Generator(np.random.PCG64([rank, 7]))
+    state = torch.from_numpy((0.02 * rng.standard_normal((B, H, D, D), dtype=np.float32))).to(dev)
+    toks = []
+    for s in range(nsteps):
+        st = make_gk_decode_step(B, H, D, D, s, dtype="bf16", gate_scale=0.01, seed=rank)
+        toks.append(tuple(to_dev(st[n], dev, torch.bfloat16) for n in ("q", "k", "v")) +
+                    tuple(to_dev(st[n], dev, torch.float32) for n in ("beta", "g")))
+    o = torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev)
+
+    def run(n):
+        for s in range(n):
+            q, k, v, b, g = toks[s % nsteps]
+            kda.gk_decode_step(q, k, v, b, g, state, decayed_read=True, out=o, stream=stream)
+
+    run(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(nsteps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / nsteps, world)
+    nbytes = 2.0 * B * H * D * D * 4 + B * H * D * 4      # state in + out, and g
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["gk_decode"] = {
+        "shape": dict(B=B, H=H, dk=D, dv=D), "decayed_read": True, "ms_per_step": ms,
+        "steps": nsteps, "gpu_launches": nsteps,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "bytes_per_launch": nbytes}}
+
+    Bp, T, Hp = 2, 2048, 16
+    d = make_gk(Bp, T, Hp, D, D, dtype="bf16", gate_scale=0.01, seed=rank)
+    q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
+    beta, g = (to_dev(d[n], dev, torch.float32) for n in ("beta", "g"))
+    o = torch.empty_like(v)
+    hT = torch.empty((Bp, Hp, D, D), dtype=torch.float32, device=dev)
+    nrep = max(1, min(args.steps, 5))
+
+    def step():
+        kda.gk_recurrent_fwd(q, k, v, beta, g, None, decayed_read=True, out=o, final_state=hT,
+                             stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    for _ in range(nrep):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / nrep, world)
+    out["gk_recurrent_prefill"] = {
+        "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D), "decayed_read": True, "ms_per_call": ms,
+        "tokens_per_s": Bp * T * world / (ms * 1e-3), "calls": nrep, "gpu_launches_per_call": 1,
+        "note": "CUDA-core token-by-token scan (latency-bound per token)"}
+    return out
+
+
 # --------------------------------------------------------------------------- decode
 def bench_decode(args, world, rank, dev, peaks):
     import torch
@@ -432,7 +505,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "secondary"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "secondary", "gk"], default=None,
                     help="run one workload (profiling); the default runs both")
     ap.add_argument("--prefill-T", type=int, default=0,
                     help="profiling only: override T of the prefill workload (no CPU baseline)")
@@ -472,6 +545,8 @@ def main():
     pre = bench_prefill(args, world, rank, dev, peaks, d) if d is not None else None
     dec = bench_decode(args, world, rank, dev, peaks) if args.only in (None, "decode") else None
     sec = bench_secondary(args, world, rank, dev, peaks) if args.only in (None, "secondary") else None
+    if args.only in (None, "secondary", "gk"):
+        sec = dict(sec or {}, kda_gk=bench_gk(args, world, rank, dev, peaks))
     if rank != 0:
         return
     if pre is None:
