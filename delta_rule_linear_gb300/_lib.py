@@ -24,7 +24,8 @@ STATUS = {
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace", "kda_chunk_fwd",
            "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "kda_decode_step",
-           "kda_varlen_fwd_workspace", "kda_varlen_fwd", "kda_gk_recurrent_fwd",
+           "kda_varlen_fwd_workspace", "kda_varlen_fwd", "kda_gk_chunk_fwd", "kda_gk_varlen_fwd",
+           "kda_gk_recurrent_fwd",
            "kda_gk_varlen_recurrent_fwd", "kda_gk_decode_step", "kda_query_device_error",
            "kda_diag_wait_timeout")
 
@@ -74,6 +75,12 @@ def load(path: str | None = None):
         lib.kda_varlen_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, I, F, I, I,
                                        P, Z, P]
         lib.kda_varlen_fwd.restype = I
+        lib.kda_gk_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P,
+                                         Z, P]
+        lib.kda_gk_chunk_fwd.restype = I
+        lib.kda_gk_varlen_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, I, F, I, I,
+                                          I, P, Z, P]
+        lib.kda_gk_varlen_fwd.restype = I
         lib.kda_gk_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I,
                                              P]
         lib.kda_gk_recurrent_fwd.restype = I
@@ -283,6 +290,59 @@ def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_
     _raise(rc, "kda_varlen_fwd", lib)
     if check_device:
         _raise(query_device_error(ws, stream), "kda_varlen_fwd (device)", lib)
+    return o, hT
+
+
+def gk_chunk_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None, cu_seqlens_cpu=None,
+                 scale=None, chunk_size=64, use_qk_l2norm=True, decayed_read=False, out=None,
+                 final_state=None, workspace=None, stream=None, check_device=False):
+    """kda_gk_chunk_fwd / kda_gk_varlen_fwd: chunked prefill with one log decay per key
+    channel (g with q's shape, fp32).  Packed when ``cu_seqlens`` is given (as
+    gk_recurrent_fwd).  check_device as in chunk_fwd.  Returns (o, final_state)."""
+    lib = load()
+    Bq, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    N = Bq if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (Bq, T, H, dv))
+    _check(beta, "beta", torch.float32, (Bq, T, H)); _check(g, "g", torch.float32, q.shape)
+    _check(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
+    o = out if out is not None else torch.empty((Bq, T, H, dv), dtype=q.dtype, device=q.device)
+    _check(o, "out", q.dtype, (Bq, T, H, dv))
+    hT = final_state if final_state is not None else torch.empty((N, H, dk, dv), dtype=torch.float32,
+                                                                  device=q.device)
+    _check(hT, "final_state", torch.float32, (N, H, dk, dv))
+    if cu_seqlens is None:
+        need = lib.kda_chunk_fwd_workspace(Bq, T, H, dk, dv, chunk_size, dt)
+        if need == 0:
+            raise KdaError(4, "kda_chunk_fwd_workspace", lib)
+        ws = _workspace(need, q.device, workspace)
+        rc = lib.kda_gk_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state),
+                                  _ptr(o), _ptr(hT), Bq, T, H, dk, dv, dt, float(scale or 0.0),
+                                  int(chunk_size), int(bool(use_qk_l2norm)), int(bool(decayed_read)),
+                                  _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+        _raise(rc, "kda_gk_chunk_fwd", lib)
+    else:
+        if Bq != 1:
+            raise ValueError("packed sequences need token arrays with B == 1")
+        _check(cu_seqlens, "cu_seqlens", torch.int32)
+        host = None
+        if cu_seqlens_cpu is not None:
+            host = cu_seqlens_cpu.to(torch.int32).contiguous()
+            if host.is_cuda:
+                raise ValueError("cu_seqlens_cpu must be a host tensor")
+        need = lib.kda_varlen_fwd_workspace(N, T, H, dk, dv, chunk_size, dt)
+        if need == 0:
+            raise KdaError(4, "kda_varlen_fwd_workspace", lib)
+        ws = _workspace(need, q.device, workspace)
+        rc = lib.kda_gk_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(cu_seqlens),
+                                   _ptr(host), N, T, H, dk, dv, _ptr(initial_state), _ptr(o), _ptr(hT),
+                                   dt, float(scale or 0.0), int(chunk_size), int(bool(use_qk_l2norm)),
+                                   int(bool(decayed_read)), _ptr(ws), ws.numel() * ws.element_size(),
+                                   _stream(stream))
+        _raise(rc, "kda_gk_varlen_fwd", lib)
+    if check_device:
+        _raise(query_device_error(ws, stream), "kda_gk_chunk_fwd (device)", lib)
     return o, hT
 
 

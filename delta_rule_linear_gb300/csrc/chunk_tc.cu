@@ -63,6 +63,8 @@ struct TcParams {
     const int *chunk_base;     // varlen: [nseq + 1] chunk prefix, device
     int nc_equal;              // equal length: chunks per sequence
     const float *beta, *decay; // [rows, H]
+    const float *gk;           // per-key-channel decay [rows, H, D] (per-channel kernels) or nullptr
+    int decayed_read;          // per-channel kernels: the delta term reads the decayed state
     const float *h0;           // [nseq, H, D, D] or nullptr
     float *hT;                 // [nseq, H, D, D] or nullptr
     const __nv_bfloat16 *q, *k;   // [rows, H, D]
@@ -179,14 +181,28 @@ __device__ __forceinline__ void named_arrive(int id, int count) {
 
 // B = [T' | P] and Bf = diag(f) B (bf16, MN-major SW128: row t, 64 columns s per half,
 // half 0 T' = T diag(w), half 1 P = T diag(beta)) for W consecutive columns s.. of row t
-// of T.  W = 4, 2, 1: 8-, 4- or 2-byte stores inside one 16-byte chunk.
+// of T.  W = 4, 2, 1: 8-, 4- or 2-byte stores inside one 16-byte chunk.  With PO ("P only")
+// just P = T diag(beta) is written, as one 8 KB tile at b.
 struct BTiles {
     uint8_t *b, *bf;             // B, Bf: two 8 KB halves each
     const float *w, *beta, *f;   // column weights of T', of P; row weights of Bf
 };
 
-template <int W>
+template <int W, bool PO = false>
 __device__ __forceinline__ void put_b(const BTiles &bt, int t, int s, const float *val) {
+    const int off = t * 128 + ((((s >> 3) ^ t) & 7) << 4) + (s & 7) * 2;
+    if constexpr (PO) {
+        float b1[W];
+#pragma unroll
+        for (int e = 0; e < W; ++e) b1[e] = val[e] * bt.beta[s + e];
+        if constexpr (W == 4)
+            *reinterpret_cast<uint2 *>(bt.b + off) = make_uint2(pack_bf16(b1[0], b1[1]), pack_bf16(b1[2], b1[3]));
+        else if constexpr (W == 2)
+            *reinterpret_cast<uint32_t *>(bt.b + off) = pack_bf16(b1[0], b1[1]);
+        else
+            *reinterpret_cast<__nv_bfloat16 *>(bt.b + off) = __float2bfloat16_rn(b1[0]);
+        return;
+    }
     const float ft = bt.f[t];
     float b0[W], b1[W];
 #pragma unroll
@@ -194,7 +210,6 @@ __device__ __forceinline__ void put_b(const BTiles &bt, int t, int s, const floa
         b0[e] = val[e] * bt.w[s + e];
         b1[e] = val[e] * bt.beta[s + e];
     }
-    const int off = t * 128 + ((((s >> 3) ^ t) & 7) << 4) + (s & 7) * 2;
     if constexpr (W == 4) {
         *reinterpret_cast<uint2 *>(bt.b + off) = make_uint2(pack_bf16(b0[0], b0[1]), pack_bf16(b0[2], b0[3]));
         *reinterpret_cast<uint2 *>(bt.b + 8192 + off) = make_uint2(pack_bf16(b1[0], b1[1]), pack_bf16(b1[2], b1[3]));
@@ -285,7 +300,7 @@ __device__ __forceinline__ void inv_op_x(float *sL, const float *sT, int i, int 
 }
 
 // T_ij[r][c0 .. c0+W) = -(T_ii X_ij)[r][c0 ..), also written into B and Bf
-template <int W>
+template <int W, bool PO>
 __device__ __forceinline__ void inv_op_t(const float *sL, float *sT, const BTiles &bt, int i, int j,
                                          int r, int c0) {
     constexpr int P = kLP;
@@ -329,10 +344,10 @@ __device__ __forceinline__ void inv_op_t(const float *sL, float *sT, const BTile
     if constexpr (W == 4) *reinterpret_cast<float4 *>(Tij) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     else if constexpr (W == 2) *reinterpret_cast<float2 *>(Tij) = make_float2(acc[0], acc[1]);
     else Tij[0] = acc[0];
-    put_b<W>(bt, 16 * i + r, 16 * j + c0, acc);
+    put_b<W, PO>(bt, 16 * i + r, 16 * j + c0, acc);
 }
 
-template <int NT, typename IdleWork>
+template <int NT, bool PO = false, typename IdleWork>
 __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int tid, int bar,
                                      IdleWork &&idle) {
     static_assert(NT == 256, "the work split below assumes 256 threads");
@@ -364,9 +379,9 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
         for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
     } else {
         // the other 192 threads zero the six strictly-upper 16 x 16 blocks of B and Bf:
-        // 6 blocks x 16 rows x 2 chunks x 4 tiles (B, Bf; T' and P halves)
+        // 6 blocks x 16 rows x 2 chunks x 4 tiles (B, Bf; T' and P halves), or of P alone
         const int zt = warp < 4 ? warp * 16 + (lane - 16) : 64 + (warp - 4) * 32 + lane;
-        for (int idx = zt; idx < 6 * 16 * 2 * 4; idx += NT - 64) {
+        for (int idx = zt; idx < 6 * 16 * 2 * (PO ? 1 : 4); idx += NT - 64) {
             const int ch = idx & 1, r = (idx >> 1) & 15, blk = (idx >> 5) % 6, tile = idx / 192;
             const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);          // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
             const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
@@ -386,11 +401,11 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
         inv_op_x<4>(sL, sT, i, j, j, j + 1, false, r4, c4);
         const float4 d = *reinterpret_cast<const float4 *>(sT + (16 * slot + r4) * P + 16 * slot + c4);
         const float dv[4] = {d.x, d.y, d.z, d.w};
-        put_b<4>(bt, 16 * slot + r4, 16 * slot + c4, dv);
+        put_b<4, PO>(bt, 16 * slot + r4, 16 * slot + c4, dv);
     }
     named_sync(bar, NT);
     // S1: T_10, T_21, T_32; X_31 = L_31 T_11
-    if (slot < 3) inv_op_t<4>(sL, sT, bt, slot + 1, slot, r4, c4);
+    if (slot < 3) inv_op_t<4, PO>(sL, sT, bt, slot + 1, slot, r4, c4);
     else inv_op_x<4>(sL, sT, 3, 1, 1, 2, false, r4, c4);
     named_sync(bar, NT);
     // S2: X_20 += L_21 T_10;  X_31 += L_32 T_21;  X_30 = L_30 T_00 + L_31 T_10 (two column halves)
@@ -405,15 +420,15 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
     {
         const int half = tid >> 7, t128 = tid & 127;
         const int r2 = t128 >> 3, c2 = (t128 & 7) * 2;
-        if (half == 0) inv_op_t<2>(sL, sT, bt, 2, 0, r2, c2);
-        else inv_op_t<2>(sL, sT, bt, 3, 1, r2, c2);
+        if (half == 0) inv_op_t<2, PO>(sL, sT, bt, 2, 0, r2, c2);
+        else inv_op_t<2, PO>(sL, sT, bt, 3, 1, r2, c2);
     }
     named_sync(bar, NT);
     // S4: X_30 += L_32 T_20 (one output per thread)
     inv_op_x<1>(sL, sT, 3, 0, 2, 3, true, tid >> 4, tid & 15);
     named_sync(bar, NT);
     // S5: T_30
-    inv_op_t<1>(sL, sT, bt, 3, 0, tid >> 4, tid & 15);
+    inv_op_t<1, PO>(sL, sT, bt, 3, 0, tid >> 4, tid & 15);
     fence_proxy_async();   // B, Bf are tensor-core operands
     tc_fence_before();
     named_sync(bar, NT);
@@ -893,6 +908,456 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
 }
 
 // ---------------------------------------------------------------------------------
+// prep with a decay per key channel (TileOPs KDAFwdOp: g [.., K]; GLARecurrentFwdOp:
+// diag(exp(gk)) applied to the state).  E_c keeps its form; the decays become diagonal
+// per channel.  With G_t[c] the in-chunk cumulative log decay of channel c (inclusive),
+// R_t = G_t when the delta term reads the decayed state and G_{t-1} otherwise, and
+//   K_R = [k^_t * exp(R_t)],  Q_G = [q~_t * exp(G_t)],  K~ = [k^_s * exp(G_n - G_s)]
+// ("*" elementwise, rows t), P = T diag(beta):
+//
+//   L[t][s]   = beta_t sum_c k^_t[c] k^_s[c] exp(R_t[c] - G_s[c])   (s < t),  T = (I + L)^{-1}
+//   Aqk[t][s] = sum_c q~_t[c] k^_s[c] exp(G_t[c] - G_s[c])          (s <= t)
+//   [ S_next ]   [ diag(exp G_n) - Z1 K_R   Z1 ] [ S ]
+//   [   O    ] = [ Q_G - Z2 K_R             Z2 ] [ V ],    Z1 = K~^T P,  Z2 = Aqk P
+//
+// (W = P K_R is never formed: Z1 K_R = K~^T W and Z2 K_R = Aqk W.)  The factor inside L
+// and Aqk is split over 16-token sub-blocks, the sub-chunk form of the kda-neuron-kernels
+// README: for rows t of sub-block b and G_ref the cumulative decay at the token before it,
+//   exp(R_t - G_s) = exp(R_t - G_ref) exp(G_ref - G_s),
+// so the Gram rows of sub-block b are one tensor-core product of two scaled copies of k
+// and q.  The row factor is <= 1, and so is the column factor of every earlier sub-block;
+// only the sub-block's own columns get a factor above 1, up to exp of its 16-token decay.
+// When that span passes kSpanLog2 in some channel, the sub-block's diagonal entries are
+// recomputed on CUDA cores with the exact factor per element, so the result is exact for
+// any decay.  One group of 256 threads per CTA (the scaled copies take the shared memory
+// of the second); E_c goes to global memory by ordinary stores from the epilogues.
+// ---------------------------------------------------------------------------------
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSpanLog2 = 60.f * kLog2e;    // sub-block spans above e^60 take the exact path
+constexpr float kClampLog2 = 100.f;           // keeps the factors of such a sub-block finite
+
+template <int D>
+struct GkSmem {
+    static constexpr int NB = D / 64;
+    static constexpr int KQ = 0;                          // raw [K;Q]: NB x 16 KB, K-major SW128
+    static constexpr int KRQG = KQ + NB * 16384;          // [K_R; Q_G], same layout
+    static constexpr int KT = KRQG + NB * 16384;          // K~: NB x 8 KB
+    static constexpr int GF = KT + NB * 8192;             // g, then G in log2 units: fp32 [64][D]
+    static constexpr int OV = GF + 64 * D * 4;            // Gram operands; later L, T | P | Aqk; Z ops
+    static constexpr int GA = OV;                         // column operands: NB x 160 rows x 128 B
+    static constexpr int GB = GA + NB * 160 * 128;        // row operands: NB x 128 rows x 128 B
+    static constexpr int LT_BYTES = 2 * 64 * kLP * 4;     // L and T fp32
+    static constexpr int PT = OV + LT_BYTES;              // P: MN-major 64 x 64
+    static constexpr int AQ = PT + 8192;                  // Aqk: K-major 64 x 64
+    static constexpr int OV_BYTES = (GB - OV + NB * 128 * 128) > (AQ + 8192 - OV)
+                                        ? (GB - OV + NB * 128 * 128) : (AQ + 8192 - OV);
+    static constexpr int SD = OV + OV_BYTES;              // exact diagonal sub-blocks: fp32 [4][2][16][16]
+    static constexpr int MISC = SD + 4 * 2 * 256 * 4;
+    // MISC: beta [2][64] | kn [64] | qn [64] | exp(G_n) [D] | prefix totals [4][D] | span flags [4]
+    static constexpr int CTRL = MISC + (2 * 64 + 64 + 64 + D + 4 * D + 4) * 4;
+    static constexpr int BYTES = ((CTRL + 64 + 1023) / 1024) * 1024;
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// g of one chunk (fp32 rows, zero past the chunk's valid tokens) by 16-byte cp.async copies
+// (warps other than 0 and 4, as load_rows)
+template <int D>
+__device__ __forceinline__ void load_g(const TcParams &p, float *gf, const ChunkItem &it, int tid) {
+    constexpr int PPR = D / 4;
+    const int w = tid >> 5;
+    if (w == 0 || w == 4) return;
+    const int lt = (w < 4 ? tid - 32 : tid - 64);
+    for (int pidx = lt; pidx < 64 * PPR; pidx += kGroupThreads - 64) {
+        const int row = pidx / PPR, pc = pidx % PPR;
+        const bool in = row < it.nv;
+        const float *src = p.gk + ((it.row0 + (in ? row : 0)) * p.H + it.h) * D + 4 * pc;
+        cp_async16(gf + row * D + 4 * pc, src, in ? 16u : 0u);
+    }
+    cp_async_commit();
+}
+__device__ __forceinline__ void load_beta(const TcParams &p, float *mbeta, const ChunkItem &it, int tid) {
+    const int t = tid - 64;   // warps 2, 3
+    if (t >= 0 && t < 64) {
+        const long gi = (it.row0 + (t < it.nv ? t : 0)) * p.H + it.h;
+        cp_async4(mbeta + t, p.beta + gi, t < it.nv ? 4u : 0u);
+    }
+    cp_async_commit();
+}
+
+template <int D>
+__device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, uint32_t tm, int tid,
+                                              int bar, long item, long stride) {
+    using Ly = GkSmem<D>;
+    constexpr int NB = D / 64;
+    constexpr int R = D + 64;
+    constexpr int NP = D / 2;                 // channel pairs
+    constexpr int TPG = 64 / (256 / NP);      // tokens per build thread: 16 (D=128) or 8 (D=64)
+    constexpr int NQ = 256 / D;               // token quarters of the prefix pass
+    constexpr int QLEN = 64 / NQ;
+    PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(sm + Ly::CTRL);
+    const int warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hh = warp >> 2;
+    const int i128 = 32 * q4 + lane;
+    const int i64 = 16 * q4 + lane;
+    const bool has64 = lane < 16;
+    const uint32_t tq = (uint32_t)(32 * q4) << 16;
+
+    uint8_t *sKQ = sm + Ly::KQ;
+    uint8_t *sKR = sm + Ly::KRQG;
+    uint8_t *sKT = sm + Ly::KT;
+    float *gf = reinterpret_cast<float *>(sm + Ly::GF);
+    uint8_t *sGA = sm + Ly::GA;
+    uint8_t *sGB = sm + Ly::GB;
+    float *sL = reinterpret_cast<float *>(sm + Ly::OV);
+    float *sT = sL + 64 * kLP;
+    uint8_t *sP = sm + Ly::PT;
+    uint8_t *sA = sm + Ly::AQ;
+    uint8_t *sZ1 = sm + Ly::OV;                 // after MMA2: Z1 (K-major D x 64)
+    uint8_t *sZ2 = sm + Ly::OV + D * 128;       // [-Z2 | I] (K-major 64 x 128)
+    static_assert(D * 128 + 16384 <= 2 * 64 * kLP * 4, "the Z operands overlay L and T only");
+    float *sd = reinterpret_cast<float *>(sm + Ly::SD);
+    float *mbeta2 = reinterpret_cast<float *>(sm + Ly::MISC);
+    float *mkn = mbeta2 + 128, *mqn = mkn + 64, *meGn = mqn + 64, *mtot = meGn + D;
+    int *mspan = reinterpret_cast<int *>(mtot + 4 * D);
+
+    ChunkItem cur;
+    while (item < p.n_items && !item_info(p, item, cur)) item += stride;
+    if (item >= p.n_items) return;
+    load_rows<D>(p, sKQ, cur, tid, true);
+    load_rows<D>(p, sKQ, cur, tid, false);
+    load_g<D>(p, gf, cur, tid);
+    load_beta(p, mbeta2, cur, tid);
+    long pend = -1;   // kStoreThread: slot whose E_c stores are issued and not yet published
+    const bool decayed = p.decayed_read != 0;
+
+    for (uint32_t it = 0;; ++it) {
+        const uint32_t ph = it & 1;
+        const int nv = cur.nv;
+        float *mbeta = mbeta2 + 64 * (it & 1);
+        if (tid < 4) mspan[tid] = 0;
+        cp_async_wait_all();
+        named_sync(bar, kGroupThreads);
+        bool ok = ctl->fail == 0;
+        long nitem = item + stride;
+        ChunkItem nx;
+        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
+        const bool more = nitem < p.n_items;
+
+        // ---- norms of the k and q rows (zero past the valid tokens); prefix over tokens of g
+        {
+            const int r = tid >> 1, part = tid & 1, t = r & 63;
+            const bool isq = r >= 64;
+            float ss = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < NB * 4; ++cc) {
+                const int chunk = part * NB * 4 + cc;
+                const uint4 w = *reinterpret_cast<const uint4 *>(sKQ + (chunk >> 3) * 16384 + (isq ? 8192 : 0) +
+                                                                 t * 128 + (((chunk ^ t) & 7) << 4));
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = bf16lo(ws[e]), b = bf16hi(ws[e]);
+                    ss = fmaf(a, a, fmaf(b, b, ss));
+                }
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            if (part == 0) {
+                const float inv = p.use_l2 ? 1.f / fmaxf(sqrtf(ss), kNormEps) : 1.f;
+                if (isq) mqn[t] = t < nv ? p.scale * inv : 0.f;
+                else mkn[t] = t < nv ? inv : 0.f;
+            }
+        }
+        {   // pass A: each quarter's inclusive prefix in place, in log2 units
+            const int c = tid % D, j = tid / D;
+            float acc = 0.f;
+            for (int t = j * QLEN; t < (j + 1) * QLEN; ++t) {
+                acc = fmaf(gf[t * D + c], kLog2e, acc);
+                gf[t * D + c] = acc;
+            }
+            mtot[j * D + c] = acc;
+        }
+        named_sync(bar, kGroupThreads);
+        {   // pass B: add the totals of the earlier quarters
+            const int c = tid % D, j = tid / D;
+            float off = 0.f;
+            for (int jj = 0; jj < j; ++jj) off += mtot[jj * D + c];
+            if (j > 0)
+                for (int t = j * QLEN; t < (j + 1) * QLEN; ++t) gf[t * D + c] += off;
+        }
+        named_sync(bar, kGroupThreads);
+
+        // ---- build: K~, [K_R; Q_G] and the sub-block Gram operands, channel pair cp of
+        // tokens [t0, t0 + TPG) (all inside sub-block b)
+        {
+            const int cp = tid % NP, c0 = 2 * cp;
+            const int t0 = (tid / NP) * TPG, b = t0 >> 4;
+            const float2 gn = *reinterpret_cast<const float2 *>(gf + 63 * D + c0);
+            if (t0 == 0) {
+                meGn[c0] = ex2f(gn.x);
+                meGn[c0 + 1] = ex2f(gn.y);
+            }
+            float2 gref[4];
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+                gref[bb] = bb == 0 ? make_float2(0.f, 0.f)
+                                   : *reinterpret_cast<const float2 *>(gf + (16 * bb - 1) * D + c0);
+            if ((t0 & 15) == 0) {   // span of sub-block b in these two channels
+                const float2 ge = *reinterpret_cast<const float2 *>(gf + (16 * b + 15) * D + c0);
+                if (fmaxf(gref[b].x - ge.x, gref[b].y - ge.y) > kSpanLog2) atomicOr(mspan + b, 1);
+            }
+            float2 gprev = t0 == 0 ? make_float2(0.f, 0.f)
+                                   : *reinterpret_cast<const float2 *>(gf + (t0 - 1) * D + c0);
+            for (int t = t0; t < t0 + TPG; ++t) {
+                const float2 g = *reinterpret_cast<const float2 *>(gf + t * D + c0);
+                const float2 rr = decayed ? g : gprev;
+                const uint32_t kw = *reinterpret_cast<const uint32_t *>(sKQ + kmajor_sw128_offset(128, t, c0));
+                const uint32_t qw = *reinterpret_cast<const uint32_t *>(sKQ + kmajor_sw128_offset(128, 64 + t, c0));
+                const float kn = mkn[t], qn = mqn[t];
+                const float k0 = bf16lo(kw) * kn, k1 = bf16hi(kw) * kn;
+                const float qa = bf16lo(qw) * qn, qb = bf16hi(qw) * qn;
+                const float eg0 = ex2f(g.x), eg1 = ex2f(g.y);
+                const float er0 = decayed ? eg0 : ex2f(rr.x), er1 = decayed ? eg1 : ex2f(rr.y);
+                *reinterpret_cast<uint32_t *>(sKT + kmajor_sw128_offset(64, t, c0)) =
+                    pack_bf16(k0 * ex2f(gn.x - g.x), k1 * ex2f(gn.y - g.y));
+                *reinterpret_cast<uint32_t *>(sKR + kmajor_sw128_offset(128, t, c0)) = pack_bf16(k0 * er0, k1 * er1);
+                *reinterpret_cast<uint32_t *>(sKR + kmajor_sw128_offset(128, 64 + t, c0)) = pack_bf16(qa * eg0, qb * eg1);
+                // row operands of sub-block b: k rows 32b + j, q rows 32b + 16 + j
+                const int j = t - 16 * b;
+                const float fk0 = ex2f(rr.x - gref[b].x), fk1 = ex2f(rr.y - gref[b].y);
+                const float fq0 = decayed ? fk0 : ex2f(g.x - gref[b].x);
+                const float fq1 = decayed ? fk1 : ex2f(g.y - gref[b].y);
+                *reinterpret_cast<uint32_t *>(sGB + kmajor_sw128_offset(128, 32 * b + j, c0)) = pack_bf16(k0 * fk0, k1 * fk1);
+                *reinterpret_cast<uint32_t *>(sGB + kmajor_sw128_offset(128, 32 * b + 16 + j, c0)) =
+                    pack_bf16(qa * fq0, qb * fq1);
+                // column operands of sub-blocks b' >= b: row off(b') + t, factor exp(G_ref(b') - G_t)
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+                    if (bb < b) continue;
+                    const int off = bb == 0 ? 0 : (bb == 1 ? 16 : (bb == 2 ? 48 : 96));
+                    const float f0 = ex2f(fminf(gref[bb].x - g.x, kClampLog2));
+                    const float f1 = ex2f(fminf(gref[bb].y - g.y, kClampLog2));
+                    *reinterpret_cast<uint32_t *>(sGA + kmajor_sw128_offset(160, off + t, c0)) =
+                        pack_bf16(k0 * f0, k1 * f1);
+                }
+                gprev = g;
+            }
+        }
+        fence_proxy_async();
+        named_sync(bar, kGroupThreads);
+
+        // ---- sub-blocks whose decay span is too wide for the split: exact diagonal entries
+        for (int b = 0; b < 4; ++b) {
+            if (mspan[b] == 0) continue;   // uniform: read after the barrier
+            const int tj = tid >> 4, sj = tid & 15, t = 16 * b + tj, s = 16 * b + sj;
+            float aq = 0.f, al = 0.f;
+            if (sj <= tj) {
+                for (int c = 0; c < D; ++c) {
+                    const float kt = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                         sKQ + kmajor_sw128_offset(128, t, c))) * mkn[t];
+                    const float qt = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                         sKQ + kmajor_sw128_offset(128, 64 + t, c))) * mqn[t];
+                    const float ks = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                         sKQ + kmajor_sw128_offset(128, s, c))) * mkn[s];
+                    const float gt = gf[t * D + c], gs = gf[s * D + c];
+                    const float rt = decayed ? gt : (t == 0 ? 0.f : gf[(t - 1) * D + c]);
+                    aq = fmaf(qt * ks, ex2f(gt - gs), aq);
+                    if (sj < tj) al = fmaf(kt * ks, ex2f(rt - gs), al);
+                }
+            }
+            sd[(b * 2 + 0) * 256 + tj * 16 + sj] = al;
+            sd[(b * 2 + 1) * 256 + tj * 16 + sj] = aq;
+        }
+        // raw q, k and g are no longer read: the next chunk's loads start now
+        float *mbeta_next = mbeta2 + 64 * ((it + 1) & 1);
+        if (mspan[0] | mspan[1] | mspan[2] | mspan[3]) named_sync(bar, kGroupThreads);
+        if (ok && more) {
+            load_rows<D>(p, sKQ, nx, tid, true);
+            load_rows<D>(p, sKQ, nx, tid, false);
+            load_g<D>(p, gf, nx, tid);
+            load_beta(p, mbeta_next, nx, tid);
+        }
+
+        // ---- MMA1: sub-block b's Gram rows, transposed: D1[s][32 b + j] for s < 16 (b + 1):
+        // column operand rows s (M = 64), row operand k rows then q rows of sub-block b (N = 32)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16_f32(64, 32, false, false);
+            const uint32_t ga = smem_u32(sGA), gb = smem_u32(sGB);
+            for (int b = 0; b < 4; ++b) {
+                const int off = b == 0 ? 0 : (b == 1 ? 16 : (b == 2 ? 48 : 96));
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_bf16_ss(tm + 32 * b, desc_kmajor_sw128(ga + off * 128, 160, ks),
+                                desc_kmajor_sw128(gb + 32 * b * 128, 128, ks), id, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&ctl->bar_mma);
+        }
+        if (tid == kStoreThread && pend >= 0) {   // the previous chunk's E_c, while MMA1 runs
+            release_slot(p, pend);
+            pend = -1;
+        }
+        if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
+        tc_fence_after();
+
+        // ---- epilogue 1: L (fp32, rows t) and Aqk (bf16 operand) from the transposed rows s
+        {
+            const int s = i64, bs = s >> 4;
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int b = 2 * hh + k2;
+                uint32_t v[32];
+                tmem_ld32(tm + tq + 32 * b, v);
+                tmem_ld_wait();
+                if (has64) {
+                    const bool exact = mspan[b] != 0 && bs == b;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int t = 16 * b + j;
+                        float lval = 0.f, aval = 0.f;
+                        if (b >= bs) {
+                            lval = exact ? sd[(b * 2) * 256 + j * 16 + (s & 15)] : __uint_as_float(v[j]);
+                            aval = exact ? sd[(b * 2 + 1) * 256 + j * 16 + (s & 15)] : __uint_as_float(v[16 + j]);
+                            lval = s < t ? mbeta[t] * lval : 0.f;
+                            aval = s <= t ? aval : 0.f;
+                            sL[t * kLP + s] = lval;
+                        }
+                        *reinterpret_cast<__nv_bfloat16 *>(sA + kmajor_sw128_offset(64, t, s)) =
+                            __float2bfloat16_rn(aval);
+                    }
+                }
+            }
+        }
+        fence_proxy_async();
+        named_sync(bar, kGroupThreads);
+        ok = ctl->fail == 0;
+
+        // ---- T = (I + L)^{-1}, written as P = T diag(beta) (MN-major: row t, columns s)
+        invert_unit_lower_64<kGroupThreads, true>(sL, sT, BTiles{sP, nullptr, nullptr, mbeta, nullptr}, tid,
+                                                  bar, [] {});
+
+        // ---- MMA2: D2a[:, 0:64] = K~^T P (M = D);  D2b[:, 128:192] = Aqk P (M = 64)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t ida = idesc_bf16_f32(D, 64, true, true);
+            const uint32_t idb = idesc_bf16_f32(64, 64, false, true);
+            const uint32_t kt = smem_u32(sKT), pp = smem_u32(sP), aa = smem_u32(sA);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tm, desc_mnmajor_sw128(kt, 64, ks), desc_mnmajor_sw128(pp, 64, ks), ida,
+                            ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tm + 128, desc_kmajor_sw128(aa, 64, ks), desc_mnmajor_sw128(pp, 64, ks), idb,
+                            ks > 0 ? 1u : 0u);
+            mma_commit(&ctl->bar_mma);
+        }
+        if (ok && !mbar_wait(&ctl->bar_mma, ph ^ 1u, kWaitNs)) ctl->fail = 1;
+        tc_fence_after();
+
+        // ---- epilogue 2: Z1 = D2a -> E[i][D + s] and MMA3a's A; Z2 = D2b -> E[D + t][D + s]
+        // and MMA3b's A = [-Z2 | I]
+        __nv_bfloat16 *Eslot = p.E + (size_t)cur.slot * R * R;
+        {
+            uint32_t v[32];
+            tmem_ld32(tm + tq + 32 * hh, v);
+            tmem_ld_wait();
+            const bool has_row = (D == 128) || has64;
+            const int i = (D == 128) ? i128 : i64;
+            if (has_row && ok) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint4 w = pack8u(v + 8 * cc);
+                    const int col = 32 * hh + 8 * cc;
+                    *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((((col >> 3) ^ i) & 7) << 4)) = w;
+                    *reinterpret_cast<uint4 *>(Eslot + (size_t)i * R + D + col) = w;
+                }
+            }
+            tmem_ld32(tm + tq + 128 + 32 * hh, v);
+            tmem_ld_wait();
+            if (has64 && ok) {
+                const int t = i64;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int col = 32 * hh + 8 * cc;
+                    const int off = t * 128 + ((((col >> 3) ^ t) & 7) << 4);
+                    *reinterpret_cast<uint4 *>(sZ2 + off) = pack8un(v + 8 * cc);
+                    *reinterpret_cast<uint4 *>(Eslot + (size_t)(D + t) * R + D + col) = pack8u(v + 8 * cc);
+                    float dg[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) dg[e] = (col + e == t) ? 1.f : 0.f;
+                    *reinterpret_cast<uint4 *>(sZ2 + 8192 + off) = pack8(dg);
+                }
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        named_sync(bar, kGroupThreads);
+        ok = ctl->fail == 0;
+
+        // ---- MMA3: D3a[:, 0:D] = Z1 K_R (M = D);  D3b[:, 128:128+D] = [-Z2 | I] [K_R; Q_G] (M = 64)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t ida = idesc_bf16_f32(D, D, false, true);
+            const uint32_t idb = idesc_bf16_f32(64, D, false, true);
+            const uint32_t kr = smem_u32(sKR), z1 = smem_u32(sZ1), z2 = smem_u32(sZ2);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tm, desc_kmajor_sw128(z1, D, ks), desc_mnmajor_sw128(kr, 128, ks), ida,
+                            ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ss(tm + 128, desc_kmajor_sw128(z2, 64, ks), desc_mnmajor_sw128(kr, 128, ks), idb,
+                            ks > 0 ? 1u : 0u);
+            mma_commit(&ctl->bar_mma);
+        }
+        if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
+        tc_fence_after();
+
+        // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
+        {
+            constexpr int HALF = D / 2;
+            const bool has_row = (D == 128) || has64;
+            const int i = (D == 128) ? i128 : i64;
+            const int t = i64;
+            uint32_t v[HALF];
+            tmem_ld32(tm + tq + 128 + hh * HALF, *reinterpret_cast<uint32_t(*)[32]>(v));
+            if (HALF == 64) tmem_ld32(tm + tq + 128 + hh * HALF + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * (HALF / 64)));
+            tmem_ld_wait();
+            if (has64 && ok) {   // E[D + t][j] = Q_G[t][j] - (Z2 K_R)[t][j] = D3b[t][j]
+#pragma unroll
+                for (int cc = 0; cc < HALF / 8; ++cc)
+                    *reinterpret_cast<uint4 *>(Eslot + (size_t)(D + t) * R + hh * HALF + 8 * cc) =
+                        pack8u(v + 8 * cc);
+            }
+            tmem_ld32(tm + tq + hh * HALF, *reinterpret_cast<uint32_t(*)[32]>(v));
+            if (HALF == 64) tmem_ld32(tm + tq + hh * HALF + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * (HALF / 64)));
+            tmem_ld_wait();
+            if (has_row && ok) {   // E[i][j] = exp(G_n[i]) delta_ij - (Z1 K_R)[i][j]
+                const float gi = meGn[i];
+#pragma unroll
+                for (int cc = 0; cc < HALF / 8; ++cc) {
+                    const int col = hh * HALF + 8 * cc;
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = (col + e == i ? gi : 0.f) - __uint_as_float(v[8 * cc + e]);
+                    *reinterpret_cast<uint4 *>(Eslot + (size_t)i * R + col) = pack8(f);
+                }
+            }
+        }
+        tc_fence_before();
+        named_sync(bar, kGroupThreads);   // every thread's E_c stores are issued
+        const bool failed = ctl->fail != 0;
+        if (tid == 0 && failed) record_error(p.ws, 2);
+        if (tid == kStoreThread && p.flags && !failed) pend = cur.slot;
+        if (!more || failed) break;
+        item = nitem;
+        cur = nx;
+    }
+    cp_async_wait_all();
+    if (tid == kStoreThread && pend >= 0) release_slot(p, pend);
+}
+
+// ---------------------------------------------------------------------------------
 // chain -- one CTA per (sequence, head), transposed so that M = dv:
 //
 //   D^T[j][r] = sum_k A[j][k] E_c[r][k],   A = [S^T | V_c^T]   (dv rows, D + 64 columns)
@@ -1185,7 +1650,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
 // others two prep groups each.  With nchain > 0 the launch is cooperative, so that
 // every chain's producers are co-resident with the prep groups they wait for.
 // ---------------------------------------------------------------------------------
-template <int D>
+template <int D, bool GK>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant__ CUtensorMap map_q,
                                                            const __grid_constant__ CUtensorMap map_k,
                                                            const __grid_constant__ CUtensorMap map_v,
@@ -1199,6 +1664,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     }
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, grp = tid >> 8;
+    if constexpr (GK) {   // one prep group per CTA; the other 256 threads only join the barriers
+        if (tid == 0) {
+            PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(sm + GkSmem<D>::CTRL);
+            mbar_init(&ctl->bar_mma, 1);
+            fence_mbar_init();
+            ctl->fail = 0;
+        }
+        if (tid < 32) {
+            tmem_alloc(&tmem_base, 256);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (grp == 0)
+            prep_group_gk<D>(p, sm, tmem_base, tid, 1, (long)((int)blockIdx.x - p.nchain),
+                             (long)((int)gridDim.x - p.nchain));
+        tc_fence_before();
+        __syncthreads();
+        if (tid < 32) {
+            __syncwarp();
+            tmem_dealloc(tmem_base, 256);
+        }
+        return;
+    }
     uint8_t *gsm = sm + grp * PrepSmem<D>::GROUP;
     if ((tid & (kGroupThreads - 1)) == 0) {
         PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(gsm + PrepSmem<D>::CTRL);
@@ -1301,7 +1791,7 @@ bool map_E(CUtensorMap *m, const void *base, long slots, int R) {
 constexpr size_t kTableBytes(int nseq) { return (((size_t)(nseq + 1) * 4 + 255) / 256) * 256; }
 constexpr size_t kFlagBytes(long slots) { return (((size_t)slots * 4 + 255) / 256) * 256; }
 
-template <int D>
+template <int D, bool GK>
 cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
     constexpr int R = D + 64;
     using Cf = ChainCfg<D>;
@@ -1309,7 +1799,9 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.nseq = a.nseq; p.H = a.H; p.T = a.T; p.use_l2 = a.use_l2; p.scale = a.scale;
     p.cu_seqlens = a.cu_seqlens;
     p.nc_equal = (a.T + kC - 1) / kC;
-    p.beta = a.beta; p.decay = a.decay; p.h0 = a.h0; p.hT = a.hT;
+    p.beta = a.beta; p.decay = GK ? nullptr : a.decay; p.h0 = a.h0; p.hT = a.hT;
+    p.gk = GK ? a.gk : nullptr;
+    p.decayed_read = a.decayed_read;
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.k = static_cast<const __nv_bfloat16 *>(a.k);
     p.rows = total_rows;
@@ -1337,9 +1829,9 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     int dev = 0, nsm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int prep_smem = 2 * PrepSmem<D>::GROUP + 1024;
+    const int prep_smem = GK ? GkSmem<D>::BYTES + 1024 : 2 * PrepSmem<D>::GROUP + 1024;
     const int one_smem = std::max(prep_smem, Cf::SMEM);
-    e = cudaFuncSetAttribute(tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, one_smem);
+    e = cudaFuncSetAttribute(tc_kernel<D, GK>, cudaFuncAttributeMaxDynamicSharedMemorySize, one_smem);
     if (e != cudaSuccess) return e;
 
     // Single launch when the chains take at most half of the SMs: chains and prep
@@ -1361,7 +1853,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc_kernel<D>, mq, mk, mv, me, pf);
+        e = cudaLaunchKernelEx(&cfg, tc_kernel<D, GK>, mq, mk, mv, me, pf);
         if (e == cudaSuccess) return cudaSuccess;
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         (void)cudaGetLastError();   // fewer SMs available than reported: two launches
@@ -1372,8 +1864,8 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.chunk_major = 0;
     p.n_items = slots_bound;
     p.nchain = 0;
-    const long ctas = std::min<long>((slots_bound + 1) / 2, (long)nsm);
-    tc_kernel<D><<<(unsigned)ctas, kTcThreads, prep_smem, st>>>(mq, mk, mv, me, p);
+    const long ctas = std::min<long>(GK ? slots_bound : (slots_bound + 1) / 2, (long)nsm);
+    tc_kernel<D, GK><<<(unsigned)ctas, kTcThreads, prep_smem, st>>>(mq, mk, mv, me, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(chain_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
@@ -1410,8 +1902,13 @@ cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t s
 
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
     if (slots_bound >= (1L << 31) || total_rows >= (1L << 31)) return cudaErrorInvalidValue;   // 32-bit indexing
-    if (a.dk == 128) return run_tc<128>(a, total_rows, slots_bound, st);
-    if (a.dk == 64) return run_tc<64>(a, total_rows, slots_bound, st);
+    if (a.per_channel) {
+        if (a.dk == 128) return run_tc<128, true>(a, total_rows, slots_bound, st);
+        if (a.dk == 64) return run_tc<64, true>(a, total_rows, slots_bound, st);
+        return cudaErrorInvalidValue;
+    }
+    if (a.dk == 128) return run_tc<128, false>(a, total_rows, slots_bound, st);
+    if (a.dk == 64) return run_tc<64, false>(a, total_rows, slots_bound, st);
     return cudaErrorInvalidValue;
 }
 

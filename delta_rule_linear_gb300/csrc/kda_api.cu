@@ -110,6 +110,8 @@ static kda_status run_prefill(SeqBatch &a, bool chunked, long total_rows, cudaSt
     } else if (chunk_tc_supported(a.dk, a.dv, a.chunk, a.dtype)) {
         const long bound = chunk_tc_slots_bound(a.nseq, total_rows, a.H, a.T, a.cu_seqlens != nullptr);
         e = launch_chunk_tc(a, total_rows, bound, st);
+    } else if (a.per_channel) {
+        e = launch_recurrent(a, st);   // the per-channel decay has no CUDA-core chunk kernel
     } else {
         e = launch_chunk_simt(a, st);
     }
@@ -218,6 +220,78 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v, const flo
     if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
     // Every sequence runs the chunk loop from its own cu_seqlens range; a sequence
     // of length 0 falls through the loop and stores its initial state.
+    return run_prefill(a, true, total_T, st);
+}
+
+kda_status kda_gk_chunk_fwd(const void *q, const void *k, const void *v, const float *beta,
+                            const float *g, const float *initial_state, void *o, float *final_state,
+                            int B, int T, int H, int dk, int dv, kda_dtype dtype, float scale,
+                            int chunk_size, int use_qk_l2norm, int decayed_read, void *ws,
+                            size_t ws_bytes, kda_stream_t stream) {
+    if (B < 0 || T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, nullptr, initial_state, o, final_state,
+                                (long)B * T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (!aligned16(g)) return KDA_ERR_ALIGN;
+    if (!supported_chunk(chunk_size)) return KDA_ERR_UNSUPPORTED;
+    const size_t need = kda_chunk_fwd_workspace(B, T, H, dk, dv, chunk_size, dtype);
+    if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
+    SeqBatch a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
+    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.o = o; a.hT = final_state; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
+    a.dk = dk; a.dv = dv; a.chunk = chunk_size;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    a.ws = static_cast<WsHeader *>(ws);
+    a.ws_body = static_cast<char *>(ws) + kWsHeader;
+    a.ws_body_bytes = ws_bytes - kWsHeader;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
+    return run_prefill(a, true, (long)B * T, st);
+}
+
+kda_status kda_gk_varlen_fwd(const void *q, const void *k, const void *v, const float *beta,
+                             const float *g, const int *cu_seqlens, const int *cu_seqlens_host,
+                             int N, int total_T, int H, int dk, int dv, const float *initial_state,
+                             void *o, float *final_state, kda_dtype dtype, float scale,
+                             int chunk_size, int use_qk_l2norm, int decayed_read, void *ws,
+                             size_t ws_bytes, kda_stream_t stream) {
+    if (N < 0 || total_T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, nullptr, initial_state, o, final_state,
+                                total_T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (!aligned16(g)) return KDA_ERR_ALIGN;
+    if (!supported_chunk(chunk_size)) return KDA_ERR_UNSUPPORTED;
+    if (N > 0 && !cu_seqlens) return KDA_ERR_NULL;
+    if (!aligned4(cu_seqlens)) return KDA_ERR_ALIGN;
+    int max_len = total_T;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != total_T) return KDA_ERR_INDEX;
+        max_len = 0;
+        for (int n = 0; n < N; ++n) {
+            const int L = cu_seqlens_host[n + 1] - cu_seqlens_host[n];
+            if (L < 0) return KDA_ERR_INDEX;
+            if (L > max_len) max_len = L;
+        }
+    }
+    const size_t need = kda_varlen_fwd_workspace(N, total_T, H, dk, dv, chunk_size, dtype);
+    if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
+    if (N == 0) return KDA_OK;
+    SeqBatch a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
+    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.o = o; a.hT = final_state; a.cu_seqlens = cu_seqlens; a.nseq = N; a.T = max_len; a.H = H;
+    a.dk = dk; a.dv = dv; a.chunk = chunk_size;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    a.ws = static_cast<WsHeader *>(ws);
+    a.ws_body = static_cast<char *>(ws) + kWsHeader;
+    a.ws_body_bytes = ws_bytes - kWsHeader;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
     return run_prefill(a, true, total_T, st);
 }
 

@@ -213,8 +213,8 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v,
  * the two placements coincide.
  *   g   [B,T,H,dk] float32, the layout of q and k; NULL means no decay.  16-byte aligned.
  * Every other argument, layout and rule as kda_recurrent_fwd / kda_varlen_fwd /
- * kda_decode_step.  These run on CUDA cores, token by token (exact for any decay
- * strength), and need no workspace.
+ * kda_decode_step.  The three *_recurrent_fwd / decode entry points run on CUDA cores,
+ * token by token (exact for any decay strength), and need no workspace.
  */
 kda_status kda_gk_recurrent_fwd(const void *q, const void *k, const void *v,
                                 const float *beta, const float *g,
@@ -222,6 +222,33 @@ kda_status kda_gk_recurrent_fwd(const void *q, const void *k, const void *v,
                                 int B, int T, int H, int dk, int dv, kda_dtype dtype,
                                 float scale, int use_qk_l2norm, int decayed_read,
                                 kda_stream_t stream);
+
+/*
+ * Chunked prefill with per-key-channel decay: the same results as kda_gk_recurrent_fwd.
+ * Arguments, workspace (its size is kda_chunk_fwd_workspace()), errors and device error
+ * word as kda_chunk_fwd, plus g and decayed_read as above.  bf16 with dk == dv in {64, 128}
+ * and chunk_size 64 runs on the tensor cores: the chunk's per-channel factors
+ * exp(G_t[c] - G_s[c]) are split at 16-token sub-blocks (kda-neuron-kernels README: the
+ * exact sub-chunk form), and a sub-block whose decay spans more than e^60 in some channel
+ * takes its diagonal entries from an exact CUDA-core evaluation, so no decay strength
+ * overflows.  Every other supported shape runs the per-channel token-by-token kernel.
+ */
+kda_status kda_gk_chunk_fwd(const void *q, const void *k, const void *v,
+                            const float *beta, const float *g,
+                            const float *initial_state, void *o, float *final_state,
+                            int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                            float scale, int chunk_size, int use_qk_l2norm, int decayed_read,
+                            void *ws, size_t ws_bytes, kda_stream_t stream);
+
+/* Packed chunked prefill with per-key-channel decay: kda_varlen_fwd's arguments and
+ * workspace (kda_varlen_fwd_workspace()) plus g [1,total_T,H,dk] and decayed_read. */
+kda_status kda_gk_varlen_fwd(const void *q, const void *k, const void *v,
+                             const float *beta, const float *g,
+                             const int *cu_seqlens, const int *cu_seqlens_host,
+                             int N, int total_T, int H, int dk, int dv,
+                             const float *initial_state, void *o, float *final_state,
+                             kda_dtype dtype, float scale, int chunk_size, int use_qk_l2norm,
+                             int decayed_read, void *ws, size_t ws_bytes, kda_stream_t stream);
 
 /* Packed form: q, k, g [1,total_T,H,dk]; v, o [1,total_T,H,dv]; beta [1,total_T,H];
  * cu_seqlens / cu_seqlens_host and the [N,H,dk,dv] states as kda_varlen_fwd. */

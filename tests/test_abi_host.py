@@ -191,3 +191,24 @@ def test_gk_entry_points_reject_bad_arguments(lib):
     assert var([0, 4, 6, 9]) == 9
     assert var([0, 4, 6, 10], cu=None) == 1
     assert var([0, 4, 6, 10], g=_fake(0x100c)) == 5
+
+
+def test_gk_chunk_entry_points_reject_bad_arguments(lib):
+    def call(**kw):
+        a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), g=_fake(), h0=None, o=_fake(),
+                 hT=None, B=1, T=64, H=2, dk=128, dv=128, dt=1, chunk=64, ws=_fake(), ws_bytes=1 << 30)
+        a.update(kw)
+        return lib.kda_gk_chunk_fwd(a["q"], a["k"], a["v"], a["beta"], a["g"], a["h0"], a["o"],
+                                    a["hT"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["dt"], 0.0,
+                                    a["chunk"], 1, 1, a["ws"], a["ws_bytes"], None)
+    assert call(k=None) == 1
+    assert call(H=-1) == 2
+    assert call(dt=4) == 3
+    assert call(chunk=48) == 4
+    assert call(g=_fake(0x1004)) == 5
+    assert call(ws=None) == 6
+    assert call(ws_bytes=300) == 6
+    hs = (ctypes.c_int * 3)(0, 5, 4)
+    assert lib.kda_gk_varlen_fwd(_fake(), _fake(), _fake(), _fake(), _fake(), _fake(),
+                                 ctypes.cast(hs, ctypes.c_void_p), 2, 4, 2, 64, 64, None, _fake(),
+                                 None, 1, 0.0, 64, 1, 0, _fake(), 1 << 30, None) == 9

@@ -190,3 +190,86 @@ def test_decode_full_size_head_sample(kda, oracle_mod, dev):
     on, hn = to_np(o), to_np(state)
     b, h = heads // H, heads % H
     assert_parity("bf16", on[b, 0, h], ro[b, 0, h], hn[b, h], rh[b, h], tag="decode sample")
+
+
+# ------------------------------------------------------------------ chunked (tensor cores)
+def _run_chunk(kda, d, dev, dtype, decayed, chunk=64, **kw):
+    import torch
+    t = _dev_inputs(d, dev, dtype)
+    o, h = kda.gk_chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["h0"],
+                            cu_seqlens=t.get("cu_seqlens"), decayed_read=decayed, chunk_size=chunk,
+                            check_device=True, **kw)
+    torch.cuda.synchronize()
+    return to_np(o), to_np(h)
+
+
+@pytest.mark.parametrize("decayed", [False, True])
+@pytest.mark.parametrize("gate", [0.01, 0.3, 2.0, 6.0, 12.0])
+@pytest.mark.parametrize("D", [128, 64])
+def test_chunk_gate_regimes(kda, oracle_mod, dev, D, gate, decayed):
+    """gate 12: about -6 per token, so most 16-token sub-blocks span more than e^60 in
+    some channel and take the exact CUDA-core diagonal."""
+    d = make_gk(2, 203, 3, D, D, dtype="bf16", gate_scale=gate, h0="normal002", seed=31)
+    o, h = _run_chunk(kda, d, dev, "bf16", decayed)
+    ro, rh = oracle_mod.forward_gk(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                                   decayed_read=decayed)
+    assert_parity("bf16", o, ro, h, rh, tag=f"gk chunk D={D} gate={gate} decayed={decayed}")
+
+
+@pytest.mark.parametrize("T", [1, 16, 63, 64, 65, 130])
+def test_chunk_lengths(kda, oracle_mod, dev, T):
+    d = make_gk(2, T, 2, 128, 128, dtype="bf16", gate_scale=0.3, h0="normal002", seed=32)
+    o, h = _run_chunk(kda, d, dev, "bf16", True)
+    ro, rh = oracle_mod.forward_gk(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                                   decayed_read=True)
+    assert_parity("bf16", o, ro, h, rh, tag=f"gk chunk T={T}")
+
+
+def test_chunk_two_launch_path(kda, oracle_mod, dev):
+    """More (sequence, head) pairs than half the SMs: separate prep and chain launches."""
+    d = make_gk(2, 100, 48, 64, 64, dtype="bf16", gate_scale=0.3, h0="normal002", seed=33)
+    o, h = _run_chunk(kda, d, dev, "bf16", False)
+    ro, rh = oracle_mod.forward_gk(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
+    assert_parity("bf16", o, ro, h, rh, tag="gk chunk two launches")
+
+
+@pytest.mark.parametrize("decayed", [False, True])
+def test_chunk_varlen(kda, oracle_mod, dev, decayed):
+    import torch
+    lengths = [0, 1, 63, 64, 65, 200, 7]
+    d = make_gk(1, 0, 4, 128, 128, dtype="bf16", gate_scale=2.0, h0="normal002", seed=34,
+                lengths=lengths)
+    o, h = _run_chunk(kda, d, dev, "bf16", decayed,
+                      cu_seqlens_cpu=torch.from_numpy(d["cu_seqlens"]))
+    ro, rh = oracle_mod.forward_gk(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                                   cu_seqlens=d["cu_seqlens"], decayed_read=decayed)
+    assert_parity("bf16", o, ro, h, rh, tag="gk chunk varlen")
+
+
+def test_chunk_other_shapes_use_the_scan(kda, oracle_mod, dev):
+    """fp32, or a chunk size other than 64: the per-channel token-by-token kernel."""
+    d = make_gk(1, 70, 2, 64, 32, dtype="f32", gate_scale=0.3, h0="normal002", seed=35)
+    o, h = _run_chunk(kda, d, dev, "f32", True, chunk=32)
+    ro, rh = oracle_mod.forward_gk(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                                   decayed_read=True)
+    assert_parity("f32", o, ro, h, rh, tag="gk chunk fp32")
+
+
+def test_chunk_training_shape(kda, oracle_mod, dev):
+    """B=2, T=2048, H=16, d=128 (the training-shape workload) with g = -0.3 U[0,1)."""
+    d = make_gk(2, 2048, 16, 128, 128, dtype="bf16", gate_scale=0.3, seed=36)
+    o, h = _run_chunk(kda, d, dev, "bf16", True)
+    ro, rh = oracle_mod.forward_gk(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                                   decayed_read=True)
+    assert_parity("bf16", o, ro, h, rh, tag="gk chunk training shape")
+
+
+def test_chunk_matches_recurrent_kernel(kda, dev):
+    """The chunked and token-by-token per-channel kernels agree (bf16 rounding of E_c)."""
+    import torch
+    d = make_gk(1, 300, 8, 128, 128, dtype="bf16", gate_scale=1.0, h0="normal002", seed=37)
+    t = _dev_inputs(d, dev, "bf16")
+    o1, h1 = kda.gk_chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["h0"], check_device=True)
+    o2, h2 = kda.gk_recurrent_fwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["h0"])
+    torch.cuda.synchronize()
+    assert_parity("bf16", to_np(o1), to_np(o2), to_np(h1), to_np(h2), tag="chunk vs scan")
