@@ -368,6 +368,41 @@ def bench_gk(args, world, rank, dev, peaks):
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                      "bytes_per_launch": nbytes}}
 
+    from delta_rule_linear_gb300 import _lib
+    for name, (Bp, T, Hp) in (("gk_chunk_prefill_long", (1, 32768, 32)),
+                              ("gk_chunk_prefill_training", (2, 2048, 16))):
+        d = make_gk(Bp, T, Hp, D, D, dtype="bf16", gate_scale=0.01, h0="normal002", seed=rank)
+        q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
+        beta, g, h0 = (to_dev(d[n], dev, torch.float32) for n in ("beta", "g", "h0"))
+        o = torch.empty_like(v)
+        hT = torch.empty((Bp, Hp, D, D), dtype=torch.float32, device=dev)
+        ws = torch.empty(_lib.chunk_fwd_workspace_bytes(Bp, T, Hp, D, D, 64, _lib.KDA_BF16),
+                         dtype=torch.uint8, device=dev)
+
+        def cstep():
+            kda.gk_chunk_fwd(q, k, v, beta, g, h0, decayed_read=True, out=o, final_state=hT,
+                             workspace=ws, stream=stream)
+
+        for _ in range(args.warmup):
+            cstep()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0.record(stream)
+        for _ in range(args.steps):
+            cstep()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        if kda.query_device_error(ws) != 0:
+            raise RuntimeError("device error recorded during the per-channel prefill benchmark")
+        flops = counted_prefill_flops(Bp, T, Hp, D, D, 64)
+        out[name] = {
+            "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D, chunk=64), "decayed_read": True,
+            "ms_per_call": ms, "tokens_per_s": Bp * T * world / (ms * 1e-3),
+            "tc_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
+            "gpu_launches_per_call": tc_prefill_launches(Bp, Hp, dev)}
+        del q, k, v, beta, g, h0, o, hT, ws
+
     Bp, T, Hp = 2, 2048, 16
     d = make_gk(Bp, T, Hp, D, D, dtype="bf16", gate_scale=0.01, seed=rank)
     q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
