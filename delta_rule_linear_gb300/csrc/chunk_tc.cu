@@ -952,11 +952,45 @@ struct GkSmem {
     static constexpr int OV_BYTES = (GB - OV + NB * 128 * 128) > (AQ + 8192 - OV)
                                         ? (GB - OV + NB * 128 * 128) : (AQ + 8192 - OV);
     static constexpr int SD = OV + OV_BYTES;              // exact diagonal sub-blocks: fp32 [4][2][16][16]
-    static constexpr int MISC = SD + 4 * 2 * 256 * 4;
-    // MISC: beta [2][64] | kn [64] | qn [64] | exp(G_n) [D] | prefix totals [4][D] | span flags [4]
-    static constexpr int CTRL = MISC + (2 * 64 + 64 + 64 + D + 4 * D + 4) * 4;
+    static constexpr int ST = SD + 4 * 2 * 256 * 4;      // per-warp E_c row staging: 8 x 2 KB
+    static constexpr int MISC = ST + 8 * 2048;
+    // MISC: beta [2][64] | kn [64] | qn [64] | exp(G_n) [D] | prefix totals [512] | span flags [4]
+    static constexpr int CTRL = MISC + (2 * 64 + 64 + 64 + D + 512 + 4) * 4;
     static constexpr int BYTES = ((CTRL + 64 + 1023) / 1024) * 1024;
 };
+
+// A warp's 32 rows x 32 columns of E_c (row `row` of lane l, or none when row < 0; 32 fp32
+// values in u) go out as 16-byte stores that cover 8 rows x 64 contiguous bytes each,
+// through a 2 KB staging tile of the warp (rows of 64 B, 16-byte chunk c of row r at
+// position c ^ ((r >> 1) & 3): conflict-free both ways).
+// With neg the values are negated and dval added at column dcol (relative to col0; none
+// when outside 0..31).
+__device__ __forceinline__ void warp_store_E(uint8_t *stage, __nv_bfloat16 *Eslot, int R, int row,
+                                             int col0, const uint32_t *u, bool neg, int lane,
+                                             int dcol = -1, float dval = 0.f) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint4 w;
+        if (neg) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = (8 * c + e == dcol ? dval : 0.f) - __uint_as_float(u[8 * c + e]);
+            w = pack8(f);
+        } else {
+            w = pack8u(u + 8 * c);
+        }
+        *reinterpret_cast<uint4 *>(stage + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = w;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int rr = 8 * k + (lane >> 2), c = lane & 3;
+        const int grow = __shfl_sync(0xffffffffu, row, rr);
+        const uint4 w = *reinterpret_cast<const uint4 *>(stage + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
+        if (grow >= 0) *reinterpret_cast<uint4 *>(Eslot + (size_t)grow * R + col0 + 8 * c) = w;
+    }
+    __syncwarp();
+}
 
 __device__ __forceinline__ float ex2f(float x) {
     float y;
@@ -997,7 +1031,7 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
     constexpr int R = D + 64;
     constexpr int NP = D / 2;                 // channel pairs
     constexpr int TPG = 64 / (256 / NP);      // tokens per build thread: 16 (D=128) or 8 (D=64)
-    constexpr int NQ = 256 / D;               // token quarters of the prefix pass
+    constexpr int NQ = 256 / NP;              // token groups of the prefix pass (channel pairs)
     constexpr int QLEN = 64 / NQ;
     PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(sm + Ly::CTRL);
     const int warp = tid >> 5, lane = tid & 31;
@@ -1023,7 +1057,8 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
     float *sd = reinterpret_cast<float *>(sm + Ly::SD);
     float *mbeta2 = reinterpret_cast<float *>(sm + Ly::MISC);
     float *mkn = mbeta2 + 128, *mqn = mkn + 64, *meGn = mqn + 64, *mtot = meGn + D;
-    int *mspan = reinterpret_cast<int *>(mtot + 4 * D);
+    int *mspan = reinterpret_cast<int *>(mtot + 512);
+    uint8_t *stage = sm + Ly::ST + warp * 2048;
 
     ChunkItem cur;
     while (item < p.n_items && !item_info(p, item, cur)) item += stride;
@@ -1072,79 +1107,116 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
                 else mkn[t] = t < nv ? inv : 0.f;
             }
         }
-        {   // pass A: each quarter's inclusive prefix in place, in log2 units
-            const int c = tid % D, j = tid / D;
-            float acc = 0.f;
+        {   // pass A: each token group's inclusive prefix in place (a channel pair per thread),
+            // in log2 units
+            const int c0 = 2 * (tid % NP), j = tid / NP;
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
             for (int t = j * QLEN; t < (j + 1) * QLEN; ++t) {
-                acc = fmaf(gf[t * D + c], kLog2e, acc);
-                gf[t * D + c] = acc;
+                float2 *x = reinterpret_cast<float2 *>(gf + t * D + c0);
+                const float2 gv = *x;
+                acc.x = fmaf(gv.x, kLog2e, acc.x);
+                acc.y = fmaf(gv.y, kLog2e, acc.y);
+                *x = acc;
             }
-            mtot[j * D + c] = acc;
+            *reinterpret_cast<float2 *>(mtot + j * D + c0) = acc;
         }
         named_sync(bar, kGroupThreads);
-        {   // pass B: add the totals of the earlier quarters
-            const int c = tid % D, j = tid / D;
-            float off = 0.f;
-            for (int jj = 0; jj < j; ++jj) off += mtot[jj * D + c];
-            if (j > 0)
-                for (int t = j * QLEN; t < (j + 1) * QLEN; ++t) gf[t * D + c] += off;
+        {   // pass B: add the totals of the earlier groups
+            const int c0 = 2 * (tid % NP), j = tid / NP;
+            float2 off = make_float2(0.f, 0.f);
+            for (int jj = 0; jj < j; ++jj) {
+                const float2 tv = *reinterpret_cast<const float2 *>(mtot + jj * D + c0);
+                off.x += tv.x;
+                off.y += tv.y;
+            }
+            if (j > 0) {
+#pragma unroll
+                for (int t = j * QLEN; t < (j + 1) * QLEN; ++t) {
+                    float2 *x = reinterpret_cast<float2 *>(gf + t * D + c0);
+                    const float2 gv = *x;
+                    *x = make_float2(gv.x + off.x, gv.y + off.y);
+                }
+            }
         }
         named_sync(bar, kGroupThreads);
 
         // ---- build: K~, [K_R; Q_G] and the sub-block Gram operands, channel pair cp of
-        // tokens [t0, t0 + TPG) (all inside sub-block b)
+        // tokens [t0, t0 + TPG) (all inside sub-block b).  Per token three exponentials of
+        // each channel, fq = e^(G_t - G_ref(b)) <= 1, fb = e^(G_ref(b) - G_t) >= 1 and
+        // f1 = e^(G_ref(b+1) - G_t) <= 1 (G_ref(4) := G_n); every other factor is one of
+        // these times a per-thread constant <= 1.
         {
             const int cp = tid % NP, c0 = 2 * cp;
             const int t0 = (tid / NP) * TPG, b = t0 >> 4;
-            const float2 gn = *reinterpret_cast<const float2 *>(gf + 63 * D + c0);
+            float2 gref[5];
+#pragma unroll
+            for (int bb = 0; bb < 5; ++bb)
+                gref[bb] = bb == 0 ? make_float2(0.f, 0.f)
+                                   : *reinterpret_cast<const float2 *>(gf + (bb == 4 ? 63 : 16 * bb - 1) * D + c0);
+            float2 grb = gref[0], grb1 = gref[1];
+#pragma unroll
+            for (int bb = 1; bb < 4; ++bb)
+                if (bb == b) { grb = gref[bb]; grb1 = gref[bb + 1]; }
+            const float2 gn = gref[4];
             if (t0 == 0) {
                 meGn[c0] = ex2f(gn.x);
                 meGn[c0 + 1] = ex2f(gn.y);
             }
-            float2 gref[4];
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb)
-                gref[bb] = bb == 0 ? make_float2(0.f, 0.f)
-                                   : *reinterpret_cast<const float2 *>(gf + (16 * bb - 1) * D + c0);
             if ((t0 & 15) == 0) {   // span of sub-block b in these two channels
                 const float2 ge = *reinterpret_cast<const float2 *>(gf + (16 * b + 15) * D + c0);
-                if (fmaxf(gref[b].x - ge.x, gref[b].y - ge.y) > kSpanLog2) atomicOr(mspan + b, 1);
+                if (fmaxf(grb.x - ge.x, grb.y - ge.y) > kSpanLog2) atomicOr(mspan + b, 1);
             }
-            float2 gprev = t0 == 0 ? make_float2(0.f, 0.f)
-                                   : *reinterpret_cast<const float2 *>(gf + (t0 - 1) * D + c0);
+            const float eb0 = ex2f(grb.x), eb1 = ex2f(grb.y);               // e^G_ref(b)
+            const float cn0 = ex2f(gn.x - grb1.x), cn1 = ex2f(gn.y - grb1.y);  // e^(G_n - G_ref(b+1))
+            float cb0[4], cb1[4];                                              // e^(G_ref(b') - G_ref(b+1))
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) {
+                cb0[bb] = ex2f(gref[bb].x - grb1.x);
+                cb1[bb] = ex2f(gref[bb].y - grb1.y);
+            }
+            float fqp0 = 1.f, fqp1 = 1.f;   // fq of the previous token (1 before the sub-block)
+            if ((t0 & 15) != 0) {
+                const float2 gp = *reinterpret_cast<const float2 *>(gf + (t0 - 1) * D + c0);
+                fqp0 = ex2f(gp.x - grb.x);
+                fqp1 = ex2f(gp.y - grb.y);
+            }
+#pragma unroll 4
             for (int t = t0; t < t0 + TPG; ++t) {
                 const float2 g = *reinterpret_cast<const float2 *>(gf + t * D + c0);
-                const float2 rr = decayed ? g : gprev;
                 const uint32_t kw = *reinterpret_cast<const uint32_t *>(sKQ + kmajor_sw128_offset(128, t, c0));
                 const uint32_t qw = *reinterpret_cast<const uint32_t *>(sKQ + kmajor_sw128_offset(128, 64 + t, c0));
                 const float kn = mkn[t], qn = mqn[t];
                 const float k0 = bf16lo(kw) * kn, k1 = bf16hi(kw) * kn;
                 const float qa = bf16lo(qw) * qn, qb = bf16hi(qw) * qn;
-                const float eg0 = ex2f(g.x), eg1 = ex2f(g.y);
-                const float er0 = decayed ? eg0 : ex2f(rr.x), er1 = decayed ? eg1 : ex2f(rr.y);
+                const float fq0 = ex2f(g.x - grb.x), fq1 = ex2f(g.y - grb.y);
+                const float fb0 = ex2f(fminf(grb.x - g.x, kClampLog2)), fb1 = ex2f(fminf(grb.y - g.y, kClampLog2));
+                const float f10 = ex2f(grb1.x - g.x), f11 = ex2f(grb1.y - g.y);
+                const float fk0 = decayed ? fq0 : fqp0, fk1 = decayed ? fq1 : fqp1;
                 *reinterpret_cast<uint32_t *>(sKT + kmajor_sw128_offset(64, t, c0)) =
-                    pack_bf16(k0 * ex2f(gn.x - g.x), k1 * ex2f(gn.y - g.y));
-                *reinterpret_cast<uint32_t *>(sKR + kmajor_sw128_offset(128, t, c0)) = pack_bf16(k0 * er0, k1 * er1);
-                *reinterpret_cast<uint32_t *>(sKR + kmajor_sw128_offset(128, 64 + t, c0)) = pack_bf16(qa * eg0, qb * eg1);
+                    pack_bf16(k0 * f10 * cn0, k1 * f11 * cn1);
+                *reinterpret_cast<uint32_t *>(sKR + kmajor_sw128_offset(128, t, c0)) =
+                    pack_bf16(k0 * fk0 * eb0, k1 * fk1 * eb1);
+                *reinterpret_cast<uint32_t *>(sKR + kmajor_sw128_offset(128, 64 + t, c0)) =
+                    pack_bf16(qa * fq0 * eb0, qb * fq1 * eb1);
                 // row operands of sub-block b: k rows 32b + j, q rows 32b + 16 + j
                 const int j = t - 16 * b;
-                const float fk0 = ex2f(rr.x - gref[b].x), fk1 = ex2f(rr.y - gref[b].y);
-                const float fq0 = decayed ? fk0 : ex2f(g.x - gref[b].x);
-                const float fq1 = decayed ? fk1 : ex2f(g.y - gref[b].y);
-                *reinterpret_cast<uint32_t *>(sGB + kmajor_sw128_offset(128, 32 * b + j, c0)) = pack_bf16(k0 * fk0, k1 * fk1);
+                *reinterpret_cast<uint32_t *>(sGB + kmajor_sw128_offset(128, 32 * b + j, c0)) =
+                    pack_bf16(k0 * fk0, k1 * fk1);
                 *reinterpret_cast<uint32_t *>(sGB + kmajor_sw128_offset(128, 32 * b + 16 + j, c0)) =
                     pack_bf16(qa * fq0, qb * fq1);
-                // column operands of sub-blocks b' >= b: row off(b') + t, factor exp(G_ref(b') - G_t)
+                // column operands of sub-blocks b' >= b: row off(b') + t, factor e^(G_ref(b') - G_t)
 #pragma unroll
                 for (int bb = 0; bb < 4; ++bb) {
                     if (bb < b) continue;
                     const int off = bb == 0 ? 0 : (bb == 1 ? 16 : (bb == 2 ? 48 : 96));
-                    const float f0 = ex2f(fminf(gref[bb].x - g.x, kClampLog2));
-                    const float f1 = ex2f(fminf(gref[bb].y - g.y, kClampLog2));
+                    const float f0 = bb == b ? fb0 : f10 * cb0[bb];
+                    const float f1 = bb == b ? fb1 : f11 * cb1[bb];
                     *reinterpret_cast<uint32_t *>(sGA + kmajor_sw128_offset(160, off + t, c0)) =
                         pack_bf16(k0 * f0, k1 * f1);
                 }
-                gprev = g;
+                fqp0 = fq0;
+                fqp1 = fq1;
             }
         }
         fence_proxy_async();
@@ -1265,31 +1337,30 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
             tmem_ld_wait();
             const bool has_row = (D == 128) || has64;
             const int i = (D == 128) ? i128 : i64;
-            if (has_row && ok) {
+            if (has_row) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    const uint4 w = pack8u(v + 8 * cc);
                     const int col = 32 * hh + 8 * cc;
-                    *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((((col >> 3) ^ i) & 7) << 4)) = w;
-                    *reinterpret_cast<uint4 *>(Eslot + (size_t)i * R + D + col) = w;
+                    *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((((col >> 3) ^ i) & 7) << 4)) = pack8u(v + 8 * cc);
                 }
             }
+            warp_store_E(stage, Eslot, R, (has_row && ok) ? i : -1, D + 32 * hh, v, false, lane);
             tmem_ld32(tm + tq + 128 + 32 * hh, v);
             tmem_ld_wait();
-            if (has64 && ok) {
-                const int t = i64;
+            const int t = i64;
+            if (has64) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int col = 32 * hh + 8 * cc;
                     const int off = t * 128 + ((((col >> 3) ^ t) & 7) << 4);
                     *reinterpret_cast<uint4 *>(sZ2 + off) = pack8un(v + 8 * cc);
-                    *reinterpret_cast<uint4 *>(Eslot + (size_t)(D + t) * R + D + col) = pack8u(v + 8 * cc);
                     float dg[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) dg[e] = (col + e == t) ? 1.f : 0.f;
                     *reinterpret_cast<uint4 *>(sZ2 + 8192 + off) = pack8(dg);
                 }
             }
+            warp_store_E(stage, Eslot, R, (has64 && ok) ? D + t : -1, D + 32 * hh, v, false, lane);
         }
         fence_proxy_async();
         tc_fence_before();
@@ -1323,26 +1394,20 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
             tmem_ld32(tm + tq + 128 + hh * HALF, *reinterpret_cast<uint32_t(*)[32]>(v));
             if (HALF == 64) tmem_ld32(tm + tq + 128 + hh * HALF + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * (HALF / 64)));
             tmem_ld_wait();
-            if (has64 && ok) {   // E[D + t][j] = Q_G[t][j] - (Z2 K_R)[t][j] = D3b[t][j]
+            // E[D + t][j] = Q_G[t][j] - (Z2 K_R)[t][j] = D3b[t][j]
 #pragma unroll
-                for (int cc = 0; cc < HALF / 8; ++cc)
-                    *reinterpret_cast<uint4 *>(Eslot + (size_t)(D + t) * R + hh * HALF + 8 * cc) =
-                        pack8u(v + 8 * cc);
-            }
+            for (int h2 = 0; h2 < HALF / 32; ++h2)
+                warp_store_E(stage, Eslot, R, (has64 && ok) ? D + t : -1, hh * HALF + 32 * h2, v + 32 * h2,
+                             false, lane);
             tmem_ld32(tm + tq + hh * HALF, *reinterpret_cast<uint32_t(*)[32]>(v));
             if (HALF == 64) tmem_ld32(tm + tq + hh * HALF + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * (HALF / 64)));
             tmem_ld_wait();
-            if (has_row && ok) {   // E[i][j] = exp(G_n[i]) delta_ij - (Z1 K_R)[i][j]
-                const float gi = meGn[i];
+            // E[i][j] = exp(G_n[i]) delta_ij - (Z1 K_R)[i][j]
+            const float gi = has_row ? meGn[i] : 0.f;
 #pragma unroll
-                for (int cc = 0; cc < HALF / 8; ++cc) {
-                    const int col = hh * HALF + 8 * cc;
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = (col + e == i ? gi : 0.f) - __uint_as_float(v[8 * cc + e]);
-                    *reinterpret_cast<uint4 *>(Eslot + (size_t)i * R + col) = pack8(f);
-                }
-            }
+            for (int h2 = 0; h2 < HALF / 32; ++h2)
+                warp_store_E(stage, Eslot, R, (has_row && ok) ? i : -1, hh * HALF + 32 * h2, v + 32 * h2,
+                             true, lane, i - (hh * HALF + 32 * h2), gi);
         }
         tc_fence_before();
         named_sync(bar, kGroupThreads);   // every thread's E_c stores are issued
