@@ -929,8 +929,9 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
 // only the sub-block's own columns get a factor above 1, up to exp of its 16-token decay.
 // When that span passes kSpanLog2 in some channel, the sub-block's diagonal entries are
 // recomputed on CUDA cores with the exact factor per element, so the result is exact for
-// any decay.  One group of 256 threads per CTA (the scaled copies take the shared memory
-// of the second); E_c goes to global memory by ordinary stores from the epilogues.
+// any decay.  One group per CTA, of all 512 threads (the scaled copies take the shared
+// memory a second group would need); E_c goes to global memory by ordinary stores from
+// the epilogues.
 // ---------------------------------------------------------------------------------
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSpanLog2 = 60.f * kLog2e;    // sub-block spans above e^60 take the exact path
@@ -949,25 +950,29 @@ struct GkSmem {
     static constexpr int LT_BYTES = 2 * 64 * kLP * 4;     // L and T fp32
     static constexpr int PT = OV + LT_BYTES;              // P: MN-major 64 x 64
     static constexpr int AQ = PT + 8192;                  // Aqk: K-major 64 x 64
-    static constexpr int OV_BYTES = (GB - OV + NB * 128 * 128) > (AQ + 8192 - OV)
-                                        ? (GB - OV + NB * 128 * 128) : (AQ + 8192 - OV);
+    static constexpr int ZOPS = D * 128 + 16384;          // Z1 and [-Z2 | I], from OV, after MMA2
+    static constexpr int ST = OV + ZOPS;                  // per-warp E_c staging (epilogues 2, 3): 16 x 2 KB
+    static constexpr int OV_A = GB - OV + NB * 128 * 128, OV_B = AQ + 8192 - OV, OV_C = ZOPS + 16 * 2048;
+    static constexpr int OV_BYTES = OV_A > OV_B ? (OV_A > OV_C ? OV_A : OV_C) : (OV_B > OV_C ? OV_B : OV_C);
     static constexpr int SD = OV + OV_BYTES;              // exact diagonal sub-blocks: fp32 [4][2][16][16]
-    static constexpr int ST = SD + 4 * 2 * 256 * 4;      // per-warp E_c row staging: 8 x 2 KB
-    static constexpr int MISC = ST + 8 * 2048;
-    // MISC: beta [2][64] | kn [64] | qn [64] | exp(G_n) [D] | prefix totals [512] | span flags [4]
-    static constexpr int CTRL = MISC + (2 * 64 + 64 + 64 + D + 512 + 4) * 4;
+    static constexpr int MISC = SD + 4 * 2 * 256 * 4;
+    // MISC: beta [2][64] | kn [64] | qn [64] | exp(G_n) [D] | prefix totals [1024] | span flags [4]
+    static constexpr int CTRL = MISC + (2 * 64 + 64 + 64 + D + 1024 + 4) * 4;
     static constexpr int BYTES = ((CTRL + 64 + 1023) / 1024) * 1024;
 };
 
-// A warp's 32 rows x 32 columns of E_c (row `row` of lane l, or none when row < 0; 32 fp32
-// values in u) go out as 16-byte stores that cover 8 rows x 64 contiguous bytes each,
-// through a 2 KB staging tile of the warp (rows of 64 B, 16-byte chunk c of row r at
-// position c ^ ((r >> 1) & 3): conflict-free both ways).
-// With neg the values are negated and dval added at column dcol (relative to col0; none
-// when outside 0..31).
-__device__ __forceinline__ void warp_store_E(uint8_t *stage, __nv_bfloat16 *Eslot, int R, int row,
-                                             int col0, const uint32_t *u, bool neg, int lane,
-                                             int dcol = -1, float dval = 0.f) {
+// A warp's rows of E_c (lane l holds row row0 + l, l < nrows = 16 or 32; 32 fp32 values
+// in u for columns col0 ..) go to global memory by TMA stores of 16-row x 32-column boxes
+// from a 2 KB staging tile of the warp, laid out in the 64-byte swizzle of the tensor map
+// (16-byte chunk c of row r at position c ^ ((r >> 1) & 3): conflict-free writes).  The
+// stores stay in flight: lane 0 waits for them (bulk_wait0) before E_c is published, and
+// every call first waits until the tile's previous store has read it.  With neg the values
+// are negated and dval added at column dcol (relative to col0; none when outside 0..31).
+__device__ __forceinline__ void warp_store_E(uint8_t *stage, const CUtensorMap *map, long slot, int row0,
+                                             int nrows, int col0, const uint32_t *u, bool neg, int lane,
+                                             bool issue, int dcol = -1, float dval = 0.f) {
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         uint4 w;
@@ -981,15 +986,13 @@ __device__ __forceinline__ void warp_store_E(uint8_t *stage, __nv_bfloat16 *Eslo
         }
         *reinterpret_cast<uint4 *>(stage + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = w;
     }
+    fence_proxy_async();
     __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int rr = 8 * k + (lane >> 2), c = lane & 3;
-        const int grow = __shfl_sync(0xffffffffu, row, rr);
-        const uint4 w = *reinterpret_cast<const uint4 *>(stage + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
-        if (grow >= 0) *reinterpret_cast<uint4 *>(Eslot + (size_t)grow * R + col0 + 8 * c) = w;
+    if (lane == 0 && issue) {
+        tma_store_3d(map, stage, col0, row0, (int)slot);
+        if (nrows == 32) tma_store_3d(map, stage + 1024, col0, row0 + 16, (int)slot);
+        bulk_commit();
     }
-    __syncwarp();
 }
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -999,7 +1002,7 @@ __device__ __forceinline__ float ex2f(float x) {
 }
 
 // g of one chunk (fp32 rows, zero past the chunk's valid tokens) by 16-byte cp.async copies
-// (warps other than 0 and 4, as load_rows)
+// (threads 0..255 without warps 0 and 4, as load_rows)
 template <int D>
 __device__ __forceinline__ void load_g(const TcParams &p, float *gf, const ChunkItem &it, int tid) {
     constexpr int PPR = D / 4;
@@ -1023,23 +1026,29 @@ __device__ __forceinline__ void load_beta(const TcParams &p, float *mbeta, const
     cp_async_commit();
 }
 
+constexpr int kGkThreads = 512;   // the whole CTA: one prep group
+constexpr int kGkBarInv = 2;      // named barrier of the inverse (threads 0..255)
+constexpr int kGkBarPark = 3;     // threads 256..511 wait there while the inverse runs
+
 template <int D>
-__device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, uint32_t tm, int tid,
-                                              int bar, long item, long stride) {
+__device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const TcParams &p, uint8_t *sm,
+                                              uint32_t tm, int tid, int bar, long item, long stride) {
     using Ly = GkSmem<D>;
+    constexpr int NT = kGkThreads;
     constexpr int NB = D / 64;
     constexpr int R = D + 64;
     constexpr int NP = D / 2;                 // channel pairs
-    constexpr int TPG = 64 / (256 / NP);      // tokens per build thread: 16 (D=128) or 8 (D=64)
-    constexpr int NQ = 256 / NP;              // token groups of the prefix pass (channel pairs)
-    constexpr int QLEN = 64 / NQ;
+    constexpr int NQ = NT / NP;               // token groups of the prefix and the build
+    constexpr int TPG = 64 / NQ;              // their tokens: 8 (D = 128) or 4 (D = 64)
+    static_assert(TPG <= 16 && 16 % TPG == 0, "a token group stays inside one 16-token sub-block");
     PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(sm + Ly::CTRL);
     const int warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, hh = warp >> 2;
+    const int q4 = warp & 3, hh = warp >> 2;   // TMEM lane quadrant; column quarter
     const int i128 = 32 * q4 + lane;
     const int i64 = 16 * q4 + lane;
     const bool has64 = lane < 16;
     const uint32_t tq = (uint32_t)(32 * q4) << 16;
+    const bool loader = tid < kGroupThreads;   // load_rows, load_g, load_beta use threads 0..255
 
     uint8_t *sKQ = sm + Ly::KQ;
     uint8_t *sKR = sm + Ly::KRQG;
@@ -1054,19 +1063,21 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
     uint8_t *sZ1 = sm + Ly::OV;                 // after MMA2: Z1 (K-major D x 64)
     uint8_t *sZ2 = sm + Ly::OV + D * 128;       // [-Z2 | I] (K-major 64 x 128)
     static_assert(D * 128 + 16384 <= 2 * 64 * kLP * 4, "the Z operands overlay L and T only");
+    uint8_t *stage = sm + Ly::ST + warp * 2048;
     float *sd = reinterpret_cast<float *>(sm + Ly::SD);
     float *mbeta2 = reinterpret_cast<float *>(sm + Ly::MISC);
     float *mkn = mbeta2 + 128, *mqn = mkn + 64, *meGn = mqn + 64, *mtot = meGn + D;
-    int *mspan = reinterpret_cast<int *>(mtot + 512);
-    uint8_t *stage = sm + Ly::ST + warp * 2048;
+    int *mspan = reinterpret_cast<int *>(mtot + 1024);
 
     ChunkItem cur;
     while (item < p.n_items && !item_info(p, item, cur)) item += stride;
     if (item >= p.n_items) return;
-    load_rows<D>(p, sKQ, cur, tid, true);
-    load_rows<D>(p, sKQ, cur, tid, false);
-    load_g<D>(p, gf, cur, tid);
-    load_beta(p, mbeta2, cur, tid);
+    if (loader) {
+        load_rows<D>(p, sKQ, cur, tid, true);
+        load_rows<D>(p, sKQ, cur, tid, false);
+        load_g<D>(p, gf, cur, tid);
+        load_beta(p, mbeta2, cur, tid);
+    }
     long pend = -1;   // kStoreThread: slot whose E_c stores are issued and not yet published
     const bool decayed = p.decayed_read != 0;
 
@@ -1076,21 +1087,23 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
         float *mbeta = mbeta2 + 64 * (it & 1);
         if (tid < 4) mspan[tid] = 0;
         cp_async_wait_all();
-        named_sync(bar, kGroupThreads);
+        if (lane == 0) bulk_wait0();   // the previous chunk's E_c stores: complete, staging free
+        named_sync(bar, NT);
         bool ok = ctl->fail == 0;
         long nitem = item + stride;
         ChunkItem nx;
         while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
         const bool more = nitem < p.n_items;
 
-        // ---- norms of the k and q rows (zero past the valid tokens); prefix over tokens of g
+        // ---- norms of the k and q rows (zero past the valid tokens), four threads a row;
+        // prefix over tokens of g
         {
-            const int r = tid >> 1, part = tid & 1, t = r & 63;
+            const int r = tid >> 2, part = tid & 3, t = r & 63;
             const bool isq = r >= 64;
             float ss = 0.f;
 #pragma unroll
-            for (int cc = 0; cc < NB * 4; ++cc) {
-                const int chunk = part * NB * 4 + cc;
+            for (int cc = 0; cc < NB * 2; ++cc) {
+                const int chunk = part * NB * 2 + cc;
                 const uint4 w = *reinterpret_cast<const uint4 *>(sKQ + (chunk >> 3) * 16384 + (isq ? 8192 : 0) +
                                                                  t * 128 + (((chunk ^ t) & 7) << 4));
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -1101,6 +1114,7 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
                 }
             }
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
             if (part == 0) {
                 const float inv = p.use_l2 ? 1.f / fmaxf(sqrtf(ss), kNormEps) : 1.f;
                 if (isq) mqn[t] = t < nv ? p.scale * inv : 0.f;
@@ -1112,7 +1126,7 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
             const int c0 = 2 * (tid % NP), j = tid / NP;
             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int t = j * QLEN; t < (j + 1) * QLEN; ++t) {
+            for (int t = j * TPG; t < (j + 1) * TPG; ++t) {
                 float2 *x = reinterpret_cast<float2 *>(gf + t * D + c0);
                 const float2 gv = *x;
                 acc.x = fmaf(gv.x, kLog2e, acc.x);
@@ -1121,7 +1135,7 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
             }
             *reinterpret_cast<float2 *>(mtot + j * D + c0) = acc;
         }
-        named_sync(bar, kGroupThreads);
+        named_sync(bar, NT);
         {   // pass B: add the totals of the earlier groups
             const int c0 = 2 * (tid % NP), j = tid / NP;
             float2 off = make_float2(0.f, 0.f);
@@ -1132,14 +1146,14 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
             }
             if (j > 0) {
 #pragma unroll
-                for (int t = j * QLEN; t < (j + 1) * QLEN; ++t) {
+                for (int t = j * TPG; t < (j + 1) * TPG; ++t) {
                     float2 *x = reinterpret_cast<float2 *>(gf + t * D + c0);
                     const float2 gv = *x;
                     *x = make_float2(gv.x + off.x, gv.y + off.y);
                 }
             }
         }
-        named_sync(bar, kGroupThreads);
+        named_sync(bar, NT);
 
         // ---- build: K~, [K_R; Q_G] and the sub-block Gram operands, channel pair cp of
         // tokens [t0, t0 + TPG) (all inside sub-block b).  Per token three exponentials of
@@ -1181,7 +1195,7 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
                 fqp0 = ex2f(gp.x - grb.x);
                 fqp1 = ex2f(gp.y - grb.y);
             }
-#pragma unroll 4
+#pragma unroll
             for (int t = t0; t < t0 + TPG; ++t) {
                 const float2 g = *reinterpret_cast<const float2 *>(gf + t * D + c0);
                 const uint32_t kw = *reinterpret_cast<const uint32_t *>(sKQ + kmajor_sw128_offset(128, t, c0));
@@ -1220,11 +1234,11 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
             }
         }
         fence_proxy_async();
-        named_sync(bar, kGroupThreads);
+        named_sync(bar, NT);
 
         // ---- sub-blocks whose decay span is too wide for the split: exact diagonal entries
         for (int b = 0; b < 4; ++b) {
-            if (mspan[b] == 0) continue;   // uniform: read after the barrier
+            if (mspan[b] == 0 || tid >= 256) continue;   // mspan: uniform, read after the barrier
             const int tj = tid >> 4, sj = tid & 15, t = 16 * b + tj, s = 16 * b + sj;
             float aq = 0.f, al = 0.f;
             if (sj <= tj) {
@@ -1246,8 +1260,8 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
         }
         // raw q, k and g are no longer read: the next chunk's loads start now
         float *mbeta_next = mbeta2 + 64 * ((it + 1) & 1);
-        if (mspan[0] | mspan[1] | mspan[2] | mspan[3]) named_sync(bar, kGroupThreads);
-        if (ok && more) {
+        if (mspan[0] | mspan[1] | mspan[2] | mspan[3]) named_sync(bar, NT);
+        if (ok && more && loader) {
             load_rows<D>(p, sKQ, nx, tid, true);
             load_rows<D>(p, sKQ, nx, tid, false);
             load_g<D>(p, gf, nx, tid);
@@ -1275,41 +1289,44 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
 
-        // ---- epilogue 1: L (fp32, rows t) and Aqk (bf16 operand) from the transposed rows s
+        // ---- epilogue 1: L (fp32, rows t) and Aqk (bf16 operand) from the transposed rows s;
+        // the warps of column quarter hh take sub-block b = hh
         {
-            const int s = i64, bs = s >> 4;
+            const int s = i64, bs = s >> 4, b = hh;
+            uint32_t v[32];
+            tmem_ld32(tm + tq + 32 * b, v);
+            tmem_ld_wait();
+            if (has64) {
+                const bool exact = mspan[b] != 0 && bs == b;
 #pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int b = 2 * hh + k2;
-                uint32_t v[32];
-                tmem_ld32(tm + tq + 32 * b, v);
-                tmem_ld_wait();
-                if (has64) {
-                    const bool exact = mspan[b] != 0 && bs == b;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int t = 16 * b + j;
-                        float lval = 0.f, aval = 0.f;
-                        if (b >= bs) {
-                            lval = exact ? sd[(b * 2) * 256 + j * 16 + (s & 15)] : __uint_as_float(v[j]);
-                            aval = exact ? sd[(b * 2 + 1) * 256 + j * 16 + (s & 15)] : __uint_as_float(v[16 + j]);
-                            lval = s < t ? mbeta[t] * lval : 0.f;
-                            aval = s <= t ? aval : 0.f;
-                            sL[t * kLP + s] = lval;
-                        }
-                        *reinterpret_cast<__nv_bfloat16 *>(sA + kmajor_sw128_offset(64, t, s)) =
-                            __float2bfloat16_rn(aval);
+                for (int j = 0; j < 16; ++j) {
+                    const int t = 16 * b + j;
+                    float lval = 0.f, aval = 0.f;
+                    if (b >= bs) {
+                        lval = exact ? sd[(b * 2) * 256 + j * 16 + (s & 15)] : __uint_as_float(v[j]);
+                        aval = exact ? sd[(b * 2 + 1) * 256 + j * 16 + (s & 15)] : __uint_as_float(v[16 + j]);
+                        lval = s < t ? mbeta[t] * lval : 0.f;
+                        aval = s <= t ? aval : 0.f;
+                        sL[t * kLP + s] = lval;
                     }
+                    *reinterpret_cast<__nv_bfloat16 *>(sA + kmajor_sw128_offset(64, t, s)) =
+                        __float2bfloat16_rn(aval);
                 }
             }
         }
         fence_proxy_async();
-        named_sync(bar, kGroupThreads);
+        named_sync(bar, NT);
         ok = ctl->fail == 0;
 
-        // ---- T = (I + L)^{-1}, written as P = T diag(beta) (MN-major: row t, columns s)
-        invert_unit_lower_64<kGroupThreads, true>(sL, sT, BTiles{sP, nullptr, nullptr, mbeta, nullptr}, tid,
-                                                  bar, [] {});
+        // ---- T = (I + L)^{-1}, written as P = T diag(beta) (MN-major: row t, columns s), by
+        // threads 0..255
+        if (tid < kGroupThreads) {
+            invert_unit_lower_64<kGroupThreads, true>(sL, sT, BTiles{sP, nullptr, nullptr, mbeta, nullptr},
+                                                      tid, kGkBarInv, [] {});
+            named_arrive(kGkBarPark, NT);
+        } else {
+            named_sync(kGkBarPark, NT);   // wait without taking issue slots from the inverse
+        }
 
         // ---- MMA2: D2a[:, 0:64] = K~^T P (M = D);  D2b[:, 128:192] = Aqk P (M = 64)
         if (tid == 0 && ok) {
@@ -1328,10 +1345,11 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
         if (ok && !mbar_wait(&ctl->bar_mma, ph ^ 1u, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
 
-        // ---- epilogue 2: Z1 = D2a -> E[i][D + s] and MMA3a's A; Z2 = D2b -> E[D + t][D + s]
-        // and MMA3b's A = [-Z2 | I]
-        __nv_bfloat16 *Eslot = p.E + (size_t)cur.slot * R * R;
-        {
+        // ---- epilogue 2: column quarters 0, 1 take Z1 = D2a (-> E[i][D + s], MMA3a's A),
+        // quarters 2, 3 take Z2 = D2b (-> E[D + t][D + s], MMA3b's A = [-Z2 | I])
+        const long slot = cur.slot;
+        constexpr int RW = D == 128 ? 32 : 16;   // rows of an M = D result per warp
+        if (hh < 2) {
             uint32_t v[32];
             tmem_ld32(tm + tq + 32 * hh, v);
             tmem_ld_wait();
@@ -1344,14 +1362,17 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
                     *reinterpret_cast<uint4 *>(sZ1 + i * 128 + ((((col >> 3) ^ i) & 7) << 4)) = pack8u(v + 8 * cc);
                 }
             }
-            warp_store_E(stage, Eslot, R, (has_row && ok) ? i : -1, D + 32 * hh, v, false, lane);
-            tmem_ld32(tm + tq + 128 + 32 * hh, v);
+            warp_store_E(stage, map_Ew, slot, RW * q4, RW, D + 32 * hh, v, false, lane, ok);
+        } else {
+            const int hq = hh - 2;
+            uint32_t v[32];
+            tmem_ld32(tm + tq + 128 + 32 * hq, v);
             tmem_ld_wait();
             const int t = i64;
             if (has64) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    const int col = 32 * hh + 8 * cc;
+                    const int col = 32 * hq + 8 * cc;
                     const int off = t * 128 + ((((col >> 3) ^ t) & 7) << 4);
                     *reinterpret_cast<uint4 *>(sZ2 + off) = pack8un(v + 8 * cc);
                     float dg[8];
@@ -1360,11 +1381,11 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
                     *reinterpret_cast<uint4 *>(sZ2 + 8192 + off) = pack8(dg);
                 }
             }
-            warp_store_E(stage, Eslot, R, (has64 && ok) ? D + t : -1, D + 32 * hh, v, false, lane);
+            warp_store_E(stage, map_Ew, slot, D + 16 * q4, 16, D + 32 * hq, v, false, lane, ok);
         }
         fence_proxy_async();
         tc_fence_before();
-        named_sync(bar, kGroupThreads);
+        named_sync(bar, NT);
         ok = ctl->fail == 0;
 
         // ---- MMA3: D3a[:, 0:D] = Z1 K_R (M = D);  D3b[:, 128:128+D] = [-Z2 | I] [K_R; Q_G] (M = 64)
@@ -1384,33 +1405,32 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
 
-        // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
+        // ---- epilogue 3: the state columns of E, 32 columns per warp.
+        //   E[D + t][j] = Q_G[t][j] - (Z2 K_R)[t][j] = D3b[t][j]
+        //   E[i][j]     = exp(G_n[i]) delta_ij - (Z1 K_R)[i][j]
         {
-            constexpr int HALF = D / 2;
-            const bool has_row = (D == 128) || has64;
-            const int i = (D == 128) ? i128 : i64;
-            const int t = i64;
-            uint32_t v[HALF];
-            tmem_ld32(tm + tq + 128 + hh * HALF, *reinterpret_cast<uint32_t(*)[32]>(v));
-            if (HALF == 64) tmem_ld32(tm + tq + 128 + hh * HALF + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * (HALF / 64)));
-            tmem_ld_wait();
-            // E[D + t][j] = Q_G[t][j] - (Z2 K_R)[t][j] = D3b[t][j]
-#pragma unroll
-            for (int h2 = 0; h2 < HALF / 32; ++h2)
-                warp_store_E(stage, Eslot, R, (has64 && ok) ? D + t : -1, hh * HALF + 32 * h2, v + 32 * h2,
-                             false, lane);
-            tmem_ld32(tm + tq + hh * HALF, *reinterpret_cast<uint32_t(*)[32]>(v));
-            if (HALF == 64) tmem_ld32(tm + tq + hh * HALF + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * (HALF / 64)));
-            tmem_ld_wait();
-            // E[i][j] = exp(G_n[i]) delta_ij - (Z1 K_R)[i][j]
-            const float gi = has_row ? meGn[i] : 0.f;
-#pragma unroll
-            for (int h2 = 0; h2 < HALF / 32; ++h2)
-                warp_store_E(stage, Eslot, R, (has_row && ok) ? i : -1, hh * HALF + 32 * h2, v + 32 * h2,
-                             true, lane, i - (hh * HALF + 32 * h2), gi);
+            uint32_t v[32];
+            if constexpr (D == 128) {
+                tmem_ld32(tm + tq + 128 + 32 * hh, v);
+                tmem_ld_wait();
+                warp_store_E(stage, map_Ew, slot, D + 16 * q4, 16, 32 * hh, v, false, lane, ok);
+                tmem_ld32(tm + tq + 32 * hh, v);
+                tmem_ld_wait();
+                warp_store_E(stage, map_Ew, slot, 32 * q4, 32, 32 * hh, v, true, lane, ok, i128 - 32 * hh,
+                             meGn[i128]);
+            } else if (hh < 2) {
+                tmem_ld32(tm + tq + 32 * hh, v);
+                tmem_ld_wait();
+                warp_store_E(stage, map_Ew, slot, 16 * q4, 16, 32 * hh, v, true, lane, ok, i64 - 32 * hh,
+                             has64 ? meGn[i64] : 0.f);
+            } else {
+                tmem_ld32(tm + tq + 128 + 32 * (hh - 2), v);
+                tmem_ld_wait();
+                warp_store_E(stage, map_Ew, slot, D + 16 * q4, 16, 32 * (hh - 2), v, false, lane, ok);
+            }
         }
         tc_fence_before();
-        named_sync(bar, kGroupThreads);   // every thread's E_c stores are issued
+        named_sync(bar, NT);   // every warp's E_c stores are issued
         const bool failed = ctl->fail != 0;
         if (tid == 0 && failed) record_error(p.ws, 2);
         if (tid == kStoreThread && p.flags && !failed) pend = cur.slot;
@@ -1419,6 +1439,8 @@ __device__ __forceinline__ void prep_group_gk(const TcParams &p, uint8_t *sm, ui
         cur = nx;
     }
     cp_async_wait_all();
+    if (lane == 0) bulk_wait0();   // the last chunk's E_c stores have completed ...
+    named_sync(bar, NT);           // ... in every warp, before it is published
     if (tid == kStoreThread && pend >= 0) release_slot(p, pend);
 }
 
@@ -1720,6 +1742,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap map_k,
                                                            const __grid_constant__ CUtensorMap map_v,
                                                            const __grid_constant__ CUtensorMap map_E,
+                                                           const __grid_constant__ CUtensorMap map_Ew,
                                                            TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -1729,7 +1752,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     }
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, grp = tid >> 8;
-    if constexpr (GK) {   // one prep group per CTA; the other 256 threads only join the barriers
+    if constexpr (GK) {   // one prep group of all 512 threads per CTA
         if (tid == 0) {
             PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(sm + GkSmem<D>::CTRL);
             mbar_init(&ctl->bar_mma, 1);
@@ -1743,9 +1766,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (grp == 0)
-            prep_group_gk<D>(p, sm, tmem_base, tid, 1, (long)((int)blockIdx.x - p.nchain),
-                             (long)((int)gridDim.x - p.nchain));
+        prep_group_gk<D>(&map_Ew, p, sm, tmem_base, tid, 1, (long)((int)blockIdx.x - p.nchain),
+                         (long)((int)gridDim.x - p.nchain));
         tc_fence_before();
         __syncthreads();
         if (tid < 32) {
@@ -1852,6 +1874,14 @@ bool map_E(CUtensorMap *m, const void *base, long slots, int R) {
     const uint32_t box[3] = {64u, (uint32_t)R, 1u};
     return make_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, true);
 }
+// E_c written in 16-row x 32-column boxes from 64-byte-swizzled staging tiles
+bool map_E_tiles(CUtensorMap *m, const void *base, long slots, int R) {
+    const uint64_t dims[3] = {(uint64_t)R, (uint64_t)R, (uint64_t)slots};
+    const uint64_t strides[2] = {(uint64_t)R * 2, (uint64_t)R * R * 2};
+    const uint32_t box[3] = {32u, 16u, 1u};
+    return make_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+}
 
 constexpr size_t kTableBytes(int nseq) { return (((size_t)(nseq + 1) * 4 + 255) / 256) * 256; }
 constexpr size_t kFlagBytes(long slots) { return (((size_t)slots * 4 + 255) / 256) * 256; }
@@ -1880,9 +1910,10 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.nsh = (long)a.nseq * a.H;
     p.maxnc = (a.T + kC - 1) / kC;   // varlen: a.T bounds the longest sequence
 
-    CUtensorMap mq, mk, mv, me;
+    CUtensorMap mq, mk, mv, me, mew;
     if (!map_tokens(&mq, a.q, total_rows, a.H, D) || !map_tokens(&mk, a.k, total_rows, a.H, D) ||
-        !map_tokens(&mv, a.v, total_rows, a.H, D) || !map_E(&me, p.E, slots_bound, R))
+        !map_tokens(&mv, a.v, total_rows, a.H, D) || !map_E(&me, p.E, slots_bound, R) ||
+        !map_E_tiles(&mew, p.E, slots_bound, R))
         return cudaErrorInvalidValue;
 
     cudaError_t e;
@@ -1918,7 +1949,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc_kernel<D, GK>, mq, mk, mv, me, pf);
+        e = cudaLaunchKernelEx(&cfg, tc_kernel<D, GK>, mq, mk, mv, me, mew, pf);
         if (e == cudaSuccess) return cudaSuccess;
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         (void)cudaGetLastError();   // fewer SMs available than reported: two launches
@@ -1930,7 +1961,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.n_items = slots_bound;
     p.nchain = 0;
     const long ctas = std::min<long>(GK ? slots_bound : (slots_bound + 1) / 2, (long)nsm);
-    tc_kernel<D, GK><<<(unsigned)ctas, kTcThreads, prep_smem, st>>>(mq, mk, mv, me, p);
+    tc_kernel<D, GK><<<(unsigned)ctas, kTcThreads, prep_smem, st>>>(mq, mk, mv, me, mew, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(chain_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);

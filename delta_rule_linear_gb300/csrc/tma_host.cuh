@@ -28,7 +28,7 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 16-bit data whose inner box is 64 elements (or no swizzle when swizzle128 = false).
 inline bool make_tensor_map(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base,
                             const uint64_t *dims, const uint64_t *strides_bytes,
-                            const uint32_t *box, bool swizzle128) {
+                            const uint32_t *box, CUtensorMapSwizzle swizzle) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     uint32_t estr[5] = {1, 1, 1, 1, 1};
@@ -36,10 +36,15 @@ inline bool make_tensor_map(CUtensorMap *map, CUtensorMapDataType dt, int rank, 
                      reinterpret_cast<const cuuint64_t *>(dims),
                      reinterpret_cast<const cuuint64_t *>(strides_bytes),
                      reinterpret_cast<const cuuint32_t *>(box), estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+inline bool make_tensor_map(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base,
+                            const uint64_t *dims, const uint64_t *strides_bytes,
+                            const uint32_t *box, bool swizzle128) {
+    return make_tensor_map(map, dt, rank, base, dims, strides_bytes, box,
+                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace kda
