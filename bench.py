@@ -325,52 +325,17 @@ def bench_secondary(args, world, rank, dev, peaks):
 
 
 # --------------------------------------------------------------------------- per-channel decay
-def bench_gk(args, world, rank, dev, peaks):
-    """Per-key-channel decay (TileOPs KDAFwdOp, g [B,T,H,K] = -0.01 U[0,1), the draw of the
-    kda-neuron-kernels README's examples): the batched decode step at the decode workload's
-    shape (HBM-bound: the fp32 state in and out), and the token-by-token prefill at the
-    training shape."""
+def bench_gk_chunk(args, world, rank, dev, peaks, out, D, e0, e1, long_only):
+    """Per-channel chunked prefill (tensor cores) at the long-sequence and training shapes."""
     import torch
     import delta_rule_linear_gb300 as kda
     stream = torch.cuda.current_stream()
-    out = {}
-
-    B, H, D, nsteps = 256, 32, 128, 32
-    rng = np.random.Generator(np.random.PCG64([rank, 7]))
-    state = torch.from_numpy((0.02 * rng.standard_normal((B, H, D, D), dtype=np.float32))).to(dev)
-    toks = []
-    for s in range(nsteps):
-        st = make_gk_decode_step(B, H, D, D, s, dtype="bf16", gate_scale=0.01, seed=rank)
-        toks.append(tuple(to_dev(st[n], dev, torch.bfloat16) for n in ("q", "k", "v")) +
-                    tuple(to_dev(st[n], dev, torch.float32) for n in ("beta", "g")))
-    o = torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev)
-
-    def run(n):
-        for s in range(n):
-            q, k, v, b, g = toks[s % nsteps]
-            kda.gk_decode_step(q, k, v, b, g, state, decayed_read=True, out=o, stream=stream)
-
-    run(3)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    run(nsteps)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1) / nsteps, world)
-    nbytes = 2.0 * B * H * D * D * 4 + B * H * D * 4      # state in + out, and g
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    out["gk_decode"] = {
-        "shape": dict(B=B, H=H, dk=D, dv=D), "decayed_read": True, "ms_per_step": ms,
-        "steps": nsteps, "gpu_launches": nsteps,
-        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                     "bytes_per_launch": nbytes}}
-
     from delta_rule_linear_gb300 import _lib
-    for name, (Bp, T, Hp) in (("gk_chunk_prefill_long", (1, 32768, 32)),
-                              ("gk_chunk_prefill_training", (2, 2048, 16))):
+    shapes = [("gk_chunk_prefill_long", (1, args.prefill_T or 32768, 32)),
+              ("gk_chunk_prefill_training", (2, 2048, 16))]
+    if long_only:
+        shapes = shapes[:1]
+    for name, (Bp, T, Hp) in shapes:
         d = make_gk(Bp, T, Hp, D, D, dtype="bf16", gate_scale=0.01, h0="normal002", seed=rank)
         q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
         beta, g, h0 = (to_dev(d[n], dev, torch.float32) for n in ("beta", "g", "h0"))
@@ -402,6 +367,55 @@ def bench_gk(args, world, rank, dev, peaks):
             "tc_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
             "gpu_launches_per_call": tc_prefill_launches(Bp, Hp, dev)}
         del q, k, v, beta, g, h0, o, hT, ws
+    return out
+
+
+def bench_gk(args, world, rank, dev, peaks):
+    """Per-key-channel decay (TileOPs KDAFwdOp, g [B,T,H,K] = -0.01 U[0,1), the draw of the
+    kda-neuron-kernels README's examples): the batched decode step at the decode workload's
+    shape (HBM-bound: the fp32 state in and out), and the token-by-token prefill at the
+    training shape."""
+    import torch
+    import delta_rule_linear_gb300 as kda
+    stream = torch.cuda.current_stream()
+    out = {}
+
+    B, H, D, nsteps = 256, 32, 128, 32
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.only == "gk_prefill":   # profiling: the long-sequence chunked prefill alone
+        return bench_gk_chunk(args, world, rank, dev, peaks, out, D, e0, e1, long_only=True)
+    rng = np.random.Generator(np.random.PCG64([rank, 7]))
+    state = torch.from_numpy((0.02 * rng.standard_normal((B, H, D, D), dtype=np.float32))).to(dev)
+    toks = []
+    for s in range(nsteps):
+        st = make_gk_decode_step(B, H, D, D, s, dtype="bf16", gate_scale=0.01, seed=rank)
+        toks.append(tuple(to_dev(st[n], dev, torch.bfloat16) for n in ("q", "k", "v")) +
+                    tuple(to_dev(st[n], dev, torch.float32) for n in ("beta", "g")))
+    o = torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev)
+
+    def run(n):
+        for s in range(n):
+            q, k, v, b, g = toks[s % nsteps]
+            kda.gk_decode_step(q, k, v, b, g, state, decayed_read=True, out=o, stream=stream)
+
+    run(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    run(nsteps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / nsteps, world)
+    nbytes = 2.0 * B * H * D * D * 4 + B * H * D * 4      # state in + out, and g
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["gk_decode"] = {
+        "shape": dict(B=B, H=H, dk=D, dv=D), "decayed_read": True, "ms_per_step": ms,
+        "steps": nsteps, "gpu_launches": nsteps,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "bytes_per_launch": nbytes}}
+
+    bench_gk_chunk(args, world, rank, dev, peaks, out, D, e0, e1, long_only=False)
 
     Bp, T, Hp = 2, 2048, 16
     d = make_gk(Bp, T, Hp, D, D, dtype="bf16", gate_scale=0.01, seed=rank)
@@ -540,7 +554,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "secondary", "gk"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "secondary", "gk", "gk_prefill"], default=None,
                     help="run one workload (profiling); the default runs both")
     ap.add_argument("--prefill-T", type=int, default=0,
                     help="profiling only: override T of the prefill workload (no CPU baseline)")
@@ -580,7 +594,7 @@ def main():
     pre = bench_prefill(args, world, rank, dev, peaks, d) if d is not None else None
     dec = bench_decode(args, world, rank, dev, peaks) if args.only in (None, "decode") else None
     sec = bench_secondary(args, world, rank, dev, peaks) if args.only in (None, "secondary") else None
-    if args.only in (None, "secondary", "gk"):
+    if args.only in (None, "secondary", "gk", "gk_prefill"):
         sec = dict(sec or {}, kda_gk=bench_gk(args, world, rank, dev, peaks))
     if rank != 0:
         return
