@@ -62,6 +62,11 @@ def _load():
             lib.kda_oracle_gk.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I,
                                           D, I, I, I, I, P, I, I]
             lib.kda_oracle_gk.restype = I
+            L = ctypes.c_long
+            lib.kda_oracle_gate_decay.argtypes = [P, P, P, P, L, I, I]
+            lib.kda_oracle_gate_decay.restype = None
+            lib.kda_oracle_beta.argtypes = [P, P, L, I]
+            lib.kda_oracle_beta.restype = None
             lib.kda_oracle_threads.argtypes = []
             lib.kda_oracle_threads.restype = I
             _lib = lib
@@ -206,3 +211,32 @@ def forward_gk(q, k, v, beta, g=None, h0=None, *, cu_seqlens=None, scale=None, u
     if rc < 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return o, hT
+
+
+def gate_decay(gate, A_log, dt_bias=None):
+    """fp64 kda_decay (ejkernel kernel_delta_attention, kda_decay): -exp(A_log) softplus(gate +
+    dt_bias).  gate [..., H] (one decay per head; A_log, dt_bias [H]) or [..., H, K] (one per key
+    channel; A_log [H], dt_bias [H, K]).  Returns float64 with gate's shape."""
+    gate = _f32(gate)
+    A_log = _f32(A_log)
+    H = A_log.shape[0]
+    if gate.shape[-1] == H and (dt_bias is None or np.asarray(dt_bias).ndim == 1):
+        K = 1
+    else:
+        K = gate.shape[-1]
+        assert gate.shape[-2] == H
+    dt_bias = _f32(dt_bias)
+    assert dt_bias is None or dt_bias.size == H * K
+    out = np.empty(gate.shape, dtype=np.float64)
+    rows = gate.size // (H * K)
+    _load().kda_oracle_gate_decay(_ptr(gate), _ptr(A_log), _ptr(dt_bias), _ptr(out), rows, H, K)
+    return out
+
+
+def beta_transform(x, allow_neg_eigval=False):
+    """fp64 beta from logits (TileOPs GDNFwdOp / KDAFwdOp use_beta_sigmoid_in_kernel):
+    sigmoid(x), or 2 sigmoid(x) with allow_neg_eigval."""
+    x = _f32(x)
+    out = np.empty(x.shape, dtype=np.float64)
+    _load().kda_oracle_beta(_ptr(x), _ptr(out), x.size, int(bool(allow_neg_eigval)))
+    return out

@@ -26,6 +26,12 @@
  *        Attention): the gated delta rule with one log-space decay per key
  *        channel, g [B,T,H,K]; GLARecurrentFwdOp prints the per-channel
  *        retention as diag(exp(gk)) applied to the state.
+ *   [P1'] the same page, kda_decay(): the per-token decay from a gate,
+ *        A = -exp(A_log), decay = A * softplus(gate + dt_bias), never positive.
+ *   [P3'] TileOPs "Linear Attention Operators", GDNFwdOp / KDAFwdOp:
+ *        use_beta_sigmoid_in_kernel (beta = sigmoid(x)), allow_neg_eigval
+ *        (beta = 2 sigmoid(x)), use_gate_in_kernel (the gate above, with A_log
+ *        and dt_bias).
  *   [P4] kda-neuron-kernels README, "What this package provides" and
  *        "Functional warning": the exact chunked form uses the per-channel
  *        factor exp(gc_i - gc_j) inside the chunk; the recurrent form is exact.
@@ -618,4 +624,32 @@ int kda_oracle_gk(const float *q, const float *k, const float *v,
     int used = run_all(pr, nprob, &op, nthreads);
     free(pr);
     return used;
+}
+
+/*
+ * [P1'] kda_decay(): decay = -exp(A_log[h]) * softplus(gate + dt_bias), with
+ * softplus(x) = log(1 + exp(x)).  gate is [rows, H, K] (K = 1 for one decay per
+ * head, K = dk for one per key channel), A_log [H], dt_bias [H, K] or NULL (zeros).
+ * Written in double; out has gate's layout.
+ */
+void kda_oracle_gate_decay(const float *gate, const float *A_log, const float *dt_bias,
+                           double *out, long rows, int H, int K)
+{
+    for (long r = 0; r < rows; ++r)
+        for (int h = 0; h < H; ++h)
+            for (int c = 0; c < K; ++c) {
+                const size_t i = ((size_t)r * H + h) * K + c;
+                const double x = (double)gate[i] + (dt_bias ? (double)dt_bias[(size_t)h * K + c] : 0.0);
+                const double sp = x > 700.0 ? x : log1p(exp(x));
+                out[i] = -exp((double)A_log[h]) * sp;
+            }
+}
+
+/* [P3'] beta = sigmoid(x) = 1 / (1 + exp(-x)), or twice that with allow_neg_eigval. */
+void kda_oracle_beta(const float *x, double *out, long n, int allow_neg_eigval)
+{
+    for (long i = 0; i < n; ++i) {
+        const double s = 1.0 / (1.0 + exp(-(double)x[i]));
+        out[i] = allow_neg_eigval ? 2.0 * s : s;
+    }
 }
