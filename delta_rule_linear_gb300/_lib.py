@@ -24,10 +24,34 @@ STATUS = {
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace", "kda_chunk_fwd",
            "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "kda_decode_step",
-           "kda_varlen_fwd_workspace", "kda_varlen_fwd", "kda_gk_chunk_fwd", "kda_gk_varlen_fwd",
-           "kda_gk_recurrent_fwd",
+           "kda_varlen_fwd_workspace", "kda_varlen_fwd", "kda_chunk_fwd_ex", "kda_varlen_fwd_ex",
+           "kda_recurrent_fwd_ex", "kda_decode_step_ex", "kda_gate_decay",
+           "kda_gk_chunk_fwd", "kda_gk_varlen_fwd", "kda_gk_recurrent_fwd",
            "kda_gk_varlen_recurrent_fwd", "kda_gk_decode_step", "kda_query_device_error",
            "kda_diag_wait_timeout")
+
+
+class KdaOptions(ctypes.Structure):
+    """struct kda_options of include/kda.h."""
+    _fields_ = [("decayed_read", ctypes.c_int), ("A_log", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p), ("beta_sigmoid", ctypes.c_int),
+                ("allow_neg_eigval", ctypes.c_int)]
+
+
+def make_options(decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
+                 allow_neg_eigval=False):
+    """A KdaOptions pointer (or None when every option is off).  A_log [H] and dt_bias
+    ([H] for a per-head decay, [H, dk] for g) are fp32 CUDA tensors; the caller keeps them
+    alive for the call."""
+    if not (decayed_read or A_log is not None or dt_bias is not None or beta_sigmoid):
+        return None
+    for t, name in ((A_log, "A_log"), (dt_bias, "dt_bias")):
+        if t is not None and (not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    o = KdaOptions(int(bool(decayed_read)), None if A_log is None else A_log.data_ptr(),
+                   None if dt_bias is None else dt_bias.data_ptr(), int(bool(beta_sigmoid)),
+                   int(bool(allow_neg_eigval)))
+    return ctypes.pointer(o)
 
 
 class KdaError(RuntimeError):
@@ -75,19 +99,31 @@ def load(path: str | None = None):
         lib.kda_varlen_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, I, F, I, I,
                                        P, Z, P]
         lib.kda_varlen_fwd.restype = I
-        lib.kda_gk_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P,
+        O = ctypes.POINTER(KdaOptions)
+        lib.kda_chunk_fwd_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, O, P, Z, P]
+        lib.kda_chunk_fwd_ex.restype = I
+        lib.kda_varlen_fwd_ex.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, I, F, I, I,
+                                          O, P, Z, P]
+        lib.kda_varlen_fwd_ex.restype = I
+        lib.kda_recurrent_fwd_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, O, P]
+        lib.kda_recurrent_fwd_ex.restype = I
+        lib.kda_decode_step_ex.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, I, O, P]
+        lib.kda_decode_step_ex.restype = I
+        lib.kda_gate_decay.argtypes = [P, P, P, P, ctypes.c_long, I, I, P]
+        lib.kda_gate_decay.restype = I
+        lib.kda_gk_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, O, P,
                                          Z, P]
         lib.kda_gk_chunk_fwd.restype = I
         lib.kda_gk_varlen_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, I, F, I, I,
-                                          I, P, Z, P]
+                                          O, P, Z, P]
         lib.kda_gk_varlen_fwd.restype = I
-        lib.kda_gk_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I,
+        lib.kda_gk_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, O,
                                              P]
         lib.kda_gk_recurrent_fwd.restype = I
         lib.kda_gk_varlen_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P,
-                                                    I, F, I, I, P]
+                                                    I, F, I, O, P]
         lib.kda_gk_varlen_recurrent_fwd.restype = I
-        lib.kda_gk_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, P]
+        lib.kda_gk_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, I, O, P]
         lib.kda_gk_decode_step.restype = I
         lib.kda_query_device_error.argtypes = [P, P]
         lib.kda_query_device_error.restype = I
@@ -150,11 +186,16 @@ def _workspace(nbytes, device, workspace):
 
 def chunk_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None, chunk_size=64,
               use_qk_l2norm=True, out=None, final_state=None, workspace=None, stream=None,
-              check_device=False):
-    """kda_chunk_fwd: chunked prefill.  Returns (o [B,T,H,dv], final_state [B,H,dk,dv] fp32).
+              check_device=False,
+              decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
+              allow_neg_eigval=False):
+    """kda_chunk_fwd (kda_chunk_fwd_ex when an option is set): chunked prefill.  Returns
+    (o [B,T,H,dv], final_state [B,H,dk,dv] fp32).
 
     check_device=True synchronises the stream afterwards and raises if a kernel recorded
-    a device error (a bounded wait that ran out) in the workspace header.
+    a device error (a bounded wait that ran out) in the workspace header.  The options are
+    those of kda_options: decayed_read, the in-kernel gate (decay holds the raw gate; A_log
+    [H], dt_bias [H]) and the beta transforms.
     """
     lib = load()
     B, T, H, dk = q.shape
@@ -172,11 +213,15 @@ def chunk_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None, chun
     if need == 0:
         raise KdaError(4, "kda_chunk_fwd_workspace", lib)
     ws = _workspace(need, q.device, workspace)
-    rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state),
-                           _ptr(o), _ptr(hT), B, T, H, dk, dv, dt, float(scale or 0.0),
-                           int(chunk_size), int(bool(use_qk_l2norm)), _ptr(ws),
-                           ws.numel() * ws.element_size(), _stream(stream))
-    _raise(rc, "kda_chunk_fwd", lib)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state), _ptr(o),
+            _ptr(hT), B, T, H, dk, dv, dt, float(scale or 0.0), int(chunk_size),
+            int(bool(use_qk_l2norm)))
+    tail = (_ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    if opts is None:
+        _raise(lib.kda_chunk_fwd(*args, *tail), "kda_chunk_fwd", lib)
+    else:
+        _raise(lib.kda_chunk_fwd_ex(*args, opts, *tail), "kda_chunk_fwd_ex", lib)
     if check_device:
         _raise(query_device_error(ws, stream), "kda_chunk_fwd (device)", lib)
     return o, hT
@@ -212,8 +257,11 @@ def chunk_fwd_noalloc(q, k, v, beta, decay=None, initial_state=None, *, scale=No
 
 
 def recurrent_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None,
-                  use_qk_l2norm=True, out=None, final_state=None, stream=None):
-    """kda_recurrent_fwd: token-by-token prefill.  Returns (o, final_state)."""
+                  use_qk_l2norm=True, out=None, final_state=None, stream=None,
+                  decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
+                  allow_neg_eigval=False):
+    """kda_recurrent_fwd (_ex with options, as chunk_fwd): token-by-token prefill.
+    Returns (o, final_state)."""
     lib = load()
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -224,15 +272,20 @@ def recurrent_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None,
     o = out if out is not None else torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     hT = final_state if final_state is not None else torch.empty((B, H, dk, dv), dtype=torch.float32,
                                                                   device=q.device)
-    rc = lib.kda_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay),
-                               _ptr(initial_state), _ptr(o), _ptr(hT), B, T, H, dk, dv, dt,
-                               float(scale or 0.0), int(bool(use_qk_l2norm)), _stream(stream))
-    _raise(rc, "kda_recurrent_fwd", lib)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state), _ptr(o),
+            _ptr(hT), B, T, H, dk, dv, dt, float(scale or 0.0), int(bool(use_qk_l2norm)))
+    if opts is None:
+        _raise(lib.kda_recurrent_fwd(*args, _stream(stream)), "kda_recurrent_fwd", lib)
+    else:
+        _raise(lib.kda_recurrent_fwd_ex(*args, opts, _stream(stream)), "kda_recurrent_fwd_ex", lib)
     return o, hT
 
 
 def decode_step(q, k, v, beta, decay, state, *, scale=None, use_qk_l2norm=True, out=None,
-                stream=None):
+                stream=None,
+                decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
+                allow_neg_eigval=False):
     """kda_decode_step: one token per sequence; ``state`` [B,H,dk,dv] fp32 is updated in place.
 
     q, k: [B,1,H,dk] (or [B,H,dk]); v: [B,1,H,dv]; beta, decay: [B,1,H] (decay may be None).
@@ -247,16 +300,21 @@ def decode_step(q, k, v, beta, decay, state, *, scale=None, use_qk_l2norm=True, 
     if q.numel() != B * H * dk or v.numel() != B * H * dv or beta.numel() != B * H:
         raise ValueError("decode inputs do not match the state's [B,H,dk,dv]")
     o = out if out is not None else torch.empty_like(v)
-    rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(state),
-                             _ptr(o), B, H, dk, dv, dt, float(scale or 0.0),
-                             int(bool(use_qk_l2norm)), _stream(stream))
-    _raise(rc, "kda_decode_step", lib)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(state), _ptr(o), B, H, dk,
+            dv, dt, float(scale or 0.0), int(bool(use_qk_l2norm)))
+    if opts is None:
+        _raise(lib.kda_decode_step(*args, _stream(stream)), "kda_decode_step", lib)
+    else:
+        _raise(lib.kda_decode_step_ex(*args, opts, _stream(stream)), "kda_decode_step_ex", lib)
     return o
 
 
 def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_seqlens_cpu=None,
                scale=None, chunk_size=64, use_qk_l2norm=True, out=None, final_state=None,
-               workspace=None, stream=None, check_device=False):
+               workspace=None, stream=None, check_device=False,
+               decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
+               allow_neg_eigval=False):
     """kda_varlen_fwd: packed sequences [1,total,H,D] split by cu_seqlens [N+1] (int32, device).
 
     Returns (o [1,total,H,dv], final_state [N,H,dk,dv] fp32).  check_device as in chunk_fwd.
@@ -283,23 +341,30 @@ def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_
     if need == 0:
         raise KdaError(4, "kda_varlen_fwd_workspace", lib)
     ws = _workspace(need, q.device, workspace)
-    rc = lib.kda_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(cu_seqlens),
-                            _ptr(host), N, total, H, dk, dv, _ptr(initial_state), _ptr(o), _ptr(hT),
-                            dt, float(scale or 0.0), int(chunk_size), int(bool(use_qk_l2norm)),
-                            _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
-    _raise(rc, "kda_varlen_fwd", lib)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(cu_seqlens), _ptr(host), N,
+            total, H, dk, dv, _ptr(initial_state), _ptr(o), _ptr(hT), dt, float(scale or 0.0),
+            int(chunk_size), int(bool(use_qk_l2norm)))
+    tail = (_ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    if opts is None:
+        _raise(lib.kda_varlen_fwd(*args, *tail), "kda_varlen_fwd", lib)
+    else:
+        _raise(lib.kda_varlen_fwd_ex(*args, opts, *tail), "kda_varlen_fwd_ex", lib)
     if check_device:
         _raise(query_device_error(ws, stream), "kda_varlen_fwd (device)", lib)
     return o, hT
 
 
 def gk_chunk_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None, cu_seqlens_cpu=None,
-                 scale=None, chunk_size=64, use_qk_l2norm=True, decayed_read=False, out=None,
-                 final_state=None, workspace=None, stream=None, check_device=False):
+                 scale=None, chunk_size=64, use_qk_l2norm=True, out=None, final_state=None,
+                 workspace=None, stream=None, check_device=False,
+                 decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
+                 allow_neg_eigval=False):
     """kda_gk_chunk_fwd / kda_gk_varlen_fwd: chunked prefill with one log decay per key
     channel (g with q's shape, fp32).  Packed when ``cu_seqlens`` is given (as
     gk_recurrent_fwd).  check_device as in chunk_fwd.  Returns (o, final_state)."""
     lib = load()
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
     Bq, T, H, dk = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -319,7 +384,7 @@ def gk_chunk_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None, 
         ws = _workspace(need, q.device, workspace)
         rc = lib.kda_gk_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state),
                                   _ptr(o), _ptr(hT), Bq, T, H, dk, dv, dt, float(scale or 0.0),
-                                  int(chunk_size), int(bool(use_qk_l2norm)), int(bool(decayed_read)),
+                                  int(chunk_size), int(bool(use_qk_l2norm)), opts,
                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
         _raise(rc, "kda_gk_chunk_fwd", lib)
     else:
@@ -338,7 +403,7 @@ def gk_chunk_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None, 
         rc = lib.kda_gk_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(cu_seqlens),
                                    _ptr(host), N, T, H, dk, dv, _ptr(initial_state), _ptr(o), _ptr(hT),
                                    dt, float(scale or 0.0), int(chunk_size), int(bool(use_qk_l2norm)),
-                                   int(bool(decayed_read)), _ptr(ws), ws.numel() * ws.element_size(),
+                                   opts, _ptr(ws), ws.numel() * ws.element_size(),
                                    _stream(stream))
         _raise(rc, "kda_gk_varlen_fwd", lib)
     if check_device:
@@ -347,14 +412,17 @@ def gk_chunk_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None, 
 
 
 def gk_recurrent_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None,
-                     cu_seqlens_cpu=None, scale=None, use_qk_l2norm=True, decayed_read=False,
-                     out=None, final_state=None, stream=None):
+                     cu_seqlens_cpu=None, scale=None, use_qk_l2norm=True, out=None,
+                     final_state=None, stream=None,
+                     decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
+                     allow_neg_eigval=False):
     """kda_gk_recurrent_fwd / kda_gk_varlen_recurrent_fwd: token-by-token prefill with one
     log decay per key channel, g with q's shape (fp32).  ``decayed_read`` selects where the
     delta term reads the memory.  With ``cu_seqlens`` (int32, device, [N+1]) the token
     arrays are packed [1,total,H,.] and the states are [N,H,dk,dv].  Returns (o, final_state).
     """
     lib = load()
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
     Bq, T, H, dk = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -371,7 +439,7 @@ def gk_recurrent_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=No
         rc = lib.kda_gk_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
                                       _ptr(initial_state), _ptr(o), _ptr(hT), Bq, T, H, dk, dv, dt,
                                       float(scale or 0.0), int(bool(use_qk_l2norm)),
-                                      int(bool(decayed_read)), _stream(stream))
+                                      opts, _stream(stream))
         _raise(rc, "kda_gk_recurrent_fwd", lib)
         return o, hT
     if Bq != 1:
@@ -386,16 +454,19 @@ def gk_recurrent_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=No
                                          _ptr(cu_seqlens), _ptr(host), N, T, H, dk, dv,
                                          _ptr(initial_state), _ptr(o), _ptr(hT), dt,
                                          float(scale or 0.0), int(bool(use_qk_l2norm)),
-                                         int(bool(decayed_read)), _stream(stream))
+                                         opts, _stream(stream))
     _raise(rc, "kda_gk_varlen_recurrent_fwd", lib)
     return o, hT
 
 
-def gk_decode_step(q, k, v, beta, g, state, *, scale=None, use_qk_l2norm=True,
-                   decayed_read=False, out=None, stream=None):
+def gk_decode_step(q, k, v, beta, g, state, *, scale=None, use_qk_l2norm=True, out=None,
+                   stream=None,
+                   decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
+                   allow_neg_eigval=False):
     """kda_gk_decode_step: one token per sequence with per-channel decay g [B,1,H,dk] fp32
     (or None); ``state`` [B,H,dk,dv] fp32 is updated in place.  Returns o with v's shape."""
     lib = load()
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
     B, H, dk, dv = state.shape
     dt = _dtype_code(q)
     _check(q, "q"); _check(k, "k", q.dtype); _check(v, "v", q.dtype)
@@ -407,7 +478,7 @@ def gk_decode_step(q, k, v, beta, g, state, *, scale=None, use_qk_l2norm=True,
     o = out if out is not None else torch.empty_like(v)
     rc = lib.kda_gk_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(state),
                                 _ptr(o), B, H, dk, dv, dt, float(scale or 0.0),
-                                int(bool(use_qk_l2norm)), int(bool(decayed_read)),
+                                int(bool(use_qk_l2norm)), opts,
                                 _stream(stream))
     _raise(rc, "kda_gk_decode_step", lib)
     return o
@@ -426,3 +497,20 @@ def diag_wait_timeout(workspace, limit_us, stream=None) -> None:
     nbytes = workspace.numel() * workspace.element_size()
     _raise(lib.kda_diag_wait_timeout(_ptr(workspace), nbytes, int(limit_us), _stream(stream)),
            "kda_diag_wait_timeout", lib)
+
+
+def gate_decay(gate, A_log, dt_bias=None, *, out=None, stream=None):
+    """kda_gate_decay (ejkernel kda_decay): -exp(A_log[h]) softplus(gate + dt_bias).
+    gate [..., H] with A_log, dt_bias [H], or [..., H, K] with dt_bias [H, K]; fp32 CUDA."""
+    lib = load()
+    H = A_log.numel()
+    K = 1 if gate.shape[-1] == H and (dt_bias is None or dt_bias.dim() == 1) else gate.shape[-1]
+    _check(gate, "gate", torch.float32); _check(A_log, "A_log", torch.float32)
+    _check(dt_bias, "dt_bias", torch.float32)
+    if dt_bias is not None and dt_bias.numel() != H * K:
+        raise ValueError("dt_bias must have H * K elements")
+    o = out if out is not None else torch.empty_like(gate)
+    rows = gate.numel() // (H * K)
+    _raise(lib.kda_gate_decay(_ptr(gate), _ptr(A_log), _ptr(dt_bias), _ptr(o), rows, H, K,
+                              _stream(stream)), "kda_gate_decay", lib)
+    return o

@@ -3,11 +3,12 @@
 // Chunked mode of ejkernel kda() ("Algorithm Modes": parallel inside a chunk,
 // sequential across chunks) in the WY / UT-transform form (the representation
 // TileOPs DeltaNetChunkFwdOp computes with prepare_wy_repr -> w, u).  For a chunk
-// of n <= C tokens entering with state S, G_t the inclusive in-chunk sum of decay:
+// of n <= C tokens entering with state S, G_t the inclusive in-chunk sum of decay, and
+// R_t = G_{t-1} (the delta term reads h_{t-1}) or G_t (it reads the decayed memory):
 //
-//   L[t][s]  = beta_t (k^_t . k^_s) exp(G_{t-1} - G_s)          s < t
+//   L[t][s]  = beta_t (k^_t . k^_s) exp(R_t - G_s)               s < t
 //   T        = (I + L)^{-1}                                      forward substitution
-//   W        = T diag(beta_s exp(G_{s-1})) K^                    [C, dk]
+//   W        = T diag(beta_s exp(R_s)) K^                        [C, dk]
 //   U0       = T diag(beta_s) V                                  [C, dv-tile]
 //   U        = U0 - W S                                          (the delta terms u_t)
 //   Aqk[t][s] = (q~_t . k^_s) exp(G_t - G_s)                     s <= t
@@ -118,8 +119,10 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(SeqBatch p) {
         }
         if (tid < C) {
             const size_t g = (size_t)(start + c0 + tid) * H + h;
-            sb[tid] = tid < nrow ? p.beta[g] : 0.f;
-            sG[tid] = (tid < nrow && p.decay) ? p.decay[g] : 0.f;  // decay; cumsum below
+            sb[tid] = tid < nrow ? beta_of(p.beta[g], p.beta_sig, p.neg_eig) : 0.f;
+            float d = (tid < nrow && p.decay) ? p.decay[g] : 0.f;  // decay; cumsum below
+            if (tid < nrow && p.decay && p.A_log) d = gate_decay(d, p.A_log[h], p.dt_bias ? p.dt_bias[h] : 0.f);
+            sG[tid] = d;
         }
         __syncthreads();
         if (tid == 0) {
@@ -132,8 +135,10 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(SeqBatch p) {
         }
         __syncthreads();
         const float gn = sG[C - 1];   // = G at the last valid row (padded decay is 0)
+        // the delta term reads h_{t-1} (R_t = G_{t-1}) or the decayed memory (R_t = G_t)
+        const float *sR = p.decayed_read ? sG : sGp;
         if (tid < C) {
-            sbg[tid] = sb[tid] * expf(sGp[tid]);
+            sbg[tid] = sb[tid] * expf(sR[tid]);
             skd[tid] = expf(gn - sG[tid]);
             seg[tid] = expf(sG[tid]);
         }
@@ -147,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(SeqBatch p) {
                 kk = fmaf(sK[t * KP + i], ks, kk);
                 qk = fmaf(sQ[t * KP + i], ks, qk);
             }
-            sL[t * CP + s] = s < t ? sb[t] * kk * expf(sGp[t] - sG[s]) : 0.f;
+            sL[t * CP + s] = s < t ? sb[t] * kk * expf(sR[t] - sG[s]) : 0.f;
             sA[t * CP + s] = s <= t ? qk * expf(sG[t] - sG[s]) : 0.f;
         }
         __syncthreads();
@@ -163,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(SeqBatch p) {
             }
         }
         __syncthreads();
-        // --- W = T diag(beta exp G_{t-1}) K^ ;  U0 = T diag(beta) V
+        // --- W = T diag(beta exp R) K^ ;  U0 = T diag(beta) V
         for (int idx = tid; idx < C * DK; idx += kThreads) {
             const int t = idx / DK, i = idx % DK;
             float acc = 0.f;

@@ -64,7 +64,10 @@ struct TcParams {
     int nc_equal;              // equal length: chunks per sequence
     const float *beta, *decay; // [rows, H]
     const float *gk;           // per-key-channel decay [rows, H, D] (per-channel kernels) or nullptr
-    int decayed_read;          // per-channel kernels: the delta term reads the decayed state
+    int decayed_read;          // the delta term reads the decayed state
+    const float *A_log;        // [H] or nullptr: decay / gk hold the raw gate (gate_decay)
+    const float *dt_bias;      // [H] (scalar decay) or [H, D] (per channel) or nullptr
+    int beta_sig, neg_eig;     // beta holds logits: sigmoid, or 2 sigmoid
     const float *h0;           // [nseq, H, D, D] or nullptr
     float *hT;                 // [nseq, H, D, D] or nullptr
     const __nv_bfloat16 *q, *k;   // [rows, H, D]
@@ -625,7 +628,16 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             mma_commit(&ctl->bar_mma);
         }
         if (warp == 0) {   // in-chunk cumulative log-decay: lane owns tokens 2 lane, 2 lane + 1
-            const float d0 = mdec[2 * lane], d1 = mdec[2 * lane + 1];
+            float d0 = mdec[2 * lane], d1 = mdec[2 * lane + 1];
+            if (p.A_log && p.decay) {   // the decay from the raw gate (zero past the valid tokens)
+                const float al = p.A_log[cur.h], bi = p.dt_bias ? p.dt_bias[cur.h] : 0.f;
+                d0 = 2 * lane < nv ? gate_decay(d0, al, bi) : 0.f;
+                d1 = 2 * lane + 1 < nv ? gate_decay(d1, al, bi) : 0.f;
+            }
+            if (p.beta_sig) {
+                mbeta[2 * lane] = 2 * lane < nv ? beta_of(mbeta[2 * lane], 1, p.neg_eig) : 0.f;
+                mbeta[2 * lane + 1] = 2 * lane + 1 < nv ? beta_of(mbeta[2 * lane + 1], 1, p.neg_eig) : 0.f;
+            }
             float incl = d0 + d1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -682,7 +694,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             const float gC = mG[63];
             if (i128 < 64) {
                 const int t = i128;
-                const float kt = mkn[t], bt = mbeta[t], gpt = mGp[t];
+                // R_t: G_{t-1} when the delta term reads h_{t-1}, G_t when it reads the decayed memory
+                const float kt = mkn[t], bt = mbeta[t], gpt = p.decayed_read ? mG[t] : mGp[t];
                 if (hh == 0) {
                     mf[t] = t < nv ? __expf(gC - mG[t]) * kt : 0.f;
                     mcw[t] = bt * __expf(gpt) * kt;   // column weight of T' = T diag(beta e^{G_{s-1}} kn)
@@ -1120,15 +1133,26 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
                 if (isq) mqn[t] = t < nv ? p.scale * inv : 0.f;
                 else mkn[t] = t < nv ? inv : 0.f;
             }
+            if (p.beta_sig && tid >= 448)   // beta from logits (zero past the valid tokens)
+                mbeta[tid - 448] = tid - 448 < nv ? beta_of(mbeta[tid - 448], 1, p.neg_eig) : 0.f;
         }
         {   // pass A: each token group's inclusive prefix in place (a channel pair per thread),
             // in log2 units
             const int c0 = 2 * (tid % NP), j = tid / NP;
             float2 acc = make_float2(0.f, 0.f);
+            const bool gate = p.A_log != nullptr;   // g holds the raw gate
+            const float al = gate ? p.A_log[cur.h] : 0.f;
+            const float2 bi = (gate && p.dt_bias)
+                                  ? make_float2(p.dt_bias[(size_t)cur.h * D + c0], p.dt_bias[(size_t)cur.h * D + c0 + 1])
+                                  : make_float2(0.f, 0.f);
 #pragma unroll
             for (int t = j * TPG; t < (j + 1) * TPG; ++t) {
                 float2 *x = reinterpret_cast<float2 *>(gf + t * D + c0);
-                const float2 gv = *x;
+                float2 gv = *x;
+                if (gate) {
+                    gv.x = t < nv ? gate_decay(gv.x, al, bi.x) : 0.f;
+                    gv.y = t < nv ? gate_decay(gv.y, al, bi.y) : 0.f;
+                }
                 acc.x = fmaf(gv.x, kLog2e, acc.x);
                 acc.y = fmaf(gv.y, kLog2e, acc.y);
                 *x = acc;
@@ -1897,6 +1921,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.beta = a.beta; p.decay = GK ? nullptr : a.decay; p.h0 = a.h0; p.hT = a.hT;
     p.gk = GK ? a.gk : nullptr;
     p.decayed_read = a.decayed_read;
+    p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_sig = a.beta_sig; p.neg_eig = a.neg_eig;
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.k = static_cast<const __nv_bfloat16 *>(a.k);
     p.rows = total_rows;

@@ -1,5 +1,6 @@
 // kda_api.cu -- the C ABI of include/kda.h: argument checks, workspace carving,
 // dispatch to the kernels.  Nothing here allocates device memory.
+#include <algorithm>
 #include <math.h>
 #include <string.h>
 
@@ -41,6 +42,28 @@ kda_status check_common(const void *q, const void *k, const void *v, const float
 }
 
 kda_status launch_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+// kda_options -> the batch fields; `gate` is the decay (or g) pointer the gate would replace
+kda_status apply_options(const kda_options *opt, const float *gate, SeqBatch &a) {
+    if (!opt) return KDA_OK;
+    if (!aligned4(opt->A_log) || !aligned4(opt->dt_bias)) return KDA_ERR_ALIGN;
+    if (opt->dt_bias && !opt->A_log) return KDA_ERR_NULL;
+    if (opt->A_log && !gate) return KDA_ERR_NULL;
+    a.decayed_read = opt->decayed_read ? 1 : 0;
+    a.A_log = opt->A_log;
+    a.dt_bias = opt->dt_bias;
+    a.beta_sig = opt->beta_sigmoid ? 1 : 0;
+    a.neg_eig = (opt->beta_sigmoid && opt->allow_neg_eigval) ? 1 : 0;
+    return KDA_OK;
+}
+
+__global__ void gate_decay_kernel(const float *gate, const float *A_log, const float *dt_bias,
+                                  float *decay, long n, int H, int K) {
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const int c = (int)(i % K), h = (int)((i / K) % H);
+        decay[i] = gate_decay(gate[i], A_log[h], dt_bias ? dt_bias[(size_t)h * K + c] : 0.f);
+    }
+}
 
 }  // namespace
 
@@ -123,6 +146,15 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const floa
                          float *final_state, int B, int T, int H, int dk, int dv,
                          kda_dtype dtype, float scale, int chunk_size, int use_qk_l2norm,
                          void *ws, size_t ws_bytes, kda_stream_t stream) {
+    return kda_chunk_fwd_ex(q, k, v, beta, decay, initial_state, o, final_state, B, T, H, dk, dv,
+                            dtype, scale, chunk_size, use_qk_l2norm, nullptr, ws, ws_bytes, stream);
+}
+
+kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *beta,
+                            const float *decay, const float *initial_state, void *o,
+                            float *final_state, int B, int T, int H, int dk, int dv,
+                            kda_dtype dtype, float scale, int chunk_size, int use_qk_l2norm,
+                            const kda_options *opt, void *ws, size_t ws_bytes, kda_stream_t stream) {
     if (B < 0 || T < 0) return KDA_ERR_SHAPE;
     kda_status c = check_common(q, k, v, beta, decay, initial_state, o, final_state,
                                 (long)B * T, H, dk, dv, dtype);
@@ -137,6 +169,7 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const floa
     a.dk = dk; a.dv = dv; a.chunk = chunk_size;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    if ((c = apply_options(opt, decay, a)) != KDA_OK) return c;
     a.ws = static_cast<WsHeader *>(ws);
     a.ws_body = static_cast<char *>(ws) + kWsHeader;
     a.ws_body_bytes = ws_bytes - kWsHeader;
@@ -150,6 +183,15 @@ kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const 
                              float *final_state, int B, int T, int H, int dk, int dv,
                              kda_dtype dtype, float scale, int use_qk_l2norm,
                              kda_stream_t stream) {
+    return kda_recurrent_fwd_ex(q, k, v, beta, decay, initial_state, o, final_state, B, T, H, dk,
+                                dv, dtype, scale, use_qk_l2norm, nullptr, stream);
+}
+
+kda_status kda_recurrent_fwd_ex(const void *q, const void *k, const void *v, const float *beta,
+                                const float *decay, const float *initial_state, void *o,
+                                float *final_state, int B, int T, int H, int dk, int dv,
+                                kda_dtype dtype, float scale, int use_qk_l2norm,
+                                const kda_options *opt, kda_stream_t stream) {
     if (B < 0 || T < 0) return KDA_ERR_SHAPE;
     kda_status c = check_common(q, k, v, beta, decay, initial_state, o, final_state,
                                 (long)B * T, H, dk, dv, dtype);
@@ -160,6 +202,7 @@ kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const 
     a.dk = dk; a.dv = dv; a.chunk = 0;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    if ((c = apply_options(opt, decay, a)) != KDA_OK) return c;
     return run_prefill(a, false, (long)B * T, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -167,12 +210,30 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
                            const float *decay, float *state, void *o, int B, int H, int dk,
                            int dv, kda_dtype dtype, float scale, int use_qk_l2norm,
                            kda_stream_t stream) {
+    return kda_decode_step_ex(q, k, v, beta, decay, state, o, B, H, dk, dv, dtype, scale,
+                              use_qk_l2norm, nullptr, stream);
+}
+
+// the decode arguments' option fields, by way of a batch
+static kda_status decode_options(const kda_options *opt, const float *gate, DecodeArgs &d) {
+    SeqBatch a{};
+    const kda_status c = apply_options(opt, gate, a);
+    d.decayed_read = a.decayed_read; d.A_log = a.A_log; d.dt_bias = a.dt_bias;
+    d.beta_sig = a.beta_sig; d.neg_eig = a.neg_eig;
+    return c;
+}
+
+kda_status kda_decode_step_ex(const void *q, const void *k, const void *v, const float *beta,
+                              const float *decay, float *state, void *o, int B, int H, int dk,
+                              int dv, kda_dtype dtype, float scale, int use_qk_l2norm,
+                              const kda_options *opt, kda_stream_t stream) {
     if (B < 0) return KDA_ERR_SHAPE;
     kda_status c = check_common(q, k, v, beta, decay, state, o, state, B, H, dk, dv, dtype);
     if (c != KDA_OK) return c;
     if (B > 0 && !state) return KDA_ERR_NULL;
-    if (B == 0) return KDA_OK;
     DecodeArgs a{};
+    if ((c = decode_options(opt, decay, a)) != KDA_OK) return c;
+    if (B == 0) return KDA_OK;
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = decay; a.state = state; a.o = o;
     a.B = B; a.H = H; a.dk = dk; a.dv = dv;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
@@ -186,6 +247,17 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v, const flo
                           void *o, float *final_state, kda_dtype dtype, float scale,
                           int chunk_size, int use_qk_l2norm, void *ws, size_t ws_bytes,
                           kda_stream_t stream) {
+    return kda_varlen_fwd_ex(q, k, v, beta, decay, cu_seqlens, cu_seqlens_host, N, total_T, H, dk,
+                             dv, initial_state, o, final_state, dtype, scale, chunk_size,
+                             use_qk_l2norm, nullptr, ws, ws_bytes, stream);
+}
+
+kda_status kda_varlen_fwd_ex(const void *q, const void *k, const void *v, const float *beta,
+                             const float *decay, const int *cu_seqlens, const int *cu_seqlens_host,
+                             int N, int total_T, int H, int dk, int dv, const float *initial_state,
+                             void *o, float *final_state, kda_dtype dtype, float scale,
+                             int chunk_size, int use_qk_l2norm, const kda_options *opt, void *ws,
+                             size_t ws_bytes, kda_stream_t stream) {
     if (N < 0 || total_T < 0) return KDA_ERR_SHAPE;
     kda_status c = check_common(q, k, v, beta, decay, initial_state, o, final_state,
                                 total_T, H, dk, dv, dtype);
@@ -213,6 +285,7 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v, const flo
     a.dk = dk; a.dv = dv; a.chunk = chunk_size;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    if ((c = apply_options(opt, decay, a)) != KDA_OK) return c;
     a.ws = static_cast<WsHeader *>(ws);
     a.ws_body = static_cast<char *>(ws) + kWsHeader;
     a.ws_body_bytes = ws_bytes - kWsHeader;
@@ -226,7 +299,7 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v, const flo
 kda_status kda_gk_chunk_fwd(const void *q, const void *k, const void *v, const float *beta,
                             const float *g, const float *initial_state, void *o, float *final_state,
                             int B, int T, int H, int dk, int dv, kda_dtype dtype, float scale,
-                            int chunk_size, int use_qk_l2norm, int decayed_read, void *ws,
+                            int chunk_size, int use_qk_l2norm, const kda_options *opt, void *ws,
                             size_t ws_bytes, kda_stream_t stream) {
     if (B < 0 || T < 0) return KDA_ERR_SHAPE;
     kda_status c = check_common(q, k, v, beta, nullptr, initial_state, o, final_state,
@@ -239,7 +312,8 @@ kda_status kda_gk_chunk_fwd(const void *q, const void *k, const void *v, const f
     if (!aligned16(ws)) return KDA_ERR_ALIGN;
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
-    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.gk = g; a.per_channel = 1;
+    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.o = o; a.hT = final_state; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
     a.dk = dk; a.dv = dv; a.chunk = chunk_size;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
@@ -256,7 +330,7 @@ kda_status kda_gk_varlen_fwd(const void *q, const void *k, const void *v, const 
                              const float *g, const int *cu_seqlens, const int *cu_seqlens_host,
                              int N, int total_T, int H, int dk, int dv, const float *initial_state,
                              void *o, float *final_state, kda_dtype dtype, float scale,
-                             int chunk_size, int use_qk_l2norm, int decayed_read, void *ws,
+                             int chunk_size, int use_qk_l2norm, const kda_options *opt, void *ws,
                              size_t ws_bytes, kda_stream_t stream) {
     if (N < 0 || total_T < 0) return KDA_ERR_SHAPE;
     kda_status c = check_common(q, k, v, beta, nullptr, initial_state, o, final_state,
@@ -282,7 +356,8 @@ kda_status kda_gk_varlen_fwd(const void *q, const void *k, const void *v, const 
     if (N == 0) return KDA_OK;
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
-    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.gk = g; a.per_channel = 1;
+    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.o = o; a.hT = final_state; a.cu_seqlens = cu_seqlens; a.nseq = N; a.T = max_len; a.H = H;
     a.dk = dk; a.dv = dv; a.chunk = chunk_size;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
@@ -299,7 +374,7 @@ kda_status kda_gk_recurrent_fwd(const void *q, const void *k, const void *v, con
                                 const float *g, const float *initial_state, void *o,
                                 float *final_state, int B, int T, int H, int dk, int dv,
                                 kda_dtype dtype, float scale, int use_qk_l2norm,
-                                int decayed_read, kda_stream_t stream) {
+                                const kda_options *opt, kda_stream_t stream) {
     if (B < 0 || T < 0) return KDA_ERR_SHAPE;
     kda_status c = check_common(q, k, v, beta, nullptr, initial_state, o, final_state,
                                 (long)B * T, H, dk, dv, dtype);
@@ -307,7 +382,8 @@ kda_status kda_gk_recurrent_fwd(const void *q, const void *k, const void *v, con
     if (!aligned16(g)) return KDA_ERR_ALIGN;
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
-    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.gk = g; a.per_channel = 1;
+    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.o = o; a.hT = final_state; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
     a.dk = dk; a.dv = dv; a.chunk = 0;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
@@ -321,7 +397,7 @@ kda_status kda_gk_varlen_recurrent_fwd(const void *q, const void *k, const void 
                                        int N, int total_T, int H, int dk, int dv,
                                        const float *initial_state, void *o, float *final_state,
                                        kda_dtype dtype, float scale, int use_qk_l2norm,
-                                       int decayed_read, kda_stream_t stream) {
+                                       const kda_options *opt, kda_stream_t stream) {
     if (N < 0 || total_T < 0) return KDA_ERR_SHAPE;
     kda_status c = check_common(q, k, v, beta, nullptr, initial_state, o, final_state,
                                 total_T, H, dk, dv, dtype);
@@ -337,7 +413,8 @@ kda_status kda_gk_varlen_recurrent_fwd(const void *q, const void *k, const void 
     if (N == 0) return KDA_OK;
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
-    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.gk = g; a.per_channel = 1;
+    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.o = o; a.hT = final_state; a.cu_seqlens = cu_seqlens; a.nseq = N; a.T = total_T; a.H = H;
     a.dk = dk; a.dv = dv; a.chunk = 0;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
@@ -350,20 +427,34 @@ kda_status kda_gk_varlen_recurrent_fwd(const void *q, const void *k, const void 
 kda_status kda_gk_decode_step(const void *q, const void *k, const void *v, const float *beta,
                               const float *g, float *state, void *o, int B, int H, int dk,
                               int dv, kda_dtype dtype, float scale, int use_qk_l2norm,
-                              int decayed_read, kda_stream_t stream) {
+                              const kda_options *opt, kda_stream_t stream) {
     if (B < 0) return KDA_ERR_SHAPE;
     kda_status c = check_common(q, k, v, beta, nullptr, state, o, state, B, H, dk, dv, dtype);
     if (c != KDA_OK) return c;
     if (!aligned16(g)) return KDA_ERR_ALIGN;
     if (B > 0 && !state) return KDA_ERR_NULL;
-    if (B == 0) return KDA_OK;
     DecodeArgs a{};
+    if ((c = decode_options(opt, g, a)) != KDA_OK) return c;
+    if (B == 0) return KDA_OK;
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.state = state; a.o = o;
-    a.gk = g; a.per_channel = 1; a.decayed_read = decayed_read ? 1 : 0;
+    a.gk = g; a.per_channel = 1;
     a.B = B; a.H = H; a.dk = dk; a.dv = dv;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
     return launch_status(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_gate_decay(const float *gate, const float *A_log, const float *dt_bias,
+                          float *decay, long rows, int H, int K, kda_stream_t stream) {
+    if (rows < 0 || H <= 0 || K <= 0) return KDA_ERR_SHAPE;
+    if (rows == 0) return KDA_OK;
+    if (!gate || !A_log || !decay) return KDA_ERR_NULL;
+    if (!aligned4(gate) || !aligned4(A_log) || !aligned4(dt_bias) || !aligned4(decay)) return KDA_ERR_ALIGN;
+    const long n = rows * (long)H * K;
+    const long blocks = std::min<long>((n + 255) / 256, 4096);
+    gate_decay_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        gate, A_log, dt_bias, decay, n, H, K);
+    return launch_status(cudaGetLastError());
 }
 
 kda_status kda_query_device_error(const void *ws, kda_stream_t stream) {

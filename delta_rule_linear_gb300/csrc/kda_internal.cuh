@@ -37,7 +37,10 @@ struct SeqBatch {
     const float *decay;       // [rows, H] or nullptr (zeros)
     const float *gk;          // per-channel decay [rows, H, dk] or nullptr (per_channel only)
     int per_channel;          // 1: the decay is gk, one value per key channel
-    int decayed_read;         // per_channel: the delta term reads the decayed state
+    int decayed_read;         // the delta term reads the decayed state
+    const float *A_log;       // [H] or nullptr: decay / gk hold the raw gate (gate_decay below)
+    const float *dt_bias;     // [H] (scalar) or [H, dk] (per channel) or nullptr
+    int beta_sig, neg_eig;    // beta holds logits: sigmoid, or 2 sigmoid with neg_eig
     const float *h0;          // [nseq, H, dk, dv] or nullptr (zeros)
     void *o;                  // [rows, H, dv]   (Tin)
     float *hT;                // [nseq, H, dk, dv] or nullptr
@@ -59,6 +62,8 @@ struct DecodeArgs {
     const float *beta, *decay;
     const float *gk;          // per-channel decay [B, H, dk] or nullptr (per_channel only)
     int per_channel, decayed_read;
+    const float *A_log, *dt_bias;   // as in SeqBatch
+    int beta_sig, neg_eig;
     float *state;
     void *o;
     int B, H, dk, dv;
@@ -99,6 +104,19 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
+}
+
+// kda_decay (ejkernel kernel_delta_attention): the log decay from a gate,
+// -exp(A_log) * softplus(gate + dt_bias), softplus(x) = log(1 + exp(x)).
+__device__ __forceinline__ float gate_decay(float gate, float a_log, float bias) {
+    const float x = gate + bias;
+    return -expf(a_log) * (x > 20.f ? x : log1pf(expf(x)));
+}
+// beta from logits (TileOPs GDNFwdOp / KDAFwdOp): sigmoid(x), or 2 sigmoid(x)
+__device__ __forceinline__ float beta_of(float x, int sig, int neg) {
+    if (!sig) return x;
+    const float s = 1.f / (1.f + expf(-x));
+    return neg ? 2.f * s : s;
 }
 
 // Token row range of sequence n.

@@ -39,7 +39,9 @@ struct ScanParams {
     int nseq, T, H, DV;
     float scale;
     int use_l2;
-    int decayed_read;  // GK kernels: the delta term reads D S instead of S
+    int decayed_read;  // the delta term reads the decayed state (D S, or alpha S)
+    const float *A_log, *dt_bias;   // raw gate -> decay (gate_decay); dt_bias [H] or [H, DK]
+    int beta_sig, neg_eig;
 };
 
 template <typename Tin, int DK, int DVS, bool GK>
@@ -92,14 +94,21 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
         const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
         if (tid < DK) {
             s_k[tid] = to_f32(k[qk_off + tid]);
-            if constexpr (GK) s_a[tid] = p.gk ? expf(p.gk[qk_off + tid]) : 1.f;
+            if constexpr (GK) {
+                float gv = p.gk ? p.gk[qk_off + tid] : 0.f;
+                if (p.gk && p.A_log)
+                    gv = gate_decay(gv, p.A_log[h], p.dt_bias ? p.dt_bias[(size_t)h * DK + tid] : 0.f);
+                s_a[tid] = expf(gv);
+            }
         } else if (tid < 2 * DK) {
             s_q[tid - DK] = to_f32(q[qk_off + tid - DK]);
         }
         if (tid < DVS) s_v[tid] = to_f32(v[v_off + tid]);
         if (tid == 0) {
-            s_sc[0] = p.beta[(size_t)row * p.H + h];
-            s_sc[1] = p.decay ? p.decay[(size_t)row * p.H + h] : 0.f;
+            s_sc[0] = beta_of(p.beta[(size_t)row * p.H + h], p.beta_sig, p.neg_eig);
+            float d = p.decay ? p.decay[(size_t)row * p.H + h] : 0.f;
+            if (p.decay && p.A_log) d = gate_decay(d, p.A_log[h], p.dt_bias ? p.dt_bias[h] : 0.f);
+            s_sc[1] = d;
         }
         __syncthreads();
 
@@ -143,7 +152,8 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
                 rs += s_red[0][g][tid];
                 ps += s_red[1][g][tid];
             }
-            const float u = s_sc[0] * (s_v[tid] - kn * rs);
+            // the decayed read with one decay per head: r = (alpha S)^T k
+            const float u = s_sc[0] * (s_v[tid] - kn * ((!GK && p.decayed_read) ? alpha * rs : rs));
             const float out = (GK ? 1.f : alpha) * (qn * ps) + (kn * qn * s_sc[4]) * u;
             s_u[tid] = u;
             o[v_off + tid] = from_f32<Tin>(out);
@@ -213,6 +223,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     p.h0 = a.state; p.hT = a.state; p.o = a.o; p.cu_seqlens = nullptr;
     p.nseq = a.B; p.T = 1; p.H = a.H; p.DV = a.dv; p.scale = a.scale; p.use_l2 = a.use_l2;
     p.gk = a.gk; p.decayed_read = a.decayed_read;
+    p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_sig = a.beta_sig; p.neg_eig = a.neg_eig;
     // one CTA per head, whole value width
     return launch_scan(p, a.dtype, a.dk, a.dv, a.per_channel != 0, s);
 }
@@ -223,6 +234,7 @@ cudaError_t launch_recurrent(const SeqBatch &a, cudaStream_t s) {
     p.h0 = a.h0; p.hT = a.hT; p.o = a.o; p.cu_seqlens = a.cu_seqlens;
     p.nseq = a.nseq; p.T = a.T; p.H = a.H; p.DV = a.dv; p.scale = a.scale; p.use_l2 = a.use_l2;
     p.gk = a.gk; p.decayed_read = a.decayed_read;
+    p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_sig = a.beta_sig; p.neg_eig = a.neg_eig;
     // 32-column slabs: a long prefill is latency-bound per token, so spread the
     // independent value columns over more CTAs.
     return launch_scan(p, a.dtype, a.dk, 32, a.per_channel != 0, s);

@@ -74,6 +74,23 @@ typedef enum kda_status {
  * (TileOPs DeltaNetFwdOp: the recurrent state is FP32). */
 typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
+/*
+ * Options of the *_ex and kda_gk_* entry points: the decay placement, and the gate and
+ * beta prologues done inside the kernels (TileOPs "Linear Attention Operators", GDNFwdOp /
+ * KDAFwdOp: use_gate_in_kernel, use_beta_sigmoid_in_kernel, allow_neg_eigval; ejkernel
+ * kda_decay()).  A NULL pointer or a zeroed struct is the plain recurrence above.
+ */
+typedef struct kda_options {
+    int decayed_read;       /* 0: the delta term reads h_{t-1} (the order printed above);
+                               1: it reads the decayed memory, exp(decay_t) h_{t-1} (per key
+                               channel: diag(exp g_t) h_{t-1}) -- the gated delta rule          */
+    const float *A_log;     /* [H], device.  Non-NULL: decay (or g) holds the raw gate and the
+                               kernels use  -exp(A_log[h]) * softplus(gate + dt_bias)  (kda_decay) */
+    const float *dt_bias;   /* [H] for a per-head decay, [H, dk] for g; device; NULL = zeros     */
+    int beta_sigmoid;       /* nonzero: beta holds logits and the kernels use sigmoid(beta) ...  */
+    int allow_neg_eigval;   /* ... or 2 sigmoid(beta) when this is nonzero as well               */
+} kda_options;
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *kda_status_string(kda_status s);
 
@@ -204,13 +221,14 @@ kda_status kda_varlen_fwd(const void *q, const void *k, const void *v,
  * GLARecurrentFwdOp writes that retention as diag(exp(gk)) applied to the state).
  * Per (b, h), with D_t = diag(exp(g_t)) scaling row i (key channel i) of the memory:
  *
- *     decayed_read == 0:   u_t = beta_t * (v_t - h_{t-1}^T k^_t)
- *     decayed_read != 0:   u_t = beta_t * (v_t - (D_t h_{t-1})^T k^_t)   (gated delta rule)
+ *     opt->decayed_read == 0:   u_t = beta_t * (v_t - h_{t-1}^T k^_t)
+ *     opt->decayed_read != 0:   u_t = beta_t * (v_t - (D_t h_{t-1})^T k^_t)   (gated delta rule)
  *     h_t = D_t h_{t-1} + k^_t u_t^T,      o_t = h_t^T q~_t
  *
  * k^, q~, scale and use_qk_l2norm as above.  With every channel of g_t equal to decay_t
  * and decayed_read == 0 this is the recurrence at the top of this header; without decay
- * the two placements coincide.
+ * the two placements coincide.  opt (may be NULL) also selects the in-kernel gate
+ * (g holds the raw gate; dt_bias is [H, dk]) and beta transforms.
  *   g   [B,T,H,dk] float32, the layout of q and k; NULL means no decay.  16-byte aligned.
  * Every other argument, layout and rule as kda_recurrent_fwd / kda_varlen_fwd /
  * kda_decode_step.  The three *_recurrent_fwd / decode entry points run on CUDA cores,
@@ -220,13 +238,13 @@ kda_status kda_gk_recurrent_fwd(const void *q, const void *k, const void *v,
                                 const float *beta, const float *g,
                                 const float *initial_state, void *o, float *final_state,
                                 int B, int T, int H, int dk, int dv, kda_dtype dtype,
-                                float scale, int use_qk_l2norm, int decayed_read,
+                                float scale, int use_qk_l2norm, const kda_options *opt,
                                 kda_stream_t stream);
 
 /*
  * Chunked prefill with per-key-channel decay: the same results as kda_gk_recurrent_fwd.
  * Arguments, workspace (its size is kda_chunk_fwd_workspace()), errors and device error
- * word as kda_chunk_fwd, plus g and decayed_read as above.  bf16 with dk == dv in {64, 128}
+ * word as kda_chunk_fwd, plus g and opt as above.  bf16 with dk == dv in {64, 128}
  * and chunk_size 64 runs on the tensor cores: the chunk's per-channel factors
  * exp(G_t[c] - G_s[c]) are split at 16-token sub-blocks (kda-neuron-kernels README: the
  * exact sub-chunk form), and a sub-block whose decay spans more than e^60 in some channel
@@ -237,18 +255,18 @@ kda_status kda_gk_chunk_fwd(const void *q, const void *k, const void *v,
                             const float *beta, const float *g,
                             const float *initial_state, void *o, float *final_state,
                             int B, int T, int H, int dk, int dv, kda_dtype dtype,
-                            float scale, int chunk_size, int use_qk_l2norm, int decayed_read,
+                            float scale, int chunk_size, int use_qk_l2norm, const kda_options *opt,
                             void *ws, size_t ws_bytes, kda_stream_t stream);
 
 /* Packed chunked prefill with per-key-channel decay: kda_varlen_fwd's arguments and
- * workspace (kda_varlen_fwd_workspace()) plus g [1,total_T,H,dk] and decayed_read. */
+ * workspace (kda_varlen_fwd_workspace()) plus g [1,total_T,H,dk] and opt. */
 kda_status kda_gk_varlen_fwd(const void *q, const void *k, const void *v,
                              const float *beta, const float *g,
                              const int *cu_seqlens, const int *cu_seqlens_host,
                              int N, int total_T, int H, int dk, int dv,
                              const float *initial_state, void *o, float *final_state,
                              kda_dtype dtype, float scale, int chunk_size, int use_qk_l2norm,
-                             int decayed_read, void *ws, size_t ws_bytes, kda_stream_t stream);
+                             const kda_options *opt, void *ws, size_t ws_bytes, kda_stream_t stream);
 
 /* Packed form: q, k, g [1,total_T,H,dk]; v, o [1,total_T,H,dv]; beta [1,total_T,H];
  * cu_seqlens / cu_seqlens_host and the [N,H,dk,dv] states as kda_varlen_fwd. */
@@ -258,13 +276,55 @@ kda_status kda_gk_varlen_recurrent_fwd(const void *q, const void *k, const void 
                                        int N, int total_T, int H, int dk, int dv,
                                        const float *initial_state, void *o, float *final_state,
                                        kda_dtype dtype, float scale, int use_qk_l2norm,
-                                       int decayed_read, kda_stream_t stream);
+                                       const kda_options *opt, kda_stream_t stream);
 
 /* One token per sequence: q, k, g [B,1,H,dk]; the state is updated in place. */
 kda_status kda_gk_decode_step(const void *q, const void *k, const void *v,
                               const float *beta, const float *g, float *state, void *o,
                               int B, int H, int dk, int dv, kda_dtype dtype, float scale,
-                              int use_qk_l2norm, int decayed_read, kda_stream_t stream);
+                              int use_qk_l2norm, const kda_options *opt, kda_stream_t stream);
+
+/*
+ * The scalar-decay entry points with options (see kda_options): the same arguments, layouts,
+ * workspace and errors as kda_chunk_fwd / kda_varlen_fwd / kda_recurrent_fwd /
+ * kda_decode_step, plus `opt` (may be NULL).  A_log and dt_bias must be 4-byte aligned
+ * (KDA_ERR_ALIGN); dt_bias without A_log is KDA_ERR_NULL.  With A_log given, decay must
+ * not be NULL (it is the gate).
+ */
+kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v,
+                            const float *beta, const float *decay,
+                            const float *initial_state, void *o, float *final_state,
+                            int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                            float scale, int chunk_size, int use_qk_l2norm,
+                            const kda_options *opt, void *ws, size_t ws_bytes,
+                            kda_stream_t stream);
+kda_status kda_varlen_fwd_ex(const void *q, const void *k, const void *v,
+                             const float *beta, const float *decay,
+                             const int *cu_seqlens, const int *cu_seqlens_host,
+                             int N, int total_T, int H, int dk, int dv,
+                             const float *initial_state, void *o, float *final_state,
+                             kda_dtype dtype, float scale, int chunk_size, int use_qk_l2norm,
+                             const kda_options *opt, void *ws, size_t ws_bytes,
+                             kda_stream_t stream);
+kda_status kda_recurrent_fwd_ex(const void *q, const void *k, const void *v,
+                                const float *beta, const float *decay,
+                                const float *initial_state, void *o, float *final_state,
+                                int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                                float scale, int use_qk_l2norm, const kda_options *opt,
+                                kda_stream_t stream);
+kda_status kda_decode_step_ex(const void *q, const void *k, const void *v,
+                              const float *beta, const float *decay, float *state, void *o,
+                              int B, int H, int dk, int dv, kda_dtype dtype, float scale,
+                              int use_qk_l2norm, const kda_options *opt, kda_stream_t stream);
+
+/*
+ * The decay from a gate on its own (ejkernel kda_decay()):
+ *     decay[r, h, c] = -exp(A_log[h]) * softplus(gate[r, h, c] + dt_bias[h, c])
+ * gate, decay [rows, H, K] float32 (K = 1: one decay per head; K = dk: per key channel);
+ * A_log [H]; dt_bias [H, K] or NULL (zeros).  Device pointers; decay may alias gate.
+ */
+kda_status kda_gate_decay(const float *gate, const float *A_log, const float *dt_bias,
+                          float *decay, long rows, int H, int K, kda_stream_t stream);
 
 /*
  * Read the device error word that the kernels of the most recent kda_chunk_fwd /

@@ -39,7 +39,7 @@ import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "round_to_bf16", "make_prefill", "make_varlen",
            "make_decode_state", "make_decode_step", "make_custom", "make_gk",
-           "make_gk_decode_step"]
+           "make_gk_decode_step", "make_gate_params"]
 
 
 @dataclass(frozen=True)
@@ -215,3 +215,16 @@ def make_gk_decode_step(B, H, dk, dv, step, *, dtype="bf16", gate_scale=0.01, se
     beta = _sigmoid(rng.standard_normal((B, 1, H), dtype=np.float32))
     g = (-gate_scale * rng.random((B, 1, H, dk), dtype=np.float32)).astype(np.float32)
     return dict(q=q, k=k, v=v, beta=beta, g=g)
+
+
+def make_gate_params(shape, H, K=1, seed=0):
+    """Raw gates for the in-kernel decay (ejkernel kda_decay; TileOPs use_gate_in_kernel), drawn
+    the usual state-space way: gate ~ N(0, 1) with the given shape (trailing dims [H] or [H, K]),
+    A = exp(A_log) ~ U[1, 16), and dt_bias the inverse softplus of dt = exp(U[ln 1e-3, ln 1e-1)),
+    [H] or [H, K].  Returns float32 (gate, A_log, dt_bias)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 99]))
+    gate = rng.standard_normal(shape, dtype=np.float32)
+    A_log = np.log(rng.uniform(1.0, 16.0, size=H)).astype(np.float32)
+    dt = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), size=(H,) if K == 1 else (H, K)))
+    dt_bias = np.log(np.expm1(dt)).astype(np.float32)
+    return gate, A_log, dt_bias

@@ -154,11 +154,11 @@ def test_gk_entry_points_reject_bad_arguments(lib):
     """Per-key-channel decay: the same checks, plus g's 16-byte alignment."""
     def rec(**kw):
         a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), g=_fake(), h0=None, o=_fake(),
-                 hT=None, B=1, T=64, H=2, dk=64, dv=64, dt=1, l2=1, dr=1)
+                 hT=None, B=1, T=64, H=2, dk=64, dv=64, dt=1, l2=1, opt=None)
         a.update(kw)
         return lib.kda_gk_recurrent_fwd(a["q"], a["k"], a["v"], a["beta"], a["g"], a["h0"],
                                         a["o"], a["hT"], a["B"], a["T"], a["H"], a["dk"],
-                                        a["dv"], a["dt"], 0.0, a["l2"], a["dr"], None)
+                                        a["dv"], a["dt"], 0.0, a["l2"], a["opt"], None)
     assert rec(q=None) == 1
     assert rec(T=-1) == 2
     assert rec(dt=9) == 3
@@ -168,11 +168,11 @@ def test_gk_entry_points_reject_bad_arguments(lib):
 
     def dec(**kw):
         a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), g=None, state=_fake(),
-                 o=_fake(), B=4, H=2, dk=128, dv=128, dt=1, l2=1, dr=0)
+                 o=_fake(), B=4, H=2, dk=128, dv=128, dt=1, l2=1, opt=None)
         a.update(kw)
         return lib.kda_gk_decode_step(a["q"], a["k"], a["v"], a["beta"], a["g"], a["state"],
                                       a["o"], a["B"], a["H"], a["dk"], a["dv"], a["dt"], 0.0,
-                                      a["l2"], a["dr"], None)
+                                      a["l2"], a["opt"], None)
     assert dec(state=None) == 1
     assert dec(g=_fake(0x1008)) == 5
     assert dec(dv=16) == 4
@@ -186,7 +186,7 @@ def test_gk_entry_points_reject_bad_arguments(lib):
         return lib.kda_gk_varlen_recurrent_fwd(a["q"], a["k"], a["v"], a["beta"], a["g"],
                                                a["cu"], ctypes.cast(hs, ctypes.c_void_p), N,
                                                total, a["H"], a["dk"], a["dv"], a["h0"], a["o"],
-                                               a["hT"], a["dt"], 0.0, 1, 0, None)
+                                               a["hT"], a["dt"], 0.0, 1, None, None)
     assert var([0, 4, 3, 10]) == 9
     assert var([0, 4, 6, 9]) == 9
     assert var([0, 4, 6, 10], cu=None) == 1
@@ -200,7 +200,7 @@ def test_gk_chunk_entry_points_reject_bad_arguments(lib):
         a.update(kw)
         return lib.kda_gk_chunk_fwd(a["q"], a["k"], a["v"], a["beta"], a["g"], a["h0"], a["o"],
                                     a["hT"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["dt"], 0.0,
-                                    a["chunk"], 1, 1, a["ws"], a["ws_bytes"], None)
+                                    a["chunk"], 1, None, a["ws"], a["ws_bytes"], None)
     assert call(k=None) == 1
     assert call(H=-1) == 2
     assert call(dt=4) == 3
@@ -211,4 +211,42 @@ def test_gk_chunk_entry_points_reject_bad_arguments(lib):
     hs = (ctypes.c_int * 3)(0, 5, 4)
     assert lib.kda_gk_varlen_fwd(_fake(), _fake(), _fake(), _fake(), _fake(), _fake(),
                                  ctypes.cast(hs, ctypes.c_void_p), 2, 4, 2, 64, 64, None, _fake(),
-                                 None, 1, 0.0, 64, 1, 0, _fake(), 1 << 30, None) == 9
+                                 None, 1, 0.0, 64, 1, None, _fake(), 1 << 30, None) == 9
+
+
+
+def _opts(**kw):
+    import ctypes as ct
+    from delta_rule_linear_gb300 import _lib
+    o = _lib.KdaOptions(kw.get("decayed_read", 0), kw.get("A_log"), kw.get("dt_bias"),
+                        kw.get("beta_sigmoid", 0), kw.get("allow_neg_eigval", 0))
+    return ct.pointer(o)
+
+
+def test_options_are_checked(lib):
+    """kda_options: dt_bias needs A_log, A_log needs the decay (gate) array, 4-byte alignment."""
+    def chunk(opt, decay=_fake()):
+        return lib.kda_chunk_fwd_ex(_fake(), _fake(), _fake(), _fake(), decay, None, _fake(), None,
+                                    1, 64, 2, 64, 64, 1, 0.0, 64, 1, opt, _fake(), 1 << 30, None)
+    assert chunk(_opts(dt_bias=0x2000)) == 1
+    assert chunk(_opts(A_log=0x2000), decay=None) == 1
+    assert chunk(_opts(A_log=0x2002)) == 5
+    assert chunk(_opts(A_log=0x2000, dt_bias=0x2001)) == 5
+
+    def dec(opt, B=4):
+        return lib.kda_decode_step_ex(_fake(), _fake(), _fake(), _fake(), _fake(), _fake(), _fake(),
+                                      B, 2, 64, 64, 1, 0.0, 1, opt, None)
+    assert dec(_opts(dt_bias=0x2000)) == 1
+    assert dec(_opts(dt_bias=0x2000), B=0) == 1    # checked before the empty-batch return
+    assert dec(_opts(decayed_read=1), B=0) == 0
+    assert lib.kda_gk_decode_step(_fake(), _fake(), _fake(), _fake(), None, _fake(), _fake(), 4, 2,
+                                  64, 64, 1, 0.0, 1, _opts(A_log=0x2000), None) == 1
+
+
+def test_gate_decay_argument_errors(lib):
+    assert lib.kda_gate_decay(_fake(), _fake(), None, _fake(), -1, 2, 1, None) == 2
+    assert lib.kda_gate_decay(_fake(), _fake(), None, _fake(), 10, 0, 1, None) == 2
+    assert lib.kda_gate_decay(None, _fake(), None, _fake(), 10, 2, 1, None) == 1
+    assert lib.kda_gate_decay(_fake(), None, None, _fake(), 10, 2, 1, None) == 1
+    assert lib.kda_gate_decay(_fake(0x1002), _fake(), None, _fake(), 10, 2, 1, None) == 5
+    assert lib.kda_gate_decay(_fake(), _fake(), None, _fake(), 0, 2, 1, None) == 0
