@@ -31,8 +31,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from kda_inputs import (WORKLOADS, make_decode_state, make_decode_step, make_gk,  # noqa: E402
-                        make_gk_decode_step, make_prefill, make_varlen)
+from kda_inputs import (WORKLOADS, make_decode_state, make_decode_step, make_gate_params,  # noqa: E402
+                        make_gk, make_gk_decode_step, make_prefill, make_varlen)
 
 METRIC = "prefill tokens/s & % bf16 TC peak; decode state GB/s vs HBM peak (1×GB300)"
 NOMINAL_HBM_GBS = 8000.0
@@ -325,6 +325,27 @@ def bench_secondary(args, world, rank, dev, peaks):
         "workload": wl.name, "ms_per_call": ms, "tokens_per_s": wl.B * wl.T * world / (ms * 1e-3),
         "tc_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
         "gpu_launches_per_call": tc_prefill_launches(wl.B, wl.H, dev)}
+
+    # the long-sequence workload with the prologues in the kernel: decay from a raw gate
+    # (kda_decay), beta from logits (sigmoid), the decayed read
+    wl = WORKLOADS[3]
+    d = make_prefill(wl, seed=rank)
+    gate, A_log, dt_bias = make_gate_params((wl.B, wl.T, wl.H), wl.H, seed=rank)
+    q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
+    braw = to_dev(((2.0 * d["beta"] - 1.0) * 3).astype(np.float32), dev, torch.float32)
+    graw, al, db, h0 = (to_dev(x, dev, torch.float32) for x in (gate, A_log, dt_bias, d["h0"]))
+    o = torch.empty_like(v)
+    hT = torch.empty((wl.B, wl.H, wl.dk, wl.dv), dtype=torch.float32, device=dev)
+    ws = torch.empty(_lib.chunk_fwd_workspace_bytes(wl.B, wl.T, wl.H, wl.dk, wl.dv, wl.chunk,
+                                                    _lib.KDA_BF16), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: kda.chunk_fwd(q, k, v, braw, graw, h0, chunk_size=wl.chunk, out=o,
+                                     final_state=hT, workspace=ws, stream=stream, decayed_read=True,
+                                     A_log=al, dt_bias=db, beta_sigmoid=True))
+    out["gated_long_prefill"] = {
+        "workload": wl.name + ", raw gate + beta logits + decayed read in the kernel",
+        "ms_per_call": ms, "tokens_per_s": wl.B * wl.T * world / (ms * 1e-3),
+        "gpu_launches_per_call": tc_prefill_launches(wl.B, wl.H, dev)}
+    del q, k, v, braw, graw, al, db, h0, o, hT, ws
 
     wl = WORKLOADS[5]
     d = make_varlen(wl, seed=rank)

@@ -483,6 +483,7 @@ struct PrepSmem {
 struct PrepCtrl {
     uint64_t bar_mma;
     int fail;
+    float gate[2];   // A_log and dt_bias of the chunk's head (raw-gate decay), loaded with beta
 };
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
@@ -522,14 +523,19 @@ __device__ __forceinline__ void load_rows(const TcParams &p, uint8_t *sKQ, const
     cp_async_commit();
 }
 // beta, decay of one chunk into the per-token scalars (zero past the chunk's valid tokens;
-// decay zero when absent)
-__device__ __forceinline__ void load_scalars(const TcParams &p, float *mbeta, float *mdec,
+// decay zero when absent); with a raw-gate decay also A_log and dt_bias of the head, so that
+// no global load sits on the prefix's path
+__device__ __forceinline__ void load_scalars(const TcParams &p, float *mbeta, float *mdec, float *gate,
                                              const ChunkItem &it, int tid) {
     const int t = tid - 64;   // warps 2, 3
     if (t >= 0 && t < 64) {
         const long gi = (it.row0 + (t < it.nv ? t : 0)) * p.H + it.h;
         cp_async4(mbeta + t, p.beta + gi, t < it.nv ? 4u : 0u);
         cp_async4(mdec + t, p.decay ? p.decay + gi : p.beta + gi, (t < it.nv && p.decay) ? 4u : 0u);
+        if (p.A_log && t < 2) {
+            const float *src = t == 0 ? p.A_log + it.h : (p.dt_bias ? p.dt_bias + it.h : p.A_log);
+            cp_async4(gate + t, src, (t == 0 || p.dt_bias) ? 4u : 0u);
+        }
     }
     cp_async_commit();
 }
@@ -547,6 +553,9 @@ __device__ __forceinline__ void release_slot(const TcParams &p, long slot) {
 // persists (measured: 0.962 -> 0.949 ms on a 32 x 32768-token prefill; a two-thirds offset
 // gained nothing).
 constexpr int kStaggerBar = 3;
+// Group g's warps 0-2 meet at named barrier g + kGateBarOffset (4, 5) when the decay comes
+// from a raw gate: warps 1 and 2 transform it, warp 0 then takes the prefix.
+constexpr int kGateBarOffset = 3;
 
 template <int D>
 __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUtensorMap *map_k,
@@ -594,13 +603,14 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     }
     load_rows<D>(p, sKQ, cur, tid, true);
     load_rows<D>(p, sKQ, cur, tid, false);
-    load_scalars(p, mbeta, mdec, cur, tid);
+    load_scalars(p, mbeta, mdec, ctl->gate, cur, tid);
     long pend = -1;     // store thread: slot whose stores are in flight and not yet published
     long staged = -1;   // store thread: slot whose state-column blocks wait in the staging area
 
     for (uint32_t it = 0;; ++it) {
         const uint32_t ph = it & 1;   // bar_mma completes three times per chunk
         const int nv = cur.nv;
+        const bool gated = p.A_log && p.decay;   // decay holds the raw gate
         cp_async_wait_all();   // this thread's share of q, k, beta, decay ...
         fence_proxy_async();   // ... visible to the tensor core behind the barrier
         named_sync(bar, kGroupThreads);
@@ -627,17 +637,15 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
                             ks > 0 ? 1u : 0u);
             mma_commit(&ctl->bar_mma);
         }
+        if (gated && (warp == 1 || warp == 2)) {   // the decay from the raw gate, a token per thread
+            const int t = tid - 32;                  // (zero past the valid tokens)
+            mdec[t] = t < nv ? gate_decay(mdec[t], ctl->gate[0], ctl->gate[1]) : 0.f;
+            named_arrive(bar + kGateBarOffset, 96);
+        }
         if (warp == 0) {   // in-chunk cumulative log-decay: lane owns tokens 2 lane, 2 lane + 1
-            float d0 = mdec[2 * lane], d1 = mdec[2 * lane + 1];
-            if (p.A_log && p.decay) {   // the decay from the raw gate (zero past the valid tokens)
-                const float al = p.A_log[cur.h], bi = p.dt_bias ? p.dt_bias[cur.h] : 0.f;
-                d0 = 2 * lane < nv ? gate_decay(d0, al, bi) : 0.f;
-                d1 = 2 * lane + 1 < nv ? gate_decay(d1, al, bi) : 0.f;
-            }
-            if (p.beta_sig) {
-                mbeta[2 * lane] = 2 * lane < nv ? beta_of(mbeta[2 * lane], 1, p.neg_eig) : 0.f;
-                mbeta[2 * lane + 1] = 2 * lane + 1 < nv ? beta_of(mbeta[2 * lane + 1], 1, p.neg_eig) : 0.f;
-            }
+            if (gated) named_sync(bar + kGateBarOffset, 96);
+            const float d0 = mdec[2 * lane], d1 = mdec[2 * lane + 1];
+
             float incl = d0 + d1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -649,6 +657,10 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             mG[2 * lane] = excl + d0;
             mGp[2 * lane + 1] = excl + d0;
             mG[2 * lane + 1] = incl;
+        }
+        if (warp == 3 && p.beta_sig) {   // beta from logits (zero past the valid tokens)
+            mbeta[2 * lane] = 2 * lane < nv ? beta_of(mbeta[2 * lane], 1, p.neg_eig) : 0.f;
+            mbeta[2 * lane + 1] = 2 * lane + 1 < nv ? beta_of(mbeta[2 * lane + 1], 1, p.neg_eig) : 0.f;
         }
         if (tid >= 128 && ok) {   // query norms: two threads per row, each summing half of its chunks
             const int t = (tid - 128) >> 1, part = tid & 1;
@@ -856,7 +868,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         if (ok && more) {
             load_rows<D>(p, sKQ, nx, tid, true);
             load_rows<D>(p, sKQ, nx, tid, false);
-            load_scalars(p, mbeta, mdec, nx, tid);
+            load_scalars(p, mbeta, mdec, ctl->gate, nx, tid);
         }
 
         // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
@@ -970,7 +982,8 @@ struct GkSmem {
     static constexpr int SD = OV + OV_BYTES;              // exact diagonal sub-blocks: fp32 [4][2][16][16]
     static constexpr int MISC = SD + 4 * 2 * 256 * 4;
     // MISC: beta [2][64] | kn [64] | qn [64] | exp(G_n) [D] | prefix totals [1024] | span flags [4]
-    static constexpr int CTRL = MISC + (2 * 64 + 64 + 64 + D + 1024 + 4) * 4;
+    //       | gate parameters: A_log, pad [3], dt_bias [D]
+    static constexpr int CTRL = MISC + (2 * 64 + 64 + 64 + D + 1024 + 4 + 4 + D) * 4;
     static constexpr int BYTES = ((CTRL + 64 + 1023) / 1024) * 1024;
 };
 
@@ -1038,6 +1051,16 @@ __device__ __forceinline__ void load_beta(const TcParams &p, float *mbeta, const
     }
     cp_async_commit();
 }
+// A_log and dt_bias [D] of the chunk's head for a raw-gate g (warps 1-3), ahead of the prefix
+template <int D>
+__device__ __forceinline__ void load_gate(const TcParams &p, float *gate, const ChunkItem &it, int tid) {
+    if (!p.A_log || tid < 32 || tid >= 128) return;
+    for (int c = tid - 32; c <= D; c += 96) {
+        if (c == D) cp_async4(gate, p.A_log + it.h, 4u);
+        else cp_async4(gate + 4 + c, p.dt_bias ? p.dt_bias + (size_t)it.h * D + c : p.A_log, p.dt_bias ? 4u : 0u);
+    }
+    cp_async_commit();
+}
 
 constexpr int kGkThreads = 512;   // the whole CTA: one prep group
 constexpr int kGkBarInv = 2;      // named barrier of the inverse (threads 0..255)
@@ -1081,6 +1104,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
     float *mbeta2 = reinterpret_cast<float *>(sm + Ly::MISC);
     float *mkn = mbeta2 + 128, *mqn = mkn + 64, *meGn = mqn + 64, *mtot = meGn + D;
     int *mspan = reinterpret_cast<int *>(mtot + 1024);
+    float *mgate = reinterpret_cast<float *>(mspan + 4);   // A_log, pad, dt_bias [D] at +4
 
     ChunkItem cur;
     while (item < p.n_items && !item_info(p, item, cur)) item += stride;
@@ -1090,6 +1114,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         load_rows<D>(p, sKQ, cur, tid, false);
         load_g<D>(p, gf, cur, tid);
         load_beta(p, mbeta2, cur, tid);
+        load_gate<D>(p, mgate, cur, tid);
     }
     long pend = -1;   // kStoreThread: slot whose E_c stores are issued and not yet published
     const bool decayed = p.decayed_read != 0;
@@ -1099,6 +1124,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         const int nv = cur.nv;
         float *mbeta = mbeta2 + 64 * (it & 1);
         if (tid < 4) mspan[tid] = 0;
+        const bool gate = p.A_log != nullptr;   // g holds the raw gate
         cp_async_wait_all();
         if (lane == 0) bulk_wait0();   // the previous chunk's E_c stores: complete, staging free
         named_sync(bar, NT);
@@ -1140,18 +1166,15 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
             // in log2 units
             const int c0 = 2 * (tid % NP), j = tid / NP;
             float2 acc = make_float2(0.f, 0.f);
-            const bool gate = p.A_log != nullptr;   // g holds the raw gate
-            const float al = gate ? p.A_log[cur.h] : 0.f;
-            const float2 bi = (gate && p.dt_bias)
-                                  ? make_float2(p.dt_bias[(size_t)cur.h * D + c0], p.dt_bias[(size_t)cur.h * D + c0 + 1])
-                                  : make_float2(0.f, 0.f);
+            const float gate_a = gate ? expf(mgate[0]) : 0.f;
+            const float2 gate_bi = gate ? *reinterpret_cast<const float2 *>(mgate + 4 + c0) : make_float2(0.f, 0.f);
 #pragma unroll
             for (int t = j * TPG; t < (j + 1) * TPG; ++t) {
                 float2 *x = reinterpret_cast<float2 *>(gf + t * D + c0);
                 float2 gv = *x;
-                if (gate) {
-                    gv.x = t < nv ? gate_decay(gv.x, al, bi.x) : 0.f;
-                    gv.y = t < nv ? gate_decay(gv.y, al, bi.y) : 0.f;
+                if (gate) {   // g holds the raw gate
+                    gv.x = t < nv ? gate_decay_a(gv.x, gate_a, gate_bi.x) : 0.f;
+                    gv.y = t < nv ? gate_decay_a(gv.y, gate_a, gate_bi.y) : 0.f;
                 }
                 acc.x = fmaf(gv.x, kLog2e, acc.x);
                 acc.y = fmaf(gv.y, kLog2e, acc.y);
@@ -1290,6 +1313,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
             load_rows<D>(p, sKQ, nx, tid, false);
             load_g<D>(p, gf, nx, tid);
             load_beta(p, mbeta_next, nx, tid);
+            load_gate<D>(p, mgate, nx, tid);
         }
 
         // ---- MMA1: sub-block b's Gram rows, transposed: D1[s][32 b + j] for s < 16 (b + 1):

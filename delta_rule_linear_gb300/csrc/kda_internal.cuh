@@ -108,14 +108,19 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 
 // kda_decay (ejkernel kernel_delta_attention): the log decay from a gate,
 // -exp(A_log) * softplus(gate + dt_bias), softplus(x) = log(1 + exp(x)).
-__device__ __forceinline__ float gate_decay(float gate, float a_log, float bias) {
+// softplus(x) = max(x, 0) + log1p(e^-|x|): no overflow, and the relative accuracy of
+// log1p where e^-|x| is small.
+__device__ __forceinline__ float gate_decay_a(float gate, float a, float bias) {   // a = exp(A_log)
     const float x = gate + bias;
-    return -expf(a_log) * (x > 20.f ? x : log1pf(expf(x)));
+    return -a * (fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x))));
+}
+__device__ __forceinline__ float gate_decay(float gate, float a_log, float bias) {
+    return gate_decay_a(gate, expf(a_log), bias);
 }
 // beta from logits (TileOPs GDNFwdOp / KDAFwdOp): sigmoid(x), or 2 sigmoid(x)
 __device__ __forceinline__ float beta_of(float x, int sig, int neg) {
     if (!sig) return x;
-    const float s = 1.f / (1.f + expf(-x));
+    const float s = __frcp_rn(1.f + __expf(-x));
     return neg ? 2.f * s : s;
 }
 
