@@ -615,10 +615,6 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         fence_proxy_async();   // ... visible to the tensor core behind the barrier
         named_sync(bar, kGroupThreads);
         bool ok = ctl->fail == 0;
-        long nitem = item + stride;   // this group's next chunk
-        ChunkItem nx;
-        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
-        const bool more = nitem < p.n_items;
         if (tid == kStoreThread && staged >= 0) {   // the previous chunk's state-column blocks of E_c
             for (int kb = 0; kb < NB; ++kb)
                 tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
@@ -684,6 +680,11 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         }
         named_sync(bar, kGroupThreads);   // the log-decay prefix is in place
         if (tid < 64) meg[tid] = __expf(mG[tid]);
+        // this group's next chunk (packed sequences read cu_seqlens here: off the path to MMA1)
+        long nitem = item + stride;
+        ChunkItem nx;
+        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
+        const bool more = nitem < p.n_items;
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
 
@@ -1129,10 +1130,6 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         if (lane == 0) bulk_wait0();   // the previous chunk's E_c stores: complete, staging free
         named_sync(bar, NT);
         bool ok = ctl->fail == 0;
-        long nitem = item + stride;
-        ChunkItem nx;
-        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
-        const bool more = nitem < p.n_items;
 
         // ---- norms of the k and q rows (zero past the valid tokens), four threads a row;
         // prefix over tokens of g
@@ -1305,16 +1302,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
             sd[(b * 2 + 0) * 256 + tj * 16 + sj] = al;
             sd[(b * 2 + 1) * 256 + tj * 16 + sj] = aq;
         }
-        // raw q, k and g are no longer read: the next chunk's loads start now
-        float *mbeta_next = mbeta2 + 64 * ((it + 1) & 1);
         if (mspan[0] | mspan[1] | mspan[2] | mspan[3]) named_sync(bar, NT);
-        if (ok && more && loader) {
-            load_rows<D>(p, sKQ, nx, tid, true);
-            load_rows<D>(p, sKQ, nx, tid, false);
-            load_g<D>(p, gf, nx, tid);
-            load_beta(p, mbeta_next, nx, tid);
-            load_gate<D>(p, mgate, nx, tid);
-        }
 
         // ---- MMA1: sub-block b's Gram rows, transposed: D1[s][32 b + j] for s < 16 (b + 1):
         // column operand rows s (M = 64), row operand k rows then q rows of sub-block b (N = 32)
@@ -1330,6 +1318,21 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
             }
             mma_commit(&ctl->bar_mma);
         }
+        // raw q, k and g are no longer read: the next chunk's loads start once MMA1 is issued
+        // (packed sequences read cu_seqlens to find it: off the path to MMA1)
+        long nitem = item + stride;
+        ChunkItem nx;
+        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
+        const bool more = nitem < p.n_items;
+        float *mbeta_next = mbeta2 + 64 * ((it + 1) & 1);
+        if (ok && more && loader) {
+            load_rows<D>(p, sKQ, nx, tid, true);
+            load_rows<D>(p, sKQ, nx, tid, false);
+            load_g<D>(p, gf, nx, tid);
+            load_beta(p, mbeta_next, nx, tid);
+            load_gate<D>(p, mgate, nx, tid);
+        }
+
         if (tid == kStoreThread && pend >= 0) {   // the previous chunk's E_c, while MMA1 runs
             release_slot(p, pend);
             pend = -1;
