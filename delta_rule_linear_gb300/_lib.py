@@ -35,22 +35,23 @@ class KdaOptions(ctypes.Structure):
     """struct kda_options of include/kda.h."""
     _fields_ = [("decayed_read", ctypes.c_int), ("A_log", ctypes.c_void_p),
                 ("dt_bias", ctypes.c_void_p), ("beta_sigmoid", ctypes.c_int),
-                ("allow_neg_eigval", ctypes.c_int)]
+                ("allow_neg_eigval", ctypes.c_int), ("v_heads_per_qk_head", ctypes.c_int)]
 
 
 def make_options(decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
-                 allow_neg_eigval=False):
-    """A KdaOptions pointer (or None when every option is off).  A_log [H] and dt_bias
-    ([H] for a per-head decay, [H, dk] for g) are fp32 CUDA tensors; the caller keeps them
+                 allow_neg_eigval=False, v_heads_per_qk_head=1):
+    """A KdaOptions pointer (or None when every option is off).  A_log [HV] and dt_bias
+    ([HV] for a per-head decay, [HV, dk] for g) are fp32 CUDA tensors; the caller keeps them
     alive for the call."""
-    if not (decayed_read or A_log is not None or dt_bias is not None or beta_sigmoid):
+    if not (decayed_read or A_log is not None or dt_bias is not None or beta_sigmoid or
+            v_heads_per_qk_head > 1):
         return None
     for t, name in ((A_log, "A_log"), (dt_bias, "dt_bias")):
         if t is not None and (not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
     o = KdaOptions(int(bool(decayed_read)), None if A_log is None else A_log.data_ptr(),
                    None if dt_bias is None else dt_bias.data_ptr(), int(bool(beta_sigmoid)),
-                   int(bool(allow_neg_eigval)))
+                   int(bool(allow_neg_eigval)), int(v_heads_per_qk_head))
     return ctypes.pointer(o)
 
 
@@ -133,6 +134,13 @@ def load(path: str | None = None):
         return lib
 
 
+def _value_heads(H, HV):
+    """Value heads per q/k head (TileOPs GDNFwdOp / KDAFwdOp: HV a multiple of H)."""
+    if HV < H or HV % H:
+        raise ValueError(f"the value heads ({HV}) must be a multiple of the q/k heads ({H})")
+    return HV // H
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -199,21 +207,22 @@ def chunk_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None, chun
     """
     lib = load()
     B, T, H, dk = q.shape
-    dv = v.shape[-1]
+    HV, dv = v.shape[2], v.shape[-1]
+    m = _value_heads(H, HV)
     dt = _dtype_code(q)
-    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, H, dv))
-    _check(beta, "beta", torch.float32, (B, T, H)); _check(decay, "decay", torch.float32, (B, T, H))
-    _check(initial_state, "initial_state", torch.float32, (B, H, dk, dv))
-    o = out if out is not None else torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
-    _check(o, "out", q.dtype, (B, T, H, dv))
-    hT = final_state if final_state is not None else torch.empty((B, H, dk, dv), dtype=torch.float32,
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, HV, dv))
+    _check(beta, "beta", torch.float32, (B, T, HV)); _check(decay, "decay", torch.float32, (B, T, HV))
+    _check(initial_state, "initial_state", torch.float32, (B, HV, dk, dv))
+    o = out if out is not None else torch.empty((B, T, HV, dv), dtype=q.dtype, device=q.device)
+    _check(o, "out", q.dtype, (B, T, HV, dv))
+    hT = final_state if final_state is not None else torch.empty((B, HV, dk, dv), dtype=torch.float32,
                                                                   device=q.device)
-    _check(hT, "final_state", torch.float32, (B, H, dk, dv))
-    need = lib.kda_chunk_fwd_workspace(B, T, H, dk, dv, chunk_size, dt)
+    _check(hT, "final_state", torch.float32, (B, HV, dk, dv))
+    need = lib.kda_chunk_fwd_workspace(B, T, HV, dk, dv, chunk_size, dt)
     if need == 0:
         raise KdaError(4, "kda_chunk_fwd_workspace", lib)
     ws = _workspace(need, q.device, workspace)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state), _ptr(o),
             _ptr(hT), B, T, H, dk, dv, dt, float(scale or 0.0), int(chunk_size),
             int(bool(use_qk_l2norm)))
@@ -264,15 +273,16 @@ def recurrent_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None,
     Returns (o, final_state)."""
     lib = load()
     B, T, H, dk = q.shape
-    dv = v.shape[-1]
+    HV, dv = v.shape[2], v.shape[-1]
+    m = _value_heads(H, HV)
     dt = _dtype_code(q)
-    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, H, dv))
-    _check(beta, "beta", torch.float32, (B, T, H)); _check(decay, "decay", torch.float32, (B, T, H))
-    _check(initial_state, "initial_state", torch.float32, (B, H, dk, dv))
-    o = out if out is not None else torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
-    hT = final_state if final_state is not None else torch.empty((B, H, dk, dv), dtype=torch.float32,
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, HV, dv))
+    _check(beta, "beta", torch.float32, (B, T, HV)); _check(decay, "decay", torch.float32, (B, T, HV))
+    _check(initial_state, "initial_state", torch.float32, (B, HV, dk, dv))
+    o = out if out is not None else torch.empty((B, T, HV, dv), dtype=q.dtype, device=q.device)
+    hT = final_state if final_state is not None else torch.empty((B, HV, dk, dv), dtype=torch.float32,
                                                                   device=q.device)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state), _ptr(o),
             _ptr(hT), B, T, H, dk, dv, dt, float(scale or 0.0), int(bool(use_qk_l2norm)))
     if opts is None:
@@ -286,21 +296,23 @@ def decode_step(q, k, v, beta, decay, state, *, scale=None, use_qk_l2norm=True, 
                 stream=None,
                 decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
                 allow_neg_eigval=False):
-    """kda_decode_step: one token per sequence; ``state`` [B,H,dk,dv] fp32 is updated in place.
+    """kda_decode_step: one token per sequence; ``state`` [B,HV,dk,dv] fp32 is updated in place.
 
-    q, k: [B,1,H,dk] (or [B,H,dk]); v: [B,1,H,dv]; beta, decay: [B,1,H] (decay may be None).
-    Returns o with v's shape.
+    q, k: [B,1,H,dk] (or [B,H,dk]); v: [B,1,HV,dv]; beta, decay: [B,1,HV] (decay may be None);
+    HV = H without grouped value heads.  Returns o with v's shape.
     """
     lib = load()
-    B, H, dk, dv = state.shape
+    B, HV, dk, dv = state.shape
+    H = q.numel() // max(B * dk, 1)
+    m = _value_heads(H, HV)
     dt = _dtype_code(q)
     _check(q, "q"); _check(k, "k", q.dtype); _check(v, "v", q.dtype)
     _check(beta, "beta", torch.float32); _check(decay, "decay", torch.float32)
     _check(state, "state", torch.float32)
-    if q.numel() != B * H * dk or v.numel() != B * H * dv or beta.numel() != B * H:
-        raise ValueError("decode inputs do not match the state's [B,H,dk,dv]")
+    if q.numel() != B * H * dk or v.numel() != B * HV * dv or beta.numel() != B * HV:
+        raise ValueError("decode inputs do not match the state's [B,HV,dk,dv]")
     o = out if out is not None else torch.empty_like(v)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(state), _ptr(o), B, H, dk,
             dv, dt, float(scale or 0.0), int(bool(use_qk_l2norm)))
     if opts is None:
@@ -321,27 +333,28 @@ def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_
     """
     lib = load()
     _, total, H, dk = q.shape
-    dv = v.shape[-1]
+    HV, dv = v.shape[2], v.shape[-1]
+    m = _value_heads(H, HV)
     N = cu_seqlens.numel() - 1
     dt = _dtype_code(q)
-    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (1, total, H, dv))
-    _check(beta, "beta", torch.float32, (1, total, H))
-    _check(decay, "decay", torch.float32, (1, total, H))
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (1, total, HV, dv))
+    _check(beta, "beta", torch.float32, (1, total, HV))
+    _check(decay, "decay", torch.float32, (1, total, HV))
     _check(cu_seqlens, "cu_seqlens", torch.int32)
-    _check(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
+    _check(initial_state, "initial_state", torch.float32, (N, HV, dk, dv))
     host = None
     if cu_seqlens_cpu is not None:
         host = cu_seqlens_cpu.to(torch.int32).contiguous()
         if host.is_cuda:
             raise ValueError("cu_seqlens_cpu must be a host tensor")
-    o = out if out is not None else torch.empty((1, total, H, dv), dtype=q.dtype, device=q.device)
-    hT = final_state if final_state is not None else torch.empty((N, H, dk, dv), dtype=torch.float32,
+    o = out if out is not None else torch.empty((1, total, HV, dv), dtype=q.dtype, device=q.device)
+    hT = final_state if final_state is not None else torch.empty((N, HV, dk, dv), dtype=torch.float32,
                                                                   device=q.device)
-    need = lib.kda_varlen_fwd_workspace(N, total, H, dk, dv, chunk_size, dt)
+    need = lib.kda_varlen_fwd_workspace(N, total, HV, dk, dv, chunk_size, dt)
     if need == 0:
         raise KdaError(4, "kda_varlen_fwd_workspace", lib)
     ws = _workspace(need, q.device, workspace)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(cu_seqlens), _ptr(host), N,
             total, H, dk, dv, _ptr(initial_state), _ptr(o), _ptr(hT), dt, float(scale or 0.0),
             int(chunk_size), int(bool(use_qk_l2norm)))
@@ -364,21 +377,22 @@ def gk_chunk_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None, 
     channel (g with q's shape, fp32).  Packed when ``cu_seqlens`` is given (as
     gk_recurrent_fwd).  check_device as in chunk_fwd.  Returns (o, final_state)."""
     lib = load()
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
     Bq, T, H, dk = q.shape
-    dv = v.shape[-1]
+    HV, dv = v.shape[2], v.shape[-1]
+    m = _value_heads(H, HV)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
     dt = _dtype_code(q)
     N = Bq if cu_seqlens is None else cu_seqlens.numel() - 1
-    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (Bq, T, H, dv))
-    _check(beta, "beta", torch.float32, (Bq, T, H)); _check(g, "g", torch.float32, q.shape)
-    _check(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
-    o = out if out is not None else torch.empty((Bq, T, H, dv), dtype=q.dtype, device=q.device)
-    _check(o, "out", q.dtype, (Bq, T, H, dv))
-    hT = final_state if final_state is not None else torch.empty((N, H, dk, dv), dtype=torch.float32,
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (Bq, T, HV, dv))
+    _check(beta, "beta", torch.float32, (Bq, T, HV)); _check(g, "g", torch.float32, (Bq, T, HV, dk))
+    _check(initial_state, "initial_state", torch.float32, (N, HV, dk, dv))
+    o = out if out is not None else torch.empty((Bq, T, HV, dv), dtype=q.dtype, device=q.device)
+    _check(o, "out", q.dtype, (Bq, T, HV, dv))
+    hT = final_state if final_state is not None else torch.empty((N, HV, dk, dv), dtype=torch.float32,
                                                                   device=q.device)
-    _check(hT, "final_state", torch.float32, (N, H, dk, dv))
+    _check(hT, "final_state", torch.float32, (N, HV, dk, dv))
     if cu_seqlens is None:
-        need = lib.kda_chunk_fwd_workspace(Bq, T, H, dk, dv, chunk_size, dt)
+        need = lib.kda_chunk_fwd_workspace(Bq, T, HV, dk, dv, chunk_size, dt)
         if need == 0:
             raise KdaError(4, "kda_chunk_fwd_workspace", lib)
         ws = _workspace(need, q.device, workspace)
@@ -396,7 +410,7 @@ def gk_chunk_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None, 
             host = cu_seqlens_cpu.to(torch.int32).contiguous()
             if host.is_cuda:
                 raise ValueError("cu_seqlens_cpu must be a host tensor")
-        need = lib.kda_varlen_fwd_workspace(N, T, H, dk, dv, chunk_size, dt)
+        need = lib.kda_varlen_fwd_workspace(N, T, HV, dk, dv, chunk_size, dt)
         if need == 0:
             raise KdaError(4, "kda_varlen_fwd_workspace", lib)
         ws = _workspace(need, q.device, workspace)
@@ -422,19 +436,20 @@ def gk_recurrent_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=No
     arrays are packed [1,total,H,.] and the states are [N,H,dk,dv].  Returns (o, final_state).
     """
     lib = load()
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
     Bq, T, H, dk = q.shape
-    dv = v.shape[-1]
+    HV, dv = v.shape[2], v.shape[-1]
+    m = _value_heads(H, HV)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
     dt = _dtype_code(q)
     N = Bq if cu_seqlens is None else cu_seqlens.numel() - 1
-    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (Bq, T, H, dv))
-    _check(beta, "beta", torch.float32, (Bq, T, H)); _check(g, "g", torch.float32, q.shape)
-    _check(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
-    o = out if out is not None else torch.empty((Bq, T, H, dv), dtype=q.dtype, device=q.device)
-    _check(o, "out", q.dtype, (Bq, T, H, dv))
-    hT = final_state if final_state is not None else torch.empty((N, H, dk, dv), dtype=torch.float32,
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (Bq, T, HV, dv))
+    _check(beta, "beta", torch.float32, (Bq, T, HV)); _check(g, "g", torch.float32, (Bq, T, HV, dk))
+    _check(initial_state, "initial_state", torch.float32, (N, HV, dk, dv))
+    o = out if out is not None else torch.empty((Bq, T, HV, dv), dtype=q.dtype, device=q.device)
+    _check(o, "out", q.dtype, (Bq, T, HV, dv))
+    hT = final_state if final_state is not None else torch.empty((N, HV, dk, dv), dtype=torch.float32,
                                                                   device=q.device)
-    _check(hT, "final_state", torch.float32, (N, H, dk, dv))
+    _check(hT, "final_state", torch.float32, (N, HV, dk, dv))
     if cu_seqlens is None:
         rc = lib.kda_gk_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
                                       _ptr(initial_state), _ptr(o), _ptr(hT), Bq, T, H, dk, dv, dt,
@@ -466,15 +481,17 @@ def gk_decode_step(q, k, v, beta, g, state, *, scale=None, use_qk_l2norm=True, o
     """kda_gk_decode_step: one token per sequence with per-channel decay g [B,1,H,dk] fp32
     (or None); ``state`` [B,H,dk,dv] fp32 is updated in place.  Returns o with v's shape."""
     lib = load()
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
-    B, H, dk, dv = state.shape
+    B, HV, dk, dv = state.shape
+    H = q.numel() // max(B * dk, 1)
+    m = _value_heads(H, HV)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
     dt = _dtype_code(q)
     _check(q, "q"); _check(k, "k", q.dtype); _check(v, "v", q.dtype)
     _check(beta, "beta", torch.float32); _check(g, "g", torch.float32)
     _check(state, "state", torch.float32)
-    if q.numel() != B * H * dk or v.numel() != B * H * dv or beta.numel() != B * H or (
-            g is not None and g.numel() != B * H * dk):
-        raise ValueError("decode inputs do not match the state's [B,H,dk,dv]")
+    if q.numel() != B * H * dk or v.numel() != B * HV * dv or beta.numel() != B * HV or (
+            g is not None and g.numel() != B * HV * dk):
+        raise ValueError("decode inputs do not match the state's [B,HV,dk,dv]")
     o = out if out is not None else torch.empty_like(v)
     rc = lib.kda_gk_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(state),
                                 _ptr(o), B, H, dk, dv, dt, float(scale or 0.0),

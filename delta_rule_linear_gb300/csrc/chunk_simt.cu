@@ -92,7 +92,8 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(SeqBatch p) {
         for (int t = warp; t < C; t += kThreads / 32) {
             float kv[EPL], qv[EPL];
             float sk = 0.f, sq = 0.f;
-            const size_t off = ((size_t)(start + c0 + t) * H + h) * DK;
+            const int G = p.G > 1 ? p.G : 1;   // q/k head h / G of value head h
+            const size_t off = ((size_t)(start + c0 + t) * (H / G) + h / G) * DK;
 #pragma unroll
             for (int e = 0; e < EPL; ++e) {
                 kv[e] = t < nrow ? to_f32(k[off + lane + 32 * e]) : 0.f;

@@ -68,6 +68,7 @@ struct TcParams {
     const float *A_log;        // [H] or nullptr: decay / gk hold the raw gate (gate_decay)
     const float *dt_bias;      // [H] (scalar decay) or [H, D] (per channel) or nullptr
     int beta_sig, neg_eig;     // beta holds logits: sigmoid, or 2 sigmoid
+    int G;                     // value heads per q/k head: H counts value heads, q/k have H / G
     const float *h0;           // [nseq, H, D, D] or nullptr
     float *hT;                 // [nseq, H, D, D] or nullptr
     const __nv_bfloat16 *q, *k;   // [rows, H, D]
@@ -516,7 +517,7 @@ __device__ __forceinline__ void load_rows(const TcParams &p, uint8_t *sKQ, const
         const int row = pidx / PPR, pc = pidx % PPR;
         const long grow = it.row0 + row;
         const bool in = grow < p.rows;
-        const __nv_bfloat16 *src = g + ((in ? grow : 0) * p.H + it.h) * D + 8 * pc;
+        const __nv_bfloat16 *src = g + ((in ? grow : 0) * (p.H / p.G) + it.h / p.G) * D + 8 * pc;
         uint8_t *dst = sKQ + (pc >> 3) * 16384 + (q ? 8192 : 0) + row * 128 + (((pc & 7) ^ (row & 7)) << 4);
         cp_async16(dst, src, in ? 16u : 0u);
     }
@@ -1949,6 +1950,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.gk = GK ? a.gk : nullptr;
     p.decayed_read = a.decayed_read;
     p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_sig = a.beta_sig; p.neg_eig = a.neg_eig;
+    p.G = a.G > 1 ? a.G : 1;
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.k = static_cast<const __nv_bfloat16 *>(a.k);
     p.rows = total_rows;
@@ -1963,7 +1965,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.maxnc = (a.T + kC - 1) / kC;   // varlen: a.T bounds the longest sequence
 
     CUtensorMap mq, mk, mv, me, mew;
-    if (!map_tokens(&mq, a.q, total_rows, a.H, D) || !map_tokens(&mk, a.k, total_rows, a.H, D) ||
+    if (!map_tokens(&mq, a.q, total_rows, a.H / p.G, D) || !map_tokens(&mk, a.k, total_rows, a.H / p.G, D) ||
         !map_tokens(&mv, a.v, total_rows, a.H, D) || !map_E(&me, p.E, slots_bound, R) ||
         !map_E_tiles(&mew, p.E, slots_bound, R))
         return cudaErrorInvalidValue;

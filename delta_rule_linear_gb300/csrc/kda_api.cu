@@ -43,6 +43,12 @@ kda_status check_common(const void *q, const void *k, const void *v, const float
 
 kda_status launch_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+// heads of v, o, beta, the decay and the state: H (q/k heads) times the value-head group
+int value_heads(int H, const kda_options *opt) {
+    const long m = (opt && opt->v_heads_per_qk_head > 1) ? opt->v_heads_per_qk_head : 1;
+    return (long)H * m > 0x7fffffffL ? H : (int)((long)H * m);
+}
+
 // kda_options -> the batch fields; `gate` is the decay (or g) pointer the gate would replace
 kda_status apply_options(const kda_options *opt, const float *gate, SeqBatch &a) {
     if (!opt) return KDA_OK;
@@ -54,6 +60,12 @@ kda_status apply_options(const kda_options *opt, const float *gate, SeqBatch &a)
     a.dt_bias = opt->dt_bias;
     a.beta_sig = opt->beta_sigmoid ? 1 : 0;
     a.neg_eig = (opt->beta_sigmoid && opt->allow_neg_eigval) ? 1 : 0;
+    if (opt->v_heads_per_qk_head < 0) return KDA_ERR_SHAPE;
+    if (opt->v_heads_per_qk_head > 1) {   // a.H (q/k heads on entry) becomes the value-head count
+        if ((long)a.H * opt->v_heads_per_qk_head > 0x7fffffffL) return KDA_ERR_SHAPE;
+        a.G = opt->v_heads_per_qk_head;
+        a.H *= a.G;
+    }
     return KDA_OK;
 }
 
@@ -160,7 +172,7 @@ kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v, const f
                                 (long)B * T, H, dk, dv, dtype);
     if (c != KDA_OK) return c;
     if (!supported_chunk(chunk_size)) return KDA_ERR_UNSUPPORTED;
-    const size_t need = kda_chunk_fwd_workspace(B, T, H, dk, dv, chunk_size, dtype);
+    const size_t need = kda_chunk_fwd_workspace(B, T, value_heads(H, opt), dk, dv, chunk_size, dtype);
     if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned16(ws)) return KDA_ERR_ALIGN;
     SeqBatch a{};
@@ -215,11 +227,13 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
 }
 
 // the decode arguments' option fields, by way of a batch
+// (d.H: the q/k heads on entry, the value heads on return)
 static kda_status decode_options(const kda_options *opt, const float *gate, DecodeArgs &d) {
     SeqBatch a{};
+    a.H = d.H;
     const kda_status c = apply_options(opt, gate, a);
     d.decayed_read = a.decayed_read; d.A_log = a.A_log; d.dt_bias = a.dt_bias;
-    d.beta_sig = a.beta_sig; d.neg_eig = a.neg_eig;
+    d.beta_sig = a.beta_sig; d.neg_eig = a.neg_eig; d.G = a.G; d.H = a.H;
     return c;
 }
 
@@ -232,10 +246,11 @@ kda_status kda_decode_step_ex(const void *q, const void *k, const void *v, const
     if (c != KDA_OK) return c;
     if (B > 0 && !state) return KDA_ERR_NULL;
     DecodeArgs a{};
+    a.H = H;
     if ((c = decode_options(opt, decay, a)) != KDA_OK) return c;
     if (B == 0) return KDA_OK;
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = decay; a.state = state; a.o = o;
-    a.B = B; a.H = H; a.dk = dk; a.dv = dv;
+    a.B = B; a.dk = dk; a.dv = dv;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
     return launch_status(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -275,7 +290,7 @@ kda_status kda_varlen_fwd_ex(const void *q, const void *k, const void *v, const 
             if (L > max_len) max_len = L;
         }
     }
-    const size_t need = kda_varlen_fwd_workspace(N, total_T, H, dk, dv, chunk_size, dtype);
+    const size_t need = kda_varlen_fwd_workspace(N, total_T, value_heads(H, opt), dk, dv, chunk_size, dtype);
     if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned16(ws)) return KDA_ERR_ALIGN;
     if (N == 0) return KDA_OK;
@@ -307,17 +322,17 @@ kda_status kda_gk_chunk_fwd(const void *q, const void *k, const void *v, const f
     if (c != KDA_OK) return c;
     if (!aligned16(g)) return KDA_ERR_ALIGN;
     if (!supported_chunk(chunk_size)) return KDA_ERR_UNSUPPORTED;
-    const size_t need = kda_chunk_fwd_workspace(B, T, H, dk, dv, chunk_size, dtype);
+    const size_t need = kda_chunk_fwd_workspace(B, T, value_heads(H, opt), dk, dv, chunk_size, dtype);
     if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned16(ws)) return KDA_ERR_ALIGN;
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
     a.gk = g; a.per_channel = 1;
-    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.o = o; a.hT = final_state; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
     a.dk = dk; a.dv = dv; a.chunk = chunk_size;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.ws = static_cast<WsHeader *>(ws);
     a.ws_body = static_cast<char *>(ws) + kWsHeader;
     a.ws_body_bytes = ws_bytes - kWsHeader;
@@ -350,18 +365,18 @@ kda_status kda_gk_varlen_fwd(const void *q, const void *k, const void *v, const 
             if (L > max_len) max_len = L;
         }
     }
-    const size_t need = kda_varlen_fwd_workspace(N, total_T, H, dk, dv, chunk_size, dtype);
+    const size_t need = kda_varlen_fwd_workspace(N, total_T, value_heads(H, opt), dk, dv, chunk_size, dtype);
     if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned16(ws)) return KDA_ERR_ALIGN;
     if (N == 0) return KDA_OK;
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
     a.gk = g; a.per_channel = 1;
-    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.o = o; a.hT = final_state; a.cu_seqlens = cu_seqlens; a.nseq = N; a.T = max_len; a.H = H;
     a.dk = dk; a.dv = dv; a.chunk = chunk_size;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.ws = static_cast<WsHeader *>(ws);
     a.ws_body = static_cast<char *>(ws) + kWsHeader;
     a.ws_body_bytes = ws_bytes - kWsHeader;
@@ -383,11 +398,11 @@ kda_status kda_gk_recurrent_fwd(const void *q, const void *k, const void *v, con
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
     a.gk = g; a.per_channel = 1;
-    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.o = o; a.hT = final_state; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
     a.dk = dk; a.dv = dv; a.chunk = 0;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     return run_prefill(a, false, (long)B * T, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -414,11 +429,11 @@ kda_status kda_gk_varlen_recurrent_fwd(const void *q, const void *k, const void 
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
     a.gk = g; a.per_channel = 1;
-    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.o = o; a.hT = final_state; a.cu_seqlens = cu_seqlens; a.nseq = N; a.T = total_T; a.H = H;
     a.dk = dk; a.dv = dv; a.chunk = 0;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     // every sequence scans its own cu_seqlens range; one of length 0 stores its
     // initial state (or zeros)
     return launch_status(launch_recurrent(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -434,11 +449,12 @@ kda_status kda_gk_decode_step(const void *q, const void *k, const void *v, const
     if (!aligned16(g)) return KDA_ERR_ALIGN;
     if (B > 0 && !state) return KDA_ERR_NULL;
     DecodeArgs a{};
+    a.H = H;
     if ((c = decode_options(opt, g, a)) != KDA_OK) return c;
     if (B == 0) return KDA_OK;
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.state = state; a.o = o;
     a.gk = g; a.per_channel = 1;
-    a.B = B; a.H = H; a.dk = dk; a.dv = dv;
+    a.B = B; a.dk = dk; a.dv = dv;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
     return launch_status(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));

@@ -41,6 +41,7 @@ struct SeqBatch {
     const float *A_log;       // [H] or nullptr: decay / gk hold the raw gate (gate_decay below)
     const float *dt_bias;     // [H] (scalar) or [H, dk] (per channel) or nullptr
     int beta_sig, neg_eig;    // beta holds logits: sigmoid, or 2 sigmoid with neg_eig
+    int G;                    // value heads per q/k head (H counts value heads; q/k have H / G)
     const float *h0;          // [nseq, H, dk, dv] or nullptr (zeros)
     void *o;                  // [rows, H, dv]   (Tin)
     float *hT;                // [nseq, H, dk, dv] or nullptr
@@ -64,6 +65,7 @@ struct DecodeArgs {
     int per_channel, decayed_read;
     const float *A_log, *dt_bias;   // as in SeqBatch
     int beta_sig, neg_eig;
+    int G;                          // value heads per q/k head (H counts value heads)
     float *state;
     void *o;
     int B, H, dk, dv;

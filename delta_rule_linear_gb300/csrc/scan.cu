@@ -42,6 +42,7 @@ struct ScanParams {
     int decayed_read;  // the delta term reads the decayed state (D S, or alpha S)
     const float *A_log, *dt_bias;   // raw gate -> decay (gate_decay); dt_bias [H] or [H, DK]
     int beta_sig, neg_eig;
+    int G;             // value heads per q/k head: H counts value heads, q/k have H / G
 };
 
 template <typename Tin, int DK, int DVS, bool GK>
@@ -90,12 +91,13 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
 
     for (int t = 0; t < len; ++t) {
         const long row = start + t;
-        const size_t qk_off = ((size_t)row * p.H + h) * DK;
+        const size_t qk_off = ((size_t)row * (p.H / p.G) + h / p.G) * DK;   // q/k head of value head h
+        const size_t g_off = ((size_t)row * p.H + h) * DK;
         const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
         if (tid < DK) {
             s_k[tid] = to_f32(k[qk_off + tid]);
             if constexpr (GK) {
-                float gv = p.gk ? p.gk[qk_off + tid] : 0.f;
+                float gv = p.gk ? p.gk[g_off + tid] : 0.f;
                 if (p.gk && p.A_log)
                     gv = gate_decay(gv, p.A_log[h], p.dt_bias ? p.dt_bias[(size_t)h * DK + tid] : 0.f);
                 s_a[tid] = expf(gv);
@@ -224,6 +226,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     p.nseq = a.B; p.T = 1; p.H = a.H; p.DV = a.dv; p.scale = a.scale; p.use_l2 = a.use_l2;
     p.gk = a.gk; p.decayed_read = a.decayed_read;
     p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_sig = a.beta_sig; p.neg_eig = a.neg_eig;
+    p.G = a.G > 1 ? a.G : 1;
     // one CTA per head, whole value width
     return launch_scan(p, a.dtype, a.dk, a.dv, a.per_channel != 0, s);
 }
@@ -235,6 +238,7 @@ cudaError_t launch_recurrent(const SeqBatch &a, cudaStream_t s) {
     p.nseq = a.nseq; p.T = a.T; p.H = a.H; p.DV = a.dv; p.scale = a.scale; p.use_l2 = a.use_l2;
     p.gk = a.gk; p.decayed_read = a.decayed_read;
     p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_sig = a.beta_sig; p.neg_eig = a.neg_eig;
+    p.G = a.G > 1 ? a.G : 1;
     // 32-column slabs: a long prefill is latency-bound per token, so spread the
     // independent value columns over more CTAs.
     return launch_scan(p, a.dtype, a.dk, 32, a.per_channel != 0, s);

@@ -89,6 +89,11 @@ typedef struct kda_options {
     const float *dt_bias;   /* [H] for a per-head decay, [H, dk] for g; device; NULL = zeros     */
     int beta_sigmoid;       /* nonzero: beta holds logits and the kernels use sigmoid(beta) ...  */
     int allow_neg_eigval;   /* ... or 2 sigmoid(beta) when this is nonzero as well               */
+    int v_heads_per_qk_head;/* m >= 2: grouped value heads (GDNFwdOp / KDAFwdOp: v, beta, g and
+                               the output use HV = m * H heads).  The H argument counts the q/k
+                               heads; v, o, beta, decay, g, A_log, dt_bias and the state have
+                               HV heads, and value head hv reads q/k head hv / m.  0 or 1: none.
+                               Workspace queries take the value-head count HV.                 */
 } kda_options;
 
 /* Human-readable name of a status code (static storage, never NULL). */

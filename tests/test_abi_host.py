@@ -250,3 +250,20 @@ def test_gate_decay_argument_errors(lib):
     assert lib.kda_gate_decay(_fake(), None, None, _fake(), 10, 2, 1, None) == 1
     assert lib.kda_gate_decay(_fake(0x1002), _fake(), None, _fake(), 10, 2, 1, None) == 5
     assert lib.kda_gate_decay(_fake(), _fake(), None, _fake(), 0, 2, 1, None) == 0
+
+
+def test_grouped_heads_option_checked(lib):
+    """v_heads_per_qk_head < 0 is a shape error; the workspace check uses the value heads."""
+    import ctypes as ct
+    from delta_rule_linear_gb300 import _lib
+
+    def chunk(m, ws_bytes):
+        o = _lib.KdaOptions(0, None, None, 0, 0, m)
+        return lib.kda_chunk_fwd_ex(_fake(), _fake(), _fake(), _fake(), None, None, _fake(), None,
+                                    1, 640, 2, 128, 128, 1, 0.0, 64, 1, ct.pointer(o), _fake(),
+                                    ws_bytes, None)
+    assert chunk(-2, 1 << 30) == 2
+    need2 = lib.kda_chunk_fwd_workspace(1, 640, 2, 128, 128, 64, 1)
+    need6 = lib.kda_chunk_fwd_workspace(1, 640, 6, 128, 128, 64, 1)
+    assert need6 > need2
+    assert chunk(3, need2) == 6          # three value heads per q/k head need the HV-sized workspace
