@@ -35,23 +35,24 @@ class KdaOptions(ctypes.Structure):
     """struct kda_options of include/kda.h."""
     _fields_ = [("decayed_read", ctypes.c_int), ("A_log", ctypes.c_void_p),
                 ("dt_bias", ctypes.c_void_p), ("beta_sigmoid", ctypes.c_int),
-                ("allow_neg_eigval", ctypes.c_int), ("v_heads_per_qk_head", ctypes.c_int)]
+                ("allow_neg_eigval", ctypes.c_int), ("v_heads_per_qk_head", ctypes.c_int),
+                ("state_v_first", ctypes.c_int)]
 
 
 def make_options(decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
-                 allow_neg_eigval=False, v_heads_per_qk_head=1):
+                 allow_neg_eigval=False, v_heads_per_qk_head=1, state_v_first=False):
     """A KdaOptions pointer (or None when every option is off).  A_log [HV] and dt_bias
     ([HV] for a per-head decay, [HV, dk] for g) are fp32 CUDA tensors; the caller keeps them
     alive for the call."""
     if not (decayed_read or A_log is not None or dt_bias is not None or beta_sigmoid or
-            v_heads_per_qk_head > 1):
+            v_heads_per_qk_head > 1 or state_v_first):
         return None
     for t, name in ((A_log, "A_log"), (dt_bias, "dt_bias")):
         if t is not None and (not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
     o = KdaOptions(int(bool(decayed_read)), None if A_log is None else A_log.data_ptr(),
                    None if dt_bias is None else dt_bias.data_ptr(), int(bool(beta_sigmoid)),
-                   int(bool(allow_neg_eigval)), int(v_heads_per_qk_head))
+                   int(bool(allow_neg_eigval)), int(v_heads_per_qk_head), int(bool(state_v_first)))
     return ctypes.pointer(o)
 
 
@@ -141,6 +142,11 @@ def _value_heads(H, HV):
     return HV // H
 
 
+def _st(n, hv, dk, dv, v_first):
+    """Shape of a state array: key-major [n, hv, dk, dv] or value-major [n, hv, dv, dk]."""
+    return (n, hv, dv, dk) if v_first else (n, hv, dk, dv)
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -196,7 +202,7 @@ def chunk_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None, chun
               use_qk_l2norm=True, out=None, final_state=None, workspace=None, stream=None,
               check_device=False,
               decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
-              allow_neg_eigval=False):
+              allow_neg_eigval=False, state_v_first=False):
     """kda_chunk_fwd (kda_chunk_fwd_ex when an option is set): chunked prefill.  Returns
     (o [B,T,H,dv], final_state [B,H,dk,dv] fp32).
 
@@ -212,17 +218,17 @@ def chunk_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None, chun
     dt = _dtype_code(q)
     _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, HV, dv))
     _check(beta, "beta", torch.float32, (B, T, HV)); _check(decay, "decay", torch.float32, (B, T, HV))
-    _check(initial_state, "initial_state", torch.float32, (B, HV, dk, dv))
+    _check(initial_state, "initial_state", torch.float32, _st(B, HV, dk, dv, state_v_first))
     o = out if out is not None else torch.empty((B, T, HV, dv), dtype=q.dtype, device=q.device)
     _check(o, "out", q.dtype, (B, T, HV, dv))
-    hT = final_state if final_state is not None else torch.empty((B, HV, dk, dv), dtype=torch.float32,
-                                                                  device=q.device)
-    _check(hT, "final_state", torch.float32, (B, HV, dk, dv))
+    hT = final_state if final_state is not None else torch.empty(_st(B, HV, dk, dv, state_v_first),
+                                                                 dtype=torch.float32, device=q.device)
+    _check(hT, "final_state", torch.float32, _st(B, HV, dk, dv, state_v_first))
     need = lib.kda_chunk_fwd_workspace(B, T, HV, dk, dv, chunk_size, dt)
     if need == 0:
         raise KdaError(4, "kda_chunk_fwd_workspace", lib)
     ws = _workspace(need, q.device, workspace)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m, state_v_first)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state), _ptr(o),
             _ptr(hT), B, T, H, dk, dv, dt, float(scale or 0.0), int(chunk_size),
             int(bool(use_qk_l2norm)))
@@ -268,7 +274,7 @@ def chunk_fwd_noalloc(q, k, v, beta, decay=None, initial_state=None, *, scale=No
 def recurrent_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None,
                   use_qk_l2norm=True, out=None, final_state=None, stream=None,
                   decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
-                  allow_neg_eigval=False):
+                  allow_neg_eigval=False, state_v_first=False):
     """kda_recurrent_fwd (_ex with options, as chunk_fwd): token-by-token prefill.
     Returns (o, final_state)."""
     lib = load()
@@ -278,11 +284,11 @@ def recurrent_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None,
     dt = _dtype_code(q)
     _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, HV, dv))
     _check(beta, "beta", torch.float32, (B, T, HV)); _check(decay, "decay", torch.float32, (B, T, HV))
-    _check(initial_state, "initial_state", torch.float32, (B, HV, dk, dv))
+    _check(initial_state, "initial_state", torch.float32, _st(B, HV, dk, dv, state_v_first))
     o = out if out is not None else torch.empty((B, T, HV, dv), dtype=q.dtype, device=q.device)
-    hT = final_state if final_state is not None else torch.empty((B, HV, dk, dv), dtype=torch.float32,
-                                                                  device=q.device)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
+    hT = final_state if final_state is not None else torch.empty(_st(B, HV, dk, dv, state_v_first),
+                                                                 dtype=torch.float32, device=q.device)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m, state_v_first)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state), _ptr(o),
             _ptr(hT), B, T, H, dk, dv, dt, float(scale or 0.0), int(bool(use_qk_l2norm)))
     if opts is None:
@@ -295,14 +301,15 @@ def recurrent_fwd(q, k, v, beta, decay=None, initial_state=None, *, scale=None,
 def decode_step(q, k, v, beta, decay, state, *, scale=None, use_qk_l2norm=True, out=None,
                 stream=None,
                 decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
-                allow_neg_eigval=False):
+                allow_neg_eigval=False, state_v_first=False):
     """kda_decode_step: one token per sequence; ``state`` [B,HV,dk,dv] fp32 is updated in place.
 
     q, k: [B,1,H,dk] (or [B,H,dk]); v: [B,1,HV,dv]; beta, decay: [B,1,HV] (decay may be None);
     HV = H without grouped value heads.  Returns o with v's shape.
     """
     lib = load()
-    B, HV, dk, dv = state.shape
+    B, HV, s2, s3 = state.shape
+    dk, dv = (s3, s2) if state_v_first else (s2, s3)
     H = q.numel() // max(B * dk, 1)
     m = _value_heads(H, HV)
     dt = _dtype_code(q)
@@ -312,7 +319,7 @@ def decode_step(q, k, v, beta, decay, state, *, scale=None, use_qk_l2norm=True, 
     if q.numel() != B * H * dk or v.numel() != B * HV * dv or beta.numel() != B * HV:
         raise ValueError("decode inputs do not match the state's [B,HV,dk,dv]")
     o = out if out is not None else torch.empty_like(v)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m, state_v_first)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(state), _ptr(o), B, H, dk,
             dv, dt, float(scale or 0.0), int(bool(use_qk_l2norm)))
     if opts is None:
@@ -326,7 +333,7 @@ def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_
                scale=None, chunk_size=64, use_qk_l2norm=True, out=None, final_state=None,
                workspace=None, stream=None, check_device=False,
                decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
-               allow_neg_eigval=False):
+               allow_neg_eigval=False, state_v_first=False):
     """kda_varlen_fwd: packed sequences [1,total,H,D] split by cu_seqlens [N+1] (int32, device).
 
     Returns (o [1,total,H,dv], final_state [N,H,dk,dv] fp32).  check_device as in chunk_fwd.
@@ -341,20 +348,20 @@ def varlen_fwd(q, k, v, beta, cu_seqlens, decay=None, initial_state=None, *, cu_
     _check(beta, "beta", torch.float32, (1, total, HV))
     _check(decay, "decay", torch.float32, (1, total, HV))
     _check(cu_seqlens, "cu_seqlens", torch.int32)
-    _check(initial_state, "initial_state", torch.float32, (N, HV, dk, dv))
+    _check(initial_state, "initial_state", torch.float32, _st(N, HV, dk, dv, state_v_first))
     host = None
     if cu_seqlens_cpu is not None:
         host = cu_seqlens_cpu.to(torch.int32).contiguous()
         if host.is_cuda:
             raise ValueError("cu_seqlens_cpu must be a host tensor")
     o = out if out is not None else torch.empty((1, total, HV, dv), dtype=q.dtype, device=q.device)
-    hT = final_state if final_state is not None else torch.empty((N, HV, dk, dv), dtype=torch.float32,
-                                                                  device=q.device)
+    hT = final_state if final_state is not None else torch.empty(_st(N, HV, dk, dv, state_v_first),
+                                                                 dtype=torch.float32, device=q.device)
     need = lib.kda_varlen_fwd_workspace(N, total, HV, dk, dv, chunk_size, dt)
     if need == 0:
         raise KdaError(4, "kda_varlen_fwd_workspace", lib)
     ws = _workspace(need, q.device, workspace)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m, state_v_first)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(cu_seqlens), _ptr(host), N,
             total, H, dk, dv, _ptr(initial_state), _ptr(o), _ptr(hT), dt, float(scale or 0.0),
             int(chunk_size), int(bool(use_qk_l2norm)))
@@ -372,7 +379,7 @@ def gk_chunk_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None, 
                  scale=None, chunk_size=64, use_qk_l2norm=True, out=None, final_state=None,
                  workspace=None, stream=None, check_device=False,
                  decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
-                 allow_neg_eigval=False):
+                 allow_neg_eigval=False, state_v_first=False):
     """kda_gk_chunk_fwd / kda_gk_varlen_fwd: chunked prefill with one log decay per key
     channel (g with q's shape, fp32).  Packed when ``cu_seqlens`` is given (as
     gk_recurrent_fwd).  check_device as in chunk_fwd.  Returns (o, final_state)."""
@@ -380,17 +387,17 @@ def gk_chunk_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=None, 
     Bq, T, H, dk = q.shape
     HV, dv = v.shape[2], v.shape[-1]
     m = _value_heads(H, HV)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m, state_v_first)
     dt = _dtype_code(q)
     N = Bq if cu_seqlens is None else cu_seqlens.numel() - 1
     _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (Bq, T, HV, dv))
     _check(beta, "beta", torch.float32, (Bq, T, HV)); _check(g, "g", torch.float32, (Bq, T, HV, dk))
-    _check(initial_state, "initial_state", torch.float32, (N, HV, dk, dv))
+    _check(initial_state, "initial_state", torch.float32, _st(N, HV, dk, dv, state_v_first))
     o = out if out is not None else torch.empty((Bq, T, HV, dv), dtype=q.dtype, device=q.device)
     _check(o, "out", q.dtype, (Bq, T, HV, dv))
-    hT = final_state if final_state is not None else torch.empty((N, HV, dk, dv), dtype=torch.float32,
-                                                                  device=q.device)
-    _check(hT, "final_state", torch.float32, (N, HV, dk, dv))
+    hT = final_state if final_state is not None else torch.empty(_st(N, HV, dk, dv, state_v_first),
+                                                                 dtype=torch.float32, device=q.device)
+    _check(hT, "final_state", torch.float32, _st(N, HV, dk, dv, state_v_first))
     if cu_seqlens is None:
         need = lib.kda_chunk_fwd_workspace(Bq, T, HV, dk, dv, chunk_size, dt)
         if need == 0:
@@ -429,7 +436,7 @@ def gk_recurrent_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=No
                      cu_seqlens_cpu=None, scale=None, use_qk_l2norm=True, out=None,
                      final_state=None, stream=None,
                      decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
-                     allow_neg_eigval=False):
+                     allow_neg_eigval=False, state_v_first=False):
     """kda_gk_recurrent_fwd / kda_gk_varlen_recurrent_fwd: token-by-token prefill with one
     log decay per key channel, g with q's shape (fp32).  ``decayed_read`` selects where the
     delta term reads the memory.  With ``cu_seqlens`` (int32, device, [N+1]) the token
@@ -439,17 +446,17 @@ def gk_recurrent_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=No
     Bq, T, H, dk = q.shape
     HV, dv = v.shape[2], v.shape[-1]
     m = _value_heads(H, HV)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m, state_v_first)
     dt = _dtype_code(q)
     N = Bq if cu_seqlens is None else cu_seqlens.numel() - 1
     _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (Bq, T, HV, dv))
     _check(beta, "beta", torch.float32, (Bq, T, HV)); _check(g, "g", torch.float32, (Bq, T, HV, dk))
-    _check(initial_state, "initial_state", torch.float32, (N, HV, dk, dv))
+    _check(initial_state, "initial_state", torch.float32, _st(N, HV, dk, dv, state_v_first))
     o = out if out is not None else torch.empty((Bq, T, HV, dv), dtype=q.dtype, device=q.device)
     _check(o, "out", q.dtype, (Bq, T, HV, dv))
-    hT = final_state if final_state is not None else torch.empty((N, HV, dk, dv), dtype=torch.float32,
-                                                                  device=q.device)
-    _check(hT, "final_state", torch.float32, (N, HV, dk, dv))
+    hT = final_state if final_state is not None else torch.empty(_st(N, HV, dk, dv, state_v_first),
+                                                                 dtype=torch.float32, device=q.device)
+    _check(hT, "final_state", torch.float32, _st(N, HV, dk, dv, state_v_first))
     if cu_seqlens is None:
         rc = lib.kda_gk_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
                                       _ptr(initial_state), _ptr(o), _ptr(hT), Bq, T, H, dk, dv, dt,
@@ -477,14 +484,15 @@ def gk_recurrent_fwd(q, k, v, beta, g=None, initial_state=None, *, cu_seqlens=No
 def gk_decode_step(q, k, v, beta, g, state, *, scale=None, use_qk_l2norm=True, out=None,
                    stream=None,
                    decayed_read=False, A_log=None, dt_bias=None, beta_sigmoid=False,
-                   allow_neg_eigval=False):
+                   allow_neg_eigval=False, state_v_first=False):
     """kda_gk_decode_step: one token per sequence with per-channel decay g [B,1,H,dk] fp32
     (or None); ``state`` [B,H,dk,dv] fp32 is updated in place.  Returns o with v's shape."""
     lib = load()
-    B, HV, dk, dv = state.shape
+    B, HV, s2, s3 = state.shape
+    dk, dv = (s3, s2) if state_v_first else (s2, s3)
     H = q.numel() // max(B * dk, 1)
     m = _value_heads(H, HV)
-    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m)
+    opts = make_options(decayed_read, A_log, dt_bias, beta_sigmoid, allow_neg_eigval, m, state_v_first)
     dt = _dtype_code(q)
     _check(q, "q"); _check(k, "k", q.dtype); _check(v, "v", q.dtype)
     _check(beta, "beta", torch.float32); _check(g, "g", torch.float32)

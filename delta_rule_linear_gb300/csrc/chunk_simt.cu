@@ -79,11 +79,15 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(SeqBatch p) {
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
     Tin *o = static_cast<Tin *>(p.o);
-    const size_t st_base = ((size_t)n * H + h) * DK * DV + col0;
+    // element (i, j) of the state: key-major at i DV + j, value-major at j DK + i
+    const size_t st_head = ((size_t)n * H + h) * DK * DV;
+    const auto st_at = [&](int i, int j) -> size_t {
+        return p.v_first ? st_head + (size_t)(col0 + j) * DK + i : st_head + (size_t)i * DV + col0 + j;
+    };
 
     for (int idx = tid; idx < DK * DVT; idx += kThreads) {
-        const int i = idx / DVT, j = idx % DVT;
-        sS[idx] = p.h0 ? p.h0[st_base + (size_t)i * DV + j] : 0.f;
+        const int i = p.v_first ? idx % DK : idx / DVT, j = p.v_first ? idx / DK : idx % DVT;
+        sS[i * DVT + j] = p.h0 ? p.h0[st_at(i, j)] : 0.f;
     }
 
     for (int c0 = 0; c0 < len; c0 += C) {
@@ -245,8 +249,8 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(SeqBatch p) {
 
     if (p.hT) {
         for (int idx = tid; idx < DK * DVT; idx += kThreads) {
-            const int i = idx / DVT, j = idx % DVT;
-            p.hT[st_base + (size_t)i * DV + j] = sS[idx];
+            const int i = p.v_first ? idx % DK : idx / DVT, j = p.v_first ? idx / DK : idx % DVT;
+            p.hT[st_at(i, j)] = sS[i * DVT + j];
         }
     }
 }

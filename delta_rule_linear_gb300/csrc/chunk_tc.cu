@@ -69,6 +69,7 @@ struct TcParams {
     const float *dt_bias;      // [H] (scalar decay) or [H, D] (per channel) or nullptr
     int beta_sig, neg_eig;     // beta holds logits: sigmoid, or 2 sigmoid
     int G;                     // value heads per q/k head: H counts value heads, q/k have H / G
+    int v_first;               // states value-major [.., D(v), D(k)]
     const float *h0;           // [nseq, H, D, D] or nullptr
     float *hT;                 // [nseq, H, D, D] or nullptr
     const __nv_bfloat16 *q, *k;   // [rows, H, D]
@@ -1674,15 +1675,17 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
         const size_t hbase = ((size_t)n * p.H + h) * D * D;
         const int i_lo = ch * HALF;
 
+        // element (i, j) of a state: key-major at i D + j, value-major at j D + i
+        const size_t si = p.v_first ? 1 : D, sj = p.v_first ? D : 1;
         if (has_row) {   // S_0^T row j from initial_state[:, j]
             for (int i0 = i_lo; i0 < i_lo + HALF; i0 += 8) {
                 float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = p.h0 ? p.h0[hbase + (size_t)(i0 + e) * D + j] : 0.f;
+                for (int e = 0; e < 8; ++e) x[e] = p.h0 ? p.h0[hbase + (size_t)(i0 + e) * si + j * sj] : 0.f;
                 if (nc == 0) {
                     if (p.hT)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) p.hT[hbase + (size_t)(i0 + e) * D + j] = x[e];
+                        for (int e = 0; e < 8; ++e) p.hT[hbase + (size_t)(i0 + e) * si + j * sj] = x[e];
                 } else {
                     const int ci = (i0 & 63) >> 3;
                     *reinterpret_cast<uint4 *>(sAS + (i0 >> 6) * D * 128 + j * 128 + ((ci ^ (j & 7)) << 4)) =
@@ -1722,7 +1725,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                 } else if (p.hT) {
 #pragma unroll
                     for (int i = 0; i < HALF; ++i)
-                        p.hT[hbase + (size_t)(i_lo + i) * D + j] = __uint_as_float(v[i]);
+                        p.hT[hbase + (size_t)(i_lo + i) * si + j * sj] = __uint_as_float(v[i]);
                 }
             }
             if (!last) fence_proxy_async();
@@ -1951,6 +1954,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.decayed_read = a.decayed_read;
     p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_sig = a.beta_sig; p.neg_eig = a.neg_eig;
     p.G = a.G > 1 ? a.G : 1;
+    p.v_first = a.v_first;
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.k = static_cast<const __nv_bfloat16 *>(a.k);
     p.rows = total_rows;

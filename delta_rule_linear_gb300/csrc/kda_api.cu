@@ -60,6 +60,7 @@ kda_status apply_options(const kda_options *opt, const float *gate, SeqBatch &a)
     a.dt_bias = opt->dt_bias;
     a.beta_sig = opt->beta_sigmoid ? 1 : 0;
     a.neg_eig = (opt->beta_sigmoid && opt->allow_neg_eigval) ? 1 : 0;
+    a.v_first = opt->state_v_first ? 1 : 0;
     if (opt->v_heads_per_qk_head < 0) return KDA_ERR_SHAPE;
     if (opt->v_heads_per_qk_head > 1) {   // a.H (q/k heads on entry) becomes the value-head count
         if ((long)a.H * opt->v_heads_per_qk_head > 0x7fffffffL) return KDA_ERR_SHAPE;
@@ -233,7 +234,7 @@ static kda_status decode_options(const kda_options *opt, const float *gate, Deco
     a.H = d.H;
     const kda_status c = apply_options(opt, gate, a);
     d.decayed_read = a.decayed_read; d.A_log = a.A_log; d.dt_bias = a.dt_bias;
-    d.beta_sig = a.beta_sig; d.neg_eig = a.neg_eig; d.G = a.G; d.H = a.H;
+    d.beta_sig = a.beta_sig; d.neg_eig = a.neg_eig; d.G = a.G; d.H = a.H; d.v_first = a.v_first;
     return c;
 }
 

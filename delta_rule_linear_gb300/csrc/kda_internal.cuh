@@ -42,6 +42,7 @@ struct SeqBatch {
     const float *dt_bias;     // [H] (scalar) or [H, dk] (per channel) or nullptr
     int beta_sig, neg_eig;    // beta holds logits: sigmoid, or 2 sigmoid with neg_eig
     int G;                    // value heads per q/k head (H counts value heads; q/k have H / G)
+    int v_first;              // states are value-major [.., dv, dk]
     const float *h0;          // [nseq, H, dk, dv] or nullptr (zeros)
     void *o;                  // [rows, H, dv]   (Tin)
     float *hT;                // [nseq, H, dk, dv] or nullptr
@@ -66,6 +67,7 @@ struct DecodeArgs {
     const float *A_log, *dt_bias;   // as in SeqBatch
     int beta_sig, neg_eig;
     int G;                          // value heads per q/k head (H counts value heads)
+    int v_first;                    // the state is value-major [B, H, dv, dk]
     float *state;
     void *o;
     int B, H, dk, dv;

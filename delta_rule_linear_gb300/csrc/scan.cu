@@ -1,7 +1,8 @@
 // scan.cu -- single-token decode and the token-by-token (recurrent) prefill.
 //
 // Both run the recurrence of ejkernel kda() ("The core recurrence") one token at
-// a time with the fp32 state held in registers:
+// a time with the fp32 state held in registers (key-major [dk, dv] per head, or value-major
+// [dv, dk] through a shared-memory tile at load and store):
 //     r = S^T k^,  p = S^T q~,  u = beta (v - r),
 //     o = alpha p + (k^ . q~) u,  S <- alpha S + k^ u^T,   alpha = exp(decay)
 // (o = h_t^T q~ expanded with h_t = alpha S + k^ u^T; with alpha = 1 this is the
@@ -45,7 +46,17 @@ struct ScanParams {
     int G;             // value heads per q/k head: H counts value heads, q/k have H / G
 };
 
-template <typename Tin, int DK, int DVS, bool GK>
+// Value-major state ([.., dv, dk], VM kernels): the slab passes through a shared-memory
+// tile of HR key rows at a time, so that global memory is read and written along dk in
+// contiguous runs while the registers keep the key-major layout above.
+template <int DK, int DVS>
+struct VmTile {
+    static constexpr int HR = DK > 64 ? 64 : DK;    // key rows per pass
+    static constexpr int TP = DVS + 4;              // tile pitch (floats): 16-byte rows
+    static constexpr int BYTES = HR * TP * 4;
+};
+
+template <typename Tin, int DK, int DVS, bool GK, bool VM>
 __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
     constexpr int TPR = DVS / 4;          // threads per state row (one float4 each)
     constexpr int RG = kThreads / TPR;    // row groups
@@ -82,11 +93,31 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
 
     const size_t sbase = ((size_t)n * p.H + h) * DK * p.DV + col0 + 4 * cg;
     float4 S[R];
+    if constexpr (!VM) {
 #pragma unroll
-    for (int m = 0; m < R; ++m) {
-        const int i = rg + RG * m;
-        S[m] = p.h0 ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)i * p.DV))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m = 0; m < R; ++m) {
+            const int i = rg + RG * m;
+            S[m] = p.h0 ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)i * p.DV))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    } else {
+        using VT = VmTile<DK, DVS>;
+        static_assert(VT::HR % RG == 0, "a thread's rows split evenly over the passes");
+        extern __shared__ __align__(16) float s_tile[];
+        const size_t vbase = ((size_t)n * p.H + h) * (size_t)p.DV * DK + (size_t)col0 * DK;
+#pragma unroll
+        for (int pp = 0; pp < DK / VT::HR; ++pp) {
+            for (int idx = tid; idx < DVS * VT::HR; idx += kThreads) {   // along dk in global memory
+                const int ii = idx % VT::HR, jj = idx / VT::HR;
+                s_tile[ii * VT::TP + jj] = p.h0 ? __ldcs(p.h0 + vbase + (size_t)jj * DK + pp * VT::HR + ii) : 0.f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int m = 0; m < R; ++m)
+                if ((RG * m) / VT::HR == pp)
+                    S[m] = *reinterpret_cast<const float4 *>(&s_tile[(rg + RG * m - pp * VT::HR) * VT::TP + 4 * cg]);
+            __syncthreads();
+        }
     }
 
     for (int t = 0; t < len; ++t) {
@@ -176,45 +207,71 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
     }
 
     if (p.hT) {
+        if constexpr (!VM) {
 #pragma unroll
-        for (int m = 0; m < R; ++m) {
-            const int i = rg + RG * m;
-            __stcs(reinterpret_cast<float4 *>(p.hT + sbase + (size_t)i * p.DV), S[m]);
+            for (int m = 0; m < R; ++m) {
+                const int i = rg + RG * m;
+                __stcs(reinterpret_cast<float4 *>(p.hT + sbase + (size_t)i * p.DV), S[m]);
+            }
+        } else {
+            using VT = VmTile<DK, DVS>;
+            extern __shared__ __align__(16) float s_tile[];
+            const size_t vbase = ((size_t)n * p.H + h) * (size_t)p.DV * DK + (size_t)col0 * DK;
+#pragma unroll
+            for (int pp = 0; pp < DK / VT::HR; ++pp) {
+#pragma unroll
+                for (int m = 0; m < R; ++m)
+                    if ((RG * m) / VT::HR == pp)
+                        *reinterpret_cast<float4 *>(&s_tile[(rg + RG * m - pp * VT::HR) * VT::TP + 4 * cg]) = S[m];
+                __syncthreads();
+                for (int idx = tid; idx < DVS * VT::HR; idx += kThreads) {
+                    const int ii = idx % VT::HR, jj = idx / VT::HR;
+                    __stcs(p.hT + vbase + (size_t)jj * DK + pp * VT::HR + ii, s_tile[ii * VT::TP + jj]);
+                }
+                __syncthreads();
+            }
         }
     }
 }
 
+template <typename Tin, int DK, bool GK, int DVS>
+void launch_vm(const ScanParams &p, int grid, bool vm, cudaStream_t s) {
+    if (vm) scan_kernel<Tin, DK, DVS, GK, true><<<grid, kThreads, VmTile<DK, DVS>::BYTES, s>>>(p);
+    else scan_kernel<Tin, DK, DVS, GK, false><<<grid, kThreads, 0, s>>>(p);
+}
+
 template <typename Tin, int DK, bool GK>
-cudaError_t launch_dk(const ScanParams &p, int dvs, int grid, cudaStream_t s) {
+cudaError_t launch_dk(const ScanParams &p, int dvs, int grid, bool vm, cudaStream_t s) {
     switch (dvs) {
-        case 32: scan_kernel<Tin, DK, 32, GK><<<grid, kThreads, 0, s>>>(p); break;
-        case 64: scan_kernel<Tin, DK, 64, GK><<<grid, kThreads, 0, s>>>(p); break;
-        case 128: scan_kernel<Tin, DK, 128, GK><<<grid, kThreads, 0, s>>>(p); break;
+        case 32: launch_vm<Tin, DK, GK, 32>(p, grid, vm, s); break;
+        case 64: launch_vm<Tin, DK, GK, 64>(p, grid, vm, s); break;
+        case 128: launch_vm<Tin, DK, GK, 128>(p, grid, vm, s); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 
 template <typename Tin, bool GK>
-cudaError_t launch_typed(const ScanParams &p, int dk, int dvs, int grid, cudaStream_t s) {
+cudaError_t launch_typed(const ScanParams &p, int dk, int dvs, int grid, bool vm, cudaStream_t s) {
     switch (dk) {
-        case 32: return launch_dk<Tin, 32, GK>(p, dvs, grid, s);
-        case 64: return launch_dk<Tin, 64, GK>(p, dvs, grid, s);
-        case 128: return launch_dk<Tin, 128, GK>(p, dvs, grid, s);
+        case 32: return launch_dk<Tin, 32, GK>(p, dvs, grid, vm, s);
+        case 64: return launch_dk<Tin, 64, GK>(p, dvs, grid, vm, s);
+        case 128: return launch_dk<Tin, 128, GK>(p, dvs, grid, vm, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-// gk selects the per-key-channel kernels (p.gk may still be null: no decay).
-cudaError_t launch_scan(const ScanParams &p, DType dt, int dk, int dvs, bool gk, cudaStream_t s) {
+// gk selects the per-key-channel kernels (p.gk may still be null: no decay); vm the
+// value-major state.
+cudaError_t launch_scan(const ScanParams &p, DType dt, int dk, int dvs, bool gk, bool vm, cudaStream_t s) {
     const long grid = (long)p.nseq * p.H * (p.DV / dvs);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     if (gk)
-        return dt == DType::BF16 ? launch_typed<__nv_bfloat16, true>(p, dk, dvs, (int)grid, s)
-                                 : launch_typed<float, true>(p, dk, dvs, (int)grid, s);
-    return dt == DType::BF16 ? launch_typed<__nv_bfloat16, false>(p, dk, dvs, (int)grid, s)
-                             : launch_typed<float, false>(p, dk, dvs, (int)grid, s);
+        return dt == DType::BF16 ? launch_typed<__nv_bfloat16, true>(p, dk, dvs, (int)grid, vm, s)
+                                 : launch_typed<float, true>(p, dk, dvs, (int)grid, vm, s);
+    return dt == DType::BF16 ? launch_typed<__nv_bfloat16, false>(p, dk, dvs, (int)grid, vm, s)
+                             : launch_typed<float, false>(p, dk, dvs, (int)grid, vm, s);
 }
 
 }  // namespace
@@ -228,7 +285,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_sig = a.beta_sig; p.neg_eig = a.neg_eig;
     p.G = a.G > 1 ? a.G : 1;
     // one CTA per head, whole value width
-    return launch_scan(p, a.dtype, a.dk, a.dv, a.per_channel != 0, s);
+    return launch_scan(p, a.dtype, a.dk, a.dv, a.per_channel != 0, a.v_first != 0, s);
 }
 
 cudaError_t launch_recurrent(const SeqBatch &a, cudaStream_t s) {
@@ -241,7 +298,7 @@ cudaError_t launch_recurrent(const SeqBatch &a, cudaStream_t s) {
     p.G = a.G > 1 ? a.G : 1;
     // 32-column slabs: a long prefill is latency-bound per token, so spread the
     // independent value columns over more CTAs.
-    return launch_scan(p, a.dtype, a.dk, 32, a.per_channel != 0, s);
+    return launch_scan(p, a.dtype, a.dk, 32, a.per_channel != 0, a.v_first != 0, s);
 }
 
 }  // namespace kda

@@ -94,6 +94,9 @@ typedef struct kda_options {
                                heads; v, o, beta, decay, g, A_log, dt_bias and the state have
                                HV heads, and value head hv reads q/k head hv / m.  0 or 1: none.
                                Workspace queries take the value-head count HV.                 */
+    int state_v_first;      /* nonzero: initial_state / final_state / the decode state are
+                               value-major [.., HV, dv, dk] (GDNFwdOp / KDAFwdOp state_v_first)
+                               instead of key-major [.., HV, dk, dv]                           */
 } kda_options;
 
 /* Human-readable name of a status code (static storage, never NULL). */
