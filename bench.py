@@ -31,8 +31,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from kda_inputs import (WORKLOADS, make_decode_state, make_decode_step, make_gate_params,  # noqa: E402
-                        make_gk, make_gk_decode_step, make_prefill, make_varlen)
+from kda_inputs import (WORKLOADS, make_custom, make_decode_state, make_decode_step,  # noqa: E402
+                        make_gate_params, make_gk, make_gk_decode_step, make_prefill, make_varlen)
 
 METRIC = "prefill tokens/s & % bf16 TC peak; decode state GB/s vs HBM peak (1×GB300)"
 NOMINAL_HBM_GBS = 8000.0
@@ -493,6 +493,80 @@ def bench_gk(args, world, rank, dev, peaks):
     return out
 
 
+# --------------------------------------------------------------------------- layouts
+def bench_layouts(args, world, rank, dev, peaks):
+    """Layout options: the decode step with value-major states (TileOPs state_v_first) at the
+    decode workload's shape, against the HBM roofline; and the training-shape prefill with
+    grouped value heads (4 q/k heads, 16 value heads)."""
+    import torch
+    import delta_rule_linear_gb300 as kda
+    from delta_rule_linear_gb300 import _lib
+    stream = torch.cuda.current_stream()
+    out = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    wl = WORKLOADS[4]
+    state = to_dev(np.ascontiguousarray(np.swapaxes(make_decode_state(wl, seed=rank), -1, -2)), dev,
+                   torch.float32)
+    nsteps = 32
+    toks = []
+    for s_ in range(nsteps):
+        st = make_decode_step(wl, s_, seed=rank)
+        toks.append(tuple(to_dev(st[n], dev, torch.bfloat16) for n in ("q", "k", "v")) +
+                    tuple(to_dev(st[n], dev, torch.float32) for n in ("beta", "decay")))
+    o = torch.empty((wl.B, 1, wl.H, wl.dv), dtype=torch.bfloat16, device=dev)
+
+    def run(n):
+        for i in range(n):
+            q, k, v, b, g = toks[i % nsteps]
+            kda.decode_step(q, k, v, b, g, state, out=o, stream=stream, state_v_first=True)
+
+    run(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    run(nsteps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / nsteps, world)
+    nbytes = 2.0 * wl.B * wl.H * wl.dk * wl.dv * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["decode_state_v_first"] = {
+        "workload": wl.name + ", value-major state", "ms_per_step": ms, "gpu_launches": nsteps,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_launch": nbytes}}
+    del state, toks
+
+    B, T, H, m, D = 2, 2048, 4, 4, 128
+    d = make_custom(B, T, H * m, D, D, dtype="bf16", decay="train", seed=rank)
+    q, k = (to_dev(np.ascontiguousarray(d[n][:, :, ::m]), dev, torch.bfloat16) for n in ("q", "k"))
+    v = to_dev(d["v"], dev, torch.bfloat16)
+    beta, decay = (to_dev(d[n], dev, torch.float32) for n in ("beta", "decay"))
+    o = torch.empty_like(v)
+    hT = torch.empty((B, H * m, D, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(_lib.chunk_fwd_workspace_bytes(B, T, H * m, D, D, 64, _lib.KDA_BF16),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.chunk_fwd(q, k, v, beta, decay, None, out=o, final_state=hT, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    out["grouped_heads_prefill"] = {
+        "shape": dict(B=B, T=T, qk_heads=H, v_heads=H * m, dk=D, dv=D, chunk=64), "ms_per_call": ms,
+        "tokens_per_s": B * T * world / (ms * 1e-3),
+        "gpu_launches_per_call": tc_prefill_launches(B, H * m, dev)}
+    return out
+
+
 # --------------------------------------------------------------------------- decode
 def bench_decode(args, world, rank, dev, peaks):
     import torch
@@ -643,6 +717,8 @@ def main():
     sec = bench_secondary(args, world, rank, dev, peaks) if args.only in (None, "secondary") else None
     if args.only in (None, "secondary", "gk", "gk_prefill"):
         sec = dict(sec or {}, kda_gk=bench_gk(args, world, rank, dev, peaks))
+    if args.only in (None, "secondary"):
+        sec = dict(sec or {}, layouts=bench_layouts(args, world, rank, dev, peaks))
     if rank != 0:
         return
     if pre is None:

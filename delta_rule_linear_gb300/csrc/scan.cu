@@ -1,8 +1,8 @@
 // scan.cu -- single-token decode and the token-by-token (recurrent) prefill.
 //
 // Both run the recurrence of ejkernel kda() ("The core recurrence") one token at
-// a time with the fp32 state held in registers (key-major [dk, dv] per head, or value-major
-// [dv, dk] through a shared-memory tile at load and store):
+// a time with the fp32 state held in registers (key-major [dk, dv] per head here; the
+// value-major [dv, dk] layout has its own kernel below):
 //     r = S^T k^,  p = S^T q~,  u = beta (v - r),
 //     o = alpha p + (k^ . q~) u,  S <- alpha S + k^ u^T,   alpha = exp(decay)
 // (o = h_t^T q~ expanded with h_t = alpha S + k^ u^T; with alpha = 1 this is the
@@ -46,17 +46,7 @@ struct ScanParams {
     int G;             // value heads per q/k head: H counts value heads, q/k have H / G
 };
 
-// Value-major state ([.., dv, dk], VM kernels): the slab passes through a shared-memory
-// tile of HR key rows at a time, so that global memory is read and written along dk in
-// contiguous runs while the registers keep the key-major layout above.
-template <int DK, int DVS>
-struct VmTile {
-    static constexpr int HR = DK > 64 ? 64 : DK;    // key rows per pass
-    static constexpr int TP = DVS + 4;              // tile pitch (floats): 16-byte rows
-    static constexpr int BYTES = HR * TP * 4;
-};
-
-template <typename Tin, int DK, int DVS, bool GK, bool VM>
+template <typename Tin, int DK, int DVS, bool GK>
 __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
     constexpr int TPR = DVS / 4;          // threads per state row (one float4 each)
     constexpr int RG = kThreads / TPR;    // row groups
@@ -93,31 +83,11 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
 
     const size_t sbase = ((size_t)n * p.H + h) * DK * p.DV + col0 + 4 * cg;
     float4 S[R];
-    if constexpr (!VM) {
 #pragma unroll
-        for (int m = 0; m < R; ++m) {
-            const int i = rg + RG * m;
-            S[m] = p.h0 ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)i * p.DV))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    } else {
-        using VT = VmTile<DK, DVS>;
-        static_assert(VT::HR % RG == 0, "a thread's rows split evenly over the passes");
-        extern __shared__ __align__(16) float s_tile[];
-        const size_t vbase = ((size_t)n * p.H + h) * (size_t)p.DV * DK + (size_t)col0 * DK;
-#pragma unroll
-        for (int pp = 0; pp < DK / VT::HR; ++pp) {
-            for (int idx = tid; idx < DVS * VT::HR; idx += kThreads) {   // along dk in global memory
-                const int ii = idx % VT::HR, jj = idx / VT::HR;
-                s_tile[ii * VT::TP + jj] = p.h0 ? __ldcs(p.h0 + vbase + (size_t)jj * DK + pp * VT::HR + ii) : 0.f;
-            }
-            __syncthreads();
-#pragma unroll
-            for (int m = 0; m < R; ++m)
-                if ((RG * m) / VT::HR == pp)
-                    S[m] = *reinterpret_cast<const float4 *>(&s_tile[(rg + RG * m - pp * VT::HR) * VT::TP + 4 * cg]);
-            __syncthreads();
-        }
+    for (int m = 0; m < R; ++m) {
+        const int i = rg + RG * m;
+        S[m] = p.h0 ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)i * p.DV))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
     for (int t = 0; t < len; ++t) {
@@ -207,37 +177,160 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
     }
 
     if (p.hT) {
-        if constexpr (!VM) {
 #pragma unroll
-            for (int m = 0; m < R; ++m) {
-                const int i = rg + RG * m;
-                __stcs(reinterpret_cast<float4 *>(p.hT + sbase + (size_t)i * p.DV), S[m]);
-            }
+        for (int m = 0; m < R; ++m) {
+            const int i = rg + RG * m;
+            __stcs(reinterpret_cast<float4 *>(p.hT + sbase + (size_t)i * p.DV), S[m]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// The same recurrence with a value-major state ([.., dv, dk] per head: TileOPs
+// state_v_first).  Lane l of a warp owns key rows [l RPL, (l + 1) RPL) of the warp's CPW
+// value columns, so that a column's dk entries are one contiguous run of a warp's loads
+// and stores; the reductions over dk are warp shuffles (all lanes end with each column's
+// sum).
+// ---------------------------------------------------------------------------------
+template <typename Tin, int DK, int DVS, bool GK>
+__global__ void __launch_bounds__(kThreads) scan_vm_kernel(ScanParams p) {
+    constexpr int NW = kThreads / 32;
+    constexpr int CPW = DVS / NW;           // value columns per warp
+    constexpr int RPL = DK / 32;            // key rows per lane
+    static_assert(CPW >= 1 && DVS % NW == 0 && RPL >= 1 && DK % 32 == 0, "slab does not tile the block");
+    static_assert(2 * DK <= kThreads && DVS <= kThreads, "staging assumes small heads");
+
+    __shared__ __align__(16) float s_k[DK];
+    __shared__ __align__(16) float s_q[DK];
+    __shared__ __align__(16) float s_a[GK ? DK : 4];
+    __shared__ float s_v[DVS];
+    __shared__ float s_sc[8];
+
+    const int nslab = p.DV / DVS;
+    const int slab = blockIdx.x % nslab;
+    const int h = (blockIdx.x / nslab) % p.H;
+    const int n = blockIdx.x / (nslab * p.H);
+    long start;
+    int len;
+    if (p.cu_seqlens) {
+        start = p.cu_seqlens[n];
+        len = p.cu_seqlens[n + 1] - p.cu_seqlens[n];
+    } else {
+        start = (long)n * p.T;
+        len = p.T;
+    }
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int col0 = slab * DVS, c0w = warp * CPW;   // the warp's first column in the slab
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    Tin *o = static_cast<Tin *>(p.o);
+
+    // S[c][e] = state(i = lane RPL + e, j = col0 + c0w + c), stored at j DK + i
+    const size_t vbase = ((size_t)n * p.H + h) * (size_t)p.DV * DK + (size_t)(col0 + c0w) * DK + lane * RPL;
+    float S[CPW][RPL];
+#pragma unroll
+    for (int c = 0; c < CPW; ++c) {
+        const float *src = p.h0 + vbase + (size_t)c * DK;
+        if (!p.h0) {
+#pragma unroll
+            for (int e = 0; e < RPL; ++e) S[c][e] = 0.f;
+        } else if constexpr (RPL == 4) {
+            const float4 x = __ldcs(reinterpret_cast<const float4 *>(src));
+            S[c][0] = x.x; S[c][1] = x.y; S[c][2] = x.z; S[c][3] = x.w;
+        } else if constexpr (RPL == 2) {
+            const float2 x = __ldcs(reinterpret_cast<const float2 *>(src));
+            S[c][0] = x.x; S[c][1] = x.y;
         } else {
-            using VT = VmTile<DK, DVS>;
-            extern __shared__ __align__(16) float s_tile[];
-            const size_t vbase = ((size_t)n * p.H + h) * (size_t)p.DV * DK + (size_t)col0 * DK;
-#pragma unroll
-            for (int pp = 0; pp < DK / VT::HR; ++pp) {
-#pragma unroll
-                for (int m = 0; m < R; ++m)
-                    if ((RG * m) / VT::HR == pp)
-                        *reinterpret_cast<float4 *>(&s_tile[(rg + RG * m - pp * VT::HR) * VT::TP + 4 * cg]) = S[m];
-                __syncthreads();
-                for (int idx = tid; idx < DVS * VT::HR; idx += kThreads) {
-                    const int ii = idx % VT::HR, jj = idx / VT::HR;
-                    __stcs(p.hT + vbase + (size_t)jj * DK + pp * VT::HR + ii, s_tile[ii * VT::TP + jj]);
-                }
-                __syncthreads();
+            S[c][0] = __ldcs(src);
+        }
+    }
+
+    for (int t = 0; t < len; ++t) {
+        const long row = start + t;
+        const size_t qk_off = ((size_t)row * (p.H / p.G) + h / p.G) * DK;
+        const size_t g_off = ((size_t)row * p.H + h) * DK;
+        const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
+        if (tid < DK) {
+            s_k[tid] = to_f32(k[qk_off + tid]);
+            if constexpr (GK) {
+                float gv = p.gk ? p.gk[g_off + tid] : 0.f;
+                if (p.gk && p.A_log)
+                    gv = gate_decay(gv, p.A_log[h], p.dt_bias ? p.dt_bias[(size_t)h * DK + tid] : 0.f);
+                s_a[tid] = expf(gv);
             }
+        } else if (tid < 2 * DK) {
+            s_q[tid - DK] = to_f32(q[qk_off + tid - DK]);
+        }
+        if (tid < DVS) s_v[tid] = to_f32(v[v_off + tid]);
+        if (tid == 0) {
+            s_sc[0] = beta_of(p.beta[(size_t)row * p.H + h], p.beta_sig, p.neg_eig);
+            float d = p.decay ? p.decay[(size_t)row * p.H + h] : 0.f;
+            if (p.decay && p.A_log) d = gate_decay(d, p.A_log[h], p.dt_bias ? p.dt_bias[h] : 0.f);
+            s_sc[1] = d;
+        }
+        __syncthreads();
+        if (warp < 3) {  // ||k||^2, ||q||^2, k.q
+            float acc = 0.f;
+            for (int i = lane; i < DK; i += 32) {
+                const float a = (warp == 1) ? s_q[i] : s_k[i];
+                const float b = (warp == 0) ? s_k[i] : s_q[i];
+                acc = fmaf(a, b, acc);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) s_sc[2 + warp] = acc;
+        }
+        __syncthreads();
+        const float kn = p.use_l2 ? 1.f / fmaxf(sqrtf(s_sc[2]), kNormEps) : 1.f;
+        const float qn = p.scale * (p.use_l2 ? 1.f / fmaxf(sqrtf(s_sc[3]), kNormEps) : 1.f);
+        const float alpha = expf(s_sc[1]), bt = s_sc[0], kq = s_sc[4];
+        float kk[RPL], qq[RPL], am[RPL];
+#pragma unroll
+        for (int e = 0; e < RPL; ++e) {
+            const int i = lane * RPL + e;
+            am[e] = GK ? s_a[i] : alpha;
+            kk[e] = s_k[i];
+            qq[e] = s_q[i];
+        }
+#pragma unroll
+        for (int c = 0; c < CPW; ++c) {
+            float r = 0.f, pq = 0.f;
+#pragma unroll
+            for (int e = 0; e < RPL; ++e) {
+                // r reads S (or D S with the decayed read); p reads D S
+                r = fmaf(S[c][e], (GK && p.decayed_read) ? am[e] * kk[e] : kk[e], r);
+                pq = fmaf(S[c][e], GK ? am[e] * qq[e] : qq[e], pq);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                r += __shfl_xor_sync(0xffffffffu, r, off);
+                pq += __shfl_xor_sync(0xffffffffu, pq, off);
+            }
+            const int j = c0w + c;
+            const float u = bt * (s_v[j] - kn * ((!GK && p.decayed_read) ? alpha * r : r));
+            if (lane == c % 32) o[v_off + j] = from_f32<Tin>((GK ? 1.f : alpha) * (qn * pq) + (kn * qn * kq) * u);
+#pragma unroll
+            for (int e = 0; e < RPL; ++e) S[c][e] = fmaf(am[e], S[c][e], kn * kk[e] * u);
+        }
+        __syncthreads();  // staging buffers are rewritten by the next token
+    }
+
+    if (p.hT) {
+#pragma unroll
+        for (int c = 0; c < CPW; ++c) {
+            float *dst = p.hT + vbase + (size_t)c * DK;
+            if constexpr (RPL == 4) __stcs(reinterpret_cast<float4 *>(dst), make_float4(S[c][0], S[c][1], S[c][2], S[c][3]));
+            else if constexpr (RPL == 2) __stcs(reinterpret_cast<float2 *>(dst), make_float2(S[c][0], S[c][1]));
+            else __stcs(dst, S[c][0]);
         }
     }
 }
 
 template <typename Tin, int DK, bool GK, int DVS>
 void launch_vm(const ScanParams &p, int grid, bool vm, cudaStream_t s) {
-    if (vm) scan_kernel<Tin, DK, DVS, GK, true><<<grid, kThreads, VmTile<DK, DVS>::BYTES, s>>>(p);
-    else scan_kernel<Tin, DK, DVS, GK, false><<<grid, kThreads, 0, s>>>(p);
+    if (vm) scan_vm_kernel<Tin, DK, DVS, GK><<<grid, kThreads, 0, s>>>(p);
+    else scan_kernel<Tin, DK, DVS, GK><<<grid, kThreads, 0, s>>>(p);
 }
 
 template <typename Tin, int DK, bool GK>
