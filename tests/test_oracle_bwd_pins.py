@@ -1,0 +1,54 @@
+"""Pins for the fp64 backward oracle: its forward equals the C oracle's per-channel scan, and
+its gradients equal central finite differences of that forward (tiny sizes, every input)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+
+def _inputs(seed, B=1, T=5, H=2, dk=3, dv=4):
+    rng = np.random.default_rng(seed)
+    return dict(q=rng.standard_normal((B, T, H, dk)), k=rng.standard_normal((B, T, H, dk)),
+                v=rng.standard_normal((B, T, H, dv)), beta=rng.uniform(0.1, 0.9, (B, T, H)),
+                g=-rng.uniform(0, 1.5, (B, T, H, dk)), h0=rng.standard_normal((B, H, dk, dv)))
+
+
+@pytest.mark.parametrize("decayed", [False, True])
+def test_forward_matches_c_oracle(oracle_mod, decayed):
+    from oracle import backward as ob
+    d = _inputs(1, B=2, T=9, H=2, dk=4, dv=5)
+    d32 = {n: np.asarray(x, np.float32) for n, x in d.items()}
+    ro, rh = oracle_mod.forward_gk(d32["q"], d32["k"], d32["v"], d32["beta"], d32["g"], d32["h0"],
+                                   decayed_read=decayed)
+    t = {n: torch.tensor(np.asarray(x, np.float64)) for n, x in d32.items()}
+    o, h = ob.forward_torch(t["q"], t["k"], t["v"], t["beta"], t["g"], t["h0"], decayed_read=decayed)
+    assert np.max(np.abs(o.numpy() - ro)) < 1e-12 and np.max(np.abs(h.numpy() - rh)) < 1e-12
+
+
+@pytest.mark.parametrize("use_l2", [True, False])
+@pytest.mark.parametrize("decayed", [False, True])
+def test_gradients_match_finite_differences(decayed, use_l2):
+    from oracle import backward as ob
+    d = _inputs(2)
+    rng = np.random.default_rng(3)
+    do = rng.standard_normal((1, 5, 2, 4))
+    dhT = rng.standard_normal((1, 2, 3, 4))
+    kw = dict(scale=0.7, use_l2=use_l2, decayed_read=decayed)
+    grads = ob.backward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], do, dhT, **kw)
+
+    def loss(dd):
+        t = {n: torch.tensor(x) for n, x in dd.items()}
+        o, h = ob.forward_torch(t["q"], t["k"], t["v"], t["beta"], t["g"], t["h0"], **kw)
+        return float((o.numpy() * do).sum() + (h.numpy() * dhT).sum())
+
+    eps = 1e-6
+    for name in ("q", "k", "v", "beta", "g", "h0"):
+        fd = np.zeros_like(d[name])
+        for idx in np.ndindex(d[name].shape):
+            p = {n: x.copy() for n, x in d.items()}
+            m = {n: x.copy() for n, x in d.items()}
+            p[name][idx] += eps
+            m[name][idx] -= eps
+            fd[idx] = (loss(p) - loss(m)) / (2 * eps)
+        err = np.max(np.abs(fd - grads["d" + name])) / max(np.max(np.abs(fd)), 1e-12)
+        assert err < 1e-7, (name, err)
