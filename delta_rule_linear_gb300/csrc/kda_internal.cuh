@@ -96,6 +96,22 @@ cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound
 // each giving up after limit_ns and recording KDA_ERR_DEVICE_TIMEOUT in the header.
 cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t s);
 
+// Gradients of the per-channel recurrence (token by token; scan_bwd.cu).
+struct BwdArgs {
+    const void *q, *k, *v, *dout;      // [rows, H, dk | dv] (Tin)
+    const float *beta, *g;             // [rows, H], [rows, H, dk] (g may be null)
+    const float *h0, *dhT;             // [B, H, dk, dv] or null
+    float *dq, *dk, *dv, *dbeta, *dg;  // fp32 gradients (dg may be null)
+    float *dh0;                        // [B, H, dk, dv] or null
+    int B, T, H, dkdim, dvdim;
+    DType dtype;
+    float scale;
+    int use_l2, decayed_read;
+    void *ws;                          // gk_bwd_scratch_bytes()
+};
+size_t gk_bwd_scratch_bytes(int nseq, int T, int H, int dk, int dv);
+cudaError_t launch_gk_bwd(const BwdArgs &a, cudaStream_t s);
+
 // L2 normalisation floor: x / max(||x||, kNormEps).
 constexpr float kNormEps = 1e-12f;
 

@@ -293,6 +293,30 @@ kda_status kda_gk_decode_step(const void *q, const void *k, const void *v,
                               int use_qk_l2norm, const kda_options *opt, kda_stream_t stream);
 
 /*
+ * Gradients of the per-key-channel recurrence above (the backward of the training mode; the
+ * kda-neuron-kernels README's kda_chunk_step_exact_bwd returns the same set): given
+ * d_o = dL/do [B,T,H,dv] (dtype of q) and dfinal_state = dL/dfinal_state [B,H,dk,dv] fp32
+ * (NULL = zero), writes the fp32 gradients
+ *     dq, dk [B,T,H,dk];  dv [B,T,H,dv];  dbeta [B,T,H];  dg [B,T,H,dk] (NULL allowed;
+ *     zeros when g is NULL);  dinitial_state [B,H,dk,dv] (NULL allowed)
+ * with respect to the raw q and k (through the L2 normalisation and the scale), v, beta,
+ * g and initial_state.  q, k, v, beta, g, initial_state, scale, use_qk_l2norm, decayed_read
+ * as in the forward (equal-length batches, key-major states).  Token by token on CUDA
+ * cores: a forward pass stores the state every 32 tokens, the backward pass recomputes each
+ * 32-token stretch and walks it in reverse.  ws: at least
+ * kda_gk_recurrent_bwd_workspace() bytes, 16-byte aligned.
+ */
+size_t kda_gk_recurrent_bwd_workspace(int B, int T, int H, int dk, int dv);
+kda_status kda_gk_recurrent_bwd(const void *q, const void *k, const void *v,
+                                const float *beta, const float *g,
+                                const float *initial_state, const void *d_o,
+                                const float *dfinal_state, float *dq, float *dk_out,
+                                float *dv_out, float *dbeta, float *dg, float *dinitial_state,
+                                int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                                float scale, int use_qk_l2norm, int decayed_read,
+                                void *ws, size_t ws_bytes, kda_stream_t stream);
+
+/*
  * The scalar-decay entry points with options (see kda_options): the same arguments, layouts,
  * workspace and errors as kda_chunk_fwd / kda_varlen_fwd / kda_recurrent_fwd /
  * kda_decode_step, plus `opt` (may be NULL).  A_log and dt_bias must be 4-byte aligned
