@@ -486,6 +486,30 @@ def bench_gk(args, world, rank, dev, peaks):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / nrep, world)
+    # the backward of the same call: gradients for q, k, v, beta, g and the initial state
+    d_o = torch.randn_like(o)
+    gates = to_dev(d["g"], dev, torch.float32)
+    h0z = torch.zeros((Bp, Hp, D, D), dtype=torch.float32, device=dev)
+    from delta_rule_linear_gb300 import _lib
+    wsb = torch.empty(_lib.load().kda_gk_recurrent_bwd_workspace(Bp, T, Hp, D, D), dtype=torch.uint8,
+                      device=dev)
+
+    def bstep():
+        kda.gk_recurrent_bwd(q, k, v, beta, gates, h0z, d_o, None, decayed_read=True, workspace=wsb,
+                             stream=stream)
+
+    bstep()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(nrep):
+        bstep()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    bms = max_over_ranks(e0.elapsed_time(e1) / nrep, world)
+    out["gk_recurrent_bwd"] = {
+        "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D), "decayed_read": True, "ms_per_call": bms,
+        "tokens_per_s": Bp * T * world / (bms * 1e-3), "calls": nrep, "gpu_launches_per_call": 3,
+        "note": "token by token on CUDA cores: 32-token checkpoints, recompute, reverse walk"}
     out["gk_recurrent_prefill"] = {
         "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D), "decayed_read": True, "ms_per_call": ms,
         "tokens_per_s": Bp * T * world / (ms * 1e-3), "calls": nrep, "gpu_launches_per_call": 1,
