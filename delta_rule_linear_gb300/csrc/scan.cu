@@ -21,7 +21,8 @@
 // head, i.e. one contiguous stretch of the key-major state: every state access is
 // a coalesced 128-bit load or store, and the state crosses HBM exactly once in
 // and once out per call.  The two reductions over dk (S^T k and S^T q) are
-// in-thread sums followed by one shared-memory pass over the row groups.
+// in-thread sums followed by one shared-memory pass over the row groups (with many row
+// groups, each column summed by a few lanes and a shuffle).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -44,6 +45,50 @@ struct ScanParams {
     const float *A_log, *dt_bias;   // raw gate -> decay (gate_decay); dt_bias [H] or [H, DK]
     int beta_sig, neg_eig;
     int G;             // value heads per q/k head: H counts value heads, q/k have H / G
+};
+
+// One token's inputs, each thread its share (k or q entry, g, v entry, beta and decay),
+// read from global memory one token ahead of its use so that the loads' latency overlaps
+// the previous token's work; put() applies the gate and beta transforms and fills the
+// shared staging arrays.
+template <typename Tin, int DK, int DVS, bool GK>
+struct TokenLoad {
+    float kq = 0.f, g = 0.f, v = 0.f, beta = 0.f, decay = 0.f;
+    __device__ __forceinline__ void fetch(const ScanParams &p, long row, int h, int col0, int tid) {
+        const size_t qk_off = ((size_t)row * (p.H / p.G) + h / p.G) * DK;   // q/k head of value head h
+        if (tid < DK) {
+            kq = to_f32(static_cast<const Tin *>(p.k)[qk_off + tid]);
+            if (GK && p.gk) g = p.gk[((size_t)row * p.H + h) * DK + tid];
+        } else if (tid < 2 * DK) {
+            kq = to_f32(static_cast<const Tin *>(p.q)[qk_off + tid - DK]);
+        }
+        if (tid < DVS) v = to_f32(static_cast<const Tin *>(p.v)[((size_t)row * p.H + h) * p.DV + col0 + tid]);
+        if (tid == 0) {
+            beta = p.beta[(size_t)row * p.H + h];
+            decay = p.decay ? p.decay[(size_t)row * p.H + h] : 0.f;
+        }
+    }
+    __device__ __forceinline__ void put(const ScanParams &p, int h, int tid, float *s_k, float *s_q, float *s_a,
+                                        float *s_v, float *s_sc) const {
+        if (tid < DK) {
+            s_k[tid] = kq;
+            if constexpr (GK) {
+                float gv = g;
+                if (p.gk && p.A_log)
+                    gv = gate_decay(gv, p.A_log[h], p.dt_bias ? p.dt_bias[(size_t)h * DK + tid] : 0.f);
+                s_a[tid] = expf(gv);
+            }
+        } else if (tid < 2 * DK) {
+            s_q[tid - DK] = kq;
+        }
+        if (tid < DVS) s_v[tid] = v;
+        if (tid == 0) {
+            s_sc[0] = beta_of(beta, p.beta_sig, p.neg_eig);
+            float d = decay;
+            if (p.decay && p.A_log) d = gate_decay(d, p.A_log[h], p.dt_bias ? p.dt_bias[h] : 0.f);
+            s_sc[1] = d;
+        }
+    }
 };
 
 template <typename Tin, int DK, int DVS, bool GK>
@@ -76,9 +121,6 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = tid % TPR, rg = tid / TPR;
     const int col0 = slab * DVS;
-    const Tin *q = static_cast<const Tin *>(p.q);
-    const Tin *k = static_cast<const Tin *>(p.k);
-    const Tin *v = static_cast<const Tin *>(p.v);
     Tin *o = static_cast<Tin *>(p.o);
 
     const size_t sbase = ((size_t)n * p.H + h) * DK * p.DV + col0 + 4 * cg;
@@ -90,29 +132,13 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
+    TokenLoad<Tin, DK, DVS, GK> tk;   // this thread's share of the token, fetched a token ahead
+    if (len > 0) tk.fetch(p, start, h, col0, tid);
     for (int t = 0; t < len; ++t) {
         const long row = start + t;
-        const size_t qk_off = ((size_t)row * (p.H / p.G) + h / p.G) * DK;   // q/k head of value head h
-        const size_t g_off = ((size_t)row * p.H + h) * DK;
         const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
-        if (tid < DK) {
-            s_k[tid] = to_f32(k[qk_off + tid]);
-            if constexpr (GK) {
-                float gv = p.gk ? p.gk[g_off + tid] : 0.f;
-                if (p.gk && p.A_log)
-                    gv = gate_decay(gv, p.A_log[h], p.dt_bias ? p.dt_bias[(size_t)h * DK + tid] : 0.f);
-                s_a[tid] = expf(gv);
-            }
-        } else if (tid < 2 * DK) {
-            s_q[tid - DK] = to_f32(q[qk_off + tid - DK]);
-        }
-        if (tid < DVS) s_v[tid] = to_f32(v[v_off + tid]);
-        if (tid == 0) {
-            s_sc[0] = beta_of(p.beta[(size_t)row * p.H + h], p.beta_sig, p.neg_eig);
-            float d = p.decay ? p.decay[(size_t)row * p.H + h] : 0.f;
-            if (p.decay && p.A_log) d = gate_decay(d, p.A_log[h], p.dt_bias ? p.dt_bias[h] : 0.f);
-            s_sc[1] = d;
-        }
+        tk.put(p, h, tid, s_k, s_q, s_a, s_v, s_sc);
+        if (t + 1 < len) tk.fetch(p, row + 1, h, col0, tid);
         __syncthreads();
 
         if (warp < 3) {  // ||k||^2, ||q||^2, k.q
@@ -148,18 +174,41 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
         const float kn = p.use_l2 ? 1.f / fmaxf(sqrtf(s_sc[2]), kNormEps) : 1.f;
         const float qn = p.scale * (p.use_l2 ? 1.f / fmaxf(sqrtf(s_sc[3]), kNormEps) : 1.f);
         const float alpha = expf(s_sc[1]);
-        if (tid < DVS) {
-            float rs = 0.f, ps = 0.f;
-#pragma unroll 8
-            for (int g = 0; g < RG; ++g) {
-                rs += s_red[0][g][tid];
-                ps += s_red[1][g][tid];
+        if constexpr (RG <= 8) {   // few row groups (whole-width slabs): one thread per column
+            if (tid < DVS) {
+                float rs = 0.f, ps = 0.f;
+#pragma unroll
+                for (int g = 0; g < RG; ++g) {
+                    rs += s_red[0][g][tid];
+                    ps += s_red[1][g][tid];
+                }
+                const float u = s_sc[0] * (s_v[tid] - kn * ((!GK && p.decayed_read) ? alpha * rs : rs));
+                const float out = (GK ? 1.f : alpha) * (qn * ps) + (kn * qn * s_sc[4]) * u;
+                s_u[tid] = u;
+                o[v_off + tid] = from_f32<Tin>(out);
             }
-            // the decayed read with one decay per head: r = (alpha S)^T k
-            const float u = s_sc[0] * (s_v[tid] - kn * ((!GK && p.decayed_read) ? alpha * rs : rs));
-            const float out = (GK ? 1.f : alpha) * (qn * ps) + (kn * qn * s_sc[4]) * u;
-            s_u[tid] = u;
-            o[v_off + tid] = from_f32<Tin>(out);
+        } else {   // sums over the RG row groups: P consecutive lanes per column, RG / P terms each
+            constexpr int P = kThreads / DVS, PER = RG / P;
+            static_assert(P * DVS == kThreads && PER * P == RG && P <= 32, "reduction split");
+            const int j = tid / P, part = tid % P;
+            float rs = 0.f, ps = 0.f;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) {
+                rs += s_red[0][part * PER + e][j];
+                ps += s_red[1][part * PER + e][j];
+            }
+#pragma unroll
+            for (int off = P / 2; off > 0; off >>= 1) {
+                rs += __shfl_xor_sync(0xffffffffu, rs, off);
+                ps += __shfl_xor_sync(0xffffffffu, ps, off);
+            }
+            if (part == 0) {
+                // the decayed read with one decay per head: r = (alpha S)^T k
+                const float u = s_sc[0] * (s_v[j] - kn * ((!GK && p.decayed_read) ? alpha * rs : rs));
+                const float out = (GK ? 1.f : alpha) * (qn * ps) + (kn * qn * s_sc[4]) * u;
+                s_u[j] = u;
+                o[v_off + j] = from_f32<Tin>(out);
+            }
         }
         __syncthreads();
 
@@ -221,9 +270,6 @@ __global__ void __launch_bounds__(kThreads) scan_vm_kernel(ScanParams p) {
     }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int col0 = slab * DVS, c0w = warp * CPW;   // the warp's first column in the slab
-    const Tin *q = static_cast<const Tin *>(p.q);
-    const Tin *k = static_cast<const Tin *>(p.k);
-    const Tin *v = static_cast<const Tin *>(p.v);
     Tin *o = static_cast<Tin *>(p.o);
 
     // S[c][e] = state(i = lane RPL + e, j = col0 + c0w + c), stored at j DK + i
@@ -246,29 +292,13 @@ __global__ void __launch_bounds__(kThreads) scan_vm_kernel(ScanParams p) {
         }
     }
 
+    TokenLoad<Tin, DK, DVS, GK> tk;   // this thread's share of the token, fetched a token ahead
+    if (len > 0) tk.fetch(p, start, h, col0, tid);
     for (int t = 0; t < len; ++t) {
         const long row = start + t;
-        const size_t qk_off = ((size_t)row * (p.H / p.G) + h / p.G) * DK;
-        const size_t g_off = ((size_t)row * p.H + h) * DK;
         const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
-        if (tid < DK) {
-            s_k[tid] = to_f32(k[qk_off + tid]);
-            if constexpr (GK) {
-                float gv = p.gk ? p.gk[g_off + tid] : 0.f;
-                if (p.gk && p.A_log)
-                    gv = gate_decay(gv, p.A_log[h], p.dt_bias ? p.dt_bias[(size_t)h * DK + tid] : 0.f);
-                s_a[tid] = expf(gv);
-            }
-        } else if (tid < 2 * DK) {
-            s_q[tid - DK] = to_f32(q[qk_off + tid - DK]);
-        }
-        if (tid < DVS) s_v[tid] = to_f32(v[v_off + tid]);
-        if (tid == 0) {
-            s_sc[0] = beta_of(p.beta[(size_t)row * p.H + h], p.beta_sig, p.neg_eig);
-            float d = p.decay ? p.decay[(size_t)row * p.H + h] : 0.f;
-            if (p.decay && p.A_log) d = gate_decay(d, p.A_log[h], p.dt_bias ? p.dt_bias[h] : 0.f);
-            s_sc[1] = d;
-        }
+        tk.put(p, h, tid, s_k, s_q, s_a, s_v, s_sc);
+        if (t + 1 < len) tk.fetch(p, row + 1, h, col0, tid);
         __syncthreads();
         if (warp < 3) {  // ||k||^2, ||q||^2, k.q
             float acc = 0.f;
