@@ -506,7 +506,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // other than 0 (the MMA issuer) and 4 (the store thread, whose flag release would wait for
 // loads in flight).  These go through the load path, not the TMA unit, where they would
 // queue behind the E_c stores.  Rows past the token array are filled with zeros.
-template <int D>
+template <int D, bool OPT>
 __device__ __forceinline__ void load_rows(const TcParams &p, uint8_t *sKQ, const ChunkItem &it,
                                           int tid, bool q) {
     constexpr int PPR = D / 8;                               // 16-byte pieces per row
@@ -518,7 +518,8 @@ __device__ __forceinline__ void load_rows(const TcParams &p, uint8_t *sKQ, const
         const int row = pidx / PPR, pc = pidx % PPR;
         const long grow = it.row0 + row;
         const bool in = grow < p.rows;
-        const __nv_bfloat16 *src = g + ((in ? grow : 0) * (p.H / p.G) + it.h / p.G) * D + 8 * pc;
+        const int G = OPT ? p.G : 1;   // value heads per q/k head
+        const __nv_bfloat16 *src = g + ((in ? grow : 0) * (p.H / G) + it.h / G) * D + 8 * pc;
         uint8_t *dst = sKQ + (pc >> 3) * 16384 + (q ? 8192 : 0) + row * 128 + (((pc & 7) ^ (row & 7)) << 4);
         cp_async16(dst, src, in ? 16u : 0u);
     }
@@ -527,6 +528,7 @@ __device__ __forceinline__ void load_rows(const TcParams &p, uint8_t *sKQ, const
 // beta, decay of one chunk into the per-token scalars (zero past the chunk's valid tokens;
 // decay zero when absent); with a raw-gate decay also A_log and dt_bias of the head, so that
 // no global load sits on the prefix's path
+template <bool OPT>
 __device__ __forceinline__ void load_scalars(const TcParams &p, float *mbeta, float *mdec, float *gate,
                                              const ChunkItem &it, int tid) {
     const int t = tid - 64;   // warps 2, 3
@@ -534,7 +536,7 @@ __device__ __forceinline__ void load_scalars(const TcParams &p, float *mbeta, fl
         const long gi = (it.row0 + (t < it.nv ? t : 0)) * p.H + it.h;
         cp_async4(mbeta + t, p.beta + gi, t < it.nv ? 4u : 0u);
         cp_async4(mdec + t, p.decay ? p.decay + gi : p.beta + gi, (t < it.nv && p.decay) ? 4u : 0u);
-        if (p.A_log && t < 2) {
+        if (OPT && p.A_log && t < 2) {
             const float *src = t == 0 ? p.A_log + it.h : (p.dt_bias ? p.dt_bias + it.h : p.A_log);
             cp_async4(gate + t, src, (t == 0 || p.dt_bias) ? 4u : 0u);
         }
@@ -559,7 +561,9 @@ constexpr int kStaggerBar = 3;
 // from a raw gate: warps 1 and 2 transform it, warp 0 then takes the prefix.
 constexpr int kGateBarOffset = 3;
 
-template <int D>
+// OPT: the kda_options code paths (decayed read, gate and beta prologues, grouped heads);
+// the plain instantiation compiles them out.
+template <int D, bool OPT>
 __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUtensorMap *map_k,
                                            const CUtensorMap *map_E, const TcParams &p,
                                            uint8_t *sm, uint32_t tm, int tid, int bar, long item,
@@ -603,20 +607,24 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         if (lead) named_arrive(kStaggerBar, 2 * kGroupThreads);
         return;
     }
-    load_rows<D>(p, sKQ, cur, tid, true);
-    load_rows<D>(p, sKQ, cur, tid, false);
-    load_scalars(p, mbeta, mdec, ctl->gate, cur, tid);
+    load_rows<D, OPT>(p, sKQ, cur, tid, true);
+    load_rows<D, OPT>(p, sKQ, cur, tid, false);
+    load_scalars<OPT>(p, mbeta, mdec, ctl->gate, cur, tid);
     long pend = -1;     // store thread: slot whose stores are in flight and not yet published
     long staged = -1;   // store thread: slot whose state-column blocks wait in the staging area
 
     for (uint32_t it = 0;; ++it) {
         const uint32_t ph = it & 1;   // bar_mma completes three times per chunk
         const int nv = cur.nv;
-        const bool gated = p.A_log && p.decay;   // decay holds the raw gate
+        const bool gated = OPT && p.A_log && p.decay;   // decay holds the raw gate
         cp_async_wait_all();   // this thread's share of q, k, beta, decay ...
         fence_proxy_async();   // ... visible to the tensor core behind the barrier
         named_sync(bar, kGroupThreads);
         bool ok = ctl->fail == 0;
+        long nitem = item + stride;   // this group's next chunk
+        ChunkItem nx;
+        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
+        const bool more = nitem < p.n_items;
         if (tid == kStoreThread && staged >= 0) {   // the previous chunk's state-column blocks of E_c
             for (int kb = 0; kb < NB; ++kb)
                 tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
@@ -656,7 +664,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             mGp[2 * lane + 1] = excl + d0;
             mG[2 * lane + 1] = incl;
         }
-        if (warp == 3 && p.beta_sig) {   // beta from logits (zero past the valid tokens)
+        if (OPT && warp == 3 && p.beta_sig) {   // beta from logits (zero past the valid tokens)
             mbeta[2 * lane] = 2 * lane < nv ? beta_of(mbeta[2 * lane], 1, p.neg_eig) : 0.f;
             mbeta[2 * lane + 1] = 2 * lane + 1 < nv ? beta_of(mbeta[2 * lane + 1], 1, p.neg_eig) : 0.f;
         }
@@ -682,11 +690,6 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         }
         named_sync(bar, kGroupThreads);   // the log-decay prefix is in place
         if (tid < 64) meg[tid] = __expf(mG[tid]);
-        // this group's next chunk (packed sequences read cu_seqlens here: off the path to MMA1)
-        long nitem = item + stride;
-        ChunkItem nx;
-        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
-        const bool more = nitem < p.n_items;
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
 
@@ -710,7 +713,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             if (i128 < 64) {
                 const int t = i128;
                 // R_t: G_{t-1} when the delta term reads h_{t-1}, G_t when it reads the decayed memory
-                const float kt = mkn[t], bt = mbeta[t], gpt = p.decayed_read ? mG[t] : mGp[t];
+                const float kt = mkn[t], bt = mbeta[t], gpt = (OPT && p.decayed_read) ? mG[t] : mGp[t];
                 if (hh == 0) {
                     mf[t] = t < nv ? __expf(gC - mG[t]) * kt : 0.f;
                     mcw[t] = bt * __expf(gpt) * kt;   // column weight of T' = T diag(beta e^{G_{s-1}} kn)
@@ -869,9 +872,9 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         // [K;Q] is free once MMA3 has read it, beta and decay after the inverse: the next
         // chunk's load starts now
         if (ok && more) {
-            load_rows<D>(p, sKQ, nx, tid, true);
-            load_rows<D>(p, sKQ, nx, tid, false);
-            load_scalars(p, mbeta, mdec, ctl->gate, nx, tid);
+            load_rows<D, OPT>(p, sKQ, nx, tid, true);
+            load_rows<D, OPT>(p, sKQ, nx, tid, false);
+            load_scalars<OPT>(p, mbeta, mdec, ctl->gate, nx, tid);
         }
 
         // ---- epilogue 3: the state columns of E; column half hh covers [hh D/2, (hh+1) D/2)
@@ -1075,8 +1078,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
     using Ly = GkSmem<D>;
     constexpr int NT = kGkThreads;
     constexpr int NB = D / 64;
-    constexpr int R = D + 64;
-    constexpr int NP = D / 2;                 // channel pairs
+        constexpr int NP = D / 2;                 // channel pairs
     constexpr int NQ = NT / NP;               // token groups of the prefix and the build
     constexpr int TPG = 64 / NQ;              // their tokens: 8 (D = 128) or 4 (D = 64)
     static_assert(TPG <= 16 && 16 % TPG == 0, "a token group stays inside one 16-token sub-block");
@@ -1113,8 +1115,8 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
     while (item < p.n_items && !item_info(p, item, cur)) item += stride;
     if (item >= p.n_items) return;
     if (loader) {
-        load_rows<D>(p, sKQ, cur, tid, true);
-        load_rows<D>(p, sKQ, cur, tid, false);
+        load_rows<D, true>(p, sKQ, cur, tid, true);
+        load_rows<D, true>(p, sKQ, cur, tid, false);
         load_g<D>(p, gf, cur, tid);
         load_beta(p, mbeta2, cur, tid);
         load_gate<D>(p, mgate, cur, tid);
@@ -1328,8 +1330,8 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         const bool more = nitem < p.n_items;
         float *mbeta_next = mbeta2 + 64 * ((it + 1) & 1);
         if (ok && more && loader) {
-            load_rows<D>(p, sKQ, nx, tid, true);
-            load_rows<D>(p, sKQ, nx, tid, false);
+            load_rows<D, true>(p, sKQ, nx, tid, true);
+            load_rows<D, true>(p, sKQ, nx, tid, false);
             load_g<D>(p, gf, nx, tid);
             load_beta(p, mbeta_next, nx, tid);
             load_gate<D>(p, mgate, nx, tid);
@@ -1528,7 +1530,7 @@ struct ChainCfg {
     static constexpr int THREADS = 448;           // producer, MMA, 8 state + 4 output warps
 };
 
-template <int D>
+template <int D, bool OPT>
 __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUtensorMap *map_v,
                                            const TcParams &p, uint8_t *sm, int task,
                                            bool wait_flags) {
@@ -1676,7 +1678,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
         const int i_lo = ch * HALF;
 
         // element (i, j) of a state: key-major at i D + j, value-major at j D + i
-        const size_t si = p.v_first ? 1 : D, sj = p.v_first ? D : 1;
+        const bool vf = OPT && p.v_first;
+        const size_t si = vf ? 1 : D, sj = vf ? D : 1;
         if (has_row) {   // S_0^T row j from initial_state[:, j]
             for (int i0 = i_lo; i0 < i_lo + HALF; i0 += 8) {
                 float x[8];
@@ -1723,9 +1726,18 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                                                    (((gc & 7) ^ (j & 7)) << 4)) = pack8u(v + 8 * cc);
                     }
                 } else if (p.hT) {
+                    if (vf) {   // value-major: row j of the state is contiguous
+                        float *dst = p.hT + hbase + (size_t)j * D + i_lo;
 #pragma unroll
-                    for (int i = 0; i < HALF; ++i)
-                        p.hT[hbase + (size_t)(i_lo + i) * si + j * sj] = __uint_as_float(v[i]);
+                        for (int i = 0; i < HALF; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) =
+                                make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                            __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < HALF; ++i)
+                            p.hT[hbase + (size_t)(i_lo + i) * D + j] = __uint_as_float(v[i]);
+                    }
                 }
             }
             if (!last) fence_proxy_async();
@@ -1792,7 +1804,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
 // others two prep groups each.  With nchain > 0 the launch is cooperative, so that
 // every chain's producers are co-resident with the prep groups they wait for.
 // ---------------------------------------------------------------------------------
-template <int D, bool GK>
+template <int D, bool GK, bool OPT>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant__ CUtensorMap map_q,
                                                            const __grid_constant__ CUtensorMap map_k,
                                                            const __grid_constant__ CUtensorMap map_v,
@@ -1802,7 +1814,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     if ((int)blockIdx.x < p.nchain) {
-        chain_body<D>(&map_E, &map_v, p, sm, (int)blockIdx.x, p.flags != nullptr);
+        chain_body<D, OPT>(&map_E, &map_v, p, sm, (int)blockIdx.x, p.flags != nullptr);
         return;
     }
     __shared__ uint32_t tmem_base;
@@ -1848,7 +1860,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     const long gidx = (long)((int)blockIdx.x - p.nchain) * 2 + grp;
     const long ngroups = (long)((int)gridDim.x - p.nchain) * 2;
     const bool stagger = p.n_items >= 16 * ngroups;   // long runs only: the offset costs a start-up delay
-    prep_group<D>(&map_q, &map_k, &map_E, p, gsm, tmem_base + (uint32_t)(grp * 256),
+    prep_group<D, OPT>(&map_q, &map_k, &map_E, p, gsm, tmem_base + (uint32_t)(grp * 256),
                   tid & (kGroupThreads - 1), 1 + grp, gidx, ngroups, stagger);
     tc_fence_before();
     __syncthreads();
@@ -1858,12 +1870,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     }
 }
 
-template <int D>
+template <int D, bool OPT>
 __global__ void __launch_bounds__(ChainCfg<D>::THREADS, 1) chain_kernel(const __grid_constant__ CUtensorMap map_E,
                                                                         const __grid_constant__ CUtensorMap map_v,
                                                                         TcParams p) {
     extern __shared__ uint8_t smem_raw[];
-    chain_body<D>(&map_E, &map_v, p, align1024(smem_raw), (int)blockIdx.x, false);
+    chain_body<D, OPT>(&map_E, &map_v, p, align1024(smem_raw), (int)blockIdx.x, false);
 }
 
 // Failure-detection probe: the two bounded waits of the kernels above, run against events
@@ -1941,7 +1953,8 @@ bool map_E_tiles(CUtensorMap *m, const void *base, long slots, int R) {
 constexpr size_t kTableBytes(int nseq) { return (((size_t)(nseq + 1) * 4 + 255) / 256) * 256; }
 constexpr size_t kFlagBytes(long slots) { return (((size_t)slots * 4 + 255) / 256) * 256; }
 
-template <int D, bool GK>
+// OPT: the kda_options paths (the per-channel kernels always take them)
+template <int D, bool GK, bool OPT>
 cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
     constexpr int R = D + 64;
     using Cf = ChainCfg<D>;
@@ -1985,7 +1998,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int prep_smem = GK ? GkSmem<D>::BYTES + 1024 : 2 * PrepSmem<D>::GROUP + 1024;
     const int one_smem = std::max(prep_smem, Cf::SMEM);
-    e = cudaFuncSetAttribute(tc_kernel<D, GK>, cudaFuncAttributeMaxDynamicSharedMemorySize, one_smem);
+    e = cudaFuncSetAttribute(tc_kernel<D, GK, OPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, one_smem);
     if (e != cudaSuccess) return e;
 
     // Single launch when the chains take at most half of the SMs: chains and prep
@@ -2007,7 +2020,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc_kernel<D, GK>, mq, mk, mv, me, mew, pf);
+        e = cudaLaunchKernelEx(&cfg, tc_kernel<D, GK, OPT>, mq, mk, mv, me, mew, pf);
         if (e == cudaSuccess) return cudaSuccess;
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         (void)cudaGetLastError();   // fewer SMs available than reported: two launches
@@ -2019,12 +2032,12 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.n_items = slots_bound;
     p.nchain = 0;
     const long ctas = std::min<long>(GK ? slots_bound : (slots_bound + 1) / 2, (long)nsm);
-    tc_kernel<D, GK><<<(unsigned)ctas, kTcThreads, prep_smem, st>>>(mq, mk, mv, me, mew, p);
+    tc_kernel<D, GK, OPT><<<(unsigned)ctas, kTcThreads, prep_smem, st>>>(mq, mk, mv, me, mew, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chain_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    e = cudaFuncSetAttribute(chain_kernel<D, OPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (e != cudaSuccess) return e;
-    chain_kernel<D><<<(unsigned)p.nsh, Cf::THREADS, Cf::SMEM, st>>>(me, mv, p);
+    chain_kernel<D, OPT><<<(unsigned)p.nsh, Cf::THREADS, Cf::SMEM, st>>>(me, mv, p);
     return cudaGetLastError();
 }
 
@@ -2057,12 +2070,17 @@ cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t s
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
     if (slots_bound >= (1L << 31) || total_rows >= (1L << 31)) return cudaErrorInvalidValue;   // 32-bit indexing
     if (a.per_channel) {
-        if (a.dk == 128) return run_tc<128, true>(a, total_rows, slots_bound, st);
-        if (a.dk == 64) return run_tc<64, true>(a, total_rows, slots_bound, st);
+        if (a.dk == 128) return run_tc<128, true, true>(a, total_rows, slots_bound, st);
+        if (a.dk == 64) return run_tc<64, true, true>(a, total_rows, slots_bound, st);
         return cudaErrorInvalidValue;
     }
-    if (a.dk == 128) return run_tc<128, false>(a, total_rows, slots_bound, st);
-    if (a.dk == 64) return run_tc<64, false>(a, total_rows, slots_bound, st);
+    const bool opt = a.decayed_read || a.A_log || a.beta_sig || a.G > 1 || a.v_first;
+    if (a.dk == 128)
+        return opt ? run_tc<128, false, true>(a, total_rows, slots_bound, st)
+                   : run_tc<128, false, false>(a, total_rows, slots_bound, st);
+    if (a.dk == 64)
+        return opt ? run_tc<64, false, true>(a, total_rows, slots_bound, st)
+                   : run_tc<64, false, false>(a, total_rows, slots_bound, st);
     return cudaErrorInvalidValue;
 }
 
