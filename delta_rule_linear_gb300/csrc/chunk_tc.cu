@@ -1072,7 +1072,8 @@ constexpr int kGkThreads = 512;   // the whole CTA: one prep group
 constexpr int kGkBarInv = 2;      // named barrier of the inverse (threads 0..255)
 constexpr int kGkBarPark = 3;     // threads 256..511 wait there while the inverse runs
 
-template <int D>
+// OPT: the gate and beta prologues and grouped heads (the decayed read is always a runtime choice)
+template <int D, bool OPT>
 __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const TcParams &p, uint8_t *sm,
                                               uint32_t tm, int tid, int bar, long item, long stride) {
     using Ly = GkSmem<D>;
@@ -1115,11 +1116,11 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
     while (item < p.n_items && !item_info(p, item, cur)) item += stride;
     if (item >= p.n_items) return;
     if (loader) {
-        load_rows<D, true>(p, sKQ, cur, tid, true);
-        load_rows<D, true>(p, sKQ, cur, tid, false);
+        load_rows<D, OPT>(p, sKQ, cur, tid, true);
+        load_rows<D, OPT>(p, sKQ, cur, tid, false);
         load_g<D>(p, gf, cur, tid);
         load_beta(p, mbeta2, cur, tid);
-        load_gate<D>(p, mgate, cur, tid);
+        if (OPT) load_gate<D>(p, mgate, cur, tid);
     }
     long pend = -1;   // kStoreThread: slot whose E_c stores are issued and not yet published
     const bool decayed = p.decayed_read != 0;
@@ -1129,7 +1130,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         const int nv = cur.nv;
         float *mbeta = mbeta2 + 64 * (it & 1);
         if (tid < 4) mspan[tid] = 0;
-        const bool gate = p.A_log != nullptr;   // g holds the raw gate
+        const bool gate = OPT && p.A_log != nullptr;   // g holds the raw gate
         cp_async_wait_all();
         if (lane == 0) bulk_wait0();   // the previous chunk's E_c stores: complete, staging free
         named_sync(bar, NT);
@@ -1160,7 +1161,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
                 if (isq) mqn[t] = t < nv ? p.scale * inv : 0.f;
                 else mkn[t] = t < nv ? inv : 0.f;
             }
-            if (p.beta_sig && tid >= 448)   // beta from logits (zero past the valid tokens)
+            if (OPT && p.beta_sig && tid >= 448)   // beta from logits (zero past the valid tokens)
                 mbeta[tid - 448] = tid - 448 < nv ? beta_of(mbeta[tid - 448], 1, p.neg_eig) : 0.f;
         }
         {   // pass A: each token group's inclusive prefix in place (a channel pair per thread),
@@ -1330,11 +1331,11 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         const bool more = nitem < p.n_items;
         float *mbeta_next = mbeta2 + 64 * ((it + 1) & 1);
         if (ok && more && loader) {
-            load_rows<D, true>(p, sKQ, nx, tid, true);
-            load_rows<D, true>(p, sKQ, nx, tid, false);
+            load_rows<D, OPT>(p, sKQ, nx, tid, true);
+            load_rows<D, OPT>(p, sKQ, nx, tid, false);
             load_g<D>(p, gf, nx, tid);
             load_beta(p, mbeta_next, nx, tid);
-            load_gate<D>(p, mgate, nx, tid);
+            if (OPT) load_gate<D>(p, mgate, nx, tid);
         }
 
         if (tid == kStoreThread && pend >= 0) {   // the previous chunk's E_c, while MMA1 runs
@@ -1833,7 +1834,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        prep_group_gk<D>(&map_Ew, p, sm, tmem_base, tid, 1, (long)((int)blockIdx.x - p.nchain),
+        prep_group_gk<D, OPT>(&map_Ew, p, sm, tmem_base, tid, 1, (long)((int)blockIdx.x - p.nchain),
                          (long)((int)gridDim.x - p.nchain));
         tc_fence_before();
         __syncthreads();
@@ -1953,7 +1954,7 @@ bool map_E_tiles(CUtensorMap *m, const void *base, long slots, int R) {
 constexpr size_t kTableBytes(int nseq) { return (((size_t)(nseq + 1) * 4 + 255) / 256) * 256; }
 constexpr size_t kFlagBytes(long slots) { return (((size_t)slots * 4 + 255) / 256) * 256; }
 
-// OPT: the kda_options paths (the per-channel kernels always take them)
+// OPT: the kda_options paths, compiled out of the plain instantiations
 template <int D, bool GK, bool OPT>
 cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
     constexpr int R = D + 64;
@@ -2069,9 +2070,14 @@ cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t s
 
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
     if (slots_bound >= (1L << 31) || total_rows >= (1L << 31)) return cudaErrorInvalidValue;   // 32-bit indexing
-    if (a.per_channel) {
-        if (a.dk == 128) return run_tc<128, true, true>(a, total_rows, slots_bound, st);
-        if (a.dk == 64) return run_tc<64, true, true>(a, total_rows, slots_bound, st);
+    if (a.per_channel) {   // the decayed read is a runtime choice of the per-channel prep
+        const bool gopt = a.A_log || a.beta_sig || a.G > 1 || a.v_first;
+        if (a.dk == 128)
+            return gopt ? run_tc<128, true, true>(a, total_rows, slots_bound, st)
+                        : run_tc<128, true, false>(a, total_rows, slots_bound, st);
+        if (a.dk == 64)
+            return gopt ? run_tc<64, true, true>(a, total_rows, slots_bound, st)
+                        : run_tc<64, true, false>(a, total_rows, slots_bound, st);
         return cudaErrorInvalidValue;
     }
     const bool opt = a.decayed_read || a.A_log || a.beta_sig || a.G > 1 || a.v_first;

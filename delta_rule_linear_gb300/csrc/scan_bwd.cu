@@ -18,6 +18,8 @@
 // columns (everything above is separable in j except the sums over j, which go to fp32
 // accumulators by atomic adds).  A last kernel turns the gradients of k^ and q~ into those
 // of the raw k and q (through the L2 normalisation and the scale).
+#include <cstddef>
+
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -25,7 +27,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kBwdChunk = 32;   // tokens between stored states
-constexpr int kSlab = 64;       // value columns per CTA
+constexpr int kSlab = 64;       // value columns per CTA (32 when that leaves SMs idle)
 
 struct BwdParams {
     const void *q, *k, *v, *dout;
@@ -44,56 +46,169 @@ struct BwdLayout {
     static constexpr int RG = kThreads / TPR;    // row groups
 };
 
-// Token staging shared by both passes: k^, q~, exp(g) per key row, beta, v (and do) of the
-// slab, and the norms.  Returns nothing; fills the shared arrays and syncs twice.
+// One token's inputs as this thread fetches them (raw, so the loads stay in flight until the
+// token is staged): k (threads [0, DK)) or q (threads [DK, 2 DK)) of one key channel, the
+// channel's log decay, v and do of one value column (threads [0, DVS)), beta (thread 0).
+template <typename Tin>
+struct TokenRegs {
+    Tin x, v, d;
+    float g, beta;
+};
+
+// The staged token: raw k, q, exp(g) per key row, v, do of the slab, beta, and per-warp sums
+// of k^2 and q^2 (the norms are finished by each thread from these).
+// Aligned so that both buffers of a stage array keep the 16-byte alignment of `d` (read as
+// float4).
+template <int DK, int DVS>
+struct __align__(16) Stage {
+    float k[DK], q[DK], a[DK], v[DVS], d[DVS];
+    float nk[DK / 32], nq[DK / 32];
+    float beta;
+};
+template <int DK, int DVS>
+constexpr bool stage_aligned() {
+    using S = Stage<DK, DVS>;
+    return sizeof(S) % 16 == 0 && offsetof(S, d) % 16 == 0;
+}
+
 template <typename Tin, int DK, int DVS>
-__device__ __forceinline__ void stage_token(const BwdParams &p, long row, int h, int col0, bool with_do,
-                                            float *s_k, float *s_q, float *s_a, float *s_v, float *s_do,
-                                            float *s_sc) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const Tin *q = static_cast<const Tin *>(p.q);
-    const Tin *k = static_cast<const Tin *>(p.k);
-    const Tin *v = static_cast<const Tin *>(p.v);
-    const Tin *dout = static_cast<const Tin *>(p.dout);
+__device__ __forceinline__ void fetch_token(const BwdParams &p, long row, int h, int col0, bool with_do,
+                                            TokenRegs<Tin> &r) {
+    const int tid = threadIdx.x;
     const size_t qk_off = ((size_t)row * p.H + h) * DK;
     const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
     if (tid < DK) {
-        s_k[tid] = to_f32(k[qk_off + tid]);
-        s_a[tid] = p.gk ? expf(p.gk[qk_off + tid]) : 1.f;
+        r.x = static_cast<const Tin *>(p.k)[qk_off + tid];
+        r.g = p.gk ? p.gk[qk_off + tid] : 0.f;
     } else if (tid < 2 * DK) {
-        s_q[tid - DK] = to_f32(q[qk_off + tid - DK]);
+        r.x = static_cast<const Tin *>(p.q)[qk_off + tid - DK];
     }
     if (tid < DVS) {
-        s_v[tid] = to_f32(v[v_off + tid]);
-        if (with_do) s_do[tid] = to_f32(dout[v_off + tid]);
+        r.v = static_cast<const Tin *>(p.v)[v_off + tid];
+        if (with_do) r.d = static_cast<const Tin *>(p.dout)[v_off + tid];
     }
-    if (tid == 0) s_sc[0] = p.beta[(size_t)row * p.H + h];
-    __syncthreads();
-    if (warp < 2) {   // ||k||^2, ||q||^2
-        const float *x = warp == 0 ? s_k : s_q;
-        float acc = 0.f;
-        for (int i = lane; i < DK; i += 32) acc = fmaf(x[i], x[i], acc);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) s_sc[1 + warp] = acc;
-    }
-    __syncthreads();
-    // normalise in place (each thread its own entry, read by everyone after the next sync)
-    const float kn = p.use_l2 ? 1.f / fmaxf(sqrtf(s_sc[1]), kNormEps) : 1.f;
-    const float qn = p.scale * (p.use_l2 ? 1.f / fmaxf(sqrtf(s_sc[2]), kNormEps) : 1.f);
-    if (tid < DK) s_k[tid] *= kn;
-    else if (tid < 2 * DK) s_q[tid - DK] *= qn;
-    __syncthreads();
+    if (tid == 0) r.beta = p.beta[(size_t)row * p.H + h];
 }
 
-// Forward pass: the state before every chunk, per (sequence, head, slab).
+// Registers -> stage (the caller syncs before anyone reads it).
+template <typename Tin, int DK, int DVS>
+__device__ __forceinline__ void put_token(const BwdParams &p, const TokenRegs<Tin> &r, bool with_do,
+                                          Stage<DK, DVS> &s) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < 2 * DK) {   // whole warps
+        const float x = to_f32(r.x);
+        float sq = x * x;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        if (tid < DK) {
+            s.k[tid] = x;
+            s.a[tid] = p.gk ? expf(r.g) : 1.f;
+            if (lane == 0) s.nk[warp] = sq;
+        } else {
+            s.q[tid - DK] = x;
+            if (lane == 0) s.nq[warp - DK / 32] = sq;
+        }
+    }
+    if (tid < DVS) {
+        s.v[tid] = to_f32(r.v);
+        if (with_do) s.d[tid] = to_f32(r.d);
+    }
+    if (tid == 0) s.beta = r.beta;
+}
+
+// The normalisation factors of the staged token: k^ = kn k, q~ = qn q.
+template <int DK, int DVS>
+__device__ __forceinline__ void token_norms(const BwdParams &p, const Stage<DK, DVS> &s, float &kn, float &qn) {
+    float nk = 0.f, nq = 0.f;
+#pragma unroll
+    for (int w = 0; w < DK / 32; ++w) {
+        nk += s.nk[w];
+        nq += s.nq[w];
+    }
+    kn = p.use_l2 ? 1.f / fmaxf(sqrtf(nk), kNormEps) : 1.f;
+    qn = p.scale * (p.use_l2 ? 1.f / fmaxf(sqrtf(nq), kNormEps) : 1.f);
+}
+
+// Sums over the RG row groups of one or two [RG][DVS] partial arrays.  Column j's sums land
+// in its owner thread (returns true there): the first DVS threads with few row groups, else
+// P = kThreads / DVS consecutive lanes per column that each add RG / P terms and shuffle.
+template <int DVS, int RG, bool TWO>
+__device__ __forceinline__ bool column_sums(const float (*a)[DVS], const float (*b)[DVS], int tid, int &j,
+                                            float &sa, float &sb) {
+    sa = 0.f;
+    sb = 0.f;
+    if constexpr (RG <= 8) {
+        j = tid;
+        if (tid >= DVS) return false;
+#pragma unroll
+        for (int g = 0; g < RG; ++g) {
+            sa += a[g][tid];
+            if (TWO) sb += b[g][tid];
+        }
+        return true;
+    } else {
+        constexpr int P = kThreads / DVS, PER = RG / P;
+        static_assert(P * DVS == kThreads && PER * P == RG && P <= 32, "reduction split");
+        const int part = tid % P;
+        j = tid / P;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            sa += a[part * PER + e][j];
+            if (TWO) sb += b[part * PER + e][j];
+        }
+#pragma unroll
+        for (int off = P / 2; off > 0; off >>= 1) {
+            sa += __shfl_xor_sync(0xffffffffu, sa, off);
+            if (TWO) sb += __shfl_xor_sync(0xffffffffu, sb, off);
+        }
+        return part == 0;
+    }
+}
+
+// One token of the forward recurrence on this thread's rows of the slab (S: the state before
+// the token on entry, after it on return).  The stage was synced by the caller; two syncs.
+template <int DK, int DVS, int RG, int R>
+__device__ __forceinline__ void forward_token(const BwdParams &p, const Stage<DK, DVS> &s, float4 (&S)[R],
+                                              float (*s_red)[DVS], float *s_u) {
+    const int tid = threadIdx.x, cg = tid % (DVS / 4), rg = tid / (DVS / 4);
+    float kn, qn;
+    token_norms(p, s, kn, qn);
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int i = rg + RG * m;
+        const float kk = s.k[i] * kn, kx = p.decayed_read ? s.a[i] * kk : kk;
+        r.x = fmaf(S[m].x, kx, r.x); r.y = fmaf(S[m].y, kx, r.y);
+        r.z = fmaf(S[m].z, kx, r.z); r.w = fmaf(S[m].w, kx, r.w);
+    }
+    *reinterpret_cast<float4 *>(&s_red[rg][4 * cg]) = r;
+    __syncthreads();
+    {
+        int j;
+        float rs, unused;
+        if (column_sums<DVS, RG, false>(s_red, s_red, tid, j, rs, unused)) s_u[j] = s.beta * (s.v[j] - rs);
+    }
+    __syncthreads();
+    const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int i = rg + RG * m;
+        const float a = s.a[i], kk = s.k[i] * kn;
+        S[m].x = fmaf(a, S[m].x, kk * u4.x); S[m].y = fmaf(a, S[m].y, kk * u4.y);
+        S[m].z = fmaf(a, S[m].z, kk * u4.z); S[m].w = fmaf(a, S[m].w, kk * u4.w);
+    }
+}
+
+// Forward pass: the state before every chunk, per (sequence, head, slab).  Each token's
+// inputs are fetched one token ahead; the stage is double-buffered, so three syncs a token.
 template <typename Tin, int DK, int DVS>
 __global__ void __launch_bounds__(kThreads) bwd_ckpt_kernel(BwdParams p) {
     using Ly = BwdLayout<DVS>;
     constexpr int TPR = Ly::TPR, RG = Ly::RG, R = DK / RG;
-    __shared__ __align__(16) float s_k[DK], s_q[DK], s_a[DK], s_v[DVS], s_do[DVS];
+    static_assert(stage_aligned<DK, DVS>(), "both stage buffers 16-byte aligned");
+    __shared__ __align__(16) Stage<DK, DVS> st[2];
     __shared__ __align__(16) float s_red[RG][DVS];
-    __shared__ float s_u[DVS], s_sc[8];
+    __shared__ __align__(16) float s_u[DVS];
     const int nslab = p.DV / DVS;
     const int slab = blockIdx.x % nslab, h = (blockIdx.x / nslab) % p.H, n = blockIdx.x / (nslab * p.H);
     const int tid = threadIdx.x, cg = tid % TPR, rg = tid / TPR, col0 = slab * DVS;
@@ -103,38 +218,20 @@ __global__ void __launch_bounds__(kThreads) bwd_ckpt_kernel(BwdParams p) {
     for (int m = 0; m < R; ++m)
         S[m] = p.h0 ? *reinterpret_cast<const float4 *>(p.h0 + sb + (size_t)(rg + RG * m) * p.DV)
                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    TokenRegs<Tin> cur{}, nxt{};
+    if (p.T > 0) fetch_token<Tin, DK, DVS>(p, (long)n * p.T, h, col0, false, cur);
     for (int t = 0; t < p.T; ++t) {
         if (t % kBwdChunk == 0) {   // the state before chunk t / kBwdChunk
             float *dst = p.ckpt + (((size_t)n * p.H + h) * p.nc + t / kBwdChunk) * DK * p.DV + col0 + 4 * cg;
 #pragma unroll
             for (int m = 0; m < R; ++m) *reinterpret_cast<float4 *>(dst + (size_t)(rg + RG * m) * p.DV) = S[m];
         }
-        stage_token<Tin, DK, DVS>(p, (long)n * p.T + t, h, col0, false, s_k, s_q, s_a, s_v, s_do, s_sc);
-        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int m = 0; m < R; ++m) {
-            const int i = rg + RG * m;
-            const float kx = p.decayed_read ? s_a[i] * s_k[i] : s_k[i];
-            r.x = fmaf(S[m].x, kx, r.x); r.y = fmaf(S[m].y, kx, r.y);
-            r.z = fmaf(S[m].z, kx, r.z); r.w = fmaf(S[m].w, kx, r.w);
-        }
-        *reinterpret_cast<float4 *>(&s_red[rg][4 * cg]) = r;
+        Stage<DK, DVS> &s = st[t & 1];
+        put_token<Tin, DK, DVS>(p, cur, false, s);
         __syncthreads();
-        if (tid < DVS) {
-            float rs = 0.f;
-            for (int g2 = 0; g2 < RG; ++g2) rs += s_red[g2][tid];
-            s_u[tid] = s_sc[0] * (s_v[tid] - rs);
-        }
-        __syncthreads();
-        const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
-#pragma unroll
-        for (int m = 0; m < R; ++m) {
-            const int i = rg + RG * m;
-            const float a = s_a[i], kk = s_k[i];
-            S[m].x = fmaf(a, S[m].x, kk * u4.x); S[m].y = fmaf(a, S[m].y, kk * u4.y);
-            S[m].z = fmaf(a, S[m].z, kk * u4.z); S[m].w = fmaf(a, S[m].w, kk * u4.w);
-        }
-        __syncthreads();
+        if (t + 1 < p.T) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + 1, h, col0, false, nxt);
+        forward_token<DK, DVS, RG, R>(p, s, S, s_red, s_u);
+        cur = nxt;
     }
 }
 
@@ -149,16 +246,20 @@ __device__ __forceinline__ float row_sum(float x) {
     return x;
 }
 
-// Backward pass, per (sequence, head, slab).
+// Backward pass, per (sequence, head, slab).  Inputs fetched one token ahead (forwards in the
+// recomputation, backwards in the walk) into a double-buffered stage, as in the forward pass.
 template <typename Tin, int DK, int DVS>
 __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
     using Ly = BwdLayout<DVS>;
     constexpr int TPR = Ly::TPR, RG = Ly::RG, R = DK / RG;
     static_assert(TPR <= 32 && 32 % TPR == 0, "a state row lies within one warp");
-    __shared__ __align__(16) float s_k[DK], s_q[DK], s_a[DK], s_v[DVS], s_do[DVS];
+    constexpr int kOwnerWarps = RG <= 8 ? (DVS + 31) / 32 : kThreads / 32;   // warps holding column sums
+    static_assert(stage_aligned<DK, DVS>(), "both stage buffers 16-byte aligned");
+    __shared__ __align__(16) Stage<DK, DVS> st[2];
     __shared__ __align__(16) float s_red[2][RG][DVS];
-    __shared__ __align__(16) float s_u[DVS], s_du[DVS];
-    __shared__ float s_sc[8], s_db[kThreads / 32];
+    __shared__ __align__(16) float s_u[DVS];
+    __shared__ __align__(16) float s_du[DVS];
+    __shared__ float s_db[kThreads / 32];
     const int nslab = p.DV / DVS;
     const int slab = blockIdx.x % nslab, h = (blockIdx.x / nslab) % p.H, n = blockIdx.x / (nslab * p.H);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -170,6 +271,8 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
     for (int m = 0; m < R; ++m)
         dH[m] = p.dhT ? *reinterpret_cast<const float4 *>(p.dhT + sb + (size_t)(rg + RG * m) * p.DV)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    TokenRegs<Tin> cur{}, nxt{};
+    int it = 0;   // tokens staged so far: selects the stage buffer
 
     for (int c = p.nc - 1; c >= 0; --c) {
         const int t0 = c * kBwdChunk, t1 = min(p.T, t0 + kBwdChunk);
@@ -177,54 +280,41 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
 #pragma unroll
         for (int m = 0; m < R; ++m) Hp[m] = *reinterpret_cast<const float4 *>(ck + (size_t)(rg + RG * m) * p.DV);
         // recompute the chunk: the state before each token into the scratch slab
-        for (int t = t0; t < t1; ++t) {
+        fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t0, h, col0, false, cur);
+        for (int t = t0; t < t1; ++t, ++it) {
 #pragma unroll
             for (int m = 0; m < R; ++m)
                 *reinterpret_cast<float4 *>(scr + ((size_t)(t - t0) * DK + rg + RG * m) * DVS) = Hp[m];
-            stage_token<Tin, DK, DVS>(p, (long)n * p.T + t, h, col0, false, s_k, s_q, s_a, s_v, s_do, s_sc);
-            float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int m = 0; m < R; ++m) {
-                const int i = rg + RG * m;
-                const float kx = p.decayed_read ? s_a[i] * s_k[i] : s_k[i];
-                r.x = fmaf(Hp[m].x, kx, r.x); r.y = fmaf(Hp[m].y, kx, r.y);
-                r.z = fmaf(Hp[m].z, kx, r.z); r.w = fmaf(Hp[m].w, kx, r.w);
-            }
-            *reinterpret_cast<float4 *>(&s_red[0][rg][4 * cg]) = r;
+            Stage<DK, DVS> &s = st[it & 1];
+            put_token<Tin, DK, DVS>(p, cur, false, s);
             __syncthreads();
-            if (tid < DVS) {
-                float rs = 0.f;
-                for (int g2 = 0; g2 < RG; ++g2) rs += s_red[0][g2][tid];
-                s_u[tid] = s_sc[0] * (s_v[tid] - rs);
-            }
-            __syncthreads();
-            const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
-#pragma unroll
-            for (int m = 0; m < R; ++m) {
-                const int i = rg + RG * m;
-                const float a = s_a[i], kk = s_k[i];
-                Hp[m].x = fmaf(a, Hp[m].x, kk * u4.x); Hp[m].y = fmaf(a, Hp[m].y, kk * u4.y);
-                Hp[m].z = fmaf(a, Hp[m].z, kk * u4.z); Hp[m].w = fmaf(a, Hp[m].w, kk * u4.w);
-            }
-            __syncthreads();
+            if (t + 1 < t1) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + 1, h, col0, false, nxt);
+            forward_token<DK, DVS, RG, R>(p, s, Hp, s_red[0], s_u);
+            cur = nxt;
         }
 #pragma unroll
         for (int m = 0; m < R; ++m) Hc[m] = Hp[m];   // the state after the chunk's last token
         // walk the chunk backwards
-        for (int t = t1 - 1; t >= t0; --t) {
+        fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t1 - 1, h, col0, true, cur);
+        for (int t = t1 - 1; t >= t0; --t, ++it) {
             const long row = (long)n * p.T + t;
 #pragma unroll
             for (int m = 0; m < R; ++m)
                 Hp[m] = *reinterpret_cast<const float4 *>(scr + ((size_t)(t - t0) * DK + rg + RG * m) * DVS);
-            stage_token<Tin, DK, DVS>(p, row, h, col0, true, s_k, s_q, s_a, s_v, s_do, s_sc);
-            const float bt = s_sc[0];
-            const float4 do4 = *reinterpret_cast<const float4 *>(&s_do[4 * cg]);
+            Stage<DK, DVS> &s = st[it & 1];
+            put_token<Tin, DK, DVS>(p, cur, true, s);
+            __syncthreads();
+            if (t > t0) fetch_token<Tin, DK, DVS>(p, row - 1, h, col0, true, nxt);
+            float kn, qn;
+            token_norms(p, s, kn, qn);
+            const float bt = s.beta;
+            const float4 do4 = *reinterpret_cast<const float4 *>(&s.d[4 * cg]);
             // dh += q~ do^T;  r = R^T k^;  du = dh^T k^   (both row sums through shared memory)
             float4 r = make_float4(0.f, 0.f, 0.f, 0.f), du = r;
 #pragma unroll
             for (int m = 0; m < R; ++m) {
                 const int i = rg + RG * m;
-                const float qq = s_q[i], kk = s_k[i], kx = p.decayed_read ? s_a[i] * kk : kk;
+                const float qq = s.q[i] * qn, kk = s.k[i] * kn, kx = p.decayed_read ? s.a[i] * kk : kk;
                 dH[m].x = fmaf(qq, do4.x, dH[m].x); dH[m].y = fmaf(qq, do4.y, dH[m].y);
                 dH[m].z = fmaf(qq, do4.z, dH[m].z); dH[m].w = fmaf(qq, do4.w, dH[m].w);
                 r.x = fmaf(Hp[m].x, kx, r.x); r.y = fmaf(Hp[m].y, kx, r.y);
@@ -236,27 +326,26 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
             *reinterpret_cast<float4 *>(&s_red[1][rg][4 * cg]) = du;
             __syncthreads();
             float dbp = 0.f;   // this column's share of dbeta
-            if (tid < DVS) {
-                float rs = 0.f, ds = 0.f;
-                for (int g2 = 0; g2 < RG; ++g2) {
-                    rs += s_red[0][g2][tid];
-                    ds += s_red[1][g2][tid];
+            {
+                int j;
+                float rs, ds;
+                if (column_sums<DVS, RG, true>(s_red[0], s_red[1], tid, j, rs, ds)) {
+                    s_u[j] = bt * (s.v[j] - rs);
+                    s_du[j] = ds;
+                    p.dv[((size_t)row * p.H + h) * p.DV + col0 + j] = bt * ds;
+                    dbp = ds * (s.v[j] - rs);
                 }
-                s_u[tid] = bt * (s_v[tid] - rs);
-                s_du[tid] = ds;
-                p.dv[((size_t)row * p.H + h) * p.DV + col0 + tid] = bt * ds;
-                dbp = ds * (s_v[tid] - rs);
             }
-            if (warp < (DVS + 31) / 32) {
+            if (warp < kOwnerWarps) {
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) dbp += __shfl_xor_sync(0xffffffffu, dbp, off);
                 if (lane == 0) s_db[warp] = dbp;
             }
             __syncthreads();
             if (tid == 0) {
-                float s = 0.f;
-                for (int w = 0; w < (DVS + 31) / 32; ++w) s += s_db[w];
-                atomicAdd(p.dbeta + (size_t)row * p.H + h, s);
+                float sum = 0.f;
+                for (int w = 0; w < kOwnerWarps; ++w) sum += s_db[w];
+                atomicAdd(p.dbeta + (size_t)row * p.H + h, sum);
             }
             const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
             const float4 du4 = *reinterpret_cast<const float4 *>(&s_du[4 * cg]);
@@ -264,7 +353,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
 #pragma unroll
             for (int m = 0; m < R; ++m) {
                 const int i = rg + RG * m;
-                const float a = s_a[i], kk = s_k[i];
+                const float a = s.a[i], kk = s.k[i] * kn;
                 // sums over this thread's four columns, then over the row's TPR threads
                 float dq_i = row_sum<TPR>(dot4(Hc[m], do4));
                 const float hu = dot4(Hp[m], du4);   // sum_j h_{t-1}[i,j] du_j
@@ -281,7 +370,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
                 dH[m].z = fmaf(a, dH[m].z, -kb * du4.z); dH[m].w = fmaf(a, dH[m].w, -kb * du4.w);
                 Hc[m] = Hp[m];
             }
-            __syncthreads();   // the staging arrays are rewritten by the next token
+            cur = nxt;
         }
     }
     if (p.dh0) {
@@ -336,7 +425,13 @@ __global__ void bwd_finish_kernel(BwdParams p, long rows_heads) {
 
 template <typename Tin, int DK>
 cudaError_t run_bwd(const BwdParams &p, long rows, cudaStream_t s) {
-    const int dvs = p.DV < kSlab ? p.DV : kSlab;
+    // one CTA per (sequence, head, slab): narrower slabs when the wide ones leave SMs idle
+    int dev = 0, nsm = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const bool narrow = p.DV < kSlab || (long)p.nseq * p.H * (p.DV / kSlab) < nsm;
+    const int dvs = narrow ? 32 : kSlab;
     const long grid = (long)p.nseq * p.H * (p.DV / dvs);
     if (dvs == 64) {
         bwd_ckpt_kernel<Tin, DK, 64><<<(unsigned)grid, kThreads, 0, s>>>(p);
@@ -353,10 +448,10 @@ cudaError_t run_bwd(const BwdParams &p, long rows, cudaStream_t s) {
 }  // namespace
 
 size_t gk_bwd_scratch_bytes(int nseq, int T, int H, int dk, int dv) {
+    // checkpoints, then one kBwdChunk x dk x (slab) scratch per CTA: nseq*H*dv columns in all,
+    // whatever the slab width
     const int nc = (T + kBwdChunk - 1) / kBwdChunk;
-    const int dvs = dv < kSlab ? dv : kSlab;
-    const size_t ctas = (size_t)nseq * H * (dv / dvs);
-    return (size_t)nseq * H * nc * dk * dv * 4 + ctas * kBwdChunk * dk * dvs * 4;
+    return (size_t)nseq * H * nc * dk * dv * 4 + (size_t)nseq * H * kBwdChunk * dk * dv * 4;
 }
 
 cudaError_t launch_gk_bwd(const BwdArgs &a, cudaStream_t s) {

@@ -1,8 +1,8 @@
 """GPU parity of the per-channel backward (kda_gk_recurrent_bwd) against the fp64 autograd
 oracle: every gradient (q, k, v, beta, g, initial state), both decay placements, ragged
-lengths across the 32-token checkpoints, head dims, no decay, no L2 normalisation.  Bar:
-max|diff| / max|ref| per gradient <= 1e-4 (fp32 inputs), <= 1e-3 (bf16 inputs, the oracle
-on the same bf16 values; the kernels' arithmetic is fp32 in both)."""
+lengths across the 32-token checkpoints, head dims, both value-slab widths, no decay, no L2
+normalisation.  Bar: max|diff| / max|ref| per gradient <= 1e-4 (fp32 inputs), <= 1e-3 (bf16
+inputs, the oracle on the same bf16 values; the kernels' arithmetic is fp32 in both)."""
 import numpy as np
 import pytest
 
@@ -83,3 +83,9 @@ def test_no_decay_no_l2_no_final_gradient(kda, dev):
 def test_lengths(kda, dev):
     for T in (1, 31, 32, 33, 64):
         _case(kda, dev, 1, T, 1, 64, 64, "f32", 0.5, True, seed=75 + T)
+
+
+@pytest.mark.parametrize("dims,H", [((64, 64), 152), ((128, 128), 80)])
+def test_wide_slabs(kda, dev, dims, H):
+    # enough (sequence, head) pairs that each CTA takes 64 value columns instead of 32
+    _case(kda, dev, 1, 37, H, dims[0], dims[1], "f32", 0.3, True, seed=76)
