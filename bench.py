@@ -65,34 +65,58 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling around the timed region.
+
+    Sampling starts (and the first sample is awaited) before the region opens and goes on
+    until a sample after it has arrived; every sample carries nvidia-smi's timestamp, and
+    the summary uses the samples taken inside the region (host wall clock marks set by
+    `begin()` / `end()`), or, when the region is shorter than the sampling interval, the
+    samples that bracket it, and says which."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []   # (host time received, line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            self._await(1, 5.0)   # sampling is live before the region opens
         except Exception:
             self.proc = None
+        self.begin()
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def _await(self, n, timeout):
+        t = time.time() + timeout
+        while len(self.lines) < n and time.time() < t and self.proc.poll() is None:
+            time.sleep(0.002)
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *a):
+        if self.t1 is None:
+            self.end()
         if self.proc is not None:
+            self._await(len(self.lines) + 1, 1.0)   # a sample after the region
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -100,23 +124,38 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
-        sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        rows = []
+        for recv, ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax = float(parts[1])
+                rows.append((self._stamp(parts[0]) or recv, float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-            for nm, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1]
+        if inside:
+            use, where = inside, "inside the timed region"
+        else:   # the region is shorter than the interval: the samples just before and after it
+            before = [r for r in rows if r[0] < (self.t0 or 0)][-1:]
+            after = [r for r in rows if r[0] > (self.t1 or 0)][:1]
+            use, where = before + after, "bracketing the timed region (shorter than the sampling interval)"
+        reasons = sorted({nm for r in use for nm, val in zip(names, r[3]) if val.lower() == "active"})
+        return {"sm_mhz": statistics.median([r[1] for r in use]) if use else None,
+                "sm_max_mhz": use[-1][2] if use else None, "reasons": reasons,
+                "samples": len(use), "samples_where": where,
+                "region_ms": round(1e3 * (self.t1 - self.t0), 1) if self.t0 and self.t1 else None,
+                "interval_ms": self.INTERVAL_MS}
 
 
 def dist_setup():
@@ -198,11 +237,13 @@ def bench_prefill(args, world, rank, dev, peaks, d):
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
+        clk.begin()
         ev0.record(stream)
         for _ in range(args.steps):
             step()
         ev1.record(stream)
         torch.cuda.synchronize()
+        clk.end()
     barrier(world)
     ms = ev0.elapsed_time(ev1) / args.steps
     ms_max = max_over_ranks(ms, world)
@@ -617,10 +658,12 @@ def bench_decode(args, world, rank, dev, peaks):
     barrier(world)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
+        clk.begin()
         ev0.record(stream)
         run(nsteps)
         ev1.record(stream)
         torch.cuda.synchronize()
+        clk.end()
     barrier(world)
     ms = ev0.elapsed_time(ev1) / nsteps
     ms_max = max_over_ranks(ms, world)

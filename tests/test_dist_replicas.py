@@ -104,3 +104,25 @@ def test_reference_arm_line_keys():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 4
     assert line["e2e"] == {"value": 1000.0, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_clock_summary_uses_the_timed_region():
+    """The clock record: samples inside the region when there are any, else the ones around it;
+    throttle reasons are read from the same samples."""
+    import datetime
+    import bench
+
+    def line(t, mhz, thermal="Not Active", power="Not Active"):
+        ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return (t, f"{ts}, {mhz}, 2070, 900.0, 0x0, Not Active, {thermal}, Not Active, {power}")
+
+    c = bench.ClockSampler(0)
+    c.t0, c.t1 = 1000.0, 1000.5
+    c.lines = [line(999.9, 1500, thermal="Active"), line(1000.1, 2070), line(1000.3, 2060, power="Active"),
+               line(1000.6, 1800)]
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 2065 and s["reasons"] == ["sw_power_cap"]
+    assert s["samples_where"] == "inside the timed region"
+    c.t0, c.t1 = 1000.11, 1000.12   # shorter than the interval: the samples on either side
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 2065 and "bracketing" in s["samples_where"]

@@ -273,3 +273,16 @@ def test_chunk_matches_recurrent_kernel(kda, dev):
     o2, h2 = kda.gk_recurrent_fwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["h0"])
     torch.cuda.synchronize()
     assert_parity("bf16", to_np(o1), to_np(o2), to_np(h1), to_np(h2), tag="chunk vs scan")
+
+
+def test_chunk_full_size_head_sample(kda, oracle_mod, dev):
+    """The per-channel long-sequence prefill as timed: B=1, T=32768, H=32, d=128, one
+    cooperative launch, g = -0.01 U[0,1), decayed read, carried-in state; four sampled heads
+    against the oracle over the full T."""
+    d = make_gk(1, 32768, 32, 128, 128, dtype="bf16", gate_scale=0.01, h0="normal002", seed=38)
+    o, h = _run_chunk(kda, d, dev, "bf16", True)
+    heads = np.array([0, 9, 22, 31])
+    ro, rh = oracle_mod.forward_gk(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                                   decayed_read=True, heads=heads)
+    assert_parity("bf16", o[:, :, heads], ro[:, :, heads], h[:, heads], rh[:, heads],
+                  tag="gk chunk full size")

@@ -171,3 +171,29 @@ def test_gate_decay_op(kda, oracle_mod, dev, K):
     assert np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1e-30)) < 1e-5
     z = kda.gate_decay(_t(np.zeros((2, 10, H), np.float32), dev), _t(np.zeros(H, np.float32), dev))
     assert np.allclose(to_np(z), -np.log(2.0), rtol=1e-6)
+
+
+def test_gated_long_prefill_head_sample(kda, oracle_mod, dev):
+    """The long-sequence workload with the prologues in the kernel, as timed (B=1, T=32768,
+    H=32, d=128, raw gate with A_log and dt_bias, beta from logits, decayed read, carried-in
+    state); three sampled heads against the oracle over the full T."""
+    import torch
+    from kda_inputs import WORKLOADS, make_prefill
+    wl = WORKLOADS[3]
+    d = make_prefill(wl, seed=3)
+    gate, A_log, dt_bias = make_gate_params((wl.B, wl.T, wl.H), wl.H, seed=3)
+    raw_beta = ((2.0 * d["beta"] - 1.0) * 3).astype(np.float32)
+    q, k, v = (_t(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
+    o, h = kda.chunk_fwd(q, k, v, _t(raw_beta, dev), _t(gate, dev), _t(d["h0"], dev),
+                         chunk_size=wl.chunk, check_device=True, decayed_read=True,
+                         A_log=_t(A_log, dev), dt_bias=_t(dt_bias, dev), beta_sigmoid=True)
+    torch.cuda.synchronize()
+    heads = np.array([2, 17, 30])
+    sub = {n: np.ascontiguousarray(d[n][:, :, heads]) for n in ("q", "k", "v")}
+    sub["h0"] = np.ascontiguousarray(d["h0"][:, heads])
+    dec_ref = oracle_mod.gate_decay(np.ascontiguousarray(gate[:, :, heads]), np.ascontiguousarray(A_log[heads]),
+                                    np.ascontiguousarray(dt_bias[heads]))
+    beta_ref = oracle_mod.beta_transform(np.ascontiguousarray(raw_beta[:, :, heads]))
+    ro, rh = _oracle(oracle_mod, sub, dec_ref, beta_ref, True)
+    on, hn = to_np(o), to_np(h)
+    assert_parity("bf16", on[:, :, heads], ro, hn[:, heads], rh, tag="gated long prefill sample")
