@@ -48,21 +48,24 @@ struct ScanParams {
 };
 
 // One token's inputs, each thread its share (k or q entry, g, v entry, beta and decay),
-// read from global memory one token ahead of its use so that the loads' latency overlaps
-// the previous token's work; put() applies the gate and beta transforms and fills the
-// shared staging arrays.
+// read from global memory ahead of their use so that the loads' latency overlaps the
+// earlier tokens' work; put() converts them, applies the gate and beta transforms and
+// fills the shared staging arrays.
 template <typename Tin, int DK, int DVS, bool GK>
 struct TokenLoad {
-    float kq = 0.f, g = 0.f, v = 0.f, beta = 0.f, decay = 0.f;
+    // raw values: no instruction uses a loaded register before put(), so the loads stay in
+    // flight until then
+    Tin kq{}, v{};
+    float g = 0.f, beta = 0.f, decay = 0.f;
     __device__ __forceinline__ void fetch(const ScanParams &p, long row, int h, int col0, int tid) {
         const size_t qk_off = ((size_t)row * (p.H / p.G) + h / p.G) * DK;   // q/k head of value head h
         if (tid < DK) {
-            kq = to_f32(static_cast<const Tin *>(p.k)[qk_off + tid]);
+            kq = static_cast<const Tin *>(p.k)[qk_off + tid];
             if (GK && p.gk) g = p.gk[((size_t)row * p.H + h) * DK + tid];
         } else if (tid < 2 * DK) {
-            kq = to_f32(static_cast<const Tin *>(p.q)[qk_off + tid - DK]);
+            kq = static_cast<const Tin *>(p.q)[qk_off + tid - DK];
         }
-        if (tid < DVS) v = to_f32(static_cast<const Tin *>(p.v)[((size_t)row * p.H + h) * p.DV + col0 + tid]);
+        if (tid < DVS) v = static_cast<const Tin *>(p.v)[((size_t)row * p.H + h) * p.DV + col0 + tid];
         if (tid == 0) {
             beta = p.beta[(size_t)row * p.H + h];
             decay = p.decay ? p.decay[(size_t)row * p.H + h] : 0.f;
@@ -71,7 +74,7 @@ struct TokenLoad {
     __device__ __forceinline__ void put(const ScanParams &p, int h, int tid, float *s_k, float *s_q, float *s_a,
                                         float *s_v, float *s_sc) const {
         if (tid < DK) {
-            s_k[tid] = kq;
+            s_k[tid] = to_f32(kq);
             if constexpr (GK) {
                 float gv = g;
                 if (p.gk && p.A_log)
@@ -79,9 +82,9 @@ struct TokenLoad {
                 s_a[tid] = expf(gv);
             }
         } else if (tid < 2 * DK) {
-            s_q[tid - DK] = kq;
+            s_q[tid - DK] = to_f32(kq);
         }
-        if (tid < DVS) s_v[tid] = v;
+        if (tid < DVS) s_v[tid] = to_f32(v);
         if (tid == 0) {
             s_sc[0] = beta_of(beta, p.beta_sig, p.neg_eig);
             float d = decay;
@@ -99,11 +102,13 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
     static_assert(R >= 1 && DK % RG == 0, "state slab does not tile the block");
     static_assert(2 * DK <= kThreads && DVS <= kThreads, "staging assumes small heads");
 
-    __shared__ float s_k[DK], s_q[DK], s_v[DVS];
-    __shared__ float s_a[GK ? DK : 1];   // exp(g_t[i]) per key channel
+    // the token's staging, double-buffered (token t uses buffer t & 1), so that the next
+    // token can be staged while slow threads still read this one: three barriers a token
+    __shared__ float s_k2[2][DK], s_q2[2][DK], s_v2[2][DVS];
+    __shared__ float s_a2[2][GK ? DK : 1];   // exp(g_t[i]) per key channel
+    __shared__ float s_sc2[2][8];
     __shared__ __align__(16) float s_u[DVS];
     __shared__ __align__(16) float s_red[2][RG][DVS];
-    __shared__ float s_sc[8];
 
     const int nslab = p.DV / DVS;
     const int slab = blockIdx.x % nslab;
@@ -132,14 +137,26 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
-    TokenLoad<Tin, DK, DVS, GK> tk;   // this thread's share of the token, fetched a token ahead
-    if (len > 0) tk.fetch(p, start, h, col0, tid);
-    for (int t = 0; t < len; ++t) {
+    // this thread's share of the next kAhead tokens, in flight: slot j is refilled as soon as
+    // its token is staged (the inner loop is unrolled, so the slots stay in registers).
+    // Prefill slabs read the inputs from DRAM and need the depth; decode has one token.
+    constexpr int kAhead = DVS <= 64 ? 4 : 1;
+    TokenLoad<Tin, DK, DVS, GK> ring[kAhead];
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j)
+        if (j < len) ring[j].fetch(p, start + j, h, col0, tid);
+    for (int t0 = 0; t0 < len; t0 += kAhead) {
+#pragma unroll
+    for (int jj = 0; jj < kAhead; ++jj) {
+        const int t = t0 + jj;
+        if (t >= len) break;
         const long row = start + t;
         const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
-        tk.put(p, h, tid, s_k, s_q, s_a, s_v, s_sc);
-        if (t + 1 < len) tk.fetch(p, row + 1, h, col0, tid);
+        float *s_k = s_k2[t & 1], *s_q = s_q2[t & 1], *s_v = s_v2[t & 1], *s_a = s_a2[t & 1];
+        float *s_sc = s_sc2[t & 1];
+        ring[jj].put(p, h, tid, s_k, s_q, s_a, s_v, s_sc);
         __syncthreads();
+        if (t + kAhead < len) ring[jj].fetch(p, row + kAhead, h, col0, tid);
 
         if (warp < 3) {  // ||k||^2, ||q||^2, k.q
             float acc = 0.f;
@@ -222,7 +239,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(ScanParams p) {
             S[m].z = fmaf(am, S[m].z, kk * u4.z);
             S[m].w = fmaf(am, S[m].w, kk * u4.w);
         }
-        __syncthreads();  // staging buffers are rewritten by the next token
+    }
     }
 
     if (p.hT) {

@@ -28,6 +28,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBwdChunk = 32;   // tokens between stored states
 constexpr int kSlab = 64;       // value columns per CTA (32 when that leaves SMs idle)
+constexpr int kAhead = 4;       // tokens whose loads are in flight in the checkpoint pass
 
 struct BwdParams {
     const void *q, *k, *v, *dout;
@@ -66,7 +67,7 @@ struct __align__(16) Stage {
     float beta;
 };
 template <int DK, int DVS>
-constexpr bool stage_aligned() {
+__host__ __device__ constexpr bool stage_aligned() {
     using S = Stage<DK, DVS>;
     return sizeof(S) % 16 == 0 && offsetof(S, d) % 16 == 0;
 }
@@ -218,20 +219,29 @@ __global__ void __launch_bounds__(kThreads) bwd_ckpt_kernel(BwdParams p) {
     for (int m = 0; m < R; ++m)
         S[m] = p.h0 ? *reinterpret_cast<const float4 *>(p.h0 + sb + (size_t)(rg + RG * m) * p.DV)
                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    TokenRegs<Tin> cur{}, nxt{};
-    if (p.T > 0) fetch_token<Tin, DK, DVS>(p, (long)n * p.T, h, col0, false, cur);
-    for (int t = 0; t < p.T; ++t) {
-        if (t % kBwdChunk == 0) {   // the state before chunk t / kBwdChunk
-            float *dst = p.ckpt + (((size_t)n * p.H + h) * p.nc + t / kBwdChunk) * DK * p.DV + col0 + 4 * cg;
+    // This pass is the first to read the inputs (from DRAM): a ring of kAhead tokens' loads
+    // stays in flight, each slot refilled as soon as its token is staged (the ring index is
+    // a compile-time constant of the unrolled inner loop, so the slots stay in registers).
+    TokenRegs<Tin> ring[kAhead];
 #pragma unroll
-            for (int m = 0; m < R; ++m) *reinterpret_cast<float4 *>(dst + (size_t)(rg + RG * m) * p.DV) = S[m];
+    for (int j = 0; j < kAhead; ++j)
+        if (j < p.T) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + j, h, col0, false, ring[j]);
+    for (int t0 = 0; t0 < p.T; t0 += kAhead) {
+#pragma unroll
+        for (int j = 0; j < kAhead; ++j) {
+            const int t = t0 + j;
+            if (t >= p.T) break;
+            if (t % kBwdChunk == 0) {   // the state before chunk t / kBwdChunk
+                float *dst = p.ckpt + (((size_t)n * p.H + h) * p.nc + t / kBwdChunk) * DK * p.DV + col0 + 4 * cg;
+#pragma unroll
+                for (int m = 0; m < R; ++m) *reinterpret_cast<float4 *>(dst + (size_t)(rg + RG * m) * p.DV) = S[m];
+            }
+            Stage<DK, DVS> &s = st[j & 1];
+            put_token<Tin, DK, DVS>(p, ring[j], false, s);
+            __syncthreads();
+            if (t + kAhead < p.T) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + kAhead, h, col0, false, ring[j]);
+            forward_token<DK, DVS, RG, R>(p, s, S, s_red, s_u);
         }
-        Stage<DK, DVS> &s = st[t & 1];
-        put_token<Tin, DK, DVS>(p, cur, false, s);
-        __syncthreads();
-        if (t + 1 < p.T) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + 1, h, col0, false, nxt);
-        forward_token<DK, DVS, RG, R>(p, s, S, s_red, s_u);
-        cur = nxt;
     }
 }
 
