@@ -266,11 +266,12 @@ __global__ void __launch_bounds__(kThreads) scan_vm_kernel(ScanParams p) {
     static_assert(CPW >= 1 && DVS % NW == 0 && RPL >= 1 && DK % 32 == 0, "slab does not tile the block");
     static_assert(2 * DK <= kThreads && DVS <= kThreads, "staging assumes small heads");
 
-    __shared__ __align__(16) float s_k[DK];
-    __shared__ __align__(16) float s_q[DK];
-    __shared__ __align__(16) float s_a[GK ? DK : 4];
-    __shared__ float s_v[DVS];
-    __shared__ float s_sc[8];
+    // double-buffered staging (token t uses buffer t & 1): two barriers a token
+    __shared__ __align__(16) float s_k2[2][DK];
+    __shared__ __align__(16) float s_q2[2][DK];
+    __shared__ __align__(16) float s_a2[2][GK ? DK : 4];
+    __shared__ float s_v2[2][DVS];
+    __shared__ float s_sc2[2][8];
 
     const int nslab = p.DV / DVS;
     const int slab = blockIdx.x % nslab;
@@ -309,14 +310,24 @@ __global__ void __launch_bounds__(kThreads) scan_vm_kernel(ScanParams p) {
         }
     }
 
-    TokenLoad<Tin, DK, DVS, GK> tk;   // this thread's share of the token, fetched a token ahead
-    if (len > 0) tk.fetch(p, start, h, col0, tid);
-    for (int t = 0; t < len; ++t) {
+    // the next kAhead tokens' loads in flight, as in scan_kernel
+    constexpr int kAhead = DVS <= 64 ? 4 : 1;
+    TokenLoad<Tin, DK, DVS, GK> ring[kAhead];
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j)
+        if (j < len) ring[j].fetch(p, start + j, h, col0, tid);
+    for (int t0 = 0; t0 < len; t0 += kAhead) {
+#pragma unroll
+    for (int jj = 0; jj < kAhead; ++jj) {
+        const int t = t0 + jj;
+        if (t >= len) break;
         const long row = start + t;
         const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
-        tk.put(p, h, tid, s_k, s_q, s_a, s_v, s_sc);
-        if (t + 1 < len) tk.fetch(p, row + 1, h, col0, tid);
+        float *s_k = s_k2[t & 1], *s_q = s_q2[t & 1], *s_v = s_v2[t & 1], *s_a = s_a2[t & 1];
+        float *s_sc = s_sc2[t & 1];
+        ring[jj].put(p, h, tid, s_k, s_q, s_a, s_v, s_sc);
         __syncthreads();
+        if (t + kAhead < len) ring[jj].fetch(p, row + kAhead, h, col0, tid);
         if (warp < 3) {  // ||k||^2, ||q||^2, k.q
             float acc = 0.f;
             for (int i = lane; i < DK; i += 32) {
@@ -360,7 +371,7 @@ __global__ void __launch_bounds__(kThreads) scan_vm_kernel(ScanParams p) {
 #pragma unroll
             for (int e = 0; e < RPL; ++e) S[c][e] = fmaf(am[e], S[c][e], kn * kk[e] * u);
         }
-        __syncthreads();  // staging buffers are rewritten by the next token
+    }
     }
 
     if (p.hT) {
