@@ -242,9 +242,13 @@ __device__ __forceinline__ void put_b(const BTiles &bt, int t, int s, const floa
 //  * the diagonal blocks T_ii by forward substitution, one lane per column, the column
 //    in registers, each row of L read with 16-byte loads;
 //  * the off-diagonal blocks  T_ij = -T_ii X_ij,  X_ij = sum_{k=j}^{i-1} L_ik T_kj,
-//    with X_ij accumulated as soon as each T_kj is known: six steps
-//      X_10 X_21 X_32 X_20 | T_10 T_21 T_32, X_31 | X_20 X_31 X_30 | T_20 T_31 | X_30 | T_30
-//    in which every thread takes 4, 2 or 1 consecutive outputs of one row.
+//    with X_ij accumulated as soon as each T_kj is known, in four steps
+//      X_10 X_21 X_32 X_20 | T_10 T_21 T_32, X_31 | X_20 X_31 X'_30 | T_20 T_31 T_30
+//    in which every thread takes 4 or 2 consecutive outputs of one row.  The corner block
+//    skips the wait for T_20: with X'_30 = L_30 T_00 + L_31 T_10 (no L_32 T_20 term),
+//    T_30 = -T_33 (X'_30 + L_32 T_20) and T_20 = -T_22 X_20, T_32 = -T_33 L_32 T_22 give
+//    T_30 = -(T_32 X_20 + T_33 X'_30), both factors known after the third step (the
+//    2 x 2 block form of the inverse of a lower-triangular matrix).
 // The unused upper blocks of L hold the partial sums X_ij (X_ij in block (j, i)).
 // ---------------------------------------------------------------------------------
 constexpr int kLP = 68;
@@ -352,6 +356,51 @@ __device__ __forceinline__ void inv_op_t(const float *sL, float *sT, const BTile
     put_b<W, PO>(bt, 16 * i + r, 16 * j + c0, acc);
 }
 
+// T_ij[r][c0 .. c0+W) = -(T_ik X_kj + T_ii X_ij)[r][c0 ..), X_kj and X_ij in L's upper blocks
+// (j, k) and (j, i); also written into B and Bf
+template <int W, bool PO>
+__device__ __forceinline__ void inv_op_t2(const float *sL, float *sT, const BTiles &bt, int i, int k, int j,
+                                          int r, int c0) {
+    static_assert(W == 2 || W == 4, "paired outputs");
+    constexpr int P = kLP;
+    float2 pr[W / 2];
+#pragma unroll
+    for (int e = 0; e < W / 2; ++e) pr[e] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int term = 0; term < 2; ++term) {
+        const int kk = term == 0 ? k : i;   // T_ik X_kj, then T_ii X_ij
+        const float *Ar = sT + (16 * i + r) * P + 16 * kk;
+        float a[16];
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const float4 v = *reinterpret_cast<const float4 *>(Ar + 4 * m4);
+            a[4 * m4] = v.x; a[4 * m4 + 1] = v.y; a[4 * m4 + 2] = v.z; a[4 * m4 + 3] = v.w;
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float2 *Xr = reinterpret_cast<const float2 *>(sL + (16 * j + m) * P + 16 * kk + c0);
+            const float2 am = make_float2(a[m], a[m]);
+            if constexpr (W == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(Xr);
+                fma2(pr[0], am, make_float2(x.x, x.y));
+                fma2(pr[1], am, make_float2(x.z, x.w));
+            } else {
+                fma2(pr[0], am, Xr[0]);
+            }
+        }
+    }
+    float acc[W];
+#pragma unroll
+    for (int e = 0; e < W / 2; ++e) {
+        acc[2 * e] = -pr[e].x;
+        acc[2 * e + 1] = -pr[e].y;
+    }
+    float *Tij = sT + (16 * i + r) * P + 16 * j + c0;
+    if constexpr (W == 4) *reinterpret_cast<float4 *>(Tij) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    else *reinterpret_cast<float2 *>(Tij) = make_float2(acc[0], acc[1]);
+    put_b<W, PO>(bt, 16 * i + r, 16 * j + c0, acc);
+}
+
 template <int NT, bool PO = false, typename IdleWork>
 __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int tid, int bar,
                                      IdleWork &&idle) {
@@ -413,7 +462,7 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
     if (slot < 3) inv_op_t<4, PO>(sL, sT, bt, slot + 1, slot, r4, c4);
     else inv_op_x<4>(sL, sT, 3, 1, 1, 2, false, r4, c4);
     named_sync(bar, NT);
-    // S2: X_20 += L_21 T_10;  X_31 += L_32 T_21;  X_30 = L_30 T_00 + L_31 T_10 (two column halves)
+    // S2: X_20 += L_21 T_10;  X_31 += L_32 T_21;  X'_30 = L_30 T_00 + L_31 T_10 (two column halves)
     if (slot == 0) inv_op_x<4>(sL, sT, 2, 0, 1, 2, true, r4, c4);
     else if (slot == 1) inv_op_x<4>(sL, sT, 3, 1, 2, 3, true, r4, c4);
     else {
@@ -421,19 +470,14 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
         inv_op_x<2>(sL, sT, 3, 0, 0, 2, false, r2, c2);
     }
     named_sync(bar, NT);
-    // S3: T_20, T_31 (128 threads each, 2 outputs)
-    {
-        const int half = tid >> 7, t128 = tid & 127;
-        const int r2 = t128 >> 3, c2 = (t128 & 7) * 2;
-        if (half == 0) inv_op_t<2, PO>(sL, sT, bt, 2, 0, r2, c2);
-        else inv_op_t<2, PO>(sL, sT, bt, 3, 1, r2, c2);
+    // S3: T_20, T_31 (64 threads each, 4 outputs); T_30 = -(T_32 X_20 + T_33 X'_30) (128 threads,
+    // 2 outputs)
+    if (slot == 0) inv_op_t<4, PO>(sL, sT, bt, 2, 0, r4, c4);
+    else if (slot == 1) inv_op_t<4, PO>(sL, sT, bt, 3, 1, r4, c4);
+    else {
+        const int t128 = tid - 128;
+        inv_op_t2<2, PO>(sL, sT, bt, 3, 2, 0, t128 >> 3, (t128 & 7) * 2);
     }
-    named_sync(bar, NT);
-    // S4: X_30 += L_32 T_20 (one output per thread)
-    inv_op_x<1>(sL, sT, 3, 0, 2, 3, true, tid >> 4, tid & 15);
-    named_sync(bar, NT);
-    // S5: T_30
-    inv_op_t<1, PO>(sL, sT, bt, 3, 0, tid >> 4, tid & 15);
     fence_proxy_async();   // B, Bf are tensor-core operands
     tc_fence_before();
     named_sync(bar, NT);
