@@ -40,11 +40,11 @@ NOMINAL_HBM_GBS = 8000.0
 # now; set to None whenever that kernel changes until it is captured again.
 #   decode: profiles/decode_scan_kernel_b256_h32_d128.md
 #   prefill: profiles/tc_kernel_long_prefill_d128.md
-NCU_TRAFFIC = {"decode": 543.26e6 + 478.36e6, "prefill": 1.0462e9 + 593.47e6}
+NCU_TRAFFIC = {"decode": 543.26e6 + 478.36e6, "prefill": None}
 # sm__pipe_tensor_cycles_active (fraction of elapsed) of the prefill kernel, from the
 # mid-size (T=8192) full capture in profiles/tc_kernel_long_prefill_d128.md; None once the
 # kernel changes until it is captured again.
-NCU_TENSOR_PIPE = {"prefill": 0.143}
+NCU_TENSOR_PIPE = {"prefill": None}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
