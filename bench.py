@@ -40,11 +40,11 @@ NOMINAL_HBM_GBS = 8000.0
 # now; set to None whenever that kernel changes until it is captured again.
 #   decode: profiles/decode_scan_kernel_b256_h32_d128.md
 #   prefill: profiles/tc_kernel_long_prefill_d128.md
-NCU_TRAFFIC = {"decode": 543.26e6 + 478.36e6, "prefill": None}
+NCU_TRAFFIC = {"decode": 543.26e6 + 478.36e6, "prefill": 1.27393e9 + 796.65e6}
 # sm__pipe_tensor_cycles_active (fraction of elapsed) of the prefill kernel, from the
 # mid-size (T=8192) full capture in profiles/tc_kernel_long_prefill_d128.md; None once the
 # kernel changes until it is captured again.
-NCU_TENSOR_PIPE = {"prefill": None}
+NCU_TENSOR_PIPE = {"prefill": 0.146}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -702,15 +702,16 @@ def oracle_prefill_sample(d, heads_in_sample, threads=0):
 def run_reference(args, world, rank):
     """The reference arm: the fp64 CPU oracle on the host cores, same workload.
 
-    Each step runs the oracle on 8 of the 32 heads over the full T (about a
-    second of wall time on 16 cores); tokens/s is scaled by the head fraction."""
+    Each step runs the oracle on as many of the 32 heads as the host has cores (one
+    thread per head) over the full T, about a second of wall time; tokens/s is scaled by
+    the head fraction."""
     if rank != 0:
         return
     import oracle
     oracle.build()
     wl = WORKLOADS[3]
     d = make_prefill(wl, seed=0)
-    heads = 8
+    heads = max(1, min(wl.H, os.cpu_count() or 1))   # one oracle thread per head: every host core busy
     for _ in range(min(args.warmup, 1)):
         oracle_prefill_sample(d, 1)
     vals, secs, used = [], 0.0, 0
