@@ -367,6 +367,20 @@ def bench_secondary(args, world, rank, dev, peaks):
         "tc_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
         "gpu_launches_per_call": tc_prefill_launches(wl.B, wl.H, dev)}
 
+    # the backward of the same call (one decay per head): gradients for q, k, v, beta, the
+    # decay and the initial state, token by token
+    d_o = torch.randn_like(o)
+    h0z = torch.zeros((wl.B, wl.H, wl.dk, wl.dv), dtype=torch.float32, device=dev)
+    wsb = torch.empty(_lib.load().kda_recurrent_bwd_workspace(wl.B, wl.T, wl.H, wl.dk, wl.dv),
+                      dtype=torch.uint8, device=dev)
+    bms = timed(lambda: kda.recurrent_bwd(q, k, v, beta, decay, h0z, d_o, None, workspace=wsb,
+                                          stream=stream))
+    out["training_backward"] = {
+        "workload": wl.name + ", backward", "ms_per_call": bms,
+        "tokens_per_s": wl.B * wl.T * world / (bms * 1e-3), "gpu_launches_per_call": 3,
+        "note": "token by token on CUDA cores: 32-token checkpoints, recompute, reverse walk"}
+    del d_o, h0z, wsb
+
     # the long-sequence workload with the prologues in the kernel: decay from a raw gate
     # (kda_decay), beta from logits (sigmoid), the decayed read
     wl = WORKLOADS[3]

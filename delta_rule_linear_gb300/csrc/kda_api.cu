@@ -519,6 +519,51 @@ kda_status kda_gk_recurrent_bwd(const void *q, const void *k, const void *v, con
     return launch_status(launch_gk_bwd(a, st));
 }
 
+size_t kda_recurrent_bwd_workspace(int B, int T, int H, int dk, int dv) {
+    return kda_gk_recurrent_bwd_workspace(B, T, H, dk, dv);
+}
+
+kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const float *beta,
+                             const float *decay, const float *initial_state, const void *d_o,
+                             const float *dfinal_state, float *dq, float *dk_out, float *dv_out,
+                             float *dbeta, float *ddecay, float *dinitial_state, int B, int T, int H,
+                             int dk, int dv, kda_dtype dtype, float scale, int use_qk_l2norm,
+                             int decayed_read, void *ws, size_t ws_bytes, kda_stream_t stream) {
+    if (B < 0 || T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, decay, initial_state, d_o, dfinal_state,
+                                (long)B * T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    const long rows = (long)B * T;
+    if (rows > 0 && (!dq || !dk_out || !dv_out || !dbeta)) return KDA_ERR_NULL;
+    if (!aligned16(dinitial_state) || !aligned4(dq) || !aligned4(dk_out) || !aligned4(dv_out) ||
+        !aligned4(dbeta) || !aligned4(ddecay))
+        return KDA_ERR_ALIGN;
+    const size_t need = kda_recurrent_bwd_workspace(B, T, H, dk, dv);
+    if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0) {   // nothing but the state: dh0 = dhT
+        if (!dinitial_state || B == 0) return KDA_OK;
+        const size_t n = (size_t)B * H * dk * dv * sizeof(float);
+        if (dfinal_state) return launch_status(cudaMemcpyAsync(dinitial_state, dfinal_state, n, cudaMemcpyDeviceToDevice, st));
+        return launch_status(cudaMemsetAsync(dinitial_state, 0, n, st));
+    }
+    BwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.dout = d_o; a.beta = beta; a.g = nullptr; a.h0 = initial_state;
+    a.decay = decay; a.ddecay = decay ? ddecay : nullptr;
+    a.dhT = dfinal_state; a.dq = dq; a.dk = dk_out; a.dv = dv_out; a.dbeta = dbeta;
+    a.dg = nullptr; a.dh0 = dinitial_state;
+    a.B = B; a.T = T; a.H = H; a.dkdim = dk; a.dvdim = dv;
+    a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    a.decayed_read = decayed_read ? 1 : 0;
+    a.ws = static_cast<char *>(ws) + kWsHeader;
+    if (!decay && ddecay &&   // ddecay without a decay: a zero gradient
+        cudaMemsetAsync(ddecay, 0, (size_t)rows * H * sizeof(float), st) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return launch_status(launch_gk_bwd(a, st));
+}
+
 kda_status kda_query_device_error(const void *ws, kda_stream_t stream) {
     if (!ws) return KDA_ERR_NULL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -100,6 +100,8 @@ cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t s
 struct BwdArgs {
     const void *q, *k, *v, *dout;      // [rows, H, dk | dv] (Tin)
     const float *beta, *g;             // [rows, H], [rows, H, dk] (g may be null)
+    const float *decay;                // [rows, H]: one decay per head (used when g is null)
+    float *ddecay;                     // its gradient [rows, H] (may be null)
     const float *h0, *dhT;             // [B, H, dk, dv] or null
     float *dq, *dk, *dv, *dbeta, *dg;  // fp32 gradients (dg may be null)
     float *dh0;                        // [B, H, dk, dv] or null

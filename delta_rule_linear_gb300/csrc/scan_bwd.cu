@@ -14,7 +14,9 @@
 //     dh      <- D_t dh - beta_t (k^ or D_t k^) du^T                          (now for h_{t-1})
 // with r = R^T k^ and a = exp(g_t).  The states h_{t-1} come back chunk by chunk: a forward
 // pass stores the state at every chunk start; the backward pass recomputes one chunk's
-// states into a scratch slab and walks it in reverse.  Each CTA owns a slab of value
+// states into a scratch slab and walks it in reverse.  With one decay per head (D_t = a_t I)
+// the same walk runs with every channel's factor equal, and the decay's gradient is the
+// channel sum of dg.  Each CTA owns a slab of value
 // columns (everything above is separable in j except the sums over j, which go to fp32
 // accumulators by atomic adds).  A last kernel turns the gradients of k^ and q~ into those
 // of the raw k and q (through the L2 normalisation and the scale).
@@ -33,6 +35,8 @@ constexpr int kAhead = 4;       // tokens whose loads are in flight in the check
 struct BwdParams {
     const void *q, *k, *v, *dout;
     const float *beta, *gk, *h0, *dhT;
+    const float *decay;                       // one decay per head [rows, H] (when gk is null)
+    float *ddecay;                            // its gradient: the channel sum of dg
     float *dq, *dk, *dv, *dbeta, *dg, *dh0;   // dq, dk: accumulators of the gradients of q~, k^
     float *ckpt;                              // [nseq, H, nc, DK, DV]
     float *scratch;                           // [grid, kBwdChunk, DK, DVS]
@@ -80,7 +84,12 @@ __device__ __forceinline__ void fetch_token(const BwdParams &p, long row, int h,
     const size_t v_off = ((size_t)row * p.H + h) * p.DV + col0;
     if (tid < DK) {
         r.x = static_cast<const Tin *>(p.k)[qk_off + tid];
-        r.g = p.gk ? p.gk[qk_off + tid] : 0.f;
+        // one load for either decay layout: per channel [rows, H, DK], or per head [rows, H]
+        // (the same element for every channel); the pointer and offset are selected, not
+        // the code path
+        const float *gsrc = p.gk ? p.gk : p.decay;
+        const size_t goff = p.gk ? qk_off + tid : (size_t)row * p.H + h;
+        r.g = gsrc ? gsrc[goff] : 0.f;
     } else if (tid < 2 * DK) {
         r.x = static_cast<const Tin *>(p.q)[qk_off + tid - DK];
     }
@@ -103,7 +112,7 @@ __device__ __forceinline__ void put_token(const BwdParams &p, const TokenRegs<Ti
         for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
         if (tid < DK) {
             s.k[tid] = x;
-            s.a[tid] = p.gk ? expf(r.g) : 1.f;
+            s.a[tid] = (p.gk || p.decay) ? expf(r.g) : 1.f;
             if (lane == 0) s.nk[warp] = sq;
         } else {
             s.q[tid - DK] = x;
@@ -360,6 +369,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
             const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
             const float4 du4 = *reinterpret_cast<const float4 *>(&s_du[4 * cg]);
             const size_t kd_off = ((size_t)row * p.H + h) * DK;
+            float dd = 0.f;   // one decay per head: sum over this thread's rows of a_i de_i
 #pragma unroll
             for (int m = 0; m < R; ++m) {
                 const int i = rg + RG * m;
@@ -374,11 +384,17 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
                     atomicAdd(p.dk + kd_off + i, dk_i);
                     if (p.dg) atomicAdd(p.dg + kd_off + i, a * de_i);
                 }
+                dd = fmaf(a, de_i, dd);
                 // dh for the state before token t
                 const float kb = bt * (p.decayed_read ? a * kk : kk);
                 dH[m].x = fmaf(a, dH[m].x, -kb * du4.x); dH[m].y = fmaf(a, dH[m].y, -kb * du4.y);
                 dH[m].z = fmaf(a, dH[m].z, -kb * du4.z); dH[m].w = fmaf(a, dH[m].w, -kb * du4.w);
                 Hc[m] = Hp[m];
+            }
+            if (p.ddecay) {   // the row groups of the warp (every lane of a group holds its sum)
+#pragma unroll
+                for (int off = TPR; off < 32; off <<= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
+                if (lane == 0) atomicAdd(p.ddecay + (size_t)row * p.H + h, dd);
             }
             cur = nxt;
         }
@@ -468,6 +484,8 @@ cudaError_t launch_gk_bwd(const BwdArgs &a, cudaStream_t s) {
     BwdParams p{};
     p.q = a.q; p.k = a.k; p.v = a.v; p.dout = a.dout;
     p.beta = a.beta; p.gk = a.g; p.h0 = a.h0; p.dhT = a.dhT;
+    p.decay = a.g ? nullptr : a.decay;
+    p.ddecay = p.decay ? a.ddecay : nullptr;
     p.dq = a.dq; p.dk = a.dk; p.dv = a.dv; p.dbeta = a.dbeta; p.dg = a.dg; p.dh0 = a.dh0;
     p.nseq = a.B; p.T = a.T; p.H = a.H; p.DV = a.dvdim;
     p.nc = (a.T + kBwdChunk - 1) / kBwdChunk;
@@ -481,6 +499,8 @@ cudaError_t launch_gk_bwd(const BwdArgs &a, cudaStream_t s) {
     if ((e = cudaMemsetAsync(a.dq, 0, nk, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(a.dk, 0, nk, s)) != cudaSuccess) return e;
     if (a.dg && (e = cudaMemsetAsync(a.dg, 0, nk, s)) != cudaSuccess) return e;
+    if (p.ddecay && (e = cudaMemsetAsync(p.ddecay, 0, (size_t)rows * a.H * sizeof(float), s)) != cudaSuccess)
+        return e;
     if ((e = cudaMemsetAsync(a.dbeta, 0, (size_t)rows * a.H * sizeof(float), s)) != cudaSuccess) return e;
     const bool bf = a.dtype == DType::BF16;
     switch (a.dkdim) {

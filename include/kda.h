@@ -317,6 +317,26 @@ kda_status kda_gk_recurrent_bwd(const void *q, const void *k, const void *v,
                                 void *ws, size_t ws_bytes, kda_stream_t stream);
 
 /*
+ * Gradients of the path's own recurrence (one decay per head, decay [B,T,H] as in
+ * kda_chunk_fwd; the delta reads h_{t-1}, or exp(decay_t) h_{t-1} with decayed_read): the
+ * same as kda_gk_recurrent_bwd with every key channel's decay equal, so that
+ *     ddecay [B,T,H] (NULL allowed; zeros when decay is NULL) = the sum over the key
+ *     channels of the per-channel dg,
+ * and dq, dk, dv, dbeta, dinitial_state as there.  decay may be NULL (no decay).  ws: at
+ * least kda_recurrent_bwd_workspace() bytes (the same size as the per-channel backward's),
+ * 16-byte aligned.  Errors: as kda_gk_recurrent_bwd; ddecay must be 4-byte aligned.
+ */
+size_t kda_recurrent_bwd_workspace(int B, int T, int H, int dk, int dv);
+kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v,
+                             const float *beta, const float *decay,
+                             const float *initial_state, const void *d_o,
+                             const float *dfinal_state, float *dq, float *dk_out,
+                             float *dv_out, float *dbeta, float *ddecay, float *dinitial_state,
+                             int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                             float scale, int use_qk_l2norm, int decayed_read,
+                             void *ws, size_t ws_bytes, kda_stream_t stream);
+
+/*
  * The scalar-decay entry points with options (see kda_options): the same arguments, layouts,
  * workspace and errors as kda_chunk_fwd / kda_varlen_fwd / kda_recurrent_fwd /
  * kda_decode_step, plus `opt` (may be NULL).  A_log and dt_bias must be 4-byte aligned

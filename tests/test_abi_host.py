@@ -267,3 +267,38 @@ def test_grouped_heads_option_checked(lib):
     need6 = lib.kda_chunk_fwd_workspace(1, 640, 6, 128, 128, 64, 1)
     assert need6 > need2
     assert chunk(3, need2) == 6          # three value heads per q/k head need the HV-sized workspace
+
+
+def test_backward_entry_points_reject_bad_arguments(lib):
+    """kda_gk_recurrent_bwd and kda_recurrent_bwd: workspace sizes, and every argument error
+    returned before anything is enqueued."""
+    assert lib.kda_gk_recurrent_bwd_workspace(2, 2048, 16, 128, 128) > 256
+    assert lib.kda_recurrent_bwd_workspace(2, 2048, 16, 128, 128) == \
+        lib.kda_gk_recurrent_bwd_workspace(2, 2048, 16, 128, 128)
+    assert lib.kda_recurrent_bwd_workspace(1, 64, 2, 48, 64) == 0      # unsupported dk
+    assert lib.kda_recurrent_bwd_workspace(1, 64, 0, 64, 64) == 0
+    need = lib.kda_recurrent_bwd_workspace(1, 64, 2, 64, 64)
+
+    def call(fn, **kw):
+        a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), dec=None, h0=None, do=_fake(),
+                 dhT=None, dq=_fake(), dk_=_fake(), dv_=_fake(), db=_fake(), dd=None, dh0=None,
+                 B=1, T=64, H=2, dk=64, dv=64, dt=1, l2=1, dr=0, ws=_fake(), wsb=need)
+        a.update(kw)
+        return fn(a["q"], a["k"], a["v"], a["beta"], a["dec"], a["h0"], a["do"], a["dhT"], a["dq"],
+                  a["dk_"], a["dv_"], a["db"], a["dd"], a["dh0"], a["B"], a["T"], a["H"], a["dk"],
+                  a["dv"], a["dt"], 0.0, a["l2"], a["dr"], a["ws"], a["wsb"], None)
+
+    for fn in (lib.kda_gk_recurrent_bwd, lib.kda_recurrent_bwd):
+        assert call(fn, q=None) == 1
+        assert call(fn, dq=None) == 1
+        assert call(fn, T=-1) == 2
+        assert call(fn, dt=9) == 3
+        assert call(fn, dk=80) == 4
+        assert call(fn, dd=_fake(0x1002)) == 5
+        assert call(fn, dh0=_fake(0x1004)) == 5
+        assert call(fn, ws=None) == 6
+        assert call(fn, wsb=need - 1) == 6
+        assert call(fn, ws=_fake(0x1008)) == 5
+        assert call(fn, B=0) == 0                   # nothing to do, no launch
+    assert call(lib.kda_gk_recurrent_bwd, dec=_fake(0x1004)) == 5   # g: 16-byte aligned
+    assert call(lib.kda_recurrent_bwd, dec=_fake(0x1002)) == 5      # decay: 4-byte aligned

@@ -89,3 +89,48 @@ def test_lengths(kda, dev):
 def test_wide_slabs(kda, dev, dims, H):
     # enough (sequence, head) pairs that each CTA takes 64 value columns instead of 32
     _case(kda, dev, 1, 37, H, dims[0], dims[1], "f32", 0.3, True, seed=76)
+
+
+# ------------------------------------------------------------------ one decay per head
+def _case_scalar(kda, dev, B, T, H, dk, dv, dtype, decay_kind, decayed, seed, use_decay=True):
+    """kda_recurrent_bwd against the fp64 oracle with every channel's decay equal: the
+    decay's gradient is the channel sum of the per-channel dg (chain rule)."""
+    import torch
+    from kda_inputs import make_custom
+    from oracle import backward as ob
+    d = make_custom(B, T, H, dk, dv, dtype=dtype, decay=decay_kind, h0="normal002", seed=seed)
+    d["h0"] = (d["h0"] * 20).astype(np.float32)
+    rng = np.random.default_rng(seed + 2000)
+    do = rng.standard_normal((B, T, H, dv)).astype(np.float32)
+    if dtype == "bf16":
+        do = round_to_bf16(do)
+    dhT = rng.standard_normal((B, H, dk, dv)).astype(np.float32)
+    dec = d["decay"] if use_decay else None
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    got = kda.recurrent_bwd(*(to_dev(d[n], dev, tdt) for n in ("q", "k", "v")),
+                            to_dev(d["beta"], dev, torch.float32),
+                            None if dec is None else to_dev(dec, dev, torch.float32),
+                            to_dev(d["h0"], dev, torch.float32), to_dev(do, dev, tdt),
+                            to_dev(dhT, dev, torch.float32), decayed_read=decayed)
+    torch.cuda.synchronize()
+    g = np.repeat((dec if dec is not None else np.zeros_like(d["beta"]))[..., None], dk, axis=-1)
+    ref = ob.backward(d["q"], d["k"], d["v"], d["beta"], g.astype(np.float32), d["h0"], do, dhT,
+                      use_l2=True, decayed_read=decayed)
+    ref["ddecay"] = ref["dg"].sum(-1) if dec is not None else np.zeros_like(d["beta"])
+    tol = 1e-4 if dtype == "f32" else 1e-3
+    for name in ("dq", "dk", "dv", "dbeta", "ddecay", "dh0"):
+        err = max_rel(to_np(got[name]), ref[name])
+        assert err <= tol, f"{name}: {err:.3e}"
+
+
+@pytest.mark.parametrize("decayed", [False, True])
+@pytest.mark.parametrize("decay_kind", ["train", "long", "strong"])
+def test_scalar_decay(kda, dev, decay_kind, decayed):
+    _case_scalar(kda, dev, 2, 70, 2, 64, 64, "f32", decay_kind, decayed, seed=81)
+
+
+def test_scalar_decay_bf16_and_shapes(kda, dev):
+    _case_scalar(kda, dev, 1, 100, 2, 128, 128, "bf16", "train", True, seed=82)
+    _case_scalar(kda, dev, 1, 45, 3, 32, 128, "f32", "train", False, seed=83)
+    _case_scalar(kda, dev, 1, 33, 2, 64, 64, "f32", "train", False, seed=84, use_decay=False)
+    _case_scalar(kda, dev, 1, 37, 160, 64, 64, "f32", "train", True, seed=85)   # 64-column slabs
