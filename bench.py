@@ -189,6 +189,33 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+def pin_to_gpu_cpus(index):
+    """Run this process on the CPUs beside GPU `index` (the local_cpulist of its PCI device),
+    so that pinned host buffers allocated afterwards sit in the memory node next to the GPU:
+    the host-device copy rate depends on it.  Returns the CPU list in use ("unchanged" when
+    the list cannot be read or covers every allowed CPU)."""
+    try:
+        bus_id = subprocess.run(["nvidia-smi", "-i", str(index), "--query-gpu=pci.bus_id",
+                                 "--format=csv,noheader"], capture_output=True, text=True,
+                                timeout=30).stdout.strip()
+        dom, bus, rest = bus_id.split(":")
+        path = f"/sys/bus/pci/devices/{int(dom, 16):04x}:{bus.lower()}:{rest.lower()}/local_cpulist"
+        with open(path) as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        allowed = os.sched_getaffinity(0)
+        cpus &= allowed
+        if not cpus or cpus == allowed:
+            return "unchanged"
+        os.sched_setaffinity(0, cpus)
+        return spec
+    except Exception:
+        return "unchanged"
+
+
 def to_dev(x, dev, dtype):
     import torch
     return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to(dev, dtype)
@@ -256,6 +283,7 @@ def bench_prefill(args, world, rank, dev, peaks, d):
     # step i's read-back and step i+1's upload (opposite copy directions) and step i's
     # kernels overlap; every byte of every step still crosses the link inside the timed
     # region.
+    host_cpus = pin_to_gpu_cpus(dev.index if dev.index is not None else 0)
     pin = lambda x: x.cpu().pin_memory()  # noqa: E731
     hin = [pin(x) for x in (q, k, v, beta, decay, h0)]
     hout = [[torch.empty_like(x, device="cpu").pin_memory() for x in (o, hT)] for _ in range(2)]
@@ -322,7 +350,8 @@ def bench_prefill(args, world, rank, dev, peaks, d):
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
-                "pipelining": "H2D, kernels and D2H on three streams, two buffer sets"},
+                "pipelining": "H2D, kernels and D2H on three streams, two buffer sets",
+                "host_cpus": host_cpus},
         "gpu_launches": args.steps * tc_prefill_launches(B, H, dev),
         "shape": dict(B=B, T=T, H=H, dk=dk, dv=dv, chunk=C),
     }
