@@ -135,8 +135,9 @@ __device__ __forceinline__ void token_norms(const BwdParams &p, const Stage<DK, 
         nk += s.nk[w];
         nq += s.nq[w];
     }
-    kn = p.use_l2 ? 1.f / fmaxf(sqrtf(nk), kNormEps) : 1.f;
-    qn = p.scale * (p.use_l2 ? 1.f / fmaxf(sqrtf(nq), kNormEps) : 1.f);
+    // 1 / max(|x|, eps) = rsqrt(max(|x|^2, eps^2))
+    kn = p.use_l2 ? rsqrtf(fmaxf(nk, kNormEps * kNormEps)) : 1.f;
+    qn = p.scale * (p.use_l2 ? rsqrtf(fmaxf(nq, kNormEps * kNormEps)) : 1.f);
 }
 
 // Sums over the RG row groups of one or two [RG][DVS] partial arrays.  Column j's sums land
@@ -177,7 +178,7 @@ __device__ __forceinline__ bool column_sums(const float (*a)[DVS], const float (
 
 // One token of the forward recurrence on this thread's rows of the slab (S: the state before
 // the token on entry, after it on return).  The stage was synced by the caller; two syncs.
-template <int DK, int DVS, int RG, int R>
+template <int DK, int DVS, int RG, int R, bool DR>
 __device__ __forceinline__ void forward_token(const BwdParams &p, const Stage<DK, DVS> &s, float4 (&S)[R],
                                               float (*s_red)[DVS], float *s_u) {
     const int tid = threadIdx.x, cg = tid % (DVS / 4), rg = tid / (DVS / 4);
@@ -187,7 +188,7 @@ __device__ __forceinline__ void forward_token(const BwdParams &p, const Stage<DK
 #pragma unroll
     for (int m = 0; m < R; ++m) {
         const int i = rg + RG * m;
-        const float kk = s.k[i] * kn, kx = p.decayed_read ? s.a[i] * kk : kk;
+        const float kk = s.k[i] * kn, kx = DR ? s.a[i] * kk : kk;
         r.x = fmaf(S[m].x, kx, r.x); r.y = fmaf(S[m].y, kx, r.y);
         r.z = fmaf(S[m].z, kx, r.z); r.w = fmaf(S[m].w, kx, r.w);
     }
@@ -211,7 +212,8 @@ __device__ __forceinline__ void forward_token(const BwdParams &p, const Stage<DK
 
 // Forward pass: the state before every chunk, per (sequence, head, slab).  Each token's
 // inputs are fetched one token ahead; the stage is double-buffered, so three syncs a token.
-template <typename Tin, int DK, int DVS>
+// DR: the delta term reads the decayed state (the decayed read), a compile-time choice
+template <typename Tin, int DK, int DVS, bool DR>
 __global__ void __launch_bounds__(kThreads) bwd_ckpt_kernel(BwdParams p) {
     using Ly = BwdLayout<DVS>;
     constexpr int TPR = Ly::TPR, RG = Ly::RG, R = DK / RG;
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(kThreads) bwd_ckpt_kernel(BwdParams p) {
             put_token<Tin, DK, DVS>(p, ring[j], false, s);
             __syncthreads();
             if (t + kAhead < p.T) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + kAhead, h, col0, false, ring[j]);
-            forward_token<DK, DVS, RG, R>(p, s, S, s_red, s_u);
+            forward_token<DK, DVS, RG, R, DR>(p, s, S, s_red, s_u);
         }
     }
 }
@@ -267,7 +269,7 @@ __device__ __forceinline__ float row_sum(float x) {
 
 // Backward pass, per (sequence, head, slab).  Inputs fetched one token ahead (forwards in the
 // recomputation, backwards in the walk) into a double-buffered stage, as in the forward pass.
-template <typename Tin, int DK, int DVS>
+template <typename Tin, int DK, int DVS, bool DR>
 __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
     using Ly = BwdLayout<DVS>;
     constexpr int TPR = Ly::TPR, RG = Ly::RG, R = DK / RG;
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
             put_token<Tin, DK, DVS>(p, cur, false, s);
             __syncthreads();
             if (t + 1 < t1) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + 1, h, col0, false, nxt);
-            forward_token<DK, DVS, RG, R>(p, s, Hp, s_red[0], s_u);
+            forward_token<DK, DVS, RG, R, DR>(p, s, Hp, s_red[0], s_u);
             cur = nxt;
         }
 #pragma unroll
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
 #pragma unroll
             for (int m = 0; m < R; ++m) {
                 const int i = rg + RG * m;
-                const float qq = s.q[i] * qn, kk = s.k[i] * kn, kx = p.decayed_read ? s.a[i] * kk : kk;
+                const float qq = s.q[i] * qn, kk = s.k[i] * kn, kx = DR ? s.a[i] * kk : kk;
                 dH[m].x = fmaf(qq, do4.x, dH[m].x); dH[m].y = fmaf(qq, do4.y, dH[m].y);
                 dH[m].z = fmaf(qq, do4.z, dH[m].z); dH[m].w = fmaf(qq, do4.w, dH[m].w);
                 r.x = fmaf(Hp[m].x, kx, r.x); r.y = fmaf(Hp[m].y, kx, r.y);
@@ -377,8 +379,8 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
                 // sums over this thread's four columns, then over the row's TPR threads
                 float dq_i = row_sum<TPR>(dot4(Hc[m], do4));
                 const float hu = dot4(Hp[m], du4);   // sum_j h_{t-1}[i,j] du_j
-                float dk_i = row_sum<TPR>(dot4(dH[m], u4) - bt * (p.decayed_read ? a : 1.f) * hu);
-                float de_i = row_sum<TPR>(dot4(dH[m], Hp[m]) - (p.decayed_read ? bt * kk * hu : 0.f));
+                float dk_i = row_sum<TPR>(dot4(dH[m], u4) - bt * (DR ? a : 1.f) * hu);
+                float de_i = row_sum<TPR>(dot4(dH[m], Hp[m]) - (DR ? bt * kk * hu : 0.f));
                 if (cg == 0) {
                     atomicAdd(p.dq + kd_off + i, dq_i);
                     atomicAdd(p.dk + kd_off + i, dk_i);
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
                 }
                 dd = fmaf(a, de_i, dd);
                 // dh for the state before token t
-                const float kb = bt * (p.decayed_read ? a * kk : kk);
+                const float kb = bt * (DR ? a * kk : kk);
                 dH[m].x = fmaf(a, dH[m].x, -kb * du4.x); dH[m].y = fmaf(a, dH[m].y, -kb * du4.y);
                 dH[m].z = fmaf(a, dH[m].z, -kb * du4.z); dH[m].w = fmaf(a, dH[m].w, -kb * du4.w);
                 Hc[m] = Hp[m];
@@ -459,12 +461,23 @@ cudaError_t run_bwd(const BwdParams &p, long rows, cudaStream_t s) {
     const bool narrow = p.DV < kSlab || (long)p.nseq * p.H * (p.DV / kSlab) < nsm;
     const int dvs = narrow ? 32 : kSlab;
     const long grid = (long)p.nseq * p.H * (p.DV / dvs);
+    const bool dr = p.decayed_read != 0;
     if (dvs == 64) {
-        bwd_ckpt_kernel<Tin, DK, 64><<<(unsigned)grid, kThreads, 0, s>>>(p);
-        bwd_kernel<Tin, DK, 64><<<(unsigned)grid, kThreads, 0, s>>>(p);
+        if (dr) {
+            bwd_ckpt_kernel<Tin, DK, 64, true><<<(unsigned)grid, kThreads, 0, s>>>(p);
+            bwd_kernel<Tin, DK, 64, true><<<(unsigned)grid, kThreads, 0, s>>>(p);
+        } else {
+            bwd_ckpt_kernel<Tin, DK, 64, false><<<(unsigned)grid, kThreads, 0, s>>>(p);
+            bwd_kernel<Tin, DK, 64, false><<<(unsigned)grid, kThreads, 0, s>>>(p);
+        }
     } else {
-        bwd_ckpt_kernel<Tin, DK, 32><<<(unsigned)grid, kThreads, 0, s>>>(p);
-        bwd_kernel<Tin, DK, 32><<<(unsigned)grid, kThreads, 0, s>>>(p);
+        if (dr) {
+            bwd_ckpt_kernel<Tin, DK, 32, true><<<(unsigned)grid, kThreads, 0, s>>>(p);
+            bwd_kernel<Tin, DK, 32, true><<<(unsigned)grid, kThreads, 0, s>>>(p);
+        } else {
+            bwd_ckpt_kernel<Tin, DK, 32, false><<<(unsigned)grid, kThreads, 0, s>>>(p);
+            bwd_kernel<Tin, DK, 32, false><<<(unsigned)grid, kThreads, 0, s>>>(p);
+        }
     }
     const long rh = rows * p.H;
     bwd_finish_kernel<Tin, DK><<<(unsigned)((rh * 32 + 255) / 256), 256, 0, s>>>(p, rh);
