@@ -52,3 +52,42 @@ def test_gradients_match_finite_differences(decayed, use_l2):
             fd[idx] = (loss(p) - loss(m)) / (2 * eps)
         err = np.max(np.abs(fd - grads["d" + name])) / max(np.max(np.abs(fd)), 1e-12)
         assert err < 1e-7, (name, err)
+
+
+@pytest.mark.parametrize("decayed", [False, True])
+def test_scalar_decay_gradient_is_the_channel_sum(oracle_mod, decayed):
+    """One decay per head (the path's own recurrence, run by the C oracle's scalar scan): the
+    gradient of that decay is the sum over key channels of the per-channel dg, checked against
+    central differences of the C oracle's forward.  The C oracle rounds its inputs to float32,
+    so the step is 1e-3 and the bar 1e-3 (rounding ~6e-5, truncation ~1e-6 relative)."""
+    from oracle import backward as ob
+    rng = np.random.default_rng(7)
+    B, T, H, dk, dv = 1, 6, 2, 4, 3
+    q, k = rng.standard_normal((B, T, H, dk)), rng.standard_normal((B, T, H, dk))
+    v = rng.standard_normal((B, T, H, dv))
+    beta = rng.uniform(0.1, 0.9, (B, T, H))
+    dec = -rng.uniform(0.05, 1.0, (B, T, H))
+    h0 = rng.standard_normal((B, H, dk, dv))
+    do = rng.standard_normal((B, T, H, dv))
+    dhT = rng.standard_normal((B, H, dk, dv))
+    g = np.repeat(dec[..., None], dk, axis=-1)
+    grads = ob.backward(q, k, v, beta, g, h0, do, dhT, use_l2=True, decayed_read=decayed)
+    dd = grads["dg"].sum(-1)
+
+    def loss(dc):
+        if decayed:   # the decayed read with one decay per head: the per-channel scan, channels equal
+            o, h = oracle_mod.forward_gk(q, k, v, beta, np.repeat(dc[..., None], dk, axis=-1), h0,
+                                         decayed_read=True)
+        else:
+            o, h = oracle_mod.forward(q, k, v, beta, dc, h0)
+        return float((o * do).sum() + (h * dhT).sum())
+
+    eps = 1e-3   # the C oracle takes float32 inputs
+    fd = np.zeros_like(dec)
+    for idx in np.ndindex(dec.shape):
+        p, m = dec.copy(), dec.copy()
+        p[idx] += eps
+        m[idx] -= eps
+        fd[idx] = (loss(p) - loss(m)) / (2 * eps)
+    err = np.max(np.abs(fd - dd)) / np.max(np.abs(fd))
+    assert err < 1e-3, err
