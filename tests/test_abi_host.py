@@ -135,8 +135,17 @@ def test_python_binding_refuses_host_tensors():
     import torch
     import delta_rule_linear_gb300 as kda
     x = torch.zeros(1, 4, 1, 32)
+    b = torch.zeros(1, 4, 1)
+    h = torch.zeros(1, 1, 32, 32)
     with pytest.raises(ValueError):
-        kda.chunk_fwd(x, x, x, torch.zeros(1, 4, 1), chunk_size=16)
+        kda.chunk_fwd(x, x, x, b, chunk_size=16)
+    for call in (lambda: kda.recurrent_fwd(x, x, x, b),
+                 lambda: kda.decode_step(x[:, :1], x[:, :1], x[:, :1], b[:, :1], None, h),
+                 lambda: kda.gk_recurrent_fwd(x, x, x, b, x),
+                 lambda: kda.recurrent_bwd(x, x, x, b, b, h, x),
+                 lambda: kda.gk_recurrent_bwd(x, x, x, b, x, h, x)):
+        with pytest.raises(ValueError):
+            call()
 
 
 def test_diag_wait_timeout_argument_errors(lib):
