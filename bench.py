@@ -36,16 +36,88 @@ from kda_inputs import (WORKLOADS, make_custom, make_decode_state, make_decode_s
 
 METRIC = "prefill tokens/s & % bf16 TC peak; decode state GB/s vs HBM peak (1×GB300)"
 NOMINAL_HBM_GBS = 8000.0
-# DRAM bytes (read + write) per launch from one ncu capture of the kernel as it is
-# now; set to None whenever that kernel changes until it is captured again.
-#   decode: profiles/decode_scan_kernel_b256_h32_d128.md
-#   prefill: profiles/tc_kernel_long_prefill_d128.md
-NCU_TRAFFIC = {"decode": 543.26e6 + 478.36e6, "prefill": 1.27393e9 + 796.65e6}
-# sm__pipe_tensor_cycles_active (fraction of elapsed) of the prefill kernel, from the
-# mid-size (T=8192) full capture in profiles/tc_kernel_long_prefill_d128.md; None once the
-# kernel changes until it is captured again.
-NCU_TENSOR_PIPE = {"prefill": 0.146}
+# Counters of one ncu capture per kernel (DRAM bytes read + written per launch, tensor-pipe
+# activity) live in profiles/ncu_counters.txt together with a hash of the kernel's sources
+# at capture time; a figure is reported only while those sources are unchanged (null
+# otherwise), and `--record-counters` writes a new capture's figures there.
+COUNTERS_FILE = os.path.join(ROOT, "profiles", "ncu_counters.txt")
+COUNTER_SOURCES = {   # the sources each kernel's counters depend on
+    "prefill": ["delta_rule_linear_gb300/csrc/chunk_tc.cu", "delta_rule_linear_gb300/csrc/tc_ptx.cuh"],
+    "decode": ["delta_rule_linear_gb300/csrc/scan.cu"],
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def sources_hash(kind):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in COUNTER_SOURCES[kind]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(rel.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_counters(kind):
+    """The recorded ncu figures of `kind` if its sources are unchanged since the capture:
+    {"dram_bytes_per_launch", "tensor_pipe_active", "capture"}, else None."""
+    try:
+        with open(COUNTERS_FILE) as f:
+            rec = json.load(f).get(kind)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("sources") != sources_hash(kind):
+        return None
+    return rec
+
+
+def record_counters(kind, csv_path, kernel_regex, scale=1.0, note=""):
+    """Parse an ncu --csv capture (raw page or --metrics list), average the DRAM bytes and
+    tensor-pipe activity over the launches of the kernels matching `kernel_regex`, scale
+    the bytes to one full launch (`scale`: units of the full launch / units captured) and
+    store them with the current hash of the kernel's sources."""
+    import csv
+    import re
+    rows = list(csv.reader(open(csv_path, newline="")))
+    head_i = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    head = rows[head_i]
+    kcol = head.index("Kernel Name")
+    launches = {}
+    if "Metric Name" in head:   # --metrics list: one row per (launch, metric)
+        idcol, mcol, vcol = head.index("ID"), head.index("Metric Name"), head.index("Metric Value")
+        for r in rows[head_i + 1:]:
+            if len(r) > vcol and re.search(kernel_regex, r[kcol]):
+                launches.setdefault(r[idcol], {})[r[mcol]] = float(r[vcol].replace(",", ""))
+    else:                       # raw page: one row per launch, one column per metric
+        for n, r in enumerate(rows[head_i + 2:]):
+            if len(r) > kcol and re.search(kernel_regex, r[kcol]):
+                launches[n] = {m: float(r[i].replace(",", "")) for i, m in enumerate(head)
+                               if m.startswith(("dram__bytes", "sm__pipe_tensor")) and r[i].strip()}
+    if not launches:
+        raise SystemExit(f"no launch of {kernel_regex!r} in {csv_path}")
+    rd = [l.get("dram__bytes_read.sum", 0.0) + l.get("dram__bytes_write.sum", 0.0) for l in launches.values()]
+    tp = [l[m] for l in launches.values() for m in l if m.startswith("sm__pipe_tensor_cycles_active")]
+    try:
+        with open(COUNTERS_FILE) as f:
+            allrec = json.load(f)
+    except (OSError, ValueError):
+        allrec = {}
+    allrec[kind] = {"sources": sources_hash(kind),
+                    "dram_bytes_per_launch": statistics.mean(rd) * scale if any(rd) else None,
+                    "tensor_pipe_active": (statistics.mean(tp) / 100.0) if tp else None,
+                    "launches_captured": len(launches), "scale_to_full_launch": scale,
+                    "capture": note}
+    with open(COUNTERS_FILE, "w") as f:
+        json.dump(allrec, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps(allrec[kind]))
+
+
+def headline_config(wl, world):
+    """The config dict both arms print for the headline workload."""
+    return {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "dk": wl.dk,
+            "dv": wl.dv, "chunk_size": wl.chunk, "state": "fp32 carried in",
+            "l2_flush": "none: inputs (805 MB) and decode state (512 MiB) exceed L2",
+            "parallelism": f"replicas x{world}"}
 
 
 def counted_prefill_flops(B, T, H, dk, dv, C):
@@ -337,15 +409,18 @@ def bench_prefill(args, world, rank, dev, peaks, d):
     peak_tf = peaks["bf16_tflops"]
     achieved_tf = flops / (ms * 1e-3) / 1e12
     min_bytes = B * T * H * (2 * dk + 2 * dv) * 2 + B * T * H * 8 + 2 * B * H * dk * dv * 4
+    ctr = recorded_counters("prefill") if not args.prefill_T else None
     return {
         "ms": ms_max, "tokens_per_s": tokens * world / (ms_max * 1e-3),
         "clocks": clk.summary(),
         "roofline": {"bound": "tensor", "achieved": round(achieved_tf, 3), "peak": peak_tf,
-                     "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 5), "traffic": NCU_TRAFFIC["prefill"],
+                     "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 5),
+                     "traffic": (ctr or {}).get("dram_bytes_per_launch"),
+                     "traffic_capture": (ctr or {}).get("capture", "none for the kernel as built"),
                      "kernel": "tc_kernel (the whole step: one launch holds the prep groups and the chains)",
                      "flops_per_launch": flops,
                      "recurrence_min_flops": 6.0 * B * T * H * dk * dv,
-                     "ncu_tensor_pipe_active": NCU_TENSOR_PIPE["prefill"],
+                     "ncu_tensor_pipe_active": (ctr or {}).get("tensor_pipe_active"),
                      "hbm_frac_of_min_bytes": round(min_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5)},
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -712,12 +787,15 @@ def bench_decode(args, world, rank, dev, peaks):
     ms_max = max_over_ranks(ms, world)
     state_bytes = 2.0 * wl.B * wl.H * wl.dk * wl.dv * 4
     gbs = state_bytes / (ms * 1e-3) / 1e9
+    ctr = recorded_counters("decode")
     return {
         "ms_per_decode_step": ms_max, "steps": nsteps,
         "state_GBps": state_bytes * world / (ms_max * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                     "frac_of_8TBps_nominal": round(gbs / NOMINAL_HBM_GBS, 4), "traffic": NCU_TRAFFIC["decode"],
+                     "frac_of_8TBps_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+                     "traffic": (ctr or {}).get("dram_bytes_per_launch"),
+                     "traffic_capture": (ctr or {}).get("capture", "none for the kernel as built"),
                      "kernel": "decode step", "bytes_per_launch": state_bytes},
         "clocks": clk.summary(),
         "gpu_launches": nsteps,
@@ -768,8 +846,7 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "dk": wl.dk,
-                   "dv": wl.dv, "chunk_size": wl.chunk},
+        "config": headline_config(wl, args.gpus),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
                          "sample": f"{heads} of {wl.H} heads x full T={wl.T}, per step; "
                                    "tokens/s scaled by heads/H"},
@@ -790,7 +867,17 @@ def main():
                     help="run one workload (profiling); the default runs both")
     ap.add_argument("--prefill-T", type=int, default=0,
                     help="profiling only: override T of the prefill workload (no CPU baseline)")
+    ap.add_argument("--record-counters", nargs=3, metavar=("KIND", "CSV", "KERNEL_REGEX"),
+                    help="store the DRAM bytes and tensor-pipe activity of an ncu --csv capture "
+                         "as the counters of KIND (prefill|decode) for the current sources; no GPU")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="with --record-counters: full-launch units / captured units")
+    ap.add_argument("--note", default="", help="with --record-counters: the capture command")
     args = ap.parse_args()
+    if args.record_counters:
+        kind, csv_path, regex = args.record_counters
+        record_counters(kind, csv_path, regex, args.scale, args.note)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -843,10 +930,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "dk": wl.dk,
-                   "dv": wl.dv, "chunk_size": wl.chunk, "state": "fp32 carried in",
-                   "l2_flush": "none: inputs (805 MB) and decode state (512 MiB) exceed L2",
-                   "parallelism": f"replicas x{world}"},
+        "config": headline_config(wl, world),
         "roofline": pre["roofline"],
         "cpu_baseline": cpu,
         "e2e": pre["e2e"],

@@ -36,8 +36,7 @@
  *        "Functional warning": the exact chunked form uses the per-channel
  *        factor exp(gc_i - gc_j) inside the chunk; the recurrent form is exact.
  *
- * Readings taken where the page is silent (each also listed in the design
- * notes of the repository):
+ * Readings taken where the page is silent:
  *   - h is [dk,dv], so "h @ k" is read as h^T k (a dv-vector) and the write
  *     "k (x) u" is the outer product k u^T.
  *   - The delta term reads the undecayed h_{t-1}, literally as printed.
