@@ -259,9 +259,10 @@ def chunk_fwd_noalloc(q, k, v, beta, decay=None, initial_state=None, *, scale=No
     """kda_chunk_fwd_noalloc: chunked prefill with the library's built-in scratch.
 
     For callers that cannot hand over device memory for a workspace.  bf16 q/k/v with
-    dk == dv in {64, 128} and chunk 64 only; raises KdaError(KDA_ERR_WORKSPACE) when the
-    problem needs more than the built-in 64 MiB.  Calls that overlap on the GPU race on
-    that one buffer, so keep them ordered.  Returns (o, final_state).
+    dk == dv in {64, 128} and chunk 64 only; the scratch is the library's built-in 48 MiB
+    array, which every such problem fits.  Calls that overlap on the GPU race on that one
+    buffer, so keep them ordered.  query_device_error(None) reads its error word.
+    Returns (o, final_state).
     """
     lib = load()
     B, T, H, dk = q.shape
@@ -522,7 +523,8 @@ def gk_decode_step(q, k, v, beta, g, state, *, scale=None, use_qk_l2norm=True, o
 
 
 def query_device_error(workspace, stream=None) -> int:
-    """kda_query_device_error: device error word of the last call on ``workspace`` (0 = none)."""
+    """kda_query_device_error: device error word of the last call on ``workspace`` (0 = none);
+    ``workspace=None``: the built-in array of chunk_fwd_noalloc on the current device."""
     return int(load().kda_query_device_error(_ptr(workspace), _stream(stream)))
 
 

@@ -31,12 +31,17 @@
 //    V_c by TMA; an MMA warp issues; eight warps turn the next state into the next
 //    operand, four others store o.
 //
-// When the (sequence, head) pairs fill at most half of the SMs, both roles run in one
-// cooperative launch: the first CTAs are chains, the rest prep groups that produce the
-// chunks in chunk-major order and publish each E_c with a release flag, which the
-// chain polls (acquire) before its TMA load.  The chains then run alongside the prep
-// work instead of after it.  Otherwise prep runs as its own persistent launch,
-// followed by the chain launch.
+// Both roles run in one cooperative launch.  The first nch <= SMs/4 CTAs are chains; chain
+// i walks the (sequence, head) tasks i, i + nch, i + 2 nch, ... (packed sequences sorted
+// longest first), one round of nch tasks after another.  The other CTAs hold the prep
+// groups, which take the chunks in (column, chain) order -- column = the chunk's position
+// in its chain's walk -- so that every chain's next chunks are built first.  E_c goes
+// into a ring of kRing slots per chain: the prep publishes a slot by a release store of
+// the chunk's column + 1 to the slot's flag, the chain acquires it before its TMA load and,
+// once the load has landed, releases its own "consumed" counter; a prep group waits for
+// that counter before it overwrites a slot, so it never runs more than kRing chunks ahead
+// of its chain.  The scratch is thus a few MB whatever the sequence length, and E_c lives
+// and dies in L2.
 //
 // Every wait (mbarrier or flag) is bounded; on time-out the kernel records
 // KDA_ERR_DEVICE_TIMEOUT in the workspace header and unwinds (no trap).
@@ -55,13 +60,19 @@ constexpr int kC = 64;                        // chunk length
 constexpr uint64_t kWaitNs = 2000000000ull;   // bounded waits: 2 s
 constexpr int kStatusDeviceTimeout = 8;       // KDA_ERR_DEVICE_TIMEOUT
 
+// E_c slots per chain: the prep's working front spans (prep groups / chains) columns (7.5
+// for 32 chains on a 152-SM part), which the ring must hold with room to spare
+constexpr int kRing = 16;
+constexpr int kMaxChains = 40;                // chain CTAs at most
+
 struct TcParams {
     int nseq, H, T;            // T: equal-length sequence length (unused for varlen)
     int use_l2;
     float scale;
     const int *cu_seqlens;     // nullptr: equal length
-    const int *chunk_base;     // varlen: [nseq + 1] chunk prefix, device
-    int nc_equal;              // equal length: chunks per sequence
+    const int *order;          // varlen: sequence indices by decreasing length [nseq] (device)
+    const int *round_base;     // varlen: [rounds + 1] first column of each round (device)
+    int nc_equal;              // equal length: chunks per sequence (= columns per round)
     const float *beta, *decay; // [rows, H]
     const float *gk;           // per-key-channel decay [rows, H, D] (per-channel kernels) or nullptr
     int decayed_read;          // the delta term reads the decayed state
@@ -75,16 +86,14 @@ struct TcParams {
     const __nv_bfloat16 *q, *k;   // [rows, H, D]
     long rows;                 // token rows of q, k, v
     __nv_bfloat16 *o;          // [rows, H, D]
-    __nv_bfloat16 *E;          // scratch: [slots][D + 64][D + 64]
-    uint32_t *flags;           // scratch: [slots], E_c published (single-launch mode) or nullptr
+    __nv_bfloat16 *E;          // scratch: the rings, [nch * kRing][D + 64][D + 64]
+    uint32_t *flags;           // [nch * kRing]: column + 1 of the E_c a slot holds
+    uint32_t *consumed;        // [nch]: chain i has loaded every E_c of a column below this
     WsHeader *ws;
-    long nsh;                  // (sequence, head) pairs
-    long n_items;              // prep work items (valid or not)
-    int maxnc;                 // chunk-major items: chunks of the longest sequence
-    int chunk_major;           // items ordered (chunk, sequence, head) instead of by slot
-    int nchain;                // CTAs with the chain role (the first ones)
+    int ntask;                 // (sequence, head) tasks
+    int nch;                   // chain CTAs (the first ones)
+    int rounds;                // ceil(ntask / nch)
 };
-
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
@@ -93,12 +102,12 @@ __device__ __forceinline__ void record_error(WsHeader *ws, int where) {
     if (ws && atomicCAS(&ws->error, 0, kStatusDeviceTimeout) == 0) ws->where = where;
 }
 
-// Wait until another CTA has released *f (gpu-scope acquire), giving up after limit_ns;
-// on success the async proxy is ordered after the acquire (for a TMA load of the data the
-// flag publishes).
-__device__ __forceinline__ bool wait_flag_acquire(const uint32_t *f, uint64_t limit_ns) {
+// Wait until another CTA has released *f with a value of at least `want` (gpu-scope
+// acquire), giving up after limit_ns; on success the async proxy is ordered after the
+// acquire (for a TMA load of the data the flag publishes).
+__device__ __forceinline__ bool wait_flag_acquire(const uint32_t *f, uint32_t want, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire_gpu(f) == 0u) {
+    while (ld_acquire_gpu(f) < want) {
         if (globaltimer_ns() - t0 > limit_ns) return false;
         __nanosleep(64);
     }
@@ -115,52 +124,59 @@ __device__ __forceinline__ void seq_info(const TcParams &p, int n, long &start, 
         len = p.T;
     }
 }
-__device__ __forceinline__ int chunk_base_of(const TcParams &p, int n) {
-    return p.cu_seqlens ? p.chunk_base[n] : n * p.nc_equal;
+// First column of round r (the chain walk's position where its r-th task begins); r may
+// be p.rounds (the total).
+__device__ __forceinline__ int round_start(const TcParams &p, int r) {
+    return p.cu_seqlens ? p.round_base[r] : r * p.nc_equal;
+}
+// Task -> (sequence, head): tasks run over the sequences in the order table (longest
+// first) and, within a sequence, over its heads.
+__device__ __forceinline__ void task_info(const TcParams &p, int task, int &n, int &h) {
+    const int rank = task / p.H;
+    h = task - rank * p.H;
+    n = p.order ? p.order[rank] : rank;
 }
 
 // One prep work item: chunk c of sequence n, head h.
 struct ChunkItem {
-    long row0, slot;   // first token row; E_c slot (= flag index)
+    long row0;         // first token row
+    int slot;          // E_c ring slot (= flag index)
+    int col;           // column: the chunk's position in its chain's walk
+    int chain;         // the chain that consumes it
     int h, nv;         // head; valid tokens in the chunk (1..64)
 };
 
-// Work item `item` -> chunk.  Chunk-major order (chunk, then (sequence, head)) lets the
-// chains of the single-launch mode start as soon as the first chunks are built; slot
-// order is compact for varlen batches.  Returns false for an item past a sequence's end.
+// Prep work items in (column, chain) order: item = column * nch + chain.  Returns false
+// for an item past its task's last chunk or past the last task.
 __device__ __forceinline__ bool item_info(const TcParams &p, long item, ChunkItem &it) {
-    // item < (chunks x heads) < 2^31 (the E_c scratch bounds it), so 32-bit division is exact
+    // item < columns x nch < 2^31 (checked on the host), so 32-bit division is exact
     const unsigned u = (unsigned)item;
-    int n, c;
-    if (p.chunk_major) {
-        const unsigned nsh = (unsigned)p.nsh, j = u % nsh;
-        c = (int)(u / nsh);
-        n = (int)(j / (unsigned)p.H);
-        it.h = (int)(j % (unsigned)p.H);
-    } else {
-        const long g = (long)(u / (unsigned)p.H);
-        it.h = (int)(u % (unsigned)p.H);
-        if (p.cu_seqlens) {
-            if (g >= p.chunk_base[p.nseq]) return false;
-            int lo = 0, hi = p.nseq;
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (p.chunk_base[mid] <= g) lo = mid; else hi = mid;
-            }
-            n = lo;
-            c = (int)(g - p.chunk_base[n]);
-        } else {
-            n = (int)(g / p.nc_equal);
-            c = (int)(g % p.nc_equal);
+    const int col = (int)(u / (unsigned)p.nch), chain = (int)(u % (unsigned)p.nch);
+    int r;
+    if (p.cu_seqlens) {
+        int lo = 0, hi = p.rounds;   // round_base[lo] <= col < round_base[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.round_base[mid] <= col) lo = mid; else hi = mid;
         }
+        r = lo;
+    } else {
+        r = col / p.nc_equal;
     }
+    const int task = r * p.nch + chain;
+    if (task >= p.ntask) return false;
+    const int c = col - round_start(p, r);
+    int n;
+    task_info(p, task, n, it.h);
     long start;
     int len;
     seq_info(p, n, start, len);
     if ((long)c * kC >= len) return false;
     it.row0 = start + (long)c * kC;
     it.nv = min(kC, len - c * kC);
-    it.slot = (long)(chunk_base_of(p, n) + c) * p.H + it.h;
+    it.col = col;
+    it.chain = chain;
+    it.slot = chain * kRing + col % kRing;
     return true;
 }
 
@@ -237,168 +253,49 @@ __device__ __forceinline__ void put_b(const BTiles &bt, int t, int s, const floa
 
 // ---------------------------------------------------------------------------------
 // T = (I + L)^{-1} for a 64 x 64 strictly-lower L, fp32 in shared memory (row pitch
-// kLP = 68 floats: 16-byte aligned rows), by the NT = 256 threads of one group (named
-// barrier `bar`), on the 4 x 4 grid of 16 x 16 blocks:
-//  * the diagonal blocks T_ii by forward substitution, one lane per column, the column
-//    in registers, each row of L read with 16-byte loads;
-//  * the off-diagonal blocks  T_ij = -T_ii X_ij,  X_ij = sum_{k=j}^{i-1} L_ik T_kj,
-//    with X_ij accumulated as soon as each T_kj is known, in four steps
-//      X_10 X_21 X_32 X_20 | T_10 T_21 T_32, X_31 | X_20 X_31 X'_30 | T_20 T_31 T_30
-//    in which every thread takes 4 or 2 consecutive outputs of one row.  The corner block
-//    skips the wait for T_20: with X'_30 = L_30 T_00 + L_31 T_10 (no L_32 T_20 term),
-//    T_30 = -T_33 (X'_30 + L_32 T_20) and T_20 = -T_22 X_20, T_32 = -T_33 L_32 T_22 give
-//    T_30 = -(T_32 X_20 + T_33 X'_30), both factors known after the third step (the
-//    2 x 2 block form of the inverse of a lower-triangular matrix).
-// The unused upper blocks of L hold the partial sums X_ij (X_ij in block (j, i)).
+// kLP = 68 floats: 16-byte aligned rows, and conflict-free A-fragment loads), by the
+// NT = 256 threads of one group (named barrier `bar`), on the 4 x 4 grid of 16 x 16 blocks
+// (the 2 x 2 block form of the inverse of a lower-triangular matrix, applied twice):
+//  * the diagonal blocks D_i = (I + L_ii)^{-1} by forward substitution, one lane per
+//    column, the column in registers, each row of L read with 16-byte loads;
+//  * T_10 = -D_1 (L_10 D_0) and T_32 = -D_3 (L_32 D_2), one warp each;
+//  * with A = blocks 0-1 and B = blocks 2-3:  T_BA = -T_BB (L_BA T_AA), the 32 x 32
+//    products split into 16 x 8 tiles, one per warp.
+// The off-diagonal products run on the tensor cores as warp-level tf32 MMAs (m16n8k8,
+// fp32 accumulation; operands rounded to tf32, which keeps 10 fraction bits -- T goes on
+// to the bf16 operands B = [T' | P] with 7).  Intermediate products sit in the unused
+// upper blocks of L.  Every block of T is written into B and Bf as soon as it is known.
 // ---------------------------------------------------------------------------------
 constexpr int kLP = 68;
 
-// X_ij[r][c0 .. c0+W) = (acc ? X_ij : 0) + sum_{k in [k0,k1)} L_ik T_kj   (X_ij in L's upper block (j, i))
-template <int W>
-__device__ __forceinline__ void inv_op_x(float *sL, const float *sT, int i, int j, int k0, int k1,
-                                         bool accumulate, int r, int c0) {
-    constexpr int P = kLP;
-    float *X = sL + (16 * j + r) * P + 16 * i + c0;
-    if constexpr (W >= 2) {   // W/2 pairs of outputs, paired FMAs
-        float2 acc[W / 2];
-        if (accumulate) {
-#pragma unroll
-            for (int e = 0; e < W / 2; ++e) acc[e] = reinterpret_cast<const float2 *>(X)[e];
-        } else {
-#pragma unroll
-            for (int e = 0; e < W / 2; ++e) acc[e] = make_float2(0.f, 0.f);
-        }
-        for (int k = k0; k < k1; ++k) {
-            const float *Lr = sL + (16 * i + r) * P + 16 * k;
-            float l[16];
-#pragma unroll
-            for (int m4 = 0; m4 < 4; ++m4) {
-                const float4 v = *reinterpret_cast<const float4 *>(Lr + 4 * m4);
-                l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
-            }
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float2 *Tr = reinterpret_cast<const float2 *>(sT + (16 * k + m) * P + 16 * j + c0);
-                const float2 lm = make_float2(l[m], l[m]);
-                if constexpr (W == 4) {
-                    const float4 t = *reinterpret_cast<const float4 *>(Tr);
-                    fma2(acc[0], lm, make_float2(t.x, t.y));
-                    fma2(acc[1], lm, make_float2(t.z, t.w));
-                } else {
-                    fma2(acc[0], lm, Tr[0]);
-                }
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < W / 2; ++e) reinterpret_cast<float2 *>(X)[e] = acc[e];
-    } else {
-        float acc = accumulate ? X[0] : 0.f;
-        for (int k = k0; k < k1; ++k) {
-            const float *Lr = sL + (16 * i + r) * P + 16 * k;
-            float l[16];
-#pragma unroll
-            for (int m4 = 0; m4 < 4; ++m4) {
-                const float4 v = *reinterpret_cast<const float4 *>(Lr + 4 * m4);
-                l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
-            }
-#pragma unroll
-            for (int m = 0; m < 16; ++m) acc = fmaf(l[m], sT[(16 * k + m) * P + 16 * j + c0], acc);
-        }
-        X[0] = acc;
-    }
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
-
-// T_ij[r][c0 .. c0+W) = -(T_ii X_ij)[r][c0 ..), also written into B and Bf
-template <int W, bool PO>
-__device__ __forceinline__ void inv_op_t(const float *sL, float *sT, const BTiles &bt, int i, int j,
-                                         int r, int c0) {
-    constexpr int P = kLP;
-    const float *Ar = sT + (16 * i + r) * P + 16 * i;
-    float a[16];
-#pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 v = *reinterpret_cast<const float4 *>(Ar + 4 * m4);
-        a[4 * m4] = v.x; a[4 * m4 + 1] = v.y; a[4 * m4 + 2] = v.z; a[4 * m4 + 3] = v.w;
-    }
-    float acc[W];
-    if constexpr (W >= 2) {
-        float2 pr[W / 2];
-#pragma unroll
-        for (int e = 0; e < W / 2; ++e) pr[e] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float2 *Xr = reinterpret_cast<const float2 *>(sL + (16 * j + m) * P + 16 * i + c0);
-            const float2 am = make_float2(a[m], a[m]);
-            if constexpr (W == 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(Xr);
-                fma2(pr[0], am, make_float2(x.x, x.y));
-                fma2(pr[1], am, make_float2(x.z, x.w));
-            } else {
-                fma2(pr[0], am, Xr[0]);
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < W / 2; ++e) {
-            acc[2 * e] = pr[e].x;
-            acc[2 * e + 1] = pr[e].y;
-        }
-    } else {
-        acc[0] = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) acc[0] = fmaf(a[m], sL[(16 * j + m) * P + 16 * i + c0], acc[0]);
-    }
-#pragma unroll
-    for (int e = 0; e < W; ++e) acc[e] = -acc[e];
-    float *Tij = sT + (16 * i + r) * P + 16 * j + c0;
-    if constexpr (W == 4) *reinterpret_cast<float4 *>(Tij) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    else if constexpr (W == 2) *reinterpret_cast<float2 *>(Tij) = make_float2(acc[0], acc[1]);
-    else Tij[0] = acc[0];
-    put_b<W, PO>(bt, 16 * i + r, 16 * j + c0, acc);
+// d += a b, m16n8k8, tf32 operands, fp32 accumulators
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
-
-// T_ij[r][c0 .. c0+W) = -(T_ik X_kj + T_ii X_ij)[r][c0 ..), X_kj and X_ij in L's upper blocks
-// (j, k) and (j, i); also written into B and Bf
-template <int W, bool PO>
-__device__ __forceinline__ void inv_op_t2(const float *sL, float *sT, const BTiles &bt, int i, int k, int j,
-                                          int r, int c0) {
-    static_assert(W == 2 || W == 4, "paired outputs");
-    constexpr int P = kLP;
-    float2 pr[W / 2];
-#pragma unroll
-    for (int e = 0; e < W / 2; ++e) pr[e] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int term = 0; term < 2; ++term) {
-        const int kk = term == 0 ? k : i;   // T_ik X_kj, then T_ii X_ij
-        const float *Ar = sT + (16 * i + r) * P + 16 * kk;
-        float a[16];
-#pragma unroll
-        for (int m4 = 0; m4 < 4; ++m4) {
-            const float4 v = *reinterpret_cast<const float4 *>(Ar + 4 * m4);
-            a[4 * m4] = v.x; a[4 * m4 + 1] = v.y; a[4 * m4 + 2] = v.z; a[4 * m4 + 3] = v.w;
-        }
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float2 *Xr = reinterpret_cast<const float2 *>(sL + (16 * j + m) * P + 16 * kk + c0);
-            const float2 am = make_float2(a[m], a[m]);
-            if constexpr (W == 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(Xr);
-                fma2(pr[0], am, make_float2(x.x, x.y));
-                fma2(pr[1], am, make_float2(x.z, x.w));
-            } else {
-                fma2(pr[0], am, Xr[0]);
-            }
-        }
-    }
-    float acc[W];
-#pragma unroll
-    for (int e = 0; e < W / 2; ++e) {
-        acc[2 * e] = -pr[e].x;
-        acc[2 * e + 1] = -pr[e].y;
-    }
-    float *Tij = sT + (16 * i + r) * P + 16 * j + c0;
-    if constexpr (W == 4) *reinterpret_cast<float4 *>(Tij) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    else *reinterpret_cast<float2 *>(Tij) = make_float2(acc[0], acc[1]);
-    put_b<W, PO>(bt, 16 * i + r, 16 * j + c0, acc);
+// Fragments of row-major fp32 matrices (pitch kLP) at M: the 16 x 8 A tile at rows 0..15,
+// columns k0..k0+7, and the 8 x 8 B tile at rows k0..k0+7, columns n0..n0+7 (lane = 4 g + t4).
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float *M, int k0, int g, int t4) {
+    a[0] = to_tf32(M[g * kLP + k0 + t4]);
+    a[1] = to_tf32(M[(g + 8) * kLP + k0 + t4]);
+    a[2] = to_tf32(M[g * kLP + k0 + t4 + 4]);
+    a[3] = to_tf32(M[(g + 8) * kLP + k0 + t4 + 4]);
+}
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float *M, int k0, int n0, int g, int t4) {
+    b[0] = to_tf32(M[(k0 + t4) * kLP + n0 + g]);
+    b[1] = to_tf32(M[(k0 + t4 + 4) * kLP + n0 + g]);
+}
+// A 16 x 8 accumulator tile (rows g, g + 8; columns 2 t4, 2 t4 + 1) stored at M[r][c]
+__device__ __forceinline__ void store_c(float *M, const float (&d)[4], int n0, int g, int t4, float sgn) {
+    *reinterpret_cast<float2 *>(M + g * kLP + n0 + 2 * t4) = make_float2(sgn * d[0], sgn * d[1]);
+    *reinterpret_cast<float2 *>(M + (g + 8) * kLP + n0 + 2 * t4) = make_float2(sgn * d[2], sgn * d[3]);
 }
 
 template <int NT, bool PO = false, typename IdleWork>
@@ -407,6 +304,7 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
     static_assert(NT == 256, "the work split below assumes 256 threads");
     constexpr int P = kLP;
     const int warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
     if (warp < 4 && lane < 16) {
         // diagonal block `warp`, column j = lane: x_r = delta_rj - sum_{s<r} L[r][s] x_s, the
         // row of L read with 16-byte loads (unrolled, so the terms with early x_s are summed
@@ -447,36 +345,80 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
         idle();   // work of the caller's that fits in the substitution's shadow
     }
     named_sync(bar, NT);
-    const int slot = tid >> 6, t64 = tid & 63;
-    const int r4 = t64 >> 2, c4 = (t64 & 3) * 4;          // 64 threads x 4 outputs
-    // S0: X_10, X_21, X_32, X_20 from the diagonal inverses; the diagonal blocks into B
+    if (warp < 2) {
+        // T_10 (warp 0) and T_32 (warp 1): X = L_ij D_j into L's free block (j, i), then
+        // T_ij = -D_i X
+        const int i = 2 * warp + 1, j = 2 * warp;
+        float *X = sL + 16 * j * P + 16 * i;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k0 = 0; k0 < 16; k0 += 8) {
+                uint32_t a[4], b[2];
+                frag_a(a, sL + 16 * i * P + 16 * j, k0, g, t4);
+                frag_b(b, sT + 16 * j * P + 16 * j, k0, 8 * nt, g, t4);
+                mma_tf32(d, a, b);
+            }
+            store_c(X, d, 8 * nt, g, t4, 1.f);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k0 = 0; k0 < 16; k0 += 8) {
+                uint32_t a[4], b[2];
+                frag_a(a, sT + 16 * i * P + 16 * i, k0, g, t4);
+                frag_b(b, X, k0, 8 * nt, g, t4);
+                mma_tf32(d, a, b);
+            }
+            store_c(sT + 16 * i * P + 16 * j, d, 8 * nt, g, t4, -1.f);
+            const float v0[2] = {-d[0], -d[1]}, v1[2] = {-d[2], -d[3]};
+            put_b<2, PO>(bt, 16 * i + g, 16 * j + 8 * nt + 2 * t4, v0);
+            put_b<2, PO>(bt, 16 * i + g + 8, 16 * j + 8 * nt + 2 * t4, v1);
+        }
+    } else {
+        // the diagonal blocks into B and Bf: 4 blocks x 16 rows x 4 quads of columns
+        for (int w = tid - 64; w < 256; w += NT - 64) {
+            const int blk = w >> 6, r = (w >> 2) & 15, c4 = (w & 3) * 4;
+            const float4 d = *reinterpret_cast<const float4 *>(sT + (16 * blk + r) * P + 16 * blk + c4);
+            const float dv[4] = {d.x, d.y, d.z, d.w};
+            put_b<4, PO>(bt, 16 * blk + r, 16 * blk + c4, dv);
+        }
+    }
+    named_sync(bar, NT);
+    // X2 = L_BA T_AA (rows 32..63, columns 0..31) into L's free upper-right 32 x 32 block;
+    // T_AA[0:16][16:32] = 0, so the right half of X2 sums over k >= 16 only
+    const int mi = warp >> 2, ni = warp & 3;
+    float *X2 = sL + 32;
     {
-        const int i = slot == 3 ? 2 : slot + 1, j = slot == 3 ? 0 : slot;
-        inv_op_x<4>(sL, sT, i, j, j, j + 1, false, r4, c4);
-        const float4 d = *reinterpret_cast<const float4 *>(sT + (16 * slot + r4) * P + 16 * slot + c4);
-        const float dv[4] = {d.x, d.y, d.z, d.w};
-        put_b<4, PO>(bt, 16 * slot + r4, 16 * slot + c4, dv);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 8) {
+            if (ni >= 2 && k0 < 16) continue;
+            uint32_t a[4], b[2];
+            frag_a(a, sL + (32 + 16 * mi) * P, k0, g, t4);
+            frag_b(b, sT, k0, 8 * ni, g, t4);
+            mma_tf32(d, a, b);
+        }
+        store_c(X2 + 16 * mi * P, d, 8 * ni, g, t4, 1.f);
     }
     named_sync(bar, NT);
-    // S1: T_10, T_21, T_32; X_31 = L_31 T_11
-    if (slot < 3) inv_op_t<4, PO>(sL, sT, bt, slot + 1, slot, r4, c4);
-    else inv_op_x<4>(sL, sT, 3, 1, 1, 2, false, r4, c4);
-    named_sync(bar, NT);
-    // S2: X_20 += L_21 T_10;  X_31 += L_32 T_21;  X'_30 = L_30 T_00 + L_31 T_10 (two column halves)
-    if (slot == 0) inv_op_x<4>(sL, sT, 2, 0, 1, 2, true, r4, c4);
-    else if (slot == 1) inv_op_x<4>(sL, sT, 3, 1, 2, 3, true, r4, c4);
-    else {
-        const int r2 = t64 >> 2, c2 = (slot - 2) * 8 + (t64 & 3) * 2;
-        inv_op_x<2>(sL, sT, 3, 0, 0, 2, false, r2, c2);
-    }
-    named_sync(bar, NT);
-    // S3: T_20, T_31 (64 threads each, 4 outputs); T_30 = -(T_32 X_20 + T_33 X'_30) (128 threads,
-    // 2 outputs)
-    if (slot == 0) inv_op_t<4, PO>(sL, sT, bt, 2, 0, r4, c4);
-    else if (slot == 1) inv_op_t<4, PO>(sL, sT, bt, 3, 1, r4, c4);
-    else {
-        const int t128 = tid - 128;
-        inv_op_t2<2, PO>(sL, sT, bt, 3, 2, 0, t128 >> 3, (t128 & 7) * 2);
+    // T_BA = -T_BB X2; T_BB[0:16][16:32] = 0, so rows 32..47 sum over k < 16 only
+    {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 8) {
+            if (mi == 0 && k0 >= 16) continue;
+            uint32_t a[4], b[2];
+            frag_a(a, sT + (32 + 16 * mi) * P + 32, k0, g, t4);
+            frag_b(b, X2, k0, 8 * ni, g, t4);
+            mma_tf32(d, a, b);
+        }
+        const float v0[2] = {-d[0], -d[1]}, v1[2] = {-d[2], -d[3]};
+        put_b<2, PO>(bt, 32 + 16 * mi + g, 8 * ni + 2 * t4, v0);
+        put_b<2, PO>(bt, 32 + 16 * mi + g + 8, 8 * ni + 2 * t4, v1);
     }
     fence_proxy_async();   // B, Bf are tensor-core operands
     tc_fence_before();
@@ -588,10 +530,32 @@ __device__ __forceinline__ void load_scalars(const TcParams &p, float *mbeta, fl
     cp_async_commit();
 }
 
-// E_c of `slot` is in global memory (its bulk stores have completed): release the flag
-__device__ __forceinline__ void release_slot(const TcParams &p, long slot) {
+// E_c of column `col` is in global memory in `slot` (its bulk stores have completed):
+// release the slot's flag
+__device__ __forceinline__ void release_slot(const TcParams &p, int slot, int col) {
     fence_proxy_async_global();
-    st_release_gpu(p.flags + slot, 1u);
+    st_release_gpu(p.flags + slot, (uint32_t)col + 1u);
+}
+
+// Before E_c of column `col` goes into its chain's ring: wait until the chain has loaded
+// the E_c that the slot held (column col - kRing), giving up after limit_ns; the async
+// proxy is then ordered after the acquire (the slot is written by TMA stores).
+__device__ __forceinline__ bool wait_slot_free(const TcParams &p, int chain, int col, uint64_t limit_ns) {
+    if (col >= kRing) {
+        const uint32_t need = (uint32_t)(col - kRing + 1);
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(p.consumed + chain) < need) {
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+            __nanosleep(64);
+        }
+    }
+    fence_proxy_async_global();
+    return true;
+}
+
+// Prep work items: columns x chains
+__device__ __forceinline__ long prep_items(const TcParams &p) {
+    return (long)round_start(p, p.rounds) * p.nch;
 }
 
 // The two prep groups of a CTA run the same phases; when they run them at the same time
@@ -645,17 +609,19 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
 
     const bool lead = stagger && bar == 1, follow = stagger && bar == 2;
     if (follow) named_sync(kStaggerBar, 2 * kGroupThreads);
+    const long n_items = prep_items(p);
     ChunkItem cur;
-    while (item < p.n_items && !item_info(p, item, cur)) item += stride;
-    if (item >= p.n_items) {
+    while (item < n_items && !item_info(p, item, cur)) item += stride;
+    if (item >= n_items) {
         if (lead) named_arrive(kStaggerBar, 2 * kGroupThreads);
         return;
     }
     load_rows<D, OPT>(p, sKQ, cur, tid, true);
     load_rows<D, OPT>(p, sKQ, cur, tid, false);
     load_scalars<OPT>(p, mbeta, mdec, ctl->gate, cur, tid);
-    long pend = -1;     // store thread: slot whose stores are in flight and not yet published
-    long staged = -1;   // store thread: slot whose state-column blocks wait in the staging area
+    // store thread: the slot (and column) whose stores are in flight and not yet published,
+    // and the one whose state-column blocks wait in the staging area
+    int pend = -1, pend_col = 0, staged = -1, staged_col = 0;
 
     for (uint32_t it = 0;; ++it) {
         const uint32_t ph = it & 1;   // bar_mma completes three times per chunk
@@ -667,13 +633,14 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         bool ok = ctl->fail == 0;
         long nitem = item + stride;   // this group's next chunk
         ChunkItem nx;
-        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
-        const bool more = nitem < p.n_items;
+        while (nitem < n_items && !item_info(p, nitem, nx)) nitem += stride;
+        const bool more = nitem < n_items;
         if (tid == kStoreThread && staged >= 0) {   // the previous chunk's state-column blocks of E_c
             for (int kb = 0; kb < NB; ++kb)
-                tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
+                tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, staged);
             bulk_commit();
-            if (p.flags) pend = staged;
+            pend = staged;
+            pend_col = staged_col;
             staged = -1;
         }
 
@@ -837,7 +804,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         // gpu-scope release, about a thousand cycles, overlaps the MMA.
         if (tid == kStoreThread && pend >= 0) {
             bulk_wait0();
-            release_slot(p, pend);
+            release_slot(p, pend, pend_col);
             pend = -1;
         }
         if (ok && !mbar_wait(&ctl->bar_mma, ph ^ 1u, kWaitNs)) ctl->fail = 1;
@@ -908,8 +875,13 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             mma_commit(&ctl->bar_mma);
         }
         if (tid == kStoreThread && ok) {   // the V-column block, to drain during MMA3 and epilogue 3
-            tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, (int)cur.slot);
-            bulk_commit();
+            if (wait_slot_free(p, cur.chain, cur.col, kWaitNs)) {   // the ring slot has been read
+                tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, cur.slot);
+                bulk_commit();
+            } else {
+                ctl->fail = 1;
+                record_error(p.ws, 3);
+            }
         }
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
@@ -964,21 +936,24 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         named_sync(bar, kGroupThreads);
         const bool failed = ctl->fail != 0;
         if (tid == 0 && failed) record_error(p.ws, 1);
-        if (tid == kStoreThread) staged = cur.slot;   // stored once the next chunk has started
+        if (tid == kStoreThread && !failed) {   // stored once the next chunk has started
+            staged = cur.slot;
+            staged_col = cur.col;
+        }
         if (!more || failed) break;
         item = nitem;
         cur = nx;
     }
     cp_async_wait_all();
     if (tid == kStoreThread) {   // the last chunk's state columns; shared memory must outlive the stores
-        for (int kb = 0; kb < NB; ++kb)
-            tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, (int)staged);
-        bulk_commit();
-        bulk_wait0();
-        if (p.flags) {
-            if (pend >= 0) release_slot(p, pend);
-            release_slot(p, staged);
+        if (staged >= 0) {
+            for (int kb = 0; kb < NB; ++kb)
+                tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, staged);
+            bulk_commit();
         }
+        bulk_wait0();
+        if (pend >= 0) release_slot(p, pend, pend_col);
+        if (staged >= 0) release_slot(p, staged, staged_col);
     }
 }
 
@@ -1044,7 +1019,7 @@ struct GkSmem {
 // stores stay in flight: lane 0 waits for them (bulk_wait0) before E_c is published, and
 // every call first waits until the tile's previous store has read it.  With neg the values
 // are negated and dval added at column dcol (relative to col0; none when outside 0..31).
-__device__ __forceinline__ void warp_store_E(uint8_t *stage, const CUtensorMap *map, long slot, int row0,
+__device__ __forceinline__ void warp_store_E(uint8_t *stage, const CUtensorMap *map, int slot, int row0,
                                              int nrows, int col0, const uint32_t *u, bool neg, int lane,
                                              bool issue, int dcol = -1, float dval = 0.f) {
     if (lane == 0) bulk_wait_read0();
@@ -1065,8 +1040,9 @@ __device__ __forceinline__ void warp_store_E(uint8_t *stage, const CUtensorMap *
     fence_proxy_async();
     __syncwarp();
     if (lane == 0 && issue) {
-        tma_store_3d(map, stage, col0, row0, (int)slot);
-        if (nrows == 32) tma_store_3d(map, stage + 1024, col0, row0 + 16, (int)slot);
+        fence_proxy_async_global();   // after the slot's acquire (wait_slot_free) in another thread
+        tma_store_3d(map, stage, col0, row0, slot);
+        if (nrows == 32) tma_store_3d(map, stage + 1024, col0, row0 + 16, slot);
         bulk_commit();
     }
 }
@@ -1156,9 +1132,10 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
     int *mspan = reinterpret_cast<int *>(mtot + 1024);
     float *mgate = reinterpret_cast<float *>(mspan + 4);   // A_log, pad, dt_bias [D] at +4
 
+    const long n_items = prep_items(p);
     ChunkItem cur;
-    while (item < p.n_items && !item_info(p, item, cur)) item += stride;
-    if (item >= p.n_items) return;
+    while (item < n_items && !item_info(p, item, cur)) item += stride;
+    if (item >= n_items) return;
     if (loader) {
         load_rows<D, OPT>(p, sKQ, cur, tid, true);
         load_rows<D, OPT>(p, sKQ, cur, tid, false);
@@ -1166,7 +1143,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         load_beta(p, mbeta2, cur, tid);
         if (OPT) load_gate<D>(p, mgate, cur, tid);
     }
-    long pend = -1;   // kStoreThread: slot whose E_c stores are issued and not yet published
+    int pend = -1, pend_col = 0;   // kStoreThread: slot (column) whose E_c stores are issued, not published
     const bool decayed = p.decayed_read != 0;
 
     for (uint32_t it = 0;; ++it) {
@@ -1371,8 +1348,8 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         // (packed sequences read cu_seqlens to find it: off the path to MMA1)
         long nitem = item + stride;
         ChunkItem nx;
-        while (nitem < p.n_items && !item_info(p, nitem, nx)) nitem += stride;
-        const bool more = nitem < p.n_items;
+        while (nitem < n_items && !item_info(p, nitem, nx)) nitem += stride;
+        const bool more = nitem < n_items;
         float *mbeta_next = mbeta2 + 64 * ((it + 1) & 1);
         if (ok && more && loader) {
             load_rows<D, OPT>(p, sKQ, nx, tid, true);
@@ -1383,8 +1360,14 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         }
 
         if (tid == kStoreThread && pend >= 0) {   // the previous chunk's E_c, while MMA1 runs
-            release_slot(p, pend);
+            release_slot(p, pend, pend_col);
             pend = -1;
+        }
+        // this chunk's ring slot must have been read by its chain before epilogue 2 stores
+        // into it (the barriers in between order every warp's stores after this wait)
+        if (tid == kStoreThread && ok && !wait_slot_free(p, cur.chain, cur.col, kWaitNs)) {
+            ctl->fail = 1;
+            record_error(p.ws, 4);
         }
         if (ok && !mbar_wait(&ctl->bar_mma, ph, kWaitNs)) ctl->fail = 1;
         tc_fence_after();
@@ -1447,7 +1430,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
 
         // ---- epilogue 2: column quarters 0, 1 take Z1 = D2a (-> E[i][D + s], MMA3a's A),
         // quarters 2, 3 take Z2 = D2b (-> E[D + t][D + s], MMA3b's A = [-Z2 | I])
-        const long slot = cur.slot;
+        const int slot = cur.slot;
         constexpr int RW = D == 128 ? 32 : 16;   // rows of an M = D result per warp
         if (hh < 2) {
             uint32_t v[32];
@@ -1533,7 +1516,10 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         named_sync(bar, NT);   // every warp's E_c stores are issued
         const bool failed = ctl->fail != 0;
         if (tid == 0 && failed) record_error(p.ws, 2);
-        if (tid == kStoreThread && p.flags && !failed) pend = cur.slot;
+        if (tid == kStoreThread && !failed) {
+            pend = cur.slot;
+            pend_col = cur.col;
+        }
         if (!more || failed) break;
         item = nitem;
         cur = nx;
@@ -1541,7 +1527,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
     cp_async_wait_all();
     if (lane == 0) bulk_wait0();   // the last chunk's E_c stores have completed ...
     named_sync(bar, NT);           // ... in every warp, before it is published
-    if (tid == kStoreThread && pend >= 0) release_slot(p, pend);
+    if (tid == kStoreThread && pend >= 0) release_slot(p, pend, pend_col);
 }
 
 // ---------------------------------------------------------------------------------
@@ -1572,13 +1558,31 @@ struct ChainCfg {
     static constexpr int O_BYTES = 64 * D * 2;    // output staging [64][D] bf16
     static constexpr int SMEM = 2 * E_BYTES + AS_BYTES + 2 * AV_BYTES + O_BYTES + 1024;
     static constexpr uint32_t TCOLS = (2 * R <= 256) ? 256u : 512u;   // two accumulators
-    static constexpr int THREADS = 448;           // producer, MMA, 8 state + 4 output warps
 };
+
+// One task of a chain CTA: the (sequence, head) of round r, or none past the last task.
+struct ChainTask {
+    long start;   // first token row
+    int len, nc;  // tokens, chunks
+    int n, h;     // sequence, head
+    int col0;     // column of its first chunk (round_start of its round)
+    int col_end;  // round_start of the next round
+};
+__device__ __forceinline__ bool chain_task(const TcParams &p, int chain, int r, ChainTask &t) {
+    if (r >= p.rounds) return false;
+    const int task = r * p.nch + chain;
+    if (task >= p.ntask) return false;
+    task_info(p, task, t.n, t.h);
+    seq_info(p, t.n, t.start, t.len);
+    t.nc = (t.len + kC - 1) / kC;
+    t.col0 = round_start(p, r);
+    t.col_end = round_start(p, r + 1);
+    return true;
+}
 
 template <int D, bool OPT>
 __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUtensorMap *map_v,
-                                           const TcParams &p, uint8_t *sm, int task,
-                                           bool wait_flags) {
+                                           const TcParams &p, uint8_t *sm, int chain) {
     using Cf = ChainCfg<D>;
     constexpr int R = Cf::R;
     constexpr int HALF = D / 2;
@@ -1589,14 +1593,10 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
     __shared__ uint64_t e_full[2], e_empty[2], v_full[2], v_empty[2], d_full[2], d_free[2], s_ready;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_fail;
+    // the chain's progress through the ring, as the MMA issuer observes the E_c loads land:
+    // every column below s_rel has been loaded (monotone; published by warp 14)
+    __shared__ volatile uint32_t s_rel;
 
-    const int h = task % p.H;
-    const int n = task / p.H;
-    long start;
-    int len;
-    seq_info(p, n, start, len);
-    const int nc = (len + kC - 1) / kC;
-    const long slot0 = (long)chunk_base_of(p, n) * p.H + h;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
@@ -1611,6 +1611,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
         mbar_init(&s_ready, 256);
         fence_mbar_init();
         s_fail = 0;
+        s_rel = 0;
     }
     if (warp == 1) {
         tmem_alloc(&tmem_slot, Cf::TCOLS);
@@ -1621,58 +1622,83 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
     tc_fence_after();
     const uint32_t tm = tmem_slot;
 
+    // Every role walks the same tasks and chunks; gc counts the chunks of this CTA's walk
+    // (stages, accumulators and mbarrier phases follow it across tasks).
+    ChainTask t;
     if (warp == 0) {
-        // ---------------- producers: lane 0 streams E_c, lane 1 streams V_c, each into
-        // two shared-memory stages freed by the MMA commit; both also prefetch the
-        // tiles kPrefetch chunks ahead into L2 so that the stage loads hit L2 (E_c only
-        // when it was built by an earlier launch; in the single launch it is waited for
-        // by flag and was just written, so it sits in L2 already).
+        // ---------------- producers: lane 0 streams E_c (after its ring slot's flag is
+        // released), lane 1 streams V_c (with L2 prefetches kPrefetch chunks ahead), each
+        // into two shared-memory stages freed by the MMA commit
         constexpr int kPrefetch = 4;
         if (lane == 0) {
-            if (!wait_flags)
-                for (int c = 0; c < kPrefetch && c < nc; ++c)
+            int gc = 0;
+            for (int r = 0; chain_task(p, chain, r, t) && !s_fail; ++r) {
+                for (int c = 0; c < t.nc && !s_fail; ++c, ++gc) {
+                    const int s = gc & 1;
+                    if (gc >= 2 && !mbar_wait(&e_empty[s], ((gc >> 1) - 1) & 1, kWaitNs)) {
+                        s_fail = 1;
+                        record_error(p.ws, 10);
+                        break;
+                    }
+                    const int col = t.col0 + c;
+                    const int slot = chain * kRing + col % kRing;
+                    if (!wait_flag_acquire(p.flags + slot, (uint32_t)col + 1u, kWaitNs)) {   // E_c published
+                        s_fail = 1;
+                        record_error(p.ws, 16);
+                        break;
+                    }
+                    mbar_expect_tx(&e_full[s], Cf::E_BYTES);
+                    uint8_t *dE = sE0 + s * Cf::E_BYTES;
                     for (int kb = 0; kb < Cf::NKB; ++kb)
-                        tma_prefetch_l2_3d(map_E, kb * 64, 0, (int)(slot0 + (long)c * p.H));
-            for (int c = 0; c < nc && !s_fail; ++c) {
-                const int s = c & 1;
-                if (c >= 2 && !mbar_wait(&e_empty[s], ((c >> 1) - 1) & 1, kWaitNs)) {
-                    s_fail = 1;
-                    record_error(p.ws, 10);
-                    break;
+                        tma_load_3d(dE + kb * (R * 128), map_E, &e_full[s], kb * 64, 0, slot);
                 }
-                const int slot = (int)(slot0 + (long)c * p.H);
-                if (wait_flags && !wait_flag_acquire(p.flags + slot, kWaitNs)) {   // E_c published
-                    s_fail = 1;
-                    record_error(p.ws, 16);
-                    break;
-                }
-                mbar_expect_tx(&e_full[s], Cf::E_BYTES);
-                uint8_t *dE = sE0 + s * Cf::E_BYTES;
-                for (int kb = 0; kb < Cf::NKB; ++kb)
-                    tma_load_3d(dE + kb * (R * 128), map_E, &e_full[s], kb * 64, 0, slot);
-                if (!wait_flags && c + kPrefetch < nc)
-                    for (int kb = 0; kb < Cf::NKB; ++kb)
-                        tma_prefetch_l2_3d(map_E, kb * 64, 0, (int)(slot0 + (long)(c + kPrefetch) * p.H));
             }
         } else if (lane == 1) {
-            for (int c = 0; c < kPrefetch && c < nc; ++c)
-                for (int mb = 0; mb < Cf::NB; ++mb)
-                    tma_prefetch_l2_3d(map_v, mb * 64, h, (int)(start + (long)c * kC));
-            for (int c = 0; c < nc && !s_fail; ++c) {
-                const int s = c & 1;
-                if (c >= 2 && !mbar_wait(&v_empty[s], ((c >> 1) - 1) & 1, kWaitNs)) {
-                    s_fail = 1;
-                    record_error(p.ws, 15);
-                    break;
-                }
-                mbar_expect_tx(&v_full[s], Cf::AV_BYTES);
-                uint8_t *dV = sAV0 + s * Cf::AV_BYTES;
-                for (int mb = 0; mb < Cf::NB; ++mb)
-                    tma_load_3d(dV + mb * 8192, map_v, &v_full[s], mb * 64, h,
-                                (int)(start + (long)c * kC));
-                if (c + kPrefetch < nc)
+            int gc = 0;
+            for (int r = 0; chain_task(p, chain, r, t) && !s_fail; ++r) {
+                for (int c = 0; c < kPrefetch && c < t.nc; ++c)
                     for (int mb = 0; mb < Cf::NB; ++mb)
-                        tma_prefetch_l2_3d(map_v, mb * 64, h, (int)(start + (long)(c + kPrefetch) * kC));
+                        tma_prefetch_l2_3d(map_v, mb * 64, t.h, (int)(t.start + (long)c * kC));
+                for (int c = 0; c < t.nc && !s_fail; ++c, ++gc) {
+                    const int s = gc & 1;
+                    if (gc >= 2 && !mbar_wait(&v_empty[s], ((gc >> 1) - 1) & 1, kWaitNs)) {
+                        s_fail = 1;
+                        record_error(p.ws, 15);
+                        break;
+                    }
+                    mbar_expect_tx(&v_full[s], Cf::AV_BYTES);
+                    uint8_t *dV = sAV0 + s * Cf::AV_BYTES;
+                    for (int mb = 0; mb < Cf::NB; ++mb)
+                        tma_load_3d(dV + mb * 8192, map_v, &v_full[s], mb * 64, t.h,
+                                    (int)(t.start + (long)c * kC));
+                    if (c + kPrefetch < t.nc)
+                        for (int mb = 0; mb < Cf::NB; ++mb)
+                            tma_prefetch_l2_3d(map_v, mb * 64, t.h, (int)(t.start + (long)(c + kPrefetch) * kC));
+                }
+            }
+        }
+    } else if (warp == 14) {
+        // ---------------- ring release: publish the chain's progress (s_rel, set by the MMA
+        // issuer when an E_c load has landed) to the prep groups by a gpu-scope release,
+        // ~900 cycles, kept off the producer and MMA threads.  Only the latest value counts,
+        // so a release that falls behind skips ahead.
+        if (lane == 0) {
+            uint32_t fin = 0;   // the counter's final value: the end of the chain's last round
+            for (int r = 0; chain_task(p, chain, r, t); ++r) fin = (uint32_t)t.col_end;
+            uint32_t done = 0;
+            uint64_t t0 = globaltimer_ns();
+            while (done < fin && !s_fail) {
+                const uint32_t v = s_rel;
+                if (v > done) {
+                    st_release_gpu(p.consumed + chain, v);
+                    done = v;
+                    t0 = globaltimer_ns();
+                } else if (globaltimer_ns() - t0 > kWaitNs) {
+                    s_fail = 1;
+                    record_error(p.ws, 17);
+                } else {
+                    __nanosleep(32);
+                }
             }
         }
     } else if (warp == 1) {
@@ -1681,112 +1707,130 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
             const uint32_t idV = idesc_bf16_f32(D, R, true, false);
             const uint32_t idS = idesc_bf16_f32(D, R, false, false);
             const uint32_t as0 = smem_u32(sAS);
-            for (int c = 0; c < nc && !s_fail; ++c) {
-                const int b = c & 1;
-                if (!mbar_wait(&e_full[b], (c >> 1) & 1, kWaitNs) ||
-                    !mbar_wait(&v_full[b], (c >> 1) & 1, kWaitNs) ||
-                    (c >= 2 && !mbar_wait(&d_free[b], ((c >> 1) - 1) & 1, kWaitNs))) {
-                    s_fail = 1;
-                    record_error(p.ws, 11);
-                    break;
+            int gc = 0;
+            for (int r = 0; chain_task(p, chain, r, t) && !s_fail; ++r) {
+                if (t.nc == 0) s_rel = (uint32_t)t.col_end;   // no chunk: straight to the next round
+                for (int c = 0; c < t.nc && !s_fail; ++c, ++gc) {
+                    const int b = gc & 1;
+                    if (!mbar_wait(&e_full[b], (gc >> 1) & 1, kWaitNs)) {
+                        s_fail = 1;
+                        record_error(p.ws, 11);
+                        break;
+                    }
+                    // E_c of this column is in shared memory: its ring slot may be rewritten
+                    // (at the task's last chunk the counter jumps to the next round's start)
+                    s_rel = (c + 1 < t.nc) ? (uint32_t)(t.col0 + c + 1) : (uint32_t)t.col_end;
+                    if (!mbar_wait(&v_full[b], (gc >> 1) & 1, kWaitNs) ||
+                        (gc >= 2 && !mbar_wait(&d_free[b], ((gc >> 1) - 1) & 1, kWaitNs))) {
+                        s_fail = 1;
+                        record_error(p.ws, 11);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t e0 = smem_u32(sE0 + b * Cf::E_BYTES);
+                    const uint32_t av0 = smem_u32(sAV0 + b * Cf::AV_BYTES);
+                    const uint32_t dcol = tm + (uint32_t)(b * R);
+                    for (int ks = 0; ks < 4; ++ks)   // V half: E_c columns D .. D + 63
+                        mma_bf16_ss(dcol, desc_mnmajor_sw128(av0, 64, ks),
+                                    desc_kmajor_sw128(e0, R, D / 16 + ks), idV, ks > 0 ? 1u : 0u);
+                    if (!mbar_wait(&s_ready, gc & 1, kWaitNs)) {
+                        s_fail = 1;
+                        record_error(p.ws, 12);
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int ks = 0; ks < D / 16; ++ks)   // state half: E_c columns 0 .. D - 1
+                        mma_bf16_ss(dcol, desc_kmajor_sw128(as0, D, ks), desc_kmajor_sw128(e0, R, ks),
+                                    idS, 1u);
+                    mma_commit(&d_full[b]);
+                    mma_commit(&e_empty[b]);
+                    mma_commit(&v_empty[b]);
                 }
-                tc_fence_after();
-                const uint32_t e0 = smem_u32(sE0 + b * Cf::E_BYTES);
-                const uint32_t av0 = smem_u32(sAV0 + b * Cf::AV_BYTES);
-                const uint32_t dcol = tm + (uint32_t)(b * R);
-                for (int ks = 0; ks < 4; ++ks)   // V half: E_c columns D .. D + 63
-                    mma_bf16_ss(dcol, desc_mnmajor_sw128(av0, 64, ks),
-                                desc_kmajor_sw128(e0, R, D / 16 + ks), idV, ks > 0 ? 1u : 0u);
-                if (!mbar_wait(&s_ready, c & 1, kWaitNs)) {
-                    s_fail = 1;
-                    record_error(p.ws, 12);
-                    break;
-                }
-                tc_fence_after();
-                for (int ks = 0; ks < D / 16; ++ks)   // state half: E_c columns 0 .. D - 1
-                    mma_bf16_ss(dcol, desc_kmajor_sw128(as0, D, ks), desc_kmajor_sw128(e0, R, ks),
-                                idS, 1u);
-                mma_commit(&d_full[b]);
-                mma_commit(&e_empty[b]);
-                mma_commit(&v_empty[b]);
             }
         }
     } else if (warp < 10) {
         // ---------------- state epilogue, warps 2..9: TMEM quadrant q, value column j,
         // state rows i in [ch D/2, (ch + 1) D/2).  Turns the fp32 next state into the
-        // bf16 S^T operand (the critical path).
+        // bf16 S^T operand (the critical path).  s_ready completes once per chunk: after a
+        // task's initial state is in place and after every chunk but the task's last.
         const int q = warp & 3, ch = (warp - 2) >> 2;
         const bool has_row = (D == 128) || (lane < 16);   // M = 64: 16 rows per quadrant
         const int j = (D == 128) ? 32 * q + lane : 16 * q + lane;
         const uint32_t lrow = (uint32_t)(32 * q) << 16;
-        const size_t hbase = ((size_t)n * p.H + h) * D * D;
         const int i_lo = ch * HALF;
-
         // element (i, j) of a state: key-major at i D + j, value-major at j D + i
         const bool vf = OPT && p.v_first;
         const size_t si = vf ? 1 : D, sj = vf ? D : 1;
-        if (has_row) {   // S_0^T row j from initial_state[:, j]
-            for (int i0 = i_lo; i0 < i_lo + HALF; i0 += 8) {
-                float x[8];
+        int gc = 0;
+        for (int r = 0; chain_task(p, chain, r, t) && !s_fail; ++r) {
+            const size_t hbase = ((size_t)t.n * p.H + t.h) * D * D;
+            if (has_row) {   // S_0^T row j from initial_state[:, j] (the previous task's MMAs are done)
+                for (int i0 = i_lo; i0 < i_lo + HALF; i0 += 8) {
+                    float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = p.h0 ? p.h0[hbase + (size_t)(i0 + e) * si + j * sj] : 0.f;
-                if (nc == 0) {
-                    if (p.hT)
+                    for (int e = 0; e < 8; ++e)
+                        x[e] = p.h0 ? p.h0[hbase + (size_t)(i0 + e) * si + j * sj] : 0.f;
+                    if (t.nc == 0) {
+                        if (p.hT)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) p.hT[hbase + (size_t)(i0 + e) * si + j * sj] = x[e];
-                } else {
-                    const int ci = (i0 & 63) >> 3;
-                    *reinterpret_cast<uint4 *>(sAS + (i0 >> 6) * D * 128 + j * 128 + ((ci ^ (j & 7)) << 4)) =
-                        make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                                   pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-                }
-            }
-        }
-        fence_proxy_async();
-        mbar_arrive(&s_ready);
-
-        for (int c = 0; c < nc; ++c) {
-            const int b = c & 1;
-            if (s_fail || !mbar_wait(&d_full[b], (c >> 1) & 1, kWaitNs)) {
-                s_fail = 1;
-                record_error(p.ws, 13);
-                break;
-            }
-            tc_fence_after();
-            const uint32_t dcol = tm + lrow + (uint32_t)(b * R) + (uint32_t)i_lo;
-            const bool last = (c + 1 == nc);
-            uint32_t v[HALF];
-#pragma unroll
-            for (int i0 = 0; i0 < HALF; i0 += 32)
-                tmem_ld32(dcol + i0, *reinterpret_cast<uint32_t(*)[32]>(v + i0));
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&d_free[b]);
-            if (has_row) {
-                if (!last) {
-#pragma unroll
-                    for (int cc = 0; cc < HALF / 8; ++cc) {
-                        const int gc = (i_lo >> 3) + cc;   // 8-column group of S^T row j
-                        *reinterpret_cast<uint4 *>(sAS + (gc >> 3) * D * 128 + j * 128 +
-                                                   (((gc & 7) ^ (j & 7)) << 4)) = pack8u(v + 8 * cc);
-                    }
-                } else if (p.hT) {
-                    if (vf) {   // value-major: row j of the state is contiguous
-                        float *dst = p.hT + hbase + (size_t)j * D + i_lo;
-#pragma unroll
-                        for (int i = 0; i < HALF; i += 4)
-                            *reinterpret_cast<float4 *>(dst + i) =
-                                make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                            __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                            for (int e = 0; e < 8; ++e) p.hT[hbase + (size_t)(i0 + e) * si + j * sj] = x[e];
                     } else {
-#pragma unroll
-                        for (int i = 0; i < HALF; ++i)
-                            p.hT[hbase + (size_t)(i_lo + i) * D + j] = __uint_as_float(v[i]);
+                        const int ci = (i0 & 63) >> 3;
+                        *reinterpret_cast<uint4 *>(sAS + (i0 >> 6) * D * 128 + j * 128 + ((ci ^ (j & 7)) << 4)) =
+                            make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                                       pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
                     }
                 }
             }
-            if (!last) fence_proxy_async();
-            mbar_arrive(&s_ready);   // S_{c+1}^T is in place
+            if (t.nc == 0) continue;
+            fence_proxy_async();
+            mbar_arrive(&s_ready);
+
+            for (int c = 0; c < t.nc; ++c, ++gc) {
+                const int b = gc & 1;
+                if (s_fail || !mbar_wait(&d_full[b], (gc >> 1) & 1, kWaitNs)) {
+                    s_fail = 1;
+                    record_error(p.ws, 13);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dcol = tm + lrow + (uint32_t)(b * R) + (uint32_t)i_lo;
+                const bool last = (c + 1 == t.nc);
+                uint32_t v[HALF];
+#pragma unroll
+                for (int i0 = 0; i0 < HALF; i0 += 32)
+                    tmem_ld32(dcol + i0, *reinterpret_cast<uint32_t(*)[32]>(v + i0));
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&d_free[b]);
+                if (has_row) {
+                    if (!last) {
+#pragma unroll
+                        for (int cc = 0; cc < HALF / 8; ++cc) {
+                            const int gcol = (i_lo >> 3) + cc;   // 8-column group of S^T row j
+                            *reinterpret_cast<uint4 *>(sAS + (gcol >> 3) * D * 128 + j * 128 +
+                                                       (((gcol & 7) ^ (j & 7)) << 4)) = pack8u(v + 8 * cc);
+                        }
+                    } else if (p.hT) {
+                        if (vf) {   // value-major: row j of the state is contiguous
+                            float *dst = p.hT + hbase + (size_t)j * D + i_lo;
+#pragma unroll
+                            for (int i = 0; i < HALF; i += 4)
+                                *reinterpret_cast<float4 *>(dst + i) =
+                                    make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < HALF; ++i)
+                                p.hT[hbase + (size_t)(i_lo + i) * D + j] = __uint_as_float(v[i]);
+                        }
+                    }
+                }
+                if (!last) {
+                    fence_proxy_async();
+                    mbar_arrive(&s_ready);   // S_{c+1}^T is in place
+                }
+            }
         }
     } else if (warp < 14) {
         // ---------------- output epilogue, warps 10..13: O[t][j] from the same
@@ -1798,41 +1842,43 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
         const int et = tid - 320;       // 0..127 over the output warps
         __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sO);
         constexpr int CPR = D / 8;      // 16-byte pieces per output row
-        for (int c = 0; c < nc; ++c) {
-            const int b = c & 1;
-            if (s_fail || !mbar_wait(&d_full[b], (c >> 1) & 1, kWaitNs)) {
-                s_fail = 1;
-                record_error(p.ws, 14);
-                break;
-            }
-            tc_fence_after();
-            {   // E_c of this chunk has been consumed: drop its lines from L2 without the
-                // write-back to HBM (nothing reads the slot again)
-                const char *eg = reinterpret_cast<const char *>(p.E) +
-                                 (size_t)(slot0 + (long)c * p.H) * Cf::E_BYTES;
-                for (int l = et; l < Cf::E_BYTES / 128; l += 128)
-                    asm volatile("discard.global.L2 [%0], 128;" ::"l"(eg + (size_t)l * 128) : "memory");
-            }
-            const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
-            uint32_t v[kC];
-            tmem_ld32(dcol + D, *reinterpret_cast<uint32_t(*)[32]>(v));
-            tmem_ld32(dcol + D + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&d_free[b]);
-            named_sync(1, 128);          // the previous chunk's rows have been written out
-            if (has_row)
+        // Every output warp passes both named barriers of every chunk, failed or not (a
+        // warp that left the loop early would leave the others waiting at the barrier);
+        // after a failure the remaining chunks are skipped without waiting.
+        int gc = 0;
+        for (int r = 0; chain_task(p, chain, r, t); ++r) {
+            for (int c = 0; c < t.nc; ++c, ++gc) {
+                const int b = gc & 1;
+                bool ok = !s_fail;
+                if (ok && !mbar_wait(&d_full[b], (gc >> 1) & 1, kWaitNs)) {
+                    s_fail = 1;
+                    record_error(p.ws, 14);
+                    ok = false;
+                }
+                uint32_t v[kC];
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
+                    tmem_ld32(dcol + D, *reinterpret_cast<uint32_t(*)[32]>(v));
+                    tmem_ld32(dcol + D + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    mbar_arrive(&d_free[b]);
+                }
+                named_sync(1, 128);          // the previous chunk's rows have been written out
+                if (ok && has_row)
 #pragma unroll
-                for (int t = 0; t < kC; ++t) stg[t * D + j] = __float2bfloat16_rn(__uint_as_float(v[t]));
-            named_sync(1, 128);
-            const int nv = min(kC, len - c * kC);
-            __nv_bfloat16 *obase = p.o + ((size_t)(start + (long)c * kC) * p.H + h) * D;
+                    for (int tt = 0; tt < kC; ++tt) stg[tt * D + j] = __float2bfloat16_rn(__uint_as_float(v[tt]));
+                named_sync(1, 128);
+                const int nv = ok ? min(kC, t.len - c * kC) : 0;
+                __nv_bfloat16 *obase = p.o + ((size_t)(t.start + (long)c * kC) * p.H + t.h) * D;
 #pragma unroll
-            for (int k = et; k < kC * CPR; k += 128) {
-                const int t = k / CPR, cc = k % CPR;
-                if (t < nv)
-                    *reinterpret_cast<uint4 *>(obase + (size_t)t * p.H * D + cc * 8) =
-                        *reinterpret_cast<const uint4 *>(stg + t * D + cc * 8);
+                for (int k = et; k < kC * CPR; k += 128) {
+                    const int tt = k / CPR, cc = k % CPR;
+                    if (tt < nv)
+                        *reinterpret_cast<uint4 *>(obase + (size_t)tt * p.H * D + cc * 8) =
+                            *reinterpret_cast<const uint4 *>(stg + tt * D + cc * 8);
+                }
             }
         }
     }
@@ -1845,9 +1891,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
 }
 
 // ---------------------------------------------------------------------------------
-// tc_kernel -- CTAs [0, nchain) take the chain role (one (sequence, head) each), the
-// others two prep groups each.  With nchain > 0 the launch is cooperative, so that
-// every chain's producers are co-resident with the prep groups they wait for.
+// tc_kernel -- CTAs [0, nch) take the chain role, the others hold the prep groups (two of
+// 256 threads, or one of 512 for the per-channel decay).  The launch is cooperative: every
+// chain is co-resident with the prep groups it waits for, and they with it.
 // ---------------------------------------------------------------------------------
 template <int D, bool GK, bool OPT>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -1858,8 +1904,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                                                            TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    if ((int)blockIdx.x < p.nchain) {
-        chain_body<D, OPT>(&map_E, &map_v, p, sm, (int)blockIdx.x, p.flags != nullptr);
+    if ((int)blockIdx.x < p.nch) {
+        chain_body<D, OPT>(&map_E, &map_v, p, sm, (int)blockIdx.x);
         return;
     }
     __shared__ uint32_t tmem_base;
@@ -1878,8 +1924,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        prep_group_gk<D, OPT>(&map_Ew, p, sm, tmem_base, tid, 1, (long)((int)blockIdx.x - p.nchain),
-                         (long)((int)gridDim.x - p.nchain));
+        prep_group_gk<D, OPT>(&map_Ew, p, sm, tmem_base, tid, 1, (long)((int)blockIdx.x - p.nch),
+                         (long)((int)gridDim.x - p.nch));
         tc_fence_before();
         __syncthreads();
         if (tid < 32) {
@@ -1902,9 +1948,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const long gidx = (long)((int)blockIdx.x - p.nchain) * 2 + grp;
-    const long ngroups = (long)((int)gridDim.x - p.nchain) * 2;
-    const bool stagger = p.n_items >= 16 * ngroups;   // long runs only: the offset costs a start-up delay
+    const long gidx = (long)((int)blockIdx.x - p.nch) * 2 + grp;
+    const long ngroups = (long)((int)gridDim.x - p.nch) * 2;
+    const bool stagger = prep_items(p) >= 16 * ngroups;   // long runs only: the offset costs a start-up delay
     prep_group<D, OPT>(&map_q, &map_k, &map_E, p, gsm, tmem_base + (uint32_t)(grp * 256),
                   tid & (kGroupThreads - 1), 1 + grp, gidx, ngroups, stagger);
     tc_fence_before();
@@ -1913,14 +1959,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         __syncwarp();
         tmem_dealloc(tmem_base, 512);
     }
-}
-
-template <int D, bool OPT>
-__global__ void __launch_bounds__(ChainCfg<D>::THREADS, 1) chain_kernel(const __grid_constant__ CUtensorMap map_E,
-                                                                        const __grid_constant__ CUtensorMap map_v,
-                                                                        TcParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    chain_body<D, OPT>(&map_E, &map_v, p, align1024(smem_raw), (int)blockIdx.x, false);
 }
 
 // Failure-detection probe: the two bounded waits of the kernels above, run against events
@@ -1932,45 +1970,52 @@ __global__ void timeout_probe_kernel(WsHeader *ws, const uint32_t *never, uint64
         mbar_init(&bar, 1);
         fence_mbar_init();
         if (!mbar_wait(&bar, 0, limit_ns)) record_error(ws, 90);
-        if (!wait_flag_acquire(never, limit_ns)) record_error(ws, 91);
+        if (!wait_flag_acquire(never, 1u, limit_ns)) record_error(ws, 91);
     }
 }
 
-// cu_seqlens -> chunk prefix: base[n] = sum_{m < n} ceil(len_m / 64), base[N] = total.
-__global__ void chunk_table_kernel(const int *cu, int N, int *base) {
-    __shared__ int warp_tot[32];
-    __shared__ int carry;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) carry = 0;
+// Packed sequences: the order of the tasks and the columns of the rounds.
+//   order[rank]  = the sequence of that rank by decreasing chunk count (ties: lower index
+//                  first); the identity for more than kSortMax sequences
+//   round_base[r] = sum over rounds r' < r of the largest chunk count among the round's
+//                  sequences; round r holds tasks [r nch, (r + 1) nch), task = rank H + head.
+// One CTA.
+constexpr int kSortMax = 2048;
+__global__ void varlen_schedule_kernel(const int *cu, int N, int H, int nch, int rounds, int *order,
+                                       int *round_base) {
+    __shared__ int snc[kSortMax];
+    const int tid = threadIdx.x;
+    const bool sort = N <= kSortMax;
+    auto nc_of = [&](int n) { return (cu[n + 1] - cu[n] + kC - 1) / kC; };
+    if (sort)
+        for (int n = tid; n < N; n += blockDim.x) snc[n] = nc_of(n);
     __syncthreads();
-    for (int s0 = 0; s0 < N; s0 += 1024) {
-        const int n = s0 + tid;
-        const int v = n < N ? (cu[n + 1] - cu[n] + kC - 1) / kC : 0;
-        int x = v;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
+    for (int n = tid; n < N; n += blockDim.x) {
+        if (!sort) {
+            order[n] = n;
+            continue;
         }
-        if (lane == 31) warp_tot[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            int w = warp_tot[lane];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, w, off);
-                if (lane >= off) w += y;
-            }
-            warp_tot[lane] = w;   // inclusive over warps
+        const int mine = snc[n];
+        int rank = 0;
+        for (int m = 0; m < N; ++m) {
+            const int o = snc[m];
+            rank += (o > mine) || (o == mine && m < n);
         }
-        __syncthreads();
-        const int before = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
-        if (n < N) base[n] = before;
-        __syncthreads();
-        if (tid == 0) carry += warp_tot[31];
-        __syncthreads();
+        order[rank] = n;
     }
-    if (tid == 0) base[N] = carry;
+    __syncthreads();
+    if (tid == 0) {   // rounds <= N * H; sorted: the round's first sequence is its longest
+        int acc = 0;
+        for (int r = 0; r < rounds; ++r) {
+            round_base[r] = acc;
+            const int first = (int)(((long)r * nch) / H);   // ranks of the round's tasks
+            const int last = (int)(min((long)(r + 1) * nch, (long)N * H) - 1) / H;
+            int m = 0;
+            for (int k = first; k <= (sort ? first : last); ++k) m = max(m, nc_of(order[k]));
+            acc += m;
+        }
+        round_base[rounds] = acc;
+    }
 }
 
 bool map_tokens(CUtensorMap *m, const void *base, long rows, int H, int D) {
@@ -1995,12 +2040,48 @@ bool map_E_tiles(CUtensorMap *m, const void *base, long slots, int R) {
                            CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-constexpr size_t kTableBytes(int nseq) { return (((size_t)(nseq + 1) * 4 + 255) / 256) * 256; }
-constexpr size_t kFlagBytes(long slots) { return (((size_t)slots * 4 + 255) / 256) * 256; }
+constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Chains for `ntask` tasks on `nsm` SMs: at most a quarter of the SMs (the prep is the
+// larger share of the work) and kMaxChains, balanced so that every round but the last is
+// full and the last nearly so.
+int chains_for(long ntask, int nsm) {
+    long nch = std::min<long>(std::min<long>(ntask, nsm / 4), kMaxChains);
+    if (nch < 1) nch = 1;
+    const long rounds = (ntask + nch - 1) / nch;
+    return (int)((ntask + rounds - 1) / rounds);
+}
+
+// Scratch layout after the workspace header (chains <= nch_max):
+//   [order: nseq ints][round_base: ntask + 1 ints]   packed sequences only
+//   [flags: nch_max * kRing][consumed: nch_max]      uint32
+//   [E_c rings: nch_max * kRing * (D + 64)^2 bf16]
+struct ScratchLayout {
+    size_t order, round_base, flags, consumed, E, total;
+};
+ScratchLayout scratch_layout(int nseq, int H, int d, bool varlen) {
+    const long ntask = (long)nseq * H;
+    const long nch_max = std::max<long>(1, std::min<long>(ntask, kMaxChains));
+    const size_t R = (size_t)d + 64;
+    ScratchLayout L{};
+    size_t off = 0;
+    L.order = off;
+    if (varlen) off += align256((size_t)nseq * 4);
+    L.round_base = off;
+    if (varlen) off += align256((size_t)(ntask + 1) * 4);
+    L.flags = off;
+    off += align256((size_t)nch_max * kRing * 4);
+    L.consumed = off;
+    off += align256((size_t)nch_max * 4);
+    L.E = off;
+    off += (size_t)nch_max * kRing * R * R * 2;
+    L.total = off;
+    return L;
+}
 
 // OPT: the kda_options paths, compiled out of the plain instantiations
 template <int D, bool GK, bool OPT>
-cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
+cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {
     constexpr int R = D + 64;
     using Cf = ChainCfg<D>;
     TcParams p{};
@@ -2018,27 +2099,19 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     p.rows = total_rows;
     p.o = static_cast<__nv_bfloat16 *>(a.o);
     p.ws = a.ws;
+    p.ntask = a.nseq * a.H;
+    const bool varlen = a.cu_seqlens != nullptr;
+    const ScratchLayout L = scratch_layout(a.nseq, a.H, D, varlen);
+    if (L.total > a.ws_body_bytes) return cudaErrorInvalidValue;
     uint8_t *body = static_cast<uint8_t *>(a.ws_body);
-    int *table = reinterpret_cast<int *>(body);
-    uint32_t *flags = reinterpret_cast<uint32_t *>(body + kTableBytes(a.nseq));
-    p.chunk_base = a.cu_seqlens ? table : nullptr;
-    p.E = reinterpret_cast<__nv_bfloat16 *>(body + kTableBytes(a.nseq) + kFlagBytes(slots_bound));
-    p.nsh = (long)a.nseq * a.H;
-    p.maxnc = (a.T + kC - 1) / kC;   // varlen: a.T bounds the longest sequence
+    p.order = varlen ? reinterpret_cast<const int *>(body + L.order) : nullptr;
+    p.round_base = varlen ? reinterpret_cast<const int *>(body + L.round_base) : nullptr;
+    p.flags = reinterpret_cast<uint32_t *>(body + L.flags);
+    p.consumed = reinterpret_cast<uint32_t *>(body + L.consumed);
+    p.E = reinterpret_cast<__nv_bfloat16 *>(body + L.E);
 
-    CUtensorMap mq, mk, mv, me, mew;
-    if (!map_tokens(&mq, a.q, total_rows, a.H / p.G, D) || !map_tokens(&mk, a.k, total_rows, a.H / p.G, D) ||
-        !map_tokens(&mv, a.v, total_rows, a.H, D) || !map_E(&me, p.E, slots_bound, R) ||
-        !map_E_tiles(&mew, p.E, slots_bound, R))
-        return cudaErrorInvalidValue;
-
-    cudaError_t e;
-    if (a.cu_seqlens) {
-        chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.nseq, table);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
     int dev = 0, nsm = 0;
+    cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int prep_smem = GK ? GkSmem<D>::BYTES + 1024 : 2 * PrepSmem<D>::GROUP + 1024;
@@ -2046,17 +2119,30 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
     e = cudaFuncSetAttribute(tc_kernel<D, GK, OPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, one_smem);
     if (e != cudaSuccess) return e;
 
-    // Single launch when the chains take at most half of the SMs: chains and prep
-    // groups co-resident (cooperative launch), E_c handed over by flags.
-    if (p.nsh <= nsm / 2) {
-        TcParams pf = p;
-        pf.flags = flags;
-        pf.chunk_major = 1;
-        pf.n_items = (long)pf.maxnc * pf.nsh;
-        pf.nchain = (int)pf.nsh;
-        if ((e = cudaMemsetAsync(flags, 0, (size_t)slots_bound * 4, st)) != cudaSuccess) return e;
+    // One cooperative launch: chains and prep groups co-resident.  If fewer SMs can take a
+    // block than the device reports (a partitioned GPU), the grid shrinks and the chains
+    // with it (the kernel is persistent: any grid with a prep CTA works).
+    for (int grid = nsm; grid >= 2; grid -= std::max(1, grid / 8)) {
+        p.nch = chains_for(p.ntask, grid);
+        p.rounds = (p.ntask + p.nch - 1) / p.nch;
+        const long cols = varlen ? (long)p.rounds * ((a.T + kC - 1) / kC) : (long)p.rounds * p.nc_equal;
+        if (cols * p.nch >= (1L << 31)) return cudaErrorInvalidValue;   // 32-bit item indexing
+        const size_t fbytes = L.consumed + (size_t)p.nch * 4 - L.flags;
+        if ((e = cudaMemsetAsync(body + L.flags, 0, fbytes, st)) != cudaSuccess) return e;
+        if (varlen) {
+            varlen_schedule_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.nseq, a.H, p.nch, p.rounds,
+                                                       reinterpret_cast<int *>(body + L.order),
+                                                       reinterpret_cast<int *>(body + L.round_base));
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        CUtensorMap mq, mk, mv, me, mew;
+        const long slots = (long)p.nch * kRing;
+        if (!map_tokens(&mq, a.q, total_rows, a.H / p.G, D) || !map_tokens(&mk, a.k, total_rows, a.H / p.G, D) ||
+            !map_tokens(&mv, a.v, total_rows, a.H, D) || !map_E(&me, p.E, slots, R) ||
+            !map_E_tiles(&mew, p.E, slots, R))
+            return cudaErrorInvalidValue;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)nsm);
+        cfg.gridDim = dim3((unsigned)grid);
         cfg.blockDim = dim3(kTcThreads);
         cfg.dynamicSmemBytes = (size_t)one_smem;
         cfg.stream = st;
@@ -2065,25 +2151,11 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStr
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc_kernel<D, GK, OPT>, mq, mk, mv, me, mew, pf);
-        if (e == cudaSuccess) return cudaSuccess;
+        e = cudaLaunchKernelEx(&cfg, tc_kernel<D, GK, OPT>, mq, mk, mv, me, mew, p);
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
-        (void)cudaGetLastError();   // fewer SMs available than reported: two launches
+        (void)cudaGetLastError();
     }
-
-    // Two launches: persistent prep groups over the E_c slots, then the chains.
-    p.flags = nullptr;
-    p.chunk_major = 0;
-    p.n_items = slots_bound;
-    p.nchain = 0;
-    const long ctas = std::min<long>(GK ? slots_bound : (slots_bound + 1) / 2, (long)nsm);
-    tc_kernel<D, GK, OPT><<<(unsigned)ctas, kTcThreads, prep_smem, st>>>(mq, mk, mv, me, mew, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chain_kernel<D, OPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
-    if (e != cudaSuccess) return e;
-    chain_kernel<D, OPT><<<(unsigned)p.nsh, Cf::THREADS, Cf::SMEM, st>>>(me, mv, p);
-    return cudaGetLastError();
+    return cudaErrorCooperativeLaunchTooLarge;
 }
 
 }  // namespace
@@ -2092,16 +2164,10 @@ bool chunk_tc_supported(int dk, int dv, int chunk, DType dt) {
     return dt == DType::BF16 && dk == dv && (dk == 64 || dk == 128) && chunk == kC;
 }
 
-// Scratch bytes after the workspace header: the chunk table, one flag and one E slot
-// per (chunk, head).  slots_bound: an upper bound on the number of chunks times H.
-size_t chunk_tc_scratch_bytes(int nseq, long slots_bound, int d) {
-    const long R = d + 64;
-    return kTableBytes(nseq) + kFlagBytes(slots_bound) + (size_t)slots_bound * R * R * 2;
-}
-
-long chunk_tc_slots_bound(int nseq, long total_rows, int H, int T_equal, bool varlen) {
-    if (!varlen) return (long)nseq * ((T_equal + kC - 1) / kC) * H;
-    return ((total_rows + kC - 1) / kC + nseq) * (long)H;
+// Scratch bytes after the workspace header: the rings of the chains (at most kMaxChains,
+// whatever the sequence length) and, for packed sequences, the schedule tables.
+size_t chunk_tc_scratch_bytes(int nseq, int H, int d, bool varlen) {
+    return scratch_layout(nseq, H, d, varlen).total;
 }
 
 cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t st) {
@@ -2112,25 +2178,21 @@ cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t s
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t st) {
-    if (slots_bound >= (1L << 31) || total_rows >= (1L << 31)) return cudaErrorInvalidValue;   // 32-bit indexing
+cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {
+    if (total_rows >= (1L << 31)) return cudaErrorInvalidValue;   // 32-bit row indexing
     if (a.per_channel) {   // the decayed read is a runtime choice of the per-channel prep
         const bool gopt = a.A_log || a.beta_sig || a.G > 1 || a.v_first;
         if (a.dk == 128)
-            return gopt ? run_tc<128, true, true>(a, total_rows, slots_bound, st)
-                        : run_tc<128, true, false>(a, total_rows, slots_bound, st);
+            return gopt ? run_tc<128, true, true>(a, total_rows, st) : run_tc<128, true, false>(a, total_rows, st);
         if (a.dk == 64)
-            return gopt ? run_tc<64, true, true>(a, total_rows, slots_bound, st)
-                        : run_tc<64, true, false>(a, total_rows, slots_bound, st);
+            return gopt ? run_tc<64, true, true>(a, total_rows, st) : run_tc<64, true, false>(a, total_rows, st);
         return cudaErrorInvalidValue;
     }
     const bool opt = a.decayed_read || a.A_log || a.beta_sig || a.G > 1 || a.v_first;
     if (a.dk == 128)
-        return opt ? run_tc<128, false, true>(a, total_rows, slots_bound, st)
-                   : run_tc<128, false, false>(a, total_rows, slots_bound, st);
+        return opt ? run_tc<128, false, true>(a, total_rows, st) : run_tc<128, false, false>(a, total_rows, st);
     if (a.dk == 64)
-        return opt ? run_tc<64, false, true>(a, total_rows, slots_bound, st)
-                   : run_tc<64, false, false>(a, total_rows, slots_bound, st);
+        return opt ? run_tc<64, false, true>(a, total_rows, st) : run_tc<64, false, false>(a, total_rows, st);
     return cudaErrorInvalidValue;
 }
 

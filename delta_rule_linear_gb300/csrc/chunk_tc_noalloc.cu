@@ -5,13 +5,16 @@
 // code on a latency-critical path where cudaMalloc / cudaFree would synchronise the
 // device, or a caller with no spare memory it can hand over.  For them this file
 // provides kda_chunk_fwd_noalloc, which runs the same prep/chain kernels as
-// kda_chunk_fwd but places their scratch (error word, chunk table, E_c slots) in a
-// file-scope __device__ array of fixed size.  It allocates nothing.
+// kda_chunk_fwd but places their scratch (error word, the chains' E_c rings and flags) in
+// a file-scope __device__ array of fixed size.  It allocates nothing.
 //
-// The array is 64 MiB and lives on every GPU that loads this library, until the process
-// exits.  Host code cannot use the array's name as a device address (on the host it is
-// only a stand-in), so the device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, on the first call made on the device.
+// The array is 48 MiB and lives on every GPU that loads this library, until the process
+// exits.  The prefill's scratch does not grow with the problem (at most kMaxChains chains,
+// each with a ring of E_c slots: about 45 MiB at head dim 128), so every supported problem
+// fits; the size check below is a guard.  Host code cannot use the array's name as a device
+// address (on the host it is only a stand-in), so the device address is looked up once per
+// device with cudaGetSymbolAddress, with that device current, on the first call made on
+// the device (or on the first kda_query_device_error(NULL, ...) there).
 #include <math.h>
 #include <mutex>
 
@@ -21,7 +24,7 @@
 namespace kda {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;   // 64 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;   // 48 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 128;
@@ -45,6 +48,13 @@ cudaError_t noalloc_scratch(void **out) {
     return cudaSuccess;
 }
 
+}  // namespace
+
+// The built-in array's header on the current device (kda_query_device_error with NULL).
+cudaError_t noalloc_header(void **out) { return noalloc_scratch(out); }
+
+namespace {
+
 bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -67,9 +77,8 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
         !aligned16(initial_state) || !aligned16(final_state) || !aligned4(beta) || !aligned4(decay))
         return KDA_ERR_ALIGN;
     const long rows = (long)B * T;
-    const long bound = chunk_tc_slots_bound(B, rows, H, T, false);
-    if (sizeof(WsHeader) + chunk_tc_scratch_bytes(B, bound, dk) > kNoAllocScratchBytes)
-        return KDA_ERR_WORKSPACE;   // the problem needs more than the built-in 64 MiB
+    if (sizeof(WsHeader) + chunk_tc_scratch_bytes(B, H, dk, false) > kNoAllocScratchBytes)
+        return KDA_ERR_WORKSPACE;   // the problem needs more than the built-in array
     if (B == 0) return KDA_OK;
     void *scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
@@ -86,6 +95,6 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the array keeps the previous call's contents: the error word must start at zero
     if (cudaMemsetAsync(scratch, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
-    cudaError_t e = (T == 0) ? launch_state_passthrough(a, st) : launch_chunk_tc(a, rows, bound, st);
+    cudaError_t e = (T == 0) ? launch_state_passthrough(a, st) : launch_chunk_tc(a, rows, st);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

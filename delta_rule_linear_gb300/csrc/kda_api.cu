@@ -120,8 +120,7 @@ size_t kda_chunk_fwd_workspace(int B, int T, int H, int dk, int dv, int chunk_si
     if (dtype != KDA_F32 && dtype != KDA_BF16) return 0;
     if (!supported_head(dk) || !supported_head(dv) || !supported_chunk(chunk_size)) return 0;
     if (chunk_tc_supported(dk, dv, chunk_size, to_dtype(dtype)) && B > 0 && T > 0)
-        return kWsHeader +
-               chunk_tc_scratch_bytes(B, chunk_tc_slots_bound(B, (long)B * T, H, T, false), dk);
+        return kWsHeader + chunk_tc_scratch_bytes(B, H, dk, false);
     return kWsHeader;
 }
 
@@ -131,8 +130,7 @@ size_t kda_varlen_fwd_workspace(int N, int total_T, int H, int dk, int dv, int c
     if (dtype != KDA_F32 && dtype != KDA_BF16) return 0;
     if (!supported_head(dk) || !supported_head(dv) || !supported_chunk(chunk_size)) return 0;
     if (chunk_tc_supported(dk, dv, chunk_size, to_dtype(dtype)) && N > 0)
-        return kWsHeader +
-               chunk_tc_scratch_bytes(N, chunk_tc_slots_bound(N, total_T, H, 0, true), dk);
+        return kWsHeader + chunk_tc_scratch_bytes(N, H, dk, true);
     return kWsHeader;
 }
 
@@ -144,8 +142,7 @@ static kda_status run_prefill(SeqBatch &a, bool chunked, long total_rows, cudaSt
     if (!chunked) {
         e = launch_recurrent(a, st);
     } else if (chunk_tc_supported(a.dk, a.dv, a.chunk, a.dtype)) {
-        const long bound = chunk_tc_slots_bound(a.nseq, total_rows, a.H, a.T, a.cu_seqlens != nullptr);
-        e = launch_chunk_tc(a, total_rows, bound, st);
+        e = launch_chunk_tc(a, total_rows, st);
     } else if (a.per_channel) {
         e = launch_recurrent(a, st);   // the per-channel decay has no CUDA-core chunk kernel
     } else {
@@ -565,7 +562,11 @@ kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const 
 }
 
 kda_status kda_query_device_error(const void *ws, kda_stream_t stream) {
-    if (!ws) return KDA_ERR_NULL;
+    if (!ws) {   // the built-in scratch of kda_chunk_fwd_noalloc on the current device
+        void *h = nullptr;
+        if (noalloc_header(&h) != cudaSuccess) return KDA_ERR_CUDA;
+        ws = h;
+    }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     WsHeader h;
     if (cudaMemcpyAsync(&h, ws, sizeof(int) * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)

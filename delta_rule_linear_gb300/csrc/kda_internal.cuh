@@ -86,12 +86,14 @@ cudaError_t launch_state_passthrough(const SeqBatch &a, cudaStream_t s);
 
 // Tensor-core chunked prefill (bf16, dk == dv in {64, 128}, chunk 64).
 bool chunk_tc_supported(int dk, int dv, int chunk, DType dt);
-// Upper bound on (chunks x heads) for a batch: equal length uses T_equal, varlen the
-// total row count plus one partial chunk per sequence.
-long chunk_tc_slots_bound(int nseq, long total_rows, int H, int T_equal, bool varlen);
-// Workspace bytes after the header for that bound.
-size_t chunk_tc_scratch_bytes(int nseq, long slots_bound, int d);
-cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, long slots_bound, cudaStream_t s);
+// Workspace bytes after the header: bounded by the chains' E_c rings (independent of the
+// sequence length) plus, for packed sequences, the schedule tables.
+size_t chunk_tc_scratch_bytes(int nseq, int H, int d, bool varlen);
+// varlen: a.T bounds the longest sequence.
+cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, cudaStream_t s);
+// Device address of kda_chunk_fwd_noalloc's built-in scratch array on the current device
+// (its first bytes are a workspace header).
+cudaError_t noalloc_header(void **out);
 // One CTA runs the tensor-core kernels' bounded waits against events that never happen,
 // each giving up after limit_ns and recording KDA_ERR_DEVICE_TIMEOUT in the header.
 cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t s);

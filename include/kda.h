@@ -39,9 +39,9 @@
  * The bf16 chunked prefill runs on the tcgen05 tensor-core path when
  * dk == dv in {64, 128} and chunk_size == 64; every other supported shape runs
  * on the fp32 CUDA-core chunk path.  Anything else returns KDA_ERR_UNSUPPORTED.
- * When the (sequence, head) pairs number at most half of the GPU's SMs, the
- * tensor-core path is one cooperative kernel launch (it occupies every SM until it
- * ends); otherwise it is two ordinary launches.
+ * The tensor-core path is one cooperative kernel launch (it occupies every SM until it
+ * ends); its workspace holds a fixed ring of chunk maps per chain (at most 40 chains), so
+ * it does not grow with the sequence length.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -148,19 +148,20 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
  *
  * Same arguments and results as kda_chunk_fwd without ws/ws_bytes, for the tensor-core
  * shapes only: dtype KDA_BF16, dk == dv in {64, 128}, chunk_size 64 (anything else
- * returns KDA_ERR_UNSUPPORTED).  Its scratch is one 64 MiB array that the library keeps
- * on every GPU that loads it, until the process exits; a problem whose scratch would not
- * fit returns KDA_ERR_WORKSPACE before anything is enqueued.  The scratch needed is
- * 256 + ceil(4(B+1)/256)*256 + ceil(4S/256)*256 + S * (D+64)^2 * 2 bytes with
- * S = B * ceil(T/64) * H (chunk, head) pairs, i.e. at most S = 910 at D = 128 and
- * 2047 at D = 64.
+ * returns KDA_ERR_UNSUPPORTED).  Its scratch is one 48 MiB array that the library keeps
+ * on every GPU that loads it, until the process exits.  The scratch needed is
+ * 256 + 256 * ceil(64 C / 256) + 256 * ceil(4 C / 256) + 32 C (D+64)^2 bytes for
+ * C = min(B*H, 40) chains, at most about 45 MiB (D = 128), whatever B, T and H; a
+ * problem whose scratch would not fit would return KDA_ERR_WORKSPACE before anything is
+ * enqueued, which no supported problem does.
  *
  * The first call on a device looks the array's device address up (with that device
- * current); make that first call before any stream capture.  Every call shares the one
- * array, so calls that overlap on the GPU (on different streams, or from different
- * threads without ordering) race and corrupt each other's results; order them.  A kernel
- * time-out of this entry point is recorded in the array's own header, which the caller
- * cannot query; kda_query_device_error does not apply.
+ * current) and keeps it for the life of the process; make that first call before any
+ * stream capture, and do not reset the device (cudaDeviceReset) after it.  Every call
+ * shares the one array, so calls that overlap on the GPU (on different streams, or from
+ * different threads without ordering) race and corrupt each other's results; order them.
+ * A kernel time-out of this entry point is recorded in the array's own header:
+ * kda_query_device_error(NULL, stream) reads it (and clears it) on the current device.
  */
 kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                  const float *beta, const float *decay,
@@ -381,7 +382,8 @@ kda_status kda_gate_decay(const float *gate, const float *A_log, const float *dt
 /*
  * Read the device error word that the kernels of the most recent kda_chunk_fwd /
  * kda_varlen_fwd call on `ws` recorded (KDA_OK if none), then clear it.  Each of
- * those calls clears the word on its stream before its kernels run.
+ * those calls clears the word on its stream before its kernels run.  ws == NULL reads
+ * the built-in array of kda_chunk_fwd_noalloc on the current device instead.
  * Synchronises `stream`; use the stream of that call.
  */
 kda_status kda_query_device_error(const void *ws, kda_stream_t stream);

@@ -226,12 +226,13 @@ def test_chunk_lengths(kda, oracle_mod, dev, T):
     assert_parity("bf16", o, ro, h, rh, tag=f"gk chunk T={T}")
 
 
-def test_chunk_two_launch_path(kda, oracle_mod, dev):
-    """More (sequence, head) pairs than half the SMs: separate prep and chain launches."""
-    d = make_gk(2, 100, 48, 64, 64, dtype="bf16", gate_scale=0.3, h0="normal002", seed=33)
+def test_chunk_several_rounds(kda, oracle_mod, dev):
+    """More (sequence, head) pairs than chains (several rounds), 20 chunks per pair (more
+    than the ring of E_c slots)."""
+    d = make_gk(2, 1250, 48, 64, 64, dtype="bf16", gate_scale=0.3, h0="normal002", seed=33)
     o, h = _run_chunk(kda, d, dev, "bf16", False)
     ro, rh = oracle_mod.forward_gk(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
-    assert_parity("bf16", o, ro, h, rh, tag="gk chunk two launches")
+    assert_parity("bf16", o, ro, h, rh, tag="gk chunk several rounds")
 
 
 @pytest.mark.parametrize("decayed", [False, True])

@@ -265,31 +265,38 @@ def test_varlen_edge_lengths(kda, oracle_mod, dev):
 
 
 @pytest.mark.parametrize("extra", [0, 1])
-def test_single_launch_boundary(kda, oracle_mod, dev, extra):
-    """B*H at half the SM count runs prep and chains in one cooperative launch; one pair
-    more switches to the two-launch path.  Both sides of the switch against the oracle."""
+def test_chain_rounds(kda, oracle_mod, dev, extra):
+    """B*H at a quarter of the SM count (the most chains there are): one chain per
+    (sequence, head), a single round; one pair more: fewer chains than pairs, two rounds.
+    T = 1100 (18 chunks) wraps every chain's ring of E_c slots.  Both against the oracle."""
     import torch
-    half = torch.cuda.get_device_properties(dev).multi_processor_count // 2
-    nsh = half + extra
+    quarter = torch.cuda.get_device_properties(dev).multi_processor_count // 4
+    nsh = quarter + extra
     H = next(h for h in (19, 17, 13, 11, 7, 5, 3, 2, 1) if nsh % h == 0)
-    d = make_custom(nsh // H, 130, H, 64, 64, dtype="bf16", decay="train", h0="normal002",
+    d = make_custom(nsh // H, 1100, H, 64, 64, dtype="bf16", decay="train", h0="normal002",
                     seed=nsh)
     o, h = _run_chunk(kda, d, dev, "bf16", 64)
     ro, rh = oracle_mod.forward(d["q"], d["k"], d["v"], d["beta"], d["decay"], d["h0"])
     assert_parity("bf16", o, ro, h, rh, tag=f"B*H={nsh}")
 
 
-def test_varlen_two_launch_path(kda, oracle_mod, dev):
-    """More (sequence, head) pairs than half the SMs, with ragged and empty sequences."""
+def test_varlen_several_rounds(kda, oracle_mod, dev):
+    """More (sequence, head) pairs than chains (several rounds, sequences taken longest
+    first), with ragged and empty sequences and some longer than the ring of E_c slots."""
     import torch
     from kda_inputs import Workload
-    wl = Workload("many", "varlen", "bf16", 1, 0, 8, 64, 64, 64, True, "long", "normal002",
-                  nseq=12)
-    d = make_varlen(wl, seed=5, lengths=[5, 130, 0, 64, 200, 1, 63, 128, 77, 0, 190, 33])
+    quarter = torch.cuda.get_device_properties(dev).multi_processor_count // 4
+    lengths = [5, 130, 0, 64, 1900, 1, 63, 128, 77, 0, 190, 33, 1100, 512, 513, 2]
+    H = -(-2 * quarter // len(lengths))   # at least twice as many pairs as chains
+    wl = Workload("many", "varlen", "bf16", 1, 0, H, 64, 64, 64, True, "long", "normal002",
+                  nseq=len(lengths))
+    d = make_varlen(wl, seed=5, lengths=lengths)
     t = inputs_to_dev(d, dev, "bf16")
-    o, h = kda.varlen_fwd(t["q"], t["k"], t["v"], t["beta"], t["cu_seqlens"], t["decay"], t["h0"],
-                          cu_seqlens_cpu=torch.from_numpy(d["cu_seqlens"]), chunk_size=64)
-    torch.cuda.synchronize()
-    ro, rh = oracle_mod.varlen(d["q"], d["k"], d["v"], d["beta"], d["cu_seqlens"], d["decay"],
-                               d["h0"])
-    assert_parity("bf16", to_np(o), ro, to_np(h), rh, tag="varlen many pairs")
+    for host in (True, False):
+        o, h = kda.varlen_fwd(t["q"], t["k"], t["v"], t["beta"], t["cu_seqlens"], t["decay"], t["h0"],
+                              cu_seqlens_cpu=torch.from_numpy(d["cu_seqlens"]) if host else None,
+                              chunk_size=64)
+        torch.cuda.synchronize()
+        ro, rh = oracle_mod.varlen(d["q"], d["k"], d["v"], d["beta"], d["cu_seqlens"], d["decay"],
+                                   d["h0"])
+        assert_parity("bf16", to_np(o), ro, to_np(h), rh, tag=f"varlen many pairs host={host}")
