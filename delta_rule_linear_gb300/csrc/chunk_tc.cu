@@ -89,6 +89,7 @@ struct TcParams {
     __nv_bfloat16 *E;          // scratch: the rings, [nch * kRing][D + 64][D + 64]
     uint32_t *flags;           // [nch * kRing]: column + 1 of the E_c a slot holds
     uint32_t *consumed;        // [nch]: chain i has loaded every E_c of a column below this
+    uint32_t *next_item;       // prep items are claimed in order from this counter
     WsHeader *ws;
     int ntask;                 // (sequence, head) tasks
     int nch;                   // chain CTAs (the first ones)
@@ -256,15 +257,14 @@ __device__ __forceinline__ void put_b(const BTiles &bt, int t, int s, const floa
 // kLP = 68 floats: 16-byte aligned rows, and conflict-free A-fragment loads), by the
 // NT = 256 threads of one group (named barrier `bar`), on the 4 x 4 grid of 16 x 16 blocks
 // (the 2 x 2 block form of the inverse of a lower-triangular matrix, applied twice):
-//  * the diagonal blocks D_i = (I + L_ii)^{-1} by forward substitution, one lane per
-//    column, the column in registers, each row of L read with 16-byte loads;
-//  * T_10 = -D_1 (L_10 D_0) and T_32 = -D_3 (L_32 D_2), one warp each;
-//  * with A = blocks 0-1 and B = blocks 2-3:  T_BA = -T_BB (L_BA T_AA), the 32 x 32
-//    products split into 16 x 8 tiles, one per warp.
+//  * with A = rows/columns 0..31 and B = 32..63: the diagonal blocks T_AA, T_BB by forward
+//    substitution, one warp each, one lane per column, the column in registers, each row
+//    of L read with 16-byte loads;
+//  * T_BA = -T_BB (L_BA T_AA), the 32 x 32 products split into 16 x 8 tiles, one per warp.
 // The off-diagonal products run on the tensor cores as warp-level tf32 MMAs (m16n8k8,
 // fp32 accumulation; operands rounded to tf32, which keeps 10 fraction bits -- T goes on
 // to the bf16 operands B = [T' | P] with 7).  Intermediate products sit in the unused
-// upper blocks of L.  Every block of T is written into B and Bf as soon as it is known.
+// upper block of L.  Every block of T is written into B and Bf as soon as it is known.
 // ---------------------------------------------------------------------------------
 constexpr int kLP = 68;
 
@@ -305,87 +305,45 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
     constexpr int P = kLP;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
-    if (warp < 4 && lane < 16) {
-        // diagonal block `warp`, column j = lane: x_r = delta_rj - sum_{s<r} L[r][s] x_s, the
-        // row of L read with 16-byte loads (unrolled, so the terms with early x_s are summed
-        // while the later ones are still being computed)
-        const int b0 = 16 * warp, j = lane;
-        float x[16];
+    if (warp < 2) {
+        // diagonal 32 x 32 block `warp` (T_AA, T_BB), column j = lane:
+        //   x_r = delta_rj - sum_{s<r} L[r][s] x_s
+        // with the row of L read by 16-byte loads; the terms with earlier x_s are summed
+        // while the later ones are still being computed, so the step from one row to the
+        // next is one paired FMA and a subtraction
+        const int b0 = 32 * warp, j = lane;
+        float x[32];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
+        for (int r = 0; r < 32; ++r) {
             const float4 *Lr = reinterpret_cast<const float4 *>(sL + (b0 + r) * P + b0);
-            float l[16];
+            float2 acc = make_float2(0.f, 0.f);   // sum_{s<r} L[r][s] x_s, by pairs of s
 #pragma unroll
             for (int m4 = 0; m4 < (r + 3) / 4; ++m4) {
                 const float4 v = Lr[m4];
-                l[4 * m4] = v.x; l[4 * m4 + 1] = v.y; l[4 * m4 + 2] = v.z; l[4 * m4 + 3] = v.w;
+                const int s0 = 4 * m4;
+                if (s0 + 1 < r) fma2(acc, make_float2(v.x, v.y), make_float2(x[s0], x[s0 + 1]));
+                else if (s0 < r) acc.x = fmaf(v.x, x[s0], acc.x);
+                if (s0 + 3 < r) fma2(acc, make_float2(v.z, v.w), make_float2(x[s0 + 2], x[s0 + 3]));
+                else if (s0 + 2 < r) acc.x = fmaf(v.z, x[s0 + 2], acc.x);
             }
-            float2 acc = make_float2(0.f, 0.f);   // sum_{s<r} L[r][s] x_s, by pairs of s
-#pragma unroll
-            for (int s = 0; s + 1 < r; s += 2)  // x_s = 0 for s < j
-                fma2(acc, make_float2(l[s], l[s + 1]), make_float2(x[s], x[s + 1]));
-            if (r & 1) acc.x = fmaf(l[r - 1], x[r - 1], acc.x);
             x[r] = ((r == j) ? 1.f : 0.f) - (acc.x + acc.y);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
+        for (int r = 0; r < 32; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
     } else {
-        // the other 192 threads zero the six strictly-upper 16 x 16 blocks of B and Bf:
-        // 6 blocks x 16 rows x 2 chunks x 4 tiles (B, Bf; T' and P halves), or of P alone
-        const int zt = warp < 4 ? warp * 16 + (lane - 16) : 64 + (warp - 4) * 32 + lane;
-        for (int idx = zt; idx < 6 * 16 * 2 * (PO ? 1 : 4); idx += NT - 64) {
-            const int ch = idx & 1, r = (idx >> 1) & 15, blk = (idx >> 5) % 6, tile = idx / 192;
-            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);          // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        // the other 192 threads zero the four 16 x 16 blocks of B and Bf above the diagonal
+        // 32 x 32 blocks: 4 blocks x 16 rows x 2 chunks x 4 tiles (B, Bf; T' and P halves),
+        // or of P alone
+        const int zt = tid - 64;
+        for (int idx = zt; idx < 4 * 16 * 2 * (PO ? 1 : 4); idx += NT - 64) {
+            const int ch = idx & 1, r = (idx >> 1) & 15, blk = (idx >> 5) & 3, tile = idx >> 7;
+            const int bi = blk >> 1, bj = 2 + (blk & 1);           // (0,2) (0,3) (1,2) (1,3)
             const int t = 16 * bi + r;
             uint8_t *base = (tile & 1 ? bt.bf : bt.b) + (tile >> 1) * 8192;
             *reinterpret_cast<uint4 *>(base + t * 128 + ((((2 * bj + ch) ^ t) & 7) << 4)) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
         idle();   // work of the caller's that fits in the substitution's shadow
-    }
-    named_sync(bar, NT);
-    if (warp < 2) {
-        // T_10 (warp 0) and T_32 (warp 1): X = L_ij D_j into L's free block (j, i), then
-        // T_ij = -D_i X
-        const int i = 2 * warp + 1, j = 2 * warp;
-        float *X = sL + 16 * j * P + 16 * i;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k0 = 0; k0 < 16; k0 += 8) {
-                uint32_t a[4], b[2];
-                frag_a(a, sL + 16 * i * P + 16 * j, k0, g, t4);
-                frag_b(b, sT + 16 * j * P + 16 * j, k0, 8 * nt, g, t4);
-                mma_tf32(d, a, b);
-            }
-            store_c(X, d, 8 * nt, g, t4, 1.f);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k0 = 0; k0 < 16; k0 += 8) {
-                uint32_t a[4], b[2];
-                frag_a(a, sT + 16 * i * P + 16 * i, k0, g, t4);
-                frag_b(b, X, k0, 8 * nt, g, t4);
-                mma_tf32(d, a, b);
-            }
-            store_c(sT + 16 * i * P + 16 * j, d, 8 * nt, g, t4, -1.f);
-            const float v0[2] = {-d[0], -d[1]}, v1[2] = {-d[2], -d[3]};
-            put_b<2, PO>(bt, 16 * i + g, 16 * j + 8 * nt + 2 * t4, v0);
-            put_b<2, PO>(bt, 16 * i + g + 8, 16 * j + 8 * nt + 2 * t4, v1);
-        }
-    } else {
-        // the diagonal blocks into B and Bf: 4 blocks x 16 rows x 4 quads of columns
-        for (int w = tid - 64; w < 256; w += NT - 64) {
-            const int blk = w >> 6, r = (w >> 2) & 15, c4 = (w & 3) * 4;
-            const float4 d = *reinterpret_cast<const float4 *>(sT + (16 * blk + r) * P + 16 * blk + c4);
-            const float dv[4] = {d.x, d.y, d.z, d.w};
-            put_b<4, PO>(bt, 16 * blk + r, 16 * blk + c4, dv);
-        }
     }
     named_sync(bar, NT);
     // X2 = L_BA T_AA (rows 32..63, columns 0..31) into L's free upper-right 32 x 32 block;
@@ -403,6 +361,14 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
             mma_tf32(d, a, b);
         }
         store_c(X2 + 16 * mi * P, d, 8 * ni, g, t4, 1.f);
+    }
+    // the diagonal blocks into B and Bf: 2 blocks x 32 rows x 8 quads of columns (the
+    // quads above a row's diagonal are zeros written by the substitution)
+    for (int w = tid; w < 512; w += NT) {
+        const int blk = w >> 8, r = (w >> 3) & 31, c4 = (w & 7) * 4;
+        const float4 d = *reinterpret_cast<const float4 *>(sT + (32 * blk + r) * P + 32 * blk + c4);
+        const float dv[4] = {d.x, d.y, d.z, d.w};
+        put_b<4, PO>(bt, 32 * blk + r, 32 * blk + c4, dv);
     }
     named_sync(bar, NT);
     // T_BA = -T_BB X2; T_BB[0:16][16:32] = 0, so rows 32..47 sum over k < 16 only
@@ -472,6 +438,7 @@ struct PrepCtrl {
     uint64_t bar_mma;
     int fail;
     float gate[2];   // A_log and dt_bias of the chunk's head (raw-gate decay), loaded with beta
+    long nxt;        // the group's next item (claimed by thread 0 while the current one runs)
 };
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
@@ -558,6 +525,20 @@ __device__ __forceinline__ long prep_items(const TcParams &p) {
     return (long)round_start(p, p.rounds) * p.nch;
 }
 
+// The next prep item, in (column, chain) order, from the launch's shared counter: a group
+// that finishes early takes the next chunk, so the prep's front stays as narrow as the
+// work allows (no group holds a chunk far ahead of the others while its chain waits for
+// another).  Items past a task's last chunk are skipped.  Returns n_items when none is
+// left.
+__device__ __forceinline__ long claim_item(const TcParams &p, long n_items) {
+    while (true) {
+        const long x = (long)atomicAdd(p.next_item, 1u);
+        if (x >= n_items) return n_items;
+        ChunkItem it;
+        if (item_info(p, x, it)) return x;
+    }
+}
+
 // The two prep groups of a CTA run the same phases; when they run them at the same time
 // they contend for issue slots and shared memory.  With `stagger`, group 1 starts its first
 // chunk only when group 0 has finished its first epilogue 1 (named barrier kStaggerBar:
@@ -574,8 +555,7 @@ constexpr int kGateBarOffset = 3;
 template <int D, bool OPT>
 __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUtensorMap *map_k,
                                            const CUtensorMap *map_E, const TcParams &p,
-                                           uint8_t *sm, uint32_t tm, int tid, int bar, long item,
-                                           long stride, bool stagger) {
+                                           uint8_t *sm, uint32_t tm, int tid, int bar, bool stagger) {
     using Ly = PrepSmem<D>;
     constexpr int NB = D / 64;
     constexpr int R = D + 64;
@@ -610,12 +590,15 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     const bool lead = stagger && bar == 1, follow = stagger && bar == 2;
     if (follow) named_sync(kStaggerBar, 2 * kGroupThreads);
     const long n_items = prep_items(p);
+    if (tid == 0) ctl->nxt = claim_item(p, n_items);
+    named_sync(bar, kGroupThreads);
+    long item = ctl->nxt;
     ChunkItem cur;
-    while (item < n_items && !item_info(p, item, cur)) item += stride;
-    if (item >= n_items) {
+    if (item >= n_items || !item_info(p, item, cur)) {
         if (lead) named_arrive(kStaggerBar, 2 * kGroupThreads);
         return;
     }
+    named_sync(bar, kGroupThreads);   // everyone has read nxt before thread 0 claims again
     load_rows<D, OPT>(p, sKQ, cur, tid, true);
     load_rows<D, OPT>(p, sKQ, cur, tid, false);
     load_scalars<OPT>(p, mbeta, mdec, ctl->gate, cur, tid);
@@ -631,10 +614,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         fence_proxy_async();   // ... visible to the tensor core behind the barrier
         named_sync(bar, kGroupThreads);
         bool ok = ctl->fail == 0;
-        long nitem = item + stride;   // this group's next chunk
-        ChunkItem nx;
-        while (nitem < n_items && !item_info(p, nitem, nx)) nitem += stride;
-        const bool more = nitem < n_items;
+        if (tid == 32) ctl->nxt = claim_item(p, n_items);   // read by all after epilogue 1's barrier
         if (tid == kStoreThread && staged >= 0) {   // the previous chunk's state-column blocks of E_c
             for (int kb = 0; kb < NB; ++kb)
                 tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, staged);
@@ -780,6 +760,17 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         named_sync(bar, kGroupThreads);
         ok = ctl->fail == 0;
         if (lead && it == 0) named_arrive(kStaggerBar, 2 * kGroupThreads);
+        // this group's next chunk; its q and k go to L2 now, ahead of their load after MMA3
+        const long nitem = ctl->nxt;
+        ChunkItem nx;
+        const bool more = nitem < n_items && item_info(p, nitem, nx);
+        if (tid == 64 && more) {
+            const int hq = OPT ? nx.h / p.G : nx.h;
+            for (int kb = 0; kb < NB; ++kb) {
+                tma_prefetch_l2_3d(map_q, kb * 64, hq, (int)nx.row0);
+                tma_prefetch_l2_3d(map_k, kb * 64, hq, (int)nx.row0);
+            }
+        }
 
         // ---- T = (I + L)^{-1}, written as B = [T' | P], Bf = diag(f) B (MN-major: row t, columns s)
         invert_unit_lower_64<kGroupThreads>(sL, sT, BTiles{sB, sBf, mcw, mbeta, mf}, tid, bar, [] {});
@@ -941,7 +932,6 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             staged_col = cur.col;
         }
         if (!more || failed) break;
-        item = nitem;
         cur = nx;
     }
     cp_async_wait_all();
@@ -1095,7 +1085,7 @@ constexpr int kGkBarPark = 3;     // threads 256..511 wait there while the inver
 // OPT: the gate and beta prologues and grouped heads (the decayed read is always a runtime choice)
 template <int D, bool OPT>
 __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const TcParams &p, uint8_t *sm,
-                                              uint32_t tm, int tid, int bar, long item, long stride) {
+                                              uint32_t tm, int tid, int bar) {
     using Ly = GkSmem<D>;
     constexpr int NT = kGkThreads;
     constexpr int NB = D / 64;
@@ -1133,9 +1123,14 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
     float *mgate = reinterpret_cast<float *>(mspan + 4);   // A_log, pad, dt_bias [D] at +4
 
     const long n_items = prep_items(p);
+    if (tid == 0) ctl->nxt = claim_item(p, n_items);
+    named_sync(bar, NT);
+    const long item = ctl->nxt;
     ChunkItem cur;
-    while (item < n_items && !item_info(p, item, cur)) item += stride;
-    if (item >= n_items) return;
+    if (item >= n_items || !item_info(p, item, cur)) return;
+    named_sync(bar, NT);   // everyone has read nxt before thread 0 claims again
+    if (tid == 0) ctl->nxt = claim_item(p, n_items);   // the next chunk, read after the barrier below
+    named_sync(bar, NT);
     if (loader) {
         load_rows<D, OPT>(p, sKQ, cur, tid, true);
         load_rows<D, OPT>(p, sKQ, cur, tid, false);
@@ -1346,10 +1341,11 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         }
         // raw q, k and g are no longer read: the next chunk's loads start once MMA1 is issued
         // (packed sequences read cu_seqlens to find it: off the path to MMA1)
-        long nitem = item + stride;
+        // the next chunk: claimed by thread 0 before the previous barrier, read here by all,
+        // claimed again after epilogue 1's barrier
+        const long nitem = ctl->nxt;
         ChunkItem nx;
-        while (nitem < n_items && !item_info(p, nitem, nx)) nitem += stride;
-        const bool more = nitem < n_items;
+        const bool more = nitem < n_items && item_info(p, nitem, nx);
         float *mbeta_next = mbeta2 + 64 * ((it + 1) & 1);
         if (ok && more && loader) {
             load_rows<D, OPT>(p, sKQ, nx, tid, true);
@@ -1400,6 +1396,8 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         fence_proxy_async();
         named_sync(bar, NT);
         ok = ctl->fail == 0;
+        // the chunk after next (a thread that waits out the inverse anyway)
+        if (tid == kGroupThreads) ctl->nxt = claim_item(p, n_items);
 
         // ---- T = (I + L)^{-1}, written as P = T diag(beta) (MN-major: row t, columns s), by
         // threads 0..255
@@ -1521,7 +1519,6 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
             pend_col = cur.col;
         }
         if (!more || failed) break;
-        item = nitem;
         cur = nx;
     }
     cp_async_wait_all();
@@ -1924,8 +1921,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        prep_group_gk<D, OPT>(&map_Ew, p, sm, tmem_base, tid, 1, (long)((int)blockIdx.x - p.nch),
-                         (long)((int)gridDim.x - p.nch));
+        prep_group_gk<D, OPT>(&map_Ew, p, sm, tmem_base, tid, 1);
         tc_fence_before();
         __syncthreads();
         if (tid < 32) {
@@ -1948,11 +1944,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const long gidx = (long)((int)blockIdx.x - p.nch) * 2 + grp;
     const long ngroups = (long)((int)gridDim.x - p.nch) * 2;
     const bool stagger = prep_items(p) >= 16 * ngroups;   // long runs only: the offset costs a start-up delay
     prep_group<D, OPT>(&map_q, &map_k, &map_E, p, gsm, tmem_base + (uint32_t)(grp * 256),
-                  tid & (kGroupThreads - 1), 1 + grp, gidx, ngroups, stagger);
+                  tid & (kGroupThreads - 1), 1 + grp, stagger);
     tc_fence_before();
     __syncthreads();
     if (tid < 32) {
@@ -2054,7 +2049,7 @@ int chains_for(long ntask, int nsm) {
 
 // Scratch layout after the workspace header (chains <= nch_max):
 //   [order: nseq ints][round_base: ntask + 1 ints]   packed sequences only
-//   [flags: nch_max * kRing][consumed: nch_max]      uint32
+//   [flags: nch_max * kRing][consumed: nch_max][next item: 1]   uint32
 //   [E_c rings: nch_max * kRing * (D + 64)^2 bf16]
 struct ScratchLayout {
     size_t order, round_base, flags, consumed, E, total;
@@ -2072,7 +2067,7 @@ ScratchLayout scratch_layout(int nseq, int H, int d, bool varlen) {
     L.flags = off;
     off += align256((size_t)nch_max * kRing * 4);
     L.consumed = off;
-    off += align256((size_t)nch_max * 4);
+    off += align256((size_t)(nch_max + 1) * 4);
     L.E = off;
     off += (size_t)nch_max * kRing * R * R * 2;
     L.total = off;
@@ -2108,6 +2103,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {
     p.round_base = varlen ? reinterpret_cast<const int *>(body + L.round_base) : nullptr;
     p.flags = reinterpret_cast<uint32_t *>(body + L.flags);
     p.consumed = reinterpret_cast<uint32_t *>(body + L.consumed);
+    p.next_item = p.consumed + std::max<long>(1, std::min<long>(p.ntask, kMaxChains));
     p.E = reinterpret_cast<__nv_bfloat16 *>(body + L.E);
 
     int dev = 0, nsm = 0;
@@ -2127,7 +2123,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {
         p.rounds = (p.ntask + p.nch - 1) / p.nch;
         const long cols = varlen ? (long)p.rounds * ((a.T + kC - 1) / kC) : (long)p.rounds * p.nc_equal;
         if (cols * p.nch >= (1L << 31)) return cudaErrorInvalidValue;   // 32-bit item indexing
-        const size_t fbytes = L.consumed + (size_t)p.nch * 4 - L.flags;
+        const size_t fbytes = reinterpret_cast<uint8_t *>(p.next_item + 1) - (body + L.flags);
         if ((e = cudaMemsetAsync(body + L.flags, 0, fbytes, st)) != cudaSuccess) return e;
         if (varlen) {
             varlen_schedule_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.nseq, a.H, p.nch, p.rounds,
