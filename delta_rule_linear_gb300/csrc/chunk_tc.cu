@@ -429,8 +429,8 @@ struct PrepSmem {
     static constexpr int R1 = KQ + NB * 16384;        // L, T fp32 [64][kLP]; later Z1, Z2
     static constexpr int R2 = R1 + 35840;             // Bf, B: MN-major [64 t][128], 16 KB each
     static constexpr int R3 = R2 + 32768;             // Aqk: K-major [64 t][64 s], 8 KB
-    static constexpr int MISC = R3 + 8192;            // per-token scalars, 9 x 64 floats
-    static constexpr int CTRL = MISC + 9 * 64 * 4;    // the group's mbarriers and status
+    static constexpr int MISC = R3 + 8192;            // per-token scalars, 10 x 64 floats
+    static constexpr int CTRL = MISC + 10 * 64 * 4;   // the group's mbarriers and status
     static constexpr int GROUP = ((CTRL + 64 + 1023) / 1024) * 1024;   // one group's share
 };
 
@@ -586,6 +586,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     float *mbeta = reinterpret_cast<float *>(sm + Ly::MISC);
     float *mdec = mbeta + 64, *mG = mdec + 64, *mGp = mG + 64, *mkn = mGp + 64, *mqn = mkn + 64;
     float *mf = mqn + 64, *meg = mf + 64, *mcw = meg + 64;
+    float *mce = mcw + 64;   // column factor exp(G_e - G_s), e the last token of s's 32-token half
 
     const bool lead = stagger && bar == 1, follow = stagger && bar == 2;
     if (follow) named_sync(kStaggerBar, 2 * kGroupThreads);
@@ -654,6 +655,10 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             mG[2 * lane] = excl + d0;
             mGp[2 * lane + 1] = excl + d0;
             mG[2 * lane + 1] = incl;
+            // G at the last token of each 32-token half: lanes 15 and 31 hold tokens 31, 63
+            const float gend = __shfl_sync(0xffffffffu, incl, lane < 16 ? 15 : 31);
+            mce[2 * lane] = __expf(gend - (excl + d0));
+            mce[2 * lane + 1] = __expf(gend - incl);
         }
         if (OPT && warp == 3 && p.beta_sig) {   // beta from logits (zero past the valid tokens)
             mbeta[2 * lane] = 2 * lane < nv ? beta_of(mbeta[2 * lane], 1, p.neg_eig) : 0.f;
@@ -701,58 +706,63 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             if (tid == kStoreThread) bulk_wait_read0();
             named_sync(bar, kGroupThreads);
             const float gC = mG[63];
-            if (i128 < 64) {
-                const int t = i128;
-                // R_t: G_{t-1} when the delta term reads h_{t-1}, G_t when it reads the decayed memory
-                const float kt = mkn[t], bt = mbeta[t], gpt = (OPT && p.decayed_read) ? mG[t] : mGp[t];
-                if (hh == 0) {
-                    mf[t] = t < nv ? __expf(gC - mG[t]) * kt : 0.f;
-                    mcw[t] = bt * __expf(gpt) * kt;   // column weight of T' = T diag(beta e^{G_{s-1}} kn)
-                }
-                float *Lrow = sL + t * kLP + 32 * hh;
-                const float bk = bt * kt;
-                float kn_s[32], g_s[32];   // this half's per-token scalars, by 16-byte loads
+            // Row t's block of 32 tokens against this warp's 32 columns (warp-uniform): above
+            // the diagonal all zeros; below it the decay factor exp(R_t - G_s) splits into
+            // exp(R_t - G_e) exp(G_e - G_s) with e the last column of the half (both <= 1 for
+            // a non-increasing G), a row factor and the column factors mce; on the diagonal
+            // block each entry takes its own exponential.
+            const bool lrows = i128 < 64;
+            const int t = lrows ? i128 : i128 - 64;
+            const int cb = t >> 5;
+            // R_t: G_{t-1} when the delta term reads h_{t-1}, G_t when it reads the decayed memory
+            const float kt = mkn[t], bt = mbeta[t];
+            const float gpt = lrows ? ((OPT && p.decayed_read) ? mG[t] : mGp[t]) : mG[t];
+            if (lrows && hh == 0) {
+                mf[t] = t < nv ? __expf(gC - mG[t]) * kt : 0.f;
+                mcw[t] = bt * __expf(gpt) * kt;   // column weight of T' = T diag(beta e^{G_{s-1}} kn)
+            }
+            // L: beta_t kn_t kn_s k_t.k_s e^{R_t - G_s} (s < t);  Aqk: qn_t kn_s q_t.k_s e^{G_t - G_s} (s <= t)
+            const float rbase = t < nv ? (lrows ? bt * kt : mqn[t]) : 0.f;
+            float v[32];
+            if (cb < hh || rbase == 0.f) {
+#pragma unroll
+                for (int s2 = 0; s2 < 32; ++s2) v[s2] = 0.f;
+            } else if (cb > hh) {
+                const float rf = rbase * __expf(gpt - mG[32 * hh + 31]);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float4 a = reinterpret_cast<const float4 *>(mkn + 32 * hh)[e];
-                    const float4 b = reinterpret_cast<const float4 *>(mG + 32 * hh)[e];
-                    kn_s[4 * e] = a.x; kn_s[4 * e + 1] = a.y; kn_s[4 * e + 2] = a.z; kn_s[4 * e + 3] = a.w;
-                    g_s[4 * e] = b.x; g_s[4 * e + 1] = b.y; g_s[4 * e + 2] = b.z; g_s[4 * e + 3] = b.w;
+                    const float4 c = reinterpret_cast<const float4 *>(mce + 32 * hh)[e];
+                    v[4 * e] = rf * a.x * c.x * __uint_as_float(r[4 * e]);
+                    v[4 * e + 1] = rf * a.y * c.y * __uint_as_float(r[4 * e + 1]);
+                    v[4 * e + 2] = rf * a.z * c.z * __uint_as_float(r[4 * e + 2]);
+                    v[4 * e + 3] = rf * a.w * c.w * __uint_as_float(r[4 * e + 3]);
                 }
-                float lv[32];
+            } else {
+                const int lim = lrows ? (t & 31) : (t & 31) + 1;   // columns s2 < lim are kept
 #pragma unroll
-                for (int s2 = 0; s2 < 32; ++s2) {
-                    const int s = 32 * hh + s2;
-                    const float val = bk * kn_s[s2] * __uint_as_float(r[s2]) * __expf(gpt - g_s[s2]);
-                    lv[s2] = (s < t && t < nv) ? val : 0.f;
+                for (int e = 0; e < 8; ++e) {
+                    const float4 a = reinterpret_cast<const float4 *>(mkn + 32 * hh)[e];
+                    const float4 g = reinterpret_cast<const float4 *>(mG + 32 * hh)[e];
+                    const float kn4[4] = {a.x, a.y, a.z, a.w}, g4[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int s2 = 4 * e + u;
+                        const float val = rbase * kn4[u] * __uint_as_float(r[s2]) * __expf(gpt - g4[u]);
+                        v[s2] = s2 < lim ? val : 0.f;
+                    }
                 }
+            }
+            if (lrows) {
+                float *Lrow = sL + t * kLP + 32 * hh;
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    reinterpret_cast<float4 *>(Lrow)[e] =
-                        make_float4(lv[4 * e], lv[4 * e + 1], lv[4 * e + 2], lv[4 * e + 3]);
+                    reinterpret_cast<float4 *>(Lrow)[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
             } else {
-                const int t = i128 - 64;
-                const float qt = mqn[t], gt = mG[t];
-                float kn_s[32], g_s[32];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float4 a = reinterpret_cast<const float4 *>(mkn + 32 * hh)[e];
-                    const float4 b = reinterpret_cast<const float4 *>(mG + 32 * hh)[e];
-                    kn_s[4 * e] = a.x; kn_s[4 * e + 1] = a.y; kn_s[4 * e + 2] = a.z; kn_s[4 * e + 3] = a.w;
-                    g_s[4 * e] = b.x; g_s[4 * e + 1] = b.y; g_s[4 * e + 2] = b.z; g_s[4 * e + 3] = b.w;
-                }
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int s = 32 * hh + cc * 8 + e;
-                        const float val = qt * kn_s[cc * 8 + e] * __uint_as_float(r[cc * 8 + e]) *
-                                          __expf(gt - g_s[cc * 8 + e]);
-                        f[e] = (s <= t && t < nv) ? val : 0.f;
-                    }
                     const int chunk = 4 * hh + cc;
-                    *reinterpret_cast<uint4 *>(sA + t * 128 + ((chunk ^ (t & 7)) << 4)) = pack8(f);
+                    *reinterpret_cast<uint4 *>(sA + t * 128 + ((chunk ^ (t & 7)) << 4)) = pack8(v + 8 * cc);
                 }
             }
         }
@@ -909,15 +919,23 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             if (HALF == 64) tmem_ld32(tm + tq + hh * HALF + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * (HALF / 64)));
             tmem_ld_wait();
             if (has_row) {   // E[i][j] = gamma_C delta_ij - (K~^T W)[i][j]
+                // the diagonal lies in this half for the warps whose rows are its rows (warp-uniform)
+                const bool dhalf = (i / HALF) == hh;
 #pragma unroll
                 for (int cc = 0; cc < HALF / 8; ++cc) {
                     const int col = hh * HALF + 8 * cc;
-                    float f[8];
+                    uint4 w;
+                    if (dhalf) {
+                        float f[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        f[e] = (col + e == i ? gamma_c : 0.f) - __uint_as_float(v[8 * cc + e]);
+                        for (int e = 0; e < 8; ++e)
+                            f[e] = (col + e == i ? gamma_c : 0.f) - __uint_as_float(v[8 * cc + e]);
+                        w = pack8(f);
+                    } else {
+                        w = pack8un(v + 8 * cc);
+                    }
                     *reinterpret_cast<uint4 *>(sEst + (col >> 6) * (R * 128) + i * 128 +
-                                               ((((col & 63) >> 3) ^ (i & 7)) << 4)) = pack8(f);
+                                               ((((col & 63) >> 3) ^ (i & 7)) << 4)) = w;
                 }
             }
         }
