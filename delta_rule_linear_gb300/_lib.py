@@ -28,7 +28,7 @@ EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace", "kda_c
            "kda_recurrent_fwd_ex", "kda_decode_step_ex", "kda_gate_decay",
            "kda_gk_chunk_fwd", "kda_gk_varlen_fwd", "kda_gk_recurrent_fwd",
            "kda_gk_recurrent_bwd_workspace", "kda_gk_recurrent_bwd",
-           "kda_recurrent_bwd_workspace", "kda_recurrent_bwd",
+           "kda_recurrent_bwd_workspace", "kda_recurrent_bwd", "kda_chunk_bwd_workspace", "kda_chunk_bwd",
            "kda_gk_varlen_recurrent_fwd", "kda_gk_decode_step", "kda_query_device_error",
            "kda_diag_wait_timeout")
 
@@ -123,6 +123,11 @@ def load(path: str | None = None):
         lib.kda_recurrent_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
                                           I, F, I, I, P, Z, P]
         lib.kda_recurrent_bwd.restype = I
+        lib.kda_chunk_bwd_workspace.argtypes = [I, I, I, I, I]
+        lib.kda_chunk_bwd_workspace.restype = Z
+        lib.kda_chunk_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
+                                      I, F, I, I, P, Z, P]
+        lib.kda_chunk_bwd.restype = I
         lib.kda_gate_decay.argtypes = [P, P, P, P, ctypes.c_long, I, I, P]
         lib.kda_gate_decay.restype = I
         lib.kda_gk_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, O, P,
@@ -617,4 +622,35 @@ def recurrent_bwd(q, k, v, beta, decay, initial_state, d_o, dfinal_state=None, *
                                int(bool(decayed_read)), _ptr(ws), ws.numel() * ws.element_size(),
                                _stream(stream))
     _raise(rc, "kda_recurrent_bwd", lib)
+    return out
+
+
+def chunk_bwd(q, k, v, beta, decay, initial_state, d_o, dfinal_state=None, *, scale=None,
+                  use_qk_l2norm=True, decayed_read=False, workspace=None, stream=None):
+    """kda_chunk_bwd: the gradients of recurrent_bwd computed by chunks on the tensor cores
+    (bf16 q/k/v/d_o, dk == dv in {64, 128}).  Returns a dict dq, dk, dv, dbeta, ddecay, dh0."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, H, dv))
+    _check(beta, "beta", torch.float32, (B, T, H)); _check(decay, "decay", torch.float32, (B, T, H))
+    _check(initial_state, "initial_state", torch.float32, (B, H, dk, dv))
+    _check(d_o, "d_o", q.dtype, (B, T, H, dv))
+    _check(dfinal_state, "dfinal_state", torch.float32, (B, H, dk, dv))
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = dict(dq=torch.empty((B, T, H, dk), **f32), dk=torch.empty((B, T, H, dk), **f32),
+               dv=torch.empty((B, T, H, dv), **f32), dbeta=torch.empty((B, T, H), **f32),
+               ddecay=torch.empty((B, T, H), **f32), dh0=torch.empty((B, H, dk, dv), **f32))
+    need = lib.kda_chunk_bwd_workspace(B, T, H, dk, dv)
+    if need == 0:
+        raise KdaError(4, "kda_chunk_bwd_workspace", lib)
+    ws = _workspace(need, q.device, workspace)
+    rc = lib.kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state),
+                               _ptr(d_o), _ptr(dfinal_state), _ptr(out["dq"]), _ptr(out["dk"]),
+                               _ptr(out["dv"]), _ptr(out["dbeta"]), _ptr(out["ddecay"]), _ptr(out["dh0"]),
+                               B, T, H, dk, dv, dt, float(scale or 0.0), int(bool(use_qk_l2norm)),
+                               int(bool(decayed_read)), _ptr(ws), ws.numel() * ws.element_size(),
+                               _stream(stream))
+    _raise(rc, "kda_chunk_bwd", lib)
     return out

@@ -86,8 +86,13 @@ struct TcParams {
     const __nv_bfloat16 *q, *k;   // [rows, H, D]
     long rows;                 // token rows of q, k, v
     __nv_bfloat16 *o;          // [rows, H, D]
-    __nv_bfloat16 *E;          // scratch: the rings, [nch * kRing][D + 64][D + 64]
-    uint32_t *flags;           // [nch * kRing]: column + 1 of the E_c a slot holds
+    __nv_bfloat16 *E;          // scratch: the rings, [nch * ring][D + 64][D + 64]
+    uint32_t *flags;           // [nch * ring]: column + 1 of the E_c a slot holds
+    int ring;                  // E_c slots per chain (kRing; every column's own slot when the
+                               // maps are kept for the backward)
+    float *states;             // or nullptr: fp32 state at every chunk start [nseq, H, nc, D, D]
+                               // (the reverse walk: the incoming state gradient of every chunk)
+    float *dv_out;             // the reverse walk: fp32 value gradient [rows, H, D]
     uint32_t *consumed;        // [nch]: chain i has loaded every E_c of a column below this
     uint32_t *next_item;       // prep items are claimed in order from this counter
     WsHeader *ws;
@@ -177,7 +182,7 @@ __device__ __forceinline__ bool item_info(const TcParams &p, long item, ChunkIte
     it.nv = min(kC, len - c * kC);
     it.col = col;
     it.chain = chain;
-    it.slot = chain * kRing + col % kRing;
+    it.slot = chain * p.ring + col % p.ring;
     return true;
 }
 
@@ -508,8 +513,8 @@ __device__ __forceinline__ void release_slot(const TcParams &p, int slot, int co
 // the E_c that the slot held (column col - kRing), giving up after limit_ns; the async
 // proxy is then ordered after the acquire (the slot is written by TMA stores).
 __device__ __forceinline__ bool wait_slot_free(const TcParams &p, int chain, int col, uint64_t limit_ns) {
-    if (col >= kRing) {
-        const uint32_t need = (uint32_t)(col - kRing + 1);
+    if (col >= p.ring) {
+        const uint32_t need = (uint32_t)(col - p.ring + 1);
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_gpu(p.consumed + chain) < need) {
             if (globaltimer_ns() - t0 > limit_ns) return false;
@@ -1595,7 +1600,13 @@ __device__ __forceinline__ bool chain_task(const TcParams &p, int chain, int r, 
     return true;
 }
 
-template <int D, bool OPT>
+// REV: the reverse walk of the backward, [dS_c; dV_c] = E_c^T [dS_{c+1}; dO_c] (E_c^T's
+// product is the same instruction sequence with E_c read MN-major): chunks last to first,
+// map_v streams dO, h0 holds the final-state gradient and hT receives the initial-state
+// gradient, the "outputs" are the fp32 value gradients (dv_out), and `states` receives
+// the incoming state gradient of every chunk.  The maps were kept by a forward launch
+// (every chunk its own slot), so nothing waits on flags.
+template <int D, bool OPT, bool REV = false>
 __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUtensorMap *map_v,
                                            const TcParams &p, uint8_t *sm, int chain) {
     using Cf = ChainCfg<D>;
@@ -1655,9 +1666,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                         record_error(p.ws, 10);
                         break;
                     }
-                    const int col = t.col0 + c;
-                    const int slot = chain * kRing + col % kRing;
-                    if (!wait_flag_acquire(p.flags + slot, (uint32_t)col + 1u, kWaitNs)) {   // E_c published
+                    const int col = t.col0 + (REV ? t.nc - 1 - c : c);
+                    const int slot = chain * p.ring + col % p.ring;
+                    if (!REV && !wait_flag_acquire(p.flags + slot, (uint32_t)col + 1u, kWaitNs)) {   // E_c published
                         s_fail = 1;
                         record_error(p.ws, 16);
                         break;
@@ -1670,10 +1681,11 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
             }
         } else if (lane == 1) {
             int gc = 0;
+            auto chunk_row = [&](int c) { return (int)(t.start + (long)(REV ? t.nc - 1 - c : c) * kC); };
             for (int r = 0; chain_task(p, chain, r, t) && !s_fail; ++r) {
                 for (int c = 0; c < kPrefetch && c < t.nc; ++c)
                     for (int mb = 0; mb < Cf::NB; ++mb)
-                        tma_prefetch_l2_3d(map_v, mb * 64, t.h, (int)(t.start + (long)c * kC));
+                        tma_prefetch_l2_3d(map_v, mb * 64, t.h, chunk_row(c));
                 for (int c = 0; c < t.nc && !s_fail; ++c, ++gc) {
                     const int s = gc & 1;
                     if (gc >= 2 && !mbar_wait(&v_empty[s], ((gc >> 1) - 1) & 1, kWaitNs)) {
@@ -1684,11 +1696,10 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                     mbar_expect_tx(&v_full[s], Cf::AV_BYTES);
                     uint8_t *dV = sAV0 + s * Cf::AV_BYTES;
                     for (int mb = 0; mb < Cf::NB; ++mb)
-                        tma_load_3d(dV + mb * 8192, map_v, &v_full[s], mb * 64, t.h,
-                                    (int)(t.start + (long)c * kC));
+                        tma_load_3d(dV + mb * 8192, map_v, &v_full[s], mb * 64, t.h, chunk_row(c));
                     if (c + kPrefetch < t.nc)
                         for (int mb = 0; mb < Cf::NB; ++mb)
-                            tma_prefetch_l2_3d(map_v, mb * 64, t.h, (int)(t.start + (long)(c + kPrefetch) * kC));
+                            tma_prefetch_l2_3d(map_v, mb * 64, t.h, chunk_row(c + kPrefetch));
                 }
             }
         }
@@ -1696,8 +1707,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
         // ---------------- ring release: publish the chain's progress (s_rel, set by the MMA
         // issuer when an E_c load has landed) to the prep groups by a gpu-scope release,
         // ~900 cycles, kept off the producer and MMA threads.  Only the latest value counts,
-        // so a release that falls behind skips ahead.
-        if (lane == 0) {
+        // so a release that falls behind skips ahead.  (The reverse walk has no prep.)
+        if (lane == 0 && !REV) {
             uint32_t fin = 0;   // the counter's final value: the end of the chain's last round
             for (int r = 0; chain_task(p, chain, r, t); ++r) fin = (uint32_t)t.col_end;
             uint32_t done = 0;
@@ -1719,8 +1730,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idV = idesc_bf16_f32(D, R, true, false);
-            const uint32_t idS = idesc_bf16_f32(D, R, false, false);
+            const uint32_t idV = idesc_bf16_f32(D, R, true, REV);
+            const uint32_t idS = idesc_bf16_f32(D, R, false, REV);
             const uint32_t as0 = smem_u32(sAS);
             int gc = 0;
             for (int r = 0; chain_task(p, chain, r, t) && !s_fail; ++r) {
@@ -1745,18 +1756,19 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                     const uint32_t e0 = smem_u32(sE0 + b * Cf::E_BYTES);
                     const uint32_t av0 = smem_u32(sAV0 + b * Cf::AV_BYTES);
                     const uint32_t dcol = tm + (uint32_t)(b * R);
-                    for (int ks = 0; ks < 4; ++ks)   // V half: E_c columns D .. D + 63
+                    for (int ks = 0; ks < 4; ++ks)   // V half: E_c columns D .. D + 63 (reverse: rows)
                         mma_bf16_ss(dcol, desc_mnmajor_sw128(av0, 64, ks),
-                                    desc_kmajor_sw128(e0, R, D / 16 + ks), idV, ks > 0 ? 1u : 0u);
+                                    REV ? desc_mnmajor_sw128(e0, R, D / 16 + ks) : desc_kmajor_sw128(e0, R, D / 16 + ks),
+                                    idV, ks > 0 ? 1u : 0u);
                     if (!mbar_wait(&s_ready, gc & 1, kWaitNs)) {
                         s_fail = 1;
                         record_error(p.ws, 12);
                         break;
                     }
                     tc_fence_after();
-                    for (int ks = 0; ks < D / 16; ++ks)   // state half: E_c columns 0 .. D - 1
-                        mma_bf16_ss(dcol, desc_kmajor_sw128(as0, D, ks), desc_kmajor_sw128(e0, R, ks),
-                                    idS, 1u);
+                    for (int ks = 0; ks < D / 16; ++ks)   // state half: E_c columns 0 .. D - 1 (reverse: rows)
+                        mma_bf16_ss(dcol, desc_kmajor_sw128(as0, D, ks),
+                                    REV ? desc_mnmajor_sw128(e0, R, ks) : desc_kmajor_sw128(e0, R, ks), idS, 1u);
                     mma_commit(&d_full[b]);
                     mma_commit(&e_empty[b]);
                     mma_commit(&v_empty[b]);
@@ -1777,14 +1789,22 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
         const bool vf = OPT && p.v_first;
         const size_t si = vf ? 1 : D, sj = vf ? D : 1;
         int gc = 0;
+        // fp32 state at a chunk's start (key-major [nseq, H, nc, D, D]), kept for the backward
+        auto dump_at = [&](int chunk) {
+            return p.states + (((size_t)t.n * p.H + t.h) * p.nc_equal + chunk) * D * D;
+        };
         for (int r = 0; chain_task(p, chain, r, t) && !s_fail; ++r) {
             const size_t hbase = ((size_t)t.n * p.H + t.h) * D * D;
             if (has_row) {   // S_0^T row j from initial_state[:, j] (the previous task's MMAs are done)
+                float *dst = (p.states && t.nc > 0) ? dump_at(REV ? t.nc - 1 : 0) : nullptr;
                 for (int i0 = i_lo; i0 < i_lo + HALF; i0 += 8) {
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         x[e] = p.h0 ? p.h0[hbase + (size_t)(i0 + e) * si + j * sj] : 0.f;
+                    if (dst)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) dst[(size_t)(i0 + e) * D + j] = x[e];
                     if (t.nc == 0) {
                         if (p.hT)
 #pragma unroll
@@ -1819,6 +1839,11 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                 tc_fence_before();
                 mbar_arrive(&d_free[b]);
                 if (has_row) {
+                    if (!last && p.states) {   // the state the next chunk starts from
+                        float *dst = dump_at(REV ? t.nc - 2 - c : c + 1) + (size_t)i_lo * D + j;
+#pragma unroll
+                        for (int i = 0; i < HALF; ++i) dst[(size_t)i * D] = __uint_as_float(v[i]);
+                    }
                     if (!last) {
 #pragma unroll
                         for (int cc = 0; cc < HALF / 8; ++cc) {
@@ -1859,7 +1884,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
         constexpr int CPR = D / 8;      // 16-byte pieces per output row
         // Every output warp passes both named barriers of every chunk, failed or not (a
         // warp that left the loop early would leave the others waiting at the barrier);
-        // after a failure the remaining chunks are skipped without waiting.
+        // after a failure the remaining chunks are skipped without waiting.  The reverse
+        // walk writes its fp32 value gradients straight from the registers instead (token
+        // by token, the warp's 32 value columns contiguous).
         int gc = 0;
         for (int r = 0; chain_task(p, chain, r, t); ++r) {
             for (int c = 0; c < t.nc; ++c, ++gc) {
@@ -1880,12 +1907,21 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                     tc_fence_before();
                     mbar_arrive(&d_free[b]);
                 }
+                if (REV) {
+                    const int cc = t.nc - 1 - c;
+                    const int nv = ok ? min(kC, t.len - cc * kC) : 0;
+                    if (has_row)
+                        for (int tt = 0; tt < nv; ++tt)
+                            p.dv_out[((size_t)(t.start + (long)cc * kC + tt) * p.H + t.h) * D + j] =
+                                __uint_as_float(v[tt]);
+                    continue;
+                }
                 named_sync(1, 128);          // the previous chunk's rows have been written out
                 if (ok && has_row)
 #pragma unroll
                     for (int tt = 0; tt < kC; ++tt) stg[tt * D + j] = __float2bfloat16_rn(__uint_as_float(v[tt]));
                 named_sync(1, 128);
-                const int nv = ok ? min(kC, t.len - c * kC) : 0;
+                const int nv = (ok && p.o) ? min(kC, t.len - c * kC) : 0;
                 __nv_bfloat16 *obase = p.o + ((size_t)(t.start + (long)c * kC) * p.H + t.h) * D;
 #pragma unroll
                 for (int k = et; k < kC * CPR; k += 128) {
@@ -2072,10 +2108,14 @@ int chains_for(long ntask, int nsm) {
 struct ScratchLayout {
     size_t order, round_base, flags, consumed, E, total;
 };
-ScratchLayout scratch_layout(int nseq, int H, int d, bool varlen) {
+// keep_nc > 0: the maps of every chunk are kept for a reverse walk (equal-length batches of
+// keep_nc chunks): each chain's ring holds all of its columns, rounds x keep_nc.
+ScratchLayout scratch_layout(int nseq, int H, int d, bool varlen, int keep_nc = 0) {
     const long ntask = (long)nseq * H;
     const long nch_max = std::max<long>(1, std::min<long>(ntask, kMaxChains));
     const size_t R = (size_t)d + 64;
+    // slots: chains x ring; when keeping, chains x rounds x keep_nc <= (ntask + chains) x keep_nc
+    const size_t slots = keep_nc > 0 ? (size_t)(ntask + nch_max) * keep_nc : (size_t)nch_max * kRing;
     ScratchLayout L{};
     size_t off = 0;
     L.order = off;
@@ -2083,18 +2123,27 @@ ScratchLayout scratch_layout(int nseq, int H, int d, bool varlen) {
     L.round_base = off;
     if (varlen) off += align256((size_t)(ntask + 1) * 4);
     L.flags = off;
-    off += align256((size_t)nch_max * kRing * 4);
+    off += align256(slots * 4);
     L.consumed = off;
     off += align256((size_t)(nch_max + 1) * 4);
     L.E = off;
-    off += (size_t)nch_max * kRing * R * R * 2;
+    off += slots * R * R * 2;
     L.total = off;
     return L;
 }
 
+// What a forward launch that kept its maps leaves for the reverse walk.
+struct TcPlan {
+    int nch, ring, rounds;
+    __nv_bfloat16 *E;
+};
+
 // OPT: the kda_options paths, compiled out of the plain instantiations
+// states: or nullptr, the fp32 state at every chunk start; keep: or nullptr, every chunk's
+// map stays in the scratch and the plan is returned (equal-length batches only).
 template <int D, bool GK, bool OPT>
-cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {
+cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st, float *states = nullptr,
+                   TcPlan *keep = nullptr) {
     constexpr int R = D + 64;
     using Cf = ChainCfg<D>;
     TcParams p{};
@@ -2114,7 +2163,9 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {
     p.ws = a.ws;
     p.ntask = a.nseq * a.H;
     const bool varlen = a.cu_seqlens != nullptr;
-    const ScratchLayout L = scratch_layout(a.nseq, a.H, D, varlen);
+    if (keep && varlen) return cudaErrorInvalidValue;
+    p.states = states;
+    const ScratchLayout L = scratch_layout(a.nseq, a.H, D, varlen, keep ? p.nc_equal : 0);
     if (L.total > a.ws_body_bytes) return cudaErrorInvalidValue;
     uint8_t *body = static_cast<uint8_t *>(a.ws_body);
     p.order = varlen ? reinterpret_cast<const int *>(body + L.order) : nullptr;
@@ -2139,6 +2190,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {
     for (int grid = nsm; grid >= 2; grid -= std::max(1, grid / 8)) {
         p.nch = chains_for(p.ntask, grid);
         p.rounds = (p.ntask + p.nch - 1) / p.nch;
+        p.ring = keep ? p.rounds * p.nc_equal : kRing;
         const long cols = varlen ? (long)p.rounds * ((a.T + kC - 1) / kC) : (long)p.rounds * p.nc_equal;
         if (cols * p.nch >= (1L << 31)) return cudaErrorInvalidValue;   // 32-bit item indexing
         const size_t fbytes = reinterpret_cast<uint8_t *>(p.next_item + 1) - (body + L.flags);
@@ -2150,7 +2202,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         CUtensorMap mq, mk, mv, me, mew;
-        const long slots = (long)p.nch * kRing;
+        const long slots = (long)p.nch * p.ring;
         if (!map_tokens(&mq, a.q, total_rows, a.H / p.G, D) || !map_tokens(&mk, a.k, total_rows, a.H / p.G, D) ||
             !map_tokens(&mv, a.v, total_rows, a.H, D) || !map_E(&me, p.E, slots, R) ||
             !map_E_tiles(&mew, p.E, slots, R))
@@ -2166,10 +2218,48 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, tc_kernel<D, GK, OPT>, mq, mk, mv, me, mew, p);
+        if (e == cudaSuccess && keep) *keep = TcPlan{p.nch, p.ring, p.rounds, p.E};
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         (void)cudaGetLastError();
     }
     return cudaErrorCooperativeLaunchTooLarge;
+}
+
+// The reverse walk over the maps a forward launch kept (plan): one chain CTA per task
+// slot of the forward, chunks last to first; d_o streamed like v, dhT in, dh0 out (either
+// may be nullptr: zeros in, not written), dv and the incoming state gradient of every chunk
+// (dstates) out.
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1) rev_chain_kernel(const __grid_constant__ CUtensorMap map_E,
+                                                                  const __grid_constant__ CUtensorMap map_do,
+                                                                  TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    chain_body<D, false, true>(&map_E, &map_do, p, align1024(smem_raw), (int)blockIdx.x);
+}
+
+template <int D>
+cudaError_t run_rev(const SeqBatch &a, const TcPlan &plan, const void *d_o, const float *dhT, float *dh0,
+                    float *dv, float *dstates, cudaStream_t st) {
+    constexpr int R = D + 64;
+    using Cf = ChainCfg<D>;
+    TcParams p{};
+    p.nseq = a.nseq; p.H = a.H; p.T = a.T;
+    p.nc_equal = (a.T + kC - 1) / kC;
+    p.h0 = dhT; p.hT = dh0;
+    p.rows = (long)a.nseq * a.T;
+    p.ws = a.ws;
+    p.ntask = a.nseq * a.H;
+    p.nch = plan.nch; p.rounds = plan.rounds; p.ring = plan.ring;
+    p.E = plan.E;
+    p.states = dstates;
+    p.dv_out = dv;
+    CUtensorMap me, mdo;
+    if (!map_E(&me, p.E, (long)p.nch * p.ring, R) || !map_tokens(&mdo, d_o, p.rows, a.H, D))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(rev_chain_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    if (e != cudaSuccess) return e;
+    rev_chain_kernel<D><<<(unsigned)p.nch, kTcThreads, Cf::SMEM, st>>>(me, mdo, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -2190,6 +2280,29 @@ cudaError_t launch_timeout_probe(WsHeader *ws, uint64_t limit_ns, cudaStream_t s
     if (e != cudaSuccess) return e;
     timeout_probe_kernel<<<1, 32, 0, st>>>(ws, never, limit_ns);
     return cudaGetLastError();
+}
+
+size_t chunk_tc_keep_bytes(int B, int H, int T, int d) {
+    return scratch_layout(B, H, d, false, (T + kC - 1) / kC).total;
+}
+
+cudaError_t launch_chunk_tc_walks(const SeqBatch &a, const void *d_o, const float *dhT, float *dh0, float *dv,
+                                  float *fstates, float *bstates, cudaStream_t st) {
+    if ((long)a.nseq * a.T >= (1L << 31) || a.cu_seqlens || a.per_channel) return cudaErrorInvalidValue;
+    const bool opt = a.decayed_read != 0;
+    TcPlan plan{};
+    cudaError_t e;
+    if (a.dk == 128) {
+        e = opt ? run_tc<128, false, true>(a, (long)a.nseq * a.T, st, fstates, &plan)
+                : run_tc<128, false, false>(a, (long)a.nseq * a.T, st, fstates, &plan);
+        return e != cudaSuccess ? e : run_rev<128>(a, plan, d_o, dhT, dh0, dv, bstates, st);
+    }
+    if (a.dk == 64) {
+        e = opt ? run_tc<64, false, true>(a, (long)a.nseq * a.T, st, fstates, &plan)
+                : run_tc<64, false, false>(a, (long)a.nseq * a.T, st, fstates, &plan);
+        return e != cudaSuccess ? e : run_rev<64>(a, plan, d_o, dhT, dh0, dv, bstates, st);
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, cudaStream_t st) {

@@ -596,3 +596,81 @@ kda_status kda_diag_wait_timeout(void *ws, size_t ws_bytes, unsigned limit_us,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------
+// Chunked backward (tensor cores): the forward walk keeping every chunk's map and state,
+// the reverse walk over the maps, then the chunk-local gradients.
+// Workspace after the header: the forward's kept scratch | states at every chunk start |
+// incoming state gradients of every chunk | the gradient kernel's per-CTA scratch.
+static size_t chunk_bwd_layout(int B, int T, int H, int d, size_t *off_states, size_t *off_dstates,
+                               size_t *off_scratch) {
+    const size_t keep = (chunk_tc_keep_bytes(B, H, T, d) + 255) / 256 * 256;
+    const size_t st = (size_t)B * H * ((T + 63) / 64) * d * d * sizeof(float);
+    if (off_states) *off_states = kWsHeader + keep;
+    if (off_dstates) *off_dstates = kWsHeader + keep + st;
+    if (off_scratch) *off_scratch = kWsHeader + keep + 2 * st;
+    return kWsHeader + keep + 2 * st + (size_t)chunk_bwd_ctas() * chunk_bwd_scratch_floats(d) * sizeof(float);
+}
+
+size_t kda_chunk_bwd_workspace(int B, int T, int H, int dk, int dv) {
+    if (B < 0 || T < 0 || H <= 0 || dk != dv || (dk != 64 && dk != 128)) return 0;
+    if (B == 0 || T == 0) return kWsHeader;
+    return chunk_bwd_layout(B, T, H, dk, nullptr, nullptr, nullptr);
+}
+
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const float *beta,
+                         const float *decay, const float *initial_state, const void *d_o,
+                         const float *dfinal_state, float *dq, float *dk_out, float *dv_out,
+                         float *dbeta, float *ddecay, float *dinitial_state, int B, int T, int H,
+                         int dk, int dv, kda_dtype dtype, float scale, int use_qk_l2norm,
+                         int decayed_read, void *ws, size_t ws_bytes, kda_stream_t stream) {
+    if (B < 0 || T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, decay, initial_state, d_o, dfinal_state,
+                                (long)B * T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (dtype != KDA_BF16 || dk != dv || (dk != 64 && dk != 128)) return KDA_ERR_UNSUPPORTED;
+    const long rows = (long)B * T;
+    if (rows >= (1L << 31)) return KDA_ERR_UNSUPPORTED;
+    if (rows > 0 && (!dq || !dk_out || !dv_out || !dbeta)) return KDA_ERR_NULL;
+    if (!aligned16(dinitial_state) || !aligned4(dq) || !aligned4(dk_out) || !aligned4(dv_out) ||
+        !aligned4(dbeta) || !aligned4(ddecay))
+        return KDA_ERR_ALIGN;
+    const size_t need = kda_chunk_bwd_workspace(B, T, H, dk, dv);
+    if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0) {   // nothing but the state: dh0 = dhT
+        if (!dinitial_state || B == 0) return KDA_OK;
+        const size_t n = (size_t)B * H * dk * dv * sizeof(float);
+        if (dfinal_state) return launch_status(cudaMemcpyAsync(dinitial_state, dfinal_state, n, cudaMemcpyDeviceToDevice, st));
+        return launch_status(cudaMemsetAsync(dinitial_state, 0, n, st));
+    }
+    size_t o_st = 0, o_dst = 0, o_scr = 0;
+    chunk_bwd_layout(B, T, H, dk, &o_st, &o_dst, &o_scr);
+    char *w = static_cast<char *>(ws);
+    float *fstates = reinterpret_cast<float *>(w + o_st), *bstates = reinterpret_cast<float *>(w + o_dst);
+    if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
+    SeqBatch a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = decay; a.h0 = initial_state;
+    a.o = nullptr; a.hT = nullptr; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
+    a.dk = dk; a.dv = dv; a.chunk = 64; a.dtype = DType::BF16;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    a.decayed_read = decayed_read ? 1 : 0;
+    a.ws = static_cast<WsHeader *>(ws);
+    a.ws_body = w + kWsHeader;
+    a.ws_body_bytes = o_st - kWsHeader;
+    cudaError_t e = launch_chunk_tc_walks(a, d_o, dfinal_state, dinitial_state, dv_out, fstates, bstates, st);
+    if (e != cudaSuccess) return launch_status(e);
+    ChunkBwdArgs g{};
+    g.q = q; g.k = k; g.v = v; g.d_o = d_o; g.beta = beta; g.decay = decay;
+    g.fstates = fstates; g.bstates = bstates;
+    g.dq = dq; g.dk = dk_out; g.dbeta = dbeta; g.ddecay = decay ? ddecay : nullptr;
+    g.B = B; g.T = T; g.H = H; g.D = dk;
+    g.scale = a.scale; g.use_l2 = a.use_l2; g.decayed_read = a.decayed_read;
+    g.scratch = reinterpret_cast<float *>(w + o_scr);
+    g.ctas = chunk_bwd_ctas();
+    if (!decay && ddecay &&   // ddecay without a decay: a zero gradient
+        cudaMemsetAsync(ddecay, 0, (size_t)rows * H * sizeof(float), st) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return launch_status(launch_chunk_bwd_grads(g, st));
+}

@@ -91,6 +91,30 @@ bool chunk_tc_supported(int dk, int dv, int chunk, DType dt);
 size_t chunk_tc_scratch_bytes(int nseq, int H, int d, bool varlen);
 // varlen: a.T bounds the longest sequence.
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, cudaStream_t s);
+// The two walks of the chunked backward (equal-length bf16 batches, per-head decay): a
+// forward launch that keeps every chunk's map and writes the fp32 state at every chunk
+// start (fstates [B, H, nc, D, D]; a.o, a.hT may be nullptr), then the reverse walk
+// [dS_c; dV_c] = E_c^T [dS_{c+1}; dO_c] writing dv (fp32 [B, T, H, D]), dh0 (or nullptr) and
+// the incoming state gradient of every chunk (bstates, same layout).  a.ws_body: at least
+// chunk_tc_keep_bytes().
+size_t chunk_tc_keep_bytes(int B, int H, int T, int d);
+cudaError_t launch_chunk_tc_walks(const SeqBatch &a, const void *d_o, const float *dhT, float *dh0, float *dv,
+                                  float *fstates, float *bstates, cudaStream_t s);
+// Gradients of q, k, beta and the decay per chunk from the two walks' states (chunk_bwd.cu).
+struct ChunkBwdArgs {
+    const void *q, *k, *v, *d_o;       // bf16 [B, T, H, D]
+    const float *beta, *decay;          // [B, T, H]; decay may be nullptr
+    const float *fstates, *bstates;     // [B, H, nc, D, D]
+    float *dq, *dk, *dbeta, *ddecay;    // outputs (ddecay may be nullptr)
+    int B, T, H, D;
+    float scale;
+    int use_l2, decayed_read;
+    float *scratch;                     // chunk_bwd_scratch_floats(D) per CTA
+    int ctas;
+};
+size_t chunk_bwd_scratch_floats(int D);
+int chunk_bwd_ctas();
+cudaError_t launch_chunk_bwd_grads(const ChunkBwdArgs &a, cudaStream_t s);
 // Device address of kda_chunk_fwd_noalloc's built-in scratch array on the current device
 // (its first bytes are a workspace header).
 cudaError_t noalloc_header(void **out);

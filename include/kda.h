@@ -380,6 +380,30 @@ kda_status kda_gate_decay(const float *gate, const float *A_log, const float *dt
                           float *decay, long rows, int H, int K, kda_stream_t stream);
 
 /*
+ * Chunked backward on the tensor cores: the same gradients as kda_recurrent_bwd (dq, dk,
+ * dv, dbeta, ddecay, dinitial_state of sum(o . d_o) + sum(final_state . dfinal_state)) for
+ * the bf16 tensor-core shapes (dtype KDA_BF16, dk == dv in {64, 128}; anything else returns
+ * KDA_ERR_UNSUPPORTED), computed by chunks of 64 tokens (kda-neuron-kernels README,
+ * kda_chunk_step_exact_bwd; TileOPs DeltaNetChunkBwdOp): a forward launch that keeps every
+ * chunk's map and state, a reverse walk [dS_c; dV_c] = E_c^T [dS_{c+1}; dO_c] over the
+ * maps (the transposed chunk map), and one kernel for the chunk-local gradients of q, k,
+ * beta and the decay.  Arguments, layouts and errors as kda_recurrent_bwd (equal-length
+ * batches, key-major states).  Arithmetic: bf16 maps and state operands on the tensor
+ * cores as in the forward, tf32 products with fp32 accumulation for the chunk gradients.
+ * ws: at least kda_chunk_bwd_workspace() bytes, 16-byte aligned (it holds every chunk's
+ * map and two fp32 states per chunk: about 200 KB per chunk and head at head dim 128).
+ */
+size_t kda_chunk_bwd_workspace(int B, int T, int H, int dk, int dv);
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v,
+                         const float *beta, const float *decay,
+                         const float *initial_state, const void *d_o,
+                         const float *dfinal_state, float *dq, float *dk_out, float *dv_out,
+                         float *dbeta, float *ddecay, float *dinitial_state,
+                         int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                         float scale, int use_qk_l2norm, int decayed_read,
+                         void *ws, size_t ws_bytes, kda_stream_t stream);
+
+/*
  * Read the device error word that the kernels of the most recent kda_chunk_fwd /
  * kda_varlen_fwd call on `ws` recorded (KDA_OK if none), then clear it.  Each of
  * those calls clears the word on its stream before its kernels run.  ws == NULL reads
