@@ -42,12 +42,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr float kNormEpsB = 1e-12f;
 
-// element (r, c) of an fp32 matrix at p[r * rs + c * cs]
-struct Mat {
-    const float *p;
-    int rs, cs;
-    __device__ __forceinline__ float operator()(int r, int c) const { return p[(size_t)r * rs + (size_t)c * cs]; }
-};
 
 __device__ __forceinline__ uint32_t tf32(float x) {
     uint32_t r;
@@ -63,38 +57,109 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// C[M x N] = A[M x K] B[K x N] (M a multiple of 16, N of 8, K of 8), the warps of the CTA
-// taking the 16 x 8 output tiles in turn; epi(r, c, v0, v1) receives C[r][c], C[r][c + 1]
-// (lane = 4 g + t4 holds rows g and g + 8, columns 2 t4 and 2 t4 + 1 of its tile).
-template <typename Epi>
-__device__ __forceinline__ void gemm(int M, int N, int K, Mat A, Mat B, Epi epi) {
+// C[M x N] = A B^T with A [M][K] and B [N][K] row-major (both contiguous along the
+// contraction; M a multiple of 32, N of 16, K of 16), the warps of the CTA taking output
+// tiles of 32 x WN (WN = 32 when the 64-row output has 8 such tiles, else 16) in turn: each
+// A fragment serves WN / 8 MMAs and each B fragment two.  epi(r, c, v0, v1) receives
+// C[r][c], C[r][c + 1] (lane = 4 g + t4 holds rows g + 8 i, columns 2 t4 + 8 j of its tile)
+// and returns a contribution to row r's sum, which is reduced over the lanes of the row and
+// added to rowsum[r] (shared memory) when rowsum is given.  Inside a 16-wide k step lane t4
+// takes the four consecutive k = 4 t4 .. 4 t4 + 3 for both operands (one 16-byte load each),
+// the first two for the first MMA and the last two for the second: the same permutation of
+// k on A and B, which leaves the sum unchanged.
+template <int WN, typename Epi>
+__device__ __forceinline__ void gemm_t(int M, int N, int K, const float *A, int lda, const float *B, int ldb,
+                                       Epi epi, float *rowsum) {
+    constexpr int NJ = WN / 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
-    const int tn = N >> 3, tiles = (M >> 4) * tn;
+    const int tn = N / WN, tiles = (M / 32) * tn;
     for (int tile = warp; tile < tiles; tile += kWarps) {
-        const int m0 = (tile / tn) << 4, n0 = (tile % tn) << 3;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int k0 = 0; k0 < K; k0 += 8) {
-            const uint32_t a[4] = {tf32(A(m0 + g, k0 + t4)), tf32(A(m0 + g + 8, k0 + t4)),
-                                   tf32(A(m0 + g, k0 + t4 + 4)), tf32(A(m0 + g + 8, k0 + t4 + 4))};
-            const uint32_t b[2] = {tf32(B(k0 + t4, n0 + g)), tf32(B(k0 + t4 + 4, n0 + g))};
-            mma_tf32(d, a, b);
+        const int m0 = (tile / tn) * 32, n0 = (tile % tn) * WN;
+        const float *ap[4], *bp[NJ];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ap[i] = A + (size_t)(m0 + g + 8 * i) * lda + 4 * t4;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) bp[j] = B + (size_t)(n0 + 8 * j + g) * ldb + 4 * t4;
+        float d[2][NJ][4] = {};
+#pragma unroll 2
+        for (int k0 = 0; k0 < K; k0 += 16) {
+            float4 x[4], z[NJ];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[i] = *reinterpret_cast<const float4 *>(ap[i] + k0);
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) z[j] = *reinterpret_cast<const float4 *>(bp[j] + k0);
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi) {
+                const uint32_t a[4] = {tf32(x[2 * mi].x), tf32(x[2 * mi + 1].x), tf32(x[2 * mi].y), tf32(x[2 * mi + 1].y)};
+                const uint32_t a2[4] = {tf32(x[2 * mi].z), tf32(x[2 * mi + 1].z), tf32(x[2 * mi].w), tf32(x[2 * mi + 1].w)};
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const uint32_t b[2] = {tf32(z[j].x), tf32(z[j].y)};
+                    const uint32_t b2[2] = {tf32(z[j].z), tf32(z[j].w)};
+                    mma_tf32(d[mi][j], a, b);
+                    mma_tf32(d[mi][j], a2, b2);
+                }
+            }
         }
-        epi(m0 + g, n0 + 2 * t4, d[0], d[1]);
-        epi(m0 + g + 8, n0 + 2 * t4, d[2], d[3]);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int r = m0 + 16 * mi + g + 8 * h2;
+                float part = 0.f;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) part += epi(r, n0 + 8 * j + 2 * t4, d[mi][j][2 * h2], d[mi][j][2 * h2 + 1]);
+                if (rowsum) {
+                    part += __shfl_xor_sync(0xffffffffu, part, 1);
+                    part += __shfl_xor_sync(0xffffffffu, part, 2);
+                    if (t4 == 0) atomicAdd(rowsum + r, part);
+                }
+            }
     }
+}
+// Operands are copied into shared memory before each product (16-byte cp.async copies,
+// many in flight), rows padded to K + 16 floats: the 16-byte fragment loads of a quarter
+// warp (rows g, g + 1, columns 4 t4) then fall on distinct banks.
+__device__ __forceinline__ void stage(float *dst, const float *src, int rows, int K) {
+    const int per_row = K >> 2, pitch = K + 16;
+    for (int x = threadIdx.x; x < rows * per_row; x += kThreads) {
+        const int r = x / per_row, c4 = x - r * per_row;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst + r * pitch + 4 * c4)),
+                     "l"(src + (size_t)r * K + 4 * c4)
+                     : "memory");
+    }
+}
+
+// C = A B^T for A [M][K], B [N][K] in global memory (row-major, contiguous rows): both staged
+// into the CTA's operand buffers sA, sB, then multiplied (see gemm_t).  Starts and ends with
+// a barrier of the CTA, so the products of a chunk run in program order.
+template <typename Epi>
+__device__ __forceinline__ void gemm(float *sA, float *sB, int M, int N, int K, const float *A, const float *B,
+                                     Epi epi, float *rowsum = nullptr) {
+    __syncthreads();   // the previous product has read the buffers; its outputs are in memory
+    stage(sA, A, M, K);
+    if (B != A) stage(sB, B, N, K);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    const float *b = B != A ? sB : sA;
+    if (N >= 128) gemm_t<32>(M, N, K, sA, K + 16, b, K + 16, epi, rowsum);
+    else gemm_t<16>(M, N, K, sA, K + 16, b, K + 16, epi, rowsum);
+    __syncthreads();
 }
 
 // The CTA's scratch, in floats: 64 x D matrices, 64 x 64 matrices, per-token scalars.
 template <int D>
 struct Scr {
-    enum { Kh, Qh, V, dO, Kt, W, U, dU, dW, dKt, DOS, dBv, dBk, dkh, dqh, NBig };
-    enum { KKE, Ekk, L, A, Eqk, T, Pv, Pk, dA, dT, X, dL, dKK, NSmall };
+    // 64 x D (a "t" suffix: the transposed copy, D x 64)
+    enum { Kh, Qh, V, dO, Kt, W, U, dU, dW, dkh, dqh, Kht, Qht, Vt, dOt, dUt, dWt, NBig };
+    enum { KKE, L, A, T, Pv, Pk, dA, dT, X, dL, At, Tt, Xt, NSmall };
+    enum { St, dSpt, NSq };   // D x D: the transposed states
     enum { beta, G, R, eG, eR, eGnG, kn, qn, knorm, qnorm, dG, dGp, dbeta, NScal };
     static constexpr size_t big(int i) { return (size_t)i * kC * D; }
     static constexpr size_t small(int i) { return (size_t)NBig * kC * D + (size_t)i * kC * kC; }
-    static constexpr size_t scal(int i) { return small(NSmall) + (size_t)i * kC; }
+    static constexpr size_t sq(int i) { return small(NSmall) + (size_t)i * D * D; }
+    static constexpr size_t scal(int i) { return sq(NSq) + (size_t)i * kC; }
     static constexpr size_t floats = scal(NScal) + 64;   // + the chunk's G_n terms
 };
 
@@ -105,26 +170,36 @@ namespace {
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) chunk_bwd_kernel(ChunkBwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) {
     using Sc = Scr<D>;
     constexpr int PL = kC + 1;   // padded rows of the inverse's shared arrays
-    __shared__ float sL[kC * PL], sT[kC * PL];
-    __shared__ float red[8 * kC];   // per-token row / column sums
+    // the products' operand buffers: A [64][D + 16], B [D][D + 16]; the inverse's L and T (and
+    // the state transposes' tiles) reuse them between products
+    extern __shared__ float smem_dyn[];
+    float *sA = smem_dyn, *sB = smem_dyn + kC * (D + 16);
+    float *sL = sB, *sT = sB + kC * PL;   // (the buffer is sized to hold both)
+    __shared__ float red[10 * kC];   // per-token row / column sums
     __shared__ float sGn[2];        // G_n, and the chunk's gradient of G_n
     float *sc = a.scratch + (size_t)blockIdx.x * Sc::floats;
     auto big = [&](int i) { return sc + Sc::big(i); };
     auto sml = [&](int i) { return sc + Sc::small(i); };
     auto scl = [&](int i) { return sc + Sc::scal(i); };
     float *Kh = big(Sc::Kh), *Qh = big(Sc::Qh), *V = big(Sc::V), *dO = big(Sc::dO), *Kt = big(Sc::Kt);
-    float *W = big(Sc::W), *U = big(Sc::U), *dU = big(Sc::dU), *dW = big(Sc::dW), *dKt = big(Sc::dKt);
-    float *DOS = big(Sc::DOS), *dBv = big(Sc::dBv), *dBk = big(Sc::dBk), *dkh = big(Sc::dkh), *dqh = big(Sc::dqh);
-    float *KKE = sml(Sc::KKE), *Ekk = sml(Sc::Ekk), *L = sml(Sc::L), *A = sml(Sc::A), *Eqk = sml(Sc::Eqk);
+    float *W = big(Sc::W), *U = big(Sc::U), *dU = big(Sc::dU), *dW = big(Sc::dW);
+    float *dkh = big(Sc::dkh), *dqh = big(Sc::dqh);
+    float *Kht = big(Sc::Kht), *Qht = big(Sc::Qht), *Vt = big(Sc::Vt), *dOt = big(Sc::dOt);
+    float *dUt = big(Sc::dUt), *dWt = big(Sc::dWt);
+    float *KKE = sml(Sc::KKE), *L = sml(Sc::L), *A = sml(Sc::A);
     float *T = sml(Sc::T), *Pv = sml(Sc::Pv), *Pk = sml(Sc::Pk), *dA = sml(Sc::dA), *dT = sml(Sc::dT);
-    float *X = sml(Sc::X), *dL = sml(Sc::dL), *dKK = sml(Sc::dKK);
+    float *X = sml(Sc::X), *dL = sml(Sc::dL), *At = sml(Sc::At), *Tt = sml(Sc::Tt), *Xt = sml(Sc::Xt);
+    // after dL: P = dL beta_t E_kk and dA (.) E_qk with their transposes reuse X, Xt, dT, Pv
+    float *dKK = X, *dKKt = Xt, *dQK = dT, *dQKt = Pv;
+    float *St = sc + Sc::sq(Sc::St), *dSpt = sc + Sc::sq(Sc::dSpt);
     float *beta = scl(Sc::beta), *G = scl(Sc::G), *R = scl(Sc::R), *eG = scl(Sc::eG), *eR = scl(Sc::eR);
     float *eGnG = scl(Sc::eGnG), *kn = scl(Sc::kn), *qn = scl(Sc::qn), *knorm = scl(Sc::knorm);
     float *qnorm = scl(Sc::qnorm), *dG = scl(Sc::dG), *dGp = scl(Sc::dGp), *dbeta = scl(Sc::dbeta);
     float *rA = red, *cA = red + kC, *rL = red + 2 * kC, *cL = red + 3 * kC, *rLK = red + 4 * kC;
+    float *rqd = red + 5 * kC, *rkd = red + 6 * kC, *rbv = red + 7 * kC, *rbk = red + 8 * kC;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nc = (a.T + kC - 1) / kC;
@@ -142,7 +217,8 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_kernel(ChunkBwdArgs a) {
         const float *S = a.fstates + (size_t)ci * D * D;    // state entering the chunk
         const float *dSp = a.bstates + (size_t)ci * D * D;  // gradient of the state leaving it
 
-        // ---- rows: norms, k^, q~, v, dO (zero past the valid tokens), cleared accumulators
+        // ---- rows: norms, k^, q~, v, dO (zero past the valid tokens) and their transposes,
+        // cleared accumulators
         for (int t = warp; t < kC; t += kWarps) {
             const bool valid = t < nv;
             const size_t gi = ((size_t)(row0 + t) * a.H + h) * D;
@@ -166,17 +242,35 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_kernel(ChunkBwdArgs a) {
 #pragma unroll
             for (int m = 0; m < D / 32; ++m) {
                 const int i = lane + 32 * m;
-                Kh[t * D + i] = kk[m] * fk;
-                Qh[t * D + i] = qq[m] * fq;
-                V[t * D + i] = valid ? bf2f(gv[gi + i]) : 0.f;
-                dO[t * D + i] = valid ? bf2f(gdo[gi + i]) : 0.f;
+                const float vv = valid ? bf2f(gv[gi + i]) : 0.f, oo = valid ? bf2f(gdo[gi + i]) : 0.f;
+                Kh[t * D + i] = kk[m] * fk; Kht[i * kC + t] = kk[m] * fk;
+                Qh[t * D + i] = qq[m] * fq; Qht[i * kC + t] = qq[m] * fq;
+                V[t * D + i] = vv; Vt[i * kC + t] = vv;
+                dO[t * D + i] = oo; dOt[i * kC + t] = oo;
                 dkh[t * D + i] = 0.f;
                 dqh[t * D + i] = 0.f;
             }
             if (lane == 0) {
+                rqd[t] = 0.f; rkd[t] = 0.f; rbv[t] = 0.f; rbk[t] = 0.f;
                 kn[t] = fk; qn[t] = fq; knorm[t] = nk; qnorm[t] = nq;
                 beta[t] = valid ? a.beta[(row0 + t) * a.H + h] : 0.f;
             }
+        }
+        // the transposed states, through 32 x 32 tiles in shared memory (the inverse's arrays)
+        for (int tile = 0; tile < (D / 32) * (D / 32); ++tile) {
+            const int r0 = (tile / (D / 32)) * 32, c0 = (tile % (D / 32)) * 32;
+            for (int x = tid; x < 1024; x += kThreads) {
+                const int r = x >> 5, cc = x & 31;
+                sL[r * 33 + cc] = S[(size_t)(r0 + r) * D + c0 + cc];
+                sT[r * 33 + cc] = dSp[(size_t)(r0 + r) * D + c0 + cc];
+            }
+            __syncthreads();
+            for (int x = tid; x < 1024; x += kThreads) {
+                const int r = x >> 5, cc = x & 31;
+                St[(size_t)(c0 + r) * D + r0 + cc] = sL[cc * 33 + r];
+                dSpt[(size_t)(c0 + r) * D + r0 + cc] = sT[cc * 33 + r];
+            }
+            __syncthreads();
         }
         if (warp == 0) {   // in-chunk cumulative log decay: lane owns tokens 2 lane, 2 lane + 1
             auto dec = [&](int t) { return (t < nv && a.decay) ? a.decay[(row0 + t) * a.H + h] : 0.f; };
@@ -201,26 +295,29 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_kernel(ChunkBwdArgs a) {
         __syncthreads();
         for (int x = tid; x < kC * D; x += kThreads) Kt[x] = eGnG[x / D] * Kh[x];
 
-        // ---- Gram products: L = beta_t (k^ k^^T) E_kk (strict), A = (q~ k^^T) E_qk (inclusive)
-        gemm(kC, kC, D, Mat{Kh, D, 1}, Mat{Kh, 1, D}, [&](int t, int s, float v0, float v1) {
-            const float vv[2] = {v0, v1};
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const float e = (s + u < t) ? __expf(R[t] - G[s + u]) : 0.f;
-                KKE[t * kC + s + u] = vv[u] * e;
-                Ekk[t * kC + s + u] = e;
-                L[t * kC + s + u] = beta[t] * vv[u] * e;
-                sL[t * PL + s + u] = beta[t] * vv[u] * e;
-            }
-        });
-        gemm(kC, kC, D, Mat{Qh, D, 1}, Mat{Kh, 1, D}, [&](int t, int s, float v0, float v1) {
+        // ---- Gram products: A = (q~ k^^T) E_qk (inclusive), L = beta_t (k^ k^^T) E_kk (strict);
+        // the second product reads one staged operand, so its epilogue may fill the inverse's L
+        // in the other buffer
+        gemm(sA, sB, kC, kC, D, Qh, Kh, [&](int t, int s, float v0, float v1) -> float {
             const float vv[2] = {v0, v1};
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const float e = (s + u <= t) ? __expf(G[t] - G[s + u]) : 0.f;
                 A[t * kC + s + u] = vv[u] * e;
-                Eqk[t * kC + s + u] = e;
+                At[(s + u) * kC + t] = vv[u] * e;
             }
+            return 0.f;
+        });
+        gemm(sA, sB, kC, kC, D, Kh, Kh, [&](int t, int s, float v0, float v1) -> float {
+            const float vv[2] = {v0, v1};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float e = (s + u < t) ? __expf(R[t] - G[s + u]) : 0.f;
+                KKE[t * kC + s + u] = vv[u] * e;
+                L[t * kC + s + u] = beta[t] * vv[u] * e;
+                sL[t * PL + s + u] = beta[t] * vv[u] * e;
+            }
+            return 0.f;
         });
         __syncthreads();
 
@@ -242,81 +339,99 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_kernel(ChunkBwdArgs a) {
             const int t = x / kC, s = x % kC;
             const float tv = sT[t * PL + s];
             T[x] = tv;
+            Tt[s * kC + t] = tv;
             Pv[x] = tv * beta[s];
             Pk[x] = tv * beta[s] * eR[s];
         }
         __syncthreads();
 
-        // ---- forward quantities: W = T diag(beta e^R) K^, U = T diag(beta) V - W S
-        gemm(kC, D, kC, Mat{Pk, kC, 1}, Mat{Kh, D, 1}, [&](int t, int j, float v0, float v1) {
+        // ---- forward quantities: W = T diag(beta e^R) K^, U = T diag(beta) V - W S;  dU = A^T dO
+        gemm(sA, sB, kC, D, kC, Pk, Kht, [&](int t, int j, float v0, float v1) -> float {
             W[t * D + j] = v0; W[t * D + j + 1] = v1;
+            return 0.f;
         });
-        gemm(kC, D, kC, Mat{Pv, kC, 1}, Mat{V, D, 1}, [&](int t, int j, float v0, float v1) {
+        gemm(sA, sB, kC, D, kC, Pv, Vt, [&](int t, int j, float v0, float v1) -> float {
             U[t * D + j] = v0; U[t * D + j + 1] = v1;
+            return 0.f;
         });
-        // dU = A^T dO (same output tiles as U: the dU writes do not race the U writes)
-        gemm(kC, D, kC, Mat{A, 1, kC}, Mat{dO, D, 1}, [&](int s, int j, float v0, float v1) {
+        gemm(sA, sB, kC, D, kC, At, dOt, [&](int s, int j, float v0, float v1) -> float {
             dU[s * D + j] = v0; dU[s * D + j + 1] = v1;
+            return 0.f;
         });
         __syncthreads();
-        gemm(kC, D, D, Mat{W, D, 1}, Mat{S, D, 1}, [&](int t, int j, float v0, float v1) {
+        // U -= W S;  dU += K~ dS' (and its transpose);  DOS = dO S^T  (each output element stays
+        // with one thread across the products that write it)
+        gemm(sA, sB, kC, D, D, W, St, [&](int t, int j, float v0, float v1) -> float {
             U[t * D + j] -= v0; U[t * D + j + 1] -= v1;
+            return 0.f;
         });
-        // dU += K~ dS';  DOS = dO S^T
-        gemm(kC, D, D, Mat{Kt, D, 1}, Mat{dSp, D, 1}, [&](int s, int j, float v0, float v1) {
-            dU[s * D + j] += v0; dU[s * D + j + 1] += v1;
+        gemm(sA, sB, kC, D, D, Kt, dSpt, [&](int s, int j, float v0, float v1) -> float {
+            const float u0 = dU[s * D + j] + v0, u1 = dU[s * D + j + 1] + v1;
+            dU[s * D + j] = u0; dU[s * D + j + 1] = u1;
+            dUt[j * kC + s] = u0; dUt[(j + 1) * kC + s] = u1;
+            return 0.f;
         });
-        gemm(kC, D, D, Mat{dO, D, 1}, Mat{S, 1, D}, [&](int t, int i, float v0, float v1) {
-            DOS[t * D + i] = v0; DOS[t * D + i + 1] = v1;
-        });
+        gemm(sA, sB, kC, D, D, dO, S, [&](int t, int i, float v0, float v1) -> float {   // dO S^T
+            dqh[t * D + i] += eG[t] * v0; dqh[t * D + i + 1] += eG[t] * v1;
+            return v0 * Qh[t * D + i] + v1 * Qh[t * D + i + 1];
+        }, rqd);
         __syncthreads();
 
         // ---- dA = mask_incl(dO U^T),  dK~ = U dS'^T,  dW = -dU S^T
-        gemm(kC, kC, D, Mat{dO, D, 1}, Mat{U, 1, D}, [&](int t, int s, float v0, float v1) {
+        gemm(sA, sB, kC, kC, D, dO, U, [&](int t, int s, float v0, float v1) -> float {
             dA[t * kC + s] = s <= t ? v0 : 0.f;
             dA[t * kC + s + 1] = s + 1 <= t ? v1 : 0.f;
+            return 0.f;
         });
-        gemm(kC, D, D, Mat{U, D, 1}, Mat{dSp, 1, D}, [&](int s, int i, float v0, float v1) {
-            dKt[s * D + i] = v0; dKt[s * D + i + 1] = v1;
-        });
-        gemm(kC, D, D, Mat{dU, D, 1}, Mat{S, 1, D}, [&](int s, int i, float v0, float v1) {
+        gemm(sA, sB, kC, D, D, U, dSp, [&](int s, int i, float v0, float v1) -> float {   // dK~
+            dkh[s * D + i] += eGnG[s] * v0; dkh[s * D + i + 1] += eGnG[s] * v1;
+            return v0 * Kt[s * D + i] + v1 * Kt[s * D + i + 1];
+        }, rkd);
+        gemm(sA, sB, kC, D, D, dU, S, [&](int s, int i, float v0, float v1) -> float {
             dW[s * D + i] = -v0; dW[s * D + i + 1] = -v1;
+            dWt[i * kC + s] = -v0; dWt[(i + 1) * kC + s] = -v1;
+            return 0.f;
         });
         __syncthreads();
 
         // ---- dT = dU (diag(beta) V)^T + dW (diag(beta e^R) K^)^T;  dBv = T^T dU;  dBk = T^T dW,
         // dK^ += diag(beta e^R) dBk
-        gemm(kC, kC, D, Mat{dU, D, 1}, Mat{V, 1, D}, [&](int t, int s, float v0, float v1) {
+        gemm(sA, sB, kC, kC, D, dU, V, [&](int t, int s, float v0, float v1) -> float {
             dT[t * kC + s] = v0 * beta[s];
             dT[t * kC + s + 1] = v1 * beta[s + 1];
+            return 0.f;
         });
-        gemm(kC, D, kC, Mat{T, 1, kC}, Mat{dU, D, 1}, [&](int s, int j, float v0, float v1) {
-            dBv[s * D + j] = v0; dBv[s * D + j + 1] = v1;
-        });
-        gemm(kC, kC, D, Mat{dW, D, 1}, Mat{Kh, 1, D}, [&](int t, int s, float v0, float v1) {
+        gemm(sA, sB, kC, D, kC, Tt, dUt, [&](int s, int j, float v0, float v1) -> float {   // dBv
+            return v0 * V[s * D + j] + v1 * V[s * D + j + 1];
+        }, rbv);
+        gemm(sA, sB, kC, kC, D, dW, Kh, [&](int t, int s, float v0, float v1) -> float {
             dT[t * kC + s] += v0 * beta[s] * eR[s];
             dT[t * kC + s + 1] += v1 * beta[s + 1] * eR[s + 1];
+            return 0.f;
         });
-        gemm(kC, D, kC, Mat{T, 1, kC}, Mat{dW, D, 1}, [&](int s, int i, float v0, float v1) {
-            dBk[s * D + i] = v0; dBk[s * D + i + 1] = v1;
+        gemm(sA, sB, kC, D, kC, Tt, dWt, [&](int s, int i, float v0, float v1) -> float {   // dBk
             const float w = beta[s] * eR[s];
             dkh[s * D + i] += w * v0; dkh[s * D + i + 1] += w * v1;
-        });
+            return v0 * Kh[s * D + i] + v1 * Kh[s * D + i + 1];
+        }, rbk);
         __syncthreads();
 
         // ---- dL = -mask_strict(T^T dT T^T)
-        gemm(kC, kC, kC, Mat{dT, kC, 1}, Mat{T, 1, kC}, [&](int t, int s, float v0, float v1) {
+        gemm(sA, sB, kC, kC, kC, dT, T, [&](int t, int s, float v0, float v1) -> float {
             X[t * kC + s] = v0; X[t * kC + s + 1] = v1;
+            Xt[s * kC + t] = v0; Xt[(s + 1) * kC + t] = v1;
+            return 0.f;
         });
         __syncthreads();
-        gemm(kC, kC, kC, Mat{T, 1, kC}, Mat{X, kC, 1}, [&](int t, int s, float v0, float v1) {
+        gemm(sA, sB, kC, kC, kC, Tt, Xt, [&](int t, int s, float v0, float v1) -> float {
             dL[t * kC + s] = s < t ? -v0 : 0.f;
             dL[t * kC + s + 1] = s + 1 < t ? -v1 : 0.f;
+            return 0.f;
         });
         __syncthreads();
 
-        // ---- row and column sums of dA (.) A and dL (.) L, dL (.) KKE; P = dL beta_t E_kk,
-        // dA (.) E_qk (into X)
+        // ---- row and column sums of dA (.) A and dL (.) L, dL (.) KKE; P = dL beta_t E_kk and
+        // dA (.) E_qk, with their transposes
         if (tid < kC) {
             const int t = tid;
             float sa = 0.f, sl = 0.f, slk = 0.f;
@@ -336,58 +451,44 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_kernel(ChunkBwdArgs a) {
             cA[s] = sa; cL[s] = sl;
         }
         for (int x = tid; x < kC * kC; x += kThreads) {
-            const int t = x / kC;
-            dKK[x] = dL[x] * beta[t] * Ekk[x];
-            X[x] = dA[x] * Eqk[x];
+            const int t = x / kC, s = x % kC;
+            const float ekk = s < t ? __expf(R[t] - G[s]) : 0.f, eqk = s <= t ? __expf(G[t] - G[s]) : 0.f;
+            const float p = dL[x] * beta[t] * ekk, qk = dA[x] * eqk;
+            dKK[x] = p; dKKt[s * kC + t] = p;
+            dQK[x] = qk; dQKt[s * kC + t] = qk;
         }
         __syncthreads();
-        // dK^ += P K^ + P^T K^ + (dA E_qk)^T Q~;  dQ~ += (dA E_qk) K^  (each element of dkh and
-        // dqh stays with one thread across these products)
-        gemm(kC, D, kC, Mat{dKK, kC, 1}, Mat{Kh, D, 1}, [&](int t, int i, float v0, float v1) {
+        // dK^ += P K^ + P^T K^ + (dA E_qk)^T Q~;  dQ~ += (dA E_qk) K^
+        gemm(sA, sB, kC, D, kC, dKK, Kht, [&](int t, int i, float v0, float v1) -> float {
             dkh[t * D + i] += v0; dkh[t * D + i + 1] += v1;
+            return 0.f;
         });
-        gemm(kC, D, kC, Mat{dKK, 1, kC}, Mat{Kh, D, 1}, [&](int s, int i, float v0, float v1) {
+        gemm(sA, sB, kC, D, kC, dKKt, Kht, [&](int s, int i, float v0, float v1) -> float {
             dkh[s * D + i] += v0; dkh[s * D + i + 1] += v1;
+            return 0.f;
         });
-        gemm(kC, D, kC, Mat{X, 1, kC}, Mat{Qh, D, 1}, [&](int s, int i, float v0, float v1) {
+        gemm(sA, sB, kC, D, kC, dQKt, Qht, [&](int s, int i, float v0, float v1) -> float {
             dkh[s * D + i] += v0; dkh[s * D + i + 1] += v1;
+            return 0.f;
         });
-        gemm(kC, D, kC, Mat{X, kC, 1}, Mat{Kh, D, 1}, [&](int t, int i, float v0, float v1) {
+        gemm(sA, sB, kC, D, kC, dQK, Kht, [&](int t, int i, float v0, float v1) -> float {
             dqh[t * D + i] += v0; dqh[t * D + i + 1] += v1;
+            return 0.f;
         });
         __syncthreads();
 
-        // ---- per token: dG, dR, dbeta; dK^ += e^{G_n - G} dK~;  dQ~ += e^G dO S^T
-        for (int t = warp; t < kC; t += kWarps) {
-            float qd = 0.f, kd = 0.f, bv = 0.f, bk = 0.f;
-            const float et = eG[t], en = eGnG[t];
-#pragma unroll
-            for (int m = 0; m < D / 32; ++m) {
-                const int x = t * D + lane + 32 * m;
-                qd = fmaf(Qh[x], DOS[x], qd);
-                kd = fmaf(dKt[x], Kt[x], kd);
-                bv = fmaf(dBv[x], V[x], bv);
-                bk = fmaf(dBk[x], Kh[x], bk);
-                dkh[x] += en * dKt[x];
-                dqh[x] += et * DOS[x];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                qd += __shfl_xor_sync(0xffffffffu, qd, o);
-                kd += __shfl_xor_sync(0xffffffffu, kd, o);
-                bv += __shfl_xor_sync(0xffffffffu, bv, o);
-                bk += __shfl_xor_sync(0xffffffffu, bk, o);
-            }
-            if (lane == 0) {
-                const float dr = rL[t] + beta[t] * eR[t] * bk;
-                float dg = et * qd + rA[t] - cA[t] - cL[t] - kd;
-                float dgp = 0.f;
-                if (a.decayed_read) dg += dr; else dgp = dr;
-                dG[t] = dg;
-                dGp[t] = dgp;
-                dbeta[t] = bv + eR[t] * bk + rLK[t];
-                atomicAdd(&sGn[1], kd);
-            }
+        // ---- per token: dG, dR, dbeta (the dots of q~ . dO S^T, dK~ . K~, dBv . v, dBk . k^ came
+        // from the products' epilogues)
+        if (tid < kC) {
+            const int t = tid;
+            const float dr = rL[t] + beta[t] * eR[t] * rbk[t];
+            float dg = eG[t] * rqd[t] + rA[t] - cA[t] - cL[t] - rkd[t];
+            float dgp = 0.f;
+            if (a.decayed_read) dg += dr; else dgp = dr;
+            dG[t] = dg;
+            dGp[t] = dgp;
+            dbeta[t] = rbv[t] + eR[t] * rbk[t] + rLK[t];
+            atomicAdd(&sGn[1], rkd[t]);
         }
         {   // e^{G_n} sum(S (.) dS')
             float acc = 0.f;
@@ -457,13 +558,21 @@ size_t chunk_bwd_scratch_floats(int D) {
 
 // Persistent CTAs of the gradient kernel: a fixed number, so that the workspace query needs
 // no device (each CTA has its own scratch region).
-int chunk_bwd_ctas() { return 160; }
+int chunk_bwd_ctas() { return 304; }
+
+template <int D>
+cudaError_t launch_grads(const ChunkBwdArgs &a, cudaStream_t st) {
+    const int smem = (int)sizeof(float) * max((kC + D) * (D + 16), kC * (D + 16) + 2 * kC * (kC + 1));
+    cudaError_t e = cudaFuncSetAttribute(chunk_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    chunk_bwd_kernel<D><<<a.ctas, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_chunk_bwd_grads(const ChunkBwdArgs &a, cudaStream_t st) {
-    if (a.D == 128) chunk_bwd_kernel<128><<<a.ctas, kThreads, 0, st>>>(a);
-    else if (a.D == 64) chunk_bwd_kernel<64><<<a.ctas, kThreads, 0, st>>>(a);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    if (a.D == 128) return launch_grads<128>(a, st);
+    if (a.D == 64) return launch_grads<64>(a, st);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace kda
