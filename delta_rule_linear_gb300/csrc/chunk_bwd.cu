@@ -25,13 +25,18 @@
 // dx = (dx^ - x^ (x^ . dx^)) / |x|.  The value gradient and the state gradients come from
 // the reverse walk (chunk_tc.cu).
 //
-// One CTA per chunk at a time (persistent CTAs over the chunks).  Every intermediate is an
-// fp32 matrix in the CTA's own scratch region of global memory, where it stays in L2 and
-// L1; the states of the two walks are read in place.  The products are warp-level tensor
-// MMAs (m16n8k8, tf32 operands, fp32 accumulation) over 16 x 8 output tiles, the warps
-// taking tiles in turn; every operand is addressed through (row stride, column stride), so
-// transposed operands cost nothing.  Padded rows past a sequence's end act as k = q = v =
-// dO = 0, beta = 0, decay = 0 and are never stored.
+// One CTA per chunk at a time (persistent CTAs over the chunks, two per SM).  The chunk's
+// fp32 intermediates live in the CTA's own scratch region of global memory (L2); the states
+// of the two walks are read in place; the per-token scalars and the row / column sums live in
+// shared memory.  A product is one or more passes over (A, B) operand pairs into register
+// accumulators: each pass stages both operands into shared memory with cp.async (one round
+// trip for the whole operand), as they lie in memory -- contraction index along rows or along
+// columns, the fragment loads read either form, so no transposed copy is ever written -- and
+// runs warp-level tensor MMAs (m16n8k8, tf32 operands, fp32 accumulation) over one 32 x 32 or
+// 32 x 16 output tile per warp.  The epilogue first issues every read it needs from memory,
+// then stores; the dot products the gradients of beta and the decay take over a product's
+// output are its row and column sums, reduced in the epilogue.  Padded rows past a
+// sequence's end act as k = q = v = dO = 0, beta = 0, decay = 0 and are never stored.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -41,7 +46,6 @@ constexpr int kC = 64;
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr float kNormEpsB = 1e-12f;
-
 
 __device__ __forceinline__ uint32_t tf32(float x) {
     uint32_t r;
@@ -57,149 +61,267 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// C[M x N] = A B^T with A [M][K] and B [N][K] row-major (both contiguous along the
-// contraction; M a multiple of 32, N of 16, K of 16), the warps of the CTA taking output
-// tiles of 32 x WN (WN = 32 when the 64-row output has 8 such tiles, else 16) in turn: each
-// A fragment serves WN / 8 MMAs and each B fragment two.  epi(r, c, v0, v1) receives
-// C[r][c], C[r][c + 1] (lane = 4 g + t4 holds rows g + 8 i, columns 2 t4 + 8 j of its tile)
-// and returns a contribution to row r's sum, which is reduced over the lanes of the row and
-// added to rowsum[r] (shared memory) when rowsum is given.  Inside a 16-wide k step lane t4
-// takes the four consecutive k = 4 t4 .. 4 t4 + 3 for both operands (one 16-byte load each),
-// the first two for the first MMA and the last two for the second: the same permutation of
-// k on A and B, which leaves the sum unchanged.
-template <int WN, typename Epi>
-__device__ __forceinline__ void gemm_t(int M, int N, int K, const float *A, int lda, const float *B, int ldb,
-                                       Epi epi, float *rowsum) {
-    constexpr int NJ = WN / 8;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int tn = N / WN, tiles = (M / 32) * tn;
-    for (int tile = warp; tile < tiles; tile += kWarps) {
-        const int m0 = (tile / tn) * 32, n0 = (tile % tn) * WN;
-        const float *ap[4], *bp[NJ];
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// 16-byte copy that reads src_bytes (0 or 16) and zero-fills the rest
+__device__ __forceinline__ void cp_async16z(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
+__device__ __forceinline__ void st2(float *p, float x, float y) { *reinterpret_cast<float2 *>(p) = make_float2(x, y); }
+__device__ __forceinline__ float2 ld2(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+
+// Operand layouts in shared memory, for an operand with w rows on its side of the product
+// (M for A, N for B) and contraction length K.  kRow: element (m, k) at m (K + 16) + k, k
+// contiguous -- a quarter warp's 16-byte loads at rows g, g + 1 and columns 4 t4 fall on
+// distinct banks since K + 16 = 16 mod 32.  kCol: element (m, k) at k (w + 2) + m, m contiguous
+// -- the warp's 4-byte loads at rows 4 t4 + j and columns g fall on distinct banks since
+// 4 (w + 2) = 8 mod 32; its rows keep 8-byte alignment only, so it is staged with 8-byte copies.
+enum Lay { kRow = 0, kCol = 1 };
+template <Lay L>
+__host__ __device__ constexpr int lay_pitch(int w, int K) { return L == kRow ? K + 16 : w + 2; }
+template <Lay L>
+__host__ __device__ constexpr int lay_floats(int w, int K) { return L == kRow ? w * (K + 16) : K * (w + 2); }
+
+// Copies an operand from global memory, where it lies as [w][K] (kRow) or [K][w] (kCol) with
+// row stride ld floats, into dst in the layout above.
+template <Lay L, int w, int K>
+__device__ __forceinline__ void stage(float *dst, const float *src, int ld) {
+    if constexpr (L == kRow) {
+        constexpr int per = K / 4, p = K + 16;
+        for (int x = threadIdx.x; x < w * per; x += kThreads) {
+            const int r = x / per, c = x % per;
+            cp_async16(dst + r * p + 4 * c, src + (size_t)r * ld + 4 * c);
+        }
+    } else {
+        constexpr int per = w / 2, p = w + 2;
+        for (int x = threadIdx.x; x < K * per; x += kThreads) {
+            const int r = x / per, c = x % per;
+            cp_async8(dst + r * p + 2 * c, src + (size_t)r * ld + 2 * c);
+        }
+    }
+}
+
+// The four elements (m, k .. k + 3) of a staged operand.
+template <Lay L, int P>
+__device__ __forceinline__ void frag4(float (&v)[4], const float *s, int m, int k) {
+    if constexpr (L == kRow) {
+        const float4 x = *reinterpret_cast<const float4 *>(s + m * P + k);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) ap[i] = A + (size_t)(m0 + g + 8 * i) * lda + 4 * t4;
+        for (int j = 0; j < 4; ++j) v[j] = s[(k + j) * P + m];
+    }
+}
+
+// A 64 x N product's accumulators: warp w owns the output tile of rows 32 (w / 4) ..,
+// columns WN (w % 4) .. (WN = 32 for N = 128, 16 for N = 64; eight warps, eight tiles).
+// Lane 4 g + t4 holds rows g + 8 i, columns 2 t4 + 8 j (+ 1) of the tile.
+template <int N>
+struct Acc {
+    static constexpr int WN = N / 4, NJ = WN / 8;
+    float d[2][NJ][4];
+    __device__ __forceinline__ void zero() {
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) bp[j] = B + (size_t)(n0 + 8 * j + g) * ldb + 4 * t4;
-        float d[2][NJ][4] = {};
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[i][j][e] = 0.f;
+    }
+};
+
+// One pass: acc += A B^T over a contraction of length K, A(m, k) for m < 64 and B(n, k) for
+// n < N given in global memory in layouts LA, LB (row strides lda, ldb).  A null pointer
+// reuses what the previous pass staged in that buffer (same layout and sizes); B == A stages
+// the operand once and reads it on both sides.  Begins with a barrier of the CTA, so the
+// stores of the previous epilogue are visible and the previous pass has finished reading the
+// buffers.  Inside a 16-wide k step lane t4 takes the four consecutive k = 4 t4 .. 4 t4 + 3 on
+// both operands, the first two for one MMA and the last two for the other: the same
+// permutation of k on A and B, which leaves the sum unchanged.
+template <Lay LA, Lay LB, int N, int K>
+__device__ __forceinline__ void pass(Acc<N> &acc, float *sA, float *sB, const float *A, int lda, const float *B,
+                                     int ldb) {
+    constexpr int PA = lay_pitch<LA>(kC, K), PB = lay_pitch<LB>(N, K), NJ = Acc<N>::NJ;
+    const bool same = (A != nullptr && B == A);
+    __syncthreads();
+    if (A) stage<LA, kC, K>(sA, A, lda);
+    if (B && !same) stage<LB, N, K>(sB, B, ldb);
+    cp_async_wait_all();
+    __syncthreads();
+    const float *bb = same ? sA : sB;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+    const int m0 = (warp >> 2) * 32, n0 = (warp & 3) * Acc<N>::WN;
 #pragma unroll 2
-        for (int k0 = 0; k0 < K; k0 += 16) {
-            float4 x[4], z[NJ];
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        float xa[4][4], zb[NJ][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] = *reinterpret_cast<const float4 *>(ap[i] + k0);
+        for (int i = 0; i < 4; ++i) frag4<LA, PA>(xa[i], sA, m0 + g + 8 * i, k0 + 4 * t4);
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) z[j] = *reinterpret_cast<const float4 *>(bp[j] + k0);
+        for (int j = 0; j < NJ; ++j) frag4<LB, PB>(zb[j], bb, n0 + 8 * j + g, k0 + 4 * t4);
 #pragma unroll
-            for (int mi = 0; mi < 2; ++mi) {
-                const uint32_t a[4] = {tf32(x[2 * mi].x), tf32(x[2 * mi + 1].x), tf32(x[2 * mi].y), tf32(x[2 * mi + 1].y)};
-                const uint32_t a2[4] = {tf32(x[2 * mi].z), tf32(x[2 * mi + 1].z), tf32(x[2 * mi].w), tf32(x[2 * mi + 1].w)};
+        for (int mi = 0; mi < 2; ++mi) {
+            const uint32_t a[4] = {tf32(xa[2 * mi][0]), tf32(xa[2 * mi + 1][0]), tf32(xa[2 * mi][1]), tf32(xa[2 * mi + 1][1])};
+            const uint32_t a2[4] = {tf32(xa[2 * mi][2]), tf32(xa[2 * mi + 1][2]), tf32(xa[2 * mi][3]), tf32(xa[2 * mi + 1][3])};
 #pragma unroll
-                for (int j = 0; j < NJ; ++j) {
-                    const uint32_t b[2] = {tf32(z[j].x), tf32(z[j].y)};
-                    const uint32_t b2[2] = {tf32(z[j].z), tf32(z[j].w)};
-                    mma_tf32(d[mi][j], a, b);
-                    mma_tf32(d[mi][j], a2, b2);
-                }
+            for (int j = 0; j < NJ; ++j) {
+                const uint32_t b[2] = {tf32(zb[j][0]), tf32(zb[j][1])};
+                const uint32_t b2[2] = {tf32(zb[j][2]), tf32(zb[j][3])};
+                mma_tf32(acc.d[mi][j], a, b);
+                mma_tf32(acc.d[mi][j], a2, b2);
             }
         }
+    }
+}
+
+// The epilogue over a product's accumulators (one or two products of the same shape, e.g. two
+// terms that the output weighs by different per-column factors).  For each half of the warp's
+// tile it first calls pre(r, c) for every element pair (r, c), (r, c + 1) it holds -- the reads
+// from memory the epilogue needs, all issued before any store -- then
+// epi(r, c, x0, x1, y0, y1, aux, cs) with the accumulated values (x from acc, y from acc2 or
+// 0), which stores the outputs, returns a contribution to row r's sum and adds the columns'
+// contributions to cs[0], cs[1] (and a second pair of column sums to cs[2], cs[3]).  Row sums
+// are reduced over the four lanes of a row and added to rowsum[r]; column sums over the warp's
+// rows and added to colsum[c], colsum2[c] (shared memory, each when given).  Ends with a
+// barrier of the CTA.
+template <int N, typename Pre, typename Epi>
+__device__ __forceinline__ void finish2(const Acc<N> &acc, const Acc<N> *acc2, Pre pre, Epi epi, float *rowsum,
+                                        float *colsum, float *colsum2) {
+    constexpr int NJ = Acc<N>::NJ;
+    using Aux = decltype(pre(0, 0));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+    const int m0 = (warp >> 2) * 32, n0 = (warp & 3) * Acc<N>::WN;
+    float cs[NJ][4] = {};
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
+    for (int mi = 0; mi < 2; ++mi) {
+        Aux aux[2][NJ];
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int r = m0 + 16 * mi + g + 8 * h2;
-                float part = 0.f;
+        for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-                for (int j = 0; j < NJ; ++j) part += epi(r, n0 + 8 * j + 2 * t4, d[mi][j][2 * h2], d[mi][j][2 * h2 + 1]);
-                if (rowsum) {
-                    part += __shfl_xor_sync(0xffffffffu, part, 1);
-                    part += __shfl_xor_sync(0xffffffffu, part, 2);
-                    if (t4 == 0) atomicAdd(rowsum + r, part);
-                }
+            for (int j = 0; j < NJ; ++j) aux[h2][j] = pre(m0 + 16 * mi + g + 8 * h2, n0 + 8 * j + 2 * t4);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int r = m0 + 16 * mi + g + 8 * h2;
+            float part = 0.f;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const float y0 = acc2 ? acc2->d[mi][j][2 * h2] : 0.f, y1 = acc2 ? acc2->d[mi][j][2 * h2 + 1] : 0.f;
+                part += epi(r, n0 + 8 * j + 2 * t4, acc.d[mi][j][2 * h2], acc.d[mi][j][2 * h2 + 1], y0, y1, aux[h2][j],
+                            cs[j]);
+            }
+            if (rowsum) {
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                if (t4 == 0) atomicAdd(rowsum + r, part);
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        float *dst = q == 0 ? colsum : colsum2;
+        if (!dst) continue;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float v = cs[j][2 * q + e];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                if (g == 0) atomicAdd(dst + n0 + 8 * j + 2 * t4 + e, v);
             }
     }
-}
-// Operands are copied into shared memory before each product (16-byte cp.async copies,
-// many in flight), rows padded to K + 16 floats: the 16-byte fragment loads of a quarter
-// warp (rows g, g + 1, columns 4 t4) then fall on distinct banks.
-__device__ __forceinline__ void stage(float *dst, const float *src, int rows, int K) {
-    const int per_row = K >> 2, pitch = K + 16;
-    for (int x = threadIdx.x; x < rows * per_row; x += kThreads) {
-        const int r = x / per_row, c4 = x - r * per_row;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst + r * pitch + 4 * c4)),
-                     "l"(src + (size_t)r * K + 4 * c4)
-                     : "memory");
-    }
-}
-
-// C = A B^T for A [M][K], B [N][K] in global memory (row-major, contiguous rows): both staged
-// into the CTA's operand buffers sA, sB, then multiplied (see gemm_t).  Starts and ends with
-// a barrier of the CTA, so the products of a chunk run in program order.
-template <typename Epi>
-__device__ __forceinline__ void gemm(float *sA, float *sB, int M, int N, int K, const float *A, const float *B,
-                                     Epi epi, float *rowsum = nullptr) {
-    __syncthreads();   // the previous product has read the buffers; its outputs are in memory
-    stage(sA, A, M, K);
-    if (B != A) stage(sB, B, N, K);
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    const float *b = B != A ? sB : sA;
-    if (N >= 128) gemm_t<32>(M, N, K, sA, K + 16, b, K + 16, epi, rowsum);
-    else gemm_t<16>(M, N, K, sA, K + 16, b, K + 16, epi, rowsum);
     __syncthreads();
 }
 
-// The CTA's scratch, in floats: 64 x D matrices, 64 x 64 matrices, per-token scalars.
+template <int N, typename Pre, typename Epi>
+__device__ __forceinline__ void finish(const Acc<N> &acc, Pre pre, Epi epi, float *rowsum = nullptr,
+                                       float *colsum = nullptr) {
+    finish2<N>(acc, nullptr, pre, epi, rowsum, colsum, nullptr);
+}
+
+// The CTA's scratch, in floats: 64 x D and 64 x 64 matrices (row-major).
 template <int D>
 struct Scr {
-    // 64 x D (a "t" suffix: the transposed copy, D x 64)
-    enum { Kh, Qh, V, dO, Kt, W, U, dU, dW, dkh, dqh, Kht, Qht, Vt, dOt, dUt, dWt, NBig };
-    enum { KKE, L, A, T, Pv, Pk, dA, dT, X, dL, At, Tt, Xt, NSmall };
-    enum { St, dSpt, NSq };   // D x D: the transposed states
-    enum { beta, G, R, eG, eR, eGnG, kn, qn, knorm, qnorm, dG, dGp, dbeta, NScal };
+    enum { Kh, Qh, V, dO, Kt, Wn, U, dU, dW, dkh, dqh, NBig };
+    enum { KKE, A, T, Pv, Pk, dT, X, P, dQK, NSmall };
     static constexpr size_t big(int i) { return (size_t)i * kC * D; }
     static constexpr size_t small(int i) { return (size_t)NBig * kC * D + (size_t)i * kC * kC; }
-    static constexpr size_t sq(int i) { return small(NSmall) + (size_t)i * D * D; }
-    static constexpr size_t scal(int i) { return sq(NSq) + (size_t)i * kC; }
-    static constexpr size_t floats = scal(NScal) + 64;   // + the chunk's G_n terms
+    static constexpr size_t floats = small(NSmall);
+};
+
+// Shared memory of the kernel (dynamic part, floats): the two operand buffers, large enough
+// for either layout of every operand the products stage; between products the inverse's two
+// padded 64 x 64 arrays and the chunk's bf16 input rows reuse them.
+template <int D>
+struct Smem {
+    static constexpr int a_floats = lay_floats<kRow>(kC, D) > lay_floats<kCol>(kC, D) ? lay_floats<kRow>(kC, D)
+                                                                                        : lay_floats<kCol>(kC, D);
+    static constexpr int b_floats = lay_floats<kRow>(D, D) > lay_floats<kCol>(D, D) ? lay_floats<kRow>(D, D)
+                                                                                      : lay_floats<kCol>(D, D);
+    static constexpr int inv_floats = 2 * kC * (kC + 1);
+    static constexpr int floats = a_floats + (b_floats > inv_floats ? b_floats : inv_floats);
+    static_assert(4 * kC * D / 2 <= floats, "bf16 input rows fit the operand buffers");
 };
 
 }  // namespace
 
 namespace {
 
-__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+// E consecutive bf16 values (E = 2 or 4) from shared memory, widened exactly.
+template <int E>
+__device__ __forceinline__ void ld_bf16(float (&f)[E], const __nv_bfloat16 *p) {
+    auto lo = [](uint32_t u) { return __uint_as_float(u << 16); };
+    auto hi = [](uint32_t u) { return __uint_as_float(u & 0xffff0000u); };
+    if constexpr (E == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        f[0] = lo(u.x); f[1] = hi(u.x); f[2] = lo(u.y); f[3] = hi(u.y);
+    } else {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        f[0] = lo(u); f[1] = hi(u);
+    }
+}
+template <int E>
+__device__ __forceinline__ void st_row(float *p, const float (&f)[E], float scale) {
+    if constexpr (E == 4) *reinterpret_cast<float4 *>(p) = make_float4(scale * f[0], scale * f[1], scale * f[2], scale * f[3]);
+    else *reinterpret_cast<float2 *>(p) = make_float2(scale * f[0], scale * f[1]);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) {
     using Sc = Scr<D>;
     constexpr int PL = kC + 1;   // padded rows of the inverse's shared arrays
-    // the products' operand buffers: A [64][D + 16], B [D][D + 16]; the inverse's L and T (and
-    // the state transposes' tiles) reuse them between products
-    extern __shared__ float smem_dyn[];
-    float *sA = smem_dyn, *sB = smem_dyn + kC * (D + 16);
-    float *sL = sB, *sT = sB + kC * PL;   // (the buffer is sized to hold both)
-    __shared__ float red[10 * kC];   // per-token row / column sums
-    __shared__ float sGn[2];        // G_n, and the chunk's gradient of G_n
+    extern __shared__ __align__(16) float smem_dyn[];
+    float *sA = smem_dyn, *sB = smem_dyn + Smem<D>::a_floats;
+    float *sL = sB, *sT = sB + kC * PL;
+    __nv_bfloat16 *sIn = reinterpret_cast<__nv_bfloat16 *>(smem_dyn);   // q, k, v, dO rows: [4][64][D]
+    // per-token scalars, then the products' row and column sums, then G_n and its gradient
+    __shared__ float sv[18 * kC + 2];
+    float *beta = sv, *G = sv + kC, *R = sv + 2 * kC, *eG = sv + 3 * kC, *eR = sv + 4 * kC;
+    float *eGnG = sv + 5 * kC, *kn = sv + 6 * kC, *qn = sv + 7 * kC;
+    float *rA = sv + 8 * kC, *cA = sv + 9 * kC, *cL = sv + 10 * kC, *rLK = sv + 11 * kC, *rqd = sv + 12 * kC;
+    float *rkd = sv + 13 * kC, *rbv = sv + 14 * kC, *rbk = sv + 15 * kC, *kdot = sv + 16 * kC, *qdot = sv + 17 * kC;
+    float *sGn = sv + 18 * kC;
+    // once the per-token gradients are formed they replace the sums they came from
+    float *dG = rA, *dGp = cA, *dbeta = cL;
+
     float *sc = a.scratch + (size_t)blockIdx.x * Sc::floats;
     auto big = [&](int i) { return sc + Sc::big(i); };
     auto sml = [&](int i) { return sc + Sc::small(i); };
-    auto scl = [&](int i) { return sc + Sc::scal(i); };
     float *Kh = big(Sc::Kh), *Qh = big(Sc::Qh), *V = big(Sc::V), *dO = big(Sc::dO), *Kt = big(Sc::Kt);
-    float *W = big(Sc::W), *U = big(Sc::U), *dU = big(Sc::dU), *dW = big(Sc::dW);
+    float *Wn = big(Sc::Wn), *U = big(Sc::U), *dU = big(Sc::dU), *dW = big(Sc::dW);
     float *dkh = big(Sc::dkh), *dqh = big(Sc::dqh);
-    float *Kht = big(Sc::Kht), *Qht = big(Sc::Qht), *Vt = big(Sc::Vt), *dOt = big(Sc::dOt);
-    float *dUt = big(Sc::dUt), *dWt = big(Sc::dWt);
-    float *KKE = sml(Sc::KKE), *L = sml(Sc::L), *A = sml(Sc::A);
-    float *T = sml(Sc::T), *Pv = sml(Sc::Pv), *Pk = sml(Sc::Pk), *dA = sml(Sc::dA), *dT = sml(Sc::dT);
-    float *X = sml(Sc::X), *dL = sml(Sc::dL), *At = sml(Sc::At), *Tt = sml(Sc::Tt), *Xt = sml(Sc::Xt);
-    // after dL: P = dL beta_t E_kk and dA (.) E_qk with their transposes reuse X, Xt, dT, Pv
-    float *dKK = X, *dKKt = Xt, *dQK = dT, *dQKt = Pv;
-    float *St = sc + Sc::sq(Sc::St), *dSpt = sc + Sc::sq(Sc::dSpt);
-    float *beta = scl(Sc::beta), *G = scl(Sc::G), *R = scl(Sc::R), *eG = scl(Sc::eG), *eR = scl(Sc::eR);
-    float *eGnG = scl(Sc::eGnG), *kn = scl(Sc::kn), *qn = scl(Sc::qn), *knorm = scl(Sc::knorm);
-    float *qnorm = scl(Sc::qnorm), *dG = scl(Sc::dG), *dGp = scl(Sc::dGp), *dbeta = scl(Sc::dbeta);
-    float *rA = red, *cA = red + kC, *rL = red + 2 * kC, *cL = red + 3 * kC, *rLK = red + 4 * kC;
-    float *rqd = red + 5 * kC, *rkd = red + 6 * kC, *rbv = red + 7 * kC, *rbk = red + 8 * kC;
+    float *KKE = sml(Sc::KKE), *A = sml(Sc::A), *T = sml(Sc::T), *Pv = sml(Sc::Pv), *Pk = sml(Sc::Pk);
+    float *dT = sml(Sc::dT), *X = sml(Sc::X), *P = sml(Sc::P), *dQK = sml(Sc::dQK);
+    auto nopre = [](int, int) { return 0; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nc = (a.T + kC - 1) / kC;
@@ -217,62 +339,20 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         const float *S = a.fstates + (size_t)ci * D * D;    // state entering the chunk
         const float *dSp = a.bstates + (size_t)ci * D * D;  // gradient of the state leaving it
 
-        // ---- rows: norms, k^, q~, v, dO (zero past the valid tokens) and their transposes,
-        // cleared accumulators
-        for (int t = warp; t < kC; t += kWarps) {
-            const bool valid = t < nv;
-            const size_t gi = ((size_t)(row0 + t) * a.H + h) * D;
-            float kk[D / 32], qq[D / 32], ssk = 0.f, ssq = 0.f;
-#pragma unroll
-            for (int m = 0; m < D / 32; ++m) {
-                const int i = lane + 32 * m;
-                kk[m] = valid ? bf2f(gk[gi + i]) : 0.f;
-                qq[m] = valid ? bf2f(gq[gi + i]) : 0.f;
-                ssk = fmaf(kk[m], kk[m], ssk);
-                ssq = fmaf(qq[m], qq[m], ssq);
+        // ---- the chunk's rows of q, k, v, dO (bf16) into shared memory, zeros past the valid
+        // tokens; beta, the in-chunk cumulative log decay, cleared sums
+        {
+            constexpr int per = D / 8;   // 16-byte pieces of a row
+            for (int x = tid; x < 4 * kC * per; x += kThreads) {
+                const int arr = x / (kC * per), t = (x / per) % kC, p = x % per;
+                const bool valid = t < nv;
+                const __nv_bfloat16 *src = arr == 0 ? gq : arr == 1 ? gk : arr == 2 ? gv : gdo;
+                const size_t gi = ((size_t)(row0 + (valid ? t : 0)) * a.H + h) * D + 8 * p;
+                cp_async16z(sIn + ((size_t)arr * kC + t) * D + 8 * p, src + gi, valid ? 16 : 0);
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                ssk += __shfl_xor_sync(0xffffffffu, ssk, o);
-                ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
-            }
-            const float nk = sqrtf(ssk), nq = sqrtf(ssq);
-            const float fk = a.use_l2 ? 1.f / fmaxf(nk, kNormEpsB) : 1.f;
-            const float fq = a.scale * (a.use_l2 ? 1.f / fmaxf(nq, kNormEpsB) : 1.f);
-#pragma unroll
-            for (int m = 0; m < D / 32; ++m) {
-                const int i = lane + 32 * m;
-                const float vv = valid ? bf2f(gv[gi + i]) : 0.f, oo = valid ? bf2f(gdo[gi + i]) : 0.f;
-                Kh[t * D + i] = kk[m] * fk; Kht[i * kC + t] = kk[m] * fk;
-                Qh[t * D + i] = qq[m] * fq; Qht[i * kC + t] = qq[m] * fq;
-                V[t * D + i] = vv; Vt[i * kC + t] = vv;
-                dO[t * D + i] = oo; dOt[i * kC + t] = oo;
-                dkh[t * D + i] = 0.f;
-                dqh[t * D + i] = 0.f;
-            }
-            if (lane == 0) {
-                rqd[t] = 0.f; rkd[t] = 0.f; rbv[t] = 0.f; rbk[t] = 0.f;
-                kn[t] = fk; qn[t] = fq; knorm[t] = nk; qnorm[t] = nq;
-                beta[t] = valid ? a.beta[(row0 + t) * a.H + h] : 0.f;
-            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
         }
-        // the transposed states, through 32 x 32 tiles in shared memory (the inverse's arrays)
-        for (int tile = 0; tile < (D / 32) * (D / 32); ++tile) {
-            const int r0 = (tile / (D / 32)) * 32, c0 = (tile % (D / 32)) * 32;
-            for (int x = tid; x < 1024; x += kThreads) {
-                const int r = x >> 5, cc = x & 31;
-                sL[r * 33 + cc] = S[(size_t)(r0 + r) * D + c0 + cc];
-                sT[r * 33 + cc] = dSp[(size_t)(r0 + r) * D + c0 + cc];
-            }
-            __syncthreads();
-            for (int x = tid; x < 1024; x += kThreads) {
-                const int r = x >> 5, cc = x & 31;
-                St[(size_t)(c0 + r) * D + r0 + cc] = sL[cc * 33 + r];
-                dSpt[(size_t)(c0 + r) * D + r0 + cc] = sT[cc * 33 + r];
-            }
-            __syncthreads();
-        }
-        if (warp == 0) {   // in-chunk cumulative log decay: lane owns tokens 2 lane, 2 lane + 1
+        if (warp == 0) {   // lane owns tokens 2 lane, 2 lane + 1
             auto dec = [&](int t) { return (t < nv && a.decay) ? a.decay[(row0 + t) * a.H + h] : 0.f; };
             const float d0 = dec(2 * lane), d1 = dec(2 * lane + 1);
             float incl = d0 + d1;
@@ -291,35 +371,72 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             eR[2 * lane] = __expf(r0); eR[2 * lane + 1] = __expf(r1);
             eGnG[2 * lane] = __expf(gn - g0); eGnG[2 * lane + 1] = __expf(gn - g1);
             if (lane == 0) { sGn[0] = gn; sGn[1] = 0.f; }
+        } else if (warp == 1) {
+            for (int t = lane; t < kC; t += 32) beta[t] = t < nv ? a.beta[(row0 + t) * a.H + h] : 0.f;
         }
+        for (int x = tid; x < 10 * kC; x += kThreads) rA[x] = 0.f;
+        asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
-        for (int x = tid; x < kC * D; x += kThreads) Kt[x] = eGnG[x / D] * Kh[x];
 
-        // ---- Gram products: A = (q~ k^^T) E_qk (inclusive), L = beta_t (k^ k^^T) E_kk (strict);
-        // the second product reads one staged operand, so its epilogue may fill the inverse's L
-        // in the other buffer
-        gemm(sA, sB, kC, kC, D, Qh, Kh, [&](int t, int s, float v0, float v1) -> float {
-            const float vv[2] = {v0, v1};
+        // ---- rows: norms; k^, q~, v, dO and K~ = diag(e^{G_n - G}) k^ into the scratch (fp32)
+        for (int t = warp; t < kC; t += kWarps) {
+            constexpr int E = D / 32;   // consecutive elements per lane
+            float fq_[E], fk_[E], fv_[E], fo_[E];
+            ld_bf16<E>(fq_, sIn + (size_t)(0 * kC + t) * D + E * lane);
+            ld_bf16<E>(fk_, sIn + (size_t)(1 * kC + t) * D + E * lane);
+            ld_bf16<E>(fv_, sIn + (size_t)(2 * kC + t) * D + E * lane);
+            ld_bf16<E>(fo_, sIn + (size_t)(3 * kC + t) * D + E * lane);
+            float ssk = 0.f, ssq = 0.f;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const float e = (s + u <= t) ? __expf(G[t] - G[s + u]) : 0.f;
-                A[t * kC + s + u] = vv[u] * e;
-                At[(s + u) * kC + t] = vv[u] * e;
+            for (int e = 0; e < E; ++e) {
+                ssk = fmaf(fk_[e], fk_[e], ssk);
+                ssq = fmaf(fq_[e], fq_[e], ssq);
             }
-            return 0.f;
-        });
-        gemm(sA, sB, kC, kC, D, Kh, Kh, [&](int t, int s, float v0, float v1) -> float {
-            const float vv[2] = {v0, v1};
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const float e = (s + u < t) ? __expf(R[t] - G[s + u]) : 0.f;
-                KKE[t * kC + s + u] = vv[u] * e;
-                L[t * kC + s + u] = beta[t] * vv[u] * e;
-                sL[t * PL + s + u] = beta[t] * vv[u] * e;
+            for (int o = 16; o > 0; o >>= 1) {
+                ssk += __shfl_xor_sync(0xffffffffu, ssk, o);
+                ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
             }
-            return 0.f;
-        });
-        __syncthreads();
+            const float nk = sqrtf(ssk), nq = sqrtf(ssq);
+            const float fk = a.use_l2 ? 1.f / fmaxf(nk, kNormEpsB) : 1.f;
+            const float fqn = a.use_l2 ? 1.f / fmaxf(nq, kNormEpsB) : 1.f;
+            const size_t o = (size_t)t * D + E * lane;
+            st_row<E>(Kh + o, fk_, fk);
+            st_row<E>(Kt + o, fk_, fk * eGnG[t]);
+            st_row<E>(Qh + o, fq_, a.scale * fqn);
+            st_row<E>(V + o, fv_, 1.f);
+            st_row<E>(dO + o, fo_, 1.f);
+            if (lane == 0) {   // the normalisation factors, negative where its adjoint is the identity
+                kn[t] = (a.use_l2 && nk > kNormEpsB) ? fk : -fk;
+                qn[t] = (a.use_l2 && nq > kNormEpsB) ? fqn : -fqn;
+            }
+        }
+
+        // ---- A = (q~ k^^T) (.) E_qk (inclusive)
+        {
+            Acc<kC> acc;
+            acc.zero();
+            pass<kRow, kRow, kC, D>(acc, sA, sB, Qh, D, Kh, D);
+            finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
+                const float e0 = s <= t ? __expf(G[t] - G[s]) : 0.f, e1 = s + 1 <= t ? __expf(G[t] - G[s + 1]) : 0.f;
+                st2(A + t * kC + s, x0 * e0, x1 * e1);
+                return 0.f;
+            });
+        }
+        // ---- (k^ k^^T) (.) E_kk (strict), kept; L = beta_t (k^ k^^T) (.) E_kk into the inverse's
+        // array (the pass reads one staged operand on both sides, leaving that buffer free)
+        {
+            Acc<kC> acc;
+            acc.zero();
+            pass<kRow, kRow, kC, D>(acc, sA, sB, Kh, D, Kh, D);
+            finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
+                const float e0 = s < t ? __expf(R[t] - G[s]) : 0.f, e1 = s + 1 < t ? __expf(R[t] - G[s + 1]) : 0.f;
+                st2(KKE + t * kC + s, x0 * e0, x1 * e1);
+                sL[t * PL + s] = beta[t] * x0 * e0;
+                sL[t * PL + s + 1] = beta[t] * x1 * e1;
+                return 0.f;
+            });
+        }
 
         // ---- T = (I + L)^{-1}: four threads per column j (a quarter of the terms each), rows
         // in order; T[r][j] = delta_rj - sum_{s<r} L[r][s] T[s][j]
@@ -335,164 +452,209 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             }
         }
         __syncthreads();
+        // T, and T with its columns scaled: Pv = T diag(beta), Pk = T diag(beta e^R)
         for (int x = tid; x < kC * kC; x += kThreads) {
             const int t = x / kC, s = x % kC;
             const float tv = sT[t * PL + s];
             T[x] = tv;
-            Tt[s * kC + t] = tv;
             Pv[x] = tv * beta[s];
             Pk[x] = tv * beta[s] * eR[s];
         }
-        __syncthreads();
 
-        // ---- forward quantities: W = T diag(beta e^R) K^, U = T diag(beta) V - W S;  dU = A^T dO
-        gemm(sA, sB, kC, D, kC, Pk, Kht, [&](int t, int j, float v0, float v1) -> float {
-            W[t * D + j] = v0; W[t * D + j + 1] = v1;
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, kC, Pv, Vt, [&](int t, int j, float v0, float v1) -> float {
-            U[t * D + j] = v0; U[t * D + j + 1] = v1;
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, kC, At, dOt, [&](int s, int j, float v0, float v1) -> float {
-            dU[s * D + j] = v0; dU[s * D + j + 1] = v1;
-            return 0.f;
-        });
-        __syncthreads();
-        // U -= W S;  dU += K~ dS' (and its transpose);  DOS = dO S^T  (each output element stays
-        // with one thread across the products that write it)
-        gemm(sA, sB, kC, D, D, W, St, [&](int t, int j, float v0, float v1) -> float {
-            U[t * D + j] -= v0; U[t * D + j + 1] -= v1;
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, D, Kt, dSpt, [&](int s, int j, float v0, float v1) -> float {
-            const float u0 = dU[s * D + j] + v0, u1 = dU[s * D + j + 1] + v1;
-            dU[s * D + j] = u0; dU[s * D + j + 1] = u1;
-            dUt[j * kC + s] = u0; dUt[(j + 1) * kC + s] = u1;
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, D, dO, S, [&](int t, int i, float v0, float v1) -> float {   // dO S^T
-            dqh[t * D + i] += eG[t] * v0; dqh[t * D + i + 1] += eG[t] * v1;
-            return v0 * Qh[t * D + i] + v1 * Qh[t * D + i + 1];
-        }, rqd);
-        __syncthreads();
+        // ---- forward quantities: W = Pk K^ (kept negated), U = Pv V - W S
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kRow, kCol, D, kC>(acc, sA, sB, Pk, kC, Kh, D);
+            finish<D>(acc, nopre, [&](int t, int j, float x0, float x1, float, float, int, float *) -> float {
+                st2(Wn + t * D + j, -x0, -x1);
+                return 0.f;
+            });
+        }
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kRow, kCol, D, kC>(acc, sA, sB, Pv, kC, V, D);
+            pass<kRow, kCol, D, D>(acc, sA, sB, Wn, D, S, D);
+            finish<D>(acc, nopre, [&](int t, int j, float x0, float x1, float, float, int, float *) -> float {
+                st2(U + t * D + j, x0, x1);
+                return 0.f;
+            });
+        }
+        // ---- dU = A^T dO + K~ dS'
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kCol, kCol, D, kC>(acc, sA, sB, A, kC, dO, D);
+            pass<kRow, kCol, D, D>(acc, sA, sB, Kt, D, dSp, D);
+            finish<D>(acc, nopre, [&](int s, int j, float x0, float x1, float, float, int, float *) -> float {
+                st2(dU + s * D + j, x0, x1);
+                return 0.f;
+            });
+        }
+        // ---- dq~ = diag(e^G) dO S^T (its first term); row sums q~ . dO S^T
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kRow, kRow, D, D>(acc, sA, sB, dO, D, S, D);
+            finish<D>(acc, [&](int t, int i) { return ld2(Qh + t * D + i); },
+                      [&](int t, int i, float x0, float x1, float, float, float2 q, float *) -> float {
+                          st2(dqh + t * D + i, eG[t] * x0, eG[t] * x1);
+                          return x0 * q.x + x1 * q.y;
+                      },
+                      rqd);
+        }
+        // ---- dA = mask_incl(dO U^T) -> dA (.) E_qk; row and column sums of dA (.) A
+        {
+            Acc<kC> acc;
+            acc.zero();
+            pass<kRow, kRow, kC, D>(acc, sA, sB, nullptr, D, U, D);   // dO is still staged
+            finish<kC>(acc, [&](int t, int s) { return ld2(A + t * kC + s); },
+                       [&](int t, int s, float x0, float x1, float, float, float2 av, float *cs) -> float {
+                           const float e0 = s <= t ? __expf(G[t] - G[s]) : 0.f;
+                           const float e1 = s + 1 <= t ? __expf(G[t] - G[s + 1]) : 0.f;
+                           const float d0 = s <= t ? x0 : 0.f, d1 = s + 1 <= t ? x1 : 0.f;
+                           st2(dQK + t * kC + s, d0 * e0, d1 * e1);
+                           const float p0 = d0 * av.x, p1 = d1 * av.y;
+                           cs[0] += p0;
+                           cs[1] += p1;
+                           return p0 + p1;
+                       },
+                       rA, cA);
+        }
+        // ---- dK~ = U dS'^T: dk^ = diag(e^{G_n - G}) dK~ (its first term); row sums K~ . dK~
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kRow, kRow, D, D>(acc, sA, sB, U, D, dSp, D);
+            finish<D>(acc, [&](int s, int i) { return ld2(Kh + s * D + i); },
+                      [&](int s, int i, float x0, float x1, float, float, float2 k, float *) -> float {
+                          const float w = eGnG[s];
+                          st2(dkh + s * D + i, w * x0, w * x1);
+                          return w * (x0 * k.x + x1 * k.y);
+                      },
+                      rkd);
+        }
+        // ---- dW = -dU S^T
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kRow, kRow, D, D>(acc, sA, sB, dU, D, S, D);
+            finish<D>(acc, nopre, [&](int s, int i, float x0, float x1, float, float, int, float *) -> float {
+                st2(dW + s * D + i, -x0, -x1);
+                return 0.f;
+            });
+        }
+        // ---- dT = diag(beta) applied to the columns of dU V^T, plus diag(beta e^R) to those of
+        // dW K^^T; the column sums of T (.) (dU V^T) and T (.) (dW K^^T) are (T^T dU) . v and
+        // (T^T dW) . k^, the terms of beta's gradient through V and through K^
+        {
+            Acc<kC> acc, acc2;
+            acc.zero();
+            acc2.zero();
+            pass<kRow, kRow, kC, D>(acc, sA, sB, nullptr, D, V, D);   // dU is still staged
+            pass<kRow, kRow, kC, D>(acc2, sA, sB, dW, D, Kh, D);
+            finish2<kC>(acc, &acc2, [&](int t, int s) { return ld2(T + t * kC + s); },
+                        [&](int t, int s, float x0, float x1, float y0, float y1, float2 tv, float *cs) -> float {
+                            const float b0 = beta[s], b1 = beta[s + 1];
+                            st2(dT + t * kC + s, b0 * (x0 + eR[s] * y0), b1 * (x1 + eR[s + 1] * y1));
+                            cs[0] += tv.x * x0;
+                            cs[1] += tv.y * x1;
+                            cs[2] += tv.x * y0;
+                            cs[3] += tv.y * y1;
+                            return 0.f;
+                        },
+                        nullptr, rbv, rbk);
+        }
+        // ---- X = dT T^T;  dL = -mask_strict(T^T X) -> P = dL (.) beta_t E_kk, with the row sums
+        // of dL (.) (k^ k^^T) E_kk and the column sums of dL (.) L
+        {
+            Acc<kC> acc;
+            acc.zero();
+            pass<kRow, kRow, kC, kC>(acc, sA, sB, dT, kC, T, kC);
+            finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
+                st2(X + t * kC + s, x0, x1);
+                return 0.f;
+            });
+        }
+        {
+            Acc<kC> acc;
+            acc.zero();
+            pass<kCol, kCol, kC, kC>(acc, sA, sB, T, kC, X, kC);
+            finish<kC>(acc, [&](int t, int s) { return ld2(KKE + t * kC + s); },
+                       [&](int t, int s, float x0, float x1, float, float, float2 kk, float *cs) -> float {
+                           const float l0 = s < t ? -x0 : 0.f, l1 = s + 1 < t ? -x1 : 0.f;
+                           const float e0 = s < t ? __expf(R[t] - G[s]) : 0.f;
+                           const float e1 = s + 1 < t ? __expf(R[t] - G[s + 1]) : 0.f;
+                           const float bt = beta[t];
+                           st2(P + t * kC + s, l0 * bt * e0, l1 * bt * e1);
+                           const float p0 = l0 * kk.x, p1 = l1 * kk.y;
+                           cs[0] += bt * p0;
+                           cs[1] += bt * p1;
+                           return p0 + p1;
+                       },
+                       rLK, cL);
+        }
+        // ---- dk^ += Pk^T dW + P K^ + P^T K^ + (dA (.) E_qk)^T Q~  (Pk^T dW = diag(beta e^R) T^T dW);
+        // row sums k^ . dk^
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kCol, kCol, D, kC>(acc, sA, sB, Pk, kC, dW, D);
+            pass<kRow, kCol, D, kC>(acc, sA, sB, P, kC, Kh, D);
+            pass<kCol, kCol, D, kC>(acc, sA, sB, P, kC, nullptr, D);   // K^ is still staged
+            pass<kCol, kCol, D, kC>(acc, sA, sB, dQK, kC, Qh, D);
+            finish<D>(acc,
+                      [&](int s, int i) {
+                          const float2 o = ld2(dkh + s * D + i), k = ld2(Kh + s * D + i);
+                          return make_float4(o.x, o.y, k.x, k.y);
+                      },
+                      [&](int s, int i, float x0, float x1, float, float, float4 ok, float *) -> float {
+                          const float d0 = ok.x + x0, d1 = ok.y + x1;
+                          st2(dkh + s * D + i, d0, d1);
+                          return d0 * ok.z + d1 * ok.w;
+                      },
+                      kdot);
+        }
+        // ---- dq~ += (dA (.) E_qk) K^;  row sums q~ . dq~
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kRow, kCol, D, kC>(acc, sA, sB, dQK, kC, Kh, D);
+            finish<D>(acc,
+                      [&](int t, int i) {
+                          const float2 o = ld2(dqh + t * D + i), q = ld2(Qh + t * D + i);
+                          return make_float4(o.x, o.y, q.x, q.y);
+                      },
+                      [&](int t, int i, float x0, float x1, float, float, float4 oq, float *) -> float {
+                          const float d0 = oq.x + x0, d1 = oq.y + x1;
+                          st2(dqh + t * D + i, d0, d1);
+                          return d0 * oq.z + d1 * oq.w;
+                      },
+                      qdot);
+        }
 
-        // ---- dA = mask_incl(dO U^T),  dK~ = U dS'^T,  dW = -dU S^T
-        gemm(sA, sB, kC, kC, D, dO, U, [&](int t, int s, float v0, float v1) -> float {
-            dA[t * kC + s] = s <= t ? v0 : 0.f;
-            dA[t * kC + s + 1] = s + 1 <= t ? v1 : 0.f;
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, D, U, dSp, [&](int s, int i, float v0, float v1) -> float {   // dK~
-            dkh[s * D + i] += eGnG[s] * v0; dkh[s * D + i + 1] += eGnG[s] * v1;
-            return v0 * Kt[s * D + i] + v1 * Kt[s * D + i + 1];
-        }, rkd);
-        gemm(sA, sB, kC, D, D, dU, S, [&](int s, int i, float v0, float v1) -> float {
-            dW[s * D + i] = -v0; dW[s * D + i + 1] = -v1;
-            dWt[i * kC + s] = -v0; dWt[(i + 1) * kC + s] = -v1;
-            return 0.f;
-        });
-        __syncthreads();
-
-        // ---- dT = dU (diag(beta) V)^T + dW (diag(beta e^R) K^)^T;  dBv = T^T dU;  dBk = T^T dW,
-        // dK^ += diag(beta e^R) dBk
-        gemm(sA, sB, kC, kC, D, dU, V, [&](int t, int s, float v0, float v1) -> float {
-            dT[t * kC + s] = v0 * beta[s];
-            dT[t * kC + s + 1] = v1 * beta[s + 1];
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, kC, Tt, dUt, [&](int s, int j, float v0, float v1) -> float {   // dBv
-            return v0 * V[s * D + j] + v1 * V[s * D + j + 1];
-        }, rbv);
-        gemm(sA, sB, kC, kC, D, dW, Kh, [&](int t, int s, float v0, float v1) -> float {
-            dT[t * kC + s] += v0 * beta[s] * eR[s];
-            dT[t * kC + s + 1] += v1 * beta[s + 1] * eR[s + 1];
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, kC, Tt, dWt, [&](int s, int i, float v0, float v1) -> float {   // dBk
-            const float w = beta[s] * eR[s];
-            dkh[s * D + i] += w * v0; dkh[s * D + i + 1] += w * v1;
-            return v0 * Kh[s * D + i] + v1 * Kh[s * D + i + 1];
-        }, rbk);
-        __syncthreads();
-
-        // ---- dL = -mask_strict(T^T dT T^T)
-        gemm(sA, sB, kC, kC, kC, dT, T, [&](int t, int s, float v0, float v1) -> float {
-            X[t * kC + s] = v0; X[t * kC + s + 1] = v1;
-            Xt[s * kC + t] = v0; Xt[(s + 1) * kC + t] = v1;
-            return 0.f;
-        });
-        __syncthreads();
-        gemm(sA, sB, kC, kC, kC, Tt, Xt, [&](int t, int s, float v0, float v1) -> float {
-            dL[t * kC + s] = s < t ? -v0 : 0.f;
-            dL[t * kC + s + 1] = s + 1 < t ? -v1 : 0.f;
-            return 0.f;
-        });
-        __syncthreads();
-
-        // ---- row and column sums of dA (.) A and dL (.) L, dL (.) KKE; P = dL beta_t E_kk and
-        // dA (.) E_qk, with their transposes
+        // ---- per token: the gradients of G, of R (through G_{t-1} or G_t) and of beta
         if (tid < kC) {
             const int t = tid;
-            float sa = 0.f, sl = 0.f, slk = 0.f;
-            for (int s = 0; s < kC; ++s) {
-                sa = fmaf(dA[t * kC + s], A[t * kC + s], sa);
-                sl = fmaf(dL[t * kC + s], L[t * kC + s], sl);
-                slk = fmaf(dL[t * kC + s], KKE[t * kC + s], slk);
-            }
-            rA[t] = sa; rL[t] = sl; rLK[t] = slk;
-        } else if (tid < 2 * kC) {
-            const int s = tid - kC;
-            float sa = 0.f, sl = 0.f;
-            for (int t = 0; t < kC; ++t) {
-                sa = fmaf(dA[t * kC + s], A[t * kC + s], sa);
-                sl = fmaf(dL[t * kC + s], L[t * kC + s], sl);
-            }
-            cA[s] = sa; cL[s] = sl;
-        }
-        for (int x = tid; x < kC * kC; x += kThreads) {
-            const int t = x / kC, s = x % kC;
-            const float ekk = s < t ? __expf(R[t] - G[s]) : 0.f, eqk = s <= t ? __expf(G[t] - G[s]) : 0.f;
-            const float p = dL[x] * beta[t] * ekk, qk = dA[x] * eqk;
-            dKK[x] = p; dKKt[s * kC + t] = p;
-            dQK[x] = qk; dQKt[s * kC + t] = qk;
-        }
-        __syncthreads();
-        // dK^ += P K^ + P^T K^ + (dA E_qk)^T Q~;  dQ~ += (dA E_qk) K^
-        gemm(sA, sB, kC, D, kC, dKK, Kht, [&](int t, int i, float v0, float v1) -> float {
-            dkh[t * D + i] += v0; dkh[t * D + i + 1] += v1;
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, kC, dKKt, Kht, [&](int s, int i, float v0, float v1) -> float {
-            dkh[s * D + i] += v0; dkh[s * D + i + 1] += v1;
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, kC, dQKt, Qht, [&](int s, int i, float v0, float v1) -> float {
-            dkh[s * D + i] += v0; dkh[s * D + i + 1] += v1;
-            return 0.f;
-        });
-        gemm(sA, sB, kC, D, kC, dQK, Kht, [&](int t, int i, float v0, float v1) -> float {
-            dqh[t * D + i] += v0; dqh[t * D + i + 1] += v1;
-            return 0.f;
-        });
-        __syncthreads();
-
-        // ---- per token: dG, dR, dbeta (the dots of q~ . dO S^T, dK~ . K~, dBv . v, dBk . k^ came
-        // from the products' epilogues)
-        if (tid < kC) {
-            const int t = tid;
-            const float dr = rL[t] + beta[t] * eR[t] * rbk[t];
+            const float dr = beta[t] * rLK[t] + beta[t] * eR[t] * rbk[t];
             float dg = eG[t] * rqd[t] + rA[t] - cA[t] - cL[t] - rkd[t];
             float dgp = 0.f;
             if (a.decayed_read) dg += dr; else dgp = dr;
+            const float db = rbv[t] + eR[t] * rbk[t] + rLK[t];
+            atomicAdd(&sGn[1], rkd[t]);
             dG[t] = dg;
             dGp[t] = dgp;
-            dbeta[t] = rbv[t] + eR[t] * rbk[t] + rLK[t];
-            atomicAdd(&sGn[1], rkd[t]);
+            dbeta[t] = db;
         }
         {   // e^{G_n} sum(S (.) dS')
+            const float4 *s4 = reinterpret_cast<const float4 *>(S), *d4 = reinterpret_cast<const float4 *>(dSp);
             float acc = 0.f;
-            for (int x = tid; x < D * D; x += kThreads) acc = fmaf(S[x], dSp[x], acc);
+#pragma unroll 8
+            for (int x = tid; x < D * D / 4; x += kThreads) {
+                const float4 u = s4[x], w = d4[x];
+                acc = fmaf(u.x, w.x, fmaf(u.y, w.y, fmaf(u.z, w.z, fmaf(u.w, w.w, acc))));
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
             if (lane == 0) atomicAdd(&sGn[1], __expf(sGn[0]) * acc);
@@ -522,31 +684,38 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             if (t0 < nv) a.dbeta[(row0 + t0) * a.H + h] = dbeta[t0];
             if (t1 < nv) a.dbeta[(row0 + t1) * a.H + h] = dbeta[t1];
         }
-        // ---- dq, dk through the normalisation: dx = f (dx^ - x^ (x^ . dx^)) for |x| > eps
-        for (int t = warp; t < nv; t += kWarps) {
-            float kdot = 0.f, qdot = 0.f;
-#pragma unroll
-            for (int m = 0; m < D / 32; ++m) {
-                const int x = t * D + lane + 32 * m;
-                kdot = fmaf(Kh[x], dkh[x], kdot);
-                qdot = fmaf(Qh[x], dqh[x], qdot);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                kdot += __shfl_xor_sync(0xffffffffu, kdot, o);
-                qdot += __shfl_xor_sync(0xffffffffu, qdot, o);
-            }
-            const bool pk = a.use_l2 && knorm[t] > kNormEpsB, pq = a.use_l2 && qnorm[t] > kNormEpsB;
+        // ---- dq, dk through the normalisation: dx = f (dx^ - x^ (x^ . dx^)) where |x| > eps
+        {
+            constexpr int per = D / 4, iters = kC * per / kThreads;   // float4 pieces
             const float qs = a.scale * a.scale;
-            const size_t gi = ((size_t)(row0 + t) * a.H + h) * D;
 #pragma unroll
-            for (int m = 0; m < D / 32; ++m) {
-                const int i = lane + 32 * m, x = t * D + i;
-                a.dk[gi + i] = kn[t] * (dkh[x] - (pk ? Kh[x] * kdot : 0.f));
-                a.dq[gi + i] = qn[t] * (dqh[x] - (pq ? Qh[x] * qdot / qs : 0.f));
+            for (int u0 = 0; u0 < iters; u0 += 4) {
+                float4 kh[4], gk[4], qh[4], gq[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int x = tid + (u0 + u) * kThreads;
+                    kh[u] = reinterpret_cast<const float4 *>(Kh)[x];
+                    gk[u] = reinterpret_cast<const float4 *>(dkh)[x];
+                    qh[u] = reinterpret_cast<const float4 *>(Qh)[x];
+                    gq[u] = reinterpret_cast<const float4 *>(dqh)[x];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int x = tid + (u0 + u) * kThreads, t = x / per, i = 4 * (x % per);
+                    if (t >= nv) continue;
+                    const float fk = fabsf(kn[t]), ck = kn[t] > 0.f ? kdot[t] : 0.f;
+                    const float fq = a.scale * fabsf(qn[t]), cq = qn[t] > 0.f ? qdot[t] / qs : 0.f;
+                    const size_t gi = ((size_t)(row0 + t) * a.H + h) * D + i;
+                    *reinterpret_cast<float4 *>(a.dk + gi) =
+                        make_float4(fk * (gk[u].x - kh[u].x * ck), fk * (gk[u].y - kh[u].y * ck),
+                                    fk * (gk[u].z - kh[u].z * ck), fk * (gk[u].w - kh[u].w * ck));
+                    *reinterpret_cast<float4 *>(a.dq + gi) =
+                        make_float4(fq * (gq[u].x - qh[u].x * cq), fq * (gq[u].y - qh[u].y * cq),
+                                    fq * (gq[u].z - qh[u].z * cq), fq * (gq[u].w - qh[u].w * cq));
+                }
             }
         }
-        __syncthreads();   // the scratch is rewritten by the next chunk
+        __syncthreads();   // the scratch and the shared arrays are rewritten by the next chunk
     }
 }
 
@@ -556,13 +725,13 @@ size_t chunk_bwd_scratch_floats(int D) {
     return D == 128 ? Scr<128>::floats : Scr<64>::floats;
 }
 
-// Persistent CTAs of the gradient kernel: a fixed number, so that the workspace query needs
-// no device (each CTA has its own scratch region).
+// Persistent CTAs of the gradient kernel: a fixed number (two per SM on a 152-SM part), so
+// that the workspace query needs no device (each CTA has its own scratch region).
 int chunk_bwd_ctas() { return 304; }
 
 template <int D>
 cudaError_t launch_grads(const ChunkBwdArgs &a, cudaStream_t st) {
-    const int smem = (int)sizeof(float) * max((kC + D) * (D + 16), kC * (D + 16) + 2 * kC * (kC + 1));
+    const int smem = (int)sizeof(float) * Smem<D>::floats;
     cudaError_t e = cudaFuncSetAttribute(chunk_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     chunk_bwd_kernel<D><<<a.ctas, kThreads, smem, st>>>(a);
