@@ -139,32 +139,20 @@ struct Acc {
     }
 };
 
-// One pass: acc += A B^T over a contraction of length K, A(m, k) for m < 64 and B(n, k) for
-// n < N given in global memory in layouts LA, LB (row strides lda, ldb).  A null pointer
-// reuses what the previous pass staged in that buffer (same layout and sizes); B == A stages
-// the operand once and reads it on both sides.  Begins with a barrier of the CTA, so the
-// stores of the previous epilogue are visible and the previous pass has finished reading the
-// buffers.  Inside a 16-wide k step lane t4 takes the four consecutive k = 4 t4 .. 4 t4 + 3 on
-// both operands, the first two for one MMA and the last two for the other: the same
-// permutation of k on A and B, which leaves the sum unchanged.
+// acc += A B^T from operands already staged at sa, sb (layouts LA, LB).  Inside a 16-wide k
+// step lane t4 takes the four consecutive k = 4 t4 .. 4 t4 + 3 on both operands, the first two
+// for one MMA and the last two for the other: the same permutation of k on A and B, which
+// leaves the sum unchanged.
 template <Lay LA, Lay LB, int N, int K>
-__device__ __forceinline__ void pass(Acc<N> &acc, float *sA, float *sB, const float *A, int lda, const float *B,
-                                     int ldb) {
+__device__ __forceinline__ void mma_staged(Acc<N> &acc, const float *sa, const float *bb) {
     constexpr int PA = lay_pitch<LA>(kC, K), PB = lay_pitch<LB>(N, K), NJ = Acc<N>::NJ;
-    const bool same = (A != nullptr && B == A);
-    __syncthreads();
-    if (A) stage<LA, kC, K>(sA, A, lda);
-    if (B && !same) stage<LB, N, K>(sB, B, ldb);
-    cp_async_wait_all();
-    __syncthreads();
-    const float *bb = same ? sA : sB;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
     const int m0 = (warp >> 2) * 32, n0 = (warp & 3) * Acc<N>::WN;
 #pragma unroll 2
     for (int k0 = 0; k0 < K; k0 += 16) {
         float xa[4][4], zb[NJ][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) frag4<LA, PA>(xa[i], sA, m0 + g + 8 * i, k0 + 4 * t4);
+        for (int i = 0; i < 4; ++i) frag4<LA, PA>(xa[i], sa, m0 + g + 8 * i, k0 + 4 * t4);
 #pragma unroll
         for (int j = 0; j < NJ; ++j) frag4<LB, PB>(zb[j], bb, n0 + 8 * j + g, k0 + 4 * t4);
 #pragma unroll
@@ -180,6 +168,24 @@ __device__ __forceinline__ void pass(Acc<N> &acc, float *sA, float *sB, const fl
             }
         }
     }
+}
+
+// One pass: acc += A B^T over a contraction of length K, A(m, k) for m < 64 and B(n, k) for
+// n < N given in global memory in layouts LA, LB (row strides lda, ldb).  A null pointer
+// reuses what the previous pass staged in that buffer (same layout and sizes); B == A stages
+// the operand once and reads it on both sides.  Begins with a barrier of the CTA, so the
+// stores of the previous epilogue are visible and the previous pass has finished reading the
+// buffers.
+template <Lay LA, Lay LB, int N, int K>
+__device__ __forceinline__ void pass(Acc<N> &acc, float *sA, float *sB, const float *A, int lda, const float *B,
+                                     int ldb) {
+    const bool same = (A != nullptr && B == A);
+    __syncthreads();
+    if (A) stage<LA, kC, K>(sA, A, lda);
+    if (B && !same) stage<LB, N, K>(sB, B, ldb);
+    cp_async_wait_all();
+    __syncthreads();
+    mma_staged<LA, LB, N, K>(acc, sA, same ? sA : sB);
 }
 
 // The epilogue over a product's accumulators (one or two products of the same shape, e.g. two
@@ -412,24 +418,21 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             }
         }
 
-        // ---- A = (q~ k^^T) (.) E_qk (inclusive)
+        // ---- A = (q~ k^^T) (.) E_qk (inclusive);  (k^ k^^T) (.) E_kk (strict), kept, and
+        // L = beta_t (k^ k^^T) (.) E_kk into the inverse's array: both from one staging of q~, k^
         {
-            Acc<kC> acc;
+            Acc<kC> acc, acck;
             acc.zero();
+            acck.zero();
             pass<kRow, kRow, kC, D>(acc, sA, sB, Qh, D, Kh, D);
+            mma_staged<kRow, kRow, kC, D>(acck, sB, sB);
             finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
                 const float e0 = s <= t ? __expf(G[t] - G[s]) : 0.f, e1 = s + 1 <= t ? __expf(G[t] - G[s + 1]) : 0.f;
                 st2(A + t * kC + s, x0 * e0, x1 * e1);
                 return 0.f;
             });
-        }
-        // ---- (k^ k^^T) (.) E_kk (strict), kept; L = beta_t (k^ k^^T) (.) E_kk into the inverse's
-        // array (the pass reads one staged operand on both sides, leaving that buffer free)
-        {
-            Acc<kC> acc;
-            acc.zero();
-            pass<kRow, kRow, kC, D>(acc, sA, sB, Kh, D, Kh, D);
-            finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
+            // (every warp is past both products: the staged k^ may be overwritten)
+            finish<kC>(acck, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
                 const float e0 = s < t ? __expf(R[t] - G[s]) : 0.f, e1 = s + 1 < t ? __expf(R[t] - G[s + 1]) : 0.f;
                 st2(KKE + t * kC + s, x0 * e0, x1 * e1);
                 sL[t * PL + s] = beta[t] * x0 * e0;
@@ -438,18 +441,48 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             });
         }
 
-        // ---- T = (I + L)^{-1}: four threads per column j (a quarter of the terms each), rows
-        // in order; T[r][j] = delta_rj - sum_{s<r} L[r][s] T[s][j]
+        // ---- T = (I + L)^{-1} in 32 x 32 blocks.  The diagonal blocks by substitution: warp w
+        // takes block w, lane j its column j, held in registers; once row s of the column is final
+        // its term is subtracted from every later row.  Meanwhile the other warps clear the upper
+        // block.  Then T_BA = -T_BB (L_BA T_AA), L_BA T_AA kept in the L array's unused upper
+        // block.
+        if (warp < 2) {
+            const int o = 32 * warp;
+            float tc[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r) tc[r] = r == lane ? 1.f : 0.f;
+#pragma unroll
+            for (int s = 0; s < 31; ++s)
+#pragma unroll
+                for (int r = s + 1; r < 32; ++r) tc[r] = fmaf(-sL[(o + r) * PL + o + s], tc[s], tc[r]);
+#pragma unroll
+            for (int r = 0; r < 32; ++r) sT[(o + r) * PL + o + lane] = tc[r];
+        } else {
+            for (int x = tid - 64; x < 32 * 32; x += kThreads - 64) sT[(x >> 5) * PL + 32 + (x & 31)] = 0.f;
+        }
+        __syncthreads();
         {
-            const int j = tid >> 2, part = tid & 3;
-            for (int r = 0; r < kC; ++r) {
-                float acc = 0.f;
-                for (int s = part; s < r; s += 4) acc = fmaf(sL[r * PL + s], sT[s * PL + j], acc);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                if (part == 0) sT[r * PL + j] = (r == j ? 1.f : 0.f) - (r > j ? acc : 0.f);
-                __syncwarp();
+            float y[4] = {};
+#pragma unroll 8
+            for (int s = 0; s < 32; ++s) {
+                const float tv = sT[s * PL + lane];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) y[q] = fmaf(sL[(32 + warp + 8 * q) * PL + s], tv, y[q]);
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sL[(warp + 8 * q) * PL + 32 + lane] = y[q];
+        }
+        __syncthreads();
+        {
+            float y[4] = {};
+#pragma unroll 8
+            for (int s = 0; s < 32; ++s) {
+                const float lv = sL[s * PL + 32 + lane];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) y[q] = fmaf(sT[(32 + warp + 8 * q) * PL + 32 + s], lv, y[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sT[(32 + warp + 8 * q) * PL + lane] = -y[q];
         }
         __syncthreads();
         // T, and T with its columns scaled: Pv = T diag(beta), Pk = T diag(beta e^R)
@@ -504,42 +537,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
                       },
                       rqd);
         }
-        // ---- dA = mask_incl(dO U^T) -> dA (.) E_qk; row and column sums of dA (.) A
-        {
-            Acc<kC> acc;
-            acc.zero();
-            pass<kRow, kRow, kC, D>(acc, sA, sB, nullptr, D, U, D);   // dO is still staged
-            finish<kC>(acc, [&](int t, int s) { return ld2(A + t * kC + s); },
-                       [&](int t, int s, float x0, float x1, float, float, float2 av, float *cs) -> float {
-                           const float e0 = s <= t ? __expf(G[t] - G[s]) : 0.f;
-                           const float e1 = s + 1 <= t ? __expf(G[t] - G[s + 1]) : 0.f;
-                           const float d0 = s <= t ? x0 : 0.f, d1 = s + 1 <= t ? x1 : 0.f;
-                           st2(dQK + t * kC + s, d0 * e0, d1 * e1);
-                           const float p0 = d0 * av.x, p1 = d1 * av.y;
-                           cs[0] += p0;
-                           cs[1] += p1;
-                           return p0 + p1;
-                       },
-                       rA, cA);
-        }
-        // ---- dK~ = U dS'^T: dk^ = diag(e^{G_n - G}) dK~ (its first term); row sums K~ . dK~
-        {
-            Acc<D> acc;
-            acc.zero();
-            pass<kRow, kRow, D, D>(acc, sA, sB, U, D, dSp, D);
-            finish<D>(acc, [&](int s, int i) { return ld2(Kh + s * D + i); },
-                      [&](int s, int i, float x0, float x1, float, float, float2 k, float *) -> float {
-                          const float w = eGnG[s];
-                          st2(dkh + s * D + i, w * x0, w * x1);
-                          return w * (x0 * k.x + x1 * k.y);
-                      },
-                      rkd);
-        }
         // ---- dW = -dU S^T
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kRow, D, D>(acc, sA, sB, dU, D, S, D);
+            pass<kRow, kRow, D, D>(acc, sA, sB, dU, D, nullptr, D);   // S is still staged
             finish<D>(acc, nopre, [&](int s, int i, float x0, float x1, float, float, int, float *) -> float {
                 st2(dW + s * D + i, -x0, -x1);
                 return 0.f;
@@ -565,6 +567,37 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
                             return 0.f;
                         },
                         nullptr, rbv, rbk);
+        }
+        // ---- dA = mask_incl(dO U^T) -> dA (.) E_qk; row and column sums of dA (.) A
+        {
+            Acc<kC> acc;
+            acc.zero();
+            pass<kRow, kRow, kC, D>(acc, sA, sB, dO, D, U, D);
+            finish<kC>(acc, [&](int t, int s) { return ld2(A + t * kC + s); },
+                       [&](int t, int s, float x0, float x1, float, float, float2 av, float *cs) -> float {
+                           const float e0 = s <= t ? __expf(G[t] - G[s]) : 0.f;
+                           const float e1 = s + 1 <= t ? __expf(G[t] - G[s + 1]) : 0.f;
+                           const float d0 = s <= t ? x0 : 0.f, d1 = s + 1 <= t ? x1 : 0.f;
+                           st2(dQK + t * kC + s, d0 * e0, d1 * e1);
+                           const float p0 = d0 * av.x, p1 = d1 * av.y;
+                           cs[0] += p0;
+                           cs[1] += p1;
+                           return p0 + p1;
+                       },
+                       rA, cA);
+        }
+        // ---- dK~ = U dS'^T: dk^ = diag(e^{G_n - G}) dK~ (its first term); row sums K~ . dK~
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kRow, kRow, D, D>(acc, sA, sB, U, D, dSp, D);
+            finish<D>(acc, [&](int s, int i) { return ld2(Kh + s * D + i); },
+                      [&](int s, int i, float x0, float x1, float, float, float2 k, float *) -> float {
+                          const float w = eGnG[s];
+                          st2(dkh + s * D + i, w * x0, w * x1);
+                          return w * (x0 * k.x + x1 * k.y);
+                      },
+                      rkd);
         }
         // ---- X = dT T^T;  dL = -mask_strict(T^T X) -> P = dL (.) beta_t E_kk, with the row sums
         // of dL (.) (k^ k^^T) E_kk and the column sums of dL (.) L
