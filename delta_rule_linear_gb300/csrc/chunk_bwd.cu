@@ -77,6 +77,9 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 __device__ __forceinline__ void st2(float *p, float x, float y) { *reinterpret_cast<float2 *>(p) = make_float2(x, y); }
+__device__ __forceinline__ float rtf(float x) { return __uint_as_float(tf32(x)); }   // rounded to tf32
+// stores an operand that only the tensor cores read, rounded to tf32 as they would round it
+__device__ __forceinline__ void st2r(float *p, float x, float y) { st2(p, rtf(x), rtf(y)); }
 __device__ __forceinline__ float2 ld2(const float *p) { return *reinterpret_cast<const float2 *>(p); }
 
 // Operand layouts in shared memory, for an operand with w rows on its side of the product
@@ -139,12 +142,15 @@ struct Acc {
     }
 };
 
-// acc += A B^T from operands already staged at sa, sb (layouts LA, LB).  Inside a 16-wide k
+// acc += A B^T from operands already staged at sa, sb (layouts LA, LB; RA, RB: the operand's
+// values are already rounded to tf32, so they enter the MMA as they are).  Inside a 16-wide k
 // step lane t4 takes the four consecutive k = 4 t4 .. 4 t4 + 3 on both operands, the first two
 // for one MMA and the last two for the other: the same permutation of k on A and B, which
 // leaves the sum unchanged.
-template <Lay LA, Lay LB, int N, int K>
+template <Lay LA, Lay LB, int N, int K, bool RA = false, bool RB = false>
 __device__ __forceinline__ void mma_staged(Acc<N> &acc, const float *sa, const float *bb) {
+    auto ca = [](float x) { return RA ? __float_as_uint(x) : tf32(x); };
+    auto cb = [](float x) { return RB ? __float_as_uint(x) : tf32(x); };
     constexpr int PA = lay_pitch<LA>(kC, K), PB = lay_pitch<LB>(N, K), NJ = Acc<N>::NJ;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
     const int m0 = (warp >> 2) * 32, n0 = (warp & 3) * Acc<N>::WN;
@@ -157,12 +163,12 @@ __device__ __forceinline__ void mma_staged(Acc<N> &acc, const float *sa, const f
         for (int j = 0; j < NJ; ++j) frag4<LB, PB>(zb[j], bb, n0 + 8 * j + g, k0 + 4 * t4);
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
-            const uint32_t a[4] = {tf32(xa[2 * mi][0]), tf32(xa[2 * mi + 1][0]), tf32(xa[2 * mi][1]), tf32(xa[2 * mi + 1][1])};
-            const uint32_t a2[4] = {tf32(xa[2 * mi][2]), tf32(xa[2 * mi + 1][2]), tf32(xa[2 * mi][3]), tf32(xa[2 * mi + 1][3])};
+            const uint32_t a[4] = {ca(xa[2 * mi][0]), ca(xa[2 * mi + 1][0]), ca(xa[2 * mi][1]), ca(xa[2 * mi + 1][1])};
+            const uint32_t a2[4] = {ca(xa[2 * mi][2]), ca(xa[2 * mi + 1][2]), ca(xa[2 * mi][3]), ca(xa[2 * mi + 1][3])};
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
-                const uint32_t b[2] = {tf32(zb[j][0]), tf32(zb[j][1])};
-                const uint32_t b2[2] = {tf32(zb[j][2]), tf32(zb[j][3])};
+                const uint32_t b[2] = {cb(zb[j][0]), cb(zb[j][1])};
+                const uint32_t b2[2] = {cb(zb[j][2]), cb(zb[j][3])};
                 mma_tf32(acc.d[mi][j], a, b);
                 mma_tf32(acc.d[mi][j], a2, b2);
             }
@@ -176,7 +182,7 @@ __device__ __forceinline__ void mma_staged(Acc<N> &acc, const float *sa, const f
 // the operand once and reads it on both sides.  Begins with a barrier of the CTA, so the
 // stores of the previous epilogue are visible and the previous pass has finished reading the
 // buffers.
-template <Lay LA, Lay LB, int N, int K>
+template <Lay LA, Lay LB, int N, int K, bool RA = false, bool RB = false>
 __device__ __forceinline__ void pass(Acc<N> &acc, float *sA, float *sB, const float *A, int lda, const float *B,
                                      int ldb) {
     const bool same = (A != nullptr && B == A);
@@ -185,7 +191,7 @@ __device__ __forceinline__ void pass(Acc<N> &acc, float *sA, float *sB, const fl
     if (B && !same) stage<LB, N, K>(sB, B, ldb);
     cp_async_wait_all();
     __syncthreads();
-    mma_staged<LA, LB, N, K>(acc, sA, same ? sA : sB);
+    mma_staged<LA, LB, N, K, RA, RB>(acc, sA, same ? sA : sB);
 }
 
 // The epilogue over a product's accumulators (one or two products of the same shape, e.g. two
@@ -295,10 +301,11 @@ __device__ __forceinline__ void ld_bf16(float (&f)[E], const __nv_bfloat16 *p) {
         f[0] = lo(u); f[1] = hi(u);
     }
 }
-template <int E>
+template <int E, bool ROUND = false>
 __device__ __forceinline__ void st_row(float *p, const float (&f)[E], float scale) {
-    if constexpr (E == 4) *reinterpret_cast<float4 *>(p) = make_float4(scale * f[0], scale * f[1], scale * f[2], scale * f[3]);
-    else *reinterpret_cast<float2 *>(p) = make_float2(scale * f[0], scale * f[1]);
+    auto r = [&](float x) { return ROUND ? rtf(scale * x) : scale * x; };
+    if constexpr (E == 4) *reinterpret_cast<float4 *>(p) = make_float4(r(f[0]), r(f[1]), r(f[2]), r(f[3]));
+    else *reinterpret_cast<float2 *>(p) = make_float2(r(f[0]), r(f[1]));
 }
 
 template <int D>
@@ -408,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             const float fqn = a.use_l2 ? 1.f / fmaxf(nq, kNormEpsB) : 1.f;
             const size_t o = (size_t)t * D + E * lane;
             st_row<E>(Kh + o, fk_, fk);
-            st_row<E>(Kt + o, fk_, fk * eGnG[t]);
+            st_row<E, true>(Kt + o, fk_, fk * eGnG[t]);
             st_row<E>(Qh + o, fq_, a.scale * fqn);
             st_row<E>(V + o, fv_, 1.f);
             st_row<E>(dO + o, fo_, 1.f);
@@ -444,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         // ---- T = (I + L)^{-1} in 32 x 32 blocks.  The diagonal blocks by substitution: warp w
         // takes block w, lane j its column j, held in registers; once row s of the column is final
         // its term is subtracted from every later row.  Meanwhile the other warps clear the upper
-        // block.  Then T_BA = -T_BB (L_BA T_AA), L_BA T_AA kept in the L array's unused upper
+        // block and sum S (.) dS'.  Then T_BA = -T_BB (L_BA T_AA), L_BA T_AA kept in the L array's unused upper
         // block.
         if (warp < 2) {
             const int o = 32 * warp;
@@ -459,6 +466,17 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             for (int r = 0; r < 32; ++r) sT[(o + r) * PL + o + lane] = tc[r];
         } else {
             for (int x = tid - 64; x < 32 * 32; x += kThreads - 64) sT[(x >> 5) * PL + 32 + (x & 31)] = 0.f;
+            // e^{G_n} sum(S (.) dS'), a term of the gradient of G_n
+            const float4 *s4 = reinterpret_cast<const float4 *>(S), *d4 = reinterpret_cast<const float4 *>(dSp);
+            float acc = 0.f;
+#pragma unroll 8
+            for (int x = tid - 64; x < D * D / 4; x += kThreads - 64) {
+                const float4 u = s4[x], w = d4[x];
+                acc = fmaf(u.x, w.x, fmaf(u.y, w.y, fmaf(u.z, w.z, fmaf(u.w, w.w, acc))));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0) atomicAdd(&sGn[1], __expf(sGn[0]) * acc);
         }
         __syncthreads();
         {
@@ -485,32 +503,34 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             for (int q = 0; q < 4; ++q) sT[(32 + warp + 8 * q) * PL + lane] = -y[q];
         }
         __syncthreads();
-        // T, and T with its columns scaled: Pv = T diag(beta), Pk = T diag(beta e^R)
+        // T, and T with its columns scaled: Pv = T diag(beta), Pk = T diag(beta e^R) (operands of
+        // the tensor cores alone, stored rounded to tf32, like those the epilogues below store
+        // with st2r)
         for (int x = tid; x < kC * kC; x += kThreads) {
             const int t = x / kC, s = x % kC;
             const float tv = sT[t * PL + s];
             T[x] = tv;
-            Pv[x] = tv * beta[s];
-            Pk[x] = tv * beta[s] * eR[s];
+            Pv[x] = rtf(tv * beta[s]);
+            Pk[x] = rtf(tv * beta[s] * eR[s]);
         }
 
         // ---- forward quantities: W = Pk K^ (kept negated), U = Pv V - W S
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kCol, D, kC>(acc, sA, sB, Pk, kC, Kh, D);
+            pass<kRow, kCol, D, kC, true>(acc, sA, sB, Pk, kC, Kh, D);
             finish<D>(acc, nopre, [&](int t, int j, float x0, float x1, float, float, int, float *) -> float {
-                st2(Wn + t * D + j, -x0, -x1);
+                st2r(Wn + t * D + j, -x0, -x1);
                 return 0.f;
             });
         }
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kCol, D, kC>(acc, sA, sB, Pv, kC, V, D);
-            pass<kRow, kCol, D, D>(acc, sA, sB, Wn, D, S, D);
+            pass<kRow, kCol, D, kC, true>(acc, sA, sB, Pv, kC, V, D);
+            pass<kRow, kCol, D, D, true>(acc, sA, sB, Wn, D, S, D);
             finish<D>(acc, nopre, [&](int t, int j, float x0, float x1, float, float, int, float *) -> float {
-                st2(U + t * D + j, x0, x1);
+                st2r(U + t * D + j, x0, x1);
                 return 0.f;
             });
         }
@@ -519,9 +539,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             Acc<D> acc;
             acc.zero();
             pass<kCol, kCol, D, kC>(acc, sA, sB, A, kC, dO, D);
-            pass<kRow, kCol, D, D>(acc, sA, sB, Kt, D, dSp, D);
+            pass<kRow, kCol, D, D, true>(acc, sA, sB, Kt, D, dSp, D);
             finish<D>(acc, nopre, [&](int s, int j, float x0, float x1, float, float, int, float *) -> float {
-                st2(dU + s * D + j, x0, x1);
+                st2r(dU + s * D + j, x0, x1);
                 return 0.f;
             });
         }
@@ -541,9 +561,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kRow, D, D>(acc, sA, sB, dU, D, nullptr, D);   // S is still staged
+            pass<kRow, kRow, D, D, true>(acc, sA, sB, dU, D, nullptr, D);   // S is still staged
             finish<D>(acc, nopre, [&](int s, int i, float x0, float x1, float, float, int, float *) -> float {
-                st2(dW + s * D + i, -x0, -x1);
+                st2r(dW + s * D + i, -x0, -x1);
                 return 0.f;
             });
         }
@@ -554,12 +574,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             Acc<kC> acc, acc2;
             acc.zero();
             acc2.zero();
-            pass<kRow, kRow, kC, D>(acc, sA, sB, nullptr, D, V, D);   // dU is still staged
-            pass<kRow, kRow, kC, D>(acc2, sA, sB, dW, D, Kh, D);
+            pass<kRow, kRow, kC, D, true>(acc, sA, sB, nullptr, D, V, D);   // dU is still staged
+            pass<kRow, kRow, kC, D, true>(acc2, sA, sB, dW, D, Kh, D);
             finish2<kC>(acc, &acc2, [&](int t, int s) { return ld2(T + t * kC + s); },
                         [&](int t, int s, float x0, float x1, float y0, float y1, float2 tv, float *cs) -> float {
                             const float b0 = beta[s], b1 = beta[s + 1];
-                            st2(dT + t * kC + s, b0 * (x0 + eR[s] * y0), b1 * (x1 + eR[s + 1] * y1));
+                            st2r(dT + t * kC + s, b0 * (x0 + eR[s] * y0), b1 * (x1 + eR[s + 1] * y1));
                             cs[0] += tv.x * x0;
                             cs[1] += tv.y * x1;
                             cs[2] += tv.x * y0;
@@ -572,13 +592,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<kC> acc;
             acc.zero();
-            pass<kRow, kRow, kC, D>(acc, sA, sB, dO, D, U, D);
+            pass<kRow, kRow, kC, D, false, true>(acc, sA, sB, dO, D, U, D);
             finish<kC>(acc, [&](int t, int s) { return ld2(A + t * kC + s); },
                        [&](int t, int s, float x0, float x1, float, float, float2 av, float *cs) -> float {
                            const float e0 = s <= t ? __expf(G[t] - G[s]) : 0.f;
                            const float e1 = s + 1 <= t ? __expf(G[t] - G[s + 1]) : 0.f;
                            const float d0 = s <= t ? x0 : 0.f, d1 = s + 1 <= t ? x1 : 0.f;
-                           st2(dQK + t * kC + s, d0 * e0, d1 * e1);
+                           st2r(dQK + t * kC + s, d0 * e0, d1 * e1);
                            const float p0 = d0 * av.x, p1 = d1 * av.y;
                            cs[0] += p0;
                            cs[1] += p1;
@@ -590,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kRow, D, D>(acc, sA, sB, U, D, dSp, D);
+            pass<kRow, kRow, D, D, true>(acc, sA, sB, U, D, dSp, D);
             finish<D>(acc, [&](int s, int i) { return ld2(Kh + s * D + i); },
                       [&](int s, int i, float x0, float x1, float, float, float2 k, float *) -> float {
                           const float w = eGnG[s];
@@ -604,23 +624,23 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<kC> acc;
             acc.zero();
-            pass<kRow, kRow, kC, kC>(acc, sA, sB, dT, kC, T, kC);
+            pass<kRow, kRow, kC, kC, true>(acc, sA, sB, dT, kC, T, kC);
             finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
-                st2(X + t * kC + s, x0, x1);
+                st2r(X + t * kC + s, x0, x1);
                 return 0.f;
             });
         }
         {
             Acc<kC> acc;
             acc.zero();
-            pass<kCol, kCol, kC, kC>(acc, sA, sB, T, kC, X, kC);
+            pass<kCol, kCol, kC, kC, false, true>(acc, sA, sB, T, kC, X, kC);
             finish<kC>(acc, [&](int t, int s) { return ld2(KKE + t * kC + s); },
                        [&](int t, int s, float x0, float x1, float, float, float2 kk, float *cs) -> float {
                            const float l0 = s < t ? -x0 : 0.f, l1 = s + 1 < t ? -x1 : 0.f;
                            const float e0 = s < t ? __expf(R[t] - G[s]) : 0.f;
                            const float e1 = s + 1 < t ? __expf(R[t] - G[s + 1]) : 0.f;
                            const float bt = beta[t];
-                           st2(P + t * kC + s, l0 * bt * e0, l1 * bt * e1);
+                           st2r(P + t * kC + s, l0 * bt * e0, l1 * bt * e1);
                            const float p0 = l0 * kk.x, p1 = l1 * kk.y;
                            cs[0] += bt * p0;
                            cs[1] += bt * p1;
@@ -633,10 +653,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kCol, kCol, D, kC>(acc, sA, sB, Pk, kC, dW, D);
-            pass<kRow, kCol, D, kC>(acc, sA, sB, P, kC, Kh, D);
-            pass<kCol, kCol, D, kC>(acc, sA, sB, P, kC, nullptr, D);   // K^ is still staged
-            pass<kCol, kCol, D, kC>(acc, sA, sB, dQK, kC, Qh, D);
+            pass<kCol, kCol, D, kC, true, true>(acc, sA, sB, Pk, kC, dW, D);
+            pass<kRow, kCol, D, kC, true>(acc, sA, sB, P, kC, Kh, D);
+            pass<kCol, kCol, D, kC, true>(acc, sA, sB, P, kC, nullptr, D);   // K^ is still staged
+            pass<kCol, kCol, D, kC, true>(acc, sA, sB, dQK, kC, Qh, D);
             finish<D>(acc,
                       [&](int s, int i) {
                           const float2 o = ld2(dkh + s * D + i), k = ld2(Kh + s * D + i);
@@ -653,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kCol, D, kC>(acc, sA, sB, dQK, kC, Kh, D);
+            pass<kRow, kCol, D, kC, true>(acc, sA, sB, dQK, kC, Kh, D);
             finish<D>(acc,
                       [&](int t, int i) {
                           const float2 o = ld2(dqh + t * D + i), q = ld2(Qh + t * D + i);
@@ -679,18 +699,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             dG[t] = dg;
             dGp[t] = dgp;
             dbeta[t] = db;
-        }
-        {   // e^{G_n} sum(S (.) dS')
-            const float4 *s4 = reinterpret_cast<const float4 *>(S), *d4 = reinterpret_cast<const float4 *>(dSp);
-            float acc = 0.f;
-#pragma unroll 8
-            for (int x = tid; x < D * D / 4; x += kThreads) {
-                const float4 u = s4[x], w = d4[x];
-                acc = fmaf(u.x, w.x, fmaf(u.y, w.y, fmaf(u.z, w.z, fmaf(u.w, w.w, acc))));
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0) atomicAdd(&sGn[1], __expf(sGn[0]) * acc);
         }
         __syncthreads();
 
