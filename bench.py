@@ -70,11 +70,13 @@ def recorded_counters(kind):
     return rec
 
 
-def record_counters(kind, csv_path, kernel_regex, scale=1.0, note=""):
-    """Parse an ncu --csv capture (raw page or --metrics list), average the DRAM bytes and
-    tensor-pipe activity over the launches of the kernels matching `kernel_regex`, scale
-    the bytes to one full launch (`scale`: units of the full launch / units captured) and
-    store them with the current hash of the kernel's sources."""
+KEPT_METRICS = ("dram__bytes_read.sum", "dram__bytes_write.sum",
+                "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active")
+
+
+def _capture_metrics(csv_path, kernel_regex):
+    """{launch: {metric: value}} for the DRAM-byte and tensor-pipe metrics of the launches
+    of kernels matching kernel_regex in an ncu --csv file (raw page or --metrics list)."""
     import csv
     import re
     rows = list(csv.reader(open(csv_path, newline="")))
@@ -87,15 +89,32 @@ def record_counters(kind, csv_path, kernel_regex, scale=1.0, note=""):
         for r in rows[head_i + 1:]:
             if len(r) > vcol and re.search(kernel_regex, r[kcol]):
                 launches.setdefault(r[idcol], {})[r[mcol]] = float(r[vcol].replace(",", ""))
-    else:                       # raw page: one row per launch, one column per metric
+    else:                       # raw page: one row per launch, one column per metric, a units row
+        units = rows[head_i + 1]
+        mult = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
         for n, r in enumerate(rows[head_i + 2:]):
             if len(r) > kcol and re.search(kernel_regex, r[kcol]):
-                launches[n] = {m: float(r[i].replace(",", "")) for i, m in enumerate(head)
-                               if m.startswith(("dram__bytes", "sm__pipe_tensor")) and r[i].strip()}
+                launches[n] = {m: float(r[i].replace(",", "")) * mult.get(units[i], 1.0)
+                               for i, m in enumerate(head) if m in KEPT_METRICS and r[i].strip()}
+    return {k: {m: v for m, v in l.items() if m in KEPT_METRICS} for k, l in launches.items()}
+
+
+def record_counters(kind, csv_path, kernel_regex, scale=1.0, note="", tensor_csv=None):
+    """Parse an ncu --csv capture (raw page or --metrics list), average the DRAM bytes and
+    tensor-pipe activity over the launches of the kernels matching `kernel_regex`, scale
+    the bytes to one full launch (`scale`: units of the full launch / units captured) and
+    store them with the current hash of the kernel's sources.  `tensor_csv`: a second
+    capture (e.g. a full set on a smaller case) that supplies the tensor-pipe activity."""
+    import csv
+    import re
+    if tensor_csv:
+        tp_only = _capture_metrics(tensor_csv, kernel_regex)
+    launches = _capture_metrics(csv_path, kernel_regex)
     if not launches:
         raise SystemExit(f"no launch of {kernel_regex!r} in {csv_path}")
     rd = [l.get("dram__bytes_read.sum", 0.0) + l.get("dram__bytes_write.sum", 0.0) for l in launches.values()]
-    tp = [l[m] for l in launches.values() for m in l if m.startswith("sm__pipe_tensor_cycles_active")]
+    tp = [l[m] for l in (tp_only if tensor_csv else launches).values() for m in l
+          if m.startswith("sm__pipe_tensor_cycles_active")]
     try:
         with open(COUNTERS_FILE) as f:
             allrec = json.load(f)
@@ -302,12 +321,31 @@ def prefill_workload(args):
     return wl
 
 
-def tc_prefill_launches(B, H, dev):
-    """Kernels of ours per tensor-core chunked prefill call: one when the (sequence, head)
-    pairs fit in half of the SMs (single cooperative launch), else prep + chain."""
-    import torch
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    return 1 if B * H <= sms // 2 else 2
+# Kernels of ours per call.  The tensor-core prefill is one cooperative launch of tc_kernel
+# (its ring flags are cleared by a cudaMemsetAsync, not a kernel of ours); packed varlen adds
+# the kernel that orders the sequences longest first; the chunked backward is three launches
+# (the forward keeping every chunk's map and state, the reverse walk, the chunk-local
+# gradients); the token-by-token backward is three (checkpoints, reverse walk, finish).
+TC_PREFILL_LAUNCHES, VARLEN_LAUNCHES, CHUNK_BWD_LAUNCHES, RECURRENT_BWD_LAUNCHES = 1, 2, 3, 3
+
+
+def prefill_min_bytes(tokens, H, dk, dv, has_decay, nseq, h0_in):
+    """Bytes a prefill call cannot avoid: q, k, v read and o written once (bf16), beta (and
+    the decay) read once, the final state written (and the initial state read) once."""
+    per_token_head = (2 * dk + 2 * dv) * 2 + 4 + (4 if has_decay else 0)
+    return tokens * H * per_token_head + nseq * H * dk * dv * 4 * (2 if h0_in else 1)
+
+
+def memory_ceiling(flops, min_bytes, ms, peaks):
+    """How the call stands against HBM: the achieved bandwidth on its minimum bytes as a
+    fraction of the measured HBM peak, and the tensor fraction it could reach at most if it
+    moved exactly those bytes at that peak (the FLOP time over the larger of the FLOP and
+    byte times)."""
+    t_flops = flops / (peaks["bf16_tflops"] * 1e12)
+    t_bytes = min_bytes / (peaks["hbm_gbs"] * 1e9)
+    return {"min_bytes": int(min_bytes),
+            "hbm_frac_of_min_bytes": round(min_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5),
+            "tc_frac_ceiling_at_hbm_peak": round(t_flops / max(t_flops, t_bytes), 4)}
 
 
 def bench_prefill(args, world, rank, dev, peaks, d):
@@ -427,15 +465,20 @@ def bench_prefill(args, world, rank, dev, peaks, d):
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "pipelining": "H2D, kernels and D2H on three streams, two buffer sets",
                 "host_cpus": host_cpus},
-        "gpu_launches": args.steps * tc_prefill_launches(B, H, dev),
+        "gpu_launches": args.steps * TC_PREFILL_LAUNCHES,
         "shape": dict(B=B, T=T, H=H, dk=dk, dv=dv, chunk=C),
     }
 
 
 # --------------------------------------------------------------------------- other prefill configs
-def bench_secondary(args, world, rank, dev, peaks):
-    """The training-shape prefill (workload 2) and the packed varlen prefill (workload 5),
-    reported beside the headline: tokens/s and counted FLOPs against the bf16 peak."""
+SECONDARY_PARTS = ("training", "backward", "gated", "varlen")
+
+
+def bench_secondary(args, world, rank, dev, peaks, parts=SECONDARY_PARTS):
+    """The training-shape prefill (workload 2) and its backward, the long-sequence prefill
+    with the gate prologues, and the packed varlen prefill (workload 5), reported beside the
+    headline: tokens/s and counted FLOPs against the bf16 peak.  `parts` selects a subset
+    (profiling captures)."""
     import torch
     import delta_rule_linear_gb300 as kda
     from delta_rule_linear_gb300 import _lib
@@ -463,28 +506,59 @@ def bench_secondary(args, world, rank, dev, peaks):
     hT = torch.empty((wl.B, wl.H, wl.dk, wl.dv), dtype=torch.float32, device=dev)
     ws = torch.empty(_lib.chunk_fwd_workspace_bytes(wl.B, wl.T, wl.H, wl.dk, wl.dv, wl.chunk,
                                                     _lib.KDA_BF16), dtype=torch.uint8, device=dev)
+    if "training" in parts:
+        training_prefill(out, timed, kda, wl, q, k, v, beta, decay, o, hT, ws, stream, world, peaks)
+    if "backward" in parts:
+        training_backward(out, timed, kda, _lib, wl, q, k, v, beta, decay, o, stream, dev, world)
+    del q, k, v, beta, decay, o, hT, ws
+    if "gated" in parts:
+        gated_prefill(out, timed, kda, _lib, rank, dev, stream, world)
+    if "varlen" in parts:
+        varlen_prefill(out, timed, kda, _lib, rank, dev, stream, world, peaks)
+    return out
+
+
+def training_prefill(out, timed, kda, wl, q, k, v, beta, decay, o, hT, ws, stream, world, peaks):
     ms = timed(lambda: kda.chunk_fwd(q, k, v, beta, decay, None, chunk_size=wl.chunk, out=o,
                                      final_state=hT, workspace=ws, stream=stream))
     flops = counted_prefill_flops(wl.B, wl.T, wl.H, wl.dk, wl.dv, wl.chunk)
     out["training_prefill"] = {
         "workload": wl.name, "ms_per_call": ms, "tokens_per_s": wl.B * wl.T * world / (ms * 1e-3),
         "tc_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
-        "gpu_launches_per_call": tc_prefill_launches(wl.B, wl.H, dev)}
+        **memory_ceiling(flops, prefill_min_bytes(wl.B * wl.T, wl.H, wl.dk, wl.dv, True, wl.B, False), ms, peaks),
+        "gpu_launches_per_call": TC_PREFILL_LAUNCHES}
 
+
+def training_backward(out, timed, kda, _lib, wl, q, k, v, beta, decay, o, stream, dev, world):
+    import torch
     # the backward of the same call (one decay per head): gradients for q, k, v, beta, the
-    # decay and the initial state, token by token
+    # decay and the initial state, by chunks on the tensor cores and token by token
     d_o = torch.randn_like(o)
     h0z = torch.zeros((wl.B, wl.H, wl.dk, wl.dv), dtype=torch.float32, device=dev)
+    wsc = torch.empty(_lib.load().kda_chunk_bwd_workspace(wl.B, wl.T, wl.H, wl.dk, wl.dv),
+                      dtype=torch.uint8, device=dev)
+    cms = timed(lambda: kda.chunk_bwd(q, k, v, beta, decay, h0z, d_o, None, workspace=wsc, stream=stream))
+    out["training_backward"] = {
+        "workload": wl.name + ", backward", "ms_per_call": cms,
+        "tokens_per_s": wl.B * wl.T * world / (cms * 1e-3), "gpu_launches_per_call": CHUNK_BWD_LAUNCHES,
+        "workspace_bytes": int(wsc.numel()),
+        "note": "chunked on the tensor cores: the forward keeping every chunk's map and fp32 state, "
+                "the reverse walk over the maps (dv, state gradients), the chunk-local gradients "
+                "(tf32 warp MMAs, persistent CTAs)"}
+    del wsc
     wsb = torch.empty(_lib.load().kda_recurrent_bwd_workspace(wl.B, wl.T, wl.H, wl.dk, wl.dv),
                       dtype=torch.uint8, device=dev)
     bms = timed(lambda: kda.recurrent_bwd(q, k, v, beta, decay, h0z, d_o, None, workspace=wsb,
                                           stream=stream))
-    out["training_backward"] = {
+    out["training_backward_recurrent"] = {
         "workload": wl.name + ", backward", "ms_per_call": bms,
-        "tokens_per_s": wl.B * wl.T * world / (bms * 1e-3), "gpu_launches_per_call": 3,
+        "tokens_per_s": wl.B * wl.T * world / (bms * 1e-3), "gpu_launches_per_call": RECURRENT_BWD_LAUNCHES,
         "note": "token by token on CUDA cores: 32-token checkpoints, recompute, reverse walk"}
     del d_o, h0z, wsb
 
+
+def gated_prefill(out, timed, kda, _lib, rank, dev, stream, world):
+    import torch
     # the long-sequence workload with the prologues in the kernel: decay from a raw gate
     # (kda_decay), beta from logits (sigmoid), the decayed read
     wl = WORKLOADS[3]
@@ -503,9 +577,12 @@ def bench_secondary(args, world, rank, dev, peaks):
     out["gated_long_prefill"] = {
         "workload": wl.name + ", raw gate + beta logits + decayed read in the kernel",
         "ms_per_call": ms, "tokens_per_s": wl.B * wl.T * world / (ms * 1e-3),
-        "gpu_launches_per_call": tc_prefill_launches(wl.B, wl.H, dev)}
+        "gpu_launches_per_call": TC_PREFILL_LAUNCHES}
     del q, k, v, braw, graw, al, db, h0, o, hT, ws
 
+
+def varlen_prefill(out, timed, kda, _lib, rank, dev, stream, world, peaks):
+    import torch
     wl = WORKLOADS[5]
     d = make_varlen(wl, seed=rank)
     q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
@@ -525,9 +602,8 @@ def bench_secondary(args, world, rank, dev, peaks):
         "workload": wl.name, "tokens": total, "ms_per_call": ms,
         "tokens_per_s": total * world / (ms * 1e-3),
         "tc_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
-        # the chunk table, then prep and chain (N*H = 256 pairs exceed half the SMs)
-        "gpu_launches_per_call": 1 + tc_prefill_launches(N, wl.H, dev)}
-    return out
+        **memory_ceiling(flops, prefill_min_bytes(total, wl.H, wl.dk, wl.dv, False, N, False), ms, peaks),
+        "gpu_launches_per_call": VARLEN_LAUNCHES}
 
 
 # --------------------------------------------------------------------------- per-channel decay
@@ -571,7 +647,7 @@ def bench_gk_chunk(args, world, rank, dev, peaks, out, D, e0, e1, long_only):
             "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D, chunk=64), "decayed_read": True,
             "ms_per_call": ms, "tokens_per_s": Bp * T * world / (ms * 1e-3),
             "tc_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
-            "gpu_launches_per_call": tc_prefill_launches(Bp, Hp, dev)}
+            "gpu_launches_per_call": TC_PREFILL_LAUNCHES}
         del q, k, v, beta, g, h0, o, hT, ws
     return out
 
@@ -667,7 +743,7 @@ def bench_gk(args, world, rank, dev, peaks):
     bms = max_over_ranks(e0.elapsed_time(e1) / nrep, world)
     out["gk_recurrent_bwd"] = {
         "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D), "decayed_read": True, "ms_per_call": bms,
-        "tokens_per_s": Bp * T * world / (bms * 1e-3), "calls": nrep, "gpu_launches_per_call": 3,
+        "tokens_per_s": Bp * T * world / (bms * 1e-3), "calls": nrep, "gpu_launches_per_call": RECURRENT_BWD_LAUNCHES,
         "note": "token by token on CUDA cores: 32-token checkpoints, recompute, reverse walk"}
     out["gk_recurrent_prefill"] = {
         "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D), "decayed_read": True, "ms_per_call": ms,
@@ -746,7 +822,7 @@ def bench_layouts(args, world, rank, dev, peaks):
     out["grouped_heads_prefill"] = {
         "shape": dict(B=B, T=T, qk_heads=H, v_heads=H * m, dk=D, dv=D, chunk=64), "ms_per_call": ms,
         "tokens_per_s": B * T * world / (ms * 1e-3),
-        "gpu_launches_per_call": tc_prefill_launches(B, H * m, dev)}
+        "gpu_launches_per_call": TC_PREFILL_LAUNCHES}
     return out
 
 
@@ -863,8 +939,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "secondary", "gk", "gk_prefill"], default=None,
-                    help="run one workload (profiling); the default runs both")
+    ap.add_argument("--only", choices=["prefill", "decode", "secondary", "gk", "gk_prefill"] + list(SECONDARY_PARTS),
+                    default=None,
+                    help="run one workload (profiling); the default runs them all")
     ap.add_argument("--prefill-T", type=int, default=0,
                     help="profiling only: override T of the prefill workload (no CPU baseline)")
     ap.add_argument("--record-counters", nargs=3, metavar=("KIND", "CSV", "KERNEL_REGEX"),
@@ -873,10 +950,12 @@ def main():
     ap.add_argument("--scale", type=float, default=1.0,
                     help="with --record-counters: full-launch units / captured units")
     ap.add_argument("--note", default="", help="with --record-counters: the capture command")
+    ap.add_argument("--tensor-csv", default=None,
+                    help="with --record-counters: a second capture that supplies the tensor-pipe activity")
     args = ap.parse_args()
     if args.record_counters:
         kind, csv_path, regex = args.record_counters
-        record_counters(kind, csv_path, regex, args.scale, args.note)
+        record_counters(kind, csv_path, regex, args.scale, args.note, args.tensor_csv)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -913,6 +992,8 @@ def main():
     pre = bench_prefill(args, world, rank, dev, peaks, d) if d is not None else None
     dec = bench_decode(args, world, rank, dev, peaks) if args.only in (None, "decode") else None
     sec = bench_secondary(args, world, rank, dev, peaks) if args.only in (None, "secondary") else None
+    if args.only in SECONDARY_PARTS:
+        sec = bench_secondary(args, world, rank, dev, peaks, parts=(args.only,))
     if args.only in (None, "secondary", "gk", "gk_prefill"):
         sec = dict(sec or {}, kda_gk=bench_gk(args, world, rank, dev, peaks))
     if args.only in (None, "secondary"):
