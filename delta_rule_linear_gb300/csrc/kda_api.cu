@@ -609,7 +609,8 @@ static size_t chunk_bwd_layout(int B, int T, int H, int d, size_t *off_states, s
     if (off_states) *off_states = kWsHeader + keep;
     if (off_dstates) *off_dstates = kWsHeader + keep + st;
     if (off_scratch) *off_scratch = kWsHeader + keep + 2 * st;
-    return kWsHeader + keep + 2 * st + (size_t)chunk_bwd_ctas() * chunk_bwd_scratch_floats(d) * sizeof(float);
+    const long nchunks = (long)B * H * ((T + 63) / 64);
+    return kWsHeader + keep + 2 * st + (size_t)chunk_bwd_ctas(nchunks) * chunk_bwd_scratch_floats(d) * sizeof(float);
 }
 
 size_t kda_chunk_bwd_workspace(int B, int T, int H, int dk, int dv) {
@@ -668,7 +669,7 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
     g.B = B; g.T = T; g.H = H; g.D = dk;
     g.scale = a.scale; g.use_l2 = a.use_l2; g.decayed_read = a.decayed_read;
     g.scratch = reinterpret_cast<float *>(w + o_scr);
-    g.ctas = chunk_bwd_ctas();
+    g.ctas = chunk_bwd_ctas((long)B * H * ((T + 63) / 64));
     if (!decay && ddecay &&   // ddecay without a decay: a zero gradient
         cudaMemsetAsync(ddecay, 0, (size_t)rows * H * sizeof(float), st) != cudaSuccess)
         return KDA_ERR_CUDA;

@@ -113,7 +113,7 @@ struct ChunkBwdArgs {
     int ctas;
 };
 size_t chunk_bwd_scratch_floats(int D);
-int chunk_bwd_ctas();
+int chunk_bwd_ctas(long nchunks);   // persistent CTAs of the gradient kernel
 cudaError_t launch_chunk_bwd_grads(const ChunkBwdArgs &a, cudaStream_t s);
 // Device address of kda_chunk_fwd_noalloc's built-in scratch array on the current device
 // (its first bytes are a workspace header).
