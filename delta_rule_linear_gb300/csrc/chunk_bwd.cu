@@ -306,8 +306,8 @@ __device__ __forceinline__ void finish(const Acc<N> &acc, Pre pre, Epi epi, floa
 // The CTA's scratch, in floats: 64 x D and 64 x 64 matrices (row-major).
 template <int D>
 struct Scr {
-    enum { Kh, Qh, Kt, Wn, U, dU, dW, dkh, dqh, NBig };   // (v and dO are read in place)
-    enum { KKE, A, T, Pv, Pk, dT, X, P, dQK, NSmall };
+    enum { Kh, Qh, Kt, U, dU, dW, dkh, dqh, NBig };   // (v and dO are read in place)
+    enum { KKE, A, T, Pv, Pk, P, dQK, NSmall };      // (-W, dT and X go straight to shared memory)
     static constexpr size_t big(int i) { return (size_t)i * kC * D; }
     static constexpr size_t small(int i) { return (size_t)NBig * kC * D + (size_t)i * kC * kC; }
     static constexpr size_t floats = small(NSmall);
@@ -373,10 +373,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
     auto big = [&](int i) { return sc + Sc::big(i); };
     auto sml = [&](int i) { return sc + Sc::small(i); };
     float *Kh = big(Sc::Kh), *Qh = big(Sc::Qh), *Kt = big(Sc::Kt);
-    float *Wn = big(Sc::Wn), *U = big(Sc::U), *dU = big(Sc::dU), *dW = big(Sc::dW);
+    float *U = big(Sc::U), *dU = big(Sc::dU), *dW = big(Sc::dW);
     float *dkh = big(Sc::dkh), *dqh = big(Sc::dqh);
     float *KKE = sml(Sc::KKE), *A = sml(Sc::A), *T = sml(Sc::T), *Pv = sml(Sc::Pv), *Pk = sml(Sc::Pk);
-    float *dT = sml(Sc::dT), *X = sml(Sc::X), *P = sml(Sc::P), *dQK = sml(Sc::dQK);
+    float *P = sml(Sc::P), *dQK = sml(Sc::dQK);
     auto nopre = [](int, int) { return 0; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -557,21 +557,23 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             Pk[x] = rtf(tv * beta[s] * eR[s]);
         }
 
-        // ---- forward quantities: W = Pk K^ (kept negated), U = Pv V - W S
+        // ---- forward quantities: W = Pk K^, negated straight into the A buffer of the next
+        // product (once every warp is done reading it), U = -W S + Pv V
         {
             Acc<D> acc;
             acc.zero();
             pass<kRow, kCol, D, kC, true>(acc, sA, sB, Pk, kC, Kh, D);
+            __syncthreads();
             finish<D>(acc, nopre, [&](int t, int j, float x0, float x1, float, float, int, float *) -> float {
-                st2r(Wn + t * D + j, -x0, -x1);
+                st2r(sA + t * (D + 16) + j, -x0, -x1);   // kRow, contraction D
                 return 0.f;
             });
         }
         {
             Acc<D> acc;
             acc.zero();
+            pass<kRow, kCol, D, D, true>(acc, sA, sB, nullptr, D, S, D);   // -W is staged
             pass<kRow, kColH, D, kC, true>(acc, sA, sB, Pv, kC, V, ldt, 1 << 30, nv);
-            pass<kRow, kCol, D, D, true>(acc, sA, sB, Wn, D, S, D);
             finish<D>(acc, nopre, [&](int t, int j, float x0, float x1, float, float, int, float *) -> float {
                 st2r(U + t * D + j, x0, x1);
                 return 0.f;
@@ -619,10 +621,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             acc2.zero();
             pass<kRow, kRowH, kC, D, true>(acc, sA, sB, nullptr, D, V, ldt, 1 << 30, nv);   // dU is still staged
             pass<kRow, kRow, kC, D, true>(acc2, sA, sB, dW, D, Kh, D);
+            __syncthreads();   // dT goes straight into the A buffer of X = dT T^T
             finish2<kC>(acc, &acc2, [&](int t, int s) { return ld2(T + t * kC + s); },
                         [&](int t, int s, float x0, float x1, float y0, float y1, float2 tv, float *cs) -> float {
                             const float b0 = beta[s], b1 = beta[s + 1];
-                            st2r(dT + t * kC + s, b0 * (x0 + eR[s] * y0), b1 * (x1 + eR[s + 1] * y1));
+                            st2r(sA + t * (kC + 16) + s, b0 * (x0 + eR[s] * y0), b1 * (x1 + eR[s + 1] * y1));
                             cs[0] += tv.x * x0;
                             cs[1] += tv.y * x1;
                             cs[2] += tv.x * y0;
@@ -630,6 +633,37 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
                             return 0.f;
                         },
                         nullptr, rbv, rbk);
+        }
+        // ---- X = dT T^T;  dL = -mask_strict(T^T X) -> P = dL (.) beta_t E_kk, with the row sums
+        // of dL (.) (k^ k^^T) E_kk and the column sums of dL (.) L
+        {
+            Acc<kC> acc;
+            acc.zero();
+            pass<kRow, kRow, kC, kC, true>(acc, sA, sB, nullptr, kC, T, kC);   // dT is staged
+            __syncthreads();   // X goes straight into the B buffer of T^T X (kCol: X[r][s] at r (64 + 2) + s)
+            finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
+                sB[t * (kC + 2) + s] = rtf(x0);
+                sB[t * (kC + 2) + s + 1] = rtf(x1);
+                return 0.f;
+            });
+        }
+        {
+            Acc<kC> acc;
+            acc.zero();
+            pass<kCol, kCol, kC, kC, false, true>(acc, sA, sB, T, kC, nullptr, kC);   // X is staged
+            finish<kC>(acc, [&](int t, int s) { return ld2(KKE + t * kC + s); },
+                       [&](int t, int s, float x0, float x1, float, float, float2 kk, float *cs) -> float {
+                           const float l0 = s < t ? -x0 : 0.f, l1 = s + 1 < t ? -x1 : 0.f;
+                           const float e0 = s < t ? __expf(R[t] - G[s]) : 0.f;
+                           const float e1 = s + 1 < t ? __expf(R[t] - G[s + 1]) : 0.f;
+                           const float bt = beta[t];
+                           st2r(P + t * kC + s, l0 * bt * e0, l1 * bt * e1);
+                           const float p0 = l0 * kk.x, p1 = l1 * kk.y;
+                           cs[0] += bt * p0;
+                           cs[1] += bt * p1;
+                           return p0 + p1;
+                       },
+                       rLK, cL);
         }
         // ---- dA = mask_incl(dO U^T) -> dA (.) E_qk; row and column sums of dA (.) A
         {
@@ -661,35 +695,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
                           return w * (x0 * k.x + x1 * k.y);
                       },
                       rkd);
-        }
-        // ---- X = dT T^T;  dL = -mask_strict(T^T X) -> P = dL (.) beta_t E_kk, with the row sums
-        // of dL (.) (k^ k^^T) E_kk and the column sums of dL (.) L
-        {
-            Acc<kC> acc;
-            acc.zero();
-            pass<kRow, kRow, kC, kC, true>(acc, sA, sB, dT, kC, T, kC);
-            finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
-                st2r(X + t * kC + s, x0, x1);
-                return 0.f;
-            });
-        }
-        {
-            Acc<kC> acc;
-            acc.zero();
-            pass<kCol, kCol, kC, kC, false, true>(acc, sA, sB, T, kC, X, kC);
-            finish<kC>(acc, [&](int t, int s) { return ld2(KKE + t * kC + s); },
-                       [&](int t, int s, float x0, float x1, float, float, float2 kk, float *cs) -> float {
-                           const float l0 = s < t ? -x0 : 0.f, l1 = s + 1 < t ? -x1 : 0.f;
-                           const float e0 = s < t ? __expf(R[t] - G[s]) : 0.f;
-                           const float e1 = s + 1 < t ? __expf(R[t] - G[s + 1]) : 0.f;
-                           const float bt = beta[t];
-                           st2r(P + t * kC + s, l0 * bt * e0, l1 * bt * e1);
-                           const float p0 = l0 * kk.x, p1 = l1 * kk.y;
-                           cs[0] += bt * p0;
-                           cs[1] += bt * p1;
-                           return p0 + p1;
-                       },
-                       rLK, cL);
         }
         // ---- dk^ += Pk^T dW + P K^ + P^T K^ + (dA (.) E_qk)^T Q~  (Pk^T dW = diag(beta e^R) T^T dW);
         // row sums k^ . dk^
