@@ -78,7 +78,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 __device__ __forceinline__ void st2(float *p, float x, float y) { *reinterpret_cast<float2 *>(p) = make_float2(x, y); }
 __device__ __forceinline__ float rtf(float x) { return __uint_as_float(tf32(x)); }   // rounded to tf32
-// stores an operand that only the tensor cores read, rounded to tf32 as they would round it
+// stores an operand of the tensor cores, rounded to tf32 as they would round it
 __device__ __forceinline__ void st2r(float *p, float x, float y) { st2(p, rtf(x), rtf(y)); }
 __device__ __forceinline__ float2 ld2(const float *p) { return *reinterpret_cast<const float2 *>(p); }
 
@@ -185,15 +185,16 @@ struct Acc {
     }
 };
 
-// acc += A B^T from operands already staged at sa, sb (layouts LA, LB; RA, RB: the operand's
-// values are already rounded to tf32, so they enter the MMA as they are).  Inside a 16-wide k
+// acc += A B^T from operands already staged at sa, sb (layouts LA, LB).  Every operand's values
+// are tf32 already (stored rounded by their producers, or bf16), so they enter the MMA as
+// they are.  Inside a 16-wide k
 // step lane t4 takes the four consecutive k = 4 t4 .. 4 t4 + 3 on both operands, the first two
 // for one MMA and the last two for the other: the same permutation of k on A and B, which
 // leaves the sum unchanged.
-template <Lay LA, Lay LB, int N, int K, bool RA = false, bool RB = false>
+template <Lay LA, Lay LB, int N, int K>
 __device__ __forceinline__ void mma_staged(Acc<N> &acc, const float *sa, const float *bb) {
-    auto ca = [](float x) { return (RA || lay_bf16<LA>()) ? __float_as_uint(x) : tf32(x); };
-    auto cb = [](float x) { return (RB || lay_bf16<LB>()) ? __float_as_uint(x) : tf32(x); };
+    auto ca = [](float x) { return __float_as_uint(x); };
+    auto cb = [](float x) { return __float_as_uint(x); };
     constexpr int PA = lay_pitch<LA>(kC, K), PB = lay_pitch<LB>(N, K), NJ = Acc<N>::NJ;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
     const int m0 = (warp >> 2) * 32, n0 = (warp & 3) * Acc<N>::WN;
@@ -225,7 +226,7 @@ __device__ __forceinline__ void mma_staged(Acc<N> &acc, const float *sa, const f
 // the operand once and reads it on both sides; va, vb: the valid rows of a bf16 operand.  Begins with a barrier of the CTA, so the
 // stores of the previous epilogue are visible and the previous pass has finished reading the
 // buffers.
-template <Lay LA, Lay LB, int N, int K, bool RA = false, bool RB = false>
+template <Lay LA, Lay LB, int N, int K>
 __device__ __forceinline__ void pass(Acc<N> &acc, float *sA, float *sB, const void *A, int lda, const void *B,
                                      int ldb, int va = 1 << 30, int vb = 1 << 30) {
     const bool same = (A != nullptr && B == A);
@@ -234,7 +235,7 @@ __device__ __forceinline__ void pass(Acc<N> &acc, float *sA, float *sB, const vo
     if (B && !same) stage<LB, N, K>(sB, B, ldb, vb);
     cp_async_wait_all();
     __syncthreads();
-    mma_staged<LA, LB, N, K, RA, RB>(acc, sA, same ? sA : sB);
+    mma_staged<LA, LB, N, K>(acc, sA, same ? sA : sB);
 }
 
 // The epilogue over a product's accumulators (one or two products of the same shape, e.g. two
@@ -459,9 +460,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             const float fk = a.use_l2 ? 1.f / fmaxf(nk, kNormEpsB) : 1.f;
             const float fqn = a.use_l2 ? 1.f / fmaxf(nq, kNormEpsB) : 1.f;
             const size_t o = (size_t)t * D + E * lane;
-            st_row<E>(Kh + o, fk_, fk);
+            st_row<E, true>(Kh + o, fk_, fk);
             st_row<E, true>(Kt + o, fk_, fk * eGnG[t]);
-            st_row<E>(Qh + o, fq_, a.scale * fqn);
+            st_row<E, true>(Qh + o, fq_, a.scale * fqn);
             if (lane == 0) {   // the normalisation factors, negative where its adjoint is the identity
                 kn[t] = (a.use_l2 && nk > kNormEpsB) ? fk : -fk;
                 qn[t] = (a.use_l2 && nq > kNormEpsB) ? fqn : -fqn;
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             mma_staged<kRow, kRow, kC, D>(acck, sB, sB);
             finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
                 const float e0 = s <= t ? __expf(G[t] - G[s]) : 0.f, e1 = s + 1 <= t ? __expf(G[t] - G[s + 1]) : 0.f;
-                st2(A + t * kC + s, x0 * e0, x1 * e1);
+                st2r(A + t * kC + s, x0 * e0, x1 * e1);
                 return 0.f;
             });
             // (every warp is past both products: the staged k^ may be overwritten)
@@ -546,13 +547,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             for (int q = 0; q < 4; ++q) sT[(32 + warp + 8 * q) * PL + lane] = -y[q];
         }
         __syncthreads();
-        // T, and T with its columns scaled: Pv = T diag(beta), Pk = T diag(beta e^R) (operands of
-        // the tensor cores alone, stored rounded to tf32, like those the epilogues below store
-        // with st2r)
+        // T, and T with its columns scaled: Pv = T diag(beta), Pk = T diag(beta e^R), stored
+        // rounded to tf32 like every operand of the products (k^, q~, A and the epilogues' st2r
+        // outputs; the walks store the states rounded)
         for (int x = tid; x < kC * kC; x += kThreads) {
             const int t = x / kC, s = x % kC;
             const float tv = sT[t * PL + s];
-            T[x] = tv;
+            T[x] = rtf(tv);
             Pv[x] = rtf(tv * beta[s]);
             Pk[x] = rtf(tv * beta[s] * eR[s]);
         }
@@ -562,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kCol, D, kC, true>(acc, sA, sB, Pk, kC, Kh, D);
+            pass<kRow, kCol, D, kC>(acc, sA, sB, Pk, kC, Kh, D);
             __syncthreads();
             finish<D>(acc, nopre, [&](int t, int j, float x0, float x1, float, float, int, float *) -> float {
                 st2r(sA + t * (D + 16) + j, -x0, -x1);   // kRow, contraction D
@@ -572,8 +573,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kCol, D, D, true>(acc, sA, sB, nullptr, D, S, D);   // -W is staged
-            pass<kRow, kColH, D, kC, true>(acc, sA, sB, Pv, kC, V, ldt, 1 << 30, nv);
+            pass<kRow, kCol, D, D>(acc, sA, sB, nullptr, D, S, D);   // -W is staged
+            pass<kRow, kColH, D, kC>(acc, sA, sB, Pv, kC, V, ldt, 1 << 30, nv);
             finish<D>(acc, nopre, [&](int t, int j, float x0, float x1, float, float, int, float *) -> float {
                 st2r(U + t * D + j, x0, x1);
                 return 0.f;
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             Acc<D> acc;
             acc.zero();
             pass<kCol, kColH, D, kC>(acc, sA, sB, A, kC, dO, ldt, 1 << 30, nv);
-            pass<kRow, kCol, D, D, true>(acc, sA, sB, Kt, D, dSp, D);
+            pass<kRow, kCol, D, D>(acc, sA, sB, Kt, D, dSp, D);
             finish<D>(acc, nopre, [&](int s, int j, float x0, float x1, float, float, int, float *) -> float {
                 st2r(dU + s * D + j, x0, x1);
                 return 0.f;
@@ -606,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kRow, D, D, true>(acc, sA, sB, dU, D, nullptr, D);   // S is still staged
+            pass<kRow, kRow, D, D>(acc, sA, sB, dU, D, nullptr, D);   // S is still staged
             finish<D>(acc, nopre, [&](int s, int i, float x0, float x1, float, float, int, float *) -> float {
                 st2r(dW + s * D + i, -x0, -x1);
                 return 0.f;
@@ -619,8 +620,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             Acc<kC> acc, acc2;
             acc.zero();
             acc2.zero();
-            pass<kRow, kRowH, kC, D, true>(acc, sA, sB, nullptr, D, V, ldt, 1 << 30, nv);   // dU is still staged
-            pass<kRow, kRow, kC, D, true>(acc2, sA, sB, dW, D, Kh, D);
+            pass<kRow, kRowH, kC, D>(acc, sA, sB, nullptr, D, V, ldt, 1 << 30, nv);   // dU is still staged
+            pass<kRow, kRow, kC, D>(acc2, sA, sB, dW, D, Kh, D);
             __syncthreads();   // dT goes straight into the A buffer of X = dT T^T
             finish2<kC>(acc, &acc2, [&](int t, int s) { return ld2(T + t * kC + s); },
                         [&](int t, int s, float x0, float x1, float y0, float y1, float2 tv, float *cs) -> float {
@@ -639,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<kC> acc;
             acc.zero();
-            pass<kRow, kRow, kC, kC, true>(acc, sA, sB, nullptr, kC, T, kC);   // dT is staged
+            pass<kRow, kRow, kC, kC>(acc, sA, sB, nullptr, kC, T, kC);   // dT is staged
             __syncthreads();   // X goes straight into the B buffer of T^T X (kCol: X[r][s] at r (64 + 2) + s)
             finish<kC>(acc, nopre, [&](int t, int s, float x0, float x1, float, float, int, float *) -> float {
                 sB[t * (kC + 2) + s] = rtf(x0);
@@ -650,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<kC> acc;
             acc.zero();
-            pass<kCol, kCol, kC, kC, false, true>(acc, sA, sB, T, kC, nullptr, kC);   // X is staged
+            pass<kCol, kCol, kC, kC>(acc, sA, sB, T, kC, nullptr, kC);   // X is staged
             finish<kC>(acc, [&](int t, int s) { return ld2(KKE + t * kC + s); },
                        [&](int t, int s, float x0, float x1, float, float, float2 kk, float *cs) -> float {
                            const float l0 = s < t ? -x0 : 0.f, l1 = s + 1 < t ? -x1 : 0.f;
@@ -669,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<kC> acc;
             acc.zero();
-            pass<kRowH, kRow, kC, D, false, true>(acc, sA, sB, dO, ldt, U, D, nv);
+            pass<kRowH, kRow, kC, D>(acc, sA, sB, dO, ldt, U, D, nv);
             finish<kC>(acc, [&](int t, int s) { return ld2(A + t * kC + s); },
                        [&](int t, int s, float x0, float x1, float, float, float2 av, float *cs) -> float {
                            const float e0 = s <= t ? __expf(G[t] - G[s]) : 0.f;
@@ -687,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kRow, D, D, true>(acc, sA, sB, U, D, dSp, D);
+            pass<kRow, kRow, D, D>(acc, sA, sB, U, D, dSp, D);
             finish<D>(acc, [&](int s, int i) { return ld2(Kh + s * D + i); },
                       [&](int s, int i, float x0, float x1, float, float, float2 k, float *) -> float {
                           const float w = eGnG[s];
@@ -701,10 +702,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kCol, kCol, D, kC, true, true>(acc, sA, sB, Pk, kC, dW, D);
-            pass<kRow, kCol, D, kC, true>(acc, sA, sB, P, kC, Kh, D);
-            pass<kCol, kCol, D, kC, true>(acc, sA, sB, P, kC, nullptr, D);   // K^ is still staged
-            pass<kCol, kCol, D, kC, true>(acc, sA, sB, dQK, kC, Qh, D);
+            pass<kCol, kCol, D, kC>(acc, sA, sB, Pk, kC, dW, D);
+            pass<kRow, kCol, D, kC>(acc, sA, sB, P, kC, Kh, D);
+            pass<kCol, kCol, D, kC>(acc, sA, sB, P, kC, nullptr, D);   // K^ is still staged
+            pass<kCol, kCol, D, kC>(acc, sA, sB, dQK, kC, Qh, D);
             finish<D>(acc,
                       [&](int s, int i) {
                           const float2 o = ld2(dkh + s * D + i), k = ld2(Kh + s * D + i);
@@ -721,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kCol, D, kC, true>(acc, sA, sB, dQK, kC, Kh, D);
+            pass<kRow, kCol, D, kC>(acc, sA, sB, dQK, kC, Kh, D);
             finish<D>(acc,
                       [&](int t, int i) {
                           const float2 o = ld2(dqh + t * D + i), q = ld2(Qh + t * D + i);

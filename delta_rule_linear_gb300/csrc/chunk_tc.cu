@@ -1802,9 +1802,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         x[e] = p.h0 ? p.h0[hbase + (size_t)(i0 + e) * si + j * sj] : 0.f;
-                    if (dst)
+                    if (dst)   // (the kept states are tensor-core operands of the backward: tf32)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) dst[(size_t)(i0 + e) * D + j] = x[e];
+                        for (int e = 0; e < 8; ++e) dst[(size_t)(i0 + e) * D + j] = __uint_as_float(to_tf32(x[e]));
                     if (t.nc == 0) {
                         if (p.hT)
 #pragma unroll
@@ -1842,7 +1842,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                     if (!last && p.states) {   // the state the next chunk starts from
                         float *dst = dump_at(REV ? t.nc - 2 - c : c + 1) + (size_t)i_lo * D + j;
 #pragma unroll
-                        for (int i = 0; i < HALF; ++i) dst[(size_t)i * D] = __uint_as_float(v[i]);
+                        for (int i = 0; i < HALF; ++i) dst[(size_t)i * D] = __uint_as_float(to_tf32(__uint_as_float(v[i])));
                     }
                     if (!last) {
 #pragma unroll
