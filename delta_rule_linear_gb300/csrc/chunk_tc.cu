@@ -1839,11 +1839,6 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                 tc_fence_before();
                 mbar_arrive(&d_free[b]);
                 if (has_row) {
-                    if (!last && p.states) {   // the state the next chunk starts from
-                        float *dst = dump_at(REV ? t.nc - 2 - c : c + 1) + (size_t)i_lo * D + j;
-#pragma unroll
-                        for (int i = 0; i < HALF; ++i) dst[(size_t)i * D] = __uint_as_float(to_tf32(__uint_as_float(v[i])));
-                    }
                     if (!last) {
 #pragma unroll
                         for (int cc = 0; cc < HALF / 8; ++cc) {
@@ -1869,6 +1864,13 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                 if (!last) {
                     fence_proxy_async();
                     mbar_arrive(&s_ready);   // S_{c+1}^T is in place
+                }
+                if (has_row && !last && p.states) {
+                    // the state the next chunk starts from, kept for the backward (after the
+                    // arrive: these stores stay off the walk's critical path)
+                    float *dst = dump_at(REV ? t.nc - 2 - c : c + 1) + (size_t)i_lo * D + j;
+#pragma unroll
+                    for (int i = 0; i < HALF; ++i) dst[(size_t)i * D] = __uint_as_float(to_tf32(__uint_as_float(v[i])));
                 }
             }
         }
