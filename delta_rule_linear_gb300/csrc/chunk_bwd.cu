@@ -15,6 +15,7 @@
 //
 //   dU  = A^T dO + K~ dS'           dA  = mask_incl(dO U^T)      dK~ = U dS'^T
 //   dW  = -dU S^T                   dT  = dU (diag(beta) V)^T + dW (diag(beta e^R) K^)^T
+//   dV  = diag(beta) T^T dU
 //   dL  = -mask_strict(T^T dT T^T)  dK^ = diag(beta e^R) T^T dW + P K^ + P^T K^
 //                                         + (dA (.) E_qk)^T Q~ + diag(e^{G_n - G}) dK~,
 //                                         P = dL (.) beta_t E_kk
@@ -22,8 +23,8 @@
 //
 // with beta and the decay collected from the same terms (the decay through G, R and G_n,
 // then a reverse cumulative sum inside the chunk) and the L2 normalisation's adjoint
-// dx = (dx^ - x^ (x^ . dx^)) / |x|.  The value gradient and the state gradients come from
-// the reverse walk (chunk_tc.cu).
+// dx = (dx^ - x^ (x^ . dx^)) / |x|.  The state gradients (dS' of every chunk) come from the
+// reverse walk (chunk_tc.cu).
 //
 // One CTA per chunk at a time (persistent CTAs over the chunks, two per SM).  The chunk's
 // fp32 intermediates live in the CTA's own scratch region of global memory (L2); the states
@@ -588,6 +589,16 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             pass<kRow, kCol, D, D>(acc, sA, sB, Kt, D, dSp, D);
             finish<D>(acc, nopre, [&](int s, int j, float x0, float x1, float, float, int, float *) -> float {
                 st2r(dU + s * D + j, x0, x1);
+                return 0.f;
+            });
+        }
+        // ---- dV = diag(beta) T^T dU, written out (fp32)
+        {
+            Acc<D> acc;
+            acc.zero();
+            pass<kCol, kCol, D, kC>(acc, sA, sB, T, kC, dU, D);
+            finish<D>(acc, nopre, [&](int s, int j, float x0, float x1, float, float, int, float *) -> float {
+                if (s < nv) st2(a.dv + ((size_t)(row0 + s) * a.H + h) * D + j, beta[s] * x0, beta[s] * x1);
                 return 0.f;
             });
         }

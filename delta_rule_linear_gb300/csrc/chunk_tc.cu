@@ -1903,16 +1903,18 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                 if (ok) {
                     tc_fence_after();
                     const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
-                    tmem_ld32(dcol + D, *reinterpret_cast<uint32_t(*)[32]>(v));
-                    tmem_ld32(dcol + D + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                    tmem_ld_wait();
+                    if (!REV || p.dv_out) {
+                        tmem_ld32(dcol + D, *reinterpret_cast<uint32_t(*)[32]>(v));
+                        tmem_ld32(dcol + D + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                        tmem_ld_wait();
+                    }
                     tc_fence_before();
                     mbar_arrive(&d_free[b]);
                 }
-                if (REV) {
+                if (REV) {   // (dv_out may be nullptr: the value gradients are formed elsewhere)
                     const int cc = t.nc - 1 - c;
                     const int nv = ok ? min(kC, t.len - cc * kC) : 0;
-                    if (has_row)
+                    if (has_row && p.dv_out)
                         for (int tt = 0; tt < nv; ++tt)
                             p.dv_out[((size_t)(t.start + (long)cc * kC + tt) * p.H + t.h) * D + j] =
                                 __uint_as_float(v[tt]);

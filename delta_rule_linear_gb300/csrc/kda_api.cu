@@ -660,12 +660,14 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
     a.ws = static_cast<WsHeader *>(ws);
     a.ws_body = w + kWsHeader;
     a.ws_body_bytes = o_st - kWsHeader;
-    cudaError_t e = launch_chunk_tc_walks(a, d_o, dfinal_state, dinitial_state, dv_out, fstates, bstates, st);
+    // the reverse walk writes the state gradients and dh0; the value gradients come from the
+    // gradient kernel (dV = diag(beta) T^T dU), which spares the walk their stores
+    cudaError_t e = launch_chunk_tc_walks(a, d_o, dfinal_state, dinitial_state, nullptr, fstates, bstates, st);
     if (e != cudaSuccess) return launch_status(e);
     ChunkBwdArgs g{};
     g.q = q; g.k = k; g.v = v; g.d_o = d_o; g.beta = beta; g.decay = decay;
     g.fstates = fstates; g.bstates = bstates;
-    g.dq = dq; g.dk = dk_out; g.dbeta = dbeta; g.ddecay = decay ? ddecay : nullptr;
+    g.dq = dq; g.dk = dk_out; g.dv = dv_out; g.dbeta = dbeta; g.ddecay = decay ? ddecay : nullptr;
     g.B = B; g.T = T; g.H = H; g.D = dk;
     g.scale = a.scale; g.use_l2 = a.use_l2; g.decayed_read = a.decayed_read;
     g.scratch = reinterpret_cast<float *>(w + o_scr);

@@ -105,7 +105,7 @@ struct ChunkBwdArgs {
     const void *q, *k, *v, *d_o;       // bf16 [B, T, H, D]
     const float *beta, *decay;          // [B, T, H]; decay may be nullptr
     const float *fstates, *bstates;     // [B, H, nc, D, D]
-    float *dq, *dk, *dbeta, *ddecay;    // outputs (ddecay may be nullptr)
+    float *dq, *dk, *dv, *dbeta, *ddecay;   // outputs (ddecay may be nullptr)
     int B, T, H, D;
     float scale;
     int use_l2, decayed_read;
