@@ -394,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         const int h = bh % a.H, b = bh / a.H;
         const long row0 = (long)b * a.T + (long)c * kC;
         const int nv = min(kC, a.T - c * kC);
-        const float *S = a.fstates + (size_t)ci * D * D;    // state entering the chunk
-        const float *dSp = a.bstates + (size_t)ci * D * D;  // gradient of the state leaving it
+        const __nv_bfloat16 *S = a.fstates + (size_t)ci * D * D;    // state entering the chunk
+        const __nv_bfloat16 *dSp = a.bstates + (size_t)ci * D * D;  // gradient of the state leaving it
 
         // the chunk's rows of v and dO, read in place by the products (bf16, row stride H D)
         const __nv_bfloat16 *V = gv + ((size_t)row0 * a.H + h) * D, *dO = gdo + ((size_t)row0 * a.H + h) * D;
@@ -512,12 +512,16 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         } else {
             for (int x = tid - 64; x < 32 * 32; x += kThreads - 64) sT[(x >> 5) * PL + 32 + (x & 31)] = 0.f;
             // e^{G_n} sum(S (.) dS'), a term of the gradient of G_n
-            const float4 *s4 = reinterpret_cast<const float4 *>(S), *d4 = reinterpret_cast<const float4 *>(dSp);
+            const uint4 *s8 = reinterpret_cast<const uint4 *>(S), *d8 = reinterpret_cast<const uint4 *>(dSp);
+            auto lo = [](uint32_t u) { return __uint_as_float(u << 16); };
+            auto hi = [](uint32_t u) { return __uint_as_float(u & 0xffff0000u); };
             float acc = 0.f;
-#pragma unroll 8
-            for (int x = tid - 64; x < D * D / 4; x += kThreads - 64) {
-                const float4 u = s4[x], w = d4[x];
-                acc = fmaf(u.x, w.x, fmaf(u.y, w.y, fmaf(u.z, w.z, fmaf(u.w, w.w, acc))));
+#pragma unroll 4
+            for (int x = tid - 64; x < D * D / 8; x += kThreads - 64) {   // 8 bf16 at a time
+                const uint4 u = s8[x], w = d8[x];
+                const uint32_t uu[4] = {u.x, u.y, u.z, u.w}, ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc = fmaf(lo(uu[e]), lo(ww[e]), fmaf(hi(uu[e]), hi(ww[e]), acc));
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -574,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kCol, D, D>(acc, sA, sB, nullptr, D, S, D);   // -W is staged
+            pass<kRow, kColH, D, D>(acc, sA, sB, nullptr, D, S, D);   // -W is staged
             pass<kRow, kColH, D, kC>(acc, sA, sB, Pv, kC, V, ldt, 1 << 30, nv);
             finish<D>(acc, nopre, [&](int t, int j, float x0, float x1, float, float, int, float *) -> float {
                 st2r(U + t * D + j, x0, x1);
@@ -586,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
             Acc<D> acc;
             acc.zero();
             pass<kCol, kColH, D, kC>(acc, sA, sB, A, kC, dO, ldt, 1 << 30, nv);
-            pass<kRow, kCol, D, D>(acc, sA, sB, Kt, D, dSp, D);
+            pass<kRow, kColH, D, D>(acc, sA, sB, Kt, D, dSp, D);
             finish<D>(acc, nopre, [&](int s, int j, float x0, float x1, float, float, int, float *) -> float {
                 st2r(dU + s * D + j, x0, x1);
                 return 0.f;
@@ -606,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRowH, kRow, D, D>(acc, sA, sB, dO, ldt, S, D, nv);
+            pass<kRowH, kRowH, D, D>(acc, sA, sB, dO, ldt, S, D, nv);
             finish<D>(acc, [&](int t, int i) { return ld2(Qh + t * D + i); },
                       [&](int t, int i, float x0, float x1, float, float, float2 q, float *) -> float {
                           st2(dqh + t * D + i, eG[t] * x0, eG[t] * x1);
@@ -618,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kRow, D, D>(acc, sA, sB, dU, D, nullptr, D);   // S is still staged
+            pass<kRow, kRowH, D, D>(acc, sA, sB, dU, D, nullptr, D);   // S is still staged
             finish<D>(acc, nopre, [&](int s, int i, float x0, float x1, float, float, int, float *) -> float {
                 st2r(dW + s * D + i, -x0, -x1);
                 return 0.f;
@@ -699,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_bwd_kernel(ChunkBwdArgs a) 
         {
             Acc<D> acc;
             acc.zero();
-            pass<kRow, kRow, D, D>(acc, sA, sB, U, D, dSp, D);
+            pass<kRow, kRowH, D, D>(acc, sA, sB, U, D, dSp, D);
             finish<D>(acc, [&](int s, int i) { return ld2(Kh + s * D + i); },
                       [&](int s, int i, float x0, float x1, float, float, float2 k, float *) -> float {
                           const float w = eGnG[s];

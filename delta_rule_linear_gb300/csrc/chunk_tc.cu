@@ -90,7 +90,8 @@ struct TcParams {
     uint32_t *flags;           // [nch * ring]: column + 1 of the E_c a slot holds
     int ring;                  // E_c slots per chain (kRing; every column's own slot when the
                                // maps are kept for the backward)
-    float *states;             // or nullptr: fp32 state at every chunk start [nseq, H, nc, D, D]
+    __nv_bfloat16 *states;     // or nullptr: the state at every chunk start [nseq, H, nc, D, D], bf16
+                               // (the walk's own operand precision)
                                // (the reverse walk: the incoming state gradient of every chunk)
     float *dv_out;             // the reverse walk: fp32 value gradient [rows, H, D]
     uint32_t *consumed;        // [nch]: chain i has loaded every E_c of a column below this
@@ -1603,7 +1604,7 @@ __device__ __forceinline__ bool chain_task(const TcParams &p, int chain, int r, 
 // REV: the reverse walk of the backward, [dS_c; dV_c] = E_c^T [dS_{c+1}; dO_c] (E_c^T's
 // product is the same instruction sequence with E_c read MN-major): chunks last to first,
 // map_v streams dO, h0 holds the final-state gradient and hT receives the initial-state
-// gradient, the "outputs" are the fp32 value gradients (dv_out), and `states` receives
+// gradient, the "outputs" are the fp32 value gradients (dv_out, or none), and `states` receives
 // the incoming state gradient of every chunk.  The maps were kept by a forward launch
 // (every chunk its own slot), so nothing waits on flags.
 template <int D, bool OPT, bool REV = false>
@@ -1796,15 +1797,15 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
         for (int r = 0; chain_task(p, chain, r, t) && !s_fail; ++r) {
             const size_t hbase = ((size_t)t.n * p.H + t.h) * D * D;
             if (has_row) {   // S_0^T row j from initial_state[:, j] (the previous task's MMAs are done)
-                float *dst = (p.states && t.nc > 0) ? dump_at(REV ? t.nc - 1 : 0) : nullptr;
+                __nv_bfloat16 *dst = (p.states && t.nc > 0) ? dump_at(REV ? t.nc - 1 : 0) : nullptr;
                 for (int i0 = i_lo; i0 < i_lo + HALF; i0 += 8) {
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         x[e] = p.h0 ? p.h0[hbase + (size_t)(i0 + e) * si + j * sj] : 0.f;
-                    if (dst)   // (the kept states are tensor-core operands of the backward: tf32)
+                    if (dst)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) dst[(size_t)(i0 + e) * D + j] = __uint_as_float(to_tf32(x[e]));
+                        for (int e = 0; e < 8; ++e) dst[(size_t)(i0 + e) * D + j] = __float2bfloat16_rn(x[e]);
                     if (t.nc == 0) {
                         if (p.hT)
 #pragma unroll
@@ -1866,11 +1867,12 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                     mbar_arrive(&s_ready);   // S_{c+1}^T is in place
                 }
                 if (has_row && !last && p.states) {
-                    // the state the next chunk starts from, kept for the backward (after the
-                    // arrive: these stores stay off the walk's critical path)
-                    float *dst = dump_at(REV ? t.nc - 2 - c : c + 1) + (size_t)i_lo * D + j;
+                    // the state the next chunk starts from, kept for the backward in bf16, the
+                    // precision of the operand the walk itself carries (after the arrive: these
+                    // stores stay off the walk's critical path)
+                    __nv_bfloat16 *dst = dump_at(REV ? t.nc - 2 - c : c + 1) + (size_t)i_lo * D + j;
 #pragma unroll
-                    for (int i = 0; i < HALF; ++i) dst[(size_t)i * D] = __uint_as_float(to_tf32(__uint_as_float(v[i])));
+                    for (int i = 0; i < HALF; ++i) dst[(size_t)i * D] = __float2bfloat16_rn(__uint_as_float(v[i]));
                 }
             }
         }
@@ -2143,10 +2145,10 @@ struct TcPlan {
 };
 
 // OPT: the kda_options paths, compiled out of the plain instantiations
-// states: or nullptr, the fp32 state at every chunk start; keep: or nullptr, every chunk's
+// states: or nullptr, the state at every chunk start (bf16); keep: or nullptr, every chunk's
 // map stays in the scratch and the plan is returned (equal-length batches only).
 template <int D, bool GK, bool OPT>
-cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st, float *states = nullptr,
+cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st, __nv_bfloat16 *states = nullptr,
                    TcPlan *keep = nullptr) {
     constexpr int R = D + 64;
     using Cf = ChainCfg<D>;
@@ -2243,7 +2245,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) rev_chain_kernel(const __grid_c
 
 template <int D>
 cudaError_t run_rev(const SeqBatch &a, const TcPlan &plan, const void *d_o, const float *dhT, float *dh0,
-                    float *dv, float *dstates, cudaStream_t st) {
+                    float *dv, __nv_bfloat16 *dstates, cudaStream_t st) {
     constexpr int R = D + 64;
     using Cf = ChainCfg<D>;
     TcParams p{};
@@ -2291,7 +2293,7 @@ size_t chunk_tc_keep_bytes(int B, int H, int T, int d) {
 }
 
 cudaError_t launch_chunk_tc_walks(const SeqBatch &a, const void *d_o, const float *dhT, float *dh0, float *dv,
-                                  float *fstates, float *bstates, cudaStream_t st) {
+                                  __nv_bfloat16 *fstates, __nv_bfloat16 *bstates, cudaStream_t st) {
     if ((long)a.nseq * a.T >= (1L << 31) || a.cu_seqlens || a.per_channel) return cudaErrorInvalidValue;
     const bool opt = a.decayed_read != 0;
     TcPlan plan{};

@@ -605,7 +605,7 @@ kda_status kda_diag_wait_timeout(void *ws, size_t ws_bytes, unsigned limit_us,
 static size_t chunk_bwd_layout(int B, int T, int H, int d, size_t *off_states, size_t *off_dstates,
                                size_t *off_scratch) {
     const size_t keep = (chunk_tc_keep_bytes(B, H, T, d) + 255) / 256 * 256;
-    const size_t st = (size_t)B * H * ((T + 63) / 64) * d * d * sizeof(float);
+    const size_t st = (size_t)B * H * ((T + 63) / 64) * d * d * 2;   // bf16 states
     if (off_states) *off_states = kWsHeader + keep;
     if (off_dstates) *off_dstates = kWsHeader + keep + st;
     if (off_scratch) *off_scratch = kWsHeader + keep + 2 * st;
@@ -649,7 +649,8 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
     size_t o_st = 0, o_dst = 0, o_scr = 0;
     chunk_bwd_layout(B, T, H, dk, &o_st, &o_dst, &o_scr);
     char *w = static_cast<char *>(ws);
-    float *fstates = reinterpret_cast<float *>(w + o_st), *bstates = reinterpret_cast<float *>(w + o_dst);
+    __nv_bfloat16 *fstates = reinterpret_cast<__nv_bfloat16 *>(w + o_st);
+    __nv_bfloat16 *bstates = reinterpret_cast<__nv_bfloat16 *>(w + o_dst);
     if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
     SeqBatch a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = decay; a.h0 = initial_state;

@@ -99,12 +99,12 @@ cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, cudaStream_t s);
 // chunk_tc_keep_bytes().
 size_t chunk_tc_keep_bytes(int B, int H, int T, int d);
 cudaError_t launch_chunk_tc_walks(const SeqBatch &a, const void *d_o, const float *dhT, float *dh0, float *dv,
-                                  float *fstates, float *bstates, cudaStream_t s);
+                                  __nv_bfloat16 *fstates, __nv_bfloat16 *bstates, cudaStream_t s);
 // Gradients of q, k, beta and the decay per chunk from the two walks' states (chunk_bwd.cu).
 struct ChunkBwdArgs {
     const void *q, *k, *v, *d_o;       // bf16 [B, T, H, D]
     const float *beta, *decay;          // [B, T, H]; decay may be nullptr
-    const float *fstates, *bstates;     // [B, H, nc, D, D]
+    const __nv_bfloat16 *fstates, *bstates;   // [B, H, nc, D, D], bf16
     float *dq, *dk, *dv, *dbeta, *ddecay;   // outputs (ddecay may be nullptr)
     int B, T, H, D;
     float scale;

@@ -385,13 +385,15 @@ kda_status kda_gate_decay(const float *gate, const float *A_log, const float *dt
  * the bf16 tensor-core shapes (dtype KDA_BF16, dk == dv in {64, 128}; anything else returns
  * KDA_ERR_UNSUPPORTED), computed by chunks of 64 tokens (kda-neuron-kernels README,
  * kda_chunk_step_exact_bwd; TileOPs DeltaNetChunkBwdOp): a forward launch that keeps every
- * chunk's map and state, a reverse walk [dS_c; dV_c] = E_c^T [dS_{c+1}; dO_c] over the
- * maps (the transposed chunk map), and one kernel for the chunk-local gradients of q, k,
- * beta and the decay.  Arguments, layouts and errors as kda_recurrent_bwd (equal-length
- * batches, key-major states).  Arithmetic: bf16 maps and state operands on the tensor
- * cores as in the forward, tf32 products with fp32 accumulation for the chunk gradients.
+ * chunk's map and state, a reverse walk dS_c = [E_c^T [dS_{c+1}; dO_c]] over the maps
+ * (the transposed chunk map) that keeps every chunk's state gradient, and one kernel for
+ * the chunk-local gradients of q, k, v, beta and the decay.  Arguments, layouts and errors
+ * as kda_recurrent_bwd (equal-length batches, key-major states).  Arithmetic: bf16 maps and
+ * state operands on the tensor cores as in the forward (the kept states and state gradients
+ * are those bf16 operands), tf32 products with fp32 accumulation for the chunk gradients.
  * ws: at least kda_chunk_bwd_workspace() bytes, 16-byte aligned (it holds every chunk's
- * map and two fp32 states per chunk: about 200 KB per chunk and head at head dim 128).
+ * map and two bf16 states per chunk, ~136 KB per chunk and head at head dim 128, plus a
+ * fixed scratch of at most 304 x 368 KB for the gradient kernel).
  */
 size_t kda_chunk_bwd_workspace(int B, int T, int H, int dk, int dv);
 kda_status kda_chunk_bwd(const void *q, const void *k, const void *v,
