@@ -513,13 +513,22 @@ __device__ __forceinline__ void release_slot(const TcParams &p, int slot, int co
 // Before E_c of column `col` goes into its chain's ring: wait until the chain has loaded
 // the E_c that the slot held (column col - kRing), giving up after limit_ns; the async
 // proxy is then ordered after the acquire (the slot is written by TMA stores).
-__device__ __forceinline__ bool wait_slot_free(const TcParams &p, int chain, int col, uint64_t limit_ns) {
+// seen: the group's record of the counters it has read (shared memory, one per chain): a
+// counter already seen at or past `need` is not read again -- that earlier acquire orders the
+// slot's reuse just as well -- so the common case costs no round trip to the counter's line,
+// which may sit in the other die's L2.
+__device__ __forceinline__ bool wait_slot_free(const TcParams &p, int chain, int col, uint64_t limit_ns,
+                                               uint32_t *seen) {
     if (col >= p.ring) {
         const uint32_t need = (uint32_t)(col - p.ring + 1);
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(p.consumed + chain) < need) {
-            if (globaltimer_ns() - t0 > limit_ns) return false;
-            __nanosleep(64);
+        if (seen[chain] < need) {
+            const uint64_t t0 = globaltimer_ns();
+            uint32_t v;
+            while ((v = ld_acquire_gpu(p.consumed + chain)) < need) {
+                if (globaltimer_ns() - t0 > limit_ns) return false;
+                __nanosleep(64);
+            }
+            seen[chain] = v;
         }
     }
     fence_proxy_async_global();
@@ -566,8 +575,11 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     constexpr int NB = D / 64;
     constexpr int R = D + 64;
     PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(sm + Ly::CTRL);
+    __shared__ uint32_t s_seen[2][kMaxChains];   // per group: the ring counters last read
+    uint32_t *seen = s_seen[bar - 1];
     const int warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hh = warp >> 2;
+    if (tid < kMaxChains) seen[tid] = 0;   // (first read after the loop's barriers)
     const int i128 = 32 * q4 + lane;
     const int i64 = 16 * q4 + lane;
     const bool has64 = lane < 16;
@@ -882,7 +894,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
             mma_commit(&ctl->bar_mma);
         }
         if (tid == kStoreThread && ok) {   // the V-column block, to drain during MMA3 and epilogue 3
-            if (wait_slot_free(p, cur.chain, cur.col, kWaitNs)) {   // the ring slot has been read
+            if (wait_slot_free(p, cur.chain, cur.col, kWaitNs, seen)) {   // the ring slot has been read
                 tma_store_3d(map_E, sEst + NB * (R * 128), NB * 64, 0, cur.slot);
                 bulk_commit();
             } else {
@@ -1113,11 +1125,14 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
     using Ly = GkSmem<D>;
     constexpr int NT = kGkThreads;
     constexpr int NB = D / 64;
-        constexpr int NP = D / 2;                 // channel pairs
+    constexpr int NP = D / 2;                 // channel pairs
     constexpr int NQ = NT / NP;               // token groups of the prefix and the build
     constexpr int TPG = 64 / NQ;              // their tokens: 8 (D = 128) or 4 (D = 64)
     static_assert(TPG <= 16 && 16 % TPG == 0, "a token group stays inside one 16-token sub-block");
     PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(sm + Ly::CTRL);
+    __shared__ uint32_t s_seen_gk[kMaxChains];   // the ring counters last read
+    uint32_t *seen = s_seen_gk;
+    if (tid < kMaxChains) seen[tid] = 0;         // (first read after the loop's barriers)
     const int warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hh = warp >> 2;   // TMEM lane quadrant; column quarter
     const int i128 = 32 * q4 + lane;
@@ -1385,7 +1400,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         }
         // this chunk's ring slot must have been read by its chain before epilogue 2 stores
         // into it (the barriers in between order every warp's stores after this wait)
-        if (tid == kStoreThread && ok && !wait_slot_free(p, cur.chain, cur.col, kWaitNs)) {
+        if (tid == kStoreThread && ok && !wait_slot_free(p, cur.chain, cur.col, kWaitNs, seen)) {
             ctl->fail = 1;
             record_error(p.ws, 4);
         }
@@ -1662,16 +1677,18 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
             for (int r = 0; chain_task(p, chain, r, t) && !s_fail; ++r) {
                 for (int c = 0; c < t.nc && !s_fail; ++c, ++gc) {
                     const int s = gc & 1;
+                    const int col = t.col0 + (REV ? t.nc - 1 - c : c);
+                    const int slot = chain * p.ring + col % p.ring;
+                    // E_c published: watched before the stage frees, so that the round trip to
+                    // the flag's line (possibly in the other die's L2) overlaps that wait
+                    if (!REV && !wait_flag_acquire(p.flags + slot, (uint32_t)col + 1u, kWaitNs)) {
+                        s_fail = 1;
+                        record_error(p.ws, 16);
+                        break;
+                    }
                     if (gc >= 2 && !mbar_wait(&e_empty[s], ((gc >> 1) - 1) & 1, kWaitNs)) {
                         s_fail = 1;
                         record_error(p.ws, 10);
-                        break;
-                    }
-                    const int col = t.col0 + (REV ? t.nc - 1 - c : c);
-                    const int slot = chain * p.ring + col % p.ring;
-                    if (!REV && !wait_flag_acquire(p.flags + slot, (uint32_t)col + 1u, kWaitNs)) {   // E_c published
-                        s_fail = 1;
-                        record_error(p.ws, 16);
                         break;
                     }
                     mbar_expect_tx(&e_full[s], Cf::E_BYTES);
