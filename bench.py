@@ -471,14 +471,14 @@ def bench_prefill(args, world, rank, dev, peaks, d):
 
 
 # --------------------------------------------------------------------------- other prefill configs
-SECONDARY_PARTS = ("training", "backward", "gated", "varlen")
+SECONDARY_PARTS = ("tiny", "training", "backward", "gated", "varlen")
 
 
 def bench_secondary(args, world, rank, dev, peaks, parts=SECONDARY_PARTS):
-    """The training-shape prefill (workload 2) and its backward, the long-sequence prefill
-    with the gate prologues, and the packed varlen prefill (workload 5), reported beside the
-    headline: tokens/s and counted FLOPs against the bf16 peak.  `parts` selects a subset
-    (profiling captures)."""
+    """The tiny fp32 workload (1, the CUDA-core chunk path), the training-shape prefill
+    (workload 2) and its backward, the long-sequence prefill with the gate prologues, and the
+    packed varlen prefill (workload 5), reported beside the headline: tokens/s and counted
+    FLOPs against the bf16 peak.  `parts` selects a subset (profiling captures)."""
     import torch
     import delta_rule_linear_gb300 as kda
     from delta_rule_linear_gb300 import _lib
@@ -498,6 +498,8 @@ def bench_secondary(args, world, rank, dev, peaks, parts=SECONDARY_PARTS):
         torch.cuda.synchronize()
         return max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
 
+    if "tiny" in parts:
+        tiny_prefill(out, timed, kda, _lib, rank, dev, stream, world)
     wl = WORKLOADS[2]
     d = make_prefill(wl, seed=rank)
     q, k, v = (to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v"))
@@ -516,6 +518,23 @@ def bench_secondary(args, world, rank, dev, peaks, parts=SECONDARY_PARTS):
     if "varlen" in parts:
         varlen_prefill(out, timed, kda, _lib, rank, dev, stream, world, peaks)
     return out
+
+
+def tiny_prefill(out, timed, kda, _lib, rank, dev, stream, world):
+    """Workload 1: fp32, B=1 T=64 H=2 d=32, chunk 16 -- the CUDA-core chunk path."""
+    import torch
+    wl = WORKLOADS[1]
+    d = make_prefill(wl, seed=rank)
+    q, k, v, beta, decay = (to_dev(d[n], dev, torch.float32) for n in ("q", "k", "v", "beta", "decay"))
+    o = torch.empty_like(v)
+    hT = torch.empty((wl.B, wl.H, wl.dk, wl.dv), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(256, _lib.chunk_fwd_workspace_bytes(wl.B, wl.T, wl.H, wl.dk, wl.dv, wl.chunk,
+                                                             _lib.KDA_F32)), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: kda.chunk_fwd(q, k, v, beta, decay, None, chunk_size=wl.chunk, out=o,
+                                     final_state=hT, workspace=ws, stream=stream))
+    out["tiny_prefill"] = {
+        "workload": wl.name, "ms_per_call": ms, "tokens_per_s": wl.B * wl.T * world / (ms * 1e-3),
+        "gpu_launches_per_call": 1, "note": "fp32 CUDA-core chunk path (chunk_simt_kernel): launch-bound at this size"}
 
 
 def training_prefill(out, timed, kda, wl, q, k, v, beta, decay, o, hT, ws, stream, world, peaks):
@@ -939,7 +958,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "secondary", "gk", "gk_prefill"] + list(SECONDARY_PARTS),
+    ap.add_argument("--only", choices=["prefill", "decode", "secondary", "gk", "gk_prefill", "layouts"] + list(SECONDARY_PARTS),
                     default=None,
                     help="run one workload (profiling); the default runs them all")
     ap.add_argument("--prefill-T", type=int, default=0,
@@ -996,7 +1015,7 @@ def main():
         sec = bench_secondary(args, world, rank, dev, peaks, parts=(args.only,))
     if args.only in (None, "secondary", "gk", "gk_prefill"):
         sec = dict(sec or {}, kda_gk=bench_gk(args, world, rank, dev, peaks))
-    if args.only in (None, "secondary"):
+    if args.only in (None, "secondary", "layouts"):
         sec = dict(sec or {}, layouts=bench_layouts(args, world, rank, dev, peaks))
     if rank != 0:
         return
