@@ -263,9 +263,10 @@ __device__ __forceinline__ void put_b(const BTiles &bt, int t, int s, const floa
 // kLP = 68 floats: 16-byte aligned rows, and conflict-free A-fragment loads), by the
 // NT = 256 threads of one group (named barrier `bar`), on the 4 x 4 grid of 16 x 16 blocks
 // (the 2 x 2 block form of the inverse of a lower-triangular matrix, applied twice):
-//  * with A = rows/columns 0..31 and B = 32..63: the diagonal blocks T_AA, T_BB by forward
-//    substitution, one warp each, one lane per column, the column in registers, each row
-//    of L read with 16-byte loads;
+//  * with A = rows/columns 0..31 and B = 32..63: the diagonal blocks T_AA, T_BB, one warp
+//    each, by the same form one level down: their 16 x 16 diagonal pieces by forward
+//    substitution (half a warp each, one lane per column, the column in registers, each row
+//    of L read with 16-byte loads), the piece below by two 16 x 16 products;
 //  * T_BA = -T_BB (L_BA T_AA), the 32 x 32 products split into 16 x 8 tiles, one per warp.
 // The off-diagonal products run on the tensor cores as warp-level tf32 MMAs (m16n8k8,
 // fp32 accumulation; operands rounded to tf32, which keeps 10 fraction bits -- T goes on
@@ -312,16 +313,20 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
     if (warp < 2) {
-        // diagonal 32 x 32 block `warp` (T_AA, T_BB), column j = lane:
-        //   x_r = delta_rj - sum_{s<r} L[r][s] x_s
-        // with the row of L read by 16-byte loads; the terms with earlier x_s are summed
-        // while the later ones are still being computed, so the step from one row to the
-        // next is one paired FMA and a subtraction
-        const int b0 = 32 * warp, j = lane;
-        float x[32];
+        // diagonal 32 x 32 block `warp` (T_AA, T_BB) in 16 x 16 pieces: lanes 0-15 take the
+        // columns of its first diagonal piece, lanes 16-31 those of its second, each by
+        // forward substitution with the column in registers,
+        //   x_r = delta_rj - sum_{s<r} L[r][s] x_s,
+        // the row of L read by 16-byte loads (the terms with earlier x_s are summed while the
+        // later ones are still being computed); then the piece below the diagonal,
+        // T_10 = -T_11 (L_10 T_00), by two warp-level tf32 MMA steps, L_10 T_00 kept in L's
+        // unused upper piece of the block
+        const int b0 = 32 * warp, j = lane & 15;
+        const int o = b0 + 16 * (lane >> 4);   // first row and column of this lane's piece
+        float x[16];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const float4 *Lr = reinterpret_cast<const float4 *>(sL + (b0 + r) * P + b0);
+        for (int r = 0; r < 16; ++r) {
+            const float4 *Lr = reinterpret_cast<const float4 *>(sL + (o + r) * P + o);
             float2 acc = make_float2(0.f, 0.f);   // sum_{s<r} L[r][s] x_s, by pairs of s
 #pragma unroll
             for (int m4 = 0; m4 < (r + 3) / 4; ++m4) {
@@ -335,7 +340,36 @@ __device__ void invert_unit_lower_64(float *sL, float *sT, const BTiles &bt, int
             x[r] = ((r == j) ? 1.f : 0.f) - (acc.x + acc.y);
         }
 #pragma unroll
-        for (int r = 0; r < 32; ++r) sT[(b0 + r) * P + b0 + j] = x[r];
+        for (int r = 0; r < 16; ++r) sT[(o + r) * P + o + j] = x[r];
+        if (lane < 16)   // T_01 = 0
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sT[(b0 + r) * P + b0 + 16 + j] = 0.f;
+        __syncwarp();
+        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int k0 = 0; k0 < 16; k0 += 8) {   // L_10 T_00
+                uint32_t a[4], b[2];
+                frag_a(a, sL + (b0 + 16) * P + b0, k0, g, t4);
+                frag_b(b, sT + b0 * P + b0, k0, 8 * nt, g, t4);
+                mma_tf32(y[nt], a, b);
+            }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) store_c(sL + b0 * P + b0 + 16, y[nt], 8 * nt, g, t4, 1.f);
+        __syncwarp();
+        float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int k0 = 0; k0 < 16; k0 += 8) {   // T_11 (L_10 T_00)
+                uint32_t a[4], b[2];
+                frag_a(a, sT + (b0 + 16) * P + b0 + 16, k0, g, t4);
+                frag_b(b, sL + b0 * P + b0 + 16, k0, 8 * nt, g, t4);
+                mma_tf32(z[nt], a, b);
+            }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) store_c(sT + (b0 + 16) * P + b0, z[nt], 8 * nt, g, t4, -1.f);
     } else {
         // the other 192 threads zero the four 16 x 16 blocks of B and Bf above the diagonal
         // 32 x 32 blocks: 4 blocks x 16 rows x 2 chunks x 4 tiles (B, Bf; T' and P halves),
