@@ -153,6 +153,15 @@ struct ChunkItem {
     int h, nv;         // head; valid tokens in the chunk (1..64)
 };
 
+struct PrepCtrl {
+    uint64_t bar_mma;
+    int fail;
+    float gate[2];   // A_log and dt_bias of the chunk's head (raw-gate decay), loaded with beta
+    ChunkItem nxi;   // the group's next item, claimed and decoded by one thread while the
+    int more;        // current one runs (more = 0: none left)
+};
+static_assert(sizeof(PrepCtrl) <= 64, "the control block's room in the group's shared memory");
+
 // Prep work items in (column, chain) order: item = column * nch + chain.  Returns false
 // for an item past its task's last chunk or past the last task.
 __device__ __forceinline__ bool item_info(const TcParams &p, long item, ChunkItem &it) {
@@ -474,12 +483,8 @@ struct PrepSmem {
     static constexpr int GROUP = ((CTRL + 64 + 1023) / 1024) * 1024;   // one group's share
 };
 
-struct PrepCtrl {
-    uint64_t bar_mma;
-    int fail;
-    float gate[2];   // A_log and dt_bias of the chunk's head (raw-gate decay), loaded with beta
-    long nxt;        // the group's next item (claimed by thread 0 while the current one runs)
-};
+struct ChunkItem;
+struct PrepCtrl;
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
@@ -577,14 +582,19 @@ __device__ __forceinline__ long prep_items(const TcParams &p) {
 // The next prep item, in (column, chain) order, from the launch's shared counter: a group
 // that finishes early takes the next chunk, so the prep's front stays as narrow as the
 // work allows (no group holds a chunk far ahead of the others while its chain waits for
-// another).  Items past a task's last chunk are skipped.  Returns n_items when none is
-// left.
-__device__ __forceinline__ long claim_item(const TcParams &p, long n_items) {
+// another).  Items past a task's last chunk are skipped.  The item is decoded into `it`
+// (shared memory) by the claiming thread, so the decode (a few integer divisions, ~1.7 K
+// cycles with their loads) runs in its shadow instead of on every thread's path.  Returns 0
+// when no item is left.
+__device__ __forceinline__ int claim_item(const TcParams &p, long n_items, ChunkItem &it) {
     while (true) {
         const long x = (long)atomicAdd(p.next_item, 1u);
-        if (x >= n_items) return n_items;
-        ChunkItem it;
-        if (item_info(p, x, it)) return x;
+        if (x >= n_items) return 0;
+        ChunkItem t;
+        if (item_info(p, x, t)) {
+            it = t;
+            return 1;
+        }
     }
 }
 
@@ -643,15 +653,14 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
     const bool lead = stagger && bar == 1, follow = stagger && bar == 2;
     if (follow) named_sync(kStaggerBar, 2 * kGroupThreads);
     const long n_items = prep_items(p);
-    if (tid == 0) ctl->nxt = claim_item(p, n_items);
+    if (tid == 0) ctl->more = claim_item(p, n_items, ctl->nxi);
     named_sync(bar, kGroupThreads);
-    long item = ctl->nxt;
-    ChunkItem cur;
-    if (item >= n_items || !item_info(p, item, cur)) {
+    if (!ctl->more) {
         if (lead) named_arrive(kStaggerBar, 2 * kGroupThreads);
         return;
     }
-    named_sync(bar, kGroupThreads);   // everyone has read nxt before thread 0 claims again
+    ChunkItem cur = ctl->nxi;
+    named_sync(bar, kGroupThreads);   // everyone has read the item before it is claimed again
     load_rows<D, OPT>(p, sKQ, cur, tid, true);
     load_rows<D, OPT>(p, sKQ, cur, tid, false);
     load_scalars<OPT>(p, mbeta, mdec, ctl->gate, cur, tid);
@@ -667,7 +676,7 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         fence_proxy_async();   // ... visible to the tensor core behind the barrier
         named_sync(bar, kGroupThreads);
         bool ok = ctl->fail == 0;
-        if (tid == 32) ctl->nxt = claim_item(p, n_items);   // read by all after epilogue 1's barrier
+        if (tid == 32) ctl->more = claim_item(p, n_items, ctl->nxi);   // read by all after epilogue 1's barrier
         if (tid == kStoreThread && staged >= 0) {   // the previous chunk's state-column blocks of E_c
             for (int kb = 0; kb < NB; ++kb)
                 tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, staged);
@@ -823,9 +832,8 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         ok = ctl->fail == 0;
         if (lead && it == 0) named_arrive(kStaggerBar, 2 * kGroupThreads);
         // this group's next chunk; its q and k go to L2 now, ahead of their load after MMA3
-        const long nitem = ctl->nxt;
-        ChunkItem nx;
-        const bool more = nitem < n_items && item_info(p, nitem, nx);
+        const bool more = ctl->more != 0;
+        const ChunkItem nx = ctl->nxi;
         if (tid == 64 && more) {
             const int hq = OPT ? nx.h / p.G : nx.h;
             for (int kb = 0; kb < NB; ++kb) {
@@ -1196,13 +1204,12 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
     float *mgate = reinterpret_cast<float *>(mspan + 4);   // A_log, pad, dt_bias [D] at +4
 
     const long n_items = prep_items(p);
-    if (tid == 0) ctl->nxt = claim_item(p, n_items);
+    if (tid == 0) ctl->more = claim_item(p, n_items, ctl->nxi);
     named_sync(bar, NT);
-    const long item = ctl->nxt;
-    ChunkItem cur;
-    if (item >= n_items || !item_info(p, item, cur)) return;
-    named_sync(bar, NT);   // everyone has read nxt before thread 0 claims again
-    if (tid == 0) ctl->nxt = claim_item(p, n_items);   // the next chunk, read after the barrier below
+    if (!ctl->more) return;
+    ChunkItem cur = ctl->nxi;
+    named_sync(bar, NT);   // everyone has read the item before it is claimed again
+    if (tid == 0) ctl->more = claim_item(p, n_items, ctl->nxi);   // the next chunk, read after the barrier below
     named_sync(bar, NT);
     if (loader) {
         load_rows<D, OPT>(p, sKQ, cur, tid, true);
@@ -1416,9 +1423,8 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         // (packed sequences read cu_seqlens to find it: off the path to MMA1)
         // the next chunk: claimed by thread 0 before the previous barrier, read here by all,
         // claimed again after epilogue 1's barrier
-        const long nitem = ctl->nxt;
-        ChunkItem nx;
-        const bool more = nitem < n_items && item_info(p, nitem, nx);
+        const bool more = ctl->more != 0;
+        const ChunkItem nx = ctl->nxi;
         float *mbeta_next = mbeta2 + 64 * ((it + 1) & 1);
         if (ok && more && loader) {
             load_rows<D, OPT>(p, sKQ, nx, tid, true);
@@ -1470,7 +1476,7 @@ __device__ __forceinline__ void prep_group_gk(const CUtensorMap *map_Ew, const T
         named_sync(bar, NT);
         ok = ctl->fail == 0;
         // the chunk after next (a thread that waits out the inverse anyway)
-        if (tid == kGroupThreads) ctl->nxt = claim_item(p, n_items);
+        if (tid == kGroupThreads) ctl->more = claim_item(p, n_items, ctl->nxi);
 
         // ---- T = (I + L)^{-1}, written as P = T diag(beta) (MN-major: row t, columns s), by
         // threads 0..255
