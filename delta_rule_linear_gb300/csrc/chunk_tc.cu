@@ -676,7 +676,6 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         fence_proxy_async();   // ... visible to the tensor core behind the barrier
         named_sync(bar, kGroupThreads);
         bool ok = ctl->fail == 0;
-        if (tid == 32) ctl->more = claim_item(p, n_items, ctl->nxi);   // read by all after epilogue 1's barrier
         if (tid == kStoreThread && staged >= 0) {   // the previous chunk's state-column blocks of E_c
             for (int kb = 0; kb < NB; ++kb)
                 tma_store_3d(map_E, sEst + kb * (R * 128), kb * 64, 0, staged);
@@ -831,19 +830,25 @@ __device__ __forceinline__ void prep_group(const CUtensorMap *map_q, const CUten
         named_sync(bar, kGroupThreads);
         ok = ctl->fail == 0;
         if (lead && it == 0) named_arrive(kStaggerBar, 2 * kGroupThreads);
-        // this group's next chunk; its q and k go to L2 now, ahead of their load after MMA3
+        // ---- T = (I + L)^{-1}, written as B = [T' | P], Bf = diag(f) B (MN-major: row t, columns s).
+        // In the substitution's shadow, one thread of the idle warps claims this group's next
+        // chunk (the atomic and the decode off every path) and starts its q and k towards L2,
+        // ahead of their load after MMA3; everyone reads the item after the inverse.
+        invert_unit_lower_64<kGroupThreads>(sL, sT, BTiles{sB, sBf, mcw, mbeta, mf}, tid, bar, [&] {
+            if (tid == 64) {
+                ctl->more = claim_item(p, n_items, ctl->nxi);
+                if (ctl->more) {
+                    const ChunkItem &n = ctl->nxi;
+                    const int hq = OPT ? n.h / p.G : n.h;
+                    for (int kb = 0; kb < NB; ++kb) {
+                        tma_prefetch_l2_3d(map_q, kb * 64, hq, (int)n.row0);
+                        tma_prefetch_l2_3d(map_k, kb * 64, hq, (int)n.row0);
+                    }
+                }
+            }
+        });
         const bool more = ctl->more != 0;
         const ChunkItem nx = ctl->nxi;
-        if (tid == 64 && more) {
-            const int hq = OPT ? nx.h / p.G : nx.h;
-            for (int kb = 0; kb < NB; ++kb) {
-                tma_prefetch_l2_3d(map_q, kb * 64, hq, (int)nx.row0);
-                tma_prefetch_l2_3d(map_k, kb * 64, hq, (int)nx.row0);
-            }
-        }
-
-        // ---- T = (I + L)^{-1}, written as B = [T' | P], Bf = diag(f) B (MN-major: row t, columns s)
-        invert_unit_lower_64<kGroupThreads>(sL, sT, BTiles{sB, sBf, mcw, mbeta, mf}, tid, bar, [] {});
 
 
         // ---- MMA2: D2a[:, 0:128] = K^T diag(f) [T'|P]  (M = D);  D2b[:, 128:256] = Aqk [T'|P]
