@@ -64,6 +64,7 @@ constexpr int kStatusDeviceTimeout = 8;       // KDA_ERR_DEVICE_TIMEOUT
 // for 32 chains on a 152-SM part), which the ring must hold with room to spare
 constexpr int kRing = 16;
 constexpr int kMaxChains = 40;                // chain CTAs at most
+constexpr int kCounterStride = 32;            // a chain's ring counter (and the item counter) each own a 128-byte line
 
 struct TcParams {
     int nseq, H, T;            // T: equal-length sequence length (unused for varlen)
@@ -561,11 +562,15 @@ __device__ __forceinline__ bool wait_slot_free(const TcParams &p, int chain, int
     if (col >= p.ring) {
         const uint32_t need = (uint32_t)(col - p.ring + 1);
         if (seen[chain] < need) {
+            // a group that has run a full ring ahead waits for its chain: the wait backs off
+            // (64 ns to 1 us), so that many waiting groups do not crowd the counter's line
+            // while the chain's release has to land on it
             const uint64_t t0 = globaltimer_ns();
-            uint32_t v;
-            while ((v = ld_acquire_gpu(p.consumed + chain)) < need) {
+            uint32_t v, ns = 64;
+            while ((v = ld_acquire_gpu(p.consumed + chain * kCounterStride)) < need) {
                 if (globaltimer_ns() - t0 > limit_ns) return false;
-                __nanosleep(64);
+                __nanosleep(ns);
+                ns = ns < 1024 ? 2 * ns : 1024;
             }
             seen[chain] = v;
         }
@@ -1779,7 +1784,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
             while (done < fin && !s_fail) {
                 const uint32_t v = s_rel;
                 if (v > done) {
-                    st_release_gpu(p.consumed + chain, v);
+                    st_release_gpu(p.consumed + chain * kCounterStride, v);
                     done = v;
                     t0 = globaltimer_ns();
                 } else if (globaltimer_ns() - t0 > kWaitNs) {
@@ -2171,7 +2176,7 @@ int chains_for(long ntask, int nsm) {
 
 // Scratch layout after the workspace header (chains <= nch_max):
 //   [order: nseq ints][round_base: ntask + 1 ints]   packed sequences only
-//   [flags: nch_max * kRing][consumed: nch_max][next item: 1]   uint32
+//   [flags: nch_max * kRing][consumed: nch_max][next item: 1]   uint32, each counter on its own 128-byte line
 //   [E_c rings: nch_max * kRing * (D + 64)^2 bf16]
 struct ScratchLayout {
     size_t order, round_base, flags, consumed, E, total;
@@ -2193,7 +2198,7 @@ ScratchLayout scratch_layout(int nseq, int H, int d, bool varlen, int keep_nc = 
     L.flags = off;
     off += align256(slots * 4);
     L.consumed = off;
-    off += align256((size_t)(nch_max + 1) * 4);
+    off += align256((size_t)(nch_max + 1) * kCounterStride * 4);
     L.E = off;
     off += slots * R * R * 2;
     L.total = off;
@@ -2240,7 +2245,7 @@ cudaError_t run_tc(const SeqBatch &a, long total_rows, cudaStream_t st, __nv_bfl
     p.round_base = varlen ? reinterpret_cast<const int *>(body + L.round_base) : nullptr;
     p.flags = reinterpret_cast<uint32_t *>(body + L.flags);
     p.consumed = reinterpret_cast<uint32_t *>(body + L.consumed);
-    p.next_item = p.consumed + std::max<long>(1, std::min<long>(p.ntask, kMaxChains));
+    p.next_item = p.consumed + std::max<long>(1, std::min<long>(p.ntask, kMaxChains)) * kCounterStride;
     p.E = reinterpret_cast<__nv_bfloat16 *>(body + L.E);
 
     int dev = 0, nsm = 0;

@@ -150,7 +150,7 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
  * shapes only: dtype KDA_BF16, dk == dv in {64, 128}, chunk_size 64 (anything else
  * returns KDA_ERR_UNSUPPORTED).  Its scratch is one 48 MiB array that the library keeps
  * on every GPU that loads it, until the process exits.  The scratch needed is
- * 256 + 256 * ceil(64 C / 256) + 256 * ceil(4 C / 256) + 32 C (D+64)^2 bytes for
+ * 256 + 256 * ceil(64 C / 256) + 256 * ceil(128 (C + 1) / 256) + 32 C (D+64)^2 bytes for
  * C = min(B*H, 40) chains, at most about 45 MiB (D = 128), whatever B, T and H; a
  * problem whose scratch would not fit would return KDA_ERR_WORKSPACE before anything is
  * enqueued, which no supported problem does.
