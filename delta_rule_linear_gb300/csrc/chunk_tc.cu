@@ -1682,7 +1682,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
     uint8_t *sAS = sm + 2 * Cf::E_BYTES;
     uint8_t *sAV0 = sAS + Cf::AS_BYTES;
     uint8_t *sO = sAV0 + 2 * Cf::AV_BYTES;
-    __shared__ uint64_t e_full[2], e_empty[2], v_full[2], v_empty[2], d_full[2], d_free[2], s_ready;
+    // s_lo, s_hi: the two K halves of the S^T operand (state rows [0, D/2) and [D/2, D))
+    __shared__ uint64_t e_full[2], e_empty[2], v_full[2], v_empty[2], d_full[2], d_free[2], s_lo, s_hi;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_fail;
     // the chain's progress through the ring, as the MMA issuer observes the E_c loads land:
@@ -1700,7 +1701,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
             mbar_init(&d_full[s], 1);
             mbar_init(&d_free[s], 384);    // the state and the output warps read the accumulator
         }
-        mbar_init(&s_ready, 256);
+        mbar_init(&s_lo, 256);
+        mbar_init(&s_hi, 256);
         fence_mbar_init();
         s_fail = 0;
         s_rel = 0;
@@ -1828,13 +1830,24 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                         mma_bf16_ss(dcol, desc_mnmajor_sw128(av0, 64, ks),
                                     REV ? desc_mnmajor_sw128(e0, R, D / 16 + ks) : desc_kmajor_sw128(e0, R, D / 16 + ks),
                                     idV, ks > 0 ? 1u : 0u);
-                    if (!mbar_wait(&s_ready, gc & 1, kWaitNs)) {
+                    // the state half in two K halves: the first D/32 k-steps read state rows
+                    // [0, D/2) and start as soon as the epilogue has published them
+                    if (!mbar_wait(&s_lo, gc & 1, kWaitNs)) {
                         s_fail = 1;
                         record_error(p.ws, 12);
                         break;
                     }
                     tc_fence_after();
-                    for (int ks = 0; ks < D / 16; ++ks)   // state half: E_c columns 0 .. D - 1 (reverse: rows)
+                    for (int ks = 0; ks < D / 32; ++ks)   // state half: E_c columns 0 .. D - 1 (reverse: rows)
+                        mma_bf16_ss(dcol, desc_kmajor_sw128(as0, D, ks),
+                                    REV ? desc_mnmajor_sw128(e0, R, ks) : desc_kmajor_sw128(e0, R, ks), idS, 1u);
+                    if (!mbar_wait(&s_hi, gc & 1, kWaitNs)) {
+                        s_fail = 1;
+                        record_error(p.ws, 12);
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int ks = D / 32; ks < D / 16; ++ks)
                         mma_bf16_ss(dcol, desc_kmajor_sw128(as0, D, ks),
                                     REV ? desc_mnmajor_sw128(e0, R, ks) : desc_kmajor_sw128(e0, R, ks), idS, 1u);
                     mma_commit(&d_full[b]);
@@ -1844,10 +1857,13 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
             }
         }
     } else if (warp < 10) {
-        // ---------------- state epilogue, warps 2..9: TMEM quadrant q, value column j,
-        // state rows i in [ch D/2, (ch + 1) D/2).  Turns the fp32 next state into the
-        // bf16 S^T operand (the critical path).  s_ready completes once per chunk: after a
-        // task's initial state is in place and after every chunk but the task's last.
+        // ---------------- state epilogue, warps 2..9: TMEM quadrant q, value column j.
+        // Turns the fp32 next state into the bf16 S^T operand (the critical path) in two
+        // halves of the contraction: every warp writes its quarter of state rows [0, D/2)
+        // (rows ch D/4 ..), publishes them (s_lo), then its quarter of [D/2, D) (s_hi), so
+        // that the next product's first k-steps overlap the second half.  s_lo and s_hi
+        // complete once per chunk: after a task's initial state is in place (rows
+        // [ch D/2, (ch + 1) D/2) there) and after every chunk but the task's last.
         const int q = warp & 3, ch = (warp - 2) >> 2;
         const bool has_row = (D == 128) || (lane < 16);   // M = 64: 16 rows per quadrant
         const int j = (D == 128) ? 32 * q + lane : 16 * q + lane;
@@ -1887,7 +1903,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
             }
             if (t.nc == 0) continue;
             fence_proxy_async();
-            mbar_arrive(&s_ready);
+            mbar_arrive(&s_lo);
+            mbar_arrive(&s_hi);
 
             for (int c = 0; c < t.nc; ++c, ++gc) {
                 const int b = gc & 1;
@@ -1897,49 +1914,65 @@ __device__ __forceinline__ void chain_body(const CUtensorMap *map_E, const CUten
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dcol = tm + lrow + (uint32_t)(b * R) + (uint32_t)i_lo;
+                constexpr int QP = HALF / 2;   // state rows per warp in each half
+                const int i_a = ch * QP, i_b = HALF + ch * QP;   // its rows in [0, D/2), [D/2, D)
+                const uint32_t dcol = tm + lrow + (uint32_t)(b * R);
                 const bool last = (c + 1 == t.nc);
-                uint32_t v[HALF];
-#pragma unroll
-                for (int i0 = 0; i0 < HALF; i0 += 32)
-                    tmem_ld32(dcol + i0, *reinterpret_cast<uint32_t(*)[32]>(v + i0));
+                uint32_t v[HALF];   // v[0, QP): rows i_a ..; v[QP, 2 QP): rows i_b ..
+                if constexpr (QP == 32) {
+                    tmem_ld32(dcol + i_a, *reinterpret_cast<uint32_t(*)[32]>(v));
+                    tmem_ld32(dcol + i_b, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                } else {
+                    tmem_ld16(dcol + i_a, *reinterpret_cast<uint32_t(*)[16]>(v));
+                    tmem_ld16(dcol + i_b, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+                }
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(&d_free[b]);
-                if (has_row) {
-                    if (!last) {
+                auto store_part = [&](int i0, const uint32_t *vp) {   // QP rows of S^T row j from i0
 #pragma unroll
-                        for (int cc = 0; cc < HALF / 8; ++cc) {
-                            const int gcol = (i_lo >> 3) + cc;   // 8-column group of S^T row j
-                            *reinterpret_cast<uint4 *>(sAS + (gcol >> 3) * D * 128 + j * 128 +
-                                                       (((gcol & 7) ^ (j & 7)) << 4)) = pack8u(v + 8 * cc);
-                        }
-                    } else if (p.hT) {
+                    for (int cc = 0; cc < QP / 8; ++cc) {
+                        const int gcol = (i0 >> 3) + cc;   // 8-column group of S^T row j
+                        *reinterpret_cast<uint4 *>(sAS + (gcol >> 3) * D * 128 + j * 128 +
+                                                   (((gcol & 7) ^ (j & 7)) << 4)) = pack8u(vp + 8 * cc);
+                    }
+                };
+                if (!last) {
+                    if (has_row) store_part(i_a, v);
+                    fence_proxy_async();
+                    mbar_arrive(&s_lo);   // the first half of S_{c+1}^T is in place
+                    if (has_row) store_part(i_b, v + QP);
+                    fence_proxy_async();
+                    mbar_arrive(&s_hi);   // and the second
+                } else if (has_row && p.hT) {
+#pragma unroll
+                    for (int hp = 0; hp < 2; ++hp) {
+                        const int i0 = hp ? i_b : i_a;
+                        const uint32_t *vp = v + hp * QP;
                         if (vf) {   // value-major: row j of the state is contiguous
-                            float *dst = p.hT + hbase + (size_t)j * D + i_lo;
+                            float *dst = p.hT + hbase + (size_t)j * D + i0;
 #pragma unroll
-                            for (int i = 0; i < HALF; i += 4)
+                            for (int i = 0; i < QP; i += 4)
                                 *reinterpret_cast<float4 *>(dst + i) =
-                                    make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                                    make_float4(__uint_as_float(vp[i]), __uint_as_float(vp[i + 1]),
+                                                __uint_as_float(vp[i + 2]), __uint_as_float(vp[i + 3]));
                         } else {
 #pragma unroll
-                            for (int i = 0; i < HALF; ++i)
-                                p.hT[hbase + (size_t)(i_lo + i) * D + j] = __uint_as_float(v[i]);
+                            for (int i = 0; i < QP; ++i)
+                                p.hT[hbase + (size_t)(i0 + i) * D + j] = __uint_as_float(vp[i]);
                         }
                     }
                 }
-                if (!last) {
-                    fence_proxy_async();
-                    mbar_arrive(&s_ready);   // S_{c+1}^T is in place
-                }
                 if (has_row && !last && p.states) {
                     // the state the next chunk starts from, kept for the backward in bf16, the
-                    // precision of the operand the walk itself carries (after the arrive: these
-                    // stores stay off the walk's critical path)
-                    __nv_bfloat16 *dst = dump_at(REV ? t.nc - 2 - c : c + 1) + (size_t)i_lo * D + j;
+                    // precision of the operand the walk itself carries (after the arrives:
+                    // these stores stay off the walk's critical path)
+                    __nv_bfloat16 *base = dump_at(REV ? t.nc - 2 - c : c + 1) + j;
 #pragma unroll
-                    for (int i = 0; i < HALF; ++i) dst[(size_t)i * D] = __float2bfloat16_rn(__uint_as_float(v[i]));
+                    for (int i = 0; i < QP; ++i) {
+                        base[(size_t)(i_a + i) * D] = __float2bfloat16_rn(__uint_as_float(v[i]));
+                        base[(size_t)(i_b + i) * D] = __float2bfloat16_rn(__uint_as_float(v[QP + i]));
+                    }
                 }
             }
         }
