@@ -561,9 +561,9 @@ def training_backward(out, timed, kda, _lib, wl, q, k, v, beta, decay, o, stream
         "workload": wl.name + ", backward", "ms_per_call": cms,
         "tokens_per_s": wl.B * wl.T * world / (cms * 1e-3), "gpu_launches_per_call": CHUNK_BWD_LAUNCHES,
         "workspace_bytes": int(wsc.numel()),
-        "note": "chunked on the tensor cores: the forward keeping every chunk's map and fp32 state, "
-                "the reverse walk over the maps (dv, state gradients), the chunk-local gradients "
-                "(tf32 warp MMAs, persistent CTAs)"}
+        "note": "chunked on the tensor cores: the forward keeping every chunk's map and state, "
+                "the reverse walk over the maps (state gradients), the chunk-local gradients of q, "
+                "k, v, beta and the decay (tf32 warp MMAs, persistent CTAs)"}
     del wsc
     wsb = torch.empty(_lib.load().kda_recurrent_bwd_workspace(wl.B, wl.T, wl.H, wl.dk, wl.dv),
                       dtype=torch.uint8, device=dev)
