@@ -9,15 +9,15 @@ served by a C-ABI CUDA library (``libkda.so``, declared in ``include/kda.h``):
 chunked prefill, recurrent prefill, single-token decode and packed varlen prefill;
 and the per-key-channel decay of TileOPs KDAFwdOp (g [B,T,H,dk], ``gk_*``); gradients of
 both recurrences (``recurrent_bwd``, ``gk_recurrent_bwd``; by chunks on the tensor cores,
-``chunk_bwd``).
+``chunk_bwd``, ``gk_chunk_bwd``).
 This package is the thin binding; all compute runs in the library's kernels.
 """
 from ._lib import (KdaError, chunk_bwd, chunk_fwd, chunk_fwd_noalloc, decode_step, diag_wait_timeout,  # noqa: F401
-                   gate_decay, gk_chunk_fwd, gk_decode_step, gk_recurrent_bwd, gk_recurrent_fwd, load,
+                   gate_decay, gk_chunk_bwd, gk_chunk_fwd, gk_decode_step, gk_recurrent_bwd, gk_recurrent_fwd, load,
                    query_device_error, recurrent_bwd, recurrent_fwd, varlen_fwd)
 
 __all__ = ["kda", "chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "recurrent_bwd", "chunk_bwd", "decode_step",
-           "varlen_fwd", "gk_chunk_fwd", "gk_recurrent_fwd", "gk_recurrent_bwd", "gk_decode_step",
+           "varlen_fwd", "gk_chunk_fwd", "gk_recurrent_fwd", "gk_recurrent_bwd", "gk_chunk_bwd", "gk_decode_step",
            "gate_decay",
            "query_device_error",
            "diag_wait_timeout", "load", "KdaError"]

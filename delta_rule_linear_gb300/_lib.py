@@ -29,6 +29,7 @@ EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace", "kda_c
            "kda_gk_chunk_fwd", "kda_gk_varlen_fwd", "kda_gk_recurrent_fwd",
            "kda_gk_recurrent_bwd_workspace", "kda_gk_recurrent_bwd",
            "kda_recurrent_bwd_workspace", "kda_recurrent_bwd", "kda_chunk_bwd_workspace", "kda_chunk_bwd",
+           "kda_gk_chunk_bwd_workspace", "kda_gk_chunk_bwd",
            "kda_gk_varlen_recurrent_fwd", "kda_gk_decode_step", "kda_query_device_error",
            "kda_diag_wait_timeout")
 
@@ -128,6 +129,11 @@ def load(path: str | None = None):
         lib.kda_chunk_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
                                       I, F, I, I, P, Z, P]
         lib.kda_chunk_bwd.restype = I
+        lib.kda_gk_chunk_bwd_workspace.argtypes = [I, I, I, I, I]
+        lib.kda_gk_chunk_bwd_workspace.restype = Z
+        lib.kda_gk_chunk_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
+                                         I, F, I, I, P, Z, P]
+        lib.kda_gk_chunk_bwd.restype = I
         lib.kda_gate_decay.argtypes = [P, P, P, P, ctypes.c_long, I, I, P]
         lib.kda_gate_decay.restype = I
         lib.kda_gk_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, O, P,
@@ -653,4 +659,36 @@ def chunk_bwd(q, k, v, beta, decay, initial_state, d_o, dfinal_state=None, *, sc
                                int(bool(decayed_read)), _ptr(ws), ws.numel() * ws.element_size(),
                                _stream(stream))
     _raise(rc, "kda_chunk_bwd", lib)
+    return out
+
+
+def gk_chunk_bwd(q, k, v, beta, g, initial_state, d_o, dfinal_state=None, *, scale=None,
+                 use_qk_l2norm=True, decayed_read=False, workspace=None, stream=None):
+    """kda_gk_chunk_bwd: the gradients of gk_recurrent_bwd with the two walks on the tensor
+    cores and every chunk's token walk at once (bf16 q/k/v/d_o, dk == dv in {64, 128}).
+    Returns a dict dq, dk, dv, dbeta, dg, dh0."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, (B, T, H, dv))
+    _check(beta, "beta", torch.float32, (B, T, H)); _check(g, "g", torch.float32, q.shape)
+    _check(initial_state, "initial_state", torch.float32, (B, H, dk, dv))
+    _check(d_o, "d_o", q.dtype, (B, T, H, dv))
+    _check(dfinal_state, "dfinal_state", torch.float32, (B, H, dk, dv))
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = dict(dq=torch.empty((B, T, H, dk), **f32), dk=torch.empty((B, T, H, dk), **f32),
+               dv=torch.empty((B, T, H, dv), **f32), dbeta=torch.empty((B, T, H), **f32),
+               dg=torch.empty((B, T, H, dk), **f32), dh0=torch.empty((B, H, dk, dv), **f32))
+    need = lib.kda_gk_chunk_bwd_workspace(B, T, H, dk, dv)
+    if need == 0:
+        raise KdaError(4, "kda_gk_chunk_bwd_workspace", lib)
+    ws = _workspace(need, q.device, workspace)
+    rc = lib.kda_gk_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state),
+                              _ptr(d_o), _ptr(dfinal_state), _ptr(out["dq"]), _ptr(out["dk"]),
+                              _ptr(out["dv"]), _ptr(out["dbeta"]), _ptr(out["dg"]), _ptr(out["dh0"]),
+                              B, T, H, dk, dv, dt, float(scale or 0.0), int(bool(use_qk_l2norm)),
+                              int(bool(decayed_read)), _ptr(ws), ws.numel() * ws.element_size(),
+                              _stream(stream))
+    _raise(rc, "kda_gk_chunk_bwd", lib)
     return out

@@ -2394,18 +2394,22 @@ size_t chunk_tc_keep_bytes(int B, int H, int T, int d) {
 
 cudaError_t launch_chunk_tc_walks(const SeqBatch &a, const void *d_o, const float *dhT, float *dh0, float *dv,
                                   __nv_bfloat16 *fstates, __nv_bfloat16 *bstates, cudaStream_t st) {
-    if ((long)a.nseq * a.T >= (1L << 31) || a.cu_seqlens || a.per_channel) return cudaErrorInvalidValue;
-    const bool opt = a.decayed_read != 0;
+    if ((long)a.nseq * a.T >= (1L << 31) || a.cu_seqlens) return cudaErrorInvalidValue;
+    // the per-channel prep takes the decayed read at run time; the scalar one compiles it in
+    const bool opt = a.decayed_read != 0 && !a.per_channel;
+    const long rows = (long)a.nseq * a.T;
     TcPlan plan{};
     cudaError_t e;
     if (a.dk == 128) {
-        e = opt ? run_tc<128, false, true>(a, (long)a.nseq * a.T, st, fstates, &plan)
-                : run_tc<128, false, false>(a, (long)a.nseq * a.T, st, fstates, &plan);
+        e = a.per_channel ? run_tc<128, true, false>(a, rows, st, fstates, &plan)
+            : opt         ? run_tc<128, false, true>(a, rows, st, fstates, &plan)
+                          : run_tc<128, false, false>(a, rows, st, fstates, &plan);
         return e != cudaSuccess ? e : run_rev<128>(a, plan, d_o, dhT, dh0, dv, bstates, st);
     }
     if (a.dk == 64) {
-        e = opt ? run_tc<64, false, true>(a, (long)a.nseq * a.T, st, fstates, &plan)
-                : run_tc<64, false, false>(a, (long)a.nseq * a.T, st, fstates, &plan);
+        e = a.per_channel ? run_tc<64, true, false>(a, rows, st, fstates, &plan)
+            : opt         ? run_tc<64, false, true>(a, rows, st, fstates, &plan)
+                          : run_tc<64, false, false>(a, rows, st, fstates, &plan);
         return e != cudaSuccess ? e : run_rev<64>(a, plan, d_o, dhT, dh0, dv, bstates, st);
     }
     return cudaErrorInvalidValue;

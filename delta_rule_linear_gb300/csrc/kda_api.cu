@@ -330,6 +330,9 @@ kda_status kda_gk_chunk_fwd(const void *q, const void *k, const void *v, const f
     a.dk = dk; a.dv = dv; a.chunk = chunk_size;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    // without g there is no decay, and the scalar tensor-core path computes the same
+    // recurrence (the per-channel prep reads g)
+    if (!g && chunk_tc_supported(dk, dv, chunk_size, a.dtype)) a.per_channel = 0;
     if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.ws = static_cast<WsHeader *>(ws);
     a.ws_body = static_cast<char *>(ws) + kWsHeader;
@@ -374,6 +377,9 @@ kda_status kda_gk_varlen_fwd(const void *q, const void *k, const void *v, const 
     a.dk = dk; a.dv = dv; a.chunk = chunk_size;
     a.dtype = dtype == KDA_BF16 ? DType::BF16 : DType::F32;
     a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    // without g there is no decay, and the scalar tensor-core path computes the same
+    // recurrence (the per-channel prep reads g)
+    if (!g && chunk_tc_supported(dk, dv, chunk_size, a.dtype)) a.per_channel = 0;
     if ((c = apply_options(opt, g, a)) != KDA_OK) return c;
     a.ws = static_cast<WsHeader *>(ws);
     a.ws_body = static_cast<char *>(ws) + kWsHeader;
@@ -677,4 +683,79 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
         cudaMemsetAsync(ddecay, 0, (size_t)rows * H * sizeof(float), st) != cudaSuccess)
         return KDA_ERR_CUDA;
     return launch_status(launch_chunk_bwd_grads(g, st));
+}
+
+// header | kept maps | kept states | state gradients | the gradient kernel's scratch
+static size_t gk_chunk_bwd_layout(int B, int T, int H, int d, size_t *off_states, size_t *off_dstates,
+                                  size_t *off_scratch) {
+    const size_t keep = (chunk_tc_keep_bytes(B, H, T, d) + 255) / 256 * 256;
+    const size_t st = (size_t)B * H * ((T + 63) / 64) * d * d * 2;   // bf16 states
+    if (off_states) *off_states = kWsHeader + keep;
+    if (off_dstates) *off_dstates = kWsHeader + keep + st;
+    if (off_scratch) *off_scratch = kWsHeader + keep + 2 * st;
+    return kWsHeader + keep + 2 * st + gk_chunk_bwd_scratch_bytes(d);
+}
+
+size_t kda_gk_chunk_bwd_workspace(int B, int T, int H, int dk, int dv) {
+    if (B < 0 || T < 0 || H <= 0 || dk != dv || (dk != 64 && dk != 128)) return 0;
+    if (B == 0 || T == 0) return kWsHeader;
+    return gk_chunk_bwd_layout(B, T, H, dk, nullptr, nullptr, nullptr);
+}
+
+kda_status kda_gk_chunk_bwd(const void *q, const void *k, const void *v, const float *beta,
+                            const float *g, const float *initial_state, const void *d_o,
+                            const float *dfinal_state, float *dq, float *dk_out, float *dv_out,
+                            float *dbeta, float *dg, float *dinitial_state, int B, int T, int H,
+                            int dk, int dv, kda_dtype dtype, float scale, int use_qk_l2norm,
+                            int decayed_read, void *ws, size_t ws_bytes, kda_stream_t stream) {
+    if (B < 0 || T < 0) return KDA_ERR_SHAPE;
+    kda_status c = check_common(q, k, v, beta, nullptr, initial_state, d_o, dfinal_state,
+                                (long)B * T, H, dk, dv, dtype);
+    if (c != KDA_OK) return c;
+    if (dtype != KDA_BF16 || dk != dv || (dk != 64 && dk != 128)) return KDA_ERR_UNSUPPORTED;
+    const long rows = (long)B * T;
+    if (rows >= (1L << 31)) return KDA_ERR_UNSUPPORTED;
+    if (rows > 0 && (!dq || !dk_out || !dv_out || !dbeta)) return KDA_ERR_NULL;
+    if (!aligned16(g) || !aligned16(dinitial_state) || !aligned4(dq) || !aligned4(dk_out) ||
+        !aligned4(dv_out) || !aligned4(dbeta) || !aligned4(dg))
+        return KDA_ERR_ALIGN;
+    const size_t need = kda_gk_chunk_bwd_workspace(B, T, H, dk, dv);
+    if (!ws || ws_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0) {   // nothing but the state: dh0 = dhT
+        if (!dinitial_state || B == 0) return KDA_OK;
+        const size_t n = (size_t)B * H * dk * dv * sizeof(float);
+        if (dfinal_state) return launch_status(cudaMemcpyAsync(dinitial_state, dfinal_state, n, cudaMemcpyDeviceToDevice, st));
+        return launch_status(cudaMemsetAsync(dinitial_state, 0, n, st));
+    }
+    size_t o_st = 0, o_dst = 0, o_scr = 0;
+    gk_chunk_bwd_layout(B, T, H, dk, &o_st, &o_dst, &o_scr);
+    char *w = static_cast<char *>(ws);
+    __nv_bfloat16 *fstates = reinterpret_cast<__nv_bfloat16 *>(w + o_st);
+    __nv_bfloat16 *bstates = reinterpret_cast<__nv_bfloat16 *>(w + o_dst);
+    if (cudaMemsetAsync(ws, 0, sizeof(int) * 2, st) != cudaSuccess) return KDA_ERR_CUDA;
+    // the two walks over the chunk maps: the per-channel prep builds them (without g there is
+    // no decay and the scalar prep's maps are the same)
+    SeqBatch a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.decay = nullptr; a.h0 = initial_state;
+    a.gk = g; a.per_channel = g ? 1 : 0;
+    a.o = nullptr; a.hT = nullptr; a.cu_seqlens = nullptr; a.nseq = B; a.T = T; a.H = H;
+    a.dk = dk; a.dv = dv; a.chunk = 64; a.dtype = DType::BF16;
+    a.scale = resolve_scale(scale, dk); a.use_l2 = use_qk_l2norm ? 1 : 0;
+    a.decayed_read = decayed_read ? 1 : 0;
+    a.ws = static_cast<WsHeader *>(ws);
+    a.ws_body = w + kWsHeader;
+    a.ws_body_bytes = o_st - kWsHeader;
+    cudaError_t e = launch_chunk_tc_walks(a, d_o, dfinal_state, dinitial_state, nullptr, fstates, bstates, st);
+    if (e != cudaSuccess) return launch_status(e);
+    BwdArgs b{};
+    b.q = q; b.k = k; b.v = v; b.dout = d_o; b.beta = beta; b.g = g;
+    b.dq = dq; b.dk = dk_out; b.dv = dv_out; b.dbeta = dbeta; b.dg = g ? dg : nullptr;
+    b.B = B; b.T = T; b.H = H; b.dkdim = dk; b.dvdim = dv; b.dtype = DType::BF16;
+    b.scale = a.scale; b.use_l2 = a.use_l2; b.decayed_read = a.decayed_read;
+    if (!g && dg &&   // dg without g: no decay, a zero gradient
+        cudaMemsetAsync(dg, 0, (size_t)rows * H * dk * sizeof(float), st) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return launch_status(launch_gk_chunk_bwd_grads(b, fstates, bstates, w + o_scr, st));
 }

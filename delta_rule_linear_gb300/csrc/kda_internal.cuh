@@ -91,12 +91,12 @@ bool chunk_tc_supported(int dk, int dv, int chunk, DType dt);
 size_t chunk_tc_scratch_bytes(int nseq, int H, int d, bool varlen);
 // varlen: a.T bounds the longest sequence.
 cudaError_t launch_chunk_tc(const SeqBatch &a, long total_rows, cudaStream_t s);
-// The two walks of the chunked backward (equal-length bf16 batches, per-head decay): a
-// forward launch that keeps every chunk's map and writes the fp32 state at every chunk
-// start (fstates [B, H, nc, D, D]; a.o, a.hT may be nullptr), then the reverse walk
-// [dS_c; dV_c] = E_c^T [dS_{c+1}; dO_c] writing dv (fp32 [B, T, H, D]), dh0 (or nullptr) and
-// the incoming state gradient of every chunk (bstates, same layout).  a.ws_body: at least
-// chunk_tc_keep_bytes().
+// The two walks of the chunked backward (equal-length bf16 batches; one decay per head, or
+// per key channel with a.per_channel): a forward launch that keeps every chunk's map and
+// writes the bf16 state at every chunk start (fstates [B, H, nc, D, D]; a.o, a.hT may be
+// nullptr), then the reverse walk [dS_c; dV_c] = E_c^T [dS_{c+1}; dO_c] writing dv (fp32
+// [B, T, H, D], or nullptr: not written), dh0 (or nullptr) and the gradient of the state
+// leaving every chunk (bstates, same layout).  a.ws_body: at least chunk_tc_keep_bytes().
 size_t chunk_tc_keep_bytes(int B, int H, int T, int d);
 cudaError_t launch_chunk_tc_walks(const SeqBatch &a, const void *d_o, const float *dhT, float *dh0, float *dv,
                                   __nv_bfloat16 *fstates, __nv_bfloat16 *bstates, cudaStream_t s);
@@ -139,6 +139,13 @@ struct BwdArgs {
 };
 size_t gk_bwd_scratch_bytes(int nseq, int T, int H, int dk, int dv);
 cudaError_t launch_gk_bwd(const BwdArgs &a, cudaStream_t s);
+// The gradient kernels of the per-channel chunked backward (bf16, dk == dv in {64, 128}):
+// every 64-token chunk walked token by token on its own, from the state entering it and the
+// gradient of the state leaving it (fstates, bstates as launch_chunk_tc_walks writes them),
+// then the gradients of the raw q, k.  scratch: gk_chunk_bwd_scratch_bytes(dk) (a.ws unused).
+size_t gk_chunk_bwd_scratch_bytes(int dk);
+cudaError_t launch_gk_chunk_bwd_grads(const BwdArgs &a, const __nv_bfloat16 *fstates,
+                                      const __nv_bfloat16 *bstates, void *scratch, cudaStream_t s);
 
 // L2 normalisation floor: x / max(||x||, kNormEps).
 constexpr float kNormEps = 1e-12f;

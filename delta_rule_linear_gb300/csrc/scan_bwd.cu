@@ -20,6 +20,7 @@
 // columns (everything above is separable in j except the sums over j, which go to fp32
 // accumulators by atomic adds).  A last kernel turns the gradients of k^ and q~ into those
 // of the raw k and q (through the L2 normalisation and the scale).
+#include <algorithm>
 #include <cstddef>
 
 #include "kda_internal.cuh"
@@ -41,6 +42,12 @@ struct BwdParams {
     float *ckpt;                              // [nseq, H, nc, DK, DV]
     float *scratch;                           // [grid, kBwdChunk, DK, DVS]
     int nseq, T, H, DV, nc;
+    // the chunk-parallel walk (bwd_chunk_kernel): the state entering every 64-token chunk and
+    // the gradient of the state leaving it, bf16 key-major [nseq, H, nc64, DK, DK], and a bf16
+    // scratch [grid, 64, DK, DVS] for the recomputed states
+    const __nv_bfloat16 *fstates, *bstates;
+    __nv_bfloat16 *scratch16;
+    int nc64;
     float scale;
     int use_l2, decayed_read;
 };
@@ -267,6 +274,92 @@ __device__ __forceinline__ float row_sum(float x) {
     return x;
 }
 
+// One token of the backward walk: the stage holds token `row` (synced by the caller), Hp is
+// the state before it and Hc the state after it (Hc becomes Hp on return), dH the gradient
+// of the state after it on entry and of the state before it on return.  Writes the token's
+// dv columns and adds its shares of dbeta, dq~, dk^, dg and ddecay.  Two syncs.
+template <int DK, int DVS, int RG, int R, bool DR>
+__device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<DK, DVS> &s, long row, int h,
+                                               int col0, float4 (&dH)[R], float4 (&Hc)[R], const float4 (&Hp)[R],
+                                               float (*s_red)[RG][DVS], float *s_u, float *s_du, float *s_db) {
+    constexpr int TPR = DVS / 4;
+    constexpr int kOwnerWarps = RG <= 8 ? (DVS + 31) / 32 : kThreads / 32;   // warps holding column sums
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid % TPR, rg = tid / TPR;
+    float kn, qn;
+    token_norms(p, s, kn, qn);
+    const float bt = s.beta;
+    const float4 do4 = *reinterpret_cast<const float4 *>(&s.d[4 * cg]);
+    // dh += q~ do^T;  r = R^T k^;  du = dh^T k^   (both row sums through shared memory)
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f), du = r;
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int i = rg + RG * m;
+        const float qq = s.q[i] * qn, kk = s.k[i] * kn, kx = DR ? s.a[i] * kk : kk;
+        dH[m].x = fmaf(qq, do4.x, dH[m].x); dH[m].y = fmaf(qq, do4.y, dH[m].y);
+        dH[m].z = fmaf(qq, do4.z, dH[m].z); dH[m].w = fmaf(qq, do4.w, dH[m].w);
+        r.x = fmaf(Hp[m].x, kx, r.x); r.y = fmaf(Hp[m].y, kx, r.y);
+        r.z = fmaf(Hp[m].z, kx, r.z); r.w = fmaf(Hp[m].w, kx, r.w);
+        du.x = fmaf(dH[m].x, kk, du.x); du.y = fmaf(dH[m].y, kk, du.y);
+        du.z = fmaf(dH[m].z, kk, du.z); du.w = fmaf(dH[m].w, kk, du.w);
+    }
+    *reinterpret_cast<float4 *>(&s_red[0][rg][4 * cg]) = r;
+    *reinterpret_cast<float4 *>(&s_red[1][rg][4 * cg]) = du;
+    __syncthreads();
+    float dbp = 0.f;   // this column's share of dbeta
+    {
+        int j;
+        float rs, ds;
+        if (column_sums<DVS, RG, true>(s_red[0], s_red[1], tid, j, rs, ds)) {
+            s_u[j] = bt * (s.v[j] - rs);
+            s_du[j] = ds;
+            p.dv[((size_t)row * p.H + h) * p.DV + col0 + j] = bt * ds;
+            dbp = ds * (s.v[j] - rs);
+        }
+    }
+    if (warp < kOwnerWarps) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dbp += __shfl_xor_sync(0xffffffffu, dbp, off);
+        if (lane == 0) s_db[warp] = dbp;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float sum = 0.f;
+        for (int w = 0; w < kOwnerWarps; ++w) sum += s_db[w];
+        atomicAdd(p.dbeta + (size_t)row * p.H + h, sum);
+    }
+    const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
+    const float4 du4 = *reinterpret_cast<const float4 *>(&s_du[4 * cg]);
+    const size_t kd_off = ((size_t)row * p.H + h) * DK;
+    float dd = 0.f;   // one decay per head: sum over this thread's rows of a_i de_i
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int i = rg + RG * m;
+        const float a = s.a[i], kk = s.k[i] * kn;
+        // sums over this thread's four columns, then over the row's TPR threads
+        float dq_i = row_sum<TPR>(dot4(Hc[m], do4));
+        const float hu = dot4(Hp[m], du4);   // sum_j h_{t-1}[i,j] du_j
+        float dk_i = row_sum<TPR>(dot4(dH[m], u4) - bt * (DR ? a : 1.f) * hu);
+        float de_i = row_sum<TPR>(dot4(dH[m], Hp[m]) - (DR ? bt * kk * hu : 0.f));
+        if (cg == 0) {
+            atomicAdd(p.dq + kd_off + i, dq_i);
+            atomicAdd(p.dk + kd_off + i, dk_i);
+            if (p.dg) atomicAdd(p.dg + kd_off + i, a * de_i);
+        }
+        dd = fmaf(a, de_i, dd);
+        // dh for the state before token t
+        const float kb = bt * (DR ? a * kk : kk);
+        dH[m].x = fmaf(a, dH[m].x, -kb * du4.x); dH[m].y = fmaf(a, dH[m].y, -kb * du4.y);
+        dH[m].z = fmaf(a, dH[m].z, -kb * du4.z); dH[m].w = fmaf(a, dH[m].w, -kb * du4.w);
+        Hc[m] = Hp[m];
+    }
+    if (p.ddecay) {   // the row groups of the warp (every lane of a group holds its sum)
+#pragma unroll
+        for (int off = TPR; off < 32; off <<= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
+        if (lane == 0) atomicAdd(p.ddecay + (size_t)row * p.H + h, dd);
+    }
+}
+
 // Backward pass, per (sequence, head, slab).  Inputs fetched one token ahead (forwards in the
 // recomputation, backwards in the walk) into a double-buffered stage, as in the forward pass.
 template <typename Tin, int DK, int DVS, bool DR>
@@ -274,7 +367,6 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
     using Ly = BwdLayout<DVS>;
     constexpr int TPR = Ly::TPR, RG = Ly::RG, R = DK / RG;
     static_assert(TPR <= 32 && 32 % TPR == 0, "a state row lies within one warp");
-    constexpr int kOwnerWarps = RG <= 8 ? (DVS + 31) / 32 : kThreads / 32;   // warps holding column sums
     static_assert(stage_aligned<DK, DVS>(), "both stage buffers 16-byte aligned");
     __shared__ __align__(16) Stage<DK, DVS> st[2];
     __shared__ __align__(16) float s_red[2][RG][DVS];
@@ -283,7 +375,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
     __shared__ float s_db[kThreads / 32];
     const int nslab = p.DV / DVS;
     const int slab = blockIdx.x % nslab, h = (blockIdx.x / nslab) % p.H, n = blockIdx.x / (nslab * p.H);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int cg = tid % TPR, rg = tid / TPR, col0 = slab * DVS;
     const size_t sb = ((size_t)n * p.H + h) * DK * p.DV + col0 + 4 * cg;
     float *scr = p.scratch + (size_t)blockIdx.x * kBwdChunk * DK * DVS + 4 * cg;   // [t][i][j] slab
@@ -326,84 +418,104 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
             put_token<Tin, DK, DVS>(p, cur, true, s);
             __syncthreads();
             if (t > t0) fetch_token<Tin, DK, DVS>(p, row - 1, h, col0, true, nxt);
-            float kn, qn;
-            token_norms(p, s, kn, qn);
-            const float bt = s.beta;
-            const float4 do4 = *reinterpret_cast<const float4 *>(&s.d[4 * cg]);
-            // dh += q~ do^T;  r = R^T k^;  du = dh^T k^   (both row sums through shared memory)
-            float4 r = make_float4(0.f, 0.f, 0.f, 0.f), du = r;
-#pragma unroll
-            for (int m = 0; m < R; ++m) {
-                const int i = rg + RG * m;
-                const float qq = s.q[i] * qn, kk = s.k[i] * kn, kx = DR ? s.a[i] * kk : kk;
-                dH[m].x = fmaf(qq, do4.x, dH[m].x); dH[m].y = fmaf(qq, do4.y, dH[m].y);
-                dH[m].z = fmaf(qq, do4.z, dH[m].z); dH[m].w = fmaf(qq, do4.w, dH[m].w);
-                r.x = fmaf(Hp[m].x, kx, r.x); r.y = fmaf(Hp[m].y, kx, r.y);
-                r.z = fmaf(Hp[m].z, kx, r.z); r.w = fmaf(Hp[m].w, kx, r.w);
-                du.x = fmaf(dH[m].x, kk, du.x); du.y = fmaf(dH[m].y, kk, du.y);
-                du.z = fmaf(dH[m].z, kk, du.z); du.w = fmaf(dH[m].w, kk, du.w);
-            }
-            *reinterpret_cast<float4 *>(&s_red[0][rg][4 * cg]) = r;
-            *reinterpret_cast<float4 *>(&s_red[1][rg][4 * cg]) = du;
-            __syncthreads();
-            float dbp = 0.f;   // this column's share of dbeta
-            {
-                int j;
-                float rs, ds;
-                if (column_sums<DVS, RG, true>(s_red[0], s_red[1], tid, j, rs, ds)) {
-                    s_u[j] = bt * (s.v[j] - rs);
-                    s_du[j] = ds;
-                    p.dv[((size_t)row * p.H + h) * p.DV + col0 + j] = bt * ds;
-                    dbp = ds * (s.v[j] - rs);
-                }
-            }
-            if (warp < kOwnerWarps) {
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) dbp += __shfl_xor_sync(0xffffffffu, dbp, off);
-                if (lane == 0) s_db[warp] = dbp;
-            }
-            __syncthreads();
-            if (tid == 0) {
-                float sum = 0.f;
-                for (int w = 0; w < kOwnerWarps; ++w) sum += s_db[w];
-                atomicAdd(p.dbeta + (size_t)row * p.H + h, sum);
-            }
-            const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
-            const float4 du4 = *reinterpret_cast<const float4 *>(&s_du[4 * cg]);
-            const size_t kd_off = ((size_t)row * p.H + h) * DK;
-            float dd = 0.f;   // one decay per head: sum over this thread's rows of a_i de_i
-#pragma unroll
-            for (int m = 0; m < R; ++m) {
-                const int i = rg + RG * m;
-                const float a = s.a[i], kk = s.k[i] * kn;
-                // sums over this thread's four columns, then over the row's TPR threads
-                float dq_i = row_sum<TPR>(dot4(Hc[m], do4));
-                const float hu = dot4(Hp[m], du4);   // sum_j h_{t-1}[i,j] du_j
-                float dk_i = row_sum<TPR>(dot4(dH[m], u4) - bt * (DR ? a : 1.f) * hu);
-                float de_i = row_sum<TPR>(dot4(dH[m], Hp[m]) - (DR ? bt * kk * hu : 0.f));
-                if (cg == 0) {
-                    atomicAdd(p.dq + kd_off + i, dq_i);
-                    atomicAdd(p.dk + kd_off + i, dk_i);
-                    if (p.dg) atomicAdd(p.dg + kd_off + i, a * de_i);
-                }
-                dd = fmaf(a, de_i, dd);
-                // dh for the state before token t
-                const float kb = bt * (DR ? a * kk : kk);
-                dH[m].x = fmaf(a, dH[m].x, -kb * du4.x); dH[m].y = fmaf(a, dH[m].y, -kb * du4.y);
-                dH[m].z = fmaf(a, dH[m].z, -kb * du4.z); dH[m].w = fmaf(a, dH[m].w, -kb * du4.w);
-                Hc[m] = Hp[m];
-            }
-            if (p.ddecay) {   // the row groups of the warp (every lane of a group holds its sum)
-#pragma unroll
-                for (int off = TPR; off < 32; off <<= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
-                if (lane == 0) atomicAdd(p.ddecay + (size_t)row * p.H + h, dd);
-            }
+            backward_token<DK, DVS, RG, R, DR>(p, s, row, h, col0, dH, Hc, Hp, s_red, s_u, s_du, s_db);
             cur = nxt;
         }
     }
     if (p.dh0) {
 #pragma unroll
         for (int m = 0; m < R; ++m) *reinterpret_cast<float4 *>(p.dh0 + sb + (size_t)(rg + RG * m) * p.DV) = dH[m];
+    }
+}
+
+// Chunk-parallel backward (bf16, dk == dv): the same token walk, but every 64-token chunk on
+// its own.  A forward launch on the tensor cores keeps the state entering each chunk, and
+// the reverse walk over the chunk maps gives the gradient of the state leaving it (both in
+// bf16); with those a unit -- (chunk, sequence, head, value slab) -- depends on no other
+// unit: it recomputes its chunk's states into its scratch (bf16) and walks them in reverse,
+// adding its shares of dq~, dk^, dbeta and dg as the sequential walk does.  Persistent
+// CTAs take the units in (chunk, sequence, head, slab) order, so that the CTAs running at
+// one time read the same tokens; the state before the next token of the reverse walk is
+// loaded one token ahead.
+constexpr int kUnitTokens = 64;   // the tensor-core chunk
+constexpr int kUnitSlab = 32;     // value columns per unit
+constexpr int kChunkBwdCtas = 304;   // persistent CTAs (two per SM on 152 SMs)
+
+__device__ __forceinline__ float4 ld_bf16x4(const __nv_bfloat16 *src) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(src);
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+__device__ __forceinline__ void st_bf16x4(__nv_bfloat16 *dst, float4 v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(*reinterpret_cast<const uint32_t *>(&a),
+                                                 *reinterpret_cast<const uint32_t *>(&b));
+}
+
+template <int DK, int DVS, bool DR>
+__global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
+    using Tin = __nv_bfloat16;
+    using Ly = BwdLayout<DVS>;
+    constexpr int TPR = Ly::TPR, RG = Ly::RG, R = DK / RG;
+    static_assert(TPR <= 32 && 32 % TPR == 0, "a state row lies within one warp");
+    static_assert(stage_aligned<DK, DVS>(), "both stage buffers 16-byte aligned");
+    __shared__ __align__(16) Stage<DK, DVS> st[2];
+    __shared__ __align__(16) float s_red[2][RG][DVS];
+    __shared__ __align__(16) float s_u[DVS];
+    __shared__ __align__(16) float s_du[DVS];
+    __shared__ float s_db[kThreads / 32];
+    const int tid = threadIdx.x, cg = tid % TPR, rg = tid / TPR;
+    constexpr int nslab = DK / DVS;   // dv == dk
+    const long units = (long)p.nc64 * p.nseq * p.H * nslab;
+    // this thread's element of the scratch: [token][row][column] of the unit's slab
+    __nv_bfloat16 *scr = p.scratch16 + (size_t)blockIdx.x * kUnitTokens * DK * DVS + 4 * cg;
+    TokenRegs<Tin> cur{}, nxt{};
+    int it = 0;   // tokens staged so far: selects the stage buffer
+    for (long u = blockIdx.x; u < units; u += gridDim.x) {
+        const int slab = (int)(u % nslab);
+        const long r = u / nslab;
+        const int h = (int)(r % p.H), n = (int)((r / p.H) % p.nseq), c = (int)(r / ((long)p.H * p.nseq));
+        const int col0 = slab * DVS;
+        const int t0 = c * kUnitTokens, t1 = min(p.T, t0 + kUnitTokens);
+        const size_t kb = (((size_t)n * p.H + h) * p.nc64 + c) * DK * DK + col0 + 4 * cg;
+        float4 dH[R], Hc[R], Hp[R], Hn[R];
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            Hp[m] = ld_bf16x4(p.fstates + kb + (size_t)(rg + RG * m) * DK);
+            dH[m] = ld_bf16x4(p.bstates + kb + (size_t)(rg + RG * m) * DK);
+        }
+        // the chunk's states, each before its token, into the scratch
+        fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t0, h, col0, false, cur);
+        for (int t = t0; t < t1; ++t, ++it) {
+#pragma unroll
+            for (int m = 0; m < R; ++m) st_bf16x4(scr + ((size_t)(t - t0) * DK + rg + RG * m) * DVS, Hp[m]);
+            Stage<DK, DVS> &s = st[it & 1];
+            put_token<Tin, DK, DVS>(p, cur, false, s);
+            __syncthreads();
+            if (t + 1 < t1) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + 1, h, col0, false, nxt);
+            forward_token<DK, DVS, RG, R, DR>(p, s, Hp, s_red[0], s_u);
+            cur = nxt;
+        }
+#pragma unroll
+        for (int m = 0; m < R; ++m) Hc[m] = Hp[m];   // the state after the chunk's last token
+        // the walk back (each thread reads back only what it wrote)
+        fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t1 - 1, h, col0, true, cur);
+#pragma unroll
+        for (int m = 0; m < R; ++m) Hn[m] = ld_bf16x4(scr + ((size_t)(t1 - 1 - t0) * DK + rg + RG * m) * DVS);
+        for (int t = t1 - 1; t >= t0; --t, ++it) {
+            const long row = (long)n * p.T + t;
+#pragma unroll
+            for (int m = 0; m < R; ++m) Hp[m] = Hn[m];
+            if (t > t0)
+#pragma unroll
+                for (int m = 0; m < R; ++m) Hn[m] = ld_bf16x4(scr + ((size_t)(t - 1 - t0) * DK + rg + RG * m) * DVS);
+            Stage<DK, DVS> &s = st[it & 1];
+            put_token<Tin, DK, DVS>(p, cur, true, s);
+            __syncthreads();
+            if (t > t0) fetch_token<Tin, DK, DVS>(p, row - 1, h, col0, true, nxt);
+            backward_token<DK, DVS, RG, R, DR>(p, s, row, h, col0, dH, Hc, Hp, s_red, s_u, s_du, s_db);
+            cur = nxt;
+        }
     }
 }
 
@@ -522,6 +634,50 @@ cudaError_t launch_gk_bwd(const BwdArgs &a, cudaStream_t s) {
         case 128: return bf ? run_bwd<__nv_bfloat16, 128>(p, rows, s) : run_bwd<float, 128>(p, rows, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+
+size_t gk_chunk_bwd_scratch_bytes(int dk) {
+    return (size_t)kChunkBwdCtas * kUnitTokens * dk * kUnitSlab * sizeof(__nv_bfloat16);
+}
+
+cudaError_t launch_gk_chunk_bwd_grads(const BwdArgs &a, const __nv_bfloat16 *fstates,
+                                      const __nv_bfloat16 *bstates, void *scratch, cudaStream_t s) {
+    if (a.dtype != DType::BF16 || a.dkdim != a.dvdim || (a.dkdim != 64 && a.dkdim != 128))
+        return cudaErrorInvalidValue;
+    BwdParams p{};
+    p.q = a.q; p.k = a.k; p.v = a.v; p.dout = a.dout;
+    p.beta = a.beta; p.gk = a.g; p.h0 = nullptr; p.dhT = nullptr;
+    p.decay = nullptr; p.ddecay = nullptr;
+    p.dq = a.dq; p.dk = a.dk; p.dv = a.dv; p.dbeta = a.dbeta; p.dg = a.dg; p.dh0 = nullptr;
+    p.nseq = a.B; p.T = a.T; p.H = a.H; p.DV = a.dvdim;
+    p.scale = a.scale; p.use_l2 = a.use_l2; p.decayed_read = a.decayed_read;
+    p.fstates = fstates; p.bstates = bstates;
+    p.scratch16 = static_cast<__nv_bfloat16 *>(scratch);
+    p.nc64 = (a.T + kUnitTokens - 1) / kUnitTokens;
+    const long rows = (long)a.B * a.T;
+    cudaError_t e;
+    // the sums over value slabs accumulate into these
+    const size_t nk = (size_t)rows * a.H * a.dkdim * sizeof(float);
+    if ((e = cudaMemsetAsync(a.dq, 0, nk, s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.dk, 0, nk, s)) != cudaSuccess) return e;
+    if (a.dg && (e = cudaMemsetAsync(a.dg, 0, nk, s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.dbeta, 0, (size_t)rows * a.H * sizeof(float), s)) != cudaSuccess) return e;
+    const long units = (long)p.nc64 * a.B * a.H * (a.dkdim / kUnitSlab);
+    const unsigned grid = (unsigned)std::min<long>(units, kChunkBwdCtas);
+    const bool dr = p.decayed_read != 0;
+    if (a.dkdim == 128) {
+        if (dr) bwd_chunk_kernel<128, kUnitSlab, true><<<grid, kThreads, 0, s>>>(p);
+        else bwd_chunk_kernel<128, kUnitSlab, false><<<grid, kThreads, 0, s>>>(p);
+    } else {
+        if (dr) bwd_chunk_kernel<64, kUnitSlab, true><<<grid, kThreads, 0, s>>>(p);
+        else bwd_chunk_kernel<64, kUnitSlab, false><<<grid, kThreads, 0, s>>>(p);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const long rh = rows * a.H;
+    if (a.dkdim == 128) bwd_finish_kernel<__nv_bfloat16, 128><<<(unsigned)((rh * 32 + 255) / 256), 256, 0, s>>>(p, rh);
+    else bwd_finish_kernel<__nv_bfloat16, 64><<<(unsigned)((rh * 32 + 255) / 256), 256, 0, s>>>(p, rh);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

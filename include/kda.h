@@ -406,6 +406,34 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v,
                          void *ws, size_t ws_bytes, kda_stream_t stream);
 
 /*
+ * Chunked backward with per-key-channel decay: the same gradients as kda_gk_recurrent_bwd
+ * (dq, dk, dv, dbeta, dg, dinitial_state; TileOPs KDAFwdOp's recurrence, kda-neuron-kernels
+ * README kda_chunk_step_exact_bwd) for the bf16 tensor-core shapes (dtype KDA_BF16, dk == dv
+ * in {64, 128}; anything else returns KDA_ERR_UNSUPPORTED).  The two walks are those of
+ * kda_chunk_bwd: a forward launch that keeps every chunk's map (built with the per-channel
+ * factors, as kda_gk_chunk_fwd builds it) and the state entering every chunk, and the
+ * reverse walk over the maps, which gives the gradient of the state leaving every chunk and
+ * dinitial_state.  With both in hand every 64-token chunk is independent: the gradient
+ * kernel walks each (chunk, head, 32 value columns) token by token, recomputing the chunk's
+ * states from the kept one, all chunks at once.  Arguments, layouts and errors as
+ * kda_gk_recurrent_bwd; g NULL means no decay (dg, if given, is zero-filled).  Arithmetic:
+ * the maps, the kept states and state gradients and the recomputed states are bf16 (the
+ * precision of the forward's tensor-core operands); every sum is fp32.  ws: at least
+ * kda_gk_chunk_bwd_workspace() bytes, 16-byte aligned (every chunk's map and two bf16
+ * states per chunk, ~136 KB per chunk and head at head dim 128, plus a fixed scratch of
+ * 304 x 512 KB at head dim 128).
+ */
+size_t kda_gk_chunk_bwd_workspace(int B, int T, int H, int dk, int dv);
+kda_status kda_gk_chunk_bwd(const void *q, const void *k, const void *v,
+                            const float *beta, const float *g,
+                            const float *initial_state, const void *d_o,
+                            const float *dfinal_state, float *dq, float *dk_out, float *dv_out,
+                            float *dbeta, float *dg, float *dinitial_state,
+                            int B, int T, int H, int dk, int dv, kda_dtype dtype,
+                            float scale, int use_qk_l2norm, int decayed_read,
+                            void *ws, size_t ws_bytes, kda_stream_t stream);
+
+/*
  * Read the device error word that the kernels of the most recent kda_chunk_fwd /
  * kda_varlen_fwd call on `ws` recorded (KDA_OK if none), then clear it.  Each of
  * those calls clears the word on its stream before its kernels run.  ws == NULL reads
