@@ -327,6 +327,7 @@ def prefill_workload(args):
 # (the forward keeping every chunk's map and state, the reverse walk, the chunk-local
 # gradients); the token-by-token backward is three (checkpoints, reverse walk, finish).
 TC_PREFILL_LAUNCHES, VARLEN_LAUNCHES, CHUNK_BWD_LAUNCHES, RECURRENT_BWD_LAUNCHES = 1, 2, 3, 3
+GK_CHUNK_BWD_LAUNCHES = 4   # kept-map forward, reverse walk, chunk-parallel token walks, q/k finish
 
 
 def prefill_min_bytes(tokens, H, dk, dv, has_decay, nseq, h0_in):
@@ -764,6 +765,32 @@ def bench_gk(args, world, rank, dev, peaks):
         "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D), "decayed_read": True, "ms_per_call": bms,
         "tokens_per_s": Bp * T * world / (bms * 1e-3), "calls": nrep, "gpu_launches_per_call": RECURRENT_BWD_LAUNCHES,
         "note": "token by token on CUDA cores: 32-token checkpoints, recompute, reverse walk"}
+    del wsb
+    wsc = torch.empty(_lib.load().kda_gk_chunk_bwd_workspace(Bp, T, Hp, D, D), dtype=torch.uint8,
+                      device=dev)
+
+    def cstep():
+        kda.gk_chunk_bwd(q, k, v, beta, gates, h0z, d_o, None, decayed_read=True, workspace=wsc,
+                         stream=stream)
+
+    for _ in range(max(1, args.warmup)):
+        cstep()
+    torch.cuda.synchronize()
+    crep = max(1, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(crep):
+        cstep()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    cms = max_over_ranks(e0.elapsed_time(e1) / crep, world)
+    out["gk_chunk_bwd"] = {
+        "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D), "decayed_read": True, "ms_per_call": cms,
+        "tokens_per_s": Bp * T * world / (cms * 1e-3), "calls": crep,
+        "gpu_launches_per_call": GK_CHUNK_BWD_LAUNCHES, "workspace_bytes": int(wsc.numel()),
+        "note": "the forward keeping every chunk's per-channel map and state and the reverse walk "
+                "over the maps on the tensor cores, then every 64-token chunk's token walk at once "
+                "(CUDA cores, persistent CTAs)"}
+    del wsc
     out["gk_recurrent_prefill"] = {
         "shape": dict(B=Bp, T=T, H=Hp, dk=D, dv=D), "decayed_read": True, "ms_per_call": ms,
         "tokens_per_s": Bp * T * world / (ms * 1e-3), "calls": nrep, "gpu_launches_per_call": 1,

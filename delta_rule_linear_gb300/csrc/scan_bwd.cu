@@ -331,6 +331,51 @@ __device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<D
     const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
     const float4 du4 = *reinterpret_cast<const float4 *>(&s_du[4 * cg]);
     const size_t kd_off = ((size_t)row * p.H + h) * DK;
+    if constexpr (TPR == 8 && R == 4) {
+        // The twelve row sums of this thread's rows (dq, dk, de of each of its four rows) by a
+        // transposing reduction over the 8 lanes of the row group: each step halves the values
+        // a lane carries (12 shuffles instead of 36), and lanes 2m, 2m + 1 of the group end
+        // with row m's three sums.
+        float x[12];
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            const int i = rg + RG * m;
+            const float a = s.a[i], kk = s.k[i] * kn;
+            const float hu = dot4(Hp[m], du4);   // sum_j h_{t-1}[i,j] du_j
+            x[3 * m] = dot4(Hc[m], do4);
+            x[3 * m + 1] = dot4(dH[m], u4) - bt * (DR ? a : 1.f) * hu;
+            x[3 * m + 2] = dot4(dH[m], Hp[m]) - (DR ? bt * kk * hu : 0.f);
+            // dh for the state before token t
+            const float kb = bt * (DR ? a * kk : kk);
+            dH[m].x = fmaf(a, dH[m].x, -kb * du4.x); dH[m].y = fmaf(a, dH[m].y, -kb * du4.y);
+            dH[m].z = fmaf(a, dH[m].z, -kb * du4.z); dH[m].w = fmaf(a, dH[m].w, -kb * du4.w);
+            Hc[m] = Hp[m];
+        }
+        const bool hi4 = (cg & 4) != 0, hi2 = (cg & 2) != 0;
+        float y[6], z[3];
+#pragma unroll
+        for (int v = 0; v < 6; ++v)   // rows 0, 1 stay with cg < 4, rows 2, 3 with cg >= 4
+            y[v] = (hi4 ? x[6 + v] : x[v]) + __shfl_xor_sync(0xffffffffu, hi4 ? x[v] : x[6 + v], 4);
+#pragma unroll
+        for (int v = 0; v < 3; ++v)   // then the even row with bit 1 clear, the odd one with it set
+            z[v] = (hi2 ? y[3 + v] : y[v]) + __shfl_xor_sync(0xffffffffu, hi2 ? y[v] : y[3 + v], 2);
+#pragma unroll
+        for (int v = 0; v < 3; ++v) z[v] += __shfl_xor_sync(0xffffffffu, z[v], 1);
+        const int i = rg + RG * ((cg >> 1) & 3);
+        const float a = s.a[i];
+        if ((cg & 1) == 0) {
+            atomicAdd(p.dq + kd_off + i, z[0]);
+            atomicAdd(p.dk + kd_off + i, z[1]);
+            if (p.dg) atomicAdd(p.dg + kd_off + i, a * z[2]);
+        }
+        if (p.ddecay) {   // one decay per head: sum over the warp's rows of a_i de_i
+            float dd = (cg & 1) == 0 ? a * z[2] : 0.f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
+            if (lane == 0) atomicAdd(p.ddecay + (size_t)row * p.H + h, dd);
+        }
+        return;
+    }
     float dd = 0.f;   // one decay per head: sum over this thread's rows of a_i de_i
 #pragma unroll
     for (int m = 0; m < R; ++m) {

@@ -266,6 +266,23 @@ def test_chunk_training_shape(kda, oracle_mod, dev):
     assert_parity("bf16", o, ro, h, rh, tag="gk chunk training shape")
 
 
+@pytest.mark.parametrize("packed", [False, True])
+def test_chunk_without_gate(kda, oracle_mod, dev, packed):
+    """g = None on the tensor-core shapes (bf16, d = 128, chunk 64), equal-length and packed:
+    no decay, against the oracle with no gate."""
+    import torch
+    kw = dict(lengths=[70, 1, 200]) if packed else {}
+    d = make_gk(2, 130, 2, 128, 128, dtype="bf16", gate_scale=0.1, h0="normal002", seed=39, **kw)
+    t = _dev_inputs(d, dev, "bf16")
+    extra = dict(cu_seqlens_cpu=torch.from_numpy(d["cu_seqlens"])) if packed else {}
+    o, h = kda.gk_chunk_fwd(t["q"], t["k"], t["v"], t["beta"], None, t["h0"],
+                            cu_seqlens=t.get("cu_seqlens"), check_device=True, **extra)
+    torch.cuda.synchronize()
+    ro, rh = oracle_mod.forward_gk(d["q"], d["k"], d["v"], d["beta"], None, d["h0"],
+                                   cu_seqlens=d.get("cu_seqlens"))
+    assert_parity("bf16", to_np(o), ro, to_np(h), rh, tag=f"gk chunk without gate packed={packed}")
+
+
 def test_chunk_matches_recurrent_kernel(kda, dev):
     """The chunked and token-by-token per-channel kernels agree (bf16 rounding of E_c)."""
     import torch
