@@ -185,9 +185,10 @@ __device__ __forceinline__ bool column_sums(const float (*a)[DVS], const float (
 
 // One token of the forward recurrence on this thread's rows of the slab (S: the state before
 // the token on entry, after it on return).  The stage was synced by the caller; two syncs.
+// y_out (optional, DVS floats): the token's v - r, kept for its backward step.
 template <int DK, int DVS, int RG, int R, bool DR>
 __device__ __forceinline__ void forward_token(const BwdParams &p, const Stage<DK, DVS> &s, float4 (&S)[R],
-                                              float (*s_red)[DVS], float *s_u) {
+                                              float (*s_red)[DVS], float *s_u, float *y_out = nullptr) {
     const int tid = threadIdx.x, cg = tid % (DVS / 4), rg = tid / (DVS / 4);
     float kn, qn;
     token_norms(p, s, kn, qn);
@@ -204,7 +205,11 @@ __device__ __forceinline__ void forward_token(const BwdParams &p, const Stage<DK
     {
         int j;
         float rs, unused;
-        if (column_sums<DVS, RG, false>(s_red, s_red, tid, j, rs, unused)) s_u[j] = s.beta * (s.v[j] - rs);
+        if (column_sums<DVS, RG, false>(s_red, s_red, tid, j, rs, unused)) {
+            const float y = s.v[j] - rs;
+            s_u[j] = s.beta * y;
+            if (y_out) y_out[j] = y;
+        }
     }
     __syncthreads();
     const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * cg]);
@@ -277,11 +282,13 @@ __device__ __forceinline__ float row_sum(float x) {
 // One token of the backward walk: the stage holds token `row` (synced by the caller), Hp is
 // the state before it and Hc the state after it (Hc becomes Hp on return), dH the gradient
 // of the state after it on entry and of the state before it on return.  Writes the token's
-// dv columns and adds its shares of dbeta, dq~, dk^, dg and ddecay.  Two syncs.
-template <int DK, int DVS, int RG, int R, bool DR>
+// dv columns and adds its shares of dbeta, dq~, dk^, dg and ddecay.  Two syncs.  KY: the
+// token's v - r was kept by its forward step (ys, DVS floats) and is not recomputed.
+template <int DK, int DVS, int RG, int R, bool DR, bool KY = false>
 __device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<DK, DVS> &s, long row, int h,
                                                int col0, float4 (&dH)[R], float4 (&Hc)[R], const float4 (&Hp)[R],
-                                               float (*s_red)[RG][DVS], float *s_u, float *s_du, float *s_db) {
+                                               float (*s_red)[RG][DVS], float *s_u, float *s_du, float *s_db,
+                                               const float *ys = nullptr) {
     constexpr int TPR = DVS / 4;
     constexpr int kOwnerWarps = RG <= 8 ? (DVS + 31) / 32 : kThreads / 32;   // warps holding column sums
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -298,23 +305,28 @@ __device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<D
         const float qq = s.q[i] * qn, kk = s.k[i] * kn, kx = DR ? s.a[i] * kk : kk;
         dH[m].x = fmaf(qq, do4.x, dH[m].x); dH[m].y = fmaf(qq, do4.y, dH[m].y);
         dH[m].z = fmaf(qq, do4.z, dH[m].z); dH[m].w = fmaf(qq, do4.w, dH[m].w);
-        r.x = fmaf(Hp[m].x, kx, r.x); r.y = fmaf(Hp[m].y, kx, r.y);
-        r.z = fmaf(Hp[m].z, kx, r.z); r.w = fmaf(Hp[m].w, kx, r.w);
+        if (!KY) {
+            r.x = fmaf(Hp[m].x, kx, r.x); r.y = fmaf(Hp[m].y, kx, r.y);
+            r.z = fmaf(Hp[m].z, kx, r.z); r.w = fmaf(Hp[m].w, kx, r.w);
+        }
         du.x = fmaf(dH[m].x, kk, du.x); du.y = fmaf(dH[m].y, kk, du.y);
         du.z = fmaf(dH[m].z, kk, du.z); du.w = fmaf(dH[m].w, kk, du.w);
     }
-    *reinterpret_cast<float4 *>(&s_red[0][rg][4 * cg]) = r;
+    if (!KY) *reinterpret_cast<float4 *>(&s_red[0][rg][4 * cg]) = r;
     *reinterpret_cast<float4 *>(&s_red[1][rg][4 * cg]) = du;
     __syncthreads();
     float dbp = 0.f;   // this column's share of dbeta
     {
         int j;
-        float rs, ds;
-        if (column_sums<DVS, RG, true>(s_red[0], s_red[1], tid, j, rs, ds)) {
-            s_u[j] = bt * (s.v[j] - rs);
+        float rs = 0.f, ds;
+        const bool owner = KY ? column_sums<DVS, RG, false>(s_red[1], s_red[1], tid, j, ds, rs)
+                              : column_sums<DVS, RG, true>(s_red[0], s_red[1], tid, j, rs, ds);
+        if (owner) {
+            const float y = KY ? ys[j] : s.v[j] - rs;
+            s_u[j] = bt * y;
             s_du[j] = ds;
             p.dv[((size_t)row * p.H + h) * p.DV + col0 + j] = bt * ds;
-            dbp = ds * (s.v[j] - rs);
+            dbp = ds * y;
         }
     }
     if (warp < kOwnerWarps) {
@@ -509,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
     __shared__ __align__(16) float s_u[DVS];
     __shared__ __align__(16) float s_du[DVS];
     __shared__ float s_db[kThreads / 32];
+    __shared__ float s_y[kUnitTokens][DVS];   // each token's v - r, from the recomputation
     const int tid = threadIdx.x, cg = tid % TPR, rg = tid / TPR;
     constexpr int nslab = DK / DVS;   // dv == dk
     const long units = (long)p.nc64 * p.nseq * p.H * nslab;
@@ -538,12 +551,13 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
             put_token<Tin, DK, DVS>(p, cur, false, s);
             __syncthreads();
             if (t + 1 < t1) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + 1, h, col0, false, nxt);
-            forward_token<DK, DVS, RG, R, DR>(p, s, Hp, s_red[0], s_u);
+            forward_token<DK, DVS, RG, R, DR>(p, s, Hp, s_red[0], s_u, s_y[t - t0]);
             cur = nxt;
         }
 #pragma unroll
         for (int m = 0; m < R; ++m) Hc[m] = Hp[m];   // the state after the chunk's last token
-        // the walk back (each thread reads back only what it wrote)
+        // the walk back (each thread reads back only what it wrote; v - r of every token is
+        // read by the thread that kept it)
         fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t1 - 1, h, col0, true, cur);
 #pragma unroll
         for (int m = 0; m < R; ++m) Hn[m] = ld_bf16x4(scr + ((size_t)(t1 - 1 - t0) * DK + rg + RG * m) * DVS);
@@ -558,7 +572,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
             put_token<Tin, DK, DVS>(p, cur, true, s);
             __syncthreads();
             if (t > t0) fetch_token<Tin, DK, DVS>(p, row - 1, h, col0, true, nxt);
-            backward_token<DK, DVS, RG, R, DR>(p, s, row, h, col0, dH, Hc, Hp, s_red, s_u, s_du, s_db);
+            backward_token<DK, DVS, RG, R, DR, true>(p, s, row, h, col0, dH, Hc, Hp, s_red, s_u, s_du, s_db,
+                                                     s_y[t - t0]);
             cur = nxt;
         }
     }
