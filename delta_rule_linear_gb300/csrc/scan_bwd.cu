@@ -147,6 +147,27 @@ __device__ __forceinline__ void token_norms(const BwdParams &p, const Stage<DK, 
     qn = p.scale * (p.use_l2 ? rsqrtf(fmaxf(nq, kNormEps * kNormEps)) : 1.f);
 }
 
+// A token as the steps read it: raw k, q and exp(g) per key row, v and do of the slab,
+// beta, and the normalisation factors (k^ = kn k, q~ = qn q).  StageTok reads a staged
+// token (Stage), ChunkTok one token of a chunk staged whole (the chunk-parallel walk).
+template <int DK, int DVS>
+struct StageTok {
+    const Stage<DK, DVS> &s;
+    float kn, qn;
+    __device__ float k(int i) const { return s.k[i]; }
+    __device__ float q(int i) const { return s.q[i]; }
+    __device__ float a(int i) const { return s.a[i]; }
+    __device__ float v(int j) const { return s.v[j]; }
+    __device__ float4 d4(int j0) const { return *reinterpret_cast<const float4 *>(&s.d[j0]); }
+    __device__ float beta() const { return s.beta; }
+};
+template <int DK, int DVS>
+__device__ __forceinline__ StageTok<DK, DVS> stage_tok(const BwdParams &p, const Stage<DK, DVS> &s) {
+    float kn, qn;
+    token_norms(p, s, kn, qn);
+    return StageTok<DK, DVS>{s, kn, qn};
+}
+
 // Sums over the RG row groups of one or two [RG][DVS] partial arrays.  Column j's sums land
 // in its owner thread (returns true there): the first DVS threads with few row groups, else
 // P = kThreads / DVS consecutive lanes per column that each add RG / P terms and shuffle.
@@ -186,17 +207,16 @@ __device__ __forceinline__ bool column_sums(const float (*a)[DVS], const float (
 // One token of the forward recurrence on this thread's rows of the slab (S: the state before
 // the token on entry, after it on return).  The stage was synced by the caller; two syncs.
 // y_out (optional, DVS floats): the token's v - r, kept for its backward step.
-template <int DK, int DVS, int RG, int R, bool DR>
-__device__ __forceinline__ void forward_token(const BwdParams &p, const Stage<DK, DVS> &s, float4 (&S)[R],
+template <int DK, int DVS, int RG, int R, bool DR, typename Tok>
+__device__ __forceinline__ void forward_token(const BwdParams &p, const Tok &s, float4 (&S)[R],
                                               float (*s_red)[DVS], float *s_u, float *y_out = nullptr) {
     const int tid = threadIdx.x, cg = tid % (DVS / 4), rg = tid / (DVS / 4);
-    float kn, qn;
-    token_norms(p, s, kn, qn);
+    const float kn = s.kn;
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < R; ++m) {
         const int i = rg + RG * m;
-        const float kk = s.k[i] * kn, kx = DR ? s.a[i] * kk : kk;
+        const float kk = s.k(i) * kn, kx = DR ? s.a(i) * kk : kk;
         r.x = fmaf(S[m].x, kx, r.x); r.y = fmaf(S[m].y, kx, r.y);
         r.z = fmaf(S[m].z, kx, r.z); r.w = fmaf(S[m].w, kx, r.w);
     }
@@ -206,8 +226,8 @@ __device__ __forceinline__ void forward_token(const BwdParams &p, const Stage<DK
         int j;
         float rs, unused;
         if (column_sums<DVS, RG, false>(s_red, s_red, tid, j, rs, unused)) {
-            const float y = s.v[j] - rs;
-            s_u[j] = s.beta * y;
+            const float y = s.v(j) - rs;
+            s_u[j] = s.beta() * y;
             if (y_out) y_out[j] = y;
         }
     }
@@ -216,7 +236,7 @@ __device__ __forceinline__ void forward_token(const BwdParams &p, const Stage<DK
 #pragma unroll
     for (int m = 0; m < R; ++m) {
         const int i = rg + RG * m;
-        const float a = s.a[i], kk = s.k[i] * kn;
+        const float a = s.a(i), kk = s.k(i) * kn;
         S[m].x = fmaf(a, S[m].x, kk * u4.x); S[m].y = fmaf(a, S[m].y, kk * u4.y);
         S[m].z = fmaf(a, S[m].z, kk * u4.z); S[m].w = fmaf(a, S[m].w, kk * u4.w);
     }
@@ -263,7 +283,7 @@ __global__ void __launch_bounds__(kThreads) bwd_ckpt_kernel(BwdParams p) {
             put_token<Tin, DK, DVS>(p, ring[j], false, s);
             __syncthreads();
             if (t + kAhead < p.T) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + kAhead, h, col0, false, ring[j]);
-            forward_token<DK, DVS, RG, R, DR>(p, s, S, s_red, s_u);
+            forward_token<DK, DVS, RG, R, DR>(p, stage_tok(p, s), S, s_red, s_u);
         }
     }
 }
@@ -284,8 +304,8 @@ __device__ __forceinline__ float row_sum(float x) {
 // of the state after it on entry and of the state before it on return.  Writes the token's
 // dv columns and adds its shares of dbeta, dq~, dk^, dg and ddecay.  Two syncs.  KY: the
 // token's v - r was kept by its forward step (ys, DVS floats) and is not recomputed.
-template <int DK, int DVS, int RG, int R, bool DR, bool KY = false>
-__device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<DK, DVS> &s, long row, int h,
+template <int DK, int DVS, int RG, int R, bool DR, bool KY = false, typename Tok>
+__device__ __forceinline__ void backward_token(const BwdParams &p, const Tok &s, long row, int h,
                                                int col0, float4 (&dH)[R], float4 (&Hc)[R], const float4 (&Hp)[R],
                                                float (*s_red)[RG][DVS], float *s_u, float *s_du, float *s_db,
                                                const float *ys = nullptr) {
@@ -293,16 +313,15 @@ __device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<D
     constexpr int kOwnerWarps = RG <= 8 ? (DVS + 31) / 32 : kThreads / 32;   // warps holding column sums
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = tid % TPR, rg = tid / TPR;
-    float kn, qn;
-    token_norms(p, s, kn, qn);
-    const float bt = s.beta;
-    const float4 do4 = *reinterpret_cast<const float4 *>(&s.d[4 * cg]);
+    const float kn = s.kn, qn = s.qn;
+    const float bt = s.beta();
+    const float4 do4 = s.d4(4 * cg);
     // dh += q~ do^T;  r = R^T k^;  du = dh^T k^   (both row sums through shared memory)
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f), du = r;
 #pragma unroll
     for (int m = 0; m < R; ++m) {
         const int i = rg + RG * m;
-        const float qq = s.q[i] * qn, kk = s.k[i] * kn, kx = DR ? s.a[i] * kk : kk;
+        const float qq = s.q(i) * qn, kk = s.k(i) * kn, kx = DR ? s.a(i) * kk : kk;
         dH[m].x = fmaf(qq, do4.x, dH[m].x); dH[m].y = fmaf(qq, do4.y, dH[m].y);
         dH[m].z = fmaf(qq, do4.z, dH[m].z); dH[m].w = fmaf(qq, do4.w, dH[m].w);
         if (!KY) {
@@ -322,7 +341,7 @@ __device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<D
         const bool owner = KY ? column_sums<DVS, RG, false>(s_red[1], s_red[1], tid, j, ds, rs)
                               : column_sums<DVS, RG, true>(s_red[0], s_red[1], tid, j, rs, ds);
         if (owner) {
-            const float y = KY ? ys[j] : s.v[j] - rs;
+            const float y = KY ? ys[j] : s.v(j) - rs;
             s_u[j] = bt * y;
             s_du[j] = ds;
             p.dv[((size_t)row * p.H + h) * p.DV + col0 + j] = bt * ds;
@@ -352,7 +371,7 @@ __device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<D
 #pragma unroll
         for (int m = 0; m < R; ++m) {
             const int i = rg + RG * m;
-            const float a = s.a[i], kk = s.k[i] * kn;
+            const float a = s.a(i), kk = s.k(i) * kn;
             const float hu = dot4(Hp[m], du4);   // sum_j h_{t-1}[i,j] du_j
             x[3 * m] = dot4(Hc[m], do4);
             x[3 * m + 1] = dot4(dH[m], u4) - bt * (DR ? a : 1.f) * hu;
@@ -374,7 +393,7 @@ __device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<D
 #pragma unroll
         for (int v = 0; v < 3; ++v) z[v] += __shfl_xor_sync(0xffffffffu, z[v], 1);
         const int i = rg + RG * ((cg >> 1) & 3);
-        const float a = s.a[i];
+        const float a = s.a(i);
         if ((cg & 1) == 0) {
             atomicAdd(p.dq + kd_off + i, z[0]);
             atomicAdd(p.dk + kd_off + i, z[1]);
@@ -392,7 +411,7 @@ __device__ __forceinline__ void backward_token(const BwdParams &p, const Stage<D
 #pragma unroll
     for (int m = 0; m < R; ++m) {
         const int i = rg + RG * m;
-        const float a = s.a[i], kk = s.k[i] * kn;
+        const float a = s.a(i), kk = s.k(i) * kn;
         // sums over this thread's four columns, then over the row's TPR threads
         float dq_i = row_sum<TPR>(dot4(Hc[m], do4));
         const float hu = dot4(Hp[m], du4);   // sum_j h_{t-1}[i,j] du_j
@@ -459,7 +478,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
             put_token<Tin, DK, DVS>(p, cur, false, s);
             __syncthreads();
             if (t + 1 < t1) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + 1, h, col0, false, nxt);
-            forward_token<DK, DVS, RG, R, DR>(p, s, Hp, s_red[0], s_u);
+            forward_token<DK, DVS, RG, R, DR>(p, stage_tok(p, s), Hp, s_red[0], s_u);
             cur = nxt;
         }
 #pragma unroll
@@ -475,7 +494,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
             put_token<Tin, DK, DVS>(p, cur, true, s);
             __syncthreads();
             if (t > t0) fetch_token<Tin, DK, DVS>(p, row - 1, h, col0, true, nxt);
-            backward_token<DK, DVS, RG, R, DR>(p, s, row, h, col0, dH, Hc, Hp, s_red, s_u, s_du, s_db);
+            backward_token<DK, DVS, RG, R, DR>(p, stage_tok(p, s), row, h, col0, dH, Hc, Hp, s_red, s_u, s_du, s_db);
             cur = nxt;
         }
     }
@@ -498,6 +517,16 @@ constexpr int kUnitTokens = 64;   // the tensor-core chunk
 constexpr int kUnitSlab = 32;     // value columns per unit
 constexpr int kChunkBwdCtas = 304;   // persistent CTAs (two per SM on 152 SMs)
 
+// 16-byte global -> shared copy (both addresses 16-byte aligned), and the wait for every copy
+// this thread has issued
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ float4 ld_bf16x4(const __nv_bfloat16 *src) {
     const uint2 w = *reinterpret_cast<const uint2 *>(src);
     return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
@@ -509,14 +538,46 @@ __device__ __forceinline__ void st_bf16x4(__nv_bfloat16 *dst, float4 v) {
                                                  *reinterpret_cast<const uint32_t *>(&b));
 }
 
+// One token of the staged chunk, read like a staged token: raw k, q (bf16), exp(g), v and do
+// of the slab (bf16), beta and the normalisation factors.
+template <int DK, int DVS>
+struct ChunkTok {
+    const __nv_bfloat16 *kr, *qr, *vr, *dr;
+    const float *ar;
+    float kn, qn, b;
+    __device__ float k(int i) const { return __bfloat162float(kr[i]); }
+    __device__ float q(int i) const { return __bfloat162float(qr[i]); }
+    __device__ float a(int i) const { return ar[i]; }
+    __device__ float v(int j) const { return __bfloat162float(vr[j]); }
+    __device__ float4 d4(int j0) const { return ld_bf16x4(dr + j0); }
+    __device__ float beta() const { return b; }
+};
+
+// The chunk staged whole in shared memory (dynamic): raw k, q rows [64][DK] bf16, exp(g)
+// [64][DK] fp32, the v and do columns of the slab [64][DVS] bf16, and beta, kn, qn [64].
+template <int DK, int DVS>
+struct ChunkStage {
+    static constexpr int K = 0, Q = K + kUnitTokens * DK * 2, A = Q + kUnitTokens * DK * 2;
+    static constexpr int V = A + kUnitTokens * DK * 4, D = V + kUnitTokens * DVS * 2;
+    static constexpr int BETA = D + kUnitTokens * DVS * 2, KN = BETA + kUnitTokens * 4, QN = KN + kUnitTokens * 4;
+    static constexpr int BYTES = QN + kUnitTokens * 4;
+};
+
 template <int DK, int DVS, bool DR>
 __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
-    using Tin = __nv_bfloat16;
     using Ly = BwdLayout<DVS>;
+    using CS = ChunkStage<DK, DVS>;
     constexpr int TPR = Ly::TPR, RG = Ly::RG, R = DK / RG;
     static_assert(TPR <= 32 && 32 % TPR == 0, "a state row lies within one warp");
-    static_assert(stage_aligned<DK, DVS>(), "both stage buffers 16-byte aligned");
-    __shared__ __align__(16) Stage<DK, DVS> st[2];
+    extern __shared__ __align__(16) uint8_t chunk_smem[];
+    __nv_bfloat16 *ck = reinterpret_cast<__nv_bfloat16 *>(chunk_smem + CS::K);
+    __nv_bfloat16 *cq = reinterpret_cast<__nv_bfloat16 *>(chunk_smem + CS::Q);
+    float *ca = reinterpret_cast<float *>(chunk_smem + CS::A);
+    __nv_bfloat16 *cv = reinterpret_cast<__nv_bfloat16 *>(chunk_smem + CS::V);
+    __nv_bfloat16 *cd = reinterpret_cast<__nv_bfloat16 *>(chunk_smem + CS::D);
+    float *cbeta = reinterpret_cast<float *>(chunk_smem + CS::BETA);
+    float *ckn = reinterpret_cast<float *>(chunk_smem + CS::KN);
+    float *cqn = reinterpret_cast<float *>(chunk_smem + CS::QN);
     __shared__ __align__(16) float s_red[2][RG][DVS];
     __shared__ __align__(16) float s_u[DVS];
     __shared__ __align__(16) float s_du[DVS];
@@ -527,54 +588,95 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
     const long units = (long)p.nc64 * p.nseq * p.H * nslab;
     // this thread's element of the scratch: [token][row][column] of the unit's slab
     __nv_bfloat16 *scr = p.scratch16 + (size_t)blockIdx.x * kUnitTokens * DK * DVS + 4 * cg;
-    TokenRegs<Tin> cur{}, nxt{};
-    int it = 0;   // tokens staged so far: selects the stage buffer
+    const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(p.q);
+    const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(p.k);
+    const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(p.v);
+    const __nv_bfloat16 *gdo = static_cast<const __nv_bfloat16 *>(p.dout);
     for (long u = blockIdx.x; u < units; u += gridDim.x) {
         const int slab = (int)(u % nslab);
         const long r = u / nslab;
         const int h = (int)(r % p.H), n = (int)((r / p.H) % p.nseq), c = (int)(r / ((long)p.H * p.nseq));
         const int col0 = slab * DVS;
-        const int t0 = c * kUnitTokens, t1 = min(p.T, t0 + kUnitTokens);
-        const size_t kb = (((size_t)n * p.H + h) * p.nc64 + c) * DK * DK + col0 + 4 * cg;
+        const int t0 = c * kUnitTokens, t1 = min(p.T, t0 + kUnitTokens), nv = t1 - t0;
+        const long row0 = (long)n * p.T + t0;
+        __syncthreads();   // the previous unit's reads of the staged chunk are done
+        // the chunk's tokens by 16-byte copies: k, q rows; g rows (exp taken below); the v
+        // and do columns of the slab; beta
+        {
+            constexpr int PK = DK / 8, PG = DK / 4, PV = DVS / 8;   // 16-byte pieces per row
+            for (int x = tid; x < 2 * kUnitTokens * PK; x += kThreads) {
+                const int isq = x / (kUnitTokens * PK), t = (x / PK) % kUnitTokens, pc = x % PK;
+                if (t < nv)
+                    cp_async16((isq ? cq : ck) + t * DK + 8 * pc,
+                               (isq ? gq : gk) + ((row0 + t) * p.H + h) * DK + 8 * pc);
+            }
+            if (p.gk)
+                for (int x = tid; x < kUnitTokens * PG; x += kThreads) {
+                    const int t = x / PG, pc = x % PG;
+                    if (t < nv) cp_async16(ca + t * DK + 4 * pc, p.gk + ((row0 + t) * p.H + h) * DK + 4 * pc);
+                }
+            for (int x = tid; x < 2 * kUnitTokens * PV; x += kThreads) {
+                const int isd = x / (kUnitTokens * PV), t = (x / PV) % kUnitTokens, pc = x % PV;
+                if (t < nv)
+                    cp_async16((isd ? cd : cv) + t * DVS + 8 * pc,
+                               (isd ? gdo : gv) + ((row0 + t) * p.H + h) * p.DV + col0 + 8 * pc);
+            }
+            if (tid < nv) cbeta[tid] = p.beta[(row0 + tid) * p.H + h];
+            cp_async_wait_all();
+        }
         float4 dH[R], Hc[R], Hp[R], Hn[R];
+        const size_t kb = (((size_t)n * p.H + h) * p.nc64 + c) * DK * DK + col0 + 4 * cg;
 #pragma unroll
         for (int m = 0; m < R; ++m) {
             Hp[m] = ld_bf16x4(p.fstates + kb + (size_t)(rg + RG * m) * DK);
             dH[m] = ld_bf16x4(p.bstates + kb + (size_t)(rg + RG * m) * DK);
         }
+        __syncthreads();
+        // exp(g) in place (1 without a decay); the norms of the k and q rows, two threads a row
+        for (int x = tid; x < kUnitTokens * DK; x += kThreads)
+            ca[x] = p.gk ? expf(ca[x]) : 1.f;
+        {
+            const int rr = tid >> 1, half = tid & 1, t = rr & (kUnitTokens - 1);
+            const __nv_bfloat16 *xr = (rr >= kUnitTokens ? cq : ck) + t * DK + half * (DK / 2);
+            float ss = 0.f;
+#pragma unroll 8
+            for (int i = 0; i < DK / 2; ++i) {
+                const float x = __bfloat162float(xr[i]);
+                ss = fmaf(x, x, ss);
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            if (half == 0 && t < nv) {
+                // 1 / max(|x|, eps) = rsqrt(max(|x|^2, eps^2))
+                const float inv = p.use_l2 ? rsqrtf(fmaxf(ss, kNormEps * kNormEps)) : 1.f;
+                if (rr >= kUnitTokens) cqn[t] = p.scale * inv;
+                else ckn[t] = inv;
+            }
+        }
+        __syncthreads();
+        auto tok = [&](int t) {
+            return ChunkTok<DK, DVS>{ck + t * DK, cq + t * DK, cv + t * DVS, cd + t * DVS, ca + t * DK,
+                                     ckn[t], cqn[t], cbeta[t]};
+        };
         // the chunk's states, each before its token, into the scratch
-        fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t0, h, col0, false, cur);
-        for (int t = t0; t < t1; ++t, ++it) {
+        for (int t = 0; t < nv; ++t) {
 #pragma unroll
-            for (int m = 0; m < R; ++m) st_bf16x4(scr + ((size_t)(t - t0) * DK + rg + RG * m) * DVS, Hp[m]);
-            Stage<DK, DVS> &s = st[it & 1];
-            put_token<Tin, DK, DVS>(p, cur, false, s);
-            __syncthreads();
-            if (t + 1 < t1) fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t + 1, h, col0, false, nxt);
-            forward_token<DK, DVS, RG, R, DR>(p, s, Hp, s_red[0], s_u, s_y[t - t0]);
-            cur = nxt;
+            for (int m = 0; m < R; ++m) st_bf16x4(scr + ((size_t)t * DK + rg + RG * m) * DVS, Hp[m]);
+            forward_token<DK, DVS, RG, R, DR>(p, tok(t), Hp, s_red[0], s_u, s_y[t]);
         }
 #pragma unroll
         for (int m = 0; m < R; ++m) Hc[m] = Hp[m];   // the state after the chunk's last token
         // the walk back (each thread reads back only what it wrote; v - r of every token is
         // read by the thread that kept it)
-        fetch_token<Tin, DK, DVS>(p, (long)n * p.T + t1 - 1, h, col0, true, cur);
 #pragma unroll
-        for (int m = 0; m < R; ++m) Hn[m] = ld_bf16x4(scr + ((size_t)(t1 - 1 - t0) * DK + rg + RG * m) * DVS);
-        for (int t = t1 - 1; t >= t0; --t, ++it) {
-            const long row = (long)n * p.T + t;
+        for (int m = 0; m < R; ++m) Hn[m] = ld_bf16x4(scr + ((size_t)(nv - 1) * DK + rg + RG * m) * DVS);
+        for (int t = nv - 1; t >= 0; --t) {
 #pragma unroll
             for (int m = 0; m < R; ++m) Hp[m] = Hn[m];
-            if (t > t0)
+            if (t > 0)
 #pragma unroll
-                for (int m = 0; m < R; ++m) Hn[m] = ld_bf16x4(scr + ((size_t)(t - 1 - t0) * DK + rg + RG * m) * DVS);
-            Stage<DK, DVS> &s = st[it & 1];
-            put_token<Tin, DK, DVS>(p, cur, true, s);
-            __syncthreads();
-            if (t > t0) fetch_token<Tin, DK, DVS>(p, row - 1, h, col0, true, nxt);
-            backward_token<DK, DVS, RG, R, DR, true>(p, s, row, h, col0, dH, Hc, Hp, s_red, s_u, s_du, s_db,
-                                                     s_y[t - t0]);
-            cur = nxt;
+                for (int m = 0; m < R; ++m) Hn[m] = ld_bf16x4(scr + ((size_t)(t - 1) * DK + rg + RG * m) * DVS);
+            backward_token<DK, DVS, RG, R, DR, true>(p, tok(t), row0 + t, h, col0, dH, Hc, Hp, s_red, s_u, s_du,
+                                                     s_db, s_y[t]);
         }
     }
 }
@@ -726,12 +828,18 @@ cudaError_t launch_gk_chunk_bwd_grads(const BwdArgs &a, const __nv_bfloat16 *fst
     const long units = (long)p.nc64 * a.B * a.H * (a.dkdim / kUnitSlab);
     const unsigned grid = (unsigned)std::min<long>(units, kChunkBwdCtas);
     const bool dr = p.decayed_read != 0;
+    auto go = [&](auto kern, int smem) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+        kern<<<grid, kThreads, smem, s>>>(p);
+        return cudaGetLastError();
+    };
     if (a.dkdim == 128) {
-        if (dr) bwd_chunk_kernel<128, kUnitSlab, true><<<grid, kThreads, 0, s>>>(p);
-        else bwd_chunk_kernel<128, kUnitSlab, false><<<grid, kThreads, 0, s>>>(p);
+        constexpr int smem = ChunkStage<128, kUnitSlab>::BYTES;
+        e = dr ? go(bwd_chunk_kernel<128, kUnitSlab, true>, smem) : go(bwd_chunk_kernel<128, kUnitSlab, false>, smem);
     } else {
-        if (dr) bwd_chunk_kernel<64, kUnitSlab, true><<<grid, kThreads, 0, s>>>(p);
-        else bwd_chunk_kernel<64, kUnitSlab, false><<<grid, kThreads, 0, s>>>(p);
+        constexpr int smem = ChunkStage<64, kUnitSlab>::BYTES;
+        e = dr ? go(bwd_chunk_kernel<64, kUnitSlab, true>, smem) : go(bwd_chunk_kernel<64, kUnitSlab, false>, smem);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long rh = rows * a.H;
