@@ -560,8 +560,61 @@ struct ChunkStage {
     static constexpr int K = 0, Q = K + kUnitTokens * DK * 2, A = Q + kUnitTokens * DK * 2;
     static constexpr int V = A + kUnitTokens * DK * 4, D = V + kUnitTokens * DVS * 2;
     static constexpr int BETA = D + kUnitTokens * DVS * 2, KN = BETA + kUnitTokens * 4, QN = KN + kUnitTokens * 4;
-    static constexpr int BYTES = QN + kUnitTokens * 4;
+    static constexpr int CD = QN + kUnitTokens * 4;   // k^_{t-1} . kx_t (kx: k^, or exp(g) k^ with the decayed read)
+    static constexpr int BYTES = CD + kUnitTokens * 4;
 };
+
+// Two tokens of the forward recurrence (t0, then t1) with two barriers: the state after t0 is
+// a_0 S + k^_0 u_0^T, so t1's read-out is S^T (a_0 kx_1) + u_0 (k^_0 . kx_1), and one pass over
+// S gives both tokens' column sums.  c01 = k^_0 . kx_1.  S holds the state before t0 on entry
+// and after t1 on return; mid receives the state between them (after t0).  y0, y1: the tokens'
+// v - r, kept for their backward steps.
+template <int DK, int DVS, int RG, int R, bool DR, typename Tok>
+__device__ __forceinline__ void forward_pair(const Tok &s0, const Tok &s1, float c01, float4 (&S)[R],
+                                             __nv_bfloat16 *mid, float (*s_red)[RG][DVS], float (*s_u2)[DVS],
+                                             float *y0, float *y1) {
+    const int tid = threadIdx.x, cg = tid % (DVS / 4), rg = tid / (DVS / 4);
+    float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = r0;
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int i = rg + RG * m;
+        const float k0 = s0.k(i) * s0.kn, kx0 = DR ? s0.a(i) * k0 : k0;
+        const float k1 = s1.k(i) * s1.kn, w1 = s0.a(i) * (DR ? s1.a(i) * k1 : k1);
+        r0.x = fmaf(S[m].x, kx0, r0.x); r0.y = fmaf(S[m].y, kx0, r0.y);
+        r0.z = fmaf(S[m].z, kx0, r0.z); r0.w = fmaf(S[m].w, kx0, r0.w);
+        r1.x = fmaf(S[m].x, w1, r1.x); r1.y = fmaf(S[m].y, w1, r1.y);
+        r1.z = fmaf(S[m].z, w1, r1.z); r1.w = fmaf(S[m].w, w1, r1.w);
+    }
+    *reinterpret_cast<float4 *>(&s_red[0][rg][4 * cg]) = r0;
+    *reinterpret_cast<float4 *>(&s_red[1][rg][4 * cg]) = r1;
+    __syncthreads();
+    {
+        int j;
+        float rs0, rs1;
+        if (column_sums<DVS, RG, true>(s_red[0], s_red[1], tid, j, rs0, rs1)) {
+            const float ya = s0.v(j) - rs0, ua = s0.beta() * ya;
+            const float yb = s1.v(j) - rs1 - c01 * ua;
+            s_u2[0][j] = ua;
+            s_u2[1][j] = s1.beta() * yb;
+            y0[j] = ya;
+            y1[j] = yb;
+        }
+    }
+    __syncthreads();
+    const float4 u0 = *reinterpret_cast<const float4 *>(&s_u2[0][4 * cg]);
+    const float4 u1 = *reinterpret_cast<const float4 *>(&s_u2[1][4 * cg]);
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int i = rg + RG * m;
+        const float a0 = s0.a(i), k0 = s0.k(i) * s0.kn;
+        S[m].x = fmaf(a0, S[m].x, k0 * u0.x); S[m].y = fmaf(a0, S[m].y, k0 * u0.y);
+        S[m].z = fmaf(a0, S[m].z, k0 * u0.z); S[m].w = fmaf(a0, S[m].w, k0 * u0.w);
+        st_bf16x4(mid + (size_t)i * DVS, S[m]);
+        const float a1 = s1.a(i), k1 = s1.k(i) * s1.kn;
+        S[m].x = fmaf(a1, S[m].x, k1 * u1.x); S[m].y = fmaf(a1, S[m].y, k1 * u1.y);
+        S[m].z = fmaf(a1, S[m].z, k1 * u1.z); S[m].w = fmaf(a1, S[m].w, k1 * u1.w);
+    }
+}
 
 template <int DK, int DVS, bool DR>
 __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
@@ -578,9 +631,11 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
     float *cbeta = reinterpret_cast<float *>(chunk_smem + CS::BETA);
     float *ckn = reinterpret_cast<float *>(chunk_smem + CS::KN);
     float *cqn = reinterpret_cast<float *>(chunk_smem + CS::QN);
+    float *ccd = reinterpret_cast<float *>(chunk_smem + CS::CD);
     __shared__ __align__(16) float s_red[2][RG][DVS];
     __shared__ __align__(16) float s_u[DVS];
     __shared__ __align__(16) float s_du[DVS];
+    __shared__ __align__(16) float s_u2[2][DVS];
     __shared__ float s_db[kThreads / 32];
     __shared__ float s_y[kUnitTokens][DVS];   // each token's v - r, from the recomputation
     const int tid = threadIdx.x, cg = tid % TPR, rg = tid / TPR;
@@ -653,12 +708,35 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
             }
         }
         __syncthreads();
+        {   // k^_{t-1} . kx_t for the token pairs of the recomputation, four threads a dot
+            const int t = tid >> 2, part = tid & 3;
+            float dot = 0.f;
+            if (t > 0 && t < nv) {
+                const __nv_bfloat16 *k0 = ck + (t - 1) * DK, *k1 = ck + t * DK;
+                const float *a1 = ca + t * DK;
+#pragma unroll 8
+                for (int i = part; i < DK; i += 4)
+                    dot = fmaf(__bfloat162float(k0[i]), DR ? a1[i] * __bfloat162float(k1[i]) : __bfloat162float(k1[i]), dot);
+            }
+            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+            if (part == 0 && t < nv) ccd[t] = t > 0 ? dot * ckn[t - 1] * ckn[t] : 0.f;
+        }
+        __syncthreads();
         auto tok = [&](int t) {
             return ChunkTok<DK, DVS>{ck + t * DK, cq + t * DK, cv + t * DVS, cd + t * DVS, ca + t * DK,
                                      ckn[t], cqn[t], cbeta[t]};
         };
-        // the chunk's states, each before its token, into the scratch
-        for (int t = 0; t < nv; ++t) {
+        // the chunk's states, each before its token, into the scratch: two tokens per pair of
+        // barriers, the last one alone when the chunk is odd
+        int t = 0;
+        for (; t + 1 < nv; t += 2) {
+#pragma unroll
+            for (int m = 0; m < R; ++m) st_bf16x4(scr + ((size_t)t * DK + rg + RG * m) * DVS, Hp[m]);
+            forward_pair<DK, DVS, RG, R, DR>(tok(t), tok(t + 1), ccd[t + 1], Hp, scr + (size_t)(t + 1) * DK * DVS,
+                                             s_red, s_u2, s_y[t], s_y[t + 1]);
+        }
+        if (t < nv) {
 #pragma unroll
             for (int m = 0; m < R; ++m) st_bf16x4(scr + ((size_t)t * DK + rg + RG * m) * DVS, Hp[m]);
             forward_token<DK, DVS, RG, R, DR>(p, tok(t), Hp, s_red[0], s_u, s_y[t]);
