@@ -353,3 +353,42 @@ def test_chunk_bwd_rejects_bad_arguments(lib):
     assert call(wsb=need - 1) == 6
     assert call(ws=_fake(0x1008)) == 5
     assert call(B=0) == 0                       # nothing to do, no launch
+
+
+def test_gk_chunk_bwd_rejects_bad_arguments(lib):
+    """kda_gk_chunk_bwd (the per-channel chunked backward): workspace sizes, and every argument
+    error returned before anything is enqueued."""
+    need = lib.kda_gk_chunk_bwd_workspace(1, 64, 2, 64, 64)
+    assert need > 256
+    assert lib.kda_gk_chunk_bwd_workspace(2, 2048, 16, 128, 128) > lib.kda_gk_chunk_bwd_workspace(1, 64, 2, 128, 128)
+    assert lib.kda_gk_chunk_bwd_workspace(1, 64, 2, 64, 128) == 0      # dk != dv
+    assert lib.kda_gk_chunk_bwd_workspace(1, 64, 2, 96, 96) == 0       # head dim not 64 / 128
+    assert lib.kda_gk_chunk_bwd_workspace(1, 64, 0, 64, 64) == 0
+    assert lib.kda_gk_chunk_bwd_workspace(0, 64, 2, 64, 64) == 256     # header only
+
+    def call(**kw):
+        a = dict(q=_fake(), k=_fake(), v=_fake(), beta=_fake(), g=_fake(), h0=None, do=_fake(),
+                 dhT=None, dq=_fake(), dk_=_fake(), dv_=_fake(), db=_fake(), dg=_fake(), dh0=None,
+                 B=1, T=64, H=2, dk=64, dv=64, dt=1, l2=1, dr=0, ws=_fake(), wsb=need)
+        a.update(kw)
+        return lib.kda_gk_chunk_bwd(a["q"], a["k"], a["v"], a["beta"], a["g"], a["h0"], a["do"], a["dhT"],
+                                    a["dq"], a["dk_"], a["dv_"], a["db"], a["dg"], a["dh0"], a["B"], a["T"],
+                                    a["H"], a["dk"], a["dv"], a["dt"], 0.0, a["l2"], a["dr"], a["ws"], a["wsb"],
+                                    None)
+
+    assert call(q=None) == 1
+    assert call(do=None) == 1
+    assert call(dk_=None) == 1
+    assert call(db=None) == 1
+    assert call(T=-1) == 2
+    assert call(dt=9) == 3
+    assert call(dt=0) == 4                      # fp32 inputs: not on this path
+    assert call(dk=96, dv=96) == 4
+    assert call(dk=64, dv=128) == 4
+    assert call(g=_fake(0x1004)) == 5           # g: 16-byte aligned
+    assert call(dg=_fake(0x1002)) == 5          # dg: 4-byte aligned
+    assert call(dh0=_fake(0x1004)) == 5         # dh0: 16-byte aligned
+    assert call(ws=None) == 6
+    assert call(wsb=need - 1) == 6
+    assert call(ws=_fake(0x1008)) == 5
+    assert call(B=0) == 0                       # nothing to do, no launch
