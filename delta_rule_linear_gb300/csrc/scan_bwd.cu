@@ -508,11 +508,12 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdParams p) {
 // its own.  A forward launch on the tensor cores keeps the state entering each chunk, and
 // the reverse walk over the chunk maps gives the gradient of the state leaving it (both in
 // bf16); with those a unit -- (chunk, sequence, head, value slab) -- depends on no other
-// unit: it recomputes its chunk's states into its scratch (bf16) and walks them in reverse,
-// adding its shares of dq~, dk^, dbeta and dg as the sequential walk does.  Persistent
-// CTAs take the units in (chunk, sequence, head, slab) order, so that the CTAs running at
-// one time read the same tokens; the state before the next token of the reverse walk is
-// loaded one token ahead.
+// unit.  A unit stages its whole chunk in shared memory, recomputes the chunk's states into
+// its scratch (bf16; two tokens per pair of barriers) keeping each token's v - r, and walks
+// them in reverse, adding its shares of dq~, dk^, dbeta and dg as the sequential walk does;
+// the state before the next token of the reverse walk is loaded one token ahead.
+// Persistent CTAs take the units in (chunk, sequence, head, slab) order, so that the CTAs
+// running at one time read the same tokens.
 constexpr int kUnitTokens = 64;   // the tensor-core chunk
 constexpr int kUnitSlab = 32;     // value columns per unit
 constexpr int kChunkBwdCtas = 304;   // persistent CTAs (two per SM on 152 SMs)
