@@ -105,3 +105,17 @@ def test_training_shape_head_sample(kda, dev):
     got = _gpu(kda, dev, d, do, dhT, False)
     heads = [0, 7, 15]
     _check(got, _oracle(d, do, dhT, False, heads=heads), "training shape", heads=heads)
+
+
+def test_more_pairs_than_chains(kda, dev):
+    """More (sequence, head) pairs than the kept-map forward runs chains at once (a quarter
+    of the SMs): the forward walks them in rounds, its ring as deep as every round's chunks."""
+    import torch
+    pairs = torch.cuda.get_device_properties(dev).multi_processor_count // 4 + 10
+    H = 8
+    B = (pairs + H - 1) // H
+    d, do, dhT = _inputs(B, 130, H, 64, "train", seed=95)
+    heads = [0, 5]
+    got = _gpu(kda, dev, d, do, dhT, False)
+    _check(got, _oracle(d, do, dhT, False, heads=heads), f"B={B} H={H}", heads=heads)
+

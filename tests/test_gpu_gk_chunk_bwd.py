@@ -121,3 +121,31 @@ def test_training_shape_head_sample(kda, dev):
     got = _gpu(kda, dev, d, do, dhT, True)
     heads = [0, 7, 15]
     _check(got, _oracle(d, do, dhT, True, heads=heads), "training shape", heads=heads)
+
+
+def test_more_pairs_than_chains(kda, dev):
+    """More (sequence, head) pairs than the kept-map forward runs chains at once (a quarter
+    of the SMs): the forward walks them in rounds, its ring as deep as every round's chunks."""
+    import torch
+    pairs = torch.cuda.get_device_properties(dev).multi_processor_count // 4 + 10
+    H = 8
+    B = (pairs + H - 1) // H
+    d, do, dhT = _inputs(B, 130, H, 64, 0.3, seed=196)
+    heads = [0, 5]
+    got = _gpu(kda, dev, d, do, dhT, True)
+    _check(got, _oracle(d, do, dhT, True, heads=heads), f"B={B} H={H}", heads=heads)
+
+
+def test_no_initial_state_no_final_gradient(kda, dev):
+    """initial_state and dfinal_state both absent (zeros): dh0 is still the gradient with
+    respect to the zero initial state."""
+    import torch
+    d, do, _ = _inputs(2, 90, 2, 128, 0.3, seed=197, with_dhT=False)
+    got = kda.gk_chunk_bwd(*(to_dev(d[n], dev, torch.bfloat16) for n in ("q", "k", "v")),
+                           to_dev(d["beta"], dev, torch.float32), to_dev(d["g"], dev, torch.float32),
+                           None, to_dev(do, dev, torch.bfloat16), None, decayed_read=False)
+    torch.cuda.synchronize()
+    got = {n: to_np(got[n]) for n in NAMES}
+    d0 = dict(d, h0=np.zeros_like(d["h0"]))
+    _check(got, _oracle(d0, do, None, False), "no h0, no dhT")
+
