@@ -528,10 +528,12 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
-__device__ __forceinline__ float4 ld_bf16x4(const __nv_bfloat16 *src) {
-    const uint2 w = *reinterpret_cast<const uint2 *>(src);
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 w) {
     return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
                        __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+__device__ __forceinline__ float4 ld_bf16x4(const __nv_bfloat16 *src) {
+    return bf16x4_to_float4(*reinterpret_cast<const uint2 *>(src));
 }
 __device__ __forceinline__ void st_bf16x4(__nv_bfloat16 *dst, float4 v) {
     const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
@@ -680,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
             if (tid < nv) cbeta[tid] = p.beta[(row0 + tid) * p.H + h];
             cp_async_wait_all();
         }
-        float4 dH[R], Hc[R], Hp[R], Hn[R];
+        float4 dH[R], Hc[R], Hp[R];
         const size_t kb = (((size_t)n * p.H + h) * p.nc64 + c) * DK * DK + col0 + 4 * cg;
 #pragma unroll
         for (int m = 0; m < R; ++m) {
@@ -745,15 +747,23 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
 #pragma unroll
         for (int m = 0; m < R; ++m) Hc[m] = Hp[m];   // the state after the chunk's last token
         // the walk back (each thread reads back only what it wrote; v - r of every token is
-        // read by the thread that kept it)
+        // read by the thread that kept it).  The states before the next two tokens of the walk
+        // are in flight, kept raw (bf16) until used.
+        auto raw_state = [&](int t, uint2 (&w)[R]) {
 #pragma unroll
-        for (int m = 0; m < R; ++m) Hn[m] = ld_bf16x4(scr + ((size_t)(nv - 1) * DK + rg + RG * m) * DVS);
+            for (int m = 0; m < R; ++m)
+                w[m] = *reinterpret_cast<const uint2 *>(scr + ((size_t)t * DK + rg + RG * m) * DVS);
+        };
+        uint2 Pa[R], Pb[R];
+        raw_state(nv - 1, Pa);
+        if (nv > 1) raw_state(nv - 2, Pb);
         for (int t = nv - 1; t >= 0; --t) {
 #pragma unroll
-            for (int m = 0; m < R; ++m) Hp[m] = Hn[m];
-            if (t > 0)
-#pragma unroll
-                for (int m = 0; m < R; ++m) Hn[m] = ld_bf16x4(scr + ((size_t)(t - 1) * DK + rg + RG * m) * DVS);
+            for (int m = 0; m < R; ++m) {
+                Hp[m] = bf16x4_to_float4(Pa[m]);
+                Pa[m] = Pb[m];
+            }
+            if (t > 1) raw_state(t - 2, Pb);
             backward_token<DK, DVS, RG, R, DR, true>(p, tok(t), row0 + t, h, col0, dH, Hc, Hp, s_red, s_u, s_du,
                                                      s_db, s_y[t]);
         }
