@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
             if (tid < nv) cbeta[tid] = p.beta[(row0 + tid) * p.H + h];
             cp_async_wait_all();
         }
-        float4 dH[R], Hc[R], Hp[R];
+        float4 dH[R], Hp[R];
         const size_t kb = (((size_t)n * p.H + h) * p.nc64 + c) * DK * DK + col0 + 4 * cg;
 #pragma unroll
         for (int m = 0; m < R; ++m) {
@@ -744,26 +744,35 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(BwdParams p) {
             for (int m = 0; m < R; ++m) st_bf16x4(scr + ((size_t)t * DK + rg + RG * m) * DVS, Hp[m]);
             forward_token<DK, DVS, RG, R, DR>(p, tok(t), Hp, s_red[0], s_u, s_y[t]);
         }
-#pragma unroll
-        for (int m = 0; m < R; ++m) Hc[m] = Hp[m];   // the state after the chunk's last token
         // the walk back (each thread reads back only what it wrote; v - r of every token is
-        // read by the thread that kept it).  The states before the next two tokens of the walk
-        // are in flight, kept raw (bf16) until used.
+        // read by the thread that kept it).  The states before the next three tokens of the
+        // walk are in flight, and the state after the current token is kept, all raw (bf16)
+        // until used; the state after the chunk's last token is rounded like the others.
         auto raw_state = [&](int t, uint2 (&w)[R]) {
 #pragma unroll
             for (int m = 0; m < R; ++m)
                 w[m] = *reinterpret_cast<const uint2 *>(scr + ((size_t)t * DK + rg + RG * m) * DVS);
         };
-        uint2 Pa[R], Pb[R];
+        uint2 Hc_raw[R], Pa[R], Pb[R], Pc[R];
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(Hp[m].x, Hp[m].y), hi = __floats2bfloat162_rn(Hp[m].z, Hp[m].w);
+            Hc_raw[m] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+        }
         raw_state(nv - 1, Pa);
         if (nv > 1) raw_state(nv - 2, Pb);
+        if (nv > 2) raw_state(nv - 3, Pc);
         for (int t = nv - 1; t >= 0; --t) {
+            float4 Hc[R];
 #pragma unroll
             for (int m = 0; m < R; ++m) {
+                Hc[m] = bf16x4_to_float4(Hc_raw[m]);
                 Hp[m] = bf16x4_to_float4(Pa[m]);
+                Hc_raw[m] = Pa[m];   // the state after the next token of the walk
                 Pa[m] = Pb[m];
+                Pb[m] = Pc[m];
             }
-            if (t > 1) raw_state(t - 2, Pb);
+            if (t > 2) raw_state(t - 3, Pc);
             backward_token<DK, DVS, RG, R, DR, true>(p, tok(t), row0 + t, h, col0, dH, Hc, Hp, s_red, s_u, s_du,
                                                      s_db, s_y[t]);
         }
