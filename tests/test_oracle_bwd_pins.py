@@ -91,3 +91,28 @@ def test_scalar_decay_gradient_is_the_channel_sum(oracle_mod, decayed):
         fd[idx] = (loss(p) - loss(m)) / (2 * eps)
     err = np.max(np.abs(fd - dd)) / np.max(np.abs(fd))
     assert err < 1e-3, err
+
+
+@pytest.mark.parametrize("decayed", [False, True])
+def test_split_sequence_gradients_chain(decayed):
+    """A sequence's gradients equal those of its two parts chained through the state at the
+    split: the second part starts from that state and hands back its gradient, which the
+    first part takes as its final-state gradient (the structure a chunked backward uses)."""
+    from oracle import backward as ob
+    d = _inputs(7, B=2, T=12, H=2, dk=3, dv=4)
+    rng = np.random.default_rng(8)
+    do = rng.standard_normal((2, 12, 2, 4))
+    dhT = rng.standard_normal((2, 2, 3, 4))
+    full = ob.backward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], do, dhT, decayed_read=decayed)
+    cut = 7
+    a = {n: (x[:, :cut] if n != "h0" else x) for n, x in d.items()}
+    b = {n: x[:, cut:] for n, x in d.items() if n != "h0"}
+    t = {n: torch.tensor(np.asarray(x, np.float64)) for n, x in a.items()}
+    _, h_mid = ob.forward_torch(t["q"], t["k"], t["v"], t["beta"], t["g"], t["h0"], decayed_read=decayed)
+    second = ob.backward(b["q"], b["k"], b["v"], b["beta"], b["g"], h_mid.numpy(), do[:, cut:], dhT,
+                         decayed_read=decayed)
+    first = ob.backward(a["q"], a["k"], a["v"], a["beta"], a["g"], a["h0"], do[:, :cut], second["dh0"],
+                        decayed_read=decayed)
+    for n in ("dq", "dk", "dv", "dbeta", "dg"):
+        np.testing.assert_allclose(np.concatenate([first[n], second[n]], axis=1), full[n], rtol=0, atol=1e-10)
+    np.testing.assert_allclose(first["dh0"], full["dh0"], rtol=0, atol=1e-10)
